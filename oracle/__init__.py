@@ -1,0 +1,159 @@
+"""fp64 CPU oracle for the chunked gated delta-rule forward pass.
+
+TEST INFRASTRUCTURE ONLY.  The product path (the CUDA library and its Python
+binding) never imports this package; only the tests, the smoke check and the
+benchmark's CPU-baseline leg do.  The oracle shares no code with the CUDA
+path.
+
+Two independent references live here:
+
+* ``oracle_fwd`` -- the token-by-token recurrence in fp64, written in plain C
+  (``gdr_oracle.c``, OpenMP over (sequence, head, column block)).  This is the
+  definition the chunked GPU method must reproduce.
+* ``chunk_ref`` -- the chunk-parallel (WY / UT) form in fp64 numpy, used only
+  to check the GPU's intermediate stages (gate cumsum, W, U) one by one.
+
+Citation keys used in this package (page title, section):
+  P1 = "Deep Dive: The Next Generation of Ultra-Long Context Sparse MoE LLMs"
+  P2 = "Core Technologies Behind Ultra-Long-Context Sparse MoE Large Models"
+  P3 = "How Trillion-Scale Sparse MoE Models Achieve Million-Token Long Context
+        Capabilities"
+  P4 = "Evaluating Next-Gen Sparse MoE and Long-Context LLMs"
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gdr_oracle.c")
+_LIB = os.path.join(_HERE, "libgdr_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+BF16, F32, F64 = 0, 1, 2
+GATES = {"bounded": 0, "softplus": 1}
+
+
+def build(force: bool = False) -> str:
+    """Compile gdr_oracle.c into libgdr_oracle.so next to it (gcc, OpenMP)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _bind(path):
+    lib = ctypes.CDLL(path)
+    lib.gdr_oracle_fwd.restype = ctypes.c_int
+    lib.gdr_oracle_fwd.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    lib.gdr_oracle_gate.restype = ctypes.c_double
+    lib.gdr_oracle_gate.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.c_int]
+    lib.gdr_oracle_max_threads.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = _bind(build())
+    return _lib
+
+
+def _as_array(x):
+    """Return (contiguous numpy array, dtype code) holding x's stored values.
+
+    bf16 torch tensors are passed as their raw 16-bit patterns so that the C
+    side widens exactly the values a GPU consumed."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach()
+            if x.device.type != "cpu":
+                x = x.cpu()
+            if x.dtype == torch.bfloat16:
+                return np.ascontiguousarray(x.view(torch.int16).numpy().view(np.uint16)), BF16
+            if x.dtype == torch.float32:
+                return np.ascontiguousarray(x.numpy()), F32
+            return np.ascontiguousarray(x.to(torch.float64).numpy()), F64
+    except ImportError:  # pragma: no cover
+        pass
+    x = np.asarray(x)
+    if x.dtype == np.uint16:
+        return np.ascontiguousarray(x), BF16
+    if x.dtype == np.float32:
+        return np.ascontiguousarray(x), F32
+    return np.ascontiguousarray(x, dtype=np.float64), F64
+
+
+def max_threads() -> int:
+    return int(_load().gdr_oracle_max_threads())
+
+
+def gate(a: float, b: float = 2.0, mode: str = "bounded") -> float:
+    """Scalar log-decay g(a) of the oracle [P1 §3.3, P2 §2.2, P3 §3.2, P4 §2.3]."""
+    return float(_load().gdr_oracle_gate(float(a), float(b), GATES[mode]))
+
+
+def oracle_fwd(q, k, v, a, beta, h0=None, cu_seqlens=None, b: float = 2.0,
+               gate: str = "bounded", erase: bool = True, nthreads: int = 0,
+               _lib_path: str | None = None):
+    """Token-by-token fp64 forward.  Returns (out [B,T,H,dv], hT [N,H,dk,dv]).
+
+    Shapes follow the library: q,k [B,T,H,dk], v [B,T,H,dv], a,beta [B,T,H];
+    with cu_seqlens (N+1 offsets) B must be 1 and the N sequences are packed
+    along T.  h0 is [N,H,dk,dv] (None means zero).  ``_lib_path`` loads another
+    build of the C source (the mutation tests use it)."""
+    lib = _load() if _lib_path is None else _bind(_lib_path)
+    arrs = [_as_array(x) for x in (q, k, v, a, beta)]
+    if len({d for _, d in arrs}) != 1:
+        # mixed storage: widen everything to fp64 first (exact)
+        arrs = [(np.ascontiguousarray(_widen_np(x, d)), F64) for x, d in arrs]
+    (qa, dt), (ka, _), (va, _), (aa, _), (ba, _) = arrs
+    B, T, H, dk = qa.shape
+    dv = va.shape[-1]
+    if cu_seqlens is not None:
+        cu = np.ascontiguousarray(np.asarray(
+            cu_seqlens.cpu().numpy() if hasattr(cu_seqlens, "cpu") else cu_seqlens,
+            dtype=np.int64))
+        assert B == 1
+        N = cu.shape[0] - 1
+    else:
+        cu = None
+        N = B
+    out = np.zeros((B, T, H, dv), dtype=np.float64)
+    hT = np.zeros((N, H, dk, dv), dtype=np.float64)
+    h0a = None
+    if h0 is not None:
+        h0a, h0d = _as_array(h0)
+        h0a = np.ascontiguousarray(_widen_np(h0a, h0d))
+        assert h0a.shape == (N, H, dk, dv)
+    rc = lib.gdr_oracle_fwd(
+        qa.ctypes.data, ka.ctypes.data, va.ctypes.data, aa.ctypes.data, ba.ctypes.data,
+        dt, None if h0a is None else h0a.ctypes.data, out.ctypes.data, hT.ctypes.data,
+        None if cu is None else cu.ctypes.data, N, T, H, dk, dv, float(b), GATES[gate],
+        1 if erase else 0, int(nthreads))
+    if rc != 0:
+        raise ValueError(f"gdr_oracle_fwd rejected its arguments (code {rc})")
+    return out, hT
+
+
+def _widen_np(x, code):
+    if code == BF16:
+        return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return x.astype(np.float64)
