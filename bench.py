@@ -1,0 +1,365 @@
+"""Benchmark of the chunked gated delta-rule forward pass (one JSON line).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload t1m] [--path auto|simt|tc] [--no-e2e] [--no-cpu]
+
+A step is one full forward pass (plan, gate + cumsum, in-tile WY, state pass,
+outputs) over one batch of synthetic input already resident in HBM.  The
+default workload is 1,048,576 tokens x 16 heads, dk = dv = 128, tile 16, bf16,
+bounded gate b = 2 (its inputs are 12.9 GB, far larger than the 129 MB L2, so
+no flush is needed between steps).  Under torchrun every rank runs its own
+replica on its own GPU (weak scaling, no collective on the data path); rank 0
+prints the line with the max-over-ranks time.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead, on
+a bounded prefix of the same workload per step, and prints the same line with
+"impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tokens/s and % roofline, gated-delta-rule chunk fwd at T=1M, H=16, d=128, bf16"
+UNIT = "tokens/s"
+
+# DRAM bytes (read + write) per launch of the dominant kernel as counted by ncu,
+# per (token, head) unit, with the hash of the kernel source they were taken at.
+# The value is reported only while the source is unchanged.
+NCU_TRAFFIC = {}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def algorithmic(w, n_tokens, with_h0):
+    """Bytes and FLOPs one pass must move / do: q, k, v, out, a, beta per
+    (token, head), the final state, and h0 when given."""
+    es = 2 if w.dtype == "bf16" else 4
+    per_tok = es * (2 * w.dk + 2 * w.dv) + 2 * es
+    nstate = (w.B if not w.varlen else 1) * w.H * w.dk * w.dv * 4
+    byt = per_tok * n_tokens * w.H + nstate * (2 if with_h0 else 1)
+    flops = (6 * w.chunk * w.dk + 4 * w.chunk * w.dv + 6 * w.dk * w.dv) * n_tokens * w.H
+    return byt, flops, per_tok
+
+
+def source_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()[:12]
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.3)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            try:
+                sm.append(float(f[1]))
+                smax = max(smax, float(f[2]))
+            except (ValueError, IndexError):
+                continue
+            for nm, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        loaded = [s for s in sm if s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def cpu_oracle_rate(x, w, budget_s, max_tokens):
+    """Time the oracle on a prefix of the workload; returns (tokens/s, tokens, threads, seconds)."""
+    import oracle
+    threads = oracle.max_threads()
+
+    def run(n):
+        sl = {k: x[k][:, :n].cpu() for k in ("q", "k", "v", "a", "beta")}
+        t0 = time.perf_counter()
+        oracle.oracle_fwd(sl["q"], sl["k"], sl["v"], sl["a"], sl["beta"], h0=None, b=w.b,
+                          gate=w.gate, nthreads=threads)
+        return time.perf_counter() - t0
+
+    n = 256
+    dt = run(n)
+    n = int(min(max_tokens, max(256, n * budget_s / max(dt, 1e-6))))
+    dt = run(n)
+    return n / dt, n, threads, dt
+
+
+def bench_reference(args, w):
+    """The oracle arm: fp64 CPU oracle, a bounded prefix of the workload per step."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    import torch
+
+    from gdr_inputs import make_inputs
+    threads = oracle.max_threads()
+    per_step_tokens = max(256, args.ref_tokens)
+    x = make_inputs(w, device="cpu", T=per_step_tokens)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.oracle_fwd(x["q"], x["k"], x["v"], x["a"], x["beta"], h0=x["h0"], b=w.b, gate=w.gate,
+                          nthreads=threads)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    tot = sum(times)
+    value = per_step_tokens * args.steps / tot
+    sample = (f"first {per_step_tokens} tokens of each of the {w.H} heads of workload {w.name} per step "
+              f"(fp64, token by token)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w):
+    shape = (f"varlen total={w.T}" if w.varlen else f"B={w.B} T={w.T}")
+    return {"workload": f"{w.name}: {shape} H={w.H} dk={w.dk} dv={w.dv} chunk={w.chunk} "
+                        f"{w.dtype} gate={w.gate} b={w.b}",
+            "tokens_per_step": w.T * (1 if w.varlen else w.B), "heads": w.H,
+            "l2_policy": "inputs larger than L2 (no flush)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="t1m")
+    ap.add_argument("--path", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    ap.add_argument("--ref-tokens", type=int, default=16384, help="tokens per reference step")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    from gdr_inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        bench_reference(args, w)
+        return
+
+    import torch
+    import chunked_gated_delta_07_gb300 as gdr
+    from gdr_inputs import make_inputs
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    gdr.lib()
+
+    x = make_inputs(w.with_(seed=w.seed + 7919 * rank), device=dev)
+    B, T, H, dk, dv = x["B"], x["T"], x["H"], x["dk"], x["dv"]
+    N = x["N"]
+    n_tokens = T if w.varlen else B * T
+    out = torch.empty_like(x["v"])
+    hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    dcode = gdr.GDR_BF16 if w.dtype == "bf16" else gdr.GDR_F32
+    gcode = gdr.GDR_GATE_BOUNDED if w.gate == "bounded" else gdr.GDR_GATE_SOFTPLUS
+    pcode = {"auto": gdr.GDR_PATH_AUTO, "simt": gdr.GDR_PATH_SIMT, "tc": gdr.GDR_PATH_TC}[args.path]
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        rc = gdr.gdr_chunk_fwd_ex(x["q"], x["k"], x["v"], x["a"], x["beta"], x["h0"], out, hT,
+                                  x["cu_seqlens"], N, T, H, dk, dv, w.chunk, w.b, dcode, gcode,
+                                  pcode, None, 0, stream)
+        if rc != gdr.GDR_OK:
+            raise gdr.GdrError(rc, "gdr_chunk_fwd_ex")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = gdr.gdr_get_status(stream)
+    if st != gdr.GDR_OK:
+        raise gdr.GdrError(st, "device status after warm-up")
+
+    # ---- timed region ----
+    gdr.gdr_profile_read()           # drop anything recorded so far
+    gdr.gdr_profile_enable(True)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        n_launch0 = gdr.gdr_launch_count()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        n_launch = gdr.gdr_launch_count() - n_launch0
+    gdr.gdr_profile_enable(False)
+    ms = ev0.elapsed_time(ev1)
+    if dist:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    prof = gdr.gdr_profile_read()
+    st = gdr.gdr_get_status(stream)
+    if st != gdr.GDR_OK:
+        raise gdr.GdrError(st, "device status after timed region")
+
+    ms_step = ms / args.steps
+    value = ws * n_tokens * args.steps / (ms / 1e3)
+    hbm, tf_burst, tf_sust, peak_src = peaks()
+    byt, flops, per_tok = algorithmic(w, n_tokens, x["h0"] is not None)
+    t_roof = max(byt / (hbm * 1e9), flops / (tf_sust * 1e12))
+    step_frac = t_roof / (ms_step / 1e3)
+
+    # dominant kernel: largest summed device time in the timed region
+    dom_name, (dom_ms, dom_n) = max(prof.items(), key=lambda kv: kv[1][0]) if prof else ("?", (0.0, 1))
+    dom_avg_s = dom_ms / max(dom_n, 1) / 1e3
+    units = n_tokens * H                                  # (token, head) units per launch
+    achieved = per_tok * units / dom_avg_s / 1e9 if dom_avg_s > 0 else 0.0
+    traffic = None
+    rec = NCU_TRAFFIC.get(dom_name)
+    if rec:
+        src = os.path.join(ROOT, "chunked_gated_delta_07_gb300", "csrc", rec["source"])
+        if os.path.exists(src) and source_hash(src) == rec["hash"] and rec.get("workload") == w.name:
+            traffic = rec["bytes_per_unit"] * units
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": traffic, "kernel": dom_name,
+                "peak_source": f"{peak_src} hbm_gbs",
+                "algorithmic_bytes_per_unit": per_tok, "units_per_launch": units,
+                "kernel_avg_ms": dom_avg_s * 1e3,
+                "kernel_share": dom_ms / sum(v[0] for v in prof.values()) if prof else None}
+
+    # ---- end to end through the host-buffer entry point ----
+    e2e = None
+    if not args.no_e2e and rank == 0:
+        e2e = bench_e2e(gdr, torch, x, w, args, dcode, gcode, pcode, n_tokens)
+
+    cpu = None
+    if not args.no_cpu and rank == 0 and ws == 1:
+        rate, ntok, threads, secs = cpu_oracle_rate(x, w, args.cpu_budget, n_tokens)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"first {ntok} tokens x {H} heads of workload {w.name}, fp64 oracle, "
+                         f"{secs:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": dict(workload_config(w), parallelism=f"replicas x{ws}", path=args.path),
+            "pct_roofline": 100.0 * step_frac,
+            "step_roofline": {"t_roof_ms": t_roof * 1e3, "bytes": byt, "flops": flops,
+                              "hbm_gbs": hbm, "bf16_tflops": tf_sust, "peak_source": peak_src},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_launch,
+            "kernels": {k: {"ms_total": v[0], "launches": v[1]} for k, v in prof.items()},
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def bench_e2e(gdr, torch, x, w, args, dcode, gcode, pcode, n_tokens):
+    """Same metric through gdr_chunk_fwd_host: pinned host inputs in, out and hT back."""
+    host = {n: x[n].cpu().pin_memory() for n in ("q", "k", "v", "a", "beta")}
+    h0 = x["h0"].cpu().pin_memory() if x["h0"] is not None else None
+    cu = x["cu_seqlens"].cpu() if x["cu_seqlens"] is not None else None
+    out = torch.empty(x["v"].shape, dtype=x["v"].dtype).pin_memory()
+    hT = torch.empty((x["N"], x["H"], x["dk"], x["dv"]), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d += 0 if h0 is None else h0.numel() * 4
+    h2d += 0 if cu is None else cu.numel() * 4
+    d2h = out.numel() * out.element_size() + hT.numel() * 4
+
+    def once():
+        rc = gdr.gdr_chunk_fwd_host(host["q"], host["k"], host["v"], host["a"], host["beta"], h0,
+                                    out, hT, cu, x["N"], x["T"], x["H"], x["dk"], x["dv"], w.chunk,
+                                    w.b, dcode, gcode, pcode, None)
+        if rc != gdr.GDR_OK:
+            raise gdr.GdrError(rc, "gdr_chunk_fwd_host")
+
+    once()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        once()
+    dt = (time.perf_counter() - t0) / args.e2e_steps
+    return {"value": n_tokens / dt, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "ms_per_step": dt * 1e3}
+
+
+if __name__ == "__main__":
+    main()

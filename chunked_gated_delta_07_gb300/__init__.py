@@ -1,0 +1,203 @@
+"""Chunked gated delta-rule forward pass on GB300 (sm_103a): Python binding.
+
+A thin ctypes layer over ``libgdr.so`` (the C ABI in ``include/gdr.h``).  It
+only marshals arguments -- tensors become device pointers, streams become
+``cudaStream_t`` -- and every step of the pass runs in the library's
+kernels.  There is no fallback: if the library is missing, importing a
+function raises.
+
+The functions keep the C names and argument order.  ``chunk_fwd`` is a
+convenience wrapper that allocates ``out`` / ``hT`` and raises on an error
+status.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libgdr.so")
+
+GDR_OK, GDR_ERR_INVALID_ARG, GDR_ERR_UNSUPPORTED, GDR_ERR_CUDA = 0, 1, 2, 3
+GDR_ERR_TIMEOUT, GDR_ERR_NO_WORKSPACE, GDR_ERR_BAD_SEQLENS = 4, 5, 6
+GDR_BF16, GDR_F32 = 0, 1
+GDR_GATE_BOUNDED, GDR_GATE_SOFTPLUS = 0, 1
+GDR_PATH_AUTO, GDR_PATH_SIMT, GDR_PATH_TC = 0, 1, 2
+
+EXPORTS = ("gdr_chunk_fwd", "gdr_chunk_fwd_ex", "gdr_chunk_fwd_workspace_size",
+           "gdr_chunk_fwd_host", "gdr_gate_cumsum", "gdr_wy_repr", "gdr_get_status",
+           "gdr_status_string", "gdr_release", "gdr_launch_count", "gdr_profile_enable",
+           "gdr_profile_read")
+
+_lock = threading.Lock()
+_lib = None
+
+_P, _I, _I64, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+_SIGS = {
+    "gdr_chunk_fwd": (_I, [_P] * 9 + [_I, _I64, _I, _I, _I, _I, _F, _P]),
+    "gdr_chunk_fwd_ex": (_I, [_P] * 9 + [_I, _I64, _I, _I, _I, _I, _F, _I, _I, _I, _P, _SZ, _P]),
+    "gdr_chunk_fwd_workspace_size": (_SZ, [_I, _I64, _I, _I, _I, _I, _I, _I]),
+    "gdr_chunk_fwd_host": (_I, [_P] * 9 + [_I, _I64, _I, _I, _I, _I, _F, _I, _I, _I, _P]),
+    "gdr_gate_cumsum": (_I, [_P, _P, _P, _I, _I64, _I, _I, _F, _I, _I, _P]),
+    "gdr_wy_repr": (_I, [_P] * 7 + [_I, _I64, _I, _I, _I, _I, _I, _P]),
+    "gdr_get_status": (_I, [_P]),
+    "gdr_status_string": (ctypes.c_char_p, [_I]),
+    "gdr_release": (None, []),
+    "gdr_launch_count": (ctypes.c_uint64, []),
+    "gdr_profile_enable": (None, [_I]),
+    "gdr_profile_read": (_I, [_P, _P, _P, _I]),
+}
+
+
+class GdrError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} (code {code})" if what else status_string(code))
+
+
+def lib():
+    """The loaded ``libgdr.so`` (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(
+                    f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; "
+                    "g.build()'` (needs nvcc)")
+            handle = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in _SIGS.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+    return _lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ---- the C functions, same names, argument marshalling only ---------------------------
+def gdr_chunk_fwd(q, k, v, a, beta, h0, out, hT, cu_seqlens, B, T, H, dk, dv, chunk, b,
+                  stream=None) -> int:
+    return lib().gdr_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(beta), _ptr(h0), _ptr(out),
+                               _ptr(hT), _ptr(cu_seqlens), B, T, H, dk, dv, chunk, float(b),
+                               _stream(stream))
+
+
+def gdr_chunk_fwd_ex(q, k, v, a, beta, h0, out, hT, cu_seqlens, B, T, H, dk, dv, chunk, b,
+                     dtype, gate, path, workspace=None, workspace_bytes=0, stream=None) -> int:
+    return lib().gdr_chunk_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(beta), _ptr(h0),
+                                  _ptr(out), _ptr(hT), _ptr(cu_seqlens), B, T, H, dk, dv, chunk,
+                                  float(b), dtype, gate, path, _ptr(workspace), workspace_bytes,
+                                  _stream(stream))
+
+
+def gdr_chunk_fwd_workspace_size(B, T, H, dk, dv, chunk, dtype=GDR_BF16, path=GDR_PATH_AUTO) -> int:
+    return int(lib().gdr_chunk_fwd_workspace_size(B, T, H, dk, dv, chunk, dtype, path))
+
+
+def gdr_chunk_fwd_host(q, k, v, a, beta, h0, out, hT, cu_seqlens, B, T, H, dk, dv, chunk, b,
+                       dtype, gate, path, stream=None) -> int:
+    """Host-buffer entry point: q..cu_seqlens are CPU tensors (pinned for full speed)."""
+    return lib().gdr_chunk_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(beta), _ptr(h0),
+                                    _ptr(out), _ptr(hT), _ptr(cu_seqlens), B, T, H, dk, dv, chunk,
+                                    float(b), dtype, gate, path, _stream(stream))
+
+
+def gdr_gate_cumsum(a, G, cu_seqlens, B, T, H, chunk, b, dtype, gate, stream=None) -> int:
+    return lib().gdr_gate_cumsum(_ptr(a), _ptr(G), _ptr(cu_seqlens), B, T, H, chunk, float(b),
+                                 dtype, gate, _stream(stream))
+
+
+def gdr_wy_repr(k, v, beta, G, W, U, cu_seqlens, B, T, H, dk, dv, chunk, dtype, stream=None) -> int:
+    return lib().gdr_wy_repr(_ptr(k), _ptr(v), _ptr(beta), _ptr(G), _ptr(W), _ptr(U),
+                             _ptr(cu_seqlens), B, T, H, dk, dv, chunk, dtype, _stream(stream))
+
+
+def gdr_get_status(stream=None) -> int:
+    return int(lib().gdr_get_status(_stream(stream)))
+
+
+def gdr_status_string(code: int) -> str:
+    return lib().gdr_status_string(int(code)).decode()
+
+
+def gdr_release() -> None:
+    lib().gdr_release()
+
+
+def gdr_launch_count() -> int:
+    return int(lib().gdr_launch_count())
+
+
+def gdr_profile_enable(on: bool) -> None:
+    lib().gdr_profile_enable(1 if on else 0)
+
+
+def gdr_profile_read(max_kernels: int = 32) -> dict:
+    """{kernel name: (total ms, launches)} since the last read (clears the record)."""
+    names = (ctypes.c_char_p * max_kernels)()
+    ms = (ctypes.c_double * max_kernels)()
+    cnt = (ctypes.c_int * max_kernels)()
+    n = lib().gdr_profile_read(ctypes.cast(names, ctypes.c_void_p), ctypes.cast(ms, ctypes.c_void_p),
+                               ctypes.cast(cnt, ctypes.c_void_p), max_kernels)
+    return {names[i].decode(): (float(ms[i]), int(cnt[i])) for i in range(min(n, max_kernels))}
+
+
+def status_string(code: int) -> str:
+    try:
+        return gdr_status_string(code)
+    except ImportError:
+        return f"status {code}"
+
+
+# ---- convenience -----------------------------------------------------------------------
+_GATES = {"bounded": GDR_GATE_BOUNDED, "softplus": GDR_GATE_SOFTPLUS}
+_PATHS = {"auto": GDR_PATH_AUTO, "simt": GDR_PATH_SIMT, "tc": GDR_PATH_TC}
+
+
+def dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return GDR_BF16
+    if t.dtype == torch.float32:
+        return GDR_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def chunk_fwd(q, k, v, a, beta, h0=None, cu_seqlens=None, chunk=16, b=2.0, gate="bounded",
+              path="auto", out=None, hT=None, want_state=True, stream=None, workspace=None):
+    """Allocate out (and hT), run gdr_chunk_fwd_ex, raise GdrError on a failing status.
+
+    q,k [B,T,H,dk], v [B,T,H,dv], a,beta [B,T,H] on one CUDA device, all of one
+    dtype (bf16 or fp32); with cu_seqlens (int32, N+1) B must be 1."""
+    import torch
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if hT is None and want_state:
+        hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = gdr_chunk_fwd_ex(q, k, v, a, beta, h0, out, hT, cu_seqlens, N if cu_seqlens is not None else B,
+                          T, H, dk, dv, chunk, b, dtype_code(q), _GATES[gate], _PATHS[path],
+                          workspace, ws_bytes, stream)
+    if rc != GDR_OK:
+        raise GdrError(rc, "gdr_chunk_fwd_ex")
+    return out, hT

@@ -1,0 +1,475 @@
+// gdr_api.cu -- the C ABI: argument checks, per-device state, workspace
+// layout and dispatch to the kernel families.  No arithmetic of the method
+// lives here; every step of the pass runs in the kernels.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "gdr_internal.cuh"
+#include "gdr_tc.cuh"
+
+namespace gdr {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+// ---- per-kernel event timing ------------------------------------------------
+namespace {
+struct ProfRec {
+    const char *name;
+    cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+std::atomic<bool> g_prof_on{false};
+std::vector<ProfRec> g_prof;
+std::vector<cudaEvent_t> g_prof_pool;
+
+cudaEvent_t prof_event() {
+    if (!g_prof_pool.empty()) {
+        cudaEvent_t e = g_prof_pool.back();
+        g_prof_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+}  // namespace
+
+ProfScope::ProfScope(cudaStream_t stream, const char *name) : stream_(stream), slot_(-1) {
+    if (!g_prof_on.load(std::memory_order_relaxed)) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    ProfRec r{name, prof_event(), prof_event()};
+    if (!r.start || !r.stop) return;
+    cudaEventRecord(r.start, stream_);
+    slot_ = (long)g_prof.size();
+    g_prof.push_back(r);
+}
+
+ProfScope::~ProfScope() {
+    if (slot_ < 0) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (slot_ < (long)g_prof.size()) cudaEventRecord(g_prof[slot_].stop, stream_);
+}
+
+namespace {
+
+struct DeviceCtx {
+    int *d_status = nullptr;
+    void *ws = nullptr;  // internal workspace cache
+    size_t ws_bytes = 0;
+    void *io = nullptr;  // device copies for the host-buffer entry point
+    size_t io_bytes = 0;
+};
+
+std::mutex g_mu;
+std::vector<DeviceCtx> g_ctx;
+
+// The calling thread's current device context, with its status word
+// allocated.  Returns nullptr on a CUDA failure.
+DeviceCtx *device_ctx() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((int)g_ctx.size() <= dev) g_ctx.resize(dev + 1);
+    DeviceCtx &c = g_ctx[dev];
+    if (!c.d_status) {
+        if (cudaMalloc(&c.d_status, sizeof(int)) != cudaSuccess) return nullptr;
+        if (cudaMemset(c.d_status, 0, sizeof(int)) != cudaSuccess) return nullptr;
+    }
+    return &c;
+}
+
+// Grow a cached device buffer to at least `bytes` (contents not preserved).
+bool grow(void **buf, size_t *have, size_t bytes) {
+    if (*have >= bytes) return true;
+    if (*buf) {
+        cudaDeviceSynchronize();  // the old buffer may still be in use
+        cudaFree(*buf);
+        *buf = nullptr;
+        *have = 0;
+    }
+    if (bytes == 0) return true;
+    if (cudaMalloc(buf, bytes) != cudaSuccess) {
+        *buf = nullptr;
+        return false;
+    }
+    *have = bytes;
+    return true;
+}
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Shape {
+    int N, H, dk, dv, C;
+    int64_t T_per, T_total;   // tokens per dense sequence / packed total
+    bool varlen;
+    int64_t max_chunks;       // upper bound on tiles over all sequences
+};
+
+// Scratch layout of one call.  Every region is 256-byte aligned.
+struct Layout {
+    size_t plan = 0, G = 0, Bt = 0, W = 0, U = 0, tc = 0, total = 0;
+};
+
+Layout layout_for(const Shape &s, gdr_path_t path) {
+    Layout L;
+    size_t off = 0;
+    L.plan = off;
+    off += align_up(3 * sizeof(int64_t) * (size_t)(s.N + 1));
+    L.G = off;
+    off += align_up(sizeof(float) * (size_t)s.H * s.T_total);
+    if (path == GDR_PATH_TC) {
+        L.Bt = off;
+        off += align_up(sizeof(float) * (size_t)s.H * s.T_total);
+        L.tc = off;
+        off += align_up(tc_workspace_bytes(s.N, s.H, s.T_total, s.C));
+    } else {
+        L.W = off;
+        off += align_up(sizeof(float) * (size_t)s.T_total * s.H * s.dk);
+        L.U = off;
+        off += align_up(sizeof(float) * (size_t)s.T_total * s.H * s.dv);
+    }
+    L.total = off;
+    return L;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const char *pa = (const char *)a, *pb = (const char *)b;
+    return pa < pb + nb && pb < pa + na;
+}
+
+// Checks shared by every forward entry point.  Fills `s` on success.
+gdr_status_t check_args(const void *q, const void *k, const void *v, const void *a,
+                        const void *beta, const float *h0, const void *out, const float *hT,
+                        const int32_t *cu, int B, int64_t T, int H, int dk, int dv, int chunk,
+                        float b, gdr_dtype_t dtype, gdr_gate_t gate, gdr_path_t path,
+                        Shape *s) {
+    if (dtype != GDR_BF16 && dtype != GDR_F32) return GDR_ERR_INVALID_ARG;
+    if (gate != GDR_GATE_BOUNDED && gate != GDR_GATE_SOFTPLUS) return GDR_ERR_INVALID_ARG;
+    if (path != GDR_PATH_AUTO && path != GDR_PATH_SIMT && path != GDR_PATH_TC)
+        return GDR_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || T < 0 || dk < 1 || dv < 1 || chunk < 1) return GDR_ERR_INVALID_ARG;
+    if (gate == GDR_GATE_BOUNDED && !(b > 0.f && std::isfinite(b))) return GDR_ERR_INVALID_ARG;
+    if ((dk != 64 && dk != 128) || (dv != 64 && dv != 128)) return GDR_ERR_UNSUPPORTED;
+    if (chunk != 16 && chunk != 32 && chunk != 64) return GDR_ERR_UNSUPPORTED;
+    if (T > ((int64_t)1 << 40) || (int64_t)B * T > ((int64_t)1 << 40)) return GDR_ERR_UNSUPPORTED;
+    const bool varlen = cu != nullptr;
+    const int64_t T_total = varlen ? T : (int64_t)B * T;
+    if (T_total > 0 && (!q || !k || !v || !a || !beta || !out)) return GDR_ERR_INVALID_ARG;
+    const size_t es = dtype == GDR_BF16 ? 2 : 4;
+    const size_t rows = (size_t)T_total * H;
+    const size_t n_state = (size_t)B * H * dk * dv * sizeof(float);
+    const void *ins[5] = {q, k, v, a, beta};
+    const size_t in_bytes[5] = {rows * dk * es, rows * dk * es, rows * dv * es, rows * es, rows * es};
+    const size_t out_bytes = rows * dv * es;
+    for (int i = 0; i < 5; ++i) {
+        if (overlaps(out, out_bytes, ins[i], in_bytes[i])) return GDR_ERR_INVALID_ARG;
+        if (overlaps(hT, n_state, ins[i], in_bytes[i])) return GDR_ERR_INVALID_ARG;
+    }
+    if (overlaps(out, out_bytes, h0, n_state) || overlaps(out, out_bytes, hT, n_state))
+        return GDR_ERR_INVALID_ARG;
+    if (hT && h0 && (const void *)hT != (const void *)h0 && overlaps(hT, n_state, h0, n_state))
+        return GDR_ERR_INVALID_ARG;
+    if (path == GDR_PATH_TC && !tc_supported(dtype, dk, dv, chunk)) return GDR_ERR_UNSUPPORTED;
+    s->N = B;
+    s->H = H;
+    s->dk = dk;
+    s->dv = dv;
+    s->C = chunk;
+    s->T_per = varlen ? 0 : T;
+    s->T_total = T_total;
+    s->varlen = varlen;
+    s->max_chunks = (T_total + chunk - 1) / chunk + (varlen ? B : 0);
+    return GDR_OK;
+}
+
+gdr_path_t resolve_path(gdr_path_t path, gdr_dtype_t dtype, int dk, int dv, int chunk) {
+    if (path != GDR_PATH_AUTO) return path;
+    return tc_supported(dtype, dk, dv, chunk) ? GDR_PATH_TC : GDR_PATH_SIMT;
+}
+
+gdr_status_t run_forward(const void *q, const void *k, const void *v, const void *a,
+                         const void *beta, const float *h0, void *out, float *hT,
+                         const int32_t *cu, const Shape &s, float b, gdr_dtype_t dtype,
+                         gdr_gate_t gate, gdr_path_t path, void *workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+    DeviceCtx *ctx = device_ctx();
+    if (!ctx) return GDR_ERR_CUDA;
+    const Layout L = layout_for(s, path);
+    char *ws = (char *)workspace;
+    if (ws) {
+        if (workspace_bytes < L.total) return GDR_ERR_NO_WORKSPACE;
+    } else {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!grow(&ctx->ws, &ctx->ws_bytes, L.total)) return GDR_ERR_CUDA;
+        ws = (char *)ctx->ws;
+    }
+    int64_t *seq_start = (int64_t *)(ws + L.plan);
+    int64_t *chunk_base = seq_start + (s.N + 1);
+    int64_t *seg_base = chunk_base + (s.N + 1);
+    float *G = (float *)(ws + L.G);
+    const int seg_chunks = path == GDR_PATH_TC ? tc_segment_chunks(s.N, s.H, s.T_total, s.C) : (1 << 30);
+    Plan plan{s.N, s.C, seg_chunks, seq_start, chunk_base, seg_base};
+
+    cudaError_t err = launch_plan(cu, s.N, s.T_per, s.T_total, s.C, seg_chunks, seq_start,
+                                  chunk_base, seg_base, ctx->d_status, stream);
+    if (err != cudaSuccess) return GDR_ERR_CUDA;
+    float *Bt = path == GDR_PATH_TC ? (float *)(ws + L.Bt) : nullptr;
+    err = launch_gate_cumsum(a, beta, dtype, G, Bt, plan, s.H, s.T_total, s.max_chunks, b, gate,
+                             stream);
+    if (err != cudaSuccess) return GDR_ERR_CUDA;
+    if (path == GDR_PATH_TC) {
+        err = launch_tc_forward(q, k, v, G, Bt, h0, out, hT, plan, s.H, s.T_total, s.max_chunks,
+                                ws + L.tc, ctx->d_status, stream);
+    } else {
+        float *W = (float *)(ws + L.W);
+        float *U = (float *)(ws + L.U);
+        err = launch_wy_simt(k, v, beta, G, W, U, dtype, plan, s.H, s.dk, s.dv, s.T_total,
+                             s.max_chunks, stream);
+        if (err != cudaSuccess) return GDR_ERR_CUDA;
+        err = launch_state_out_simt(q, k, W, U, G, h0, out, hT, dtype, plan, s.H, s.dk, s.dv,
+                                    s.T_total, stream);
+    }
+    return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace gdr
+
+using namespace gdr;
+
+extern "C" {
+
+gdr_status_t gdr_chunk_fwd_ex(const void *q, const void *k, const void *v, const void *a,
+                              const void *beta, const float *h0, void *out, float *hT,
+                              const int32_t *cu_seqlens, int B, int64_t T, int H, int dk,
+                              int dv, int chunk, float b, gdr_dtype_t dtype, gdr_gate_t gate,
+                              gdr_path_t path, void *workspace, size_t workspace_bytes,
+                              gdr_stream_t stream) {
+    Shape s;
+    gdr_status_t st = check_args(q, k, v, a, beta, h0, out, hT, cu_seqlens, B, T, H, dk, dv,
+                                 chunk, b, dtype, gate, path, &s);
+    if (st != GDR_OK) return st;
+    path = resolve_path(path, dtype, dk, dv, chunk);
+    return run_forward(q, k, v, a, beta, h0, out, hT, cu_seqlens, s, b, dtype, gate, path,
+                       workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+gdr_status_t gdr_chunk_fwd(const void *q, const void *k, const void *v, const void *a,
+                           const void *beta, const float *h0, void *out, float *hT,
+                           const int32_t *cu_seqlens, int B, int64_t T, int H, int dk, int dv,
+                           int chunk, float b, gdr_stream_t stream) {
+    return gdr_chunk_fwd_ex(q, k, v, a, beta, h0, out, hT, cu_seqlens, B, T, H, dk, dv, chunk, b,
+                            GDR_BF16, GDR_GATE_BOUNDED, GDR_PATH_AUTO, nullptr, 0, stream);
+}
+
+size_t gdr_chunk_fwd_workspace_size(int B, int64_t T, int H, int dk, int dv, int chunk,
+                                    gdr_dtype_t dtype, gdr_path_t path) {
+    if (B < 1 || H < 1 || T < 0 || (dk != 64 && dk != 128) || (dv != 64 && dv != 128) ||
+        (chunk != 16 && chunk != 32 && chunk != 64) || (dtype != GDR_BF16 && dtype != GDR_F32))
+        return 0;
+    path = resolve_path(path, dtype, dk, dv, chunk);
+    if (path == GDR_PATH_TC && !tc_supported(dtype, dk, dv, chunk)) return 0;
+    Shape s;
+    s.N = B;
+    s.H = H;
+    s.dk = dk;
+    s.dv = dv;
+    s.C = chunk;
+    // the larger of the dense (B*T tokens) and varlen (T tokens) readings
+    s.T_total = (int64_t)B * T > T ? (int64_t)B * T : T;
+    s.T_per = T;
+    s.varlen = false;
+    s.max_chunks = (s.T_total + chunk - 1) / chunk + B;
+    return layout_for(s, path).total;
+}
+
+gdr_status_t gdr_chunk_fwd_host(const void *q, const void *k, const void *v, const void *a,
+                                const void *beta, const float *h0, void *out, float *hT,
+                                const int32_t *cu_seqlens, int B, int64_t T, int H, int dk,
+                                int dv, int chunk, float b, gdr_dtype_t dtype, gdr_gate_t gate,
+                                gdr_path_t path, gdr_stream_t stream_) {
+    Shape s;
+    gdr_status_t st = check_args(q, k, v, a, beta, h0, out, hT, cu_seqlens, B, T, H, dk, dv,
+                                 chunk, b, dtype, gate, path, &s);
+    if (st != GDR_OK) return st;
+    cudaStream_t stream = (cudaStream_t)stream_;
+    DeviceCtx *ctx = device_ctx();
+    if (!ctx) return GDR_ERR_CUDA;
+    const size_t es = dtype == GDR_BF16 ? 2 : 4;
+    const size_t rows = (size_t)s.T_total * H;
+    const size_t nst = (size_t)B * H * dk * dv * sizeof(float);
+    const size_t sz[9] = {rows * dk * es, rows * dk * es, rows * dv * es, rows * es, rows * es,
+                          h0 ? nst : 0,   rows * dv * es, hT ? nst : 0,
+                          cu_seqlens ? sizeof(int32_t) * (size_t)(B + 1) : 0};
+    size_t off[9], tot = 0;
+    for (int i = 0; i < 9; ++i) {
+        off[i] = tot;
+        tot += align_up(sz[i]);
+    }
+    char *io;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!grow(&ctx->io, &ctx->io_bytes, tot)) return GDR_ERR_CUDA;
+        io = (char *)ctx->io;
+    }
+    const void *src[9] = {q, k, v, a, beta, h0, nullptr, nullptr, cu_seqlens};
+    for (int i = 0; i < 9; ++i)
+        if (src[i] && sz[i] &&
+            cudaMemcpyAsync(io + off[i], src[i], sz[i], cudaMemcpyHostToDevice, stream) != cudaSuccess)
+            return GDR_ERR_CUDA;
+    path = resolve_path(path, dtype, dk, dv, chunk);
+    st = run_forward(io + off[0], io + off[1], io + off[2], io + off[3], io + off[4],
+                     h0 ? (const float *)(io + off[5]) : nullptr, io + off[6],
+                     hT ? (float *)(io + off[7]) : nullptr,
+                     cu_seqlens ? (const int32_t *)(io + off[8]) : nullptr, s, b, dtype, gate,
+                     path, nullptr, 0, stream);
+    if (st != GDR_OK) return st;
+    if (s.T_total > 0 &&
+        cudaMemcpyAsync(out, io + off[6], sz[6], cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return GDR_ERR_CUDA;
+    if (hT && cudaMemcpyAsync(hT, io + off[7], sz[7], cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return GDR_ERR_CUDA;
+    return cudaStreamSynchronize(stream) == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
+gdr_status_t gdr_gate_cumsum(const void *a, float *G, const int32_t *cu_seqlens, int B,
+                             int64_t T, int H, int chunk, float b, gdr_dtype_t dtype,
+                             gdr_gate_t gate, gdr_stream_t stream) {
+    if (dtype != GDR_BF16 && dtype != GDR_F32) return GDR_ERR_INVALID_ARG;
+    if (gate != GDR_GATE_BOUNDED && gate != GDR_GATE_SOFTPLUS) return GDR_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || T < 0 || chunk < 1) return GDR_ERR_INVALID_ARG;
+    if (gate == GDR_GATE_BOUNDED && !(b > 0.f && std::isfinite(b))) return GDR_ERR_INVALID_ARG;
+    if (chunk != 16 && chunk != 32 && chunk != 64) return GDR_ERR_UNSUPPORTED;
+    const int64_t T_total = cu_seqlens ? T : (int64_t)B * T;
+    if (T_total > 0 && (!a || !G)) return GDR_ERR_INVALID_ARG;
+    DeviceCtx *ctx = device_ctx();
+    if (!ctx) return GDR_ERR_CUDA;
+    const size_t need = align_up(3 * sizeof(int64_t) * (size_t)(B + 1));
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!grow(&ctx->ws, &ctx->ws_bytes, need)) return GDR_ERR_CUDA;
+    }
+    int64_t *seq_start = (int64_t *)ctx->ws;
+    Plan plan{B, chunk, 1 << 30, seq_start, seq_start + (B + 1), seq_start + 2 * (B + 1)};
+    cudaStream_t st = (cudaStream_t)stream;
+    if (launch_plan(cu_seqlens, B, cu_seqlens ? 0 : T, T_total, chunk, 1 << 30, seq_start,
+                    seq_start + (B + 1), seq_start + 2 * (B + 1), ctx->d_status, st) != cudaSuccess)
+        return GDR_ERR_CUDA;
+    const int64_t max_chunks = (T_total + chunk - 1) / chunk + (cu_seqlens ? B : 0);
+    if (launch_gate_cumsum(a, nullptr, dtype, G, nullptr, plan, H, T_total, max_chunks, b, gate,
+                           st) != cudaSuccess)
+        return GDR_ERR_CUDA;
+    return GDR_OK;
+}
+
+gdr_status_t gdr_wy_repr(const void *k, const void *v, const void *beta, const float *G,
+                         float *W, float *U, const int32_t *cu_seqlens, int B, int64_t T, int H,
+                         int dk, int dv, int chunk, gdr_dtype_t dtype, gdr_stream_t stream) {
+    if (dtype != GDR_BF16 && dtype != GDR_F32) return GDR_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || T < 0 || chunk < 1 || dk < 1 || dv < 1) return GDR_ERR_INVALID_ARG;
+    if ((dk != 64 && dk != 128) || (dv != 64 && dv != 128)) return GDR_ERR_UNSUPPORTED;
+    if (chunk != 16 && chunk != 32 && chunk != 64) return GDR_ERR_UNSUPPORTED;
+    const int64_t T_total = cu_seqlens ? T : (int64_t)B * T;
+    if (T_total > 0 && (!k || !v || !beta || !G || !W || !U)) return GDR_ERR_INVALID_ARG;
+    DeviceCtx *ctx = device_ctx();
+    if (!ctx) return GDR_ERR_CUDA;
+    const size_t need = align_up(3 * sizeof(int64_t) * (size_t)(B + 1));
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!grow(&ctx->ws, &ctx->ws_bytes, need)) return GDR_ERR_CUDA;
+    }
+    int64_t *seq_start = (int64_t *)ctx->ws;
+    Plan plan{B, chunk, 1 << 30, seq_start, seq_start + (B + 1), seq_start + 2 * (B + 1)};
+    cudaStream_t st = (cudaStream_t)stream;
+    if (launch_plan(cu_seqlens, B, cu_seqlens ? 0 : T, T_total, chunk, 1 << 30, seq_start,
+                    seq_start + (B + 1), seq_start + 2 * (B + 1), ctx->d_status, st) != cudaSuccess)
+        return GDR_ERR_CUDA;
+    const int64_t max_chunks = (T_total + chunk - 1) / chunk + (cu_seqlens ? B : 0);
+    if (launch_wy_simt(k, v, beta, G, W, U, dtype, plan, H, dk, dv, T_total, max_chunks, st) !=
+        cudaSuccess)
+        return GDR_ERR_CUDA;
+    return GDR_OK;
+}
+
+gdr_status_t gdr_get_status(gdr_stream_t stream) {
+    DeviceCtx *ctx = device_ctx();
+    if (!ctx) return GDR_ERR_CUDA;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return GDR_ERR_CUDA;
+    int code = 0;
+    if (cudaMemcpy(&code, ctx->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GDR_ERR_CUDA;
+    if (code != 0 && cudaMemset(ctx->d_status, 0, sizeof(int)) != cudaSuccess) return GDR_ERR_CUDA;
+    return (gdr_status_t)code;
+}
+
+const char *gdr_status_string(gdr_status_t status) {
+    switch (status) {
+        case GDR_OK: return "ok";
+        case GDR_ERR_INVALID_ARG: return "invalid argument";
+        case GDR_ERR_UNSUPPORTED: return "unsupported size or option";
+        case GDR_ERR_CUDA: return "CUDA runtime error";
+        case GDR_ERR_TIMEOUT: return "device-side wait timed out";
+        case GDR_ERR_NO_WORKSPACE: return "workspace too small";
+        case GDR_ERR_BAD_SEQLENS: return "cu_seqlens is not a valid offset list";
+    }
+    return "unknown status";
+}
+
+void gdr_release(void) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (size_t d = 0; d < g_ctx.size(); ++d) {
+        DeviceCtx &c = g_ctx[d];
+        if (!c.ws && !c.io && !c.d_status) continue;
+        cudaSetDevice((int)d);
+        cudaDeviceSynchronize();
+        if (c.ws) cudaFree(c.ws);
+        if (c.io) cudaFree(c.io);
+        if (c.d_status) cudaFree(c.d_status);
+        c = DeviceCtx{};
+    }
+    cudaSetDevice(cur);
+}
+
+uint64_t gdr_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+void gdr_profile_enable(int on) { g_prof_on.store(on != 0); }
+
+int gdr_profile_read(const char **names, double *total_ms, int *launches, int max) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    std::vector<const char *> nm;
+    std::vector<double> ms;
+    std::vector<int> cnt;
+    for (const ProfRec &r : g_prof) {
+        float t = 0.f;
+        cudaEventSynchronize(r.stop);
+        if (cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess) t = 0.f;
+        size_t i = 0;
+        while (i < nm.size() && std::strcmp(nm[i], r.name) != 0) ++i;
+        if (i == nm.size()) {
+            nm.push_back(r.name);
+            ms.push_back(0.0);
+            cnt.push_back(0);
+        }
+        ms[i] += t;
+        cnt[i] += 1;
+        g_prof_pool.push_back(r.start);
+        g_prof_pool.push_back(r.stop);
+    }
+    g_prof.clear();
+    for (size_t i = 0; i < nm.size() && (int)i < max; ++i) {
+        if (names) names[i] = nm[i];
+        if (total_ms) total_ms[i] = ms[i];
+        if (launches) launches[i] = cnt[i];
+    }
+    return (int)nm.size();
+}
+
+}  // extern "C"

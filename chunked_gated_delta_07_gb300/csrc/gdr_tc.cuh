@@ -1,0 +1,23 @@
+// gdr_tc.cuh -- the tcgen05 (5th-generation tensor core) path: host-side entry points.
+#pragma once
+
+#include "gdr_internal.cuh"
+
+namespace gdr {
+
+// True when the tensor-core path implements this shape and dtype.
+bool tc_supported(gdr_dtype_t dtype, int dk, int dv, int chunk);
+
+// Tiles per segment for the segment-parallel state pass.
+int tc_segment_chunks(int N, int H, int64_t T_total, int C);
+
+// Scratch bytes of the tensor-core path beyond the plan, G and Bt.
+size_t tc_workspace_bytes(int N, int H, int64_t T_total, int C);
+
+// Stages 2-4 on the tensor cores (stage 1, plan and G/Bt already enqueued).
+cudaError_t launch_tc_forward(const void *q, const void *k, const void *v, const float *G,
+                              const float *Bt, const float *h0, void *out, float *hT, Plan plan,
+                              int H, int64_t T_total, int64_t max_chunks, void *scratch,
+                              int *status, cudaStream_t stream);
+
+}  // namespace gdr

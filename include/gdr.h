@@ -1,0 +1,202 @@
+/*
+ * gdr.h -- C ABI of the chunked gated delta-rule forward pass on GB300 (sm_103a).
+ *
+ * The operation.  For every (sequence, head) unit, with per-token inputs
+ * q_t, k_t in R^dk, v_t in R^dv, a gate logit a_t and a write strength
+ * beta_t, the library computes
+ *
+ *     g_t   = -b * sigmoid(a_t)        (bounded gate, GDR_GATE_BOUNDED)
+ *           = -softplus(a_t)           (unbounded gate, GDR_GATE_SOFTPLUS)
+ *     H_t   = exp(g_t) H_{t-1} + beta_t k_t (v_t - exp(g_t) H_{t-1}^T k_t)^T
+ *     o_t   = H_t^T q_t
+ *
+ * with H the dk x dv fp32 state (H = S^T for the dv x dk delta-rule state
+ * S_t = alpha_t S_{t-1}(I - beta_t k_t k_t^T) + beta_t v_t k_t^T, o_t = S_t q_t,
+ * alpha_t = exp(g_t)),
+ * starting from h0 and ending in hT.  The bounded gate is the scaled-sigmoid
+ * log-decay the pages introduce in place of the unbounded negative softplus
+ * ("Deep Dive: The Next Generation of Ultra-Long Context Sparse MoE LLMs",
+ * §3.3; "Core Technologies Behind Ultra-Long-Context Sparse MoE Large
+ * Models", §2.2; "How Trillion-Scale Sparse MoE Models Achieve Million-Token
+ * Long Context Capabilities", §3.2; "Evaluating Next-Gen Sparse MoE and
+ * Long-Context LLMs", §2.3); the pages fix b = 5 there, b is a parameter
+ * here.  The state update is the delta-rule write with data-dependent decay
+ * of the incremental linear-attention layer ("Evaluating Next-Gen Sparse MoE
+ * and Long-Context LLMs", §2.2).  It is computed chunk-parallel: the
+ * sequence is cut into tiles of `chunk` tokens, each tile is a set of dense
+ * products, and the state is passed from tile to tile ("Deep Dive ...",
+ * §3.2; "Core Technologies ...", §2.1).  The result does not depend on
+ * `chunk` beyond rounding.
+ *
+ * Layouts (row-major, contiguous, element type = dtype unless stated):
+ *   dense  (cu_seqlens == NULL): q,k [B,T,H,dk]  v,out [B,T,H,dv]  a,beta [B,T,H]
+ *   varlen (cu_seqlens != NULL): the same tensors with a leading 1 instead of B
+ *          and T = total tokens; cu_seqlens holds N+1 int32 offsets (device
+ *          memory), cu[0] = 0, non-decreasing, cu[N] = T; B is then N.
+ *          Tiles restart at every sequence start; a partial last tile is masked.
+ *   h0, hT : [N,H,dk,dv] fp32 (N = B for dense input).  h0 == NULL means zero.
+ *          hT may be NULL (not written) and may alias h0 (in-place carry).
+ *   beta is a probability (used as given, not passed through a sigmoid).
+ *   q and k are used as given: no scaling, no normalisation.
+ *
+ * Ownership and concurrency.  All tensor pointers of gdr_chunk_fwd* and of
+ * the stage calls are DEVICE pointers owned by the caller; the library
+ * retains none of them.  Calls are asynchronous on `stream` (NULL = the
+ * legacy default stream).  Scratch memory comes from `workspace` if given,
+ * else from a cache the library keeps per device (grown with cudaMalloc,
+ * freed by gdr_release).  Calls that share the internal cache must not
+ * overlap on the GPU: issue them on one stream, or pass each stream its own
+ * workspace.
+ *
+ * Errors.  Arguments are checked before anything is launched: unsupported
+ * sizes return GDR_ERR_UNSUPPORTED, malformed ones GDR_ERR_INVALID_ARG.  A
+ * failed CUDA call returns GDR_ERR_CUDA.  Conditions only the device can see
+ * (cu_seqlens that are not a valid offset list, a bounded wait that gave
+ * up) set a per-device status word; gdr_get_status() reads and clears it.
+ */
+#ifndef GDR_H_
+#define GDR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define GDR_API __attribute__((visibility("default")))
+#else
+#define GDR_API
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *gdr_stream_t; /* the same type as cudaStream_t */
+
+typedef enum {
+    GDR_OK = 0,
+    GDR_ERR_INVALID_ARG = 1,  /* null required pointer, negative size, ...     */
+    GDR_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. dk = 96)       */
+    GDR_ERR_CUDA = 3,         /* a CUDA runtime call failed                      */
+    GDR_ERR_TIMEOUT = 4,      /* a bounded device-side wait ran out              */
+    GDR_ERR_NO_WORKSPACE = 5, /* caller workspace smaller than required          */
+    GDR_ERR_BAD_SEQLENS = 6   /* cu_seqlens is not 0 = c0 <= c1 <= ... <= cN = T */
+} gdr_status_t;
+
+typedef enum { GDR_BF16 = 0, GDR_F32 = 1 } gdr_dtype_t;
+
+typedef enum {
+    GDR_GATE_BOUNDED = 0, /* g = -b * sigmoid(a), g in [-b, 0]   */
+    GDR_GATE_SOFTPLUS = 1 /* g = -softplus(a),    g in (-inf, 0) */
+} gdr_gate_t;
+
+typedef enum {
+    GDR_PATH_AUTO = 0, /* tensor-core path where supported, else SIMT            */
+    GDR_PATH_SIMT = 1, /* fp32 CUDA-core path (any supported shape and dtype)     */
+    GDR_PATH_TC = 2    /* tcgen05 path; GDR_ERR_UNSUPPORTED where it does not apply */
+} gdr_path_t;
+
+/*
+ * The forward pass with the defaults: dtype bf16, bounded gate with bound b,
+ * automatic path, internal workspace.
+ *   q,k,v,a,beta : inputs, layouts above (bf16)
+ *   h0           : initial state or NULL (zero)
+ *   out          : output, bf16, layout above; must not alias an input
+ *   hT           : final state or NULL
+ *   cu_seqlens   : NULL (dense) or N+1 int32 device offsets (varlen)
+ *   B, T, H      : batch (or N), tokens per sequence (or total), heads
+ *   dk, dv       : key / value width, each 64 or 128
+ *   chunk        : tile length, 16, 32 or 64
+ *   b            : gate bound, > 0 and finite
+ * Supported sizes: B, H >= 1, T >= 0 (T = 0 copies h0 to hT, or zeroes hT).
+ */
+GDR_API gdr_status_t gdr_chunk_fwd(const void *q, const void *k, const void *v, const void *a,
+                           const void *beta, const float *h0, void *out, float *hT,
+                           const int32_t *cu_seqlens, int B, int64_t T, int H, int dk,
+                           int dv, int chunk, float b, gdr_stream_t stream);
+
+/*
+ * The forward pass with every option.
+ *   dtype       : element type of q, k, v, a, beta and out
+ *   gate        : gate form; b is ignored for GDR_GATE_SOFTPLUS
+ *   path        : kernel family (see gdr_path_t)
+ *   workspace   : device scratch of workspace_bytes >= gdr_chunk_fwd_workspace_size(...),
+ *                 or NULL for the internal per-device cache
+ */
+GDR_API gdr_status_t gdr_chunk_fwd_ex(const void *q, const void *k, const void *v, const void *a,
+                              const void *beta, const float *h0, void *out, float *hT,
+                              const int32_t *cu_seqlens, int B, int64_t T, int H, int dk,
+                              int dv, int chunk, float b, gdr_dtype_t dtype, gdr_gate_t gate,
+                              gdr_path_t path, void *workspace, size_t workspace_bytes,
+                              gdr_stream_t stream);
+
+/* Scratch bytes gdr_chunk_fwd_ex needs for these sizes (0 on invalid sizes).
+ * B is N (the sequence count) for varlen input. */
+GDR_API size_t gdr_chunk_fwd_workspace_size(int B, int64_t T, int H, int dk, int dv, int chunk,
+                                    gdr_dtype_t dtype, gdr_path_t path);
+
+/*
+ * The forward pass on HOST buffers: inputs are copied to the device, the
+ * pass runs, out (and hT) are copied back, and the call returns after the
+ * copies have finished (it synchronises `stream`).  Same arguments and
+ * layouts as gdr_chunk_fwd_ex except that every tensor pointer, including
+ * cu_seqlens, is host memory (pinned memory gives full copy bandwidth).
+ * Device buffers come from the internal per-device cache.
+ */
+GDR_API gdr_status_t gdr_chunk_fwd_host(const void *q, const void *k, const void *v, const void *a,
+                                const void *beta, const float *h0, void *out, float *hT,
+                                const int32_t *cu_seqlens, int B, int64_t T, int H, int dk,
+                                int dv, int chunk, float b, gdr_dtype_t dtype, gdr_gate_t gate,
+                                gdr_path_t path, gdr_stream_t stream);
+
+/*
+ * Stage 1 alone: the gate and its in-tile cumulative sum.
+ *   G[h, r] = sum over tokens r' of r's tile with r' <= r of g(a[r', h]),
+ * written head-major as G [H, B*T] fp32 (token rows packed as in a).
+ * Tiles restart at every sequence start ("Deep Dive ...", §3.2-3.3).
+ */
+GDR_API gdr_status_t gdr_gate_cumsum(const void *a, float *G, const int32_t *cu_seqlens, int B,
+                             int64_t T, int H, int chunk, float b, gdr_dtype_t dtype,
+                             gdr_gate_t gate, gdr_stream_t stream);
+
+/*
+ * Stage 2 alone: the per-tile WY / UT representation.  With G from
+ * gdr_gate_cumsum (layout above), per tile of length C
+ *   A_ij = beta_i exp(G_i - G_j) (k_i . k_j) for j < i,  T = (I + A)^{-1},
+ *   W = T diag(beta exp(G)) K  [C x dk],  U = T diag(beta) V  [C x dv],
+ * written fp32 in the layouts of k and v: W [B,T,H,dk], U [B,T,H,dv].
+ */
+GDR_API gdr_status_t gdr_wy_repr(const void *k, const void *v, const void *beta, const float *G,
+                         float *W, float *U, const int32_t *cu_seqlens, int B, int64_t T,
+                         int H, int dk, int dv, int chunk, gdr_dtype_t dtype,
+                         gdr_stream_t stream);
+
+/* Synchronise `stream`, then read and clear the current device's status word.
+ * Returns GDR_OK, GDR_ERR_BAD_SEQLENS, GDR_ERR_TIMEOUT or GDR_ERR_CUDA. */
+GDR_API gdr_status_t gdr_get_status(gdr_stream_t stream);
+
+/* Static description of a status code (never NULL). */
+GDR_API const char *gdr_status_string(gdr_status_t status);
+
+/* Free the internal per-device caches of every device (synchronises them). */
+GDR_API void gdr_release(void);
+
+/* Number of kernels this library has launched so far in this process. */
+GDR_API uint64_t gdr_launch_count(void);
+
+/*
+ * Per-kernel timing.  While enabled, every kernel the library launches is
+ * bracketed by a pair of CUDA events recorded on its launch stream.
+ * gdr_profile_read synchronises those events, writes for up to `max`
+ * distinct kernels its name (a static string), the summed device time in
+ * milliseconds and the launch count, returns the number of distinct kernels
+ * seen (which may exceed `max`), and clears the record.  Enabling adds two
+ * event records per launch and nothing else.
+ */
+GDR_API void gdr_profile_enable(int on);
+GDR_API int gdr_profile_read(const char **names, double *total_ms, int *launches, int max);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDR_H_ */

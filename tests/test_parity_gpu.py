@@ -1,0 +1,232 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Every comparison is element by element on the same seeded inputs, at sizes
+the oracle finishes in seconds that span several tiles and a ragged tail.
+Tolerances: fp32 workloads rel-L2 <= 1e-4; bf16 workloads rel-L2 <= 1e-2 and
+max-abs <= 5e-2, on both out and hT.
+"""
+import numpy as np
+import pytest
+import torch
+
+import chunked_gated_delta_07_gb300 as gdr
+from gdr_inputs import WORKLOADS, h32_variant, make_inputs, softplus_variant
+from gpu_helpers import assert_close, rel_l2, run_gpu, run_oracle, to64
+from oracle import chunk_ref
+
+pytestmark = pytest.mark.gpu
+
+
+def _tc_available(chunk=16):
+    return gdr.gdr_chunk_fwd_workspace_size(1, 64, 1, 128, 128, chunk, gdr.GDR_BF16,
+                                            gdr.GDR_PATH_TC) > 0
+
+
+def _paths(dtype="bf16", d=128, chunk=16):
+    ps = ["simt"]
+    if dtype == "bf16" and d == 128 and _tc_available(chunk):
+        ps.append("tc")
+    return ps
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from chunked_gated_delta_07_gb300 import _build
+    _build.build()
+    torch.cuda.set_device(0)
+
+
+# ---------------------------------------------------------------------------
+# stage 1: gate + in-tile cumsum
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("gate,b,a_std", [("bounded", 2.0, 1.0), ("bounded", 8.0, 2.0),
+                                          ("bounded", 5.0, 1.0), ("softplus", 0.0, 3.0)])
+@pytest.mark.parametrize("chunk", [16, 64])
+def test_gate_cumsum_stage(gate, b, a_std, chunk):
+    w = WORKLOADS["varlen_1m"].with_(gate=gate, b=b or 2.0, a_std=a_std, chunk=chunk,
+                                     len_min=1, len_max=700)
+    x = make_inputs(w, device="cuda", T=3000)
+    T, H = x["T"], x["H"]
+    G = torch.empty((H, T), dtype=torch.float32, device="cuda")
+    rc = gdr.gdr_gate_cumsum(x["a"], G, x["cu_seqlens"], x["N"], T, H, chunk, b or 2.0,
+                             gdr.GDR_BF16, gdr.GDR_GATE_BOUNDED if gate == "bounded" else gdr.GDR_GATE_SOFTPLUS)
+    assert rc == gdr.GDR_OK
+    assert gdr.gdr_get_status() == gdr.GDR_OK
+    cu = x["cu_seqlens"].cpu().numpy()
+    a = to64(x["a"])[0]
+    ref = np.zeros((H, T))
+    for n in range(len(cu) - 1):
+        for h in range(H):
+            g = chunk_ref.gate(a[cu[n]:cu[n + 1], h], b or 2.0, gate)
+            ref[h, cu[n]:cu[n + 1]] = chunk_ref.tile_cumsum(g, chunk)
+    got = to64(G)
+    scale = np.maximum(1.0, np.abs(ref))
+    assert np.max(np.abs(got - ref) / scale) < 2e-5
+
+
+# ---------------------------------------------------------------------------
+# stage 2: WY / UT representation
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("chunk", [16, 32, 64])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_wy_stage(chunk, dtype):
+    w = WORKLOADS["b2_t4k"].with_(chunk=chunk, dtype=dtype, H=3)
+    x = make_inputs(w, device="cuda", T=300)
+    B, T, H, dk, dv = x["B"], x["T"], x["H"], x["dk"], x["dv"]
+    dcode = gdr.GDR_BF16 if dtype == "bf16" else gdr.GDR_F32
+    G = torch.empty((H, B * T), dtype=torch.float32, device="cuda")
+    assert gdr.gdr_gate_cumsum(x["a"], G, None, B, T, H, chunk, 2.0, dcode, 0) == gdr.GDR_OK
+    W = torch.empty((B, T, H, dk), dtype=torch.float32, device="cuda")
+    U = torch.empty((B, T, H, dv), dtype=torch.float32, device="cuda")
+    assert gdr.gdr_wy_repr(x["k"], x["v"], x["beta"], G, W, U, None, B, T, H, dk, dv, chunk,
+                           dcode) == gdr.GDR_OK
+    assert gdr.gdr_get_status() == gdr.GDR_OK
+    k, v, a, beta = (to64(x[n]) for n in ("k", "v", "a", "beta"))
+    Wg, Ug = to64(W), to64(U)
+    for bi in range(B):
+        for h in range(H):
+            g = chunk_ref.gate(a[bi, :, h], 2.0)
+            Wr, Ur = chunk_ref.unit_wy(k[bi, :, h], v[bi, :, h], beta[bi, :, h], g, chunk)
+            assert rel_l2(Wg[bi, :, h], Wr) < 1e-5
+            assert rel_l2(Ug[bi, :, h], Ur) < 1e-5
+
+
+# ---------------------------------------------------------------------------
+# the whole pass: out and hT against the token-by-token oracle
+# ---------------------------------------------------------------------------
+def test_small_fp32_full_size():
+    w = WORKLOADS["small_fp32"]
+    x = make_inputs(w, device="cuda")
+    out, hT = run_gpu(x, path="simt")
+    ro, rh = run_oracle(x)
+    assert_close(to64(out), ro, "f32", "out")
+    assert_close(to64(hT), rh, "f32", "hT")
+
+
+@pytest.mark.parametrize("path", _paths())
+def test_b2_t4k_full_size(path):
+    w = WORKLOADS["b2_t4k"]
+    x = make_inputs(w, device="cuda")
+    out, hT = run_gpu(x, path=path)
+    ro, rh = run_oracle(x)
+    assert_close(to64(out), ro, "bf16", "out")
+    assert_close(to64(hT), rh, "bf16", "hT")
+
+
+@pytest.mark.parametrize("chunk", [16, 32, 64])
+@pytest.mark.parametrize("b", [2, 8])
+def test_h32_sweep_reduced(chunk, b):
+    w = h32_variant(chunk, b)
+    x = make_inputs(w, device="cuda", T=1500)
+    ro, rh = run_oracle(x)
+    for path in _paths(chunk=chunk):
+        out, hT = run_gpu(x, path=path)
+        assert_close(to64(out), ro, "bf16", f"out[{path}]")
+        assert_close(to64(hT), rh, "bf16", f"hT[{path}]")
+
+
+@pytest.mark.parametrize("gate", ["bounded", "softplus"])
+def test_varlen_reduced(gate):
+    w = WORKLOADS["varlen_1m"].with_(len_min=40, len_max=2000)
+    if gate == "softplus":
+        w = softplus_variant(w)
+    x = make_inputs(w, device="cuda", T=12000)
+    ro, rh = run_oracle(x)
+    for path in _paths():
+        out, hT = run_gpu(x, path=path)
+        assert_close(to64(out), ro, "bf16", f"out[{path}]")
+        assert_close(to64(hT), rh, "bf16", f"hT[{path}]")
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 128), (128, 64), (64, 64)])
+def test_mixed_widths_bf16(dk, dv):
+    w = WORKLOADS["b2_t4k"].with_(dk=dk, dv=dv, H=2)
+    x = make_inputs(w, device="cuda", T=333)
+    out, hT = run_gpu(x)
+    ro, rh = run_oracle(x)
+    assert_close(to64(out), ro, "bf16", "out")
+    assert_close(to64(hT), rh, "bf16", "hT")
+
+
+# ---------------------------------------------------------------------------
+# edge cases
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("T", [1, 5, 16, 17])
+def test_short_sequences(T):
+    w = WORKLOADS["b2_t4k"].with_(H=2)
+    x = make_inputs(w, device="cuda", T=T)
+    ro, rh = run_oracle(x)
+    for path in _paths():
+        out, hT = run_gpu(x, path=path)
+        assert_close(to64(out), ro, "bf16", f"out[{path}]")
+        assert_close(to64(hT), rh, "bf16", f"hT[{path}]")
+
+
+def test_zero_length_copies_state():
+    w = WORKLOADS["b2_t4k"].with_(H=2)
+    x = make_inputs(w, device="cuda", T=0)
+    for path in _paths():
+        out, hT = run_gpu(x, path=path)
+        assert torch.equal(hT, x["h0"])
+        x2 = dict(x, h0=None)
+        _, hT0 = run_gpu(x2, path=path, h0=None)
+        assert torch.count_nonzero(hT0).item() == 0
+
+
+def test_varlen_with_empty_sequences():
+    w = WORKLOADS["varlen_1m"]
+    x = make_inputs(w, device="cuda", T=500)
+    cu = torch.tensor([0, 0, 100, 100, 117, 500, 500], dtype=torch.int32, device="cuda")
+    h0 = 0.02 * torch.randn((6, w.H, 128, 128), device="cuda",
+                            generator=torch.Generator(device="cuda").manual_seed(5))
+    x = dict(x, cu_seqlens=cu, h0=h0, N=6)
+    ro, rh = run_oracle(x)
+    for path in _paths():
+        out, hT = run_gpu(x, path=path)
+        assert_close(to64(out), ro, "bf16", f"out[{path}]")
+        assert_close(to64(hT), rh, "bf16", f"hT[{path}]")
+        for n in (0, 2, 5):   # empty sequences carry h0 through unchanged
+            assert torch.equal(hT[n], h0[n])
+
+
+def test_in_place_state_carry():
+    w = WORKLOADS["b2_t4k"].with_(H=2)
+    x = make_inputs(w, device="cuda", T=100)
+    ro, rh = run_oracle(x)
+    for path in _paths():
+        h = x["h0"].clone()
+        out, hT = gdr.chunk_fwd(x["q"], x["k"], x["v"], x["a"], x["beta"], h0=h, hT=h,
+                                chunk=16, b=2.0, path=path)
+        torch.cuda.synchronize()
+        assert hT.data_ptr() == h.data_ptr()
+        assert_close(to64(h), rh, "bf16", f"hT[{path}]")
+
+
+def test_bad_cu_seqlens_sets_status():
+    w = WORKLOADS["varlen_1m"]
+    x = make_inputs(w, device="cuda", T=256)
+    for bad in ([0, 100, 50, 256], [1, 100, 256], [0, 100, 200]):
+        cu = torch.tensor(bad, dtype=torch.int32, device="cuda")
+        out = torch.empty_like(x["v"])
+        hT = torch.empty((len(bad) - 1, w.H, 128, 128), device="cuda")
+        rc = gdr.gdr_chunk_fwd_ex(x["q"], x["k"], x["v"], x["a"], x["beta"], None, out, hT, cu,
+                                  len(bad) - 1, 256, w.H, 128, 128, 16, 2.0, gdr.GDR_BF16,
+                                  gdr.GDR_GATE_BOUNDED, gdr.GDR_PATH_AUTO, None, 0, None)
+        assert rc == gdr.GDR_OK   # the offsets live on the device: caught there
+        assert gdr.gdr_get_status() == gdr.GDR_ERR_BAD_SEQLENS
+        assert gdr.gdr_get_status() == gdr.GDR_OK   # read-and-clear
+
+
+def test_host_buffer_entry_point():
+    w = WORKLOADS["b2_t4k"].with_(H=2)
+    x = make_inputs(w, device="cpu", T=150)
+    out = torch.empty_like(x["v"]).pin_memory()
+    hT = torch.empty((x["B"], 2, 128, 128), dtype=torch.float32).pin_memory()
+    args = [x[n].pin_memory() for n in ("q", "k", "v", "a", "beta")]
+    rc = gdr.gdr_chunk_fwd_host(*args, x["h0"].pin_memory(), out, hT, None, x["B"], x["T"], 2, 128,
+                                128, 16, 2.0, gdr.GDR_BF16, gdr.GDR_GATE_BOUNDED,
+                                gdr.GDR_PATH_AUTO, None)
+    assert rc == gdr.GDR_OK
+    ro, rh = run_oracle(x)
+    assert_close(to64(out), ro, "bf16", "out")
+    assert_close(to64(hT), rh, "bf16", "hT")
