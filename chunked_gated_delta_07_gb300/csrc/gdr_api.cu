@@ -100,6 +100,12 @@ bool grow(void **buf, size_t *have, size_t bytes) {
     return true;
 }
 
+// Upper bound on the tiles of all sequences: every dense sequence ends in its
+// own partial tile; packed sequences can each add one partial tile.
+inline int64_t tile_bound(bool varlen, int B, int64_t T, int chunk) {
+    return varlen ? (T + chunk - 1) / chunk + B : (int64_t)B * ((T + chunk - 1) / chunk);
+}
+
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -184,7 +190,7 @@ gdr_status_t check_args(const void *q, const void *k, const void *v, const void 
     s->T_per = varlen ? 0 : T;
     s->T_total = T_total;
     s->varlen = varlen;
-    s->max_chunks = (T_total + chunk - 1) / chunk + (varlen ? B : 0);
+    s->max_chunks = tile_bound(varlen, B, T, chunk);
     return GDR_OK;
 }
 
@@ -285,7 +291,7 @@ size_t gdr_chunk_fwd_workspace_size(int B, int64_t T, int H, int dk, int dv, int
     s.T_total = (int64_t)B * T > T ? (int64_t)B * T : T;
     s.T_per = T;
     s.varlen = false;
-    s.max_chunks = (s.T_total + chunk - 1) / chunk + B;
+    s.max_chunks = tile_bound(true, B, s.T_total, chunk);
     return layout_for(s, path).total;
 }
 
@@ -361,7 +367,7 @@ gdr_status_t gdr_gate_cumsum(const void *a, float *G, const int32_t *cu_seqlens,
     if (launch_plan(cu_seqlens, B, cu_seqlens ? 0 : T, T_total, chunk, 1 << 30, seq_start,
                     seq_start + (B + 1), seq_start + 2 * (B + 1), ctx->d_status, st) != cudaSuccess)
         return GDR_ERR_CUDA;
-    const int64_t max_chunks = (T_total + chunk - 1) / chunk + (cu_seqlens ? B : 0);
+    const int64_t max_chunks = tile_bound(cu_seqlens != nullptr, B, T, chunk);
     if (launch_gate_cumsum(a, nullptr, dtype, G, nullptr, plan, H, T_total, max_chunks, b, gate,
                            st) != cudaSuccess)
         return GDR_ERR_CUDA;
@@ -390,7 +396,7 @@ gdr_status_t gdr_wy_repr(const void *k, const void *v, const void *beta, const f
     if (launch_plan(cu_seqlens, B, cu_seqlens ? 0 : T, T_total, chunk, 1 << 30, seq_start,
                     seq_start + (B + 1), seq_start + 2 * (B + 1), ctx->d_status, st) != cudaSuccess)
         return GDR_ERR_CUDA;
-    const int64_t max_chunks = (T_total + chunk - 1) / chunk + (cu_seqlens ? B : 0);
+    const int64_t max_chunks = tile_bound(cu_seqlens != nullptr, B, T, chunk);
     if (launch_wy_simt(k, v, beta, G, W, U, dtype, plan, H, dk, dv, T_total, max_chunks, st) !=
         cudaSuccess)
         return GDR_ERR_CUDA;
