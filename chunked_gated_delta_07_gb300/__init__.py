@@ -28,7 +28,7 @@ GDR_PATH_AUTO, GDR_PATH_SIMT, GDR_PATH_TC = 0, 1, 2
 EXPORTS = ("gdr_chunk_fwd", "gdr_chunk_fwd_ex", "gdr_chunk_fwd_workspace_size",
            "gdr_chunk_fwd_host", "gdr_gate_cumsum", "gdr_wy_repr", "gdr_get_status",
            "gdr_status_string", "gdr_release", "gdr_launch_count", "gdr_profile_enable",
-           "gdr_profile_read")
+           "gdr_profile_read", "gdr_chunk_fwd_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -47,6 +47,7 @@ _SIGS = {
     "gdr_launch_count": (ctypes.c_uint64, []),
     "gdr_profile_enable": (None, [_I]),
     "gdr_profile_read": (_I, [_P, _P, _P, _I]),
+    "gdr_chunk_fwd_noalloc": (_I, [_P] * 8 + [_I, _I64, _I, _I, _I, _I, _F, _I, _I, _P]),
 }
 
 
@@ -117,6 +118,14 @@ def gdr_chunk_fwd_host(q, k, v, a, beta, h0, out, hT, cu_seqlens, B, T, H, dk, d
     return lib().gdr_chunk_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(beta), _ptr(h0),
                                     _ptr(out), _ptr(hT), _ptr(cu_seqlens), B, T, H, dk, dv, chunk,
                                     float(b), dtype, gate, path, _stream(stream))
+
+
+def gdr_chunk_fwd_noalloc(q, k, v, a, beta, h0, out, hT, B, T, H, dk, dv, chunk, b, dtype, gate,
+                          stream=None) -> int:
+    """Dense-input forward whose scratch is the library's static device array (no allocation)."""
+    return lib().gdr_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(beta), _ptr(h0),
+                                       _ptr(out), _ptr(hT), B, T, H, dk, dv, chunk, float(b), dtype,
+                                       gate, _stream(stream))
 
 
 def gdr_gate_cumsum(a, G, cu_seqlens, B, T, H, chunk, b, dtype, gate, stream=None) -> int:

@@ -150,6 +150,32 @@ GDR_API gdr_status_t gdr_chunk_fwd_host(const void *q, const void *k, const void
                                 gdr_path_t path, gdr_stream_t stream);
 
 /*
+ * The forward pass without any device allocation by the library.  The pages
+ * have no counterpart to this call; it exists for callers that must not
+ * allocate device memory when they run the pass (during CUDA graph capture,
+ * inside engines that pre-reserve all device memory, in allocation-free
+ * latency loops).  It runs the fp32 CUDA-core path on DENSE input only (no
+ * cu_seqlens) and keeps its scratch in one statically allocated 32 MiB device
+ * array that every GPU loading the library holds until exit.
+ *   Arguments, layouts and ownership are those of gdr_chunk_fwd_ex.
+ *   Limit: sizes whose scratch (4 * B*T*H * (1 + dk + dv) bytes plus
+ *   24 * (B+1) bytes, each part rounded up to 256) exceeds 32 MiB return
+ *   GDR_ERR_NO_WORKSPACE before anything is launched -- about 32K
+ *   (token, head) pairs at dk = dv = 128.
+ *   The first call on a device looks up the array's device address once
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   Every call reuses the same array, so calls that overlap on the GPU (on
+ *   different streams, or from several threads) race and must be
+ *   serialised by the caller.  Nothing in the array needs clearing between
+ *   calls: each call writes every scratch element before reading it.
+ */
+GDR_API gdr_status_t gdr_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
+                                           const void *a, const void *beta, const float *h0,
+                                           void *out, float *hT, int B, int64_t T, int H, int dk,
+                                           int dv, int chunk, float b, gdr_dtype_t dtype,
+                                           gdr_gate_t gate, gdr_stream_t stream);
+
+/*
  * Stage 1 alone: the gate and its in-tile cumulative sum.
  *   G[h, r] = sum over tokens r' of r's tile with r' <= r of g(a[r', h]),
  * written head-major as G [H, B*T] fp32 (token rows packed as in a).
