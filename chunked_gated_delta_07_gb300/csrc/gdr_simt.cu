@@ -47,7 +47,7 @@ plan_kernel(const int32_t *__restrict__ cu, int N, int64_t T_per, int64_t T_tota
         const int64_t len = e > s ? e - s : 0;
         const int64_t nc = (len + C - 1) / C;
         lc += nc;
-        ls += (nc + seg_chunks - 1) / seg_chunks;
+        ls += nc > seg_chunks ? (nc + seg_chunks - 1) / seg_chunks : 1;  // >= 1 segment per sequence
     }
     if (cu && tid == 0 && (cu[0] != 0 || (int64_t)cu[N] != T_total)) bad = 1;
     s_ch[tid] = lc;
@@ -78,7 +78,7 @@ plan_kernel(const int32_t *__restrict__ cu, int N, int64_t T_per, int64_t T_tota
         chunk_base[n] = cb;
         seg_base[n] = sb;
         cb += nc;
-        sb += (nc + seg_chunks - 1) / seg_chunks;
+        sb += nc > seg_chunks ? (nc + seg_chunks - 1) / seg_chunks : 1;
     }
     if (tid == 1023) {
         seq_start[N] = cu ? T_total : (int64_t)N * T_per;
