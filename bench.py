@@ -203,11 +203,15 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--ref-tokens", type=int, default=16384, help="tokens per reference step")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the tokens per sequence (or total, varlen) of the workload")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
     from gdr_inputs import WORKLOADS
     w = WORKLOADS[args.workload]
+    if args.tokens > 0:
+        w = w.with_(T=args.tokens)
     if args.impl == "reference":
         bench_reference(args, w)
         return

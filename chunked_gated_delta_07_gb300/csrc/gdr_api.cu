@@ -281,18 +281,23 @@ size_t gdr_chunk_fwd_workspace_size(int B, int64_t T, int H, int dk, int dv, int
         return 0;
     path = resolve_path(path, dtype, dk, dv, chunk);
     if (path == GDR_PATH_TC && !tc_supported(dtype, dk, dv, chunk)) return 0;
-    Shape s;
-    s.N = B;
-    s.H = H;
-    s.dk = dk;
-    s.dv = dv;
-    s.C = chunk;
-    // the larger of the dense (B*T tokens) and varlen (T tokens) readings
-    s.T_total = (int64_t)B * T > T ? (int64_t)B * T : T;
-    s.T_per = T;
-    s.varlen = false;
-    s.max_chunks = tile_bound(true, B, s.T_total, chunk);
-    return layout_for(s, path).total;
+    // the larger of the dense (B*T tokens) and varlen (T tokens) readings of (B, T)
+    size_t best = 0;
+    for (int varlen = 0; varlen < 2; ++varlen) {
+        Shape s;
+        s.N = B;
+        s.H = H;
+        s.dk = dk;
+        s.dv = dv;
+        s.C = chunk;
+        s.T_total = varlen ? T : (int64_t)B * T;
+        s.T_per = varlen ? 0 : T;
+        s.varlen = varlen != 0;
+        s.max_chunks = tile_bound(s.varlen, B, T, chunk);
+        const size_t n = layout_for(s, path).total;
+        if (n > best) best = n;
+    }
+    return best;
 }
 
 gdr_status_t gdr_chunk_fwd_host(const void *q, const void *k, const void *v, const void *a,

@@ -48,14 +48,14 @@ using namespace sm100;
 constexpr int kD = 128;          // dk = dv
 constexpr int kC = 16;           // tile length on this path
 constexpr int kNS = 3;           // pipeline stages, one per prep warp
-constexpr int kThreads = 32 * (4 + kNS);   // 4 state warps + kNS prep warps
+constexpr int kThreads = 32 * (4 + kNS + 1);   // 4 state warps, kNS prep warps, 1 MMA issuer
 constexpr uint64_t kWaitNs = 2000000000ull;  // bounded waits: 2 s
 
 // TMEM columns
 constexpr uint32_t kColH = 0;                    // state H^ (128 fp32 columns)
-constexpr uint32_t kColX = 128;                  // D_X, 2 buffers x 2C
-constexpr uint32_t kColU = kColX + 2 * 2 * kC;   // D_U, C columns
-constexpr uint32_t kColA = kColU + kC;           // bf16 A operands: Dt (C/2) and D/Gamma (C/2)
+constexpr uint32_t kColB = 128;                  // 2 buffers of [U (C) | -W H (C) | out (C)]
+constexpr uint32_t kColBuf = 3 * kC;
+constexpr uint32_t kColA = kColB + 2 * kColBuf;  // bf16 A operands: Dt (C/2) and D/Gamma (C/2)
 constexpr uint32_t kTmemCols = 256;
 static_assert(kColA + kC <= kTmemCols, "TMEM budget");
 
@@ -72,13 +72,14 @@ constexpr uint32_t kOffHdr = kOffP + kC * kC * 2;
 constexpr uint32_t kStage = 30720;
 static_assert(kOffHdr + 256 <= kStage, "stage layout");
 // per-prep-warp scratch after the stages
-constexpr uint32_t kScrSkk = 0;                  // fp32 [C][C+1]
-constexpr uint32_t kScrSqk = kScrSkk + kC * (kC + 1) * 4;
+constexpr uint32_t kScrSkk = 0;                  // fp32 [C][C]
+constexpr uint32_t kScrSqk = kScrSkk + kC * kC * 4;
 constexpr uint32_t kScrBW = 2304;                // bf16 [C][C] row-major (32 B rows)
 constexpr uint32_t kScr = 2816;
-static_assert(kScrSqk + kC * (kC + 1) * 4 <= kScrBW, "scratch layout");
+static_assert(kScrSqk + kC * kC * 4 <= kScrBW, "scratch layout");
 constexpr uint32_t kOffScr = kNS * kStage;
-constexpr uint32_t kOffBar = kOffScr + kNS * kScr;
+constexpr uint32_t kOffOut = kOffScr + kNS * kScr;   // per state warp: [C][32] bf16 output block
+constexpr uint32_t kOffBar = kOffOut + 4 * kC * 32 * 2;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // + alignment slack
 
 // core-matrix (no swizzle) K-major layout of a C x C bf16 operand [n][k]
@@ -87,8 +88,10 @@ __device__ __forceinline__ uint32_t cc_off(int n, int k) {
 }
 
 struct Hdr {
-    float G[kC];
-    float beta[kC];
+    float G[kC];       // in-tile cumulative log-decay (padded past the end with the last value)
+    float beta[kC];    // write strengths (0 past the end)
+    float eR[kC];      // exp(G_C - G_i)
+    float gam;         // exp(G_C), the tile's decay
     int len;
 };
 
@@ -103,6 +106,8 @@ struct TcArgs {
     float *Hin;   // [segs][H][D][D] entering states (pass C, s >= 1)
     float *Bs;    // [segs][H][D][D] transition offsets
     float *Ms;    // [segs][H][D][D] transition matrices
+    const int *first;   // [segs][H] first tile of the B stream (truncated transition)
+    const int *mneed;   // [segs][H] 1 if the transition matrix is not negligible
     Plan plan;
     int H;
     int64_t T_total;
@@ -114,6 +119,27 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
 }
+
+// Per-tile clock stamps of CTA (0, 0) for performance work; compiled only with
+// -DGDR_TC_TRACE (then gdr_tc_trace_buffer points at a [3 modes][64 tiles][16] buffer).
+#ifdef GDR_TC_TRACE
+}  // namespace
+__device__ long long *gdr_tc_trace_buffer = nullptr;
+__device__ int gdr_tc_trace_first = 0;
+namespace {
+#define TC_TRACE(c, slot)                                                                    \
+    do {                                                                                     \
+        long long *tb_ = gdr_tc_trace_buffer;                                                \
+        const int r_ = (c) - gdr_tc_trace_first;                                             \
+        if (tb_ && blockIdx.x == 0 && blockIdx.y == 0 && r_ >= 0 && r_ < 64)                 \
+            tb_[(args.mode * 64 + r_) * 16 + (slot)] = clock64();                           \
+    } while (0)
+#else
+#define TC_TRACE(c, slot) \
+    do {                  \
+    } while (0)
+#endif
+
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -171,7 +197,9 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     uint64_t *bar_x = bar_free + kNS;    // [2]
     uint64_t *bar_h = bar_x + 2;         // [1]
     uint64_t *bar_fin = bar_h + 1;       // [1]
-    uint32_t *tmem_slot = (uint32_t *)(bar_fin + 1);
+    uint64_t *bar_a = bar_fin + 1;       // [1] A operands of the tile written (4 state warps)
+    uint64_t *bar_init = bar_a + 1;      // [1] state initialised (4 state warps)
+    uint32_t *tmem_slot = (uint32_t *)(bar_init + 1);
     volatile int *abort_prep = (volatile int *)(tmem_slot + 1);   // set by prep warps
     volatile int *abort_state = abort_prep + 1;                   // set by state warps only
 
@@ -181,12 +209,16 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     SegInfo si;
     if (!seg_info(args.plan, blockIdx.x, si)) return;
     const bool last_seg = si.s == si.nseg - 1;
-    if (mode != kModeOut) {  // transition passes: only non-last segments
-        if (last_seg) return;
-        if (mode == kModeM && si.s == 0) return;
-    }
     const int H = args.H;
     const int64_t gsh = (int64_t)blockIdx.x * H + h;   // (global segment, head) slot
+    if (mode != kModeOut) {  // transition passes: only non-last segments
+        if (last_seg) return;
+        if (mode == kModeM && (si.s == 0 || args.mneed[gsh] == 0)) return;
+    }
+    // the B stream may start late: earlier tiles' contributions to the segment's
+    // end state are attenuated below the truncation bound
+    const bool truncated = mode == kModeB && args.first[gsh] > si.c0;
+    if (truncated) si.c0 = args.first[gsh];
     const float *h_in = nullptr;
     float *h_out = nullptr;
     if (mode == kModeOut) {
@@ -194,7 +226,8 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                          : args.Hin + gsh * kD * kD;
         h_out = (last_seg && args.hT) ? args.hT + ((int64_t)si.n * H + h) * kD * kD : nullptr;
     } else if (mode == kModeB) {
-        h_in = (si.s == 0 && args.h0) ? args.h0 + ((int64_t)si.n * H + h) * kD * kD : nullptr;
+        h_in = (si.s == 0 && args.h0 && !truncated) ? args.h0 + ((int64_t)si.n * H + h) * kD * kD
+                                                      : nullptr;
         h_out = args.Bs + gsh * kD * kD;
     } else {
         h_out = args.Ms + gsh * kD * kD;
@@ -213,6 +246,8 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mbar_init(&bar_x[1], 1);
         mbar_init(&bar_h[0], 1);
         mbar_init(&bar_fin[0], 1);
+        mbar_init(&bar_a[0], 4);
+        mbar_init(&bar_init[0], 4);
         *abort_prep = 0;
         *abort_state = 0;
         fence_mbar_init();
@@ -232,7 +267,7 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     tc_fence_after();
     const uint32_t tm = *tmem_slot;
 
-    if (warp >= 4) {
+    if (warp >= 4 && warp < 4 + kNS) {
         // ============================ prep warps ============================
         const int pw = warp - 4;
         uint8_t *scr = smem + kOffScr + pw * kScr;
@@ -246,6 +281,7 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // stage barrier is for the phase right after the one this warp consumed
         for (int c = pw; c < nch; c += kNS) {
             if (__any_sync(kFull, *abort_prep != 0 || *abort_state != 0)) break;
+            if (lane == 0) TC_TRACE(c, 0);
             const int st = pw;
             const uint32_t ph = (uint32_t)(c / kNS) & 1u;
             uint8_t *stg = smem + st * kStage;
@@ -266,6 +302,7 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 break;
             }
             if (lane == 0) {
+                TC_TRACE(c, 1);
                 mbar_arrive_expect_tx(&bar_full[st], tx_bytes);
                 tma_load_3d(stg + kOffK, &tmK, 0, h, (int)t0, &bar_full[st]);
                 tma_load_3d(stg + kOffK + kBox, &tmK, 64, h, (int)t0, &bar_full[st]);
@@ -280,17 +317,25 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
             pend_st = st;
             pend_ph = ph;
-            if (lane < kC) {
-                hdr->G[lane] = g_i;
-                hdr->beta[lane] = b_i;
+            {
+                const float g_last = __shfl_sync(kFull, g_i, kC - 1);
+                if (lane < kC) {
+                    hdr->G[lane] = g_i;
+                    hdr->beta[lane] = b_i;
+                    hdr->eR[lane] = __expf(fminf(g_last - g_i, 0.f));
+                }
+                if (lane == 0) {
+                    hdr->len = len;
+                    hdr->gam = __expf(g_last);
+                }
             }
-            if (lane == 0) hdr->len = len;
             if (!__all_sync(kFull, mbar_wait(&bar_full[st], ph, kWaitNs))) {
                 if (lane == 0) set_status(args.status, GDR_ERR_TIMEOUT);
                 *abort_prep = 1;
                 break;
             }
             pend_st = -1;
+            if (lane == 0) TC_TRACE(c, 2);
             // rows past the end of the sequence hold another sequence's tokens: zero them
             if (len < kC) {
                 const int nt = 1 + (use_v ? 1 : 0) + (use_q ? 1 : 0);
@@ -330,53 +375,82 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
                     const int col = 8 * nt + 2 * (lane & 3);
-                    Skk[r0 * (kC + 1) + col] = skk[nt][0];
-                    Skk[r0 * (kC + 1) + col + 1] = skk[nt][1];
-                    Skk[(r0 + 8) * (kC + 1) + col] = skk[nt][2];
-                    Skk[(r0 + 8) * (kC + 1) + col + 1] = skk[nt][3];
-                    Sqk[r0 * (kC + 1) + col] = sqk[nt][0];
-                    Sqk[r0 * (kC + 1) + col + 1] = sqk[nt][1];
-                    Sqk[(r0 + 8) * (kC + 1) + col] = sqk[nt][2];
-                    Sqk[(r0 + 8) * (kC + 1) + col + 1] = sqk[nt][3];
+                    *(float2 *)&Skk[r0 * kC + col] = make_float2(skk[nt][0], skk[nt][1]);
+                    *(float2 *)&Skk[(r0 + 8) * kC + col] = make_float2(skk[nt][2], skk[nt][3]);
+                    *(float2 *)&Sqk[r0 * kC + col] = make_float2(sqk[nt][0], sqk[nt][1]);
+                    *(float2 *)&Sqk[(r0 + 8) * kC + col] = make_float2(sqk[nt][2], sqk[nt][3]);
                 }
             }
             __syncwarp();
-            // ---- A (in place over Skk) and P (bf16, core-matrix layout in the stage)
-            for (int e = lane; e < kC * kC; e += 32) {
-                const int i = e / kC, j = e % kC;
-                const float dg = __expf(fminf(hdr->G[i] - hdr->G[j], 0.f));
-                const float a_ij = j < i ? hdr->beta[i] * dg * Skk[i * (kC + 1) + j] : 0.f;
-                Skk[i * (kC + 1) + j] = a_ij;
+            if (lane == 0) TC_TRACE(c, 3);
+            // ---- A (in place over Skk) and P (bf16, core-matrix layout in the stage):
+            // lane -> row i = lane / 2, columns 8 (lane & 1) .. + 7
+            {
+                const int i = lane >> 1, j0 = 8 * (lane & 1);
+                const float Gi = hdr->G[i], bi = hdr->beta[i];
+                const float4 k0 = *(const float4 *)&Skk[i * kC + j0];
+                const float4 k1 = *(const float4 *)&Skk[i * kC + j0 + 4];
+                const float sk[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+                float a[8], pv[8];
+                float sq[8];
                 if (use_q) {
-                    const float p_ij = j <= i ? Sqk[i * (kC + 1) + j] * dg : 0.f;
-                    *(__nv_bfloat16 *)(stg + kOffP + cc_off(i, j)) = __float2bfloat16_rn(p_ij);
+                    const float4 q0 = *(const float4 *)&Sqk[i * kC + j0];
+                    const float4 q1 = *(const float4 *)&Sqk[i * kC + j0 + 4];
+                    sq[0] = q0.x; sq[1] = q0.y; sq[2] = q0.z; sq[3] = q0.w;
+                    sq[4] = q1.x; sq[5] = q1.y; sq[6] = q1.z; sq[7] = q1.w;
                 }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int j = j0 + u;
+                    const float dg = __expf(fminf(Gi - hdr->G[j], 0.f));
+                    a[u] = j < i ? bi * dg * sk[u] : 0.f;
+                    pv[u] = (use_q && j <= i) ? sq[u] * dg : 0.f;
+                }
+                __syncwarp();   // every lane has read its Skk row segment before it is overwritten
+                *(float4 *)&Skk[i * kC + j0] = make_float4(a[0], a[1], a[2], a[3]);
+                *(float4 *)&Skk[i * kC + j0 + 4] = make_float4(a[4], a[5], a[6], a[7]);
+                if (use_q)
+                    *(uint4 *)(stg + kOffP + cc_off(i, j0)) =
+                        make_uint4(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]),
+                                   pack_bf16(pv[4], pv[5]), pack_bf16(pv[6], pv[7]));
             }
             __syncwarp();
-            // ---- T = (I + A)^{-1}, one column per lane (forward substitution)
+            // ---- T = (I + A)^{-1}, one column per lane (forward substitution over
+            // broadcast row loads); lanes 16..31 repeat lanes 0..15
             {
                 const int j = lane & (kC - 1);
                 float tcol[kC];
 #pragma unroll
                 for (int i = 0; i < kC; ++i) {
+                    float row[kC];
+#pragma unroll
+                    for (int q4 = 0; q4 < kC / 4; ++q4) {
+                        const float4 v4 = *(const float4 *)&Skk[i * kC + 4 * q4];
+                        row[4 * q4] = v4.x;
+                        row[4 * q4 + 1] = v4.y;
+                        row[4 * q4 + 2] = v4.z;
+                        row[4 * q4 + 3] = v4.w;
+                    }
                     float acc = 0.f;
 #pragma unroll
-                    for (int m = 0; m < i; ++m) acc = fmaf(Skk[i * (kC + 1) + m], tcol[m], acc);
+                    for (int m = 0; m < i; ++m) acc = fmaf(row[m], tcol[m], acc);
                     tcol[i] = (i < j) ? 0.f : ((i == j) ? 1.f : -acc);
                 }
-                if (lane < kC) {
-                    const float bj = hdr->beta[j];
+                const float bj = hdr->beta[j];
+                if (lane < kC) {          // Bu = T diag(beta)
+                    if (use_v)
+#pragma unroll
+                        for (int i = 0; i < kC; ++i)
+                            *(__nv_bfloat16 *)(stg + kOffBU + cc_off(i, j)) = __float2bfloat16_rn(tcol[i] * bj);
+                } else {                  // Bw = T diag(beta e^G), row-major for ldmatrix
                     const float bej = bj * __expf(hdr->G[j]);
 #pragma unroll
-                    for (int i = 0; i < kC; ++i) {
-                        if (use_v)
-                            *(__nv_bfloat16 *)(stg + kOffBU + cc_off(i, j)) =
-                                __float2bfloat16_rn(tcol[i] * bj);
+                    for (int i = 0; i < kC; ++i)
                         *(__nv_bfloat16 *)(BW + i * 32 + j * 2) = __float2bfloat16_rn(tcol[i] * bej);
-                    }
                 }
             }
             __syncwarp();
+            if (lane == 0) TC_TRACE(c, 4);
             // ---- W = Bw K (mma.sync) -> rows [0, C) of WQ as -W in tf32
             {
                 uint32_t af[4];
@@ -401,6 +475,7 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     }
                 }
             }
+            if (lane == 0) TC_TRACE(c, 5);
             // ---- rows [C, 2C) of WQ: diag(e^G) Q in tf32
             if (use_q) {
                 const int i = lane >> 1, hb = lane & 1;
@@ -424,6 +499,7 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
             fence_proxy_async_smem();
             __syncwarp();
+            if (lane == 0) TC_TRACE(c, 6);
             if (lane == 0) mbar_arrive(&bar_prep[st]);
         }
         // never leave with a tile copy still in flight
@@ -431,6 +507,64 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             mbar_wait(&bar_full[pend_st], pend_ph, kWaitNs);
             __syncwarp();
         }
+    } else if (warp == 4 + kNS) {
+        // ============================ MMA issuer ============================
+        // One thread issues every tcgen05 MMA of the CTA, in tile order, so the
+        // tensor pipe executes them in that order: a tile's front MMAs may read
+        // the state the previous tile's update MMA writes without waiting for it.
+        if (lane == 0) {
+            const uint32_t id_u = instr_desc(128, kC, 1, true, false);
+            const uint32_t id_x = instr_desc(128, use_q ? 2 * kC : kC, 2, false, false);
+            const uint32_t id_h = instr_desc(128, kD, 1, false, true);
+            const uint32_t id_o = instr_desc(128, kC, 1, false, false);
+            bool ok = nch == 0 || mbar_wait(&bar_init[0], 0, kWaitNs);
+            for (int c = 0; c < nch && ok; ++c) {
+                if (*abort_state || *abort_prep) {
+                    ok = false;
+                    break;
+                }
+                const int st = c % kNS, buf = c & 1;
+                const uint32_t sb = smem_u32(smem + st * kStage);
+                const uint32_t cb = kColB + buf * kColBuf;
+                if (!mbar_wait(&bar_prep[st], (uint32_t)(c / kNS) & 1u, kWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // front: U^T and [-W ; Qt] H^ into buffer c & 1
+                if (use_v)
+                    mma_f16_ss(tm + cb, smem_desc(sb + kOffV, kBox, 1024, kSw128),
+                               smem_desc(sb + kOffBU, 128, (kC / 8) * 128, kSwNone), id_u, 0);
+#pragma unroll
+                for (int s8 = 0; s8 < kD / 8; ++s8)
+                    mma_tf32_ts(tm + cb + kC, tm + kColH + 8 * s8,
+                                smem_desc(sb + kOffWQ + (s8 >> 2) * kWQBlock + 32 * (s8 & 3), 16, 1024, kSw128),
+                                id_x, s8 > 0);
+                mma_commit(&bar_x[buf]);
+                // back: the state update and the in-tile output term, once the
+                // state warps have written this tile's A operands
+                if (!mbar_wait(&bar_a[0], (uint32_t)c & 1u, kWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                mma_f16_ts(tm + kColH, tm + kColA, smem_desc(sb + kOffK, kBox, 1024, kSw128), id_h, 1);
+                if (use_q)
+                    mma_f16_ts(tm + cb + 2 * kC, tm + kColA + kC / 2,
+                               smem_desc(sb + kOffP, 128, (kC / 8) * 128, kSwNone), id_o, 1);
+                mma_commit(&bar_free[st]);
+            }
+            if (ok) {
+                mma_commit(&bar_h[0]);   // the state warps' drain waits on the last tile's MMAs
+            } else {
+                set_status(args.status, GDR_ERR_TIMEOUT);
+                *abort_state = 1;
+            }
+            // teardown: no tensor-core operation may still run when the TMEM is released
+            mma_commit(&bar_fin[0]);
+            mbar_wait(&bar_fin[0], 0, kWaitNs);
+        }
+        __syncwarp();
     } else {
         // ============================ state warps ============================
         const int e = tid;                       // value index = TMEM lane
@@ -450,63 +584,55 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         tmem_st_wait();
         tc_fence_before();
-        named_barrier(1, 128);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_init[0]);
+        // One tile's output for this warp's 32 value columns: transposed through a
+        // per-warp shared block so that each row goes out as 16-byte stores.
+        __nv_bfloat16 *oblk = (__nv_bfloat16 *)(smem + kOffOut + warp * (kC * 32 * 2));
+        auto store_out = [&](const uint32_t (&o)[kC], int len, int64_t t0, float scale) {
+#pragma unroll
+            for (int i = 0; i < kC; ++i) oblk[i * 32 + lane] = __float2bfloat16_rn(__uint_as_float(o[i]) * scale);
+            __syncwarp();
+            __nv_bfloat16 *out = (__nv_bfloat16 *)args.out;
+#pragma unroll
+            for (int k = lane; k < kC * 4; k += 32) {
+                const int row = k >> 2, q4 = k & 3;
+                if (row < len)
+                    *(uint4 *)(out + ((t0 + row) * H + h) * kD + warp * 32 + q4 * 8) =
+                        *(const uint4 *)(oblk + row * 32 + q4 * 8);
+            }
+            __syncwarp();
+        };
         float Gamma = 1.f;                // H = Gamma * H^
         float gamma_prev = 1.f;           // Gamma of the previous tile's output
         int64_t t0_prev = 0;
         int len_prev = 0;
-        const uint32_t id_u = instr_desc(128, kC, 1, true, false);
-        const uint32_t id_x = instr_desc(128, use_q ? 2 * kC : kC, 2, false, false);
-        const uint32_t id_h = instr_desc(128, kD, 1, false, true);
-        const uint32_t id_o = instr_desc(128, kC, 1, false, false);
-        int done = 0;                     // tiles whose state update was issued
+        int done = 0;
         for (int c = 0; c < nch; ++c) {
+            if (__any_sync(kFull, *abort_state != 0 || *abort_prep != 0)) break;
             const int st = c % kNS;
             const uint32_t ph = (uint32_t)(c / kNS) & 1u;
             const int buf = c & 1;
             uint8_t *stg = smem + st * kStage;
-            const uint32_t sb = smem_u32(stg);
-            if (tid == 0) {
-                tc_fence_after();
-                bool okw = c == 0 || mbar_wait(&bar_h[0], (uint32_t)(c - 1) & 1u, kWaitNs);
-                okw = okw && mbar_wait(&bar_prep[st], ph, kWaitNs);
-                if (okw) {
-                    tc_fence_after();
-                    if (use_v)
-                        mma_f16_ss(tm + kColU, smem_desc(sb + kOffV, kBox, 1024, kSw128),
-                                   smem_desc(sb + kOffBU, 128, (kC / 8) * 128, kSwNone), id_u, 0);
-#pragma unroll
-                    for (int s8 = 0; s8 < kD / 8; ++s8)
-                        mma_tf32_ts(tm + kColX + buf * 2 * kC, tm + kColH + 8 * s8,
-                                    smem_desc(sb + kOffWQ + (s8 >> 2) * kWQBlock + 32 * (s8 & 3), 16, 1024, kSw128),
-                                    id_x, s8 > 0);
-                    mma_commit(&bar_x[buf]);
-                } else {
-                    set_status(args.status, GDR_ERR_TIMEOUT);
-                    *abort_state = 1;
-                }
-            }
-            __syncwarp();
-            // everyone: the tile's header and the MMA results (a missing result times out)
+            const uint32_t cb = kColB + buf * kColBuf;
+            if (lane == 0) TC_TRACE(c, 8);
+            // the tile's header and its front MMAs (a missing result times out)
             const bool okw = mbar_wait(&bar_prep[st], ph, kWaitNs) &&
                              mbar_wait(&bar_x[buf], (uint32_t)(c >> 1) & 1u, kWaitNs);
-            if (!okw) {
-                set_status(args.status, GDR_ERR_TIMEOUT);
+            if (!__all_sync(kFull, okw)) {
+                if (lane == 0) set_status(args.status, GDR_ERR_TIMEOUT);
                 *abort_state = 1;
+                break;
             }
-            __syncwarp();
-            named_barrier(1, 128);        // one view of abort_state for the whole group
-            if (*abort_state) break;
             tc_fence_after();
+            if (lane == 0) TC_TRACE(c, 9);
             const Hdr *hdr = (const Hdr *)(stg + kOffHdr);
-            const int len_c = hdr->len;   // read before the stage can be recycled
-            uint32_t xr[kC], ur[kC], orr[kC];
-            tmem_ld16(tm + lane_base + kColX + buf * 2 * kC, xr);
-            if (use_v) tmem_ld16(tm + lane_base + kColU, ur);
-            if (use_q && c > 0) tmem_ld16(tm + lane_base + kColX + (buf ^ 1) * 2 * kC + kC, orr);
+            const int len_c = hdr->len;
+            uint32_t ux[2 * kC], orr[kC];
+            tmem_ld32(tm + lane_base + cb, ux);            // [U | -W H^] of this tile
+            if (use_q && c > 0) tmem_ld16(tm + lane_base + kColB + (buf ^ 1) * kColBuf + 2 * kC, orr);
             tmem_ld_wait();
-            const float GC = hdr->G[kC - 1];
-            const float gam = __expf(GC);
+            const float gam = hdr->gam;
             float Gp = Gamma * gam;
             const bool renorm = !(Gp >= 1e-30f);   // ~2^-100; also catches gam == 0
             float s2;
@@ -521,7 +647,6 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * f);
                     tmem_st16(tm + lane_base + kColH + d0, r);
                 }
-                tmem_st_wait();
                 s2 = 1.f;
                 Gp = 1.f;
             } else {
@@ -531,39 +656,25 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const float inv_g = 1.f / Gamma;
 #pragma unroll
             for (int i = 0; i < kC; i += 2) {
-                float dl0 = Gamma * __uint_as_float(xr[i]);
-                float dl1 = Gamma * __uint_as_float(xr[i + 1]);
+                float dl0 = Gamma * __uint_as_float(ux[kC + i]);
+                float dl1 = Gamma * __uint_as_float(ux[kC + i + 1]);
                 if (use_v) {
-                    dl0 += __uint_as_float(ur[i]);
-                    dl1 += __uint_as_float(ur[i + 1]);
+                    dl0 += __uint_as_float(ux[i]);
+                    dl1 += __uint_as_float(ux[i + 1]);
                 }
-                const float r0 = __expf(fminf(GC - hdr->G[i], 0.f)) * s2;
-                const float r1 = __expf(fminf(GC - hdr->G[i + 1], 0.f)) * s2;
-                a2[i / 2] = pack_bf16(dl0 * r0, dl1 * r1);
+                a2[i / 2] = pack_bf16(dl0 * hdr->eR[i] * s2, dl1 * hdr->eR[i + 1] * s2);
                 a3[i / 2] = pack_bf16(dl0 * inv_g, dl1 * inv_g);
             }
             tmem_st8(tm + lane_base + kColA, a2);
             if (use_q) tmem_st8(tm + lane_base + kColA + kC / 2, a3);
             tmem_st_wait();
             tc_fence_before();
-            named_barrier(1, 128);
-            if (tid == 0) {
-                tc_fence_after();
-                mma_f16_ts(tm + kColH, tm + kColA, smem_desc(sb + kOffK, kBox, 1024, kSw128), id_h, 1);
-                if (use_q)
-                    mma_f16_ts(tm + kColX + buf * 2 * kC + kC, tm + kColA + kC / 2,
-                               smem_desc(sb + kOffP, 128, (kC / 8) * 128, kSwNone), id_o, 1);
-                mma_commit(&bar_free[st]);
-                mma_commit(&bar_h[0]);
-            }
             __syncwarp();
-            // output of the previous tile (its MMAs completed before this tile's D_X)
-            if (use_q && c > 0) {
-                __nv_bfloat16 *out = (__nv_bfloat16 *)args.out;
-                for (int i = 0; i < len_prev; ++i)
-                    out[((t0_prev + i) * H + h) * kD + e] =
-                        __float2bfloat16_rn(__uint_as_float(orr[i]) * gamma_prev);
-            }
+            if (lane == 0) mbar_arrive(&bar_a[0]);
+            if (lane == 0) TC_TRACE(c, 10);
+            // output of the previous tile (its MMAs completed before this tile's front)
+            if (use_q && c > 0) store_out(orr, len_prev, t0_prev, gamma_prev);
+            if (lane == 0) TC_TRACE(c, 13);
             gamma_prev = Gamma;
             t0_prev = si.tok0 + (si.c0 + c) * kC;
             len_prev = len_c;
@@ -571,24 +682,15 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             done = c + 1;
         }
         // drain: the last tile's output, then the final state
-        if (done > 0 && done == nch) {
-            if (!mbar_wait(&bar_h[0], (uint32_t)(nch - 1) & 1u, kWaitNs)) {
-                set_status(args.status, GDR_ERR_TIMEOUT);
-                *abort_state = 1;
-            }
-        }
-        __syncwarp();
-        named_barrier(1, 128);
-        const bool ok = *abort_state == 0 && done == nch;
+        bool ok = done == nch;
+        if (ok && nch > 0) ok = __all_sync(kFull, mbar_wait(&bar_h[0], 0, kWaitNs));
+        ok = __all_sync(kFull, ok && *abort_state == 0);
         tc_fence_after();
         if (ok && use_q && nch > 0) {
             uint32_t orr[kC];
-            tmem_ld16(tm + lane_base + kColX + ((nch - 1) & 1) * 2 * kC + kC, orr);
+            tmem_ld16(tm + lane_base + kColB + ((nch - 1) & 1) * kColBuf + 2 * kC, orr);
             tmem_ld_wait();
-            __nv_bfloat16 *out = (__nv_bfloat16 *)args.out;
-            for (int i = 0; i < len_prev; ++i)
-                out[((t0_prev + i) * H + h) * kD + e] =
-                    __float2bfloat16_rn(__uint_as_float(orr[i]) * gamma_prev);
+            store_out(orr, len_prev, t0_prev, gamma_prev);
         }
         if (ok && h_out) {
             for (int d0 = 0; d0 < kD; d0 += 16) {
@@ -600,19 +702,51 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
         }
     }
-    // teardown: no tensor-core operation may still be running when the TMEM is released
     tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-        tc_fence_after();
-        mma_commit(&bar_fin[0]);
-        mbar_wait(&bar_fin[0], 0, kWaitNs);
-    }
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tm, kTmemCols);
     }
+}
+
+// ---------------------------------------------------------------------------
+// transition truncation: for each non-last segment, the first tile r such that
+// the accumulated log-decay from the start of tile r to the segment's end is at
+// most -kTruncLog.  Everything that enters the recurrence before tile r reaches
+// the segment's end attenuated by at least exp(-kTruncLog) = 2^-64 (the state
+// norm bound: each step contracts by its decay), so the segment's offset B is
+// computed from a zero state at r, and its transition matrix M, whose norm is
+// bounded by the same product of decays, is taken as zero.  When no such r
+// exists the full transition is computed.
+// ---------------------------------------------------------------------------
+constexpr float kTruncLog = 44.3614195558365f;   // 64 ln 2
+
+__global__ void __launch_bounds__(128)
+tc_horizon_kernel(const float *G, Plan p, int H, int64_t T_total, int64_t nslots, int *first,
+                  int *mneed, int truncate) {
+    const int64_t slot = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (slot >= nslots) return;
+    const int64_t gseg = slot / H;
+    const int h = (int)(slot % H);
+    SegInfo si;
+    if (!seg_info(p, gseg, si)) return;
+    int r = (int)si.c0;
+    int need = 1;
+    if (truncate) {
+        float acc = 0.f;
+        for (int64_t c = si.c1 - 1; c >= si.c0; --c) {
+            const int64_t last = min((int64_t)kC, si.len - c * kC) - 1;
+            acc += G[(int64_t)h * T_total + si.tok0 + c * kC + last];
+            if (acc <= -kTruncLog) {
+                r = (int)c;
+                need = 0;
+                break;
+            }
+        }
+    }
+    first[slot] = r;
+    mneed[slot] = need;
 }
 
 // ---------------------------------------------------------------------------
@@ -622,7 +756,7 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 constexpr int kCombCols = 32;
 
 __global__ void __launch_bounds__(256)
-tc_combine_kernel(float *Hin, const float *Bs, const float *Ms, Plan p, int H) {
+tc_combine_kernel(float *Hin, const float *Bs, const float *Ms, const int *mneed, Plan p, int H) {
     extern __shared__ float cs[];
     float *Msh = cs;                  // [128][129]
     float *Hs = Msh + kD * (kD + 1);  // [128][32]
@@ -637,7 +771,7 @@ tc_combine_kernel(float *Hin, const float *Bs, const float *Ms, Plan p, int H) {
         const int64_t prev = (g0 + s - 1) * H + h, cur = (g0 + s) * H + h;
         const float *B = Bs + prev * kD * kD;
         float *Hc = Hin + cur * kD * kD;
-        if (s == 1) {
+        if (s == 1 || mneed[prev] == 0) {   // M of the previous segment is negligible (or s = 1)
             for (int e = tid; e < kD * kCombCols; e += 256) {
                 const int d = e / kCombCols, j = e % kCombCols;
                 const float x = B[d * kD + j0 + j];
@@ -747,8 +881,10 @@ int tc_segment_chunks(int N, int H, int64_t T_total, int C) {
 
 size_t tc_workspace_bytes(int N, int H, int64_t T_total, int C) {
     const int sc = tc_segment_chunks(N, H, T_total, C);
-    const size_t per = (size_t)max_segments(N, T_total, sc) * H * kD * kD * sizeof(float);
-    return 3 * ((per + 255) / 256 * 256);
+    const int64_t nseg = max_segments(N, T_total, sc);
+    const size_t per = (size_t)nseg * H * kD * kD * sizeof(float);
+    const size_t flags = (size_t)nseg * H * sizeof(int);
+    return 3 * ((per + 255) / 256 * 256) + 2 * ((flags + 255) / 256 * 256);
 }
 
 cudaError_t launch_tc_forward(const void *q, const void *k, const void *v, const float *G,
@@ -770,10 +906,24 @@ cudaError_t launch_tc_forward(const void *q, const void *k, const void *v, const
     a.Hin = (float *)scratch;
     a.Bs = (float *)((char *)scratch + per);
     a.Ms = (float *)((char *)scratch + 2 * per);
+    const size_t flags_b = ((size_t)nseg * H * sizeof(int) + 255) / 256 * 256;
+    int *first = (int *)((char *)scratch + 3 * per);
+    int *mneed = (int *)((char *)scratch + 3 * per + flags_b);
+    a.first = first;
+    a.mneed = mneed;
     a.plan = plan;
     a.H = H;
     a.T_total = T_total;
     a.status = status;
+    const char *exact = std::getenv("GDR_TC_EXACT");
+    const int truncate = (exact && std::atoi(exact) != 0) ? 0 : 1;
+    {
+        ProfScope prof(stream, "tc_horizon_kernel");
+        const int64_t nslots = nseg * H;
+        tc_horizon_kernel<<<(unsigned)((nslots + 127) / 128), 128, 0, stream>>>(
+            G, plan, H, T_total, nslots, first, mneed, truncate);
+        count_launch();
+    }
     cudaError_t err = cudaFuncSetAttribute(tc_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSmemBytes);
     if (err != cudaSuccess) return err;
@@ -797,7 +947,7 @@ cudaError_t launch_tc_forward(const void *q, const void *k, const void *v, const
     {
         ProfScope prof(stream, "tc_combine_kernel");
         tc_combine_kernel<<<(unsigned)(plan.N * H * (kD / kCombCols)), 256, comb_smem, stream>>>(
-            a.Hin, a.Bs, a.Ms, plan, H);
+            a.Hin, a.Bs, a.Ms, mneed, plan, H);
         count_launch();
     }
     {
@@ -810,3 +960,10 @@ cudaError_t launch_tc_forward(const void *q, const void *k, const void *v, const
 }
 
 }  // namespace gdr
+
+#ifdef GDR_TC_TRACE
+extern "C" __attribute__((visibility("default"))) int gdr_tc_trace_set(long long *buf, int first) {
+    if (cudaMemcpyToSymbol(gdr::gdr_tc_trace_buffer, &buf, sizeof(buf)) != cudaSuccess) return 1;
+    return cudaMemcpyToSymbol(gdr::gdr_tc_trace_first, &first, sizeof(first)) == cudaSuccess ? 0 : 1;
+}
+#endif

@@ -43,6 +43,7 @@ class Workload:
     b: float = 2.0         # bound of the scaled-sigmoid gate
     gate: str = "bounded"  # or "softplus"
     a_std: float = 1.0
+    a_mean: float = 0.0    # shifts the gate logits (a very negative mean = weak decay)
     h0_std: float = 0.0
     varlen: bool = False
     len_min: int = 1024
@@ -137,7 +138,7 @@ def make_inputs(w: Workload, device="cpu", T: int | None = None, block: int = 1 
             k[bi, t0:t1] = (x / x.norm(dim=-1, keepdim=True).clamp_min(1e-30)).to(dt)
             v[bi, t0:t1] = _randn((n, H, dv), g, device).to(dt)
             beta[bi, t0:t1] = torch.sigmoid(_randn((n, H), g, device)).to(dt)
-            a[bi, t0:t1] = (w.a_std * _randn((n, H), g, device)).to(dt)
+            a[bi, t0:t1] = (w.a_mean + w.a_std * _randn((n, H), g, device)).to(dt)
     h0 = None
     if w.h0_std > 0:
         h0 = (w.h0_std * _randn((N, H, dk, dv), g, device)).contiguous()

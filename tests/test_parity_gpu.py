@@ -230,3 +230,40 @@ def test_host_buffer_entry_point():
     ro, rh = run_oracle(x)
     assert_close(to64(out), ro, "bf16", "out")
     assert_close(to64(hT), rh, "bf16", "hT")
+
+
+# ---------------------------------------------------------------------------
+# tensor-core segment scan: many short segments, weak and strong decay
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("exact", [False, True])
+@pytest.mark.parametrize("a_mean", [-6.0, 0.0])
+def test_tc_segment_scan(monkeypatch, exact, a_mean):
+    """Short segments (4 tiles) force the transition pass, the combine and the
+    output pass on every sequence.  a_mean = -6 gives g ~ -0.005 per token, so
+    transitions are far from negligible and the full scan runs; a_mean = 0
+    decays fast, so the truncated transition is taken unless exact mode is set."""
+    if not _tc_available():
+        pytest.skip("tensor-core path unavailable")
+    monkeypatch.setenv("GDR_TC_SEG_CHUNKS", "4")
+    if exact:
+        monkeypatch.setenv("GDR_TC_EXACT", "1")
+    w = WORKLOADS["b2_t4k"].with_(H=4, a_mean=a_mean, a_std=0.5, h0_std=0.05)
+    x = make_inputs(w, device="cuda", T=1000)
+    ro, rh = run_oracle(x)
+    out, hT = run_gpu(x, path="tc")
+    assert_close(to64(out), ro, "bf16", "out")
+    assert_close(to64(hT), rh, "bf16", "hT")
+
+
+def test_tc_varlen_softplus_segments(monkeypatch):
+    """Unbounded gate with large logits: tile decays underflow to zero, which
+    exercises the state-rescaling path, on packed sequences split into segments."""
+    if not _tc_available():
+        pytest.skip("tensor-core path unavailable")
+    monkeypatch.setenv("GDR_TC_SEG_CHUNKS", "3")
+    w = softplus_variant(WORKLOADS["varlen_1m"].with_(len_min=30, len_max=1500))
+    x = make_inputs(w, device="cuda", T=6000)
+    ro, rh = run_oracle(x)
+    out, hT = run_gpu(x, path="tc")
+    assert_close(to64(out), ro, "bf16", "out")
+    assert_close(to64(hT), rh, "bf16", "hT")
