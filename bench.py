@@ -36,7 +36,12 @@ UNIT = "tokens/s"
 # DRAM bytes (read + write) per launch of the dominant kernel as counted by ncu,
 # per (token, head) unit, with the hash of the kernel source they were taken at.
 # The value is reported only while the source is unchanged.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # ncu --set full, t1m shape cut to 262,144 tokens (4,194,304 units, inputs 3.2 GB > L2):
+    # dram__bytes_read.sum 3.274033 GB + dram__bytes_write.sum 1.052366 GB per launch
+    "tc_output_kernel": {"source": "gdr_tc.cu", "hash": "0ff169c1c535", "workload": "t1m",
+                         "bytes_per_unit": 4326399000.0 / 4194304},
+}
 
 
 def peaks():
@@ -171,7 +176,7 @@ def bench_reference(args, w):
     sample = (f"first {per_step_tokens} tokens of each of the {w.H} heads of workload {w.name} per step "
               f"(fp64, token by token)")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(w),
