@@ -132,6 +132,26 @@ def dist_env():
     return ws, rank, local
 
 
+def rank_workload(w, rank):
+    """Each replica draws its own inputs: same shapes, seed offset by rank."""
+    return w.with_(seed=w.seed + 7919 * rank)
+
+
+def max_over_ranks(ms, dist, device):
+    """The timed region's length as the slowest rank measured it."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(ws, n_tokens, steps, ms):
+    """Whole-job tokens/s: every rank processed n_tokens per step."""
+    return ws * n_tokens * steps / (ms / 1e3)
+
+
 def cpu_oracle_rate(x, w, budget_s, max_tokens):
     """Time the oracle on a prefix of the workload; returns (tokens/s, tokens, threads, seconds)."""
     import oracle
@@ -195,7 +215,7 @@ def workload_config(w):
             "l2_policy": "inputs larger than L2 (no flush)"}
 
 
-def main():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
@@ -210,8 +230,13 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the tokens per sequence (or total, varlen) of the workload")
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
+    return args
+
+
+def main(argv=None):
+    args = parse_args(argv)
 
     from gdr_inputs import WORKLOADS
     w = WORKLOADS[args.workload]
@@ -234,7 +259,7 @@ def main():
     dev = torch.device("cuda", local)
     gdr.lib()
 
-    x = make_inputs(w.with_(seed=w.seed + 7919 * rank), device=dev)
+    x = make_inputs(rank_workload(w, rank), device=dev)
     B, T, H, dk, dv = x["B"], x["T"], x["H"], x["dk"], x["dv"]
     N = x["N"]
     n_tokens = T if w.varlen else B * T
@@ -277,10 +302,8 @@ def main():
         n_launch = gdr.gdr_launch_count() - n_launch0
     gdr.gdr_profile_enable(False)
     ms = ev0.elapsed_time(ev1)
+    ms = max_over_ranks(ms, dist, dev)
     if dist:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
     prof = gdr.gdr_profile_read()
     st = gdr.gdr_get_status(stream)
@@ -288,7 +311,7 @@ def main():
         raise gdr.GdrError(st, "device status after timed region")
 
     ms_step = ms / args.steps
-    value = ws * n_tokens * args.steps / (ms / 1e3)
+    value = job_value(ws, n_tokens, args.steps, ms)
     hbm, tf_burst, tf_sust, peak_src = peaks()
     byt, flops, per_tok = algorithmic(w, n_tokens, x["h0"] is not None)
     t_roof = max(byt / (hbm * 1e9), flops / (tf_sust * 1e12))
