@@ -47,7 +47,7 @@ using namespace sm100;
 
 constexpr int kD = 128;          // dk = dv
 constexpr int kC = 16;           // tile length on this path
-constexpr int kNS = 3;           // pipeline stages, one per prep warp
+constexpr int kNS = 4;           // pipeline stages, one per prep warp
 constexpr int kThreads = 32 * (4 + kNS + 1);   // 4 state warps, kNS prep warps, 1 MMA issuer
 constexpr uint64_t kWaitNs = 2000000000ull;  // bounded waits: 2 s
 
@@ -59,27 +59,30 @@ constexpr uint32_t kColA = kColB + 2 * kColBuf;  // bf16 A operands: Dt (C/2) an
 constexpr uint32_t kTmemCols = 256;
 static_assert(kColA + kC <= kTmemCols, "TMEM budget");
 
-// Shared memory, per stage
+// Shared memory, per stage (26 KB, so that 4 stages fit at 2 CTAs per SM).
+// [-W ; Qt] in tf32 is 4 column blocks of 2C rows x 128 B (rows 0..C-1: -W,
+// rows C..2C-1: Qt).  The -W rows are written last, so until then they hold
+// the raw Q tile (blocks 0, 1: one 64-column box each) and the prep warp's
+// scratch (blocks 2, 3).
 constexpr uint32_t kBox = kC * 128;              // one 64-column box of a [C][128] bf16 tile
 constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kOffK + 2 * kBox;
-constexpr uint32_t kOffQ = kOffV + 2 * kBox;
-constexpr uint32_t kOffWQ = kOffQ + 2 * kBox;    // tf32 [2C rows][128], 4 swizzled 32-wide column blocks
+constexpr uint32_t kOffWQ = kOffV + 2 * kBox;
 constexpr uint32_t kWQBlock = 2 * kC * 128;
+constexpr uint32_t kOffQ0 = kOffWQ;                  // raw Q, columns 0..63
+constexpr uint32_t kOffQ1 = kOffWQ + kWQBlock;       // raw Q, columns 64..127
+constexpr uint32_t kOffSkk = kOffWQ + 2 * kWQBlock;  // fp32 [C][C] K K^T, then A
+constexpr uint32_t kOffSqk = kOffSkk + kC * kC * 4;  // fp32 [C][C] Q K^T
+constexpr uint32_t kOffBW = kOffWQ + 3 * kWQBlock;   // bf16 [C][C] row-major (32 B rows)
 constexpr uint32_t kOffBU = kOffWQ + 4 * kWQBlock;
 constexpr uint32_t kOffP = kOffBU + kC * kC * 2;
 constexpr uint32_t kOffHdr = kOffP + kC * kC * 2;
-constexpr uint32_t kStage = 30720;
-static_assert(kOffHdr + 256 <= kStage, "stage layout");
-// per-prep-warp scratch after the stages
-constexpr uint32_t kScrSkk = 0;                  // fp32 [C][C]
-constexpr uint32_t kScrSqk = kScrSkk + kC * kC * 4;
-constexpr uint32_t kScrBW = 2304;                // bf16 [C][C] row-major (32 B rows)
-constexpr uint32_t kScr = 2816;
-static_assert(kScrSqk + kC * kC * 4 <= kScrBW, "scratch layout");
-constexpr uint32_t kOffScr = kNS * kStage;
-constexpr uint32_t kOffOut = kOffScr + kNS * kScr;   // per state warp: [C][32] bf16 output block
-constexpr uint32_t kOffBar = kOffOut + 4 * kC * 32 * 2;
+constexpr uint32_t kStage = 26624;
+static_assert(kOffSqk + kC * kC * 4 <= kOffWQ + 2 * kWQBlock + kC * 128, "scratch in -W rows");
+static_assert(kOffBW + kC * kC * 2 <= kOffWQ + 3 * kWQBlock + kC * 128, "scratch in -W rows");
+static_assert(kOffHdr + 256 <= kStage && kStage % 1024 == 0, "stage layout");
+__host__ __device__ constexpr uint32_t q_box(int b) { return b == 0 ? kOffQ0 : kOffQ1; }
+constexpr uint32_t kOffBar = kNS * kStage;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // + alignment slack
 
 // core-matrix (no swizzle) K-major layout of a C x C bf16 operand [n][k]
@@ -270,10 +273,9 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if (warp >= 4 && warp < 4 + kNS) {
         // ============================ prep warps ============================
         const int pw = warp - 4;
-        uint8_t *scr = smem + kOffScr + pw * kScr;
-        float *Skk = (float *)(scr + kScrSkk);
-        float *Sqk = (float *)(scr + kScrSqk);
-        uint8_t *BW = scr + kScrBW;
+        float *Skk = (float *)(smem + pw * kStage + kOffSkk);
+        float *Sqk = (float *)(smem + pw * kStage + kOffSqk);
+        uint8_t *BW = smem + pw * kStage + kOffBW;
         const uint32_t tx_bytes = 2 * kBox * (1 + (use_v ? 1 : 0) + (use_q ? 1 : 0));
         int pend_st = -1;          // stage whose TMA is issued but not yet seen complete
         uint32_t pend_ph = 0;
@@ -311,8 +313,8 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     tma_load_3d(stg + kOffV + kBox, &tmV, 64, h, (int)t0, &bar_full[st]);
                 }
                 if (use_q) {
-                    tma_load_3d(stg + kOffQ, &tmQ, 0, h, (int)t0, &bar_full[st]);
-                    tma_load_3d(stg + kOffQ + kBox, &tmQ, 64, h, (int)t0, &bar_full[st]);
+                    tma_load_3d(stg + kOffQ0, &tmQ, 0, h, (int)t0, &bar_full[st]);
+                    tma_load_3d(stg + kOffQ1, &tmQ, 64, h, (int)t0, &bar_full[st]);
                 }
             }
             pend_st = st;
@@ -344,10 +346,9 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     const int chunk16 = e & 7, rem = e >> 3;
                     const int row = len + rem % nrow, box = (rem / nrow) & 1;
                     const int tsel = rem / (nrow * 2);
-                    const uint32_t toff =
-                        tsel == 0 ? kOffK : ((tsel == 1 && use_v) ? kOffV : kOffQ);
-                    *(uint4 *)(stg + toff + box * kBox + sw128_off(row, chunk16 * 16)) =
-                        make_uint4(0, 0, 0, 0);
+                    const uint32_t toff = tsel == 0 ? kOffK + box * kBox
+                                          : ((tsel == 1 && use_v) ? kOffV + box * kBox : q_box(box));
+                    *(uint4 *)(stg + toff + sw128_off(row, chunk16 * 16)) = make_uint4(0, 0, 0, 0);
                 }
             }
             __syncwarp();
@@ -357,14 +358,14 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const int r = lane & 15, half = lane >> 4;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t off = (ks >> 2) * kBox + sw128_off(r, 32 * (ks & 3) + 16 * half);
+                    const uint32_t off = sw128_off(r, 32 * (ks & 3) + 16 * half);
                     uint32_t kf[4];
-                    ldsm_x4(smem_u32(stg + kOffK + off), kf);
+                    ldsm_x4(smem_u32(stg + kOffK + (ks >> 2) * kBox + off), kf);
                     mma16816(skk[0], kf, kf[0], kf[2]);
                     mma16816(skk[1], kf, kf[1], kf[3]);
                     if (use_q) {
                         uint32_t qf[4];
-                        ldsm_x4(smem_u32(stg + kOffQ + off), qf);
+                        ldsm_x4(smem_u32(stg + q_box(ks >> 2) + off), qf);
                         mma16816(sqk[0], qf, kf[0], kf[2]);
                         mma16816(sqk[1], qf, kf[1], kf[3]);
                     }
@@ -451,10 +452,35 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
             __syncwarp();
             if (lane == 0) TC_TRACE(c, 4);
+            // ---- rows [C, 2C) of WQ: diag(e^G) Q in tf32 (reads the raw Q tile, which
+            // the -W rows below overwrite)
+            if (use_q) {
+                const int i = lane >> 1, hb = lane & 1;
+                const float eg = __expf(hdr->G[i]);
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    const uint4 raw = *(const uint4 *)(stg + q_box(hb) + sw128_off(i, 16 * c8));
+                    const __nv_bfloat162 *bp = (const __nv_bfloat162 *)&raw;
+                    float f[8];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float2 x = __bfloat1622float2(bp[u]);
+                        f[2 * u] = x.x * eg;
+                        f[2 * u + 1] = x.y * eg;
+                    }
+                    const int d = 64 * hb + 8 * c8;
+                    uint8_t *base = stg + kOffWQ + (d >> 5) * kWQBlock;
+                    *(float4 *)(base + sw128_off(kC + i, (d & 31) * 4)) = make_float4(f[0], f[1], f[2], f[3]);
+                    *(float4 *)(base + sw128_off(kC + i, (d & 31) * 4 + 16)) = make_float4(f[4], f[5], f[6], f[7]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) TC_TRACE(c, 5);
             // ---- W = Bw K (mma.sync) -> rows [0, C) of WQ as -W in tf32
             {
                 uint32_t af[4];
                 ldsm_x4(smem_u32(BW + (lane & 15) * 32 + (lane >> 4) * 16), af);
+                __syncwarp();   // Bw is read before the -W rows (which hold it) are written
                 const int jrow = (lane & 7) + 8 * ((lane >> 3) & 1);
 #pragma unroll
                 for (int np = 0; np < 8; ++np) {
@@ -473,28 +499,6 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         *(float2 *)(base + sw128_off(i0, (d & 31) * 4)) = make_float2(-w[0], -w[1]);
                         *(float2 *)(base + sw128_off(i0 + 8, (d & 31) * 4)) = make_float2(-w[2], -w[3]);
                     }
-                }
-            }
-            if (lane == 0) TC_TRACE(c, 5);
-            // ---- rows [C, 2C) of WQ: diag(e^G) Q in tf32
-            if (use_q) {
-                const int i = lane >> 1, hb = lane & 1;
-                const float eg = __expf(hdr->G[i]);
-#pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    const uint4 raw = *(const uint4 *)(stg + kOffQ + hb * kBox + sw128_off(i, 16 * c8));
-                    const __nv_bfloat162 *bp = (const __nv_bfloat162 *)&raw;
-                    float f[8];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float2 x = __bfloat1622float2(bp[u]);
-                        f[2 * u] = x.x * eg;
-                        f[2 * u + 1] = x.y * eg;
-                    }
-                    const int d = 64 * hb + 8 * c8;
-                    uint8_t *base = stg + kOffWQ + (d >> 5) * kWQBlock;
-                    *(float4 *)(base + sw128_off(kC + i, (d & 31) * 4)) = make_float4(f[0], f[1], f[2], f[3]);
-                    *(float4 *)(base + sw128_off(kC + i, (d & 31) * 4 + 16)) = make_float4(f[4], f[5], f[6], f[7]);
                 }
             }
             fence_proxy_async_smem();
@@ -586,22 +590,13 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_init[0]);
-        // One tile's output for this warp's 32 value columns: transposed through a
-        // per-warp shared block so that each row goes out as 16-byte stores.
-        __nv_bfloat16 *oblk = (__nv_bfloat16 *)(smem + kOffOut + warp * (kC * 32 * 2));
+        // One tile's output for this warp's 32 value columns: per token row, the
+        // warp writes 64 contiguous bytes.
         auto store_out = [&](const uint32_t (&o)[kC], int len, int64_t t0, float scale) {
+            __nv_bfloat16 *out = (__nv_bfloat16 *)args.out + (t0 * H + h) * kD + e;
 #pragma unroll
-            for (int i = 0; i < kC; ++i) oblk[i * 32 + lane] = __float2bfloat16_rn(__uint_as_float(o[i]) * scale);
-            __syncwarp();
-            __nv_bfloat16 *out = (__nv_bfloat16 *)args.out;
-#pragma unroll
-            for (int k = lane; k < kC * 4; k += 32) {
-                const int row = k >> 2, q4 = k & 3;
-                if (row < len)
-                    *(uint4 *)(out + ((t0 + row) * H + h) * kD + warp * 32 + q4 * 8) =
-                        *(const uint4 *)(oblk + row * 32 + q4 * 8);
-            }
-            __syncwarp();
+            for (int i = 0; i < kC; ++i)
+                if (i < len) out[(int64_t)i * H * kD] = __float2bfloat16_rn(__uint_as_float(o[i]) * scale);
         };
         float Gamma = 1.f;                // H = Gamma * H^
         float gamma_prev = 1.f;           // Gamma of the previous tile's output
@@ -628,10 +623,6 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             if (lane == 0) TC_TRACE(c, 9);
             const Hdr *hdr = (const Hdr *)(stg + kOffHdr);
             const int len_c = hdr->len;
-            uint32_t ux[2 * kC], orr[kC];
-            tmem_ld32(tm + lane_base + cb, ux);            // [U | -W H^] of this tile
-            if (use_q && c > 0) tmem_ld16(tm + lane_base + kColB + (buf ^ 1) * kColBuf + 2 * kC, orr);
-            tmem_ld_wait();
             const float gam = hdr->gam;
             float Gp = Gamma * gam;
             const bool renorm = !(Gp >= 1e-30f);   // ~2^-100; also catches gam == 0
@@ -652,6 +643,9 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             } else {
                 s2 = 1.f / Gp;
             }
+            uint32_t ux[2 * kC];
+            tmem_ld32(tm + lane_base + cb, ux);            // [U | -W H^] of this tile
+            tmem_ld_wait();
             uint32_t a2[kC / 2], a3[kC / 2];
             const float inv_g = 1.f / Gamma;
 #pragma unroll
@@ -673,7 +667,12 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             if (lane == 0) mbar_arrive(&bar_a[0]);
             if (lane == 0) TC_TRACE(c, 10);
             // output of the previous tile (its MMAs completed before this tile's front)
-            if (use_q && c > 0) store_out(orr, len_prev, t0_prev, gamma_prev);
+            if (use_q && c > 0) {
+                uint32_t orr[kC];
+                tmem_ld16(tm + lane_base + kColB + (buf ^ 1) * kColBuf + 2 * kC, orr);
+                tmem_ld_wait();
+                store_out(orr, len_prev, t0_prev, gamma_prev);
+            }
             if (lane == 0) TC_TRACE(c, 13);
             gamma_prev = Gamma;
             t0_prev = si.tok0 + (si.c0 + c) * kC;
