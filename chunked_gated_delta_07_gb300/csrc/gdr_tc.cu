@@ -50,6 +50,12 @@ constexpr int kC = 16;           // tile length on this path
 constexpr int kNS = 4;           // pipeline stages, one per prep warp
 constexpr int kThreads = 32 * (4 + kNS + 1);   // 4 state warps, kNS prep warps, 1 MMA issuer
 constexpr uint64_t kWaitNs = 2000000000ull;  // bounded waits: 2 s
+// The state is kept as H = Gamma * H^.  Gamma runs down by each tile's decay and
+// is folded into H^ (Gamma reset to 1) before it would drop below kGammaMin, so
+// H^ stays within |H| / kGammaMin and the scaled writes within |Delta| /
+// kGammaMin: both far inside fp32 / bf16 range.  (Resetting to a large Gamma
+// instead, to fold less often, measured slower.)
+constexpr float kGammaMin = 1e-30f;
 
 // TMEM columns
 constexpr uint32_t kColH = 0;                    // state H^ (128 fp32 columns)
@@ -534,6 +540,7 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     ok = false;
                     break;
                 }
+                TC_TRACE(c, 14);
                 tc_fence_after();
                 // front: U^T and [-W ; Qt] H^ into buffer c & 1
                 if (use_v)
@@ -545,18 +552,21 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                 smem_desc(sb + kOffWQ + (s8 >> 2) * kWQBlock + 32 * (s8 & 3), 16, 1024, kSw128),
                                 id_x, s8 > 0);
                 mma_commit(&bar_x[buf]);
+                TC_TRACE(c, 15);
                 // back: the state update and the in-tile output term, once the
                 // state warps have written this tile's A operands
                 if (!mbar_wait(&bar_a[0], (uint32_t)c & 1u, kWaitNs)) {
                     ok = false;
                     break;
                 }
+                TC_TRACE(c, 11);
                 tc_fence_after();
                 mma_f16_ts(tm + kColH, tm + kColA, smem_desc(sb + kOffK, kBox, 1024, kSw128), id_h, 1);
                 if (use_q)
                     mma_f16_ts(tm + cb + 2 * kC, tm + kColA + kC / 2,
                                smem_desc(sb + kOffP, 128, (kC / 8) * 128, kSwNone), id_o, 1);
                 mma_commit(&bar_free[st]);
+                TC_TRACE(c, 12);
             }
             if (ok) {
                 mma_commit(&bar_h[0]);   // the state warps' drain waits on the last tile's MMAs
@@ -624,27 +634,29 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const Hdr *hdr = (const Hdr *)(stg + kOffHdr);
             const int len_c = hdr->len;
             const float gam = hdr->gam;
-            float Gp = Gamma * gam;
-            const bool renorm = !(Gp >= 1e-30f);   // ~2^-100; also catches gam == 0
-            float s2;
+            float Gp = Gamma * gam;                  // Gamma after this tile, if not reset
+            const bool renorm = !(Gp >= kGammaMin);  // also catches gam == 0
             if (renorm) {
-                // fold Gamma * gam into H^ (the MMAs reading H^ for this tile are done)
-                const float f = Gamma * gam;
+                // fold Gp into H^ and reset Gamma to 1; no MMA reads or writes H^ now
+                // (this tile's front is done, its update not issued)
                 for (int d0 = 0; d0 < kD; d0 += 16) {
                     uint32_t r[16];
                     tmem_ld16(tm + lane_base + kColH + d0, r);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * f);
+                    for (int j = 0; j < 16; ++j)
+                        r[j] = __float_as_uint(__uint_as_float(r[j]) * Gp);
                     tmem_st16(tm + lane_base + kColH + d0, r);
                 }
-                s2 = 1.f;
                 Gp = 1.f;
-            } else {
-                s2 = 1.f / Gp;
             }
-            uint32_t ux[2 * kC];
-            tmem_ld32(tm + lane_base + cb, ux);            // [U | -W H^] of this tile
+            const float s2 = 1.f / Gp;               // the tile's writes enter H^ scaled by 1 / Gamma
+            // [U | -W H^] of this tile, and the previous tile's output (complete with
+            // this tile's bar_x; read before the arrive, since the next front MMA
+            // overwrites its buffer)
+            uint32_t ux[2 * kC], orr[kC];
+            tmem_ld32(tm + lane_base + cb, ux);
+            if (use_q && c > 0) tmem_ld16(tm + lane_base + kColB + (buf ^ 1) * kColBuf + 2 * kC, orr);
             tmem_ld_wait();
             uint32_t a2[kC / 2], a3[kC / 2];
             const float inv_g = 1.f / Gamma;
@@ -666,18 +678,12 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_a[0]);
             if (lane == 0) TC_TRACE(c, 10);
-            // output of the previous tile (its MMAs completed before this tile's front)
-            if (use_q && c > 0) {
-                uint32_t orr[kC];
-                tmem_ld16(tm + lane_base + kColB + (buf ^ 1) * kColBuf + 2 * kC, orr);
-                tmem_ld_wait();
-                store_out(orr, len_prev, t0_prev, gamma_prev);
-            }
+            if (use_q && c > 0) store_out(orr, len_prev, t0_prev, gamma_prev);
             if (lane == 0) TC_TRACE(c, 13);
             gamma_prev = Gamma;
             t0_prev = si.tok0 + (si.c0 + c) * kC;
             len_prev = len_c;
-            Gamma = renorm ? 1.f : Gp;
+            Gamma = Gp;
             done = c + 1;
         }
         // drain: the last tile's output, then the final state
