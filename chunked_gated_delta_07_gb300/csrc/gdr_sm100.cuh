@@ -138,6 +138,12 @@ __device__ __forceinline__ void mma_tf32_ts(uint32_t d, uint32_t a, uint64_t b, 
         "r"(a), "l"(b), "r"(idesc), "r"(accum)
         : "memory");
 }
+// True in exactly one lane of a converged warp (the warp stays converged around it).
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile("{ .reg .pred p; elect.sync _|p, 0xffffffff; selp.u32 %0, 1, 0, p; }" : "=r"(pred));
+    return pred != 0;
+}
 // Arrive (once) on `bar` when every tcgen05 operation this thread issued so far is complete.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile(

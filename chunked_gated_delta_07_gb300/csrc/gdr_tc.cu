@@ -522,61 +522,72 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // One thread issues every tcgen05 MMA of the CTA, in tile order, so the
         // tensor pipe executes them in that order: a tile's front MMAs may read
         // the state the previous tile's update MMA writes without waiting for it.
-        if (lane == 0) {
+        // The warp runs the loop converged (operand descriptors are warp-uniform)
+        // and elects the issuing lane at each group of MMAs.
+        {
             const uint32_t id_u = instr_desc(128, kC, 1, true, false);
             const uint32_t id_x = instr_desc(128, use_q ? 2 * kC : kC, 2, false, false);
             const uint32_t id_h = instr_desc(128, kD, 1, false, true);
             const uint32_t id_o = instr_desc(128, kC, 1, false, false);
-            bool ok = nch == 0 || mbar_wait(&bar_init[0], 0, kWaitNs);
+            bool ok = nch == 0 || __all_sync(kFull, mbar_wait(&bar_init[0], 0, kWaitNs));
             for (int c = 0; c < nch && ok; ++c) {
-                if (*abort_state || *abort_prep) {
+                if (__any_sync(kFull, *abort_state != 0 || *abort_prep != 0)) {
                     ok = false;
                     break;
                 }
                 const int st = c % kNS, buf = c & 1;
                 const uint32_t sb = smem_u32(smem + st * kStage);
                 const uint32_t cb = kColB + buf * kColBuf;
-                if (!mbar_wait(&bar_prep[st], (uint32_t)(c / kNS) & 1u, kWaitNs)) {
+                if (!__all_sync(kFull, mbar_wait(&bar_prep[st], (uint32_t)(c / kNS) & 1u, kWaitNs))) {
                     ok = false;
                     break;
                 }
-                TC_TRACE(c, 14);
+                if (lane == 0) TC_TRACE(c, 14);
                 tc_fence_after();
                 // front: U^T and [-W ; Qt] H^ into buffer c & 1
-                if (use_v)
-                    mma_f16_ss(tm + cb, smem_desc(sb + kOffV, kBox, 1024, kSw128),
-                               smem_desc(sb + kOffBU, 128, (kC / 8) * 128, kSwNone), id_u, 0);
+                if (elect_one()) {
+                    if (use_v)
+                        mma_f16_ss(tm + cb, smem_desc(sb + kOffV, kBox, 1024, kSw128),
+                                   smem_desc(sb + kOffBU, 128, (kC / 8) * 128, kSwNone), id_u, 0);
 #pragma unroll
-                for (int s8 = 0; s8 < kD / 8; ++s8)
-                    mma_tf32_ts(tm + cb + kC, tm + kColH + 8 * s8,
-                                smem_desc(sb + kOffWQ + (s8 >> 2) * kWQBlock + 32 * (s8 & 3), 16, 1024, kSw128),
-                                id_x, s8 > 0);
-                mma_commit(&bar_x[buf]);
-                TC_TRACE(c, 15);
+                    for (int s8 = 0; s8 < kD / 8; ++s8)
+                        mma_tf32_ts(tm + cb + kC, tm + kColH + 8 * s8,
+                                    smem_desc(sb + kOffWQ + (s8 >> 2) * kWQBlock + 32 * (s8 & 3), 16, 1024, kSw128),
+                                    id_x, s8 > 0);
+                    mma_commit(&bar_x[buf]);
+                }
+                __syncwarp();
+                if (lane == 0) TC_TRACE(c, 15);
                 // back: the state update and the in-tile output term, once the
                 // state warps have written this tile's A operands
-                if (!mbar_wait(&bar_a[0], (uint32_t)c & 1u, kWaitNs)) {
+                if (!__all_sync(kFull, mbar_wait(&bar_a[0], (uint32_t)c & 1u, kWaitNs))) {
                     ok = false;
                     break;
                 }
-                TC_TRACE(c, 11);
+                if (lane == 0) TC_TRACE(c, 11);
                 tc_fence_after();
-                mma_f16_ts(tm + kColH, tm + kColA, smem_desc(sb + kOffK, kBox, 1024, kSw128), id_h, 1);
-                if (use_q)
-                    mma_f16_ts(tm + cb + 2 * kC, tm + kColA + kC / 2,
-                               smem_desc(sb + kOffP, 128, (kC / 8) * 128, kSwNone), id_o, 1);
-                mma_commit(&bar_free[st]);
-                TC_TRACE(c, 12);
+                if (elect_one()) {
+                    mma_f16_ts(tm + kColH, tm + kColA, smem_desc(sb + kOffK, kBox, 1024, kSw128), id_h, 1);
+                    if (use_q)
+                        mma_f16_ts(tm + cb + 2 * kC, tm + kColA + kC / 2,
+                                   smem_desc(sb + kOffP, 128, (kC / 8) * 128, kSwNone), id_o, 1);
+                    mma_commit(&bar_free[st]);
+                }
+                __syncwarp();
+                if (lane == 0) TC_TRACE(c, 12);
             }
-            if (ok) {
-                mma_commit(&bar_h[0]);   // the state warps' drain waits on the last tile's MMAs
-            } else {
-                set_status(args.status, GDR_ERR_TIMEOUT);
+            // the state warps' drain waits on the last tile's MMAs; on a failure, no
+            // tensor-core operation may still run when the TMEM is released
+            if (elect_one()) {
+                if (ok) mma_commit(&bar_h[0]);
+                mma_commit(&bar_fin[0]);
+            }
+            __syncwarp();
+            if (!ok) {
+                if (lane == 0) set_status(args.status, GDR_ERR_TIMEOUT);
                 *abort_state = 1;
             }
-            // teardown: no tensor-core operation may still run when the TMEM is released
-            mma_commit(&bar_fin[0]);
-            mbar_wait(&bar_fin[0], 0, kWaitNs);
+            __all_sync(kFull, mbar_wait(&bar_fin[0], 0, kWaitNs));
         }
         __syncwarp();
     } else {
