@@ -99,28 +99,74 @@ cudaError_t launch_plan(const int32_t *cu_seqlens, int N, int64_t T_per, int64_t
 
 // ---------------------------------------------------------------------------
 // stage 1: gate + in-tile cumulative sum [P1 §3.3, P2 §2.2, P3 §3.2, P4 §2.3]
-// one thread per (tile, head); G and the transposed beta are head-major so a
-// tile's values are contiguous for the later stages.
+// G and the transposed beta are head-major so a tile's values are contiguous
+// for the later stages.  One block per 128 / C consecutive tiles (at most 128
+// tokens, contiguous along the token axis) and 32 heads: a and beta are read
+// row by row (coalesced), transposed through shared memory, summed per
+// (tile, head), and written head row by head row (coalesced).
 // ---------------------------------------------------------------------------
+constexpr int kGateTok = 128, kGateMaxTiles = kGateTok / 16, kGateHeads = 32;
+
 template <typename T>
 __global__ void __launch_bounds__(256)
 gate_cumsum_kernel(const T *__restrict__ a, const T *__restrict__ beta, float *__restrict__ G,
                    float *__restrict__ Bt, Plan p, int H, int64_t T_total, int64_t max_chunks,
                    float b, int gate) {
-    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int h = (int)(gid % H);
-    const int64_t c = gid / H;
-    if (c >= max_chunks) return;
-    const int n = find_owner(p.chunk_base, p.N, c);
-    if (n < 0) return;
-    const int64_t t0 = p.seq_start[n] + (c - p.chunk_base[n]) * p.C;
-    const int len = (int)min((int64_t)p.C, p.seq_start[n + 1] - t0);
-    float acc = 0.f;
-    for (int i = 0; i < len; ++i) {
-        const int64_t row = t0 + i;
-        acc += gate_logdecay(to_f32(a[row * H + h]), b, gate);
-        G[(int64_t)h * T_total + row] = acc;
-        if (Bt) Bt[(int64_t)h * T_total + row] = to_f32(beta[row * H + h]);
+    __shared__ float gsm[2 * kGateHeads * (kGateTok + 1)];   // [head][token] gates, then beta
+    __shared__ int64_t tstart[kGateMaxTiles];
+    __shared__ int tlen[kGateMaxTiles];
+    const int tid = threadIdx.x;
+    const int nt = kGateTok / p.C;                           // tiles per block
+    const int64_t c0 = (int64_t)blockIdx.x * nt;
+    const int h0 = blockIdx.y * kGateHeads;
+    const int nh = min(kGateHeads, H - h0);
+    if (tid < kGateMaxTiles) {
+        const int64_t c = c0 + tid;
+        const int n = (tid < nt && c < max_chunks) ? find_owner(p.chunk_base, p.N, c) : -1;
+        int64_t t0 = 0;
+        int len = 0;
+        if (n >= 0) {
+            t0 = p.seq_start[n] + (c - p.chunk_base[n]) * p.C;
+            len = (int)min((int64_t)p.C, p.seq_start[n + 1] - t0);
+        }
+        tstart[tid] = t0;
+        tlen[tid] = len;
+    }
+    __syncthreads();
+    if (tlen[0] == 0) return;   // tiles are enumerated densely: nothing from here on
+    // the tiles present are consecutive and cover [Tb, Te) without gaps
+    const int64_t Tb = tstart[0];
+    int64_t Te = Tb;
+    for (int j = 0; j < nt; ++j)
+        if (tlen[j] > 0) Te = tstart[j] + tlen[j];
+    const int ntok = (int)(Te - Tb);
+    const int ld = ntok + 1;
+    float *sg = gsm;
+    float *sb = gsm + kGateHeads * ld;
+    for (int e = tid; e < ntok * nh; e += blockDim.x) {
+        const int t = e / nh, hh = e - t * nh;
+        const int64_t src = (Tb + t) * H + h0 + hh;
+        sg[hh * ld + t] = gate_logdecay(to_f32(a[src]), b, gate);
+        if (Bt) sb[hh * ld + t] = to_f32(beta[src]);
+    }
+    __syncthreads();
+    {
+        const int j = tid / kGateHeads, hh = tid % kGateHeads;
+        if (j < nt && hh < nh && tlen[j] > 0) {
+            float *row = sg + hh * ld + (int)(tstart[j] - Tb);
+            float acc = 0.f;
+            for (int i = 0; i < tlen[j]; ++i) {
+                acc += row[i];
+                row[i] = acc;
+            }
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < nh * ntok; e += blockDim.x) {
+        const int hh = e / ntok, t = e - hh * ntok;
+        const int64_t dst = (int64_t)(h0 + hh) * T_total + Tb + t;
+        G[dst] = sg[hh * ld + t];
+        if (Bt) Bt[dst] = sb[hh * ld + t];
     }
 }
 
@@ -128,16 +174,18 @@ cudaError_t launch_gate_cumsum(const void *a, const void *beta, gdr_dtype_t dtyp
                                float *Bt, Plan plan, int H, int64_t T_total,
                                int64_t max_chunks, float b, gdr_gate_t gate,
                                cudaStream_t stream) {
-    const int64_t threads = max_chunks * H;
-    if (threads == 0) return cudaSuccess;
-    const unsigned grid = (unsigned)((threads + 255) / 256);
+    if (max_chunks == 0 || H == 0) return cudaSuccess;
+    if (plan.C < 16 || plan.C > kGateTok || kGateTok % plan.C != 0) return cudaErrorInvalidValue;
+    const int nt = kGateTok / plan.C;
+    const dim3 grid((unsigned)((max_chunks + nt - 1) / nt), (unsigned)((H + kGateHeads - 1) / kGateHeads));
+    const size_t smem = 0;
     ProfScope prof(stream, "gate_cumsum_kernel");
     if (dtype == GDR_BF16)
-        gate_cumsum_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+        gate_cumsum_kernel<__nv_bfloat16><<<grid, 256, smem, stream>>>(
             (const __nv_bfloat16 *)a, (const __nv_bfloat16 *)beta, G, Bt, plan, H, T_total,
             max_chunks, b, (int)gate);
     else
-        gate_cumsum_kernel<float><<<grid, 256, 0, stream>>>(
+        gate_cumsum_kernel<float><<<grid, 256, smem, stream>>>(
             (const float *)a, (const float *)beta, G, Bt, plan, H, T_total, max_chunks, b,
             (int)gate);
     count_launch();

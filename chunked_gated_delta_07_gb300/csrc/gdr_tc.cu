@@ -30,6 +30,7 @@
 //           as two streams of the same kernel: B from a zero state (or from
 //           h0 for the first segment) and M from the identity with v = 0;
 //   combine: H_in(s+1) = M_s H_in(s) + B_s, serial over segments (fp32);
+//           where M_s is negligible, H_in(s+1) = B_s is read in place;
 //   pass C (every segment): the outputs from the true entering state.
 #include <cudaTypedefs.h>
 
@@ -231,8 +232,15 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const float *h_in = nullptr;
     float *h_out = nullptr;
     if (mode == kModeOut) {
-        h_in = si.s == 0 ? (args.h0 ? args.h0 + ((int64_t)si.n * H + h) * kD * kD : nullptr)
-                         : args.Hin + gsh * kD * kD;
+        if (si.s == 0) {
+            h_in = args.h0 ? args.h0 + ((int64_t)si.n * H + h) * kD * kD : nullptr;
+        } else {
+            // the previous segment's transition: with no (or a negligible) matrix the
+            // entering state is its offset B, which the combine does not copy
+            const int64_t prev = gsh - H;
+            h_in = (si.s == 1 || args.mneed[prev] == 0) ? args.Bs + prev * kD * kD
+                                                         : args.Hin + gsh * kD * kD;
+        }
         h_out = (last_seg && args.hT) ? args.hT + ((int64_t)si.n * H + h) * kD * kD : nullptr;
     } else if (mode == kModeB) {
         h_in = (si.s == 0 && args.h0 && !truncated) ? args.h0 + ((int64_t)si.n * H + h) * kD * kD
@@ -787,12 +795,12 @@ tc_combine_kernel(float *Hin, const float *Bs, const float *Ms, const int *mneed
         const int64_t prev = (g0 + s - 1) * H + h, cur = (g0 + s) * H + h;
         const float *B = Bs + prev * kD * kD;
         float *Hc = Hin + cur * kD * kD;
-        if (s == 1 || mneed[prev] == 0) {   // M of the previous segment is negligible (or s = 1)
+        if (s == 1 || mneed[prev] == 0) {
+            // M of the previous segment is negligible (or s = 1): H_in(s) = B(s-1),
+            // which the output pass reads in place; only the running copy is kept
             for (int e = tid; e < kD * kCombCols; e += 256) {
                 const int d = e / kCombCols, j = e % kCombCols;
-                const float x = B[d * kD + j0 + j];
-                Hc[d * kD + j0 + j] = x;
-                Hs[e] = x;
+                Hs[e] = B[d * kD + j0 + j];
             }
             __syncthreads();
             continue;
