@@ -669,7 +669,7 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
                 Gp = 1.f;
             }
-            const float s2 = 1.f / Gp;               // the tile's writes enter H^ scaled by 1 / Gamma
+            const float s2 = __frcp_rn(Gp);               // the tile's writes enter H^ scaled by 1 / Gamma
             // [U | -W H^] of this tile, and the previous tile's output (complete with
             // this tile's bar_x; read before the arrive, since the next front MMA
             // overwrites its buffer)
@@ -678,17 +678,20 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             if (use_q && c > 0) tmem_ld16(tm + lane_base + kColB + (buf ^ 1) * kColBuf + 2 * kC, orr);
             tmem_ld_wait();
             uint32_t a2[kC / 2], a3[kC / 2];
-            const float inv_g = 1.f / Gamma;
+            const float inv_g = __frcp_rn(Gamma);
 #pragma unroll
-            for (int i = 0; i < kC; i += 2) {
-                float dl0 = Gamma * __uint_as_float(ux[kC + i]);
-                float dl1 = Gamma * __uint_as_float(ux[kC + i + 1]);
-                if (use_v) {
-                    dl0 += __uint_as_float(ux[i]);
-                    dl1 += __uint_as_float(ux[i + 1]);
+            for (int i = 0; i < kC; i += 4) {
+                const float4 e4 = *(const float4 *)&hdr->eR[i];
+                float dl[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    dl[u] = Gamma * __uint_as_float(ux[kC + i + u]);
+                    if (use_v) dl[u] += __uint_as_float(ux[i + u]);
                 }
-                a2[i / 2] = pack_bf16(dl0 * hdr->eR[i] * s2, dl1 * hdr->eR[i + 1] * s2);
-                a3[i / 2] = pack_bf16(dl0 * inv_g, dl1 * inv_g);
+                a2[i / 2] = pack_bf16(dl[0] * (e4.x * s2), dl[1] * (e4.y * s2));
+                a2[i / 2 + 1] = pack_bf16(dl[2] * (e4.z * s2), dl[3] * (e4.w * s2));
+                a3[i / 2] = pack_bf16(dl[0] * inv_g, dl[1] * inv_g);
+                a3[i / 2 + 1] = pack_bf16(dl[2] * inv_g, dl[3] * inv_g);
             }
             tmem_st8(tm + lane_base + kColA, a2);
             if (use_q) tmem_st8(tm + lane_base + kColA + kC / 2, a3);
