@@ -143,11 +143,25 @@ gate_cumsum_kernel(const T *__restrict__ a, const T *__restrict__ beta, float *_
     const int ld = ntok + 1;
     float *sg = gsm;
     float *sb = gsm + kGateHeads * ld;
-    for (int e = tid; e < ntok * nh; e += blockDim.x) {
-        const int t = e / nh, hh = e - t * nh;
-        const int64_t src = (Tb + t) * H + h0 + hh;
-        sg[hh * ld + t] = gate_logdecay(to_f32(a[src]), b, gate);
-        if (Bt) sb[hh * ld + t] = to_f32(beta[src]);
+    const int warp = tid >> 5, lane = tid & 31;
+    constexpr int kRows = kGateTok / 8;   // token rows per warp (8 warps)
+    if (lane < nh) {   // warp per token row, lane per head; all loads in flight at once
+        float av[kRows], bv[kRows];
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+            const int t = warp + 8 * r;
+            const int64_t src = (Tb + min(t, ntok - 1)) * H + h0 + lane;
+            av[r] = to_f32(a[src]);
+            bv[r] = Bt ? to_f32(beta[src]) : 0.f;
+        }
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+            const int t = warp + 8 * r;
+            if (t < ntok) {
+                sg[lane * ld + t] = gate_logdecay(av[r], b, gate);
+                sb[lane * ld + t] = bv[r];
+            }
+        }
     }
     __syncthreads();
     {
@@ -162,11 +176,12 @@ gate_cumsum_kernel(const T *__restrict__ a, const T *__restrict__ beta, float *_
         }
     }
     __syncthreads();
-    for (int e = tid; e < nh * ntok; e += blockDim.x) {
-        const int hh = e / ntok, t = e - hh * ntok;
-        const int64_t dst = (int64_t)(h0 + hh) * T_total + Tb + t;
-        G[dst] = sg[hh * ld + t];
-        if (Bt) Bt[dst] = sb[hh * ld + t];
+    for (int hh = warp; hh < nh; hh += 8) {   // warp per head row, lane per token
+        const int64_t dst = (int64_t)(h0 + hh) * T_total + Tb;
+        for (int t = lane; t < ntok; t += 32) {
+            G[dst + t] = sg[hh * ld + t];
+            if (Bt) Bt[dst + t] = sb[hh * ld + t];
+        }
     }
 }
 
