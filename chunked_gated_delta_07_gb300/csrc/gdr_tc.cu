@@ -557,11 +557,14 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     if (use_v)
                         mma_f16_ss(tm + cb, smem_desc(sb + kOffV, kBox, 1024, kSw128),
                                    smem_desc(sb + kOffBU, 128, (kC / 8) * 128, kSwNone), id_u, 0);
+                    // K-step s8 of [-W ; Qt] starts (s8 / 4) column blocks and 32 (s8 % 4)
+                    // bytes in: added to the start-address field (shared addresses are
+                    // below 256 KiB, so the 14-bit field never carries)
+                    const uint64_t dwq = smem_desc(sb + kOffWQ, 16, 1024, kSw128);
 #pragma unroll
                     for (int s8 = 0; s8 < kD / 8; ++s8)
                         mma_tf32_ts(tm + cb + kC, tm + kColH + 8 * s8,
-                                    smem_desc(sb + kOffWQ + (s8 >> 2) * kWQBlock + 32 * (s8 & 3), 16, 1024, kSw128),
-                                    id_x, s8 > 0);
+                                    dwq + (uint64_t)(((s8 >> 2) * kWQBlock + 32 * (s8 & 3)) >> 4), id_x, s8 > 0);
                     mma_commit(&bar_x[buf]);
                 }
                 __syncwarp();
@@ -794,19 +797,26 @@ tc_combine_kernel(float *Hin, const float *Bs, const float *Ms, const int *mneed
     const int64_t g0 = p.seg_base[n];
     const int nseg = (int)(p.seg_base[n + 1] - g0);
     const int j0 = slice * kCombCols, tid = threadIdx.x;
+    // Hs holds H_in(s - 1) for this block's columns, or (lazily) it is B of the
+    // segment before, still in global memory: a run of negligible transitions
+    // costs nothing until a transition that needs H_in arrives
+    const float *pending = nullptr;
     for (int s = 1; s < nseg; ++s) {
         const int64_t prev = (g0 + s - 1) * H + h, cur = (g0 + s) * H + h;
         const float *B = Bs + prev * kD * kD;
         float *Hc = Hin + cur * kD * kD;
         if (s == 1 || mneed[prev] == 0) {
             // M of the previous segment is negligible (or s = 1): H_in(s) = B(s-1),
-            // which the output pass reads in place; only the running copy is kept
+            // which the output pass reads in place
+            pending = B;
+            continue;
+        }
+        if (pending) {
             for (int e = tid; e < kD * kCombCols; e += 256) {
                 const int d = e / kCombCols, j = e % kCombCols;
-                Hs[e] = B[d * kD + j0 + j];
+                Hs[e] = pending[d * kD + j0 + j];
             }
-            __syncthreads();
-            continue;
+            pending = nullptr;
         }
         const float *M = Ms + prev * kD * kD;
         for (int e = tid; e < kD * kD; e += 256) Msh[(e / kD) * (kD + 1) + e % kD] = M[e];
