@@ -457,8 +457,8 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                         for (int i = 0; i < kC; ++i)
                             *(__nv_bfloat16 *)(stg + kOffBU + cc_off(i, j)) = __float2bfloat16_rn(tcol[i] * bj);
-                } else {                  // Bw = T diag(beta e^G), row-major for ldmatrix
-                    const float bej = bj * __expf(hdr->G[j]);
+                } else {                  // -Bw = -T diag(beta e^G), row-major for ldmatrix
+                    const float bej = -bj * __expf(hdr->G[j]);
 #pragma unroll
                     for (int i = 0; i < kC; ++i)
                         *(__nv_bfloat16 *)(BW + i * 32 + j * 2) = __float2bfloat16_rn(tcol[i] * bej);
@@ -490,7 +490,7 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
             __syncwarp();
             if (lane == 0) TC_TRACE(c, 5);
-            // ---- W = Bw K (mma.sync) -> rows [0, C) of WQ as -W in tf32
+            // ---- -W = (-Bw) K (mma.sync) -> rows [0, C) of WQ in tf32
             {
                 uint32_t af[4];
                 ldsm_x4(smem_u32(BW + (lane & 15) * 32 + (lane >> 4) * 16), af);
@@ -510,8 +510,8 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         const float *w = t == 0 ? w0 : w1;
                         const int d = 16 * np + 8 * t + 2 * (lane & 3);
                         uint8_t *base = stg + kOffWQ + (d >> 5) * kWQBlock;
-                        *(float2 *)(base + sw128_off(i0, (d & 31) * 4)) = make_float2(-w[0], -w[1]);
-                        *(float2 *)(base + sw128_off(i0 + 8, (d & 31) * 4)) = make_float2(-w[2], -w[3]);
+                        *(float2 *)(base + sw128_off(i0, (d & 31) * 4)) = make_float2(w[0], w[1]);
+                        *(float2 *)(base + sw128_off(i0 + 8, (d & 31) * 4)) = make_float2(w[2], w[3]);
                     }
                 }
             }
@@ -537,6 +537,14 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const uint32_t id_x = instr_desc(128, use_q ? 2 * kC : kC, 2, false, false);
             const uint32_t id_h = instr_desc(128, kD, 1, false, true);
             const uint32_t id_o = instr_desc(128, kC, 1, false, false);
+            // operand descriptors of stage 0; stage st adds st * kStage to the
+            // start-address field (shared addresses are below 256 KiB: no carry)
+            const uint32_t s0 = smem_u32(smem);
+            const uint64_t dV = smem_desc(s0 + kOffV, kBox, 1024, kSw128);
+            const uint64_t dK = smem_desc(s0 + kOffK, kBox, 1024, kSw128);
+            const uint64_t dBU = smem_desc(s0 + kOffBU, 128, (kC / 8) * 128, kSwNone);
+            const uint64_t dP = smem_desc(s0 + kOffP, 128, (kC / 8) * 128, kSwNone);
+            const uint64_t dWQ = smem_desc(s0 + kOffWQ, 16, 1024, kSw128);
             bool ok = nch == 0 || __all_sync(kFull, mbar_wait(&bar_init[0], 0, kWaitNs));
             for (int c = 0; c < nch && ok; ++c) {
                 if (__any_sync(kFull, *abort_state != 0 || *abort_prep != 0)) {
@@ -544,7 +552,7 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     break;
                 }
                 const int st = c % kNS, buf = c & 1;
-                const uint32_t sb = smem_u32(smem + st * kStage);
+                const uint64_t so = (uint64_t)((st * kStage) >> 4);   // stage offset in descriptor units
                 const uint32_t cb = kColB + buf * kColBuf;
                 if (!__all_sync(kFull, mbar_wait(&bar_prep[st], (uint32_t)(c / kNS) & 1u, kWaitNs))) {
                     ok = false;
@@ -555,12 +563,11 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 // front: U^T and [-W ; Qt] H^ into buffer c & 1
                 if (elect_one()) {
                     if (use_v)
-                        mma_f16_ss(tm + cb, smem_desc(sb + kOffV, kBox, 1024, kSw128),
-                                   smem_desc(sb + kOffBU, 128, (kC / 8) * 128, kSwNone), id_u, 0);
+                        mma_f16_ss(tm + cb, dV + so, dBU + so, id_u, 0);
                     // K-step s8 of [-W ; Qt] starts (s8 / 4) column blocks and 32 (s8 % 4)
                     // bytes in: added to the start-address field (shared addresses are
                     // below 256 KiB, so the 14-bit field never carries)
-                    const uint64_t dwq = smem_desc(sb + kOffWQ, 16, 1024, kSw128);
+                    const uint64_t dwq = dWQ + so;
 #pragma unroll
                     for (int s8 = 0; s8 < kD / 8; ++s8)
                         mma_tf32_ts(tm + cb + kC, tm + kColH + 8 * s8,
@@ -578,10 +585,10 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (lane == 0) TC_TRACE(c, 11);
                 tc_fence_after();
                 if (elect_one()) {
-                    mma_f16_ts(tm + kColH, tm + kColA, smem_desc(sb + kOffK, kBox, 1024, kSw128), id_h, 1);
+                    mma_f16_ts(tm + kColH, tm + kColA, dK + so, id_h, 1);
                     if (use_q)
                         mma_f16_ts(tm + cb + 2 * kC, tm + kColA + kC / 2,
-                                   smem_desc(sb + kOffP, 128, (kC / 8) * 128, kSwNone), id_o, 1);
+                                   dP + so, id_o, 1);
                     mma_commit(&bar_free[st]);
                 }
                 __syncwarp();
@@ -624,11 +631,17 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (lane == 0) mbar_arrive(&bar_init[0]);
         // One tile's output for this warp's 32 value columns: per token row, the
         // warp writes 64 contiguous bytes.
+        const int64_t orow = (int64_t)H * kD;   // elements between token rows
         auto store_out = [&](const uint32_t (&o)[kC], int len, int64_t t0, float scale) {
             __nv_bfloat16 *out = (__nv_bfloat16 *)args.out + (t0 * H + h) * kD + e;
+            if (len == kC) {
 #pragma unroll
-            for (int i = 0; i < kC; ++i)
-                if (i < len) out[(int64_t)i * H * kD] = __float2bfloat16_rn(__uint_as_float(o[i]) * scale);
+                for (int i = 0; i < kC; ++i) out[i * orow] = __float2bfloat16_rn(__uint_as_float(o[i]) * scale);
+            } else {
+#pragma unroll
+                for (int i = 0; i < kC; ++i)
+                    if (i < len) out[i * orow] = __float2bfloat16_rn(__uint_as_float(o[i]) * scale);
+            }
         };
         float Gamma = 1.f;                // H = Gamma * H^
         float gamma_prev = 1.f;           // Gamma of the previous tile's output
