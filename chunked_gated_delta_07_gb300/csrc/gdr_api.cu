@@ -56,12 +56,17 @@ ProfScope::~ProfScope() {
 
 namespace {
 
+constexpr int kMaxPieces = 8;   // pieces of a pipelined host-buffer call
+
 struct DeviceCtx {
     int *d_status = nullptr;
     void *ws = nullptr;  // internal workspace cache
     size_t ws_bytes = 0;
     void *io = nullptr;  // device copies for the host-buffer entry point
     size_t io_bytes = 0;
+    // copy streams and per-piece events of the pipelined host-buffer entry point
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t ev_in[kMaxPieces] = {}, ev_comp[kMaxPieces] = {}, ev_out[kMaxPieces] = {};
 };
 
 std::mutex g_mu;
@@ -244,6 +249,202 @@ gdr_status_t run_forward(const void *q, const void *k, const void *v, const void
     return err == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------------------
+// host-buffer forward, pipelined: the tokens are cut into pieces (dense input:
+// tile-aligned ranges of every sequence, the state carried from piece to
+// piece; packed input: groups of whole sequences), and piece p runs while
+// piece p + 1 is copied in and piece p - 1 is copied out, on two copy streams.
+// Device buffers of the pieces are double buffered.
+// ---------------------------------------------------------------------------
+struct Piece {
+    int64_t t0, t1;   // dense: token range of every sequence; packed: token range
+    int g0, g1;       // packed: sequence range
+};
+
+bool pipe_ready(DeviceCtx *c) {
+    if (c->s_in) return true;
+    if (cudaStreamCreateWithFlags(&c->s_in, cudaStreamNonBlocking) != cudaSuccess) return false;
+    if (cudaStreamCreateWithFlags(&c->s_out, cudaStreamNonBlocking) != cudaSuccess) return false;
+    for (int i = 0; i < kMaxPieces; ++i)
+        if (cudaEventCreateWithFlags(&c->ev_in[i], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&c->ev_comp[i], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&c->ev_out[i], cudaEventDisableTiming) != cudaSuccess)
+            return false;
+    return true;
+}
+
+// The pieces of a call, or none (fewer than two) when it is better run whole.
+std::vector<Piece> host_pieces(const Shape &s, const int32_t *cu) {
+    std::vector<Piece> pcs;
+    const int64_t units = s.T_total * s.H;
+    if (units < ((int64_t)1 << 21)) return pcs;            // small: one piece
+    const int want = (int)std::min<int64_t>(kMaxPieces, std::max<int64_t>(2, units >> 21));
+    if (!s.varlen) {
+        int64_t step = (s.T_per + want - 1) / want;
+        step = (step + s.C - 1) / s.C * s.C;                // tile aligned
+        for (int64_t t0 = 0; t0 < s.T_per; t0 += step)
+            pcs.push_back({t0, std::min(s.T_per, t0 + step), 0, s.N});
+    } else {
+        // only well-formed offsets are cut here; anything else runs whole, where
+        // the device-side plan reports it
+        if (cu[0] != 0 || cu[s.N] != s.T_total) return pcs;
+        for (int g = 0; g < s.N; ++g)
+            if (cu[g + 1] < cu[g]) return pcs;
+        const int64_t target = (s.T_total + want - 1) / want;
+        int g0 = 0;
+        for (int g = 0; g < s.N; ++g) {
+            if (cu[g + 1] - cu[g0] >= target || g == s.N - 1) {
+                pcs.push_back({cu[g0], cu[g + 1], g0, g + 1});
+                g0 = g + 1;
+            }
+        }
+        if (pcs.size() > (size_t)kMaxPieces) pcs.clear();   // cannot happen; be safe
+    }
+    if (pcs.size() < 2) pcs.clear();
+    return pcs;
+}
+
+gdr_status_t fwd_host_pipelined(const void *q, const void *k, const void *v, const void *a,
+                                const void *beta, const float *h0, void *out, float *hT,
+                                const int32_t *cu, const Shape &s, const std::vector<Piece> &pcs,
+                                float b, gdr_dtype_t dtype, gdr_gate_t gate, gdr_path_t path,
+                                cudaStream_t stream) {
+    DeviceCtx *ctx = device_ctx();
+    if (!ctx) return GDR_ERR_CUDA;
+    const size_t es = dtype == GDR_BF16 ? 2 : 4;
+    const int H = s.H;
+    const size_t rk = (size_t)H * s.dk * es, rv = (size_t)H * s.dv * es, r1 = (size_t)H * es;
+    const size_t nst1 = (size_t)H * s.dk * s.dv * sizeof(float);   // one sequence's state
+    const int np = (int)pcs.size();
+    // the largest piece, in token rows and sequences
+    int64_t max_rows = 0;
+    int max_seq = 0;
+    for (const Piece &pc : pcs) {
+        const int64_t rows = s.varlen ? pc.t1 - pc.t0 : (int64_t)s.N * (pc.t1 - pc.t0);
+        max_rows = std::max(max_rows, rows);
+        max_seq = std::max(max_seq, pc.g1 - pc.g0);
+    }
+    // device layout: 2 x [q k v a beta cu] in, 2 x out, states
+    const size_t in_sz[6] = {max_rows * rk, max_rows * rk, max_rows * rv, max_rows * r1,
+                             max_rows * r1, sizeof(int32_t) * (size_t)(max_seq + 1)};
+    size_t in_off[6], in_tot = 0;
+    for (int i = 0; i < 6; ++i) {
+        in_off[i] = in_tot;
+        in_tot += align_up(in_sz[i]);
+    }
+    const size_t out_tot = align_up(max_rows * rv);
+    const size_t st_tot = align_up((size_t)s.N * nst1);
+    // dense: 2 carried states (+ h0); packed: all entering states and all final states
+    const size_t tot = 2 * in_tot + 2 * out_tot + 3 * st_tot;
+    char *io;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!pipe_ready(ctx)) return GDR_ERR_CUDA;
+        if (!grow(&ctx->io, &ctx->io_bytes, tot)) return GDR_ERR_CUDA;
+        io = (char *)ctx->io;
+    }
+    char *IN[2] = {io, io + in_tot};
+    char *OUT[2] = {io + 2 * in_tot, io + 2 * in_tot + out_tot};
+    float *ST0 = (float *)(io + 2 * in_tot + 2 * out_tot);        // dense: carried state A / packed: h0
+    float *ST1 = (float *)((char *)ST0 + st_tot);                 // dense: carried state B / packed: hT
+    float *dH0 = (float *)((char *)ST1 + st_tot);                 // dense: h0
+    // the workspace of the largest piece, grown once before anything is queued
+    {
+        Shape ps = s;
+        ps.N = s.varlen ? max_seq : s.N;
+        ps.T_total = max_rows;
+        ps.T_per = s.varlen ? 0 : max_rows / s.N;
+        ps.max_chunks = tile_bound(s.varlen, ps.N, s.varlen ? max_rows : ps.T_per, s.C);
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!grow(&ctx->ws, &ctx->ws_bytes, layout_for(ps, path).total)) return GDR_ERR_CUDA;
+    }
+    auto ck = [](cudaError_t e) { return e == cudaSuccess; };
+    cudaStream_t si = ctx->s_in, so = ctx->s_out;
+    // everything queued before this call on `stream` precedes the copies
+    if (!ck(cudaEventRecord(ctx->ev_out[0], stream)) || !ck(cudaStreamWaitEvent(si, ctx->ev_out[0], 0)) ||
+        !ck(cudaStreamWaitEvent(so, ctx->ev_out[0], 0)))
+        return GDR_ERR_CUDA;
+    if (h0 && !ck(cudaMemcpyAsync(s.varlen ? ST0 : dH0, h0, (size_t)s.N * nst1, cudaMemcpyHostToDevice, si)))
+        return GDR_ERR_CUDA;
+    std::vector<std::vector<int32_t>> cus(np);
+    for (int p = 0; p < np; ++p) {
+        const Piece &pc = pcs[p];
+        char *in = IN[p & 1];
+        // ---- copy in (after the compute of piece p - 2 released the buffer)
+        if (p >= 2 && !ck(cudaStreamWaitEvent(si, ctx->ev_comp[p - 2], 0))) return GDR_ERR_CUDA;
+        const void *src[5] = {q, k, v, a, beta};
+        const size_t rb[5] = {rk, rk, rv, r1, r1};
+        for (int i = 0; i < 5; ++i) {
+            if (s.varlen) {
+                if (!ck(cudaMemcpyAsync(in + in_off[i], (const char *)src[i] + pc.t0 * rb[i],
+                                        (pc.t1 - pc.t0) * rb[i], cudaMemcpyHostToDevice, si)))
+                    return GDR_ERR_CUDA;
+            } else {
+                const size_t w = (size_t)(pc.t1 - pc.t0) * rb[i];
+                if (!ck(cudaMemcpy2DAsync(in + in_off[i], w, (const char *)src[i] + pc.t0 * rb[i],
+                                          (size_t)s.T_per * rb[i], w, s.N, cudaMemcpyHostToDevice, si)))
+                    return GDR_ERR_CUDA;
+            }
+        }
+        if (s.varlen) {
+            cus[p].resize(pc.g1 - pc.g0 + 1);
+            for (int g = pc.g0; g <= pc.g1; ++g) cus[p][g - pc.g0] = (int32_t)(cu[g] - cu[pc.g0]);
+            if (!ck(cudaMemcpyAsync(in + in_off[5], cus[p].data(), sizeof(int32_t) * cus[p].size(),
+                                    cudaMemcpyHostToDevice, si)))
+                return GDR_ERR_CUDA;
+        }
+        if (!ck(cudaEventRecord(ctx->ev_in[p], si))) return GDR_ERR_CUDA;
+        // ---- compute (after its copy-in, and after the copy-out of piece p - 2)
+        if (!ck(cudaStreamWaitEvent(stream, ctx->ev_in[p], 0))) return GDR_ERR_CUDA;
+        if (p >= 2 && !ck(cudaStreamWaitEvent(stream, ctx->ev_out[p - 2], 0))) return GDR_ERR_CUDA;
+        Shape ps = s;
+        const float *hin;
+        float *hout;
+        if (s.varlen) {
+            ps.N = pc.g1 - pc.g0;
+            ps.T_total = pc.t1 - pc.t0;
+            ps.T_per = 0;
+            ps.max_chunks = tile_bound(true, ps.N, ps.T_total, s.C);
+            hin = h0 ? ST0 + (size_t)pc.g0 * (nst1 / sizeof(float)) : nullptr;
+            hout = ST1 + (size_t)pc.g0 * (nst1 / sizeof(float));
+        } else {
+            ps.T_per = pc.t1 - pc.t0;
+            ps.T_total = (int64_t)s.N * ps.T_per;
+            ps.max_chunks = tile_bound(false, s.N, ps.T_per, s.C);
+            hin = p == 0 ? (h0 ? dH0 : nullptr) : ((p - 1) & 1 ? ST1 : ST0);
+            hout = (p & 1) ? ST1 : ST0;
+        }
+        const gdr_status_t st =
+            run_forward(in + in_off[0], in + in_off[1], in + in_off[2], in + in_off[3], in + in_off[4],
+                        hin, OUT[p & 1], hout, s.varlen ? (const int32_t *)(in + in_off[5]) : nullptr, ps, b,
+                        dtype, gate, path, nullptr, 0, stream);
+        if (st != GDR_OK) return st;
+        if (!ck(cudaEventRecord(ctx->ev_comp[p], stream))) return GDR_ERR_CUDA;
+        // ---- copy out
+        if (!ck(cudaStreamWaitEvent(so, ctx->ev_comp[p], 0))) return GDR_ERR_CUDA;
+        if (s.varlen) {
+            if (!ck(cudaMemcpyAsync((char *)out + pc.t0 * rv, OUT[p & 1], (pc.t1 - pc.t0) * rv,
+                                    cudaMemcpyDeviceToHost, so)))
+                return GDR_ERR_CUDA;
+            if (hT && !ck(cudaMemcpyAsync((char *)hT + (size_t)pc.g0 * nst1, hout,
+                                          (size_t)(pc.g1 - pc.g0) * nst1, cudaMemcpyDeviceToHost, so)))
+                return GDR_ERR_CUDA;
+        } else {
+            const size_t w = (size_t)(pc.t1 - pc.t0) * rv;
+            if (!ck(cudaMemcpy2DAsync((char *)out + pc.t0 * rv, (size_t)s.T_per * rv, OUT[p & 1], w, w,
+                                      s.N, cudaMemcpyDeviceToHost, so)))
+                return GDR_ERR_CUDA;
+            if (p == np - 1 && hT &&
+                !ck(cudaMemcpyAsync(hT, hout, (size_t)s.N * nst1, cudaMemcpyDeviceToHost, so)))
+                return GDR_ERR_CUDA;
+        }
+        if (!ck(cudaEventRecord(ctx->ev_out[p], so))) return GDR_ERR_CUDA;
+    }
+    const bool ok = ck(cudaStreamSynchronize(so)) && ck(cudaStreamSynchronize(stream)) &&
+                    ck(cudaStreamSynchronize(si));
+    return ok ? GDR_OK : GDR_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace gdr
 
@@ -310,6 +511,12 @@ gdr_status_t gdr_chunk_fwd_host(const void *q, const void *k, const void *v, con
                                  chunk, b, dtype, gate, path, &s);
     if (st != GDR_OK) return st;
     cudaStream_t stream = (cudaStream_t)stream_;
+    {
+        const std::vector<Piece> pcs = host_pieces(s, cu_seqlens);
+        if (!pcs.empty())
+            return fwd_host_pipelined(q, k, v, a, beta, h0, out, hT, cu_seqlens, s, pcs, b, dtype,
+                                      gate, resolve_path(path, dtype, dk, dv, chunk), stream);
+    }
     DeviceCtx *ctx = device_ctx();
     if (!ctx) return GDR_ERR_CUDA;
     const size_t es = dtype == GDR_BF16 ? 2 : 4;
@@ -438,12 +645,19 @@ void gdr_release(void) {
     cudaGetDevice(&cur);
     for (size_t d = 0; d < g_ctx.size(); ++d) {
         DeviceCtx &c = g_ctx[d];
-        if (!c.ws && !c.io && !c.d_status) continue;
+        if (!c.ws && !c.io && !c.d_status && !c.s_in) continue;
         cudaSetDevice((int)d);
         cudaDeviceSynchronize();
         if (c.ws) cudaFree(c.ws);
         if (c.io) cudaFree(c.io);
         if (c.d_status) cudaFree(c.d_status);
+        if (c.s_in) cudaStreamDestroy(c.s_in);
+        if (c.s_out) cudaStreamDestroy(c.s_out);
+        for (int i = 0; i < kMaxPieces; ++i) {
+            if (c.ev_in[i]) cudaEventDestroy(c.ev_in[i]);
+            if (c.ev_comp[i]) cudaEventDestroy(c.ev_comp[i]);
+            if (c.ev_out[i]) cudaEventDestroy(c.ev_out[i]);
+        }
         c = DeviceCtx{};
     }
     cudaSetDevice(cur);

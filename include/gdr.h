@@ -142,6 +142,13 @@ GDR_API size_t gdr_chunk_fwd_workspace_size(int B, int64_t T, int H, int dk, int
  * layouts as gdr_chunk_fwd_ex except that every tensor pointer, including
  * cu_seqlens, is host memory (pinned memory gives full copy bandwidth).
  * Device buffers come from the internal per-device cache.
+ * From 2^21 (token, head) units up, the call is pipelined: the tokens are cut
+ * into up to 8 pieces (dense input: tile-aligned token ranges of every
+ * sequence, the state carried from piece to piece; packed input: groups of
+ * whole sequences, when cu_seqlens is well formed) and a piece's copies in
+ * and out overlap the neighbouring pieces' passes, on two internal copy
+ * streams.  The result then differs from gdr_chunk_fwd_ex's only by the
+ * rounding of the different segment split.
  */
 GDR_API gdr_status_t gdr_chunk_fwd_host(const void *q, const void *k, const void *v, const void *a,
                                 const void *beta, const float *h0, void *out, float *hT,
