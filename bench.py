@@ -230,6 +230,10 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the tokens per sequence (or total, varlen) of the workload")
+    ap.add_argument("--mode", default="prefill", choices=["prefill", "decode"],
+                    help="prefill: the chunked forward (the headline); decode: one recurrent "
+                         "step of --decode-seqs sequences")
+    ap.add_argument("--decode-seqs", type=int, default=256)
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     return args
@@ -244,6 +248,9 @@ def main(argv=None):
         w = w.with_(T=args.tokens)
     if args.impl == "reference":
         bench_reference(args, w)
+        return
+    if args.mode == "decode":
+        bench_decode(args)
         return
 
     import torch
@@ -363,6 +370,58 @@ def main(argv=None):
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def bench_decode(args):
+    """One decode step (gdr_recurrent_fwd, T = 1) of N sequences x 16 heads, d = 128, bf16:
+    bound by reading and writing the fp32 state (268 MB at N = 256, larger than L2)."""
+    import torch
+    import chunked_gated_delta_07_gb300 as gdr
+    N, H, d = args.decode_seqs, 16, 128
+    from gdr_inputs import WORKLOADS, make_inputs   # the t1m recipe, one token per sequence
+    x = make_inputs(WORKLOADS["t1m"].with_(B=N, h0_std=0.02, seed=4000), device="cuda", T=1)
+    state = x["h0"].clone()
+    out = torch.empty_like(x["v"])
+    stream = torch.cuda.current_stream()
+
+    def step():
+        rc = gdr.gdr_recurrent_fwd(x["q"], x["k"], x["v"], x["a"], x["beta"], state, out, N, 1, H,
+                                   d, d, 2.0, gdr.GDR_BF16, gdr.GDR_GATE_BOUNDED, stream)
+        if rc != gdr.GDR_OK:
+            raise gdr.GdrError(rc, "gdr_recurrent_fwd")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    steps = max(args.steps, 20)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        n0 = gdr.gdr_launch_count()
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        n_launch = gdr.gdr_launch_count() - n0
+    st = gdr.gdr_get_status(stream)
+    if st != gdr.GDR_OK:
+        raise gdr.GdrError(st, "device status after decode")
+    ms = ev0.elapsed_time(ev1) / steps
+    hbm, _, _, peak_src = peaks()
+    byt = 2 * N * H * d * d * 4 + N * H * (4 * d * 2 + 2 * 2)   # state in + out, q k v out, a beta
+    achieved = byt / (ms / 1e3) / 1e9
+    print(json.dumps({
+        "metric": "decode tokens/s, one recurrent step, 16 heads, d=128, bf16, fp32 state",
+        "value": N / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"decode: N={N} sequences x H={H}, dk=dv={d}, T=1 per step",
+                   "l2_policy": "state larger than L2 (no flush)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None, "kernel": "recurrent_kernel",
+                     "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_step": byt},
+        "gpu_launches": n_launch, "clocks": clk.summary(),
+    }), flush=True)
 
 
 def bench_e2e(gdr, torch, x, w, args, dcode, gcode, pcode, n_tokens):

@@ -28,7 +28,7 @@ GDR_PATH_AUTO, GDR_PATH_SIMT, GDR_PATH_TC = 0, 1, 2
 EXPORTS = ("gdr_chunk_fwd", "gdr_chunk_fwd_ex", "gdr_chunk_fwd_workspace_size",
            "gdr_chunk_fwd_host", "gdr_gate_cumsum", "gdr_wy_repr", "gdr_get_status",
            "gdr_status_string", "gdr_release", "gdr_launch_count", "gdr_profile_enable",
-           "gdr_profile_read", "gdr_chunk_fwd_noalloc")
+           "gdr_profile_read", "gdr_chunk_fwd_noalloc", "gdr_recurrent_fwd")
 
 _lock = threading.Lock()
 _lib = None
@@ -48,6 +48,7 @@ _SIGS = {
     "gdr_profile_enable": (None, [_I]),
     "gdr_profile_read": (_I, [_P, _P, _P, _I]),
     "gdr_chunk_fwd_noalloc": (_I, [_P] * 8 + [_I, _I64, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "gdr_recurrent_fwd": (_I, [_P] * 7 + [_I, _I64, _I, _I, _I, _F, _I, _I, _P]),
 }
 
 
@@ -126,6 +127,28 @@ def gdr_chunk_fwd_noalloc(q, k, v, a, beta, h0, out, hT, B, T, H, dk, dv, chunk,
     return lib().gdr_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(beta), _ptr(h0),
                                        _ptr(out), _ptr(hT), B, T, H, dk, dv, chunk, float(b), dtype,
                                        gate, _stream(stream))
+
+
+def gdr_recurrent_fwd(q, k, v, a, beta, state, out, N, T, H, dk, dv, b, dtype, gate,
+                      stream=None) -> int:
+    """Token-by-token form (decoding): advances state [N,H,dk,dv] in place over T tokens."""
+    return lib().gdr_recurrent_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(beta), _ptr(state),
+                                   _ptr(out), N, T, H, dk, dv, float(b), dtype, gate, _stream(stream))
+
+
+def recurrent_fwd(q, k, v, a, beta, state, b=2.0, gate="bounded", out=None, stream=None):
+    """Decode T tokens: q,k [N,T,H,dk], v [N,T,H,dv], a,beta [N,T,H] on one device, state
+    [N,H,dk,dv] fp32 updated in place; returns out [N,T,H,dv] (raises GdrError on failure)."""
+    import torch
+    N, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((N, T, H, dv), dtype=q.dtype, device=q.device)
+    rc = gdr_recurrent_fwd(q, k, v, a, beta, state, out, N, T, H, dk, dv, b, dtype_code(q),
+                           _GATES[gate], stream)
+    if rc != GDR_OK:
+        raise GdrError(rc, "gdr_recurrent_fwd")
+    return out
 
 
 def gdr_gate_cumsum(a, G, cu_seqlens, B, T, H, chunk, b, dtype, gate, stream=None) -> int:

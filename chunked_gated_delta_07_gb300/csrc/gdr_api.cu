@@ -556,6 +556,33 @@ gdr_status_t gdr_chunk_fwd_host(const void *q, const void *k, const void *v, con
     return cudaStreamSynchronize(stream) == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 
+gdr_status_t gdr_recurrent_fwd(const void *q, const void *k, const void *v, const void *a,
+                               const void *beta, float *state, void *out, int N, int64_t T,
+                               int H, int dk, int dv, float b, gdr_dtype_t dtype,
+                               gdr_gate_t gate, gdr_stream_t stream) {
+    if (dtype != GDR_BF16 && dtype != GDR_F32) return GDR_ERR_INVALID_ARG;
+    if (gate != GDR_GATE_BOUNDED && gate != GDR_GATE_SOFTPLUS) return GDR_ERR_INVALID_ARG;
+    if (N < 1 || H < 1 || T < 0) return GDR_ERR_INVALID_ARG;
+    if (gate == GDR_GATE_BOUNDED && !(b > 0.f && std::isfinite(b))) return GDR_ERR_INVALID_ARG;
+    if ((dk != 64 && dk != 128) || (dv != 64 && dv != 128)) return GDR_ERR_UNSUPPORTED;
+    if (T > ((int64_t)1 << 40) || (int64_t)N * T > ((int64_t)1 << 40)) return GDR_ERR_UNSUPPORTED;
+    if (T == 0) return GDR_OK;
+    if (!q || !k || !v || !a || !beta || !state || !out) return GDR_ERR_INVALID_ARG;
+    const size_t es = dtype == GDR_BF16 ? 2 : 4;
+    const size_t rows = (size_t)N * T * H;
+    const size_t out_bytes = rows * dv * es, n_state = (size_t)N * H * dk * dv * sizeof(float);
+    const void *ins[5] = {q, k, v, a, beta};
+    const size_t in_bytes[5] = {rows * dk * es, rows * dk * es, rows * dv * es, rows * es, rows * es};
+    for (int i = 0; i < 5; ++i)
+        if (overlaps(out, out_bytes, ins[i], in_bytes[i]) || overlaps(state, n_state, ins[i], in_bytes[i]))
+            return GDR_ERR_INVALID_ARG;
+    if (overlaps(out, out_bytes, state, n_state)) return GDR_ERR_INVALID_ARG;
+    return launch_recurrent(q, k, v, a, beta, state, out, dtype, N, T, H, dk, dv, b, gate,
+                            (cudaStream_t)stream) == cudaSuccess
+               ? GDR_OK
+               : GDR_ERR_CUDA;
+}
+
 gdr_status_t gdr_gate_cumsum(const void *a, float *G, const int32_t *cu_seqlens, int B,
                              int64_t T, int H, int chunk, float b, gdr_dtype_t dtype,
                              gdr_gate_t gate, gdr_stream_t stream) {

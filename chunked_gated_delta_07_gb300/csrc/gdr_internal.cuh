@@ -92,6 +92,11 @@ cudaError_t launch_wy_simt(const void *k, const void *v, const void *beta, const
                            int dv, int64_t T_total, int64_t max_chunks, cudaStream_t stream);
 
 // Stages 3+4 on CUDA cores: the tile-to-tile state pass and the outputs.
+// The recurrent form over T tokens per sequence, the fp32 state updated in place.
+cudaError_t launch_recurrent(const void *q, const void *k, const void *v, const void *a,
+                             const void *beta, float *state, void *out, gdr_dtype_t dtype, int N,
+                             int64_t T, int H, int dk, int dv, float b, gdr_gate_t gate,
+                             cudaStream_t stream);
 cudaError_t launch_state_out_simt(const void *q, const void *k, const float *W, const float *U,
                                   const float *G, const float *h0, void *out, float *hT,
                                   gdr_dtype_t dtype, Plan plan, int H, int dk, int dv,

@@ -204,6 +204,31 @@ GDR_API gdr_status_t gdr_wy_repr(const void *k, const void *v, const void *beta,
                          int H, int dk, int dv, int chunk, gdr_dtype_t dtype,
                          gdr_stream_t stream);
 
+/*
+ * The recurrent (token-by-token) form, for decoding: advances each sequence's
+ * state over T tokens and writes their outputs; T = 1 is one decode step of
+ * an inference engine that keeps a constant-size state per sequence instead
+ * of a cache that grows with the context ("Evaluating Next-Gen Sparse MoE and
+ * Long-Context LLMs", §2.2: the state is updated token by token; §4, §5:
+ * chunked prefill and constant-state layers on the inference side).  A prompt
+ * is prefilled with gdr_chunk_fwd_ex (its hT is the state), then decoded here.
+ *
+ *   q, k   [N, T, H, dk]   v, out [N, T, H, dv]   a, beta [N, T, H]   (dtype)
+ *   state  [N, H, dk, dv]  fp32, read as the entering state and overwritten
+ *          with the state after the last token (same layout as h0 / hT)
+ * Per token: alpha = exp(g(a)), H <- alpha H + beta k (v - alpha H^T k)^T,
+ * o = H^T q (the same recurrence as gdr_chunk_fwd_ex, computed without tiles).
+ * Device pointers owned by the caller; nothing is retained or allocated.
+ * dk, dv in {64, 128}; N, H >= 1; T >= 0 (T = 0 leaves state untouched).
+ * out must not alias any input or state.  Returns GDR_ERR_INVALID_ARG or
+ * GDR_ERR_UNSUPPORTED before any launch, GDR_ERR_CUDA on a launch failure;
+ * the call is asynchronous on `stream`.
+ */
+GDR_API gdr_status_t gdr_recurrent_fwd(const void *q, const void *k, const void *v, const void *a,
+                               const void *beta, float *state, void *out, int N, int64_t T,
+                               int H, int dk, int dv, float b, gdr_dtype_t dtype,
+                               gdr_gate_t gate, gdr_stream_t stream);
+
 /* Synchronise `stream`, then read and clear the current device's status word.
  * Returns GDR_OK, GDR_ERR_BAD_SEQLENS, GDR_ERR_TIMEOUT or GDR_ERR_CUDA. */
 GDR_API gdr_status_t gdr_get_status(gdr_stream_t stream);
