@@ -10,6 +10,9 @@ Two independent references live here:
 * ``oracle_fwd`` -- the token-by-token recurrence in fp64, written in plain C
   (``gdr_oracle.c``, OpenMP over (sequence, head, column block)).  This is the
   definition the chunked GPU method must reproduce.
+* ``oracle_bwd`` -- the gradients of <dout, out> + <dhT, hT> with respect to
+  every input, by the token-by-token adjoint recurrence in fp64 (the same C
+  file), pinned by finite differences of ``oracle_fwd``.
 * ``chunk_ref`` -- the chunk-parallel (WY / UT) form in fp64 numpy, used only
   to check the GPU's intermediate stages (gate cumsum, W, U) one by one.
 
@@ -61,6 +64,11 @@ def _bind(path):
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
         ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    lib.gdr_oracle_bwd.restype = ctypes.c_int
+    lib.gdr_oracle_bwd.argtypes = (
+        [ctypes.c_void_p] * 5 + [ctypes.c_int] + [ctypes.c_void_p] * 9
+        + [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+           ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int])
     lib.gdr_oracle_gate.restype = ctypes.c_double
     lib.gdr_oracle_gate.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.c_int]
     lib.gdr_oracle_max_threads.restype = ctypes.c_int
@@ -99,6 +107,58 @@ def _as_array(x):
     if x.dtype == np.float32:
         return np.ascontiguousarray(x), F32
     return np.ascontiguousarray(x, dtype=np.float64), F64
+
+
+def oracle_bwd(q, k, v, a, beta, dout=None, dhT=None, h0=None, cu_seqlens=None,
+               b: float = 2.0, gate: str = "bounded", nthreads: int = 0,
+               _lib_path: str | None = None):
+    """fp64 gradients of <dout, out> + <dhT, hT> of the token-by-token forward.
+
+    Same shapes as ``oracle_fwd``; dout is [B,T,H,dv] and dhT [N,H,dk,dv] (None
+    means zero).  Returns a dict with dq, dk [B,T,H,dk], dv [B,T,H,dv], da, dbeta
+    [B,T,H] and dh0 [N,H,dk,dv], all fp64, with respect to the stored input values
+    (bf16 inputs widened exactly)."""
+    lib = _load() if _lib_path is None else _bind(_lib_path)
+    arrs = [_as_array(x) for x in (q, k, v, a, beta)]
+    if len({d for _, d in arrs}) != 1:
+        arrs = [(np.ascontiguousarray(_widen_np(x, d)), F64) for x, d in arrs]
+    (qa, dt), (ka, _), (va, _), (aa, _), (ba, _) = arrs
+    B, T, H, dk = qa.shape
+    dv = va.shape[-1]
+    if cu_seqlens is not None:
+        cu = np.ascontiguousarray(np.asarray(
+            cu_seqlens.cpu().numpy() if hasattr(cu_seqlens, "cpu") else cu_seqlens,
+            dtype=np.int64))
+        assert B == 1
+        N = cu.shape[0] - 1
+    else:
+        cu = None
+        N = B
+
+    def f64(x, shape):
+        if x is None:
+            return None
+        xa, xd = _as_array(x)
+        xa = np.ascontiguousarray(_widen_np(xa, xd))
+        assert xa.shape == shape, (xa.shape, shape)
+        return xa
+
+    h0a = f64(h0, (N, H, dk, dv))
+    dout_a = f64(dout, (B, T, H, dv))
+    dhT_a = f64(dhT, (N, H, dk, dv))
+    g = {"dq": np.zeros((B, T, H, dk)), "dk": np.zeros((B, T, H, dk)),
+         "dv": np.zeros((B, T, H, dv)), "da": np.zeros((B, T, H)),
+         "dbeta": np.zeros((B, T, H)), "dh0": np.zeros((N, H, dk, dv))}
+    ptr = lambda x: None if x is None else x.ctypes.data
+    rc = lib.gdr_oracle_bwd(
+        qa.ctypes.data, ka.ctypes.data, va.ctypes.data, aa.ctypes.data, ba.ctypes.data, dt,
+        ptr(h0a), ptr(dout_a), ptr(dhT_a), g["dq"].ctypes.data, g["dk"].ctypes.data,
+        g["dv"].ctypes.data, g["da"].ctypes.data, g["dbeta"].ctypes.data, g["dh0"].ctypes.data,
+        None if cu is None else cu.ctypes.data, N, T, H, dk, dv, float(b), GATES[gate],
+        int(nthreads))
+    if rc != 0:
+        raise ValueError(f"gdr_oracle_bwd rejected its arguments (code {rc})")
+    return g
 
 
 def max_threads() -> int:

@@ -179,6 +179,192 @@ int gdr_oracle_fwd(const void *q, const void *k, const void *v, const void *a,
     return 0;
 }
 
+/* d g / d a of the log-decay, for the backward pass. */
+static double gate_grad(double a, double b, int gate)
+{
+    const double s = sigmoid(a);
+    if (gate == OR_GATE_SOFTPLUS) return -s;
+    return -b * s * (1.0 - s);
+}
+
+/*
+ * Gradients of L = <dout, out> + <dhT, hT> with respect to q, k, v, a, beta
+ * and h0, for the recurrence of gdr_oracle_fwd (erase on).  Per token, with
+ * Hb = alpha H_{t-1}, p = Hb^T k, delta = beta (v - p), H_t = Hb + k delta^T,
+ * o = H_t^T q, the adjoints run backwards over the tokens:
+ *     dH     += q do^T            dq     = H_t do
+ *     dk     += dH delta          ddelta = dH^T k
+ *     dv      = beta ddelta       dbeta  = ddelta . (v - p)
+ *     dp      = -beta ddelta      dHb    = dH + k dp^T        dk += Hb dp
+ *     dalpha  = <H_{t-1}, dHb>    da     = dalpha alpha g'(a)  dH <- alpha dHb
+ * and dh0 is the final dH.  The states are recomputed forward from
+ * checkpoints kept every CK tokens.  dout and dhT may be NULL (zero); dhT and
+ * dh0 are [N,H,dk,dv]; the token gradients have the input layouts.
+ */
+int gdr_oracle_bwd(const void *q, const void *k, const void *v, const void *a,
+                   const void *beta, int in_dtype, const double *h0, const double *dout,
+                   const double *dhT, double *dq, double *dk_out, double *dv_out, double *da,
+                   double *dbeta, double *dh0, const int64_t *cu_seqlens, int B, int64_t T,
+                   int H, int dk, int dv, double b, int gate, int nthreads)
+{
+    if (B < 1 || T < 0 || H < 1 || dk < 1 || dv < 1) return 1;
+    if (in_dtype < OR_BF16 || in_dtype > OR_F64) return 1;
+    const int N = B;
+    if (cu_seqlens) {
+        if (cu_seqlens[0] != 0) return 2;
+        for (int n = 0; n < N; n++)
+            if (cu_seqlens[n + 1] < cu_seqlens[n]) return 2;
+        if (cu_seqlens[N] != T) return 2;
+    }
+    enum { CK = 64 };
+    const int64_t S = (int64_t)dk * dv;
+    const int64_t nunit = (int64_t)N * H;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int rc = 0;
+#pragma omp parallel
+    {
+        double *blk = (double *)malloc(sizeof(double) * (size_t)(CK + 1) * S); /* states of a block */
+        double *dH = (double *)malloc(sizeof(double) * (size_t)S);
+        double *kt = (double *)malloc(sizeof(double) * (size_t)dk);
+        double *qt = (double *)malloc(sizeof(double) * (size_t)dk);
+        double *p = (double *)malloc(sizeof(double) * (size_t)dv);
+        double *dl = (double *)malloc(sizeof(double) * (size_t)dv);
+        double *ddl = (double *)malloc(sizeof(double) * (size_t)dv);
+        double *dp = (double *)malloc(sizeof(double) * (size_t)dv);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t u = 0; u < nunit; u++) {
+            const int h = (int)(u % H);
+            const int n = (int)(u / H);
+            int64_t t_begin, t_end;
+            if (cu_seqlens) {
+                t_begin = cu_seqlens[n];
+                t_end = cu_seqlens[n + 1];
+            } else {
+                t_begin = (int64_t)n * T;
+                t_end = t_begin + T;
+            }
+            const int64_t len = t_end - t_begin;
+            const int64_t nck = (len + CK - 1) / CK + 1;
+            double *ck = (double *)malloc(sizeof(double) * (size_t)(nck > 0 ? nck : 1) * S);
+            if (!ck) {
+                rc = 3;
+                continue;
+            }
+            /* one forward step: from state Hp to Hn at token row, also p and delta */
+#define STEP(Hp, Hn, row, alpha, bt)                                                   \
+    do {                                                                               \
+        for (int i = 0; i < dk; i++) kt[i] = widen(k, in_dtype, (row) * dk + i);       \
+        for (int j = 0; j < dv; j++) {                                                 \
+            double acc = 0.0;                                                          \
+            for (int i = 0; i < dk; i++) acc += (Hp)[i * dv + j] * kt[i];              \
+            p[j] = (alpha) * acc;                                                      \
+            dl[j] = (bt) * (widen(v, in_dtype, (row) * dv + j) - p[j]);                \
+        }                                                                              \
+        for (int i = 0; i < dk; i++)                                                   \
+            for (int j = 0; j < dv; j++)                                               \
+                (Hn)[i * dv + j] = (alpha) * (Hp)[i * dv + j] + kt[i] * dl[j];         \
+    } while (0)
+            /* forward: checkpoints at tokens 0, CK, 2 CK, ... of the sequence */
+            double *Hc = blk, *Hn = blk + S;
+            for (int64_t e = 0; e < S; e++) Hc[e] = h0 ? h0[u * S + e] : 0.0;
+            memcpy(ck, Hc, sizeof(double) * (size_t)S);
+            for (int64_t t = 0; t < len; t++) {
+                const int64_t row = (t_begin + t) * H + h;
+                const double alpha = exp(gdr_oracle_gate(widen(a, in_dtype, row), b, gate));
+                const double bt = widen(beta, in_dtype, row);
+                STEP(Hc, Hn, row, alpha, bt);
+                double *tmp = Hc;
+                Hc = Hn;
+                Hn = tmp;
+                if ((t + 1) % CK == 0) memcpy(ck + ((t + 1) / CK) * S, Hc, sizeof(double) * (size_t)S);
+            }
+            /* backward */
+            for (int64_t e = 0; e < S; e++) dH[e] = dhT ? dhT[u * S + e] : 0.0;
+            for (int64_t c0 = ((len - 1) / CK) * CK; len > 0 && c0 >= 0; c0 -= CK) {
+                const int64_t c1 = (c0 + CK < len) ? c0 + CK : len;
+                /* states H_{c0} .. H_{c1} of this block */
+                memcpy(blk, ck + (c0 / CK) * S, sizeof(double) * (size_t)S);
+                for (int64_t t = c0; t < c1; t++) {
+                    const int64_t row = (t_begin + t) * H + h;
+                    const double alpha = exp(gdr_oracle_gate(widen(a, in_dtype, row), b, gate));
+                    const double bt = widen(beta, in_dtype, row);
+                    STEP(blk + (t - c0) * S, blk + (t - c0 + 1) * S, row, alpha, bt);
+                }
+                for (int64_t t = c1 - 1; t >= c0; t--) {
+                    const int64_t row = (t_begin + t) * H + h;
+                    const double av = widen(a, in_dtype, row);
+                    const double alpha = exp(gdr_oracle_gate(av, b, gate));
+                    const double bt = widen(beta, in_dtype, row);
+                    const double *Hp = blk + (t - c0) * S;     /* H_{t-1} */
+                    const double *Ht = blk + (t - c0 + 1) * S; /* H_t */
+                    for (int i = 0; i < dk; i++) {
+                        kt[i] = widen(k, in_dtype, row * dk + i);
+                        qt[i] = widen(q, in_dtype, row * dk + i);
+                    }
+                    /* p and delta of this token */
+                    for (int j = 0; j < dv; j++) {
+                        double acc = 0.0;
+                        for (int i = 0; i < dk; i++) acc += Hp[i * dv + j] * kt[i];
+                        p[j] = alpha * acc;
+                        dl[j] = bt * (widen(v, in_dtype, row * dv + j) - p[j]);
+                    }
+                    /* o = H_t^T q */
+                    for (int i = 0; i < dk; i++) {
+                        double acc = 0.0;
+                        for (int j = 0; j < dv; j++) {
+                            const double g_o = dout ? dout[row * dv + j] : 0.0;
+                            dH[i * dv + j] += qt[i] * g_o;
+                            acc += Ht[i * dv + j] * g_o;
+                        }
+                        dq[row * dk + i] = acc;
+                    }
+                    /* H_t = Hb + k delta^T */
+                    double dbt = 0.0;
+                    for (int j = 0; j < dv; j++) {
+                        double acc = 0.0;
+                        for (int i = 0; i < dk; i++) acc += dH[i * dv + j] * kt[i];
+                        ddl[j] = acc;
+                        dv_out[row * dv + j] = bt * acc;
+                        dbt += acc * (widen(v, in_dtype, row * dv + j) - p[j]);
+                        dp[j] = -bt * acc;
+                    }
+                    dbeta[row] = dbt;
+                    double dalpha = 0.0;
+                    for (int i = 0; i < dk; i++) {
+                        double g_k = 0.0;
+                        for (int j = 0; j < dv; j++) {
+                            g_k += dH[i * dv + j] * dl[j];                   /* from k delta^T */
+                            g_k += alpha * Hp[i * dv + j] * dp[j];           /* from p = Hb^T k */
+                            const double dhb = dH[i * dv + j] + kt[i] * dp[j];
+                            dalpha += Hp[i * dv + j] * dhb;
+                            dH[i * dv + j] = alpha * dhb;
+                        }
+                        dk_out[row * dk + i] = g_k;
+                    }
+                    da[row] = dalpha * alpha * gate_grad(av, b, gate);
+                }
+            }
+#undef STEP
+            for (int64_t e = 0; e < S; e++)
+                if (dh0) dh0[u * S + e] = dH[e];
+            free(ck);
+        }
+        free(blk);
+        free(dH);
+        free(kt);
+        free(qt);
+        free(p);
+        free(dl);
+        free(ddl);
+        free(dp);
+    }
+    return rc;
+}
+
 /* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
 int gdr_oracle_max_threads(void)
 {
