@@ -230,10 +230,13 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the tokens per sequence (or total, varlen) of the workload")
-    ap.add_argument("--mode", default="prefill", choices=["prefill", "decode"],
+    ap.add_argument("--mode", default="prefill", choices=["prefill", "decode", "backward"],
                     help="prefill: the chunked forward (the headline); decode: one recurrent "
-                         "step of --decode-seqs sequences")
+                         "step of --decode-seqs sequences; backward: gdr_chunk_bwd on "
+                         "--bwd-seqs sequences of --bwd-tokens tokens")
     ap.add_argument("--decode-seqs", type=int, default=256)
+    ap.add_argument("--bwd-seqs", type=int, default=8)
+    ap.add_argument("--bwd-tokens", type=int, default=4096)
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     return args
@@ -251,6 +254,9 @@ def main(argv=None):
         return
     if args.mode == "decode":
         bench_decode(args)
+        return
+    if args.mode == "backward":
+        bench_backward(args)
         return
 
     import torch
@@ -421,6 +427,75 @@ def bench_decode(args):
                      "frac": achieved / hbm, "traffic": None, "kernel": "recurrent_kernel",
                      "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_step": byt},
         "gpu_launches": n_launch, "clocks": clk.summary(),
+    }), flush=True)
+
+
+def bench_backward(args):
+    """The backward pass (gdr_chunk_bwd) of N sequences x 16 heads x T tokens, d = 128,
+    bf16, with h0, dout and dhT given.  It runs in fp32 on the SIMT pipes; its
+    algorithmic work is 20 dk dv flops per (token, head): the forward recomputed
+    (p and the state update) and the adjoint recurrence (dH, dq, ddelta, dk, dHb,
+    dalpha and the decay of dH)."""
+    import torch
+    import chunked_gated_delta_07_gb300 as gdr
+    from gdr_inputs import WORKLOADS, make_inputs
+    N, T, H, d = args.bwd_seqs, args.bwd_tokens, 16, 128
+    x = make_inputs(WORKLOADS["t1m"].with_(B=N, h0_std=0.02, seed=4500), device="cuda", T=T)
+    g = torch.Generator(device="cuda").manual_seed(4501)
+    dout = torch.randn(x["v"].shape, generator=g, device="cuda").to(torch.bfloat16)
+    dhT = 0.1 * torch.randn((N, H, d, d), generator=g, device="cuda")
+    outs = [torch.empty_like(x[n]) for n in ("q", "k", "v", "a", "beta")]
+    dh0 = torch.empty_like(dhT)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        rc = gdr.gdr_chunk_bwd(x["q"], x["k"], x["v"], x["a"], x["beta"], x["h0"], dout, dhT,
+                               *outs, dh0, None, N, T, H, d, d, 16, 2.0, gdr.GDR_BF16,
+                               gdr.GDR_GATE_BOUNDED, stream)
+        if rc != gdr.GDR_OK:
+            raise gdr.GdrError(rc, "gdr_chunk_bwd")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    steps = max(args.steps, 3)
+    gdr.gdr_profile_read()
+    gdr.gdr_profile_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        n0 = gdr.gdr_launch_count()
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        n_launch = gdr.gdr_launch_count() - n0
+    gdr.gdr_profile_enable(False)
+    prof = gdr.gdr_profile_read()
+    st = gdr.gdr_get_status(stream)
+    if st != gdr.GDR_OK:
+        raise gdr.GdrError(st, "device status after backward")
+    ms = ev0.elapsed_time(ev1) / steps
+    dom_ms, dom_n = prof.get("bwd_slice_kernel", (0.0, 1))
+    kern_ms = dom_ms / max(dom_n, 1)
+    flops = 20.0 * d * d * N * T * H
+    summ = clk.summary() or {}
+    mhz = float(summ.get("sm_max_mhz") or 2070.0)
+    peak = 152 * 128 * 2 * mhz * 1e6 / 1e12   # fp32 FMA lanes x 2 flops x max SM clock
+    achieved = flops / (kern_ms / 1e3) / 1e12 if kern_ms > 0 else 0.0
+    print(json.dumps({
+        "metric": "backward tokens/s, gated delta rule, 16 heads, d=128, bf16 in/out, fp32 math",
+        "value": N * T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"backward: N={N} sequences x T={T} x H={H}, dk=dv={d}",
+                   "l2_policy": "no flush; the per-step inputs and scratch exceed L2"},
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None, "kernel": "bwd_slice_kernel",
+                     "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x max SM clock",
+                     "algorithmic_flops_per_step": flops, "kernel_ms": kern_ms},
+        "kernels": {k: {"ms_total": v[0], "launches": v[1]} for k, v in prof.items()},
+        "gpu_launches": n_launch, "clocks": summ or None,
     }), flush=True)
 
 

@@ -28,7 +28,7 @@ GDR_PATH_AUTO, GDR_PATH_SIMT, GDR_PATH_TC = 0, 1, 2
 EXPORTS = ("gdr_chunk_fwd", "gdr_chunk_fwd_ex", "gdr_chunk_fwd_workspace_size",
            "gdr_chunk_fwd_host", "gdr_gate_cumsum", "gdr_wy_repr", "gdr_get_status",
            "gdr_status_string", "gdr_release", "gdr_launch_count", "gdr_profile_enable",
-           "gdr_profile_read", "gdr_chunk_fwd_noalloc", "gdr_recurrent_fwd")
+           "gdr_profile_read", "gdr_chunk_fwd_noalloc", "gdr_recurrent_fwd", "gdr_chunk_bwd")
 
 _lock = threading.Lock()
 _lib = None
@@ -49,6 +49,7 @@ _SIGS = {
     "gdr_profile_read": (_I, [_P, _P, _P, _I]),
     "gdr_chunk_fwd_noalloc": (_I, [_P] * 8 + [_I, _I64, _I, _I, _I, _I, _F, _I, _I, _P]),
     "gdr_recurrent_fwd": (_I, [_P] * 7 + [_I, _I64, _I, _I, _I, _F, _I, _I, _P]),
+    "gdr_chunk_bwd": (_I, [_P] * 15 + [_I, _I64, _I, _I, _I, _I, _F, _I, _I, _P]),
 }
 
 
@@ -149,6 +150,33 @@ def recurrent_fwd(q, k, v, a, beta, state, b=2.0, gate="bounded", out=None, stre
     if rc != GDR_OK:
         raise GdrError(rc, "gdr_recurrent_fwd")
     return out
+
+
+def gdr_chunk_bwd(q, k, v, a, beta, h0, dout, dhT, dq, dk, dv, da, dbeta, dh0, cu_seqlens, B, T,
+                  H, dk_dim, dv_dim, chunk, b, dtype, gate, stream=None) -> int:
+    """Backward pass: gradients of <dout, out> + <dhT, hT> for every input."""
+    return lib().gdr_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(beta), _ptr(h0),
+                               _ptr(dout), _ptr(dhT), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(da),
+                               _ptr(dbeta), _ptr(dh0), _ptr(cu_seqlens), B, T, H, dk_dim, dv_dim,
+                               chunk, float(b), dtype, gate, _stream(stream))
+
+
+def chunk_bwd(q, k, v, a, beta, dout=None, dhT=None, h0=None, cu_seqlens=None, chunk=16, b=2.0,
+              gate="bounded", want_dh0=True, stream=None):
+    """Allocate and return (dq, dk, dv, da, dbeta, dh0) for tensors laid out as in chunk_fwd."""
+    import torch
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    dq, dkk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    da, dbeta = torch.empty_like(a), torch.empty_like(beta)
+    dh0 = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device) if want_dh0 else None
+    rc = gdr_chunk_bwd(q, k, v, a, beta, h0, dout, dhT, dq, dkk, dvv, da, dbeta, dh0, cu_seqlens,
+                       N if cu_seqlens is not None else B, T, H, dk, dv, chunk, b, dtype_code(q),
+                       _GATES[gate], stream)
+    if rc != GDR_OK:
+        raise GdrError(rc, "gdr_chunk_bwd")
+    return dq, dkk, dvv, da, dbeta, dh0
 
 
 def gdr_gate_cumsum(a, G, cu_seqlens, B, T, H, chunk, b, dtype, gate, stream=None) -> int:

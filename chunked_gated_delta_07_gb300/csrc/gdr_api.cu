@@ -583,6 +583,60 @@ gdr_status_t gdr_recurrent_fwd(const void *q, const void *k, const void *v, cons
                : GDR_ERR_CUDA;
 }
 
+gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const void *a,
+                           const void *beta, const float *h0, const void *dout,
+                           const float *dhT, void *dq, void *dk_out, void *dv_out, void *da,
+                           void *dbeta, float *dh0, const int32_t *cu_seqlens, int B,
+                           int64_t T, int H, int dk, int dv, int chunk, float b,
+                           gdr_dtype_t dtype, gdr_gate_t gate, gdr_stream_t stream_) {
+    Shape s;
+    // the forward's checks (with dq standing in for out in the aliasing tests)
+    gdr_status_t st = check_args(q, k, v, a, beta, h0, dq, nullptr, cu_seqlens, B, T, H, dk, dv,
+                                 chunk, b, dtype, gate, GDR_PATH_SIMT, &s);
+    if (st != GDR_OK) return st;
+    if (s.T_total > 0 && (!dq || !dk_out || !dv_out || !da || !dbeta)) return GDR_ERR_INVALID_ARG;
+    const size_t es = dtype == GDR_BF16 ? 2 : 4;
+    const size_t rows = (size_t)s.T_total * H;
+    const void *ins[6] = {q, k, v, a, beta, dout};
+    const size_t in_b[6] = {rows * dk * es, rows * dk * es, rows * dv * es, rows * es, rows * es,
+                            rows * dv * es};
+    void *outs[5] = {dq, dk_out, dv_out, da, dbeta};
+    const size_t out_b[5] = {rows * dk * es, rows * dk * es, rows * dv * es, rows * es, rows * es};
+    for (int i = 0; i < 5; ++i)
+        for (int j = 0; j < 6; ++j)
+            if (overlaps(outs[i], out_b[i], ins[j], in_b[j])) return GDR_ERR_INVALID_ARG;
+    const size_t nst = (size_t)B * H * dk * dv * sizeof(float);
+    if (dh0 && (overlaps(dh0, nst, h0, nst) || overlaps(dh0, nst, dhT, nst))) return GDR_ERR_INVALID_ARG;
+    if (s.T_total == 0) {   // no tokens: dh0 = dhT
+        if (!dh0) return GDR_OK;
+        cudaStream_t stream = (cudaStream_t)stream_;
+        const cudaError_t e = dhT ? cudaMemcpyAsync(dh0, dhT, nst, cudaMemcpyDeviceToDevice, stream)
+                                  : cudaMemsetAsync(dh0, 0, nst, stream);
+        return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+    }
+    DeviceCtx *ctx = device_ctx();
+    if (!ctx) return GDR_ERR_CUDA;
+    const int64_t tiles = tile_bound(s.varlen, B, s.varlen ? T : s.T_per, kBwTile);
+    const size_t plan_b = align_up(3 * sizeof(int64_t) * (size_t)(B + 1));
+    const size_t need = plan_b + bwd_scratch_bytes(tiles, s.T_total, H, dk, dv);
+    char *ws;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!grow(&ctx->ws, &ctx->ws_bytes, need)) return GDR_ERR_CUDA;
+        ws = (char *)ctx->ws;
+    }
+    cudaStream_t stream = (cudaStream_t)stream_;
+    int64_t *seq_start = (int64_t *)ws;
+    Plan plan{B, kBwTile, 1 << 30, seq_start, seq_start + (B + 1), seq_start + 2 * (B + 1)};
+    if (launch_plan(cu_seqlens, B, s.T_per, s.T_total, kBwTile, 1 << 30, seq_start, seq_start + (B + 1),
+                    seq_start + 2 * (B + 1), ctx->d_status, stream) != cudaSuccess)
+        return GDR_ERR_CUDA;
+    return launch_bwd(q, k, v, a, beta, h0, dout, dhT, dq, dk_out, dv_out, da, dbeta, dh0, dtype,
+                      plan, H, dk, dv, s.T_total, tiles, b, gate, ws + plan_b, stream) == cudaSuccess
+               ? GDR_OK
+               : GDR_ERR_CUDA;
+}
+
 gdr_status_t gdr_gate_cumsum(const void *a, float *G, const int32_t *cu_seqlens, int B,
                              int64_t T, int H, int chunk, float b, gdr_dtype_t dtype,
                              gdr_gate_t gate, gdr_stream_t stream) {

@@ -92,6 +92,16 @@ cudaError_t launch_wy_simt(const void *k, const void *v, const void *beta, const
                            int dv, int64_t T_total, int64_t max_chunks, cudaStream_t stream);
 
 // Stages 3+4 on CUDA cores: the tile-to-tile state pass and the outputs.
+// The backward pass (gdr_backward.cu).  The plan must be built with 16-token
+// tiles (the checkpoint interval); scratch holds bwd_scratch_bytes(...) bytes.
+constexpr int kBwTile = 16;
+size_t bwd_scratch_bytes(int64_t tiles, int64_t T_total, int H, int dk, int dv);
+cudaError_t launch_bwd(const void *q, const void *k, const void *v, const void *a, const void *beta,
+                       const float *h0, const void *dout, const float *dhT, void *dq, void *dk_,
+                       void *dv, void *da, void *dbeta, float *dh0, gdr_dtype_t dtype, Plan plan,
+                       int H, int dk, int dv_dim, int64_t T_total, int64_t tiles, float b,
+                       gdr_gate_t gate, void *scratch, cudaStream_t stream);
+
 // The recurrent form over T tokens per sequence, the fp32 state updated in place.
 cudaError_t launch_recurrent(const void *q, const void *k, const void *v, const void *a,
                              const void *beta, float *state, void *out, gdr_dtype_t dtype, int N,

@@ -229,6 +229,30 @@ GDR_API gdr_status_t gdr_recurrent_fwd(const void *q, const void *k, const void 
                                int H, int dk, int dv, float b, gdr_dtype_t dtype,
                                gdr_gate_t gate, gdr_stream_t stream);
 
+/*
+ * The backward pass: gradients of  L = <dout, out> + <dhT, hT>  with respect to
+ * q, k, v, a, beta and h0, for the forward of gdr_chunk_fwd_ex on the same
+ * inputs (same layouts, dtype, gate, b and cu_seqlens; B is N for varlen).
+ * The pages train the layer in bf16 mixed precision ("Core Technologies ...",
+ * §2.3; "Deep Dive ...", §3.3) but print no backward; the adjoints here are
+ * those of the recurrence H_t = alpha H_{t-1} + beta k (v - alpha H^T k)^T,
+ * o = H_t^T q, written out per token:
+ *   dout [tokens, H, dv] (dtype) or NULL (zero);  dhT [N, H, dk, dv] fp32 or NULL
+ *   dq, dk [tokens, H, dk], dv [tokens, H, dv], da, dbeta [tokens, H]  (dtype, all
+ *   written);  dh0 [N, H, dk, dv] fp32 (written when not NULL)
+ * `chunk` is validated like the forward's; the pass keeps checkpoints of the
+ * state every 16 tokens and recomputes between them.  Device pointers owned
+ * by the caller; scratch comes from the internal per-device cache.  Outputs
+ * must not alias inputs.  The result is deterministic (no atomics).  Errors as
+ * for gdr_chunk_fwd_ex; asynchronous on `stream`.
+ */
+GDR_API gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const void *a,
+                           const void *beta, const float *h0, const void *dout,
+                           const float *dhT, void *dq, void *dk_out, void *dv_out, void *da,
+                           void *dbeta, float *dh0, const int32_t *cu_seqlens, int B,
+                           int64_t T, int H, int dk, int dv, int chunk, float b,
+                           gdr_dtype_t dtype, gdr_gate_t gate, gdr_stream_t stream);
+
 /* Synchronise `stream`, then read and clear the current device's status word.
  * Returns GDR_OK, GDR_ERR_BAD_SEQLENS, GDR_ERR_TIMEOUT or GDR_ERR_CUDA. */
 GDR_API gdr_status_t gdr_get_status(gdr_stream_t stream);
