@@ -5,11 +5,15 @@ binding) never imports this package; only the tests, the smoke check and the
 benchmark's CPU-baseline leg do.  The oracle shares no code with the CUDA
 path.
 
-Two independent references live here:
+Independent references live here:
 
 * ``oracle_fwd`` -- the token-by-token recurrence in fp64, written in plain C
   (``gdr_oracle.c``, OpenMP over (sequence, head, column block)).  This is the
   definition the chunked GPU method must reproduce.
+* ``oracle_fwd_vec`` -- the same recurrence with one decay factor per key
+  channel (a is [B,T,H,dk]), pinned by its reduction to ``oracle_fwd`` when all
+  channels agree, by the closed form of the per-channel linear-attention sum
+  without the erase term, and by exact special cases.
 * ``oracle_bwd`` -- the gradients of <dout, out> + <dhT, hT> with respect to
   every input, by the token-by-token adjoint recurrence in fp64 (the same C
   file), pinned by finite differences of ``oracle_fwd``.
@@ -59,6 +63,13 @@ def _bind(path):
     lib = ctypes.CDLL(path)
     lib.gdr_oracle_fwd.restype = ctypes.c_int
     lib.gdr_oracle_fwd.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    lib.gdr_oracle_fwd_vec.restype = ctypes.c_int
+    lib.gdr_oracle_fwd_vec.argtypes = [
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
         ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
@@ -179,6 +190,20 @@ def oracle_fwd(q, k, v, a, beta, h0=None, cu_seqlens=None, b: float = 2.0,
     with cu_seqlens (N+1 offsets) B must be 1 and the N sequences are packed
     along T.  h0 is [N,H,dk,dv] (None means zero).  ``_lib_path`` loads another
     build of the C source (the mutation tests use it)."""
+    return _fwd("gdr_oracle_fwd", q, k, v, a, beta, h0, cu_seqlens, b, gate, erase, nthreads,
+                _lib_path)
+
+
+def oracle_fwd_vec(q, k, v, a, beta, h0=None, cu_seqlens=None, b: float = 2.0,
+                   gate: str = "bounded", erase: bool = True, nthreads: int = 0,
+                   _lib_path: str | None = None):
+    """The per-channel decay form: as ``oracle_fwd`` but a is [B,T,H,dk], one gate
+    input per key channel, and row i of the state decays by exp(g(a[..., i]))."""
+    return _fwd("gdr_oracle_fwd_vec", q, k, v, a, beta, h0, cu_seqlens, b, gate, erase,
+                nthreads, _lib_path)
+
+
+def _fwd(fn, q, k, v, a, beta, h0, cu_seqlens, b, gate, erase, nthreads, _lib_path):
     lib = _load() if _lib_path is None else _bind(_lib_path)
     arrs = [_as_array(x) for x in (q, k, v, a, beta)]
     if len({d for _, d in arrs}) != 1:
@@ -187,6 +212,8 @@ def oracle_fwd(q, k, v, a, beta, h0=None, cu_seqlens=None, b: float = 2.0,
     (qa, dt), (ka, _), (va, _), (aa, _), (ba, _) = arrs
     B, T, H, dk = qa.shape
     dv = va.shape[-1]
+    want_a = (B, T, H, dk) if fn == "gdr_oracle_fwd_vec" else (B, T, H)
+    assert aa.shape == want_a, (aa.shape, want_a)
     if cu_seqlens is not None:
         cu = np.ascontiguousarray(np.asarray(
             cu_seqlens.cpu().numpy() if hasattr(cu_seqlens, "cpu") else cu_seqlens,
@@ -203,13 +230,13 @@ def oracle_fwd(q, k, v, a, beta, h0=None, cu_seqlens=None, b: float = 2.0,
         h0a, h0d = _as_array(h0)
         h0a = np.ascontiguousarray(_widen_np(h0a, h0d))
         assert h0a.shape == (N, H, dk, dv)
-    rc = lib.gdr_oracle_fwd(
+    rc = getattr(lib, fn)(
         qa.ctypes.data, ka.ctypes.data, va.ctypes.data, aa.ctypes.data, ba.ctypes.data,
         dt, None if h0a is None else h0a.ctypes.data, out.ctypes.data, hT.ctypes.data,
         None if cu is None else cu.ctypes.data, N, T, H, dk, dv, float(b), GATES[gate],
         1 if erase else 0, int(nthreads))
     if rc != 0:
-        raise ValueError(f"gdr_oracle_fwd rejected its arguments (code {rc})")
+        raise ValueError(f"{fn} rejected its arguments (code {rc})")
     return out, hT
 
 

@@ -179,6 +179,97 @@ int gdr_oracle_fwd(const void *q, const void *k, const void *v, const void *a,
     return 0;
 }
 
+/*
+ * Per-channel (vector) decay: a carries one gate input per key channel, a is
+ * [rows, dk], and token t decays row i of H by its own factor
+ * alpha_{t,i} = exp(g(a_{t,i})) [P1 §2.1-2.2 and P4 §3 give the decay as the
+ * data-dependent factor whose log is bounded; a decay per key channel is the
+ * plainest reading of a vector-valued log-decay g_t]:
+ *
+ *   Hb  = diag(alpha_t) H_{t-1}
+ *   H_t = Hb + beta_t k_t (v_t - Hb^T k_t)^T = (I - beta_t k_t k_t^T) Hb + beta_t k_t v_t^T
+ *   o_t = H_t^T q_t
+ *
+ * With every channel given the same a this is gdr_oracle_fwd exactly.
+ */
+int gdr_oracle_fwd_vec(const void *q, const void *k, const void *v, const void *a,
+                       const void *beta, int in_dtype, const double *h0, double *out,
+                       double *hT, const int64_t *cu_seqlens, int B, int64_t T, int H,
+                       int dk, int dv, double b, int gate, int erase, int nthreads)
+{
+    if (B < 1 || T < 0 || H < 1 || dk < 1 || dv < 1) return 1;
+    if (in_dtype < OR_BF16 || in_dtype > OR_F64) return 1;
+    int N = B;
+    if (cu_seqlens) {
+        if (cu_seqlens[0] != 0) return 2;
+        for (int n = 0; n < N; n++)
+            if (cu_seqlens[n + 1] < cu_seqlens[n]) return 2;
+        if (cu_seqlens[N] != T) return 2;
+    }
+    const int CB = 16;
+    const int ncb = (dv + CB - 1) / CB;
+    const int64_t ntask = (int64_t)N * H * ncb;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+
+#pragma omp parallel
+    {
+        double *Hs = (double *)malloc(sizeof(double) * (size_t)dk * CB);
+        double *kt = (double *)malloc(sizeof(double) * (size_t)dk);
+        double *qt = (double *)malloc(sizeof(double) * (size_t)dk);
+        double *al = (double *)malloc(sizeof(double) * (size_t)dk);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t task = 0; task < ntask; task++) {
+            const int cb = (int)(task % ncb);
+            const int h = (int)((task / ncb) % H);
+            const int n = (int)(task / ((int64_t)ncb * H));
+            const int j0 = cb * CB;
+            const int nc = (dv - j0) < CB ? (dv - j0) : CB;
+            const int64_t t_begin = cu_seqlens ? cu_seqlens[n] : (int64_t)n * T;
+            const int64_t t_end = cu_seqlens ? cu_seqlens[n + 1] : t_begin + T;
+            for (int i = 0; i < dk; i++)
+                for (int c = 0; c < nc; c++)
+                    Hs[i * CB + c] = h0 ? h0[((int64_t)(n * H + h) * dk + i) * dv + j0 + c] : 0.0;
+            for (int64_t t = t_begin; t < t_end; t++) {
+                const int64_t row = t * H + h;
+                const double bt = widen(beta, in_dtype, row);
+                for (int i = 0; i < dk; i++) {
+                    al[i] = exp(gdr_oracle_gate(widen(a, in_dtype, row * dk + i), b, gate));
+                    kt[i] = widen(k, in_dtype, row * dk + i);
+                    qt[i] = widen(q, in_dtype, row * dk + i);
+                }
+                for (int c = 0; c < nc; c++) {
+                    /* decay each row by its channel's factor, then predict v */
+                    double p = 0.0;
+                    for (int i = 0; i < dk; i++) {
+                        Hs[i * CB + c] *= al[i];
+                        p += kt[i] * Hs[i * CB + c];
+                    }
+                    const double delta = bt * (widen(v, in_dtype, row * dv + j0 + c) - (erase ? p : 0.0));
+                    double o = 0.0;
+                    for (int i = 0; i < dk; i++) {
+                        Hs[i * CB + c] += kt[i] * delta;
+                        o += Hs[i * CB + c] * qt[i];
+                    }
+                    out[row * dv + j0 + c] = o;
+                }
+            }
+            if (hT)
+                for (int i = 0; i < dk; i++)
+                    for (int c = 0; c < nc; c++)
+                        hT[(((int64_t)n * H + h) * dk + i) * dv + j0 + c] = Hs[i * CB + c];
+        }
+        free(Hs);
+        free(kt);
+        free(qt);
+        free(al);
+    }
+    return 0;
+}
+
 /* d g / d a of the log-decay, for the backward pass. */
 static double gate_grad(double a, double b, int gate)
 {

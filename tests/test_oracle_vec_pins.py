@@ -1,0 +1,155 @@
+"""Pins of the per-channel decay oracle (``oracle_fwd_vec``), CPU only.
+
+The per-channel form gives every key channel i its own decay factor
+alpha_{t,i} = exp(g(a_{t,i})) and applies it to row i of the dk x dv state
+before the delta-rule write:  H_t = (I - beta_t k_t k_t^T) diag(alpha_t) H_{t-1}
++ beta_t k_t v_t^T,  o_t = H_t^T q_t.  The pins check it against:
+  - the scalar oracle (itself pinned elsewhere) when all channels share a;
+  - a brute-force expansion in dense dk x dk transition matrices;
+  - the closed form of per-channel gated linear attention when the erase term
+    is dropped;
+  - beta = 0 (pure per-channel decay) and one-hot keys (only that row is
+    rewritten, every other row only decays).
+Planted one-token mistakes in copies of the C source must fail the battery.
+"""
+import math
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from test_oracle_pins import _case, _g
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "gdr_oracle.c")
+
+
+def _vec_case(rng, T, H=1, dk=6, dv=5, B=1, a_std=1.0):
+    q, k, v, _, beta, h0 = _case(rng, T, H=H, dk=dk, dv=dv, B=B)
+    a = a_std * rng.standard_normal((B, T, H, dk))
+    return q, k, v, a, beta, h0
+
+
+def _brute_force_vec(q, k, v, g, beta, h0):
+    """Dense transitions Phi_t = (I - beta k k^T) diag(exp(g_t)); H_t expanded as
+    Phi_{1:t} h0 + sum_s Phi_{s+1:t} beta_s k_s v_s^T."""
+    T, dk = k.shape
+    Phi = [(np.eye(dk) - beta[t] * np.outer(k[t], k[t])) @ np.diag(np.exp(g[t])) for t in range(T)]
+    out = np.zeros((T, v.shape[1]))
+    Ht = h0
+    for t in range(T):
+        P = np.eye(dk)
+        for r in range(t, -1, -1):
+            P = P @ Phi[r]
+        Ht = P @ h0
+        for s in range(t + 1):
+            Ps = np.eye(dk)
+            for r in range(t, s, -1):
+                Ps = Ps @ Phi[r]
+            Ht = Ht + Ps @ (beta[s] * np.outer(k[s], v[s]))
+        out[t] = Ht.T @ q[t]
+    return out, Ht
+
+
+def test_equal_channels_reduce_to_scalar_oracle():
+    rng = np.random.default_rng(21)
+    q, k, v, _, beta, h0 = _case(rng, 50, H=2, dk=8, dv=6, B=2)
+    a = rng.standard_normal((2, 50, 2))
+    av = np.repeat(a[..., None], 8, axis=-1)
+    for gate, b in (("bounded", 2.0), ("softplus", 0.0)):
+        o1, h1 = oracle.oracle_fwd(q, k, v, a, beta, h0=h0, b=b, gate=gate)
+        o2, h2 = oracle.oracle_fwd_vec(q, k, v, av, beta, h0=h0, b=b, gate=gate)
+        np.testing.assert_allclose(o2, o1, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(h2, h1, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("T,dk,dv,b", [(1, 4, 3, 2.0), (9, 6, 5, 2.0), (24, 8, 4, 5.0)])
+def test_matches_dense_transition_products(T, dk, dv, b):
+    rng = np.random.default_rng(30 + T)
+    q, k, v, a, beta, h0 = _vec_case(rng, T, dk=dk, dv=dv)
+    out, hT = oracle.oracle_fwd_vec(q, k, v, a, beta, h0=h0, b=b)
+    g = _g(a[0, :, 0], b)
+    ro, rh = _brute_force_vec(q[0, :, 0], k[0, :, 0], v[0, :, 0], g, beta[0, :, 0], h0[0, 0])
+    np.testing.assert_allclose(out[0, :, 0], ro, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(hT[0, 0], rh, rtol=1e-11, atol=1e-12)
+
+
+def test_no_erase_is_per_channel_gated_linear_attention():
+    """Without the erase term: o_t = sum_{s<=t} beta_s sum_i q_ti k_si
+    exp(G_ti - G_si) v_s + sum_i q_ti exp(G_ti) h0[i], G the per-channel cumsum."""
+    rng = np.random.default_rng(22)
+    T, dk, dv = 20, 6, 4
+    q, k, v, a, beta, h0 = _vec_case(rng, T, dk=dk, dv=dv)
+    out, _ = oracle.oracle_fwd_vec(q, k, v, a, beta, h0=h0, b=2.0, erase=False)
+    G = np.cumsum(_g(a[0, :, 0], 2.0), axis=0)
+    qq, kk, vv, bb = q[0, :, 0], k[0, :, 0], v[0, :, 0], beta[0, :, 0]
+    ref = np.zeros((T, dv))
+    for t in range(T):
+        acc = (qq[t] * np.exp(G[t])) @ h0[0, 0]
+        for s in range(t + 1):
+            acc = acc + bb[s] * float(np.sum(qq[t] * kk[s] * np.exp(G[t] - G[s]))) * vv[s]
+        ref[t] = acc
+    np.testing.assert_allclose(out[0, :, 0], ref, rtol=1e-11, atol=1e-13)
+
+
+def test_beta_zero_is_per_channel_decay():
+    rng = np.random.default_rng(23)
+    q, k, v, a, beta, h0 = _vec_case(rng, 30, H=2, dk=5, dv=4, B=2)
+    beta[:] = 0.0
+    out, hT = oracle.oracle_fwd_vec(q, k, v, a, beta, h0=h0, b=2.0)
+    for n in range(2):
+        for h in range(2):
+            G = np.cumsum(_g(a[n, :, h], 2.0), axis=0)       # [T, dk]
+            ref = np.stack([(q[n, t, h] * np.exp(G[t])) @ h0[n, h] for t in range(30)])
+            np.testing.assert_allclose(out[n, :, h], ref, rtol=1e-12, atol=1e-14)
+            np.testing.assert_allclose(hT[n, h], np.exp(G[-1])[:, None] * h0[n, h], rtol=1e-12)
+
+
+def test_one_hot_key_rewrites_only_its_row():
+    """k = e_r, beta = 1: row r of H becomes v_t, every other row i only decays
+    by exp(g_{t,i})."""
+    rng = np.random.default_rng(24)
+    T, dk, dv = 6, 5, 3
+    q, k, v, a, beta, h0 = _vec_case(rng, T, dk=dk, dv=dv)
+    beta[:] = 1.0
+    rows = [2, 0, 4, 2, 1, 3]
+    k[:] = 0.0
+    for t, r in enumerate(rows):
+        k[0, t, 0, r] = 1.0
+    _, hT = oracle.oracle_fwd_vec(q, k, v, a, beta, h0=h0, b=2.0)
+    g = _g(a[0, :, 0], 2.0)
+    H = h0[0, 0].copy()
+    for t, r in enumerate(rows):
+        H = np.exp(g[t])[:, None] * H
+        H[r] = v[0, t, 0]
+    np.testing.assert_allclose(hT[0, 0], H, rtol=1e-13, atol=1e-15)
+
+
+# one-token edits of the per-channel forward in gdr_oracle.c
+VEC_MUTANTS = {
+    "decay_after_prediction": ("Hs[i * CB + c] *= al[i];\n                        p += kt[i] * Hs[i * CB + c];",
+                               "p += kt[i] * Hs[i * CB + c];\n                        Hs[i * CB + c] *= al[i];"),
+    "one_factor_for_all_rows": ("Hs[i * CB + c] *= al[i];", "Hs[i * CB + c] *= al[0];"),
+    "gate_reads_channel_zero": ("widen(a, in_dtype, row * dk + i)", "widen(a, in_dtype, row * dk)"),
+    "erase_dropped": ("(erase ? p : 0.0)", "0.0"),
+}
+
+
+@pytest.mark.parametrize("name", list(VEC_MUTANTS))
+def test_vec_mutant_is_rejected(tmp_path, name):
+    old, new = VEC_MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, name
+    c, so = tmp_path / f"{name}.c", tmp_path / f"{name}.so"
+    c.write_text(src.replace(old, new))
+    subprocess.run(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-o", str(so), str(c),
+                    "-lm"], check=True)
+    rng = np.random.default_rng(31)
+    q, k, v, a, beta, h0 = _vec_case(rng, 9, dk=6, dv=5)
+    out, hT = oracle.oracle_fwd_vec(q, k, v, a, beta, h0=h0, b=2.0, _lib_path=str(so))
+    g = _g(a[0, :, 0], 2.0)
+    ro, rh = _brute_force_vec(q[0, :, 0], k[0, :, 0], v[0, :, 0], g, beta[0, :, 0], h0[0, 0])
+    ok = np.allclose(out[0, :, 0], ro, rtol=1e-11, atol=1e-12) and \
+        np.allclose(hT[0, 0], rh, rtol=1e-11, atol=1e-12)
+    assert not ok
