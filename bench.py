@@ -230,10 +230,11 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the tokens per sequence (or total, varlen) of the workload")
-    ap.add_argument("--mode", default="prefill", choices=["prefill", "decode", "backward"],
+    ap.add_argument("--mode", default="prefill", choices=["prefill", "decode", "backward", "vec"],
                     help="prefill: the chunked forward (the headline); decode: one recurrent "
                          "step of --decode-seqs sequences; backward: gdr_chunk_bwd on "
-                         "--bwd-seqs sequences of --bwd-tokens tokens")
+                         "--bwd-seqs sequences of --bwd-tokens tokens; vec: the per-channel "
+                         "decay forward on --workload")
     ap.add_argument("--decode-seqs", type=int, default=256)
     ap.add_argument("--bwd-seqs", type=int, default=8)
     ap.add_argument("--bwd-tokens", type=int, default=4096)
@@ -257,6 +258,9 @@ def main(argv=None):
         return
     if args.mode == "backward":
         bench_backward(args)
+        return
+    if args.mode == "vec":
+        bench_vec(args, w)
         return
 
     import torch
@@ -496,6 +500,73 @@ def bench_backward(args):
                      "algorithmic_flops_per_step": flops, "kernel_ms": kern_ms},
         "kernels": {k: {"ms_total": v[0], "launches": v[1]} for k, v in prof.items()},
         "gpu_launches": n_launch, "clocks": summ or None,
+    }), flush=True)
+
+
+def bench_vec(args, w):
+    """The per-channel decay forward (gdr_chunk_fwd_vec) on the workload's shapes,
+    a drawn per key channel.  Algorithmic bytes per (token, head): q, k, v, out and
+    the dk gate inputs in the storage dtype plus beta, and the state in and out."""
+    import torch
+    import chunked_gated_delta_07_gb300 as gdr
+    from gdr_inputs import make_channel_gate, make_inputs
+    x = make_inputs(w, device="cuda")
+    av = make_channel_gate(x, w.seed + 7)
+    out = torch.empty_like(x["v"])
+    hT = torch.empty((x["N"], w.H, w.dk, w.dv), dtype=torch.float32, device="cuda")
+    dcode = gdr.GDR_BF16 if w.dtype == "bf16" else gdr.GDR_F32
+    stream = torch.cuda.current_stream()
+    n_tok = x["q"].shape[0] * x["q"].shape[1]
+
+    def step():
+        rc = gdr.gdr_chunk_fwd_vec(x["q"], x["k"], x["v"], av, x["beta"], x["h0"], out, hT,
+                                   x["cu_seqlens"], x["N"], x["T"], w.H, w.dk, w.dv, 16, w.b,
+                                   dcode, stream)
+        if rc != gdr.GDR_OK:
+            raise gdr.GdrError(rc, "gdr_chunk_fwd_vec")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    steps = max(args.steps, 3)
+    gdr.gdr_profile_read()
+    gdr.gdr_profile_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        n0 = gdr.gdr_launch_count()
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        n_launch = gdr.gdr_launch_count() - n0
+    gdr.gdr_profile_enable(False)
+    prof = gdr.gdr_profile_read()
+    st = gdr.gdr_get_status(stream)
+    if st != gdr.GDR_OK:
+        raise gdr.GdrError(st, "device status after the per-channel forward")
+    ms = ev0.elapsed_time(ev1) / steps
+    es = 2 if w.dtype == "bf16" else 4
+    nstate = x["N"] * w.H * w.dk * w.dv * 4
+    byt = n_tok * w.H * (es * (3 * w.dk + 2 * w.dv) + es) + nstate * (2 if x["h0"] is not None else 1)
+    hbm, _, _, peak_src = peaks()
+    dom_name, (dom_ms, dom_n) = max(prof.items(), key=lambda kv: kv[1][0]) if prof else ("?", (0.0, 1))
+    achieved = byt / (ms / 1e3) / 1e9
+    print(json.dumps({
+        "metric": "per-channel decay forward tokens/s, bounded gate, bf16 in/out, fp32 state",
+        "value": n_tok / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": f"{w.name} with a per key channel: {x['N']} sequences, "
+                               f"{n_tok} tokens, H={w.H}, dk=dv={w.dk}, C=16, b={w.b}",
+                   "l2_policy": "inputs larger than L2 (no flush)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None, "kernel": "whole step",
+                     "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_step": byt,
+                     "dominant_kernel": dom_name, "dominant_share":
+                         dom_ms / sum(v[0] for v in prof.values()) if prof else None},
+        "kernels": {k: {"ms_total": v[0], "launches": v[1]} for k, v in prof.items()},
+        "gpu_launches": n_launch, "clocks": clk.summary(),
     }), flush=True)
 
 

@@ -28,7 +28,7 @@ GDR_PATH_AUTO, GDR_PATH_SIMT, GDR_PATH_TC = 0, 1, 2
 EXPORTS = ("gdr_chunk_fwd", "gdr_chunk_fwd_ex", "gdr_chunk_fwd_workspace_size",
            "gdr_chunk_fwd_host", "gdr_gate_cumsum", "gdr_wy_repr", "gdr_get_status",
            "gdr_status_string", "gdr_release", "gdr_launch_count", "gdr_profile_enable",
-           "gdr_profile_read", "gdr_chunk_fwd_noalloc", "gdr_recurrent_fwd", "gdr_chunk_bwd")
+           "gdr_profile_read", "gdr_chunk_fwd_noalloc", "gdr_recurrent_fwd", "gdr_chunk_bwd", "gdr_chunk_fwd_vec")
 
 _lock = threading.Lock()
 _lib = None
@@ -50,6 +50,7 @@ _SIGS = {
     "gdr_chunk_fwd_noalloc": (_I, [_P] * 8 + [_I, _I64, _I, _I, _I, _I, _F, _I, _I, _P]),
     "gdr_recurrent_fwd": (_I, [_P] * 7 + [_I, _I64, _I, _I, _I, _F, _I, _I, _P]),
     "gdr_chunk_bwd": (_I, [_P] * 15 + [_I, _I64, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "gdr_chunk_fwd_vec": (_I, [_P] * 9 + [_I, _I64, _I, _I, _I, _I, _F, _I, _P]),
 }
 
 
@@ -159,6 +160,30 @@ def gdr_chunk_bwd(q, k, v, a, beta, h0, dout, dhT, dq, dk, dv, da, dbeta, dh0, c
                                _ptr(dout), _ptr(dhT), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(da),
                                _ptr(dbeta), _ptr(dh0), _ptr(cu_seqlens), B, T, H, dk_dim, dv_dim,
                                chunk, float(b), dtype, gate, _stream(stream))
+
+
+def gdr_chunk_fwd_vec(q, k, v, a, beta, h0, out, hT, cu_seqlens, B, T, H, dk, dv, chunk, b, dtype,
+                      stream=None) -> int:
+    """Forward pass with one decay factor per key channel (a is [..., H, dk])."""
+    return lib().gdr_chunk_fwd_vec(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(beta), _ptr(h0),
+                                   _ptr(out), _ptr(hT), _ptr(cu_seqlens), B, T, H, dk, dv, chunk,
+                                   float(b), dtype, _stream(stream))
+
+
+def chunk_fwd_vec(q, k, v, a, beta, h0=None, cu_seqlens=None, b=2.0, want_state=True,
+                  stream=None):
+    """Allocate and return (out, hT) of the per-channel decay form."""
+    import torch
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    out = torch.empty_like(v)
+    hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device) if want_state else None
+    rc = gdr_chunk_fwd_vec(q, k, v, a, beta, h0, out, hT, cu_seqlens, N, T, H, dk, dv, 16, b,
+                           dtype_code(q), stream)
+    if rc != GDR_OK:
+        raise GdrError(rc, "gdr_chunk_fwd_vec")
+    return out, hT
 
 
 def chunk_bwd(q, k, v, a, beta, dout=None, dhT=None, h0=None, cu_seqlens=None, chunk=16, b=2.0,

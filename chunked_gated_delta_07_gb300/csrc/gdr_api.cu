@@ -637,6 +637,50 @@ gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const vo
                : GDR_ERR_CUDA;
 }
 
+gdr_status_t gdr_chunk_fwd_vec(const void *q, const void *k, const void *v, const void *a,
+                               const void *beta, const float *h0, void *out, float *hT,
+                               const int32_t *cu_seqlens, int B, int64_t T, int H, int dk, int dv,
+                               int chunk, float b, gdr_dtype_t dtype, gdr_stream_t stream_) {
+    Shape s;
+    gdr_status_t st = check_args(q, k, v, a, beta, h0, out, hT, cu_seqlens, B, T, H, dk, dv, chunk,
+                                 b, dtype, GDR_GATE_BOUNDED, GDR_PATH_SIMT, &s);
+    if (st != GDR_OK) return st;
+    if (chunk != kVecTile || b > kVecMaxB) return GDR_ERR_UNSUPPORTED;
+    // a holds dk gate inputs per (token, head): check it against the outputs too
+    const size_t es = dtype == GDR_BF16 ? 2 : 4;
+    const size_t rows = (size_t)s.T_total * H;
+    const size_t a_bytes = rows * dk * es, out_bytes = rows * dv * es;
+    const size_t nst = (size_t)B * H * dk * dv * sizeof(float);
+    if (overlaps(out, out_bytes, a, a_bytes) || overlaps(hT, nst, a, a_bytes)) return GDR_ERR_INVALID_ARG;
+    cudaStream_t stream = (cudaStream_t)stream_;
+    if (s.T_total == 0) {   // no tokens: hT = h0
+        if (!hT) return GDR_OK;
+        const cudaError_t e = h0 ? cudaMemcpyAsync(hT, h0, nst, cudaMemcpyDeviceToDevice, stream)
+                                 : cudaMemsetAsync(hT, 0, nst, stream);
+        return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+    }
+    DeviceCtx *ctx = device_ctx();
+    if (!ctx) return GDR_ERR_CUDA;
+    const int64_t tiles = tile_bound(s.varlen, B, T, kVecTile);
+    const size_t plan_b = align_up(3 * sizeof(int64_t) * (size_t)(B + 1));
+    const size_t need = plan_b + vec_scratch_bytes(tiles, s.T_total, H, dk, dv);
+    char *ws;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!grow(&ctx->ws, &ctx->ws_bytes, need)) return GDR_ERR_CUDA;
+        ws = (char *)ctx->ws;
+    }
+    int64_t *seq_start = (int64_t *)ws;
+    Plan plan{B, kVecTile, 1 << 30, seq_start, seq_start + (B + 1), seq_start + 2 * (B + 1)};
+    if (launch_plan(cu_seqlens, B, s.T_per, s.T_total, kVecTile, 1 << 30, seq_start,
+                    seq_start + (B + 1), seq_start + 2 * (B + 1), ctx->d_status, stream) != cudaSuccess)
+        return GDR_ERR_CUDA;
+    return launch_vec_forward(q, k, v, a, beta, h0, out, hT, dtype, plan, H, dk, dv, s.T_total, tiles,
+                              b, ws + plan_b, stream) == cudaSuccess
+               ? GDR_OK
+               : GDR_ERR_CUDA;
+}
+
 gdr_status_t gdr_gate_cumsum(const void *a, float *G, const int32_t *cu_seqlens, int B,
                              int64_t T, int H, int chunk, float b, gdr_dtype_t dtype,
                              gdr_gate_t gate, gdr_stream_t stream) {

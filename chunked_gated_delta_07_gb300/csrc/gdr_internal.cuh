@@ -95,6 +95,8 @@ cudaError_t launch_wy_simt(const void *k, const void *v, const void *beta, const
 // The backward pass (gdr_backward.cu).  The plan must be built with 16-token
 // tiles (the checkpoint interval); scratch holds bwd_scratch_bytes(...) bytes.
 constexpr int kBwTile = 16;
+constexpr int kVecTile = 16;        // tile of the per-channel decay path
+constexpr float kVecMaxB = 5.0f;    // largest gate bound it takes: exp(16 b) < FLT_MAX
 size_t bwd_scratch_bytes(int64_t tiles, int64_t T_total, int H, int dk, int dv);
 cudaError_t launch_bwd(const void *q, const void *k, const void *v, const void *a, const void *beta,
                        const float *h0, const void *dout, const float *dhT, void *dq, void *dk_,
@@ -113,6 +115,14 @@ cudaError_t launch_state_out_simt(const void *q, const void *k, const float *W, 
                                   int64_t T_total, cudaStream_t stream);
 
 // Count of kernels launched by the library (incremented by every launcher).
+// per-channel decay path (gdr_vec.cu); tiles of 16 tokens, bounded gate
+size_t vec_scratch_bytes(int64_t tiles, int64_t T_total, int H, int dk, int dv);
+cudaError_t launch_vec_forward(const void *q, const void *k, const void *v, const void *a,
+                               const void *beta, const float *h0, void *out, float *hT,
+                               gdr_dtype_t dtype, Plan plan, int H, int dk, int dv,
+                               int64_t T_total, int64_t max_tiles, float b, void *scratch,
+                               cudaStream_t stream);
+
 void count_launch(uint64_t n = 1);
 
 // Brackets one kernel launch with CUDA events while profiling is enabled

@@ -146,3 +146,18 @@ def make_inputs(w: Workload, device="cpu", T: int | None = None, block: int = 1 
         cu = cu.to(device)
     return dict(q=q, k=k, v=v, a=a, beta=beta, h0=h0, cu_seqlens=cu, B=B, T=Tt,
                 N=N, H=H, dk=dk, dv=dv, chunk=w.chunk, b=w.b, gate=w.gate, dtype=w.dtype)
+
+
+def make_channel_gate(x: dict, seed: int, a_std: float = 1.0, a_mean: float = 0.0,
+                      block: int = 1 << 14):
+    """Gate inputs of the per-channel decay form: a [B, T, H, dk] in x's storage
+    dtype on x's device, ~ N(a_mean, a_std^2), drawn in token blocks."""
+    q = x["q"]
+    B, T, H, dk = q.shape
+    g = torch.Generator(device=q.device).manual_seed(seed)
+    a = torch.empty((B, T, H, dk), dtype=q.dtype, device=q.device)
+    for bi in range(B):
+        for t0 in range(0, T, block):
+            t1 = min(T, t0 + block)
+            a[bi, t0:t1] = (a_mean + a_std * _randn((t1 - t0, H, dk), g, q.device)).to(q.dtype)
+    return a

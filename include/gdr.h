@@ -230,6 +230,29 @@ GDR_API gdr_status_t gdr_recurrent_fwd(const void *q, const void *k, const void 
                                gdr_gate_t gate, gdr_stream_t stream);
 
 /*
+ * Per-channel (vector) decay: the forward pass of gdr_chunk_fwd_ex with one
+ * gate input per key channel.  Token t decays row i of the dk x dv state by
+ * exp(g(a[t, h, i])) before the delta-rule write:
+ *     H_t = (I - beta k k^T) diag(exp(g(a_t))) H_{t-1} + beta k v^T,  o_t = H_t^T q_t,
+ * g(a) = -b sigmoid(a) (the bounded gate).  Inside each 16-token tile the
+ * pairwise decays exp(G_i - G_j) are split into the factors exp(G_i) and
+ * exp(-G_j), which turns every in-tile product into a plain matrix product;
+ * the bound keeps exp(-G) finite ("Deep Dive: The Next Generation of
+ * Ultra-Long Context Sparse MoE LLMs", §2.1-2.2; "How Trillion-Scale Sparse
+ * MoE Models Achieve Million-Token Long Context Capabilities", §3.2).
+ *   a    [B, T, H, dk] in dtype (varlen: [1, T, H, dk]); every other argument as
+ *        for gdr_chunk_fwd_ex.
+ * chunk must be 16 and 0 < b <= 5 (exp(16 b) must stay below FLT_MAX):
+ * GDR_ERR_UNSUPPORTED otherwise; b <= 0 is GDR_ERR_INVALID_ARG.  Only the
+ * bounded gate is taken (an unbounded one can overflow exp(-G)).  Scratch
+ * comes from the internal per-device cache; asynchronous on `stream`.
+ */
+GDR_API gdr_status_t gdr_chunk_fwd_vec(const void *q, const void *k, const void *v, const void *a,
+                               const void *beta, const float *h0, void *out, float *hT,
+                               const int32_t *cu_seqlens, int B, int64_t T, int H, int dk, int dv,
+                               int chunk, float b, gdr_dtype_t dtype, gdr_stream_t stream);
+
+/*
  * The backward pass: gradients of  L = <dout, out> + <dhT, hT>  with respect to
  * q, k, v, a, beta and h0, for the forward of gdr_chunk_fwd_ex on the same
  * inputs (same layouts, dtype, gate, b and cu_seqlens; B is N for varlen).
