@@ -17,6 +17,10 @@ Independent references live here:
 * ``oracle_bwd`` -- the gradients of <dout, out> + <dhT, hT> with respect to
   every input, by the token-by-token adjoint recurrence in fp64 (the same C
   file), pinned by finite differences of ``oracle_fwd``.
+* ``router_topk`` / ``router_update`` -- the quantile-balancing router-bias
+  update (``router_oracle.c``): top-k of logit + bias per token, per-expert
+  load counts, linear-interpolation quantiles and the sign or proportional
+  bias step, pinned by numpy's stable argsort and quantile and by closed forms.
 * ``chunk_ref`` -- the chunk-parallel (WY / UT) form in fp64 numpy, used only
   to check the GPU's intermediate stages (gate cumsum, W, U) one by one.
 
@@ -46,17 +50,26 @@ BF16, F32, F64 = 0, 1, 2
 GATES = {"bounded": 0, "softplus": 1}
 
 
-def build(force: bool = False) -> str:
-    """Compile gdr_oracle.c into libgdr_oracle.so next to it (gcc, OpenMP)."""
-    if (not force and os.path.exists(_LIB)
-            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
-        return _LIB
-    tmp = _LIB + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
-           "-o", tmp, _SRC, "-lm"]
+_RSRC = os.path.join(_HERE, "router_oracle.c")
+_RLIB = os.path.join(_HERE, "librouter_oracle.so")
+_rlib = None
+
+
+def _compile(src, lib, force):
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= os.path.getmtime(src):
+        return lib
+    tmp = lib + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-o", tmp, src, "-lm"]
     subprocess.run(cmd, check=True)
-    os.replace(tmp, _LIB)
-    return _LIB
+    os.replace(tmp, lib)
+    return lib
+
+
+def build(force: bool = False) -> str:
+    """Compile gdr_oracle.c into libgdr_oracle.so and router_oracle.c into
+    librouter_oracle.so next to them (gcc, OpenMP, ISO C11: no FMA contraction)."""
+    _compile(_RSRC, _RLIB, force)
+    return _compile(_SRC, _LIB, force)
 
 
 def _bind(path):
@@ -92,6 +105,63 @@ def _load():
         if _lib is None:
             _lib = _bind(build())
     return _lib
+
+
+def _rbind(path):
+    lib = ctypes.CDLL(path)
+    P, I, I64, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+    lib.gdr_oracle_router_topk.restype = I
+    lib.gdr_oracle_router_topk.argtypes = [P, I, P, I64, I, I, P, P, P]
+    lib.gdr_oracle_router_update.restype = I
+    lib.gdr_oracle_router_update.argtypes = [P, I, P, I, D, D, ctypes.c_float, P]
+    return lib
+
+
+def _rload():
+    global _rlib
+    with _lock:
+        if _rlib is None:
+            build()
+            _rlib = _rbind(_RLIB)
+    return _rlib
+
+
+ROUTER_MODES = {"sign": 0, "proportional": 1}
+
+
+def router_topk(logits, bias, k, load=None, _lib_path=None):
+    """Top-k experts of every token by score logit + bias (binary32 add), ties to
+    the lower index.  logits [T, E] (bf16 bit patterns or fp32), bias [E] fp32.
+    Returns (idx [T, k] int32 in rank order, selected logits [T, k] fp32, load
+    [E] int64 = the given load (or zeros) plus this call's counts)."""
+    lib = _rload() if _lib_path is None else _rbind(_lib_path)
+    xa, dt = _as_array(logits)
+    assert dt in (BF16, F32), "logits must be bf16 or fp32"
+    T, E = xa.shape
+    b = np.ascontiguousarray(np.asarray(bias.cpu().numpy() if hasattr(bias, "cpu") else bias,
+                                        dtype=np.float32))
+    idx = np.zeros((T, k), dtype=np.int32)
+    sel = np.zeros((T, k), dtype=np.float32)
+    ld = np.zeros(E, dtype=np.int64) if load is None else np.array(load, dtype=np.int64)
+    rc = lib.gdr_oracle_router_topk(xa.ctypes.data, dt, b.ctypes.data, T, E, k, idx.ctypes.data,
+                                    sel.ctypes.data, ld.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"gdr_oracle_router_topk rejected its arguments (code {rc})")
+    return idx, sel, ld
+
+
+def router_update(load, bias, mode="sign", q_lo=0.1, q_hi=0.9, eta=1e-3, _lib_path=None):
+    """Quantile-balancing bias update.  Returns (new bias [E] fp32, (Q_lo, Q_hi))."""
+    lib = _rload() if _lib_path is None else _rbind(_lib_path)
+    ld = np.ascontiguousarray(np.asarray(load, dtype=np.int64))
+    b = np.array(bias.cpu().numpy() if hasattr(bias, "cpu") else bias, dtype=np.float32)
+    thr = np.zeros(2, dtype=np.float64)
+    rc = lib.gdr_oracle_router_update(ld.ctypes.data, ld.shape[0], b.ctypes.data,
+                                      ROUTER_MODES[mode], float(q_lo), float(q_hi), float(eta),
+                                      thr.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"gdr_oracle_router_update rejected its arguments (code {rc})")
+    return b, (float(thr[0]), float(thr[1]))
 
 
 def _as_array(x):
