@@ -230,11 +230,14 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the tokens per sequence (or total, varlen) of the workload")
-    ap.add_argument("--mode", default="prefill", choices=["prefill", "decode", "backward", "vec"],
+    ap.add_argument("--mode", default="prefill", choices=["prefill", "decode", "backward", "vec", "router"],
                     help="prefill: the chunked forward (the headline); decode: one recurrent "
                          "step of --decode-seqs sequences; backward: gdr_chunk_bwd on "
                          "--bwd-seqs sequences of --bwd-tokens tokens; vec: the per-channel "
-                         "decay forward on --workload")
+                         "decay forward on --workload; router: one quantile-balancing window of "
+                         "--router-tokens tokens over 896 experts")
+    ap.add_argument("--router-tokens", type=int, default=1 << 20)
+    ap.add_argument("--router-k", type=int, default=8)
     ap.add_argument("--decode-seqs", type=int, default=256)
     ap.add_argument("--bwd-seqs", type=int, default=8)
     ap.add_argument("--bwd-tokens", type=int, default=4096)
@@ -261,6 +264,9 @@ def main(argv=None):
         return
     if args.mode == "vec":
         bench_vec(args, w)
+        return
+    if args.mode == "router":
+        bench_router(args)
         return
 
     import torch
@@ -566,6 +572,71 @@ def bench_vec(args, w):
                      "dominant_kernel": dom_name, "dominant_share":
                          dom_ms / sum(v[0] for v in prof.values()) if prof else None},
         "kernels": {k: {"ms_total": v[0], "launches": v[1]} for k, v in prof.items()},
+        "gpu_launches": n_launch, "clocks": clk.summary(),
+    }), flush=True)
+
+
+def bench_router(args):
+    """One statistics window of quantile balancing: zero the counts, route T tokens
+    over E = 896 experts (top-k of logit + bias, picked logits returned), then the
+    two-sided sign step at q = 0.1 / 0.9.  Algorithmic bytes: the bf16 logits read
+    once, the picked indices and logits written, plus the bias and the counts."""
+    import torch
+    import chunked_gated_delta_07_gb300 as gdr
+    from gdr_inputs import make_router_logits
+    T, E, k = args.router_tokens, 896, args.router_k
+    x, bias = make_router_logits(T, E, 6000, "bf16", device="cuda")
+    load = torch.zeros(E, dtype=torch.int64, device="cuda")
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    sel = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    thr = torch.empty(2, dtype=torch.float64, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        load.zero_()
+        rc = gdr.gdr_router_topk(x, bias, idx, sel, load, T, E, k, gdr.GDR_BF16, stream)
+        if rc != gdr.GDR_OK:
+            raise gdr.GdrError(rc, "gdr_router_topk")
+        rc = gdr.gdr_router_bias_update(load, bias, thr, E, gdr.GDR_QB_SIGN, 0.1, 0.9, 1e-3, stream)
+        if rc != gdr.GDR_OK:
+            raise gdr.GdrError(rc, "gdr_router_bias_update")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    steps = max(args.steps, 10)
+    gdr.gdr_profile_read()
+    gdr.gdr_profile_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        n0 = gdr.gdr_launch_count()
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        n_launch = gdr.gdr_launch_count() - n0
+    gdr.gdr_profile_enable(False)
+    prof = gdr.gdr_profile_read()
+    ms = ev0.elapsed_time(ev1) / steps
+    kern_total, kern_n = prof.get("router_topk_kernel", (0.0, 1))
+    kern_ms = kern_total / max(kern_n, 1)
+    byt = T * E * 2 + T * k * 8 + E * (4 + 8)
+    hbm, _, _, peak_src = peaks()
+    achieved = byt / (kern_ms / 1e3) / 1e9 if kern_ms > 0 else 0.0
+    print(json.dumps({
+        "metric": "router tokens/s, quantile-balancing window (top-8 of 896 experts + bias step)",
+        "value": T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"router: T={T} tokens x E={E} experts, k={k}, bf16 logits, "
+                               f"sign step q=0.1/0.9",
+                   "l2_policy": "logits larger than L2 (no flush)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None, "kernel": "router_topk_kernel",
+                     "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": byt,
+                     "kernel_ms": kern_ms},
+        "kernels": {kk: {"ms_total": v[0], "launches": v[1]} for kk, v in prof.items()},
         "gpu_launches": n_launch, "clocks": clk.summary(),
     }), flush=True)
 

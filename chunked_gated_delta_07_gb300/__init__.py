@@ -28,7 +28,8 @@ GDR_PATH_AUTO, GDR_PATH_SIMT, GDR_PATH_TC = 0, 1, 2
 EXPORTS = ("gdr_chunk_fwd", "gdr_chunk_fwd_ex", "gdr_chunk_fwd_workspace_size",
            "gdr_chunk_fwd_host", "gdr_gate_cumsum", "gdr_wy_repr", "gdr_get_status",
            "gdr_status_string", "gdr_release", "gdr_launch_count", "gdr_profile_enable",
-           "gdr_profile_read", "gdr_chunk_fwd_noalloc", "gdr_recurrent_fwd", "gdr_chunk_bwd", "gdr_chunk_fwd_vec")
+           "gdr_profile_read", "gdr_chunk_fwd_noalloc", "gdr_recurrent_fwd", "gdr_chunk_bwd", "gdr_chunk_fwd_vec",
+           "gdr_router_topk", "gdr_router_bias_update")
 
 _lock = threading.Lock()
 _lib = None
@@ -51,6 +52,8 @@ _SIGS = {
     "gdr_recurrent_fwd": (_I, [_P] * 7 + [_I, _I64, _I, _I, _I, _F, _I, _I, _P]),
     "gdr_chunk_bwd": (_I, [_P] * 15 + [_I, _I64, _I, _I, _I, _I, _F, _I, _I, _P]),
     "gdr_chunk_fwd_vec": (_I, [_P] * 9 + [_I, _I64, _I, _I, _I, _I, _F, _I, _P]),
+    "gdr_router_topk": (_I, [_P] * 5 + [_I64, _I, _I, _I, _P]),
+    "gdr_router_bias_update": (_I, [_P] * 3 + [_I, _I, ctypes.c_double, ctypes.c_double, _F, _P]),
 }
 
 
@@ -184,6 +187,44 @@ def chunk_fwd_vec(q, k, v, a, beta, h0=None, cu_seqlens=None, b=2.0, want_state=
     if rc != GDR_OK:
         raise GdrError(rc, "gdr_chunk_fwd_vec")
     return out, hT
+
+
+GDR_QB_SIGN, GDR_QB_PROPORTIONAL = 0, 1
+_QB = {"sign": GDR_QB_SIGN, "proportional": GDR_QB_PROPORTIONAL}
+
+
+def gdr_router_topk(logits, bias, topk_idx, topk_logit, load, T, E, k, dtype, stream=None) -> int:
+    """Top-k experts of logits + bias per token; load counts are added."""
+    return lib().gdr_router_topk(_ptr(logits), _ptr(bias), _ptr(topk_idx), _ptr(topk_logit),
+                                 _ptr(load), T, E, k, dtype, _stream(stream))
+
+
+def gdr_router_bias_update(load, bias, thresholds, E, mode, q_lo, q_hi, eta, stream=None) -> int:
+    """Quantile-balancing bias step (sign or proportional), in place on bias."""
+    return lib().gdr_router_bias_update(_ptr(load), _ptr(bias), _ptr(thresholds), E, mode,
+                                        float(q_lo), float(q_hi), float(eta), _stream(stream))
+
+
+def router_topk(logits, bias, k, load=None, want_logits=True, stream=None):
+    """Return (idx [T, k] int32, picked logits [T, k] fp32 or None); counts go to load."""
+    import torch
+    T, E = logits.shape
+    idx = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    sel = torch.empty((T, k), dtype=torch.float32, device=logits.device) if want_logits else None
+    rc = gdr_router_topk(logits, bias, idx, sel, load, T, E, k, dtype_code(logits), stream)
+    if rc != GDR_OK:
+        raise GdrError(rc, "gdr_router_topk")
+    return idx, sel
+
+
+def router_bias_update(load, bias, mode="sign", q_lo=0.1, q_hi=0.9, eta=1e-3, stream=None):
+    """Update bias in place; returns the fp64 thresholds (Q(q_lo), Q(q_hi)) on the device."""
+    import torch
+    thr = torch.empty(2, dtype=torch.float64, device=bias.device)
+    rc = gdr_router_bias_update(load, bias, thr, bias.numel(), _QB[mode], q_lo, q_hi, eta, stream)
+    if rc != GDR_OK:
+        raise GdrError(rc, "gdr_router_bias_update")
+    return thr
 
 
 def chunk_bwd(q, k, v, a, beta, dout=None, dhT=None, h0=None, cu_seqlens=None, chunk=16, b=2.0,

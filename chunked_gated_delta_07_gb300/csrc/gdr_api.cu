@@ -681,6 +681,53 @@ gdr_status_t gdr_chunk_fwd_vec(const void *q, const void *k, const void *v, cons
                : GDR_ERR_CUDA;
 }
 
+gdr_status_t gdr_router_topk(const void *logits, const float *bias, int32_t *topk_idx,
+                             float *topk_logit, int64_t *load, int64_t T, int E, int k,
+                             gdr_dtype_t dtype, gdr_stream_t stream) {
+    if (dtype != GDR_BF16 && dtype != GDR_F32) return GDR_ERR_INVALID_ARG;
+    if (T < 0 || E < 1 || k < 1) return GDR_ERR_INVALID_ARG;
+    if (E > kRouterMaxE || E % 4 != 0 || k > E || k > kRouterMaxK) return GDR_ERR_UNSUPPORTED;
+    if (T > ((int64_t)1 << 40)) return GDR_ERR_UNSUPPORTED;
+    if (T == 0) return GDR_OK;
+    if (!logits || !bias || !topk_idx) return GDR_ERR_INVALID_ARG;
+    if ((uintptr_t)logits % 16 != 0) return GDR_ERR_INVALID_ARG;
+    const size_t es = dtype == GDR_BF16 ? 2 : 4;
+    const size_t xb = (size_t)T * E * es, bb = sizeof(float) * (size_t)E;
+    const size_t ib = sizeof(int32_t) * (size_t)T * k, sb = sizeof(float) * (size_t)T * k;
+    const size_t lb = sizeof(int64_t) * (size_t)E;
+    const void *outs[3] = {topk_idx, topk_logit, load};
+    const size_t ob[3] = {ib, sb, lb};
+    for (int i = 0; i < 3; ++i) {
+        if (overlaps(outs[i], ob[i], logits, xb) || overlaps(outs[i], ob[i], bias, bb))
+            return GDR_ERR_INVALID_ARG;
+        for (int j = i + 1; j < 3; ++j)
+            if (overlaps(outs[i], ob[i], outs[j], ob[j])) return GDR_ERR_INVALID_ARG;
+    }
+    return launch_router_topk(logits, bias, topk_idx, topk_logit, load, T, E, k, dtype,
+                              (cudaStream_t)stream) == cudaSuccess
+               ? GDR_OK
+               : GDR_ERR_CUDA;
+}
+
+gdr_status_t gdr_router_bias_update(const int64_t *load, float *bias, double *thresholds, int E,
+                                    gdr_qb_mode_t mode, double q_lo, double q_hi, float eta,
+                                    gdr_stream_t stream) {
+    if (E < 1) return GDR_ERR_INVALID_ARG;
+    if (E > kRouterMaxE) return GDR_ERR_UNSUPPORTED;
+    if (mode != GDR_QB_SIGN && mode != GDR_QB_PROPORTIONAL) return GDR_ERR_INVALID_ARG;
+    if (!(q_lo >= 0.0 && q_lo <= 1.0) || !(q_hi >= 0.0 && q_hi <= 1.0) || !std::isfinite(eta))
+        return GDR_ERR_INVALID_ARG;
+    if (!load || !bias) return GDR_ERR_INVALID_ARG;
+    const size_t lb = sizeof(int64_t) * (size_t)E, bb = sizeof(float) * (size_t)E;
+    if (overlaps(bias, bb, load, lb) || overlaps(thresholds, 16, load, lb) ||
+        overlaps(thresholds, 16, bias, bb))
+        return GDR_ERR_INVALID_ARG;
+    return launch_router_update(load, bias, thresholds, E, (int)mode, q_lo, q_hi, eta,
+                                (cudaStream_t)stream) == cudaSuccess
+               ? GDR_OK
+               : GDR_ERR_CUDA;
+}
+
 gdr_status_t gdr_gate_cumsum(const void *a, float *G, const int32_t *cu_seqlens, int B,
                              int64_t T, int H, int chunk, float b, gdr_dtype_t dtype,
                              gdr_gate_t gate, gdr_stream_t stream) {

@@ -123,6 +123,15 @@ cudaError_t launch_vec_forward(const void *q, const void *k, const void *v, cons
                                int64_t T_total, int64_t max_tiles, float b, void *scratch,
                                cudaStream_t stream);
 
+// quantile-balancing router-bias update (gdr_router.cu)
+constexpr int kRouterMaxE = 2048;
+constexpr int kRouterMaxK = 32;
+cudaError_t launch_router_topk(const void *logits, const float *bias, int32_t *idx, float *sel,
+                               int64_t *load, int64_t T, int E, int k, gdr_dtype_t dtype,
+                               cudaStream_t stream);
+cudaError_t launch_router_update(const int64_t *load, float *bias, double *thr, int E, int mode,
+                                 double q_lo, double q_hi, float eta, cudaStream_t stream);
+
 void count_launch(uint64_t n = 1);
 
 // Brackets one kernel launch with CUDA events while profiling is enabled

@@ -1,0 +1,319 @@
+// gdr_router.cu -- the quantile-balancing router-bias update (aux-loss-free
+// load balancing) [P1 §4.2, P2 §3.2, P3 §4.3, P4 §3.2]:
+//   1. every token picks the k experts of largest score logit + bias
+//      (binary32 add; equal scores go to the lower expert index);
+//   2. load_e counts the tokens that picked expert e (int64, accumulated);
+//   3. quantiles of the loads by linear interpolation between order statistics;
+//   4. sign step (bias -= eta above Q(q_hi), += eta below Q(q_lo)) or
+//      proportional step (bias += eta (Q - load) / Q), binary64 then rounded.
+//
+// router_topk_kernel is the hot part: it reads the [T, E] logits once.  One
+// warp per token; lane l owns experts 4c..4c+3 for c = l, l + 32, ..., so its
+// slice of the bias stays in registers for every token.  Each score becomes an
+// order-preserving 32-bit key.  The k-th largest of the 32 lane maxima, found
+// with k warp-wide max reductions, is a lower bound tau for the k-th largest
+// score: the k lanes it came from hold k scores >= tau.  Only scores >= tau
+// can be selected; they are gathered (usually a dozen) and ranked exactly by
+// (score, -index).  When more than kCap scores tie at or above tau, the warp
+// falls back to k rounds of a warp-wide arg-max over (score, -index).
+// Loads are counted in a shared-memory histogram per block and added to the
+// int64 counts once per block.
+#include <algorithm>
+
+#include "gdr_internal.cuh"
+
+namespace gdr {
+namespace {
+
+constexpr int kRtThreads = 256;
+constexpr int kRtWarps = kRtThreads / 32;
+constexpr int kCap = 64;     // gathered candidates per warp
+constexpr int kRtBlocksPerSm = 4;
+
+// Order-preserving map of a binary32 score onto uint32 (-0 taken as +0).
+__device__ __forceinline__ uint32_t score_key(float s) {
+    const uint32_t u = __float_as_uint(s + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// (key, -index) packed so that a larger value is the better expert.
+__device__ __forceinline__ uint64_t pack(uint32_t key, int e) {
+    return ((uint64_t)key << 32) | (uint64_t)(0xffffffffu - (uint32_t)e);
+}
+
+template <typename T> struct Vec4;
+template <> struct Vec4<__nv_bfloat16> {
+    using type = uint2;   // four bf16 in 8 bytes
+    __device__ static void unpack(const type &x, float (&f)[4]) {
+        f[0] = __uint_as_float(x.x << 16);
+        f[1] = __uint_as_float(x.x & 0xffff0000u);
+        f[2] = __uint_as_float(x.y << 16);
+        f[3] = __uint_as_float(x.y & 0xffff0000u);
+    }
+};
+template <> struct Vec4<float> {
+    using type = float4;
+    __device__ static void unpack(const type &x, float (&f)[4]) {
+        f[0] = x.x;
+        f[1] = x.y;
+        f[2] = x.z;
+        f[3] = x.w;
+    }
+};
+
+template <typename T, int NCH>
+__global__ void __launch_bounds__(kRtThreads, NCH > 8 ? 1 : 2)
+router_topk_kernel(const T *__restrict__ logits, const float *__restrict__ bias,
+                   int32_t *__restrict__ idx, float *__restrict__ sel,
+                   unsigned long long *__restrict__ load, int64_t Tn, int E, int k) {
+    extern __shared__ unsigned int hist[];                // [E] counts, then [E] bias
+    float *bsm = (float *)(hist + E);
+    __shared__ uint64_t cand[kRtWarps][kCap];
+    __shared__ float cand_x[kRtWarps][kCap];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int e = threadIdx.x; e < E; e += kRtThreads) {
+        hist[e] = 0;
+        bsm[e] = bias[e];
+    }
+    __syncthreads();
+    using V = typename Vec4<T>::type;
+    const int64_t nwarps = (int64_t)gridDim.x * kRtWarps;
+    // the next token's row is loaded while the current one is ranked
+    V nxt[NCH];
+    int64_t t = (int64_t)blockIdx.x * kRtWarps + warp;
+    auto fetch = [&](int64_t tt) {
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+            const int c = lane + 32 * j;
+            if (tt < Tn && 4 * c < E) nxt[j] = __ldcs((const V *)(logits + tt * E + 4 * c));
+        }
+    };
+    fetch(t);
+    for (; t < Tn; t += nwarps) {
+        V cur[NCH];
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) cur[j] = nxt[j];
+        fetch(t + nwarps);
+        uint32_t key[NCH][4];
+        uint32_t lmax = 0;
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+            const int c = lane + 32 * j;
+            if (4 * c < E) {
+                float x[4];
+                Vec4<T>::unpack(cur[j], x);
+                const float4 bz = *(const float4 *)&bsm[4 * c];
+                key[j][0] = score_key(x[0] + bz.x);
+                key[j][1] = score_key(x[1] + bz.y);
+                key[j][2] = score_key(x[2] + bz.z);
+                key[j][3] = score_key(x[3] + bz.w);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) lmax = max(lmax, key[j][u]);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) key[j][u] = 0;
+            }
+        }
+        // tau: the k-th largest lane maximum (lanes without experts offer 0)
+        uint32_t tau = 0;
+        bool alive = true;
+        for (int r = 0; r < k; ++r) {
+            const uint32_t m = __reduce_max_sync(0xffffffffu, alive ? lmax : 0u);
+            const unsigned who = __ballot_sync(0xffffffffu, alive && lmax == m);
+            if (who == 0) break;           // fewer live lanes than k: tau stays 0
+            if (lane == __ffs(who) - 1) alive = false;
+            tau = m;
+        }
+        // gather the scores >= tau
+        int cnt = 0;
+#pragma unroll
+        for (int j = 0; j < NCH; ++j)
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                cnt += (4 * (lane + 32 * j) + u < E && key[j][u] >= tau) ? 1 : 0;
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        if (total <= kCap) {
+            int pos = incl - cnt;
+#pragma unroll
+            for (int j = 0; j < NCH; ++j)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int e = 4 * (lane + 32 * j) + u;
+                    if (e < E && key[j][u] >= tau) {
+                        float x[4];
+                        Vec4<T>::unpack(cur[j], x);
+                        cand[warp][pos] = pack(key[j][u], e);
+                        cand_x[warp][pos] = x[u];
+                        ++pos;
+                    }
+                }
+            __syncwarp();
+            for (int ci = lane; ci < total; ci += 32) {
+                const uint64_t me = cand[warp][ci];
+                int rank = 0;
+                for (int cj = 0; cj < total; ++cj) rank += cand[warp][cj] > me ? 1 : 0;
+                if (rank < k) {
+                    const int e = (int)(0xffffffffu - (uint32_t)me);
+                    idx[t * k + rank] = e;
+                    if (sel) sel[t * k + rank] = cand_x[warp][ci];
+                    atomicAdd(&hist[e], 1u);
+                }
+            }
+            __syncwarp();
+        } else {
+            // many ties at the threshold: k rounds of a warp-wide arg-max
+            for (int r = 0; r < k; ++r) {
+                uint64_t best = 0;
+                float bx = 0.f;
+#pragma unroll
+                for (int j = 0; j < NCH; ++j)
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int e = 4 * (lane + 32 * j) + u;
+                        const uint64_t p = e < E ? pack(key[j][u], e) : 0ull;
+                        if (p > best) {
+                            float x[4];
+                            Vec4<T>::unpack(cur[j], x);
+                            best = p;
+                            bx = x[u];
+                        }
+                    }
+                uint64_t w = best;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const uint64_t y = __shfl_xor_sync(0xffffffffu, w, o);
+                    w = y > w ? y : w;
+                }
+                const int e = (int)(0xffffffffu - (uint32_t)w);
+                if (best == w) {   // the lane that owns the winner records and removes it
+                    idx[t * k + r] = e;
+                    if (sel) sel[t * k + r] = bx;
+                    atomicAdd(&hist[e], 1u);
+                }
+                const int cw = e >> 2, jw = cw >> 5, uw = e & 3;   // e = 4 (lane + 32 j) + u
+                if (lane == (cw & 31)) {
+#pragma unroll
+                    for (int j = 0; j < NCH; ++j)
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            if (j == jw && u == uw) key[j][u] = 0;
+                }
+                __syncwarp();
+            }
+        }
+    }
+    __syncthreads();
+    if (load)
+        for (int e = threadIdx.x; e < E; e += kRtThreads)
+            if (hist[e]) atomicAdd(&load[e], (unsigned long long)hist[e]);
+}
+
+// One block: rank sort of the loads, the two quantiles, then the bias step.
+__global__ void __launch_bounds__(1024)
+router_update_kernel(const long long *__restrict__ load, float *__restrict__ bias,
+                     double *__restrict__ thr, int E, int mode, double q_lo, double q_hi,
+                     float eta) {
+    extern __shared__ long long sm_load[];   // [E] loads, then [E] sorted
+    long long *srt = sm_load + E;
+    __shared__ double Q[2];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) sm_load[e] = load[e];
+    __syncthreads();
+    for (int i = threadIdx.x; i < E; i += blockDim.x) {
+        const long long li = sm_load[i];
+        int r = 0;
+        for (int j = 0; j < E; ++j) {
+            const long long lj = sm_load[j];
+            r += (lj < li || (lj == li && j < i)) ? 1 : 0;
+        }
+        srt[r] = li;
+    }
+    __syncthreads();
+    if (threadIdx.x < 2) {
+        const double q = threadIdx.x == 0 ? q_lo : q_hi;
+        const double p = __dmul_rn(q, (double)(E - 1));
+        int i = (int)floor(p);
+        if (i > E - 1) i = E - 1;
+        const int j = i + 1 < E ? i + 1 : i;
+        const double xi = (double)srt[i], xj = (double)srt[j];
+        Q[threadIdx.x] = __dadd_rn(xi, __dmul_rn(__dsub_rn(p, (double)i), __dsub_rn(xj, xi)));
+        if (thr) thr[threadIdx.x] = Q[threadIdx.x];
+    }
+    __syncthreads();
+    const double Qlo = Q[0], Qhi = Q[1];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const double l = (double)sm_load[e];
+        const float b0 = bias[e];
+        float b1 = b0;
+        if (mode == GDR_QB_SIGN) {
+            if (l > Qhi) b1 = __fsub_rn(b0, eta);
+            else if (l < Qlo) b1 = __fadd_rn(b0, eta);
+        } else if (Qhi != 0.0) {
+            b1 = __double2float_rn(
+                __dadd_rn((double)b0, __ddiv_rn(__dmul_rn((double)eta, __dsub_rn(Qhi, l)), Qhi)));
+        }
+        bias[e] = b1;
+    }
+}
+
+template <typename T, int NCH>
+cudaError_t launch_topk_t(const void *logits, const float *bias, int32_t *idx, float *sel,
+                          int64_t *load, int64_t Tn, int E, int k, cudaStream_t stream) {
+    auto kern = router_topk_kernel<T, NCH>;
+    const size_t smem = (sizeof(unsigned int) + sizeof(float)) * (size_t)E;
+    int dev = 0, sms = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    // a few blocks per SM: enough warps in flight to cover HBM latency, few
+    // enough that the per-block count flush stays small
+    const int64_t want = (Tn + kRtWarps - 1) / kRtWarps;
+    const int64_t grid = std::min<int64_t>(want, (int64_t)sms * kRtBlocksPerSm);
+    ProfScope prof(stream, "router_topk_kernel");
+    kern<<<(unsigned)grid, kRtThreads, smem, stream>>>((const T *)logits, bias, idx, sel,
+                                                       (unsigned long long *)load, Tn, E, k);
+    count_launch();
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_topk_dt(const void *logits, const float *bias, int32_t *idx, float *sel,
+                           int64_t *load, int64_t Tn, int E, int k, cudaStream_t stream) {
+    if (E <= 128) return launch_topk_t<T, 1>(logits, bias, idx, sel, load, Tn, E, k, stream);
+    if (E <= 256) return launch_topk_t<T, 2>(logits, bias, idx, sel, load, Tn, E, k, stream);
+    if (E <= 512) return launch_topk_t<T, 4>(logits, bias, idx, sel, load, Tn, E, k, stream);
+    if (E <= 896) return launch_topk_t<T, 7>(logits, bias, idx, sel, load, Tn, E, k, stream);
+    if (E <= 1024) return launch_topk_t<T, 8>(logits, bias, idx, sel, load, Tn, E, k, stream);
+    return launch_topk_t<T, 16>(logits, bias, idx, sel, load, Tn, E, k, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_router_topk(const void *logits, const float *bias, int32_t *idx, float *sel,
+                               int64_t *load, int64_t T, int E, int k, gdr_dtype_t dtype,
+                               cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    if (dtype == GDR_BF16)
+        return launch_topk_dt<__nv_bfloat16>(logits, bias, idx, sel, load, T, E, k, stream);
+    return launch_topk_dt<float>(logits, bias, idx, sel, load, T, E, k, stream);
+}
+
+cudaError_t launch_router_update(const int64_t *load, float *bias, double *thr, int E, int mode,
+                                 double q_lo, double q_hi, float eta, cudaStream_t stream) {
+    const size_t smem = 2 * sizeof(long long) * (size_t)E;
+    cudaError_t err = cudaFuncSetAttribute(router_update_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    ProfScope prof(stream, "router_update_kernel");
+    router_update_kernel<<<1, 1024, smem, stream>>>((const long long *)load, bias, thr, E, mode,
+                                                    q_lo, q_hi, eta);
+    count_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace gdr

@@ -161,3 +161,25 @@ def make_channel_gate(x: dict, seed: int, a_std: float = 1.0, a_mean: float = 0.
             t1 = min(T, t0 + block)
             a[bi, t0:t1] = (a_mean + a_std * _randn((t1 - t0, H, dk), g, q.device)).to(q.dtype)
     return a
+
+
+def make_router_logits(T: int, E: int, seed: int, dtype: str = "bf16", device="cpu",
+                       skew: float = 1.0, ties: bool = False, block: int = 1 << 16):
+    """Synthetic routing logits [T, E]: N(0, 1) plus a fixed per-expert offset of
+    scale ``skew`` (drawn once), so that some experts are systematically
+    over-picked -- the imbalance the bias update corrects.  ``ties`` rounds the
+    logits to multiples of 1/2 (many equal scores).  Also returns a bias [E] fp32
+    ~ N(0, 0.01^2)."""
+    device = torch.device(device)
+    g = torch.Generator(device=device).manual_seed(seed)
+    dt = torch_dtype(dtype)
+    off = skew * _randn((E,), g, device)
+    x = torch.empty((T, E), dtype=dt, device=device)
+    for t0 in range(0, T, block):
+        t1 = min(T, t0 + block)
+        y = _randn((t1 - t0, E), g, device) + off
+        if ties:
+            y = torch.round(y * 2) / 2
+        x[t0:t1] = y.to(dt)
+    bias = 0.01 * _randn((E,), g, device)
+    return x, bias

@@ -252,6 +252,52 @@ GDR_API gdr_status_t gdr_chunk_fwd_vec(const void *q, const void *k, const void 
                                const int32_t *cu_seqlens, int B, int64_t T, int H, int dk, int dv,
                                int chunk, float b, gdr_dtype_t dtype, gdr_stream_t stream);
 
+/* Bias-update rule of the quantile-balancing router (see gdr_router_bias_update). */
+typedef enum { GDR_QB_SIGN = 0, GDR_QB_PROPORTIONAL = 1 } gdr_qb_mode_t;
+
+/*
+ * Routing step of aux-loss-free quantile balancing ("Deep Dive: The Next
+ * Generation of Ultra-Long Context Sparse MoE LLMs", §4.2; "Core Technologies
+ * Behind Ultra-Long-Context Sparse MoE Large Models", §3.2): every token t
+ * picks the k experts of largest score logits[t, e] + bias[e], the sum taken
+ * in binary32; equal scores go to the lower expert index.  The bias only
+ * steers the selection: topk_logit returns the unbiased logits.
+ *   logits     [T, E] in dtype (bf16 or fp32), 16-byte aligned (device)
+ *   bias       [E] fp32 (device)
+ *   topk_idx   [T, k] int32, experts in descending score order (device, written)
+ *   topk_logit [T, k] fp32 logits of the picked experts, or NULL
+ *   load       [E] int64: this call's per-expert counts are ADDED (a window may
+ *              span several calls; zero it at the window start), or NULL
+ * 1 <= E <= 2048 with E % 4 == 0 and 1 <= k <= min(E, 32): GDR_ERR_UNSUPPORTED
+ * otherwise.  NaN logits or biases give an unspecified (but in-bounds)
+ * selection.  Outputs must not overlap inputs: GDR_ERR_INVALID_ARG.
+ * Asynchronous on `stream`; the counts are exact (integer atomics).
+ */
+GDR_API gdr_status_t gdr_router_topk(const void *logits, const float *bias, int32_t *topk_idx,
+                             float *topk_logit, int64_t *load, int64_t T, int E, int k,
+                             gdr_dtype_t dtype, gdr_stream_t stream);
+
+/*
+ * Bias step of quantile balancing (the four pages print it in two forms;
+ * "Core Technologies ...", §3.2, "How Trillion-Scale Sparse MoE Models Achieve
+ * Million-Token Long Context Capabilities", §4.3, "Evaluating Next-Gen Sparse
+ * MoE and Long-Context LLMs", §3.2).  Q(q) is the q-quantile of the E loads by
+ * linear interpolation between order statistics (sorted x, p = q (E - 1),
+ * i = floor p: Q = x_i + (p - i)(x_{i+1} - x_i)), in binary64.
+ *   GDR_QB_SIGN:         bias[e] -= eta if load[e] > Q(q_hi), else
+ *                        bias[e] += eta if load[e] < Q(q_lo)   (binary32 steps;
+ *                        q_lo = q_hi is the single-threshold form)
+ *   GDR_QB_PROPORTIONAL: bias[e] += eta (Q(q_hi) - load[e]) / Q(q_hi) in
+ *                        binary64, rounded to binary32; no change if Q(q_hi) = 0
+ *   load [E] int64 (device), bias [E] fp32 (device, updated in place),
+ *   thresholds [2] fp64 = {Q(q_lo), Q(q_hi)} (device, written) or NULL.
+ * 1 <= E <= 2048 (GDR_ERR_UNSUPPORTED otherwise); q_lo, q_hi in [0, 1] and eta
+ * finite (GDR_ERR_INVALID_ARG otherwise).  Asynchronous on `stream`.
+ */
+GDR_API gdr_status_t gdr_router_bias_update(const int64_t *load, float *bias, double *thresholds,
+                                    int E, gdr_qb_mode_t mode, double q_lo, double q_hi,
+                                    float eta, gdr_stream_t stream);
+
 /*
  * The backward pass: gradients of  L = <dout, out> + <dhT, hT>  with respect to
  * q, k, v, a, beta and h0, for the forward of gdr_chunk_fwd_ex on the same
