@@ -661,9 +661,14 @@ gdr_status_t gdr_chunk_fwd_vec(const void *q, const void *k, const void *v, cons
     }
     DeviceCtx *ctx = device_ctx();
     if (!ctx) return GDR_ERR_CUDA;
+    const bool fused = dtype == GDR_BF16 && dk == 128 && dv == 128;   // tensor-core kernel
     const int64_t tiles = tile_bound(s.varlen, B, T, kVecTile);
     const size_t plan_b = align_up(3 * sizeof(int64_t) * (size_t)(B + 1));
-    const size_t need = plan_b + vec_scratch_bytes(tiles, s.T_total, H, dk, dv);
+    const int seg = fused ? vec_mma_segment_tiles() : (1 << 30);
+    // segments: at most one partial segment per sequence beyond the full ones
+    const int64_t segs = s.varlen ? (tiles + seg - 1) / seg + B : (int64_t)B * ((tiles / B + seg - 1) / seg);
+    const size_t need = plan_b + (fused ? vec_mma_scratch_bytes(tiles, B, H)
+                                        : vec_scratch_bytes(tiles, s.T_total, H, dk, dv));
     char *ws;
     {
         std::lock_guard<std::mutex> lk(g_mu);
@@ -671,10 +676,15 @@ gdr_status_t gdr_chunk_fwd_vec(const void *q, const void *k, const void *v, cons
         ws = (char *)ctx->ws;
     }
     int64_t *seq_start = (int64_t *)ws;
-    Plan plan{B, kVecTile, 1 << 30, seq_start, seq_start + (B + 1), seq_start + 2 * (B + 1)};
-    if (launch_plan(cu_seqlens, B, s.T_per, s.T_total, kVecTile, 1 << 30, seq_start,
+    Plan plan{B, kVecTile, seg, seq_start, seq_start + (B + 1), seq_start + 2 * (B + 1)};
+    if (launch_plan(cu_seqlens, B, s.T_per, s.T_total, kVecTile, seg, seq_start,
                     seq_start + (B + 1), seq_start + 2 * (B + 1), ctx->d_status, stream) != cudaSuccess)
         return GDR_ERR_CUDA;
+    if (fused)
+        return launch_vec_mma(q, k, v, a, beta, h0, out, hT, plan, H, b, tiles, segs, ws + plan_b,
+                              stream) == cudaSuccess
+                   ? GDR_OK
+                   : GDR_ERR_CUDA;
     return launch_vec_forward(q, k, v, a, beta, h0, out, hT, dtype, plan, H, dk, dv, s.T_total, tiles,
                               b, ws + plan_b, stream) == cudaSuccess
                ? GDR_OK

@@ -123,6 +123,14 @@ cudaError_t launch_vec_forward(const void *q, const void *k, const void *v, cons
                                int64_t T_total, int64_t max_tiles, float b, void *scratch,
                                cudaStream_t stream);
 
+// per-channel decay, bf16 and dk = dv = 128: fused tensor-core kernel (gdr_vec_mma.cu)
+size_t vec_mma_scratch_bytes(int64_t tiles, int N, int H);
+int vec_mma_segment_tiles();
+cudaError_t launch_vec_mma(const void *q, const void *k, const void *v, const void *a,
+                           const void *beta, const float *h0, void *out, float *hT, Plan plan,
+                           int H, float b, int64_t max_tiles, int64_t max_segs, void *scratch,
+                           cudaStream_t stream);
+
 // quantile-balancing router-bias update (gdr_router.cu)
 constexpr int kRouterMaxE = 2048;
 constexpr int kRouterMaxK = 32;

@@ -1,0 +1,457 @@
+// gdr_vec_mma.cu -- per-channel decay forward, bf16 inputs, dk = dv = 128:
+// one fused kernel per (sequence, head) that keeps the 128 x 128 fp32 state in
+// shared memory and runs every dense product of a 16-token tile on the tensor
+// cores (mma.sync m16n8k8, tf32 operands, fp32 accumulation).
+//
+// Per tile, with per-channel cumulative log-decay G (resetting each tile) and
+// the factored decays Kt = K (.) exp(G), Kh = K (.) exp(-G), Qt = Q (.) exp(G)
+// [P1 §2.1-2.2, P3 §3.2]:
+//   A = beta (.) strict_lower(Kt Kh^T),  P = lower(Qt Kh^T)          (tensor cores)
+//   W = (I + A)^{-1} diag(beta) Kt,  U = (I + A)^{-1} diag(beta) V    (forward
+//        substitution, one column per thread: no explicit inverse)
+//   D = U - W H,  O = Qt H + P D                                       (tensor cores)
+//   H <- diag(exp(G_C)) H + (Kh exp(G_C))^T D                          (tensor cores)
+// Warp w owns the state columns 16w..16w+15 for D, O and the state update, so
+// those three steps need no block barrier between them; a tile takes four.
+// The next tile's inputs are loaded into registers while the current tile is
+// computed.
+//
+// Long sequences are cut into segments of kSegTiles tiles, one block per
+// (segment, head).  A block starts from a zero state at a warm-up tile w before
+// its segment and runs the state update alone up to the segment start.  The
+// state entering tile w reaches the segment start multiplied by a product of
+// (I - beta k k^T) diag(alpha_t); with beta |k|^2 in [0, 2] each factor has
+// norm <= max_d alpha_{t,d}, so the neglected term is at most
+// exp(sum_t max_d g_{t,d}) times that state.  w is the latest tile that makes
+// this bound <= 2^-64 (far below fp32 resolution), or the sequence start,
+// where the block starts from h0 exactly.  vec_bound_kernel sums
+// max_d g per (tile, head); vec_decide_kernel marks the (sequence, head)
+// pairs whose decay is too weak for a warm-up of at most kMaxWarm tiles: those
+// run as one block over the whole sequence, exactly as without segments.
+#include "gdr_internal.cuh"
+
+namespace gdr {
+namespace {
+
+constexpr int kT = 16;       // tile
+constexpr int kD = 128;      // dk = dv
+constexpr int kLd = 132;     // row stride (floats) of 128-wide shared matrices
+constexpr int kPd = 20;      // row stride of 16 x 16 shared matrices
+constexpr int kThreads = 256;
+constexpr int kSegTiles = 64;          // tiles per segment
+constexpr int kMaxWarm = 4 * kSegTiles;  // longest warm-up before a pair runs unsegmented
+constexpr float kHorizonLog = -46.0f;    // below ln(2^-64) = -44.4, with room for fp32 sums
+
+// shared layout, in floats
+constexpr int kOffH = 0;                      // H   [128][kLd]
+constexpr int kOffKt = kOffH + kD * kLd;      // Kt, then -W   [16][kLd]
+constexpr int kOffKh = kOffKt + kT * kLd;     // Kh, then Kh exp(G_C)
+constexpr int kOffQt = kOffKh + kT * kLd;     // Qt
+constexpr int kOffU = kOffQt + kT * kLd;      // V, then U, then D
+constexpr int kOffA = kOffU + kT * kLd;       // A [16][kPd]
+constexpr int kOffP = kOffA + kT * kPd;       // P [16][kPd]
+constexpr int kOffEg = kOffP + kT * kPd;      // exp(G_C) [128]
+constexpr int kOffB = kOffEg + kD;            // beta [16]
+constexpr int kSmemFloats = kOffB + kT;
+constexpr size_t kSmemBytes = sizeof(float) * kSmemFloats;
+
+__device__ __forceinline__ uint32_t tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// d += a * b, m16n8k8, tf32 inputs, fp32 accumulators
+__device__ __forceinline__ void mma8(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// A fragment of rows r0..r0+15, columns k0..k0+7 of a row-major matrix
+__device__ __forceinline__ void load_a(uint32_t (&a)[4], const float *M, int ld, int r0, int k0,
+                                       int g, int t) {
+    a[0] = tf32(M[(r0 + g) * ld + k0 + t]);
+    a[1] = tf32(M[(r0 + g + 8) * ld + k0 + t]);
+    a[2] = tf32(M[(r0 + g) * ld + k0 + t + 4]);
+    a[3] = tf32(M[(r0 + g + 8) * ld + k0 + t + 4]);
+}
+
+// Per (tile, head): the log of a bound on the norm of the tile's transition,
+// sum over its tokens of  max_d g_{t,d} + ln max(1, |1 - beta_t |k_t|^2|),
+// with max_d g = -b sigmoid(min_d a) (the gate is decreasing in a).
+__global__ void __launch_bounds__(128)
+vec_bound_kernel(const __nv_bfloat16 *__restrict__ a, const __nv_bfloat16 *__restrict__ k,
+                 const __nv_bfloat16 *__restrict__ beta, float *__restrict__ lam, Plan p, int H,
+                 float b) {
+    __shared__ float red[2][4][kT];
+    const int64_t c = blockIdx.x;
+    const int h = blockIdx.y;
+    const int n = find_owner(p.chunk_base, p.N, c);
+    if (n < 0) return;
+    const int64_t t0 = p.seq_start[n] + (c - p.chunk_base[n]) * kT;
+    const int len = (int)min((int64_t)kT, p.seq_start[n + 1] - t0);
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+#pragma unroll 4
+    for (int i = 0; i < kT; ++i) {
+        float m = 3.0e38f, kk = 0.f;
+        if (i < len) {
+            const int64_t r = ((t0 + i) * H + h) * kD + tid;
+            m = __bfloat162float(a[r]);
+            const float kd = __bfloat162float(k[r]);
+            kk = kd * kd;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            m = fminf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            kk += __shfl_xor_sync(0xffffffffu, kk, o);
+        }
+        if (lane == 0) {
+            red[0][w][i] = m;
+            red[1][w][i] = kk;
+        }
+    }
+    __syncthreads();
+    if (tid < 32) {
+        float x = 0.f;
+        if (tid < len) {
+            const float m = fminf(fminf(red[0][0][tid], red[0][1][tid]), fminf(red[0][2][tid], red[0][3][tid]));
+            const float kk = red[1][0][tid] + red[1][1][tid] + red[1][2][tid] + red[1][3][tid];
+            const float bt = __bfloat162float(beta[(t0 + tid) * H + h]);
+            x = gate_logdecay(m, b, GDR_GATE_BOUNDED) + logf(fmaxf(1.f, fabsf(1.f - bt * kk)));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        if (tid == 0) lam[c * H + h] = x;
+    }
+}
+
+// Per (sequence, head): 1 if every segment start has a bound <= 2^-64 within
+// kMaxWarm tiles before it (or the sequence start within reach), else 0.
+__global__ void __launch_bounds__(32)
+vec_decide_kernel(const float *__restrict__ lam, int *__restrict__ ok, Plan p, int H) {
+    const int h = blockIdx.x % H, n = blockIdx.x / H;
+    const int lane = threadIdx.x;
+    const int64_t base = p.chunk_base[n], nt = p.chunk_base[n + 1] - base;
+    int good = 1;
+    for (int64_t s0 = kSegTiles; s0 < nt && good; s0 += kSegTiles) {
+        if (s0 <= kMaxWarm) continue;   // the warm-up can always reach the sequence start
+        float acc = 0.f;
+        for (int i = lane; i < kMaxWarm; i += 32) acc += lam[(base + s0 - 1 - i) * H + h];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        good = acc <= kHorizonLog;
+    }
+    if (lane == 0) ok[(int64_t)n * H + h] = good;
+}
+
+__global__ void __launch_bounds__(kThreads)
+vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+               const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ a,
+               const __nv_bfloat16 *__restrict__ beta, const float *__restrict__ h0,
+               __nv_bfloat16 *__restrict__ out, float *__restrict__ hT, Plan p, int H, float b,
+               const float *__restrict__ lam, const int *__restrict__ seg_ok) {
+    extern __shared__ float sm[];
+    float *Hs = sm + kOffH, *Kt = sm + kOffKt, *Kh = sm + kOffKh, *Qt = sm + kOffQt;
+    float *Ub = sm + kOffU, *Am = sm + kOffA, *Pm = sm + kOffP, *eg = sm + kOffEg, *bs = sm + kOffB;
+    __shared__ int warm_start;
+    const int h = blockIdx.x % H;
+    const int64_t sg = blockIdx.x / H;   // global segment
+    const int n = find_owner(p.seg_base, p.N, sg);
+    if (n < 0) return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int c0 = 16 * warp;   // this warp's 16 state columns
+    const int64_t tile0 = p.chunk_base[n], ntiles = p.chunk_base[n + 1] - tile0;
+    const int64_t j = sg - p.seg_base[n];
+    const bool segmented = seg_ok[(int64_t)n * H + h] != 0;
+    if (!segmented && j > 0) return;   // one block runs the whole sequence
+    const int64_t s0 = segmented ? j * kSegTiles : 0;
+    const int64_t s1 = segmented ? min(ntiles, s0 + kSegTiles) : ntiles;
+    // warm-up start: the latest tile w <= s0 whose bound to s0 is <= 2^-64
+    if (warp == 0) {
+        int64_t w = s0;
+        float acc = 0.f;
+        bool done = s0 == 0;
+        while (!done) {
+            const int64_t i = w - 1 - lane;
+            float x = i >= 0 ? lam[(tile0 + i) * H + h] : 0.f;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, i >= 0 && acc + x <= kHorizonLog);
+            if (hit) {
+                w = w - 1 - (__ffs(hit) - 1);
+                done = true;
+            } else {
+                acc += __shfl_sync(0xffffffffu, x, 31);
+                w = max(w - 32, (int64_t)0);
+                done = w == 0;
+            }
+        }
+        if (lane == 0) warm_start = (int)(s0 - w);
+    }
+    __syncthreads();
+    const int64_t w0 = s0 - warm_start;   // first tile run
+    const size_t hbase = ((size_t)n * H + h) * kD * kD;
+    const bool from_h0 = w0 == 0 && h0;
+    for (int e = tid; e < kD * kD; e += kThreads) {
+        const int r = e >> 7, c = e & (kD - 1);
+        Hs[r * kLd + c] = from_h0 ? h0[hbase + e] : 0.f;
+    }
+    const int64_t sstart = p.seq_start[n], e_end = p.seq_start[n + 1];
+    // registers holding the next tile's inputs
+    __nv_bfloat16 ra[kT], rk[kT], rq[kT];
+    float rb = 0.f;
+    auto fetch = [&](int64_t tt) {
+        const int64_t t0 = sstart + tt * kT;
+        const int len = tt < s1 ? (int)min((int64_t)kT, e_end - t0) : 0;
+        if (tid < kD) {
+#pragma unroll
+            for (int i = 0; i < kT; ++i)
+                if (i < len) {
+                    const int64_t r = ((t0 + i) * H + h) * kD + tid;
+                    ra[i] = a[r];
+                    rk[i] = k[r];
+                    rq[i] = q[r];
+                }
+        } else {
+            const int c = tid - kD;
+#pragma unroll
+            for (int i = 0; i < kT; ++i)
+                if (i < len) ra[i] = v[((t0 + i) * H + h) * kD + c];
+            if (c < len) rb = __bfloat162float(beta[(t0 + c) * H + h]);
+        }
+    };
+    fetch(w0);
+    for (int64_t tt = w0; tt < s1; ++tt) {
+        const int64_t t0 = sstart + tt * kT;
+        const int len = (int)min((int64_t)kT, e_end - t0);
+        const bool emit = tt >= s0;   // warm-up tiles only advance the state
+        __syncthreads();   // the previous tile is done with every staging buffer
+        // ---- stage the tile: factored decays per key channel, V and beta
+        if (tid < kD) {
+            const int d = tid;
+            float G = 0.f, eGC = 1.f;
+#pragma unroll
+            for (int i = 0; i < kT; ++i) {
+                float kt = 0.f, kh = 0.f, qt = 0.f;
+                if (i < len) {
+                    G += gate_logdecay(__bfloat162float(ra[i]), b, GDR_GATE_BOUNDED);
+                    const float e = expf(G), en = expf(-G), kd = __bfloat162float(rk[i]);
+                    kt = kd * e;
+                    kh = kd * en;
+                    qt = __bfloat162float(rq[i]) * e;
+                    eGC = e;
+                }
+                Kt[i * kLd + d] = kt;
+                Kh[i * kLd + d] = kh;
+                Qt[i * kLd + d] = qt;
+            }
+            eg[d] = eGC;
+        } else {
+            const int c = tid - kD;
+#pragma unroll
+            for (int i = 0; i < kT; ++i) Ub[i * kLd + c] = i < len ? __bfloat162float(ra[i]) : 0.f;
+            if (c < kT) bs[c] = c < len ? rb : 0.f;
+        }
+        __syncthreads();
+        fetch(tt + 1);   // in flight while this tile is computed
+        // ---- A = beta (.) strict_lower(Kt Kh^T) and P = lower(Qt Kh^T): warps 0-3
+        if (warp < 4) {
+            const float *Aop = (warp < 2) ? Kt : Qt;
+            const int j0 = 8 * (warp & 1);
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+            for (int k0 = 0; k0 < kD; k0 += 8) {
+                uint32_t af[4];
+                load_a(af, Aop, kLd, 0, k0, g, t);
+                mma8(acc, af, tf32(Kh[(j0 + g) * kLd + k0 + t]), tf32(Kh[(j0 + g) * kLd + k0 + t + 4]));
+            }
+            const int i0 = g, i1 = g + 8, ja = j0 + 2 * t, jb = ja + 1;
+            if (warp < 2) {
+                Am[i0 * kPd + ja] = ja < i0 ? bs[i0] * acc[0] : 0.f;
+                Am[i0 * kPd + jb] = jb < i0 ? bs[i0] * acc[1] : 0.f;
+                Am[i1 * kPd + ja] = ja < i1 ? bs[i1] * acc[2] : 0.f;
+                Am[i1 * kPd + jb] = jb < i1 ? bs[i1] * acc[3] : 0.f;
+            } else {
+                Pm[i0 * kPd + ja] = ja <= i0 ? acc[0] : 0.f;
+                Pm[i0 * kPd + jb] = jb <= i0 ? acc[1] : 0.f;
+                Pm[i1 * kPd + ja] = ja <= i1 ? acc[2] : 0.f;
+                Pm[i1 * kPd + jb] = jb <= i1 ? acc[3] : 0.f;
+            }
+        }
+        __syncthreads();
+        // ---- W and U by forward substitution, one column per thread
+        {
+            const int col = tid & (kD - 1);
+            float *X = tid < kD ? Kt : Ub;   // Kt -> -W, V -> U
+            float x[kT];
+#pragma unroll
+            for (int i = 0; i < kT; ++i) {
+                float acc = bs[i] * X[i * kLd + col];
+#pragma unroll
+                for (int j = 0; j < i; ++j) acc = fmaf(-Am[i * kPd + j], x[j], acc);
+                x[i] = acc;
+            }
+            if (tid < kD) {
+                const float egc = eg[col];
+#pragma unroll
+                for (int i = 0; i < kT; ++i) {
+                    X[i * kLd + col] = -x[i];
+                    Kh[i * kLd + col] *= egc;   // Kh exp(G_C) = K exp(G_C - G)
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < kT; ++i) X[i * kLd + col] = x[i];
+            }
+        }
+        __syncthreads();
+        // ---- D = U - W H and O = Qt H on this warp's 16 columns
+        float dacc[2][4], oacc[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int n0 = c0 + 8 * nt;
+            dacc[nt][0] = Ub[g * kLd + n0 + 2 * t];
+            dacc[nt][1] = Ub[g * kLd + n0 + 2 * t + 1];
+            dacc[nt][2] = Ub[(g + 8) * kLd + n0 + 2 * t];
+            dacc[nt][3] = Ub[(g + 8) * kLd + n0 + 2 * t + 1];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) oacc[nt][u] = 0.f;
+        }
+#pragma unroll 2
+        for (int k0 = 0; k0 < kD; k0 += 8) {
+            uint32_t aw[4], aq[4];
+            load_a(aw, Kt, kLd, 0, k0, g, t);
+            load_a(aq, Qt, kLd, 0, k0, g, t);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int n0 = c0 + 8 * nt;
+                const uint32_t b0 = tf32(Hs[(k0 + t) * kLd + n0 + g]);
+                const uint32_t b1 = tf32(Hs[(k0 + t + 4) * kLd + n0 + g]);
+                mma8(dacc[nt], aw, b0, b1);
+                mma8(oacc[nt], aq, b0, b1);
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int n0 = c0 + 8 * nt;
+            Ub[g * kLd + n0 + 2 * t] = dacc[nt][0];
+            Ub[g * kLd + n0 + 2 * t + 1] = dacc[nt][1];
+            Ub[(g + 8) * kLd + n0 + 2 * t] = dacc[nt][2];
+            Ub[(g + 8) * kLd + n0 + 2 * t + 1] = dacc[nt][3];
+        }
+        __syncwarp();
+        // ---- O += P D, then the outputs
+        uint32_t bd[2][2][2];   // D fragments [k-step][n-tile][2]
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int n0 = c0 + 8 * nt;
+                bd[ks][nt][0] = tf32(Ub[(8 * ks + t) * kLd + n0 + g]);
+                bd[ks][nt][1] = tf32(Ub[(8 * ks + t + 4) * kLd + n0 + g]);
+            }
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            uint32_t ap[4];
+            load_a(ap, Pm, kPd, 0, 8 * ks, g, t);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) mma8(oacc[nt], ap, bd[ks][nt][0], bd[ks][nt][1]);
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int col = c0 + 8 * nt + 2 * t;
+            if (!emit) break;
+            if (g < len)
+                *(__nv_bfloat162 *)&out[((t0 + g) * H + h) * kD + col] =
+                    __floats2bfloat162_rn(oacc[nt][0], oacc[nt][1]);
+            if (g + 8 < len)
+                *(__nv_bfloat162 *)&out[((t0 + g + 8) * H + h) * kD + col] =
+                    __floats2bfloat162_rn(oacc[nt][2], oacc[nt][3]);
+        }
+        // ---- H <- diag(exp(G_C)) H + (Kh exp(G_C))^T D on this warp's columns
+#pragma unroll 2
+        for (int mt = 0; mt < kD / 16; ++mt) {
+            const int r0 = 16 * mt;
+            const float e0 = eg[r0 + g], e1 = eg[r0 + g + 8];
+            uint32_t ak[2][4];
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const int k0 = 8 * ks;
+                ak[ks][0] = tf32(Kh[(k0 + t) * kLd + r0 + g]);
+                ak[ks][1] = tf32(Kh[(k0 + t) * kLd + r0 + g + 8]);
+                ak[ks][2] = tf32(Kh[(k0 + t + 4) * kLd + r0 + g]);
+                ak[ks][3] = tf32(Kh[(k0 + t + 4) * kLd + r0 + g + 8]);
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int col = c0 + 8 * nt + 2 * t;
+                float *h0p = &Hs[(r0 + g) * kLd + col], *h1p = &Hs[(r0 + g + 8) * kLd + col];
+                float acc[4] = {e0 * h0p[0], e0 * h0p[1], e1 * h1p[0], e1 * h1p[1]};
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) mma8(acc, ak[ks], bd[ks][nt][0], bd[ks][nt][1]);
+                h0p[0] = acc[0];
+                h0p[1] = acc[1];
+                h1p[0] = acc[2];
+                h1p[1] = acc[3];
+            }
+        }
+    }
+    __syncthreads();
+    if (hT && s1 == ntiles)
+        for (int e = tid; e < kD * kD; e += kThreads) {
+            const int r = e >> 7, c = e & (kD - 1);
+            hT[hbase + e] = Hs[r * kLd + c];
+        }
+}
+
+}  // namespace
+
+size_t vec_mma_scratch_bytes(int64_t tiles, int N, int H) {
+    return sizeof(float) * (size_t)tiles * H + sizeof(int) * (size_t)N * H + 2 * 256;
+}
+
+int vec_mma_segment_tiles() { return kSegTiles; }
+
+cudaError_t launch_vec_mma(const void *q, const void *k, const void *v, const void *a,
+                           const void *beta, const float *h0, void *out, float *hT, Plan plan,
+                           int H, float b, int64_t max_tiles, int64_t max_segs, void *scratch,
+                           cudaStream_t stream) {
+    if (plan.C != kT || plan.seg_chunks != kSegTiles) return cudaErrorInvalidValue;
+    float *lam = (float *)scratch;
+    int *ok = (int *)((char *)scratch + (sizeof(float) * (size_t)max_tiles * H + 255) / 256 * 256);
+    cudaError_t err;
+    if (max_tiles > 0) {
+        ProfScope prof(stream, "vec_bound_kernel");
+        vec_bound_kernel<<<dim3((unsigned)max_tiles, (unsigned)H), 128, 0, stream>>>(
+            (const __nv_bfloat16 *)a, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)beta, lam,
+            plan, H, b);
+        count_launch();
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    {
+        ProfScope prof(stream, "vec_decide_kernel");
+        vec_decide_kernel<<<(unsigned)((int64_t)plan.N * H), 32, 0, stream>>>(lam, ok, plan, H);
+        count_launch();
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    err = cudaFuncSetAttribute(vec_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kSmemBytes);
+    if (err != cudaSuccess) return err;
+    const int64_t blocks = max_segs * H;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+    ProfScope prof(stream, "vec_mma_kernel");
+    vec_mma_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(
+        (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v,
+        (const __nv_bfloat16 *)a, (const __nv_bfloat16 *)beta, h0, (__nv_bfloat16 *)out, hT, plan,
+        H, b, lam, ok);
+    count_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace gdr

@@ -25,11 +25,11 @@ def _built():
     torch.cuda.set_device(0)
 
 
-def _inputs(dtype, d, T, seed, N=2, H=3, h0=True, b=2.0, a_std=1.0, varlen=False):
+def _inputs(dtype, d, T, seed, N=2, H=3, h0=True, b=2.0, a_std=1.0, varlen=False, a_mean=0.0):
     w = WORKLOADS["b2_t4k"].with_(B=N, H=H, dk=d, dv=d, dtype=dtype, h0_std=0.05 if h0 else 0.0,
                                   seed=seed, b=b, varlen=varlen, len_min=1, len_max=max(1, T // 3))
     x = make_inputs(w, device="cuda", T=T)
-    x["av"] = make_channel_gate(x, seed + 7, a_std=a_std)
+    x["av"] = make_channel_gate(x, seed + 7, a_std=a_std, a_mean=a_mean)
     return x
 
 
@@ -95,3 +95,32 @@ def test_vec_zero_tokens_and_bad_args():
     bad = list(args)
     bad[6] = x["av"]   # out on top of a
     assert gdr.gdr_chunk_fwd_vec(*bad, 16, 2.0, gdr.GDR_BF16) == gdr.GDR_ERR_INVALID_ARG
+
+
+def test_vec_long_sequences_run_in_segments():
+    """3000 tokens = 188 tiles: three 64-tile segments, the later two started from
+    a zero state at a warm-up tile where the decay bound is below 2^-64."""
+    _check(_inputs("bf16", 128, 3000, seed=5500, N=1, H=2), "bf16")
+
+
+def test_vec_weak_decay_runs_unsegmented():
+    """a ~ N(-6, 1) per channel: the weakest channel decays by about 1 - 0.005 per
+    token, so no warm-up within 256 tiles reaches 2^-64 and the pair runs as one
+    block from h0 (5000 tokens = 313 tiles)."""
+    _check(_inputs("bf16", 128, 5000, seed=5600, N=1, H=2, a_mean=-6.0), "bf16")
+
+
+def test_vec_unnormalised_keys_lengthen_the_warm_up():
+    """|k| = 2: each token's erase factor I - beta k k^T can stretch the state by
+    |1 - 4 beta|, which the warm-up bound includes."""
+    x = _inputs("bf16", 128, 2500, seed=5700, N=1, H=2)
+    x["k"] = (2.0 * x["k"].float()).to(torch.bfloat16)
+    _check(x, "bf16")
+
+
+def test_vec_packed_long_and_short_sequences():
+    x = _inputs("bf16", 128, 6000, seed=5800, N=1, H=2, varlen=True)
+    x["cu_seqlens"] = torch.tensor([0, 7, 7, 2100, 2116, 6000], dtype=torch.int32, device="cuda")
+    g = torch.Generator(device="cpu").manual_seed(5801)
+    x["h0"] = (0.05 * torch.randn((5, 2, 128, 128), generator=g)).cuda()
+    _check(x, "bf16")
