@@ -442,10 +442,12 @@ def bench_decode(args):
 
 def bench_backward(args):
     """The backward pass (gdr_chunk_bwd) of N sequences x 16 heads x T tokens, d = 128,
-    bf16, with h0, dout and dhT given.  It runs in fp32 on the SIMT pipes; its
-    algorithmic work is 20 dk dv flops per (token, head): the forward recomputed
-    (p and the state update) and the adjoint recurrence (dH, dq, ddelta, dk, dHb,
-    dalpha and the decay of dH)."""
+    bf16, with h0, dout and dhT given: the chunked form on the tensor cores (tf32
+    operands).  Its algorithmic work is counted as 20 dk dv flops per (token, head):
+    the forward recomputed (prediction and state update) and the adjoint recurrence
+    (dH, dq, ddelta, dk, dHb, dalpha and the decay of dH).  The roofline takes the
+    whole step against the tf32 tensor rate (the measured bf16 rate x 1/2, the
+    nominal tf32 : bf16 ratio)."""
     import torch
     import chunked_gated_delta_07_gb300 as gdr
     from gdr_inputs import WORKLOADS, make_inputs
@@ -486,13 +488,12 @@ def bench_backward(args):
     if st != gdr.GDR_OK:
         raise gdr.GdrError(st, "device status after backward")
     ms = ev0.elapsed_time(ev1) / steps
-    dom_ms, dom_n = prof.get("bwd_slice_kernel", (0.0, 1))
-    kern_ms = dom_ms / max(dom_n, 1)
+    dom_name, (dom_ms, dom_n) = max(prof.items(), key=lambda kv: kv[1][0]) if prof else ("?", (0.0, 1))
     flops = 20.0 * d * d * N * T * H
     summ = clk.summary() or {}
-    mhz = float(summ.get("sm_max_mhz") or 2070.0)
-    peak = 152 * 128 * 2 * mhz * 1e6 / 1e12   # fp32 FMA lanes x 2 flops x max SM clock
-    achieved = flops / (kern_ms / 1e3) / 1e12 if kern_ms > 0 else 0.0
+    _, bf16_tf, _, peak_src = peaks()
+    peak = bf16_tf / 2.0
+    achieved = flops / (ms / 1e3) / 1e12
     print(json.dumps({
         "metric": "backward tokens/s, gated delta rule, 16 heads, d=128, bf16 in/out, fp32 math",
         "value": N * T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": steps,
@@ -500,10 +501,11 @@ def bench_backward(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"backward: N={N} sequences x T={T} x H={H}, dk=dv={d}",
                    "l2_policy": "no flush; the per-step inputs and scratch exceed L2"},
-        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None, "kernel": "bwd_slice_kernel",
-                     "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x max SM clock",
-                     "algorithmic_flops_per_step": flops, "kernel_ms": kern_ms},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None, "kernel": "whole step",
+                     "peak_source": f"{peak_src} bf16_tflops x 0.5 (tf32)",
+                     "algorithmic_flops_per_step": flops, "dominant_kernel": dom_name,
+                     "dominant_share": dom_ms / sum(v[0] for v in prof.values()) if prof else None},
         "kernels": {k: {"ms_total": v[0], "launches": v[1]} for k, v in prof.items()},
         "gpu_launches": n_launch, "clocks": summ or None,
     }), flush=True)

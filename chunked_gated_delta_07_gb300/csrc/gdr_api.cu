@@ -3,6 +3,7 @@
 // lives here; every step of the pass runs in the kernels.
 #include <atomic>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -583,6 +584,13 @@ gdr_status_t gdr_recurrent_fwd(const void *q, const void *k, const void *v, cons
                : GDR_ERR_CUDA;
 }
 
+// GDR_BWD_TOKEN=1 sends every backward call to the token-by-token kernels (the
+// parity tests compare the two forms).
+static bool bwd_force_token_path() {
+    const char *e = std::getenv("GDR_BWD_TOKEN");
+    return e && e[0] == '1';
+}
+
 gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const void *a,
                            const void *beta, const float *h0, const void *dout,
                            const float *dhT, void *dq, void *dk_out, void *dv_out, void *da,
@@ -618,7 +626,12 @@ gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const vo
     if (!ctx) return GDR_ERR_CUDA;
     const int64_t tiles = tile_bound(s.varlen, B, s.varlen ? T : s.T_per, kBwTile);
     const size_t plan_b = align_up(3 * sizeof(int64_t) * (size_t)(B + 1));
-    const size_t need = plan_b + bwd_scratch_bytes(tiles, s.T_total, H, dk, dv);
+    // the chunked tensor-core form takes bf16, d = 128 and the bounded gate (its
+    // factored in-tile decays need exp(16 b) < FLT_MAX); the rest runs token by token
+    const bool chunked = dtype == GDR_BF16 && dk == 128 && dv == 128 && gate == GDR_GATE_BOUNDED &&
+                         b <= kVecMaxB && !bwd_force_token_path();
+    const size_t need = plan_b + (chunked ? chunk_bwd_scratch_bytes(tiles, H)
+                                          : bwd_scratch_bytes(tiles, s.T_total, H, dk, dv));
     char *ws;
     {
         std::lock_guard<std::mutex> lk(g_mu);
@@ -631,6 +644,11 @@ gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const vo
     if (launch_plan(cu_seqlens, B, s.T_per, s.T_total, kBwTile, 1 << 30, seq_start, seq_start + (B + 1),
                     seq_start + 2 * (B + 1), ctx->d_status, stream) != cudaSuccess)
         return GDR_ERR_CUDA;
+    if (chunked)
+        return launch_chunk_bwd(q, k, v, a, beta, h0, dout, dhT, dq, dk_out, dv_out, da, dbeta, dh0,
+                                plan, H, tiles, b, false, ws + plan_b, stream) == cudaSuccess
+                   ? GDR_OK
+                   : GDR_ERR_CUDA;
     return launch_bwd(q, k, v, a, beta, h0, dout, dhT, dq, dk_out, dv_out, da, dbeta, dh0, dtype,
                       plan, H, dk, dv, s.T_total, tiles, b, gate, ws + plan_b, stream) == cudaSuccess
                ? GDR_OK

@@ -1,0 +1,61 @@
+// gdr_mma.cuh -- warp-level tensor-core helpers (mma.sync m16n8k8, tf32 inputs,
+// fp32 accumulators) shared by the fused per-tile kernels.
+//
+// Fragment layout of m16n8k8 with g = lane / 4 and t = lane % 4:
+//   A (16 x 8, row major): a0 = A[g][t], a1 = A[g+8][t], a2 = A[g][t+4], a3 = A[g+8][t+4]
+//   B (8 x 8):             b0 = B[t][g], b1 = B[t+4][g]
+//   C (16 x 8):            c0 = C[g][2t], c1 = C[g][2t+1], c2 = C[g+8][2t], c3 = C[g+8][2t+1]
+#pragma once
+
+#include <cstdint>
+
+namespace gdr {
+
+__device__ __forceinline__ uint32_t tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// d += a * b
+__device__ __forceinline__ void mma8(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// A fragment: rows r0..r0+15, columns k0..k0+7 of a row-major matrix M (stride ld)
+__device__ __forceinline__ void load_a(uint32_t (&a)[4], const float *M, int ld, int r0, int k0,
+                                       int g, int t) {
+    a[0] = tf32(M[(r0 + g) * ld + k0 + t]);
+    a[1] = tf32(M[(r0 + g + 8) * ld + k0 + t]);
+    a[2] = tf32(M[(r0 + g) * ld + k0 + t + 4]);
+    a[3] = tf32(M[(r0 + g + 8) * ld + k0 + t + 4]);
+}
+
+// A fragment of the transpose: A = M^T, i.e. A[r][k] = M[k][r]
+__device__ __forceinline__ void load_at(uint32_t (&a)[4], const float *M, int ld, int r0, int k0,
+                                        int g, int t) {
+    a[0] = tf32(M[(k0 + t) * ld + r0 + g]);
+    a[1] = tf32(M[(k0 + t) * ld + r0 + g + 8]);
+    a[2] = tf32(M[(k0 + t + 4) * ld + r0 + g]);
+    a[3] = tf32(M[(k0 + t + 4) * ld + r0 + g + 8]);
+}
+
+// B fragment: B[k][n] = M[k][n] (row-major K x N), k0..k0+7, n0..n0+7
+__device__ __forceinline__ void load_b(uint32_t &b0, uint32_t &b1, const float *M, int ld, int k0,
+                                       int n0, int g, int t) {
+    b0 = tf32(M[(k0 + t) * ld + n0 + g]);
+    b1 = tf32(M[(k0 + t + 4) * ld + n0 + g]);
+}
+
+// B fragment of the transpose: B[k][n] = M[n][k]
+__device__ __forceinline__ void load_bt(uint32_t &b0, uint32_t &b1, const float *M, int ld, int k0,
+                                        int n0, int g, int t) {
+    b0 = tf32(M[(n0 + g) * ld + k0 + t]);
+    b1 = tf32(M[(n0 + g) * ld + k0 + t + 4]);
+}
+
+}  // namespace gdr

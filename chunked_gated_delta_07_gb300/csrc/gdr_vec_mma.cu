@@ -29,6 +29,7 @@
 // pairs whose decay is too weak for a warm-up of at most kMaxWarm tiles: those
 // run as one block over the whole sequence, exactly as without segments.
 #include "gdr_internal.cuh"
+#include "gdr_mma.cuh"
 
 namespace gdr {
 namespace {
@@ -54,30 +55,6 @@ constexpr int kOffEg = kOffP + kT * kPd;      // exp(G_C) [128]
 constexpr int kOffB = kOffEg + kD;            // beta [16]
 constexpr int kSmemFloats = kOffB + kT;
 constexpr size_t kSmemBytes = sizeof(float) * kSmemFloats;
-
-__device__ __forceinline__ uint32_t tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
-// d += a * b, m16n8k8, tf32 inputs, fp32 accumulators
-__device__ __forceinline__ void mma8(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// A fragment of rows r0..r0+15, columns k0..k0+7 of a row-major matrix
-__device__ __forceinline__ void load_a(uint32_t (&a)[4], const float *M, int ld, int r0, int k0,
-                                       int g, int t) {
-    a[0] = tf32(M[(r0 + g) * ld + k0 + t]);
-    a[1] = tf32(M[(r0 + g + 8) * ld + k0 + t]);
-    a[2] = tf32(M[(r0 + g) * ld + k0 + t + 4]);
-    a[3] = tf32(M[(r0 + g + 8) * ld + k0 + t + 4]);
-}
 
 // Per (tile, head): the log of a bound on the norm of the tile's transition,
 // sum over its tokens of  max_d g_{t,d} + ln max(1, |1 - beta_t |k_t|^2|),

@@ -129,3 +129,25 @@ def test_backward_zero_tokens_and_bad_args():
     aliased = [x["q"]] + outs[1:]   # dq on top of q
     assert gdr.gdr_chunk_bwd(*base, *aliased, None, None, 2, 1, 3, 128, 128, 16, 2.0,
                              gdr.GDR_BF16, gdr.GDR_GATE_BOUNDED) == gdr.GDR_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("T,N,H,h0", [(300, 2, 2, True), (1000, 1, 2, False), (17, 3, 4, True)])
+def test_chunked_backward_matches_oracle(T, N, H, h0):
+    """bf16, d = 128, bounded gate: the chunked tensor-core form (forward state chain,
+    adjoint chain, per-tile gradients), over many tiles and a ragged tail."""
+    x = _inputs("bf16", 128, T, "bounded", seed=4600 + T, N=N, H=H, h0=h0)
+    got, ref = _run(x, "bounded", h0=h0)
+    _check(got, ref, "bf16")
+
+
+def test_chunked_and_token_forms_agree(monkeypatch):
+    """The same bf16 call through the chunked form and the token-by-token form."""
+    x = _inputs("bf16", 128, 200, "bounded", seed=4700)
+    chunked, ref = _run(x, "bounded")
+    monkeypatch.setenv("GDR_BWD_TOKEN", "1")
+    token, _ = _run(x, "bounded")
+    for name in NAMES:
+        r = rel_l2(to64(chunked[name]), to64(token[name]))
+        assert r <= 1e-2, f"{name}: chunked vs token rel-L2 {r:.3e}"
+    _check(chunked, ref, "bf16")
+    _check(token, ref, "bf16")
