@@ -630,7 +630,9 @@ gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const vo
     // factored in-tile decays need exp(16 b) < FLT_MAX); the rest runs token by token
     const bool chunked = dtype == GDR_BF16 && dk == 128 && dv == 128 && gate == GDR_GATE_BOUNDED &&
                          b <= kVecMaxB && !bwd_force_token_path();
-    const size_t need = plan_b + (chunked ? chunk_bwd_scratch_bytes(tiles, H)
+    const int seg = chunked ? chunk_bwd_segment_tiles() : (1 << 30);
+    const int64_t segs = s.varlen ? (tiles + seg - 1) / seg + B : (int64_t)B * ((tiles / B + seg - 1) / seg);
+    const size_t need = plan_b + (chunked ? chunk_bwd_scratch_bytes(tiles, B, H)
                                           : bwd_scratch_bytes(tiles, s.T_total, H, dk, dv));
     char *ws;
     {
@@ -640,13 +642,13 @@ gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const vo
     }
     cudaStream_t stream = (cudaStream_t)stream_;
     int64_t *seq_start = (int64_t *)ws;
-    Plan plan{B, kBwTile, 1 << 30, seq_start, seq_start + (B + 1), seq_start + 2 * (B + 1)};
-    if (launch_plan(cu_seqlens, B, s.T_per, s.T_total, kBwTile, 1 << 30, seq_start, seq_start + (B + 1),
+    Plan plan{B, kBwTile, seg, seq_start, seq_start + (B + 1), seq_start + 2 * (B + 1)};
+    if (launch_plan(cu_seqlens, B, s.T_per, s.T_total, kBwTile, seg, seq_start, seq_start + (B + 1),
                     seq_start + 2 * (B + 1), ctx->d_status, stream) != cudaSuccess)
         return GDR_ERR_CUDA;
     if (chunked)
         return launch_chunk_bwd(q, k, v, a, beta, h0, dout, dhT, dq, dk_out, dv_out, da, dbeta, dh0,
-                                plan, H, tiles, b, false, ws + plan_b, stream) == cudaSuccess
+                                plan, H, tiles, segs, b, false, ws + plan_b, stream) == cudaSuccess
                    ? GDR_OK
                    : GDR_ERR_CUDA;
     return launch_bwd(q, k, v, a, beta, h0, dout, dhT, dq, dk_out, dv_out, da, dbeta, dh0, dtype,

@@ -25,6 +25,16 @@
 //                         dH1 of every tile and writes dh0
 //   bwd_tile_kernel       per (tile, head), all tiles at once: every input gradient
 // The scalar-gate form is the per-channel form with every channel's gate equal.
+//
+// The two chains run in 64-tile segments, one block per (segment, head), each
+// started at a warm-up tile whose neglected transition is provably below 2^-64:
+// the forward chain from a zero state some tiles before its segment, the adjoint
+// chain from a zero gradient some tiles after it.  Both transitions have norm at
+// most prod_t max(1, |1 - beta_t |k_t|^2|) max_d alpha_{t,d} (the adjoint one is
+// the transpose), summed in log form per tile by bwd_bound_kernel.  A (sequence,
+// head) pair without such a warm-up within kMaxWarm tiles of every segment
+// boundary runs as one block, as without segments (bwd_decide_kernel).
+// The stored states are bf16 (they only feed the per-tile products).
 #include "gdr_internal.cuh"
 #include "gdr_mma.cuh"
 
@@ -37,13 +47,20 @@ constexpr int kLd = 132;
 constexpr int kPd = 20;
 constexpr int kThreads = 256;
 constexpr int kTile2 = kT * kLd;   // floats of one [16][kLd] buffer
+constexpr int kSegTiles = 64;
+constexpr int kMaxWarm = 4 * kSegTiles;
+constexpr float kHorizonLog = -46.0f;   // below ln(2^-64) = -44.4, with room for fp32 sums
+constexpr int kLdh = 136;               // row stride (elements) of the bf16 state in shared memory
 
 struct BcArgs {
     const __nv_bfloat16 *q, *k, *v, *a, *beta, *dout;
     const float *h0, *dhT;
     __nv_bfloat16 *dq, *dk, *dv, *da, *dbeta;
     float *dh0;
-    float *Hst, *dHst, *Dst;   // [tiles][H][128][128], [tiles][H][128][128], [tiles][H][16][128]
+    __nv_bfloat16 *Hst, *dHst;   // [tiles][H][128][128]: entering state, end gradient
+    float *Dst;                  // [tiles][H][16][128]
+    const float *lam;            // [tiles][H]: log bound of each tile's transition
+    const int *seg_ok;           // [N][H]: 1 if the pair runs in segments
     Plan p;
     int H;
     float b;
@@ -63,17 +80,26 @@ __device__ __forceinline__ void stage_tile(const BcArgs &A, int64_t t0, int len,
     const int tid = threadIdx.x;
     if (tid < kD) {
         const int d = tid;
+        // every load of the tile first, then the arithmetic
+        __nv_bfloat16 ra[kT], rk[kT], rq[kT];
+#pragma unroll
+        for (int i = 0; i < kT; ++i)
+            if (i < len) {
+                const int64_t row = (t0 + i) * A.H + h;
+                ra[i] = VEC ? A.a[row * kD + d] : A.a[row];
+                rk[i] = A.k[row * kD + d];
+                if (Qt) rq[i] = A.q[row * kD + d];
+            }
         float G = 0.f, eGC = 1.f;
-#pragma unroll 4
+#pragma unroll
         for (int i = 0; i < kT; ++i) {
             float kt = 0.f, kh = 0.f, qt = 0.f, gg = 0.f;
             if (i < len) {
-                const int64_t row = (t0 + i) * A.H + h;
-                G += gate_logdecay(gate_in<VEC>(A.a, row, d), A.b, GDR_GATE_BOUNDED);
-                const float e = expf(G), en = expf(-G), kd = __bfloat162float(A.k[row * kD + d]);
+                G += gate_logdecay(__bfloat162float(ra[i]), A.b, GDR_GATE_BOUNDED);
+                const float e = expf(G), en = expf(-G), kd = __bfloat162float(rk[i]);
                 kt = kd * e;
                 kh = kd * en;
-                if (Qt) qt = __bfloat162float(A.q[row * kD + d]) * e;
+                if (Qt) qt = __bfloat162float(rq[i]) * e;
                 eGC = e;
                 gg = G;
             }
@@ -85,10 +111,14 @@ __device__ __forceinline__ void stage_tile(const BcArgs &A, int64_t t0, int len,
         eg[d] = eGC;
     } else {
         const int c = tid - kD;
-#pragma unroll 4
+        __nv_bfloat16 ro[kT];
+#pragma unroll
         for (int i = 0; i < kT; ++i)
-            Ob[i * kLd + c] = (i < len && other) ? __bfloat162float(other[((t0 + i) * A.H + h) * kD + c]) : 0.f;
-        if (c < kT) bs[c] = c < len ? __bfloat162float(A.beta[(t0 + c) * A.H + h]) : 0.f;
+            if (i < len && other) ro[i] = other[((t0 + i) * A.H + h) * kD + c];
+        const float bt = c < len ? __bfloat162float(A.beta[(t0 + c) * A.H + h]) : 0.f;
+#pragma unroll
+        for (int i = 0; i < kT; ++i) Ob[i * kLd + c] = (i < len && other) ? __bfloat162float(ro[i]) : 0.f;
+        if (c < kT) bs[c] = bt;
     }
 }
 
@@ -174,11 +204,145 @@ __device__ __forceinline__ void copy_state_out(const float *Hs, float *dst) {
     }
 }
 
+__device__ __forceinline__ void copy_state_out_h(const float *Hs, __nv_bfloat16 *dst) {
+    for (int e = threadIdx.x * 4; e < kD * kD; e += kThreads * 4) {
+        const int r = e >> 7, c = e & (kD - 1);
+        const float4 x = *(const float4 *)&Hs[r * kLd + c];
+        __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y), hi = __floats2bfloat162_rn(x.z, x.w);
+        uint2 u;
+        u.x = *(uint32_t *)&lo;
+        u.y = *(uint32_t *)&hi;
+        *(uint2 *)&dst[e] = u;
+    }
+}
+
 __device__ __forceinline__ void copy_state_in(float *Hs, const float *src) {
     for (int e = threadIdx.x * 4; e < kD * kD; e += kThreads * 4) {
         const int r = e >> 7, c = e & (kD - 1);
         *(float4 *)&Hs[r * kLd + c] = src ? *(const float4 *)&src[e] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+}
+
+// Per (tile, head): sum over its tokens of max_d g_{t,d} + ln max(1, |1 - beta |k|^2|).
+template <bool VEC>
+__global__ void __launch_bounds__(128)
+bwd_bound_kernel(const BcArgs A, float *lam) {
+    __shared__ float red[2][4][kT];
+    const int64_t c = blockIdx.x;
+    const int h = blockIdx.y;
+    const int n = find_owner(A.p.chunk_base, A.p.N, c);
+    if (n < 0) return;
+    const int64_t t0 = A.p.seq_start[n] + (c - A.p.chunk_base[n]) * kT;
+    const int len = (int)min((int64_t)kT, A.p.seq_start[n + 1] - t0);
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+#pragma unroll 4
+    for (int i = 0; i < kT; ++i) {
+        float m = 3.0e38f, kk = 0.f;
+        if (i < len) {
+            const int64_t row = (t0 + i) * A.H + h;
+            m = gate_in<VEC>(A.a, row, tid);
+            const float kd = __bfloat162float(A.k[row * kD + tid]);
+            kk = kd * kd;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            m = fminf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            kk += __shfl_xor_sync(0xffffffffu, kk, o);
+        }
+        if (lane == 0) {
+            red[0][w][i] = m;
+            red[1][w][i] = kk;
+        }
+    }
+    __syncthreads();
+    if (tid < 32) {
+        float x = 0.f;
+        if (tid < len) {
+            const float m = fminf(fminf(red[0][0][tid], red[0][1][tid]), fminf(red[0][2][tid], red[0][3][tid]));
+            const float kk = red[1][0][tid] + red[1][1][tid] + red[1][2][tid] + red[1][3][tid];
+            const float bt = __bfloat162float(A.beta[(t0 + tid) * A.H + h]);
+            x = gate_logdecay(m, A.b, GDR_GATE_BOUNDED) + logf(fmaxf(1.f, fabsf(1.f - bt * kk)));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        if (tid == 0) lam[c * A.H + h] = x;
+    }
+}
+
+// Per (sequence, head): 1 if every interior segment boundary has a bound <= e^-46
+// within kMaxWarm tiles on both sides (or the sequence's end within reach).
+__global__ void __launch_bounds__(32)
+bwd_decide_kernel(const float *__restrict__ lam, int *__restrict__ ok, Plan p, int H) {
+    const int h = blockIdx.x % H, n = blockIdx.x / H;
+    const int lane = threadIdx.x;
+    const int64_t base = p.chunk_base[n], nt = p.chunk_base[n + 1] - base;
+    int good = 1;
+    for (int64_t B = kSegTiles; B < nt && good; B += kSegTiles) {
+        float before = 0.f, after = 0.f;
+        for (int i = lane; i < kMaxWarm; i += 32) {
+            if (B - 1 - i >= 0) before += lam[(base + B - 1 - i) * H + h];
+            if (B + i < nt) after += lam[(base + B + i) * H + h];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            before += __shfl_xor_sync(0xffffffffu, before, o);
+            after += __shfl_xor_sync(0xffffffffu, after, o);
+        }
+        good = (B <= kMaxWarm || before <= kHorizonLog) && (B + kMaxWarm >= nt || after <= kHorizonLog);
+    }
+    if (lane == 0) ok[(int64_t)n * H + h] = good;
+}
+
+// Warp-wide walk over the per-tile log bounds from tile `from` of a sequence with
+// `nt` tiles: backwards (dir < 0) to the latest start w <= from whose tiles
+// [w, from) sum to <= e^-46, or 0; forwards (dir > 0) to the earliest end
+// e >= from whose tiles [from, e) do, or nt.
+__device__ __forceinline__ int64_t warm_walk(const float *lam, int64_t tile0, int64_t nt, int H, int h,
+                                             int64_t from, int dir) {
+    const int lane = threadIdx.x & 31;
+    int64_t w = from;
+    float acc = 0.f;
+    bool done = dir < 0 ? from == 0 : from >= nt;
+    while (!done) {
+        const int64_t i = dir < 0 ? w - 1 - lane : w + lane;
+        const bool in = i >= 0 && i < nt;
+        float x = in ? lam[(tile0 + i) * H + h] : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, in && acc + x <= kHorizonLog);
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            w = dir < 0 ? w - 1 - l : w + 1 + l;
+            done = true;
+        } else {
+            acc += __shfl_sync(0xffffffffu, x, 31);
+            w = dir < 0 ? max(w - 32, (int64_t)0) : min(w + 32, nt);
+            done = dir < 0 ? w == 0 : w == nt;
+        }
+    }
+    return w;
+}
+
+// Segment of block `sg` (global segment index): sequence n and tiles [s0, s1);
+// false when the block has nothing to do.
+__device__ __forceinline__ bool segment_of(const BcArgs &A, int64_t sg, int h, int &n, int64_t &s0,
+                                           int64_t &s1) {
+    n = find_owner(A.p.seg_base, A.p.N, sg);
+    if (n < 0) return false;
+    const int64_t nt = A.p.chunk_base[n + 1] - A.p.chunk_base[n];
+    const int64_t j = sg - A.p.seg_base[n];
+    if (A.seg_ok[(int64_t)n * A.H + h]) {
+        s0 = j * kSegTiles;
+        s1 = min(nt, s0 + kSegTiles);
+    } else {
+        if (j > 0) return false;
+        s0 = 0;
+        s1 = nt;
+    }
+    return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -194,17 +358,29 @@ bwd_fwd_chain_kernel(const BcArgs A) {
     extern __shared__ float sm[];
     float *Hs = sm + kF_H, *Kt = sm + kF_Kt, *Kh = sm + kF_Kh, *Ub = sm + kF_U, *Am = sm + kF_A;
     float *eg = sm + kF_eg, *bs = sm + kF_b;
-    const int h = blockIdx.x % A.H, n = blockIdx.x / A.H;
+    __shared__ int64_t first;
+    const int h = blockIdx.x % A.H;
+    int n;
+    int64_t s0, s1;
+    if (!segment_of(A, blockIdx.x / A.H, h, n, s0, s1)) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
     const int c0 = 16 * warp;
-    const size_t sbase = ((size_t)n * A.H + h) * kD * kD;
-    copy_state_in(Hs, A.h0 ? A.h0 + sbase : nullptr);
     const int64_t s = A.p.seq_start[n], e_end = A.p.seq_start[n + 1], tile0 = A.p.chunk_base[n];
-    int64_t c = tile0;
-    for (int64_t t0 = s; t0 < e_end; t0 += kT, ++c) {
+    const int64_t ntiles = A.p.chunk_base[n + 1] - tile0;
+    if (warp == 0) {
+        const int64_t w = warm_walk(A.lam, tile0, ntiles, A.H, h, s0, -1);
+        if (lane == 0) first = w;
+    }
+    __syncthreads();
+    const int64_t w0 = first;
+    const size_t sbase = ((size_t)n * A.H + h) * kD * kD;
+    copy_state_in(Hs, (w0 == 0 && A.h0) ? A.h0 + sbase : nullptr);
+    for (int64_t tt = w0; tt < s1; ++tt) {
+        const int64_t t0 = s + tt * kT, c = tile0 + tt;
         const int len = (int)min((int64_t)kT, e_end - t0);
+        const bool keep = tt >= s0;   // warm-up tiles only advance the state
         __syncthreads();
-        copy_state_out(Hs, A.Hst + ((size_t)c * A.H + h) * kD * kD);
+        if (keep) copy_state_out_h(Hs, A.Hst + ((size_t)c * A.H + h) * kD * kD);
         stage_tile<VEC>(A, t0, len, h, Kt, Kh, nullptr, nullptr, eg, A.v, Ub, bs);
         __syncthreads();
         if (warp < 2) build_A(Kt, Kh, bs, Am, nullptr, warp, g, t);
@@ -246,8 +422,10 @@ bwd_fwd_chain_kernel(const BcArgs A) {
             Ub[g * kLd + col + 1] = dacc[nt][1];
             Ub[(g + 8) * kLd + col] = dacc[nt][2];
             Ub[(g + 8) * kLd + col + 1] = dacc[nt][3];
-            *(float2 *)&Dg[g * kD + col] = make_float2(dacc[nt][0], dacc[nt][1]);
-            *(float2 *)&Dg[(g + 8) * kD + col] = make_float2(dacc[nt][2], dacc[nt][3]);
+            if (keep) {
+                *(float2 *)&Dg[g * kD + col] = make_float2(dacc[nt][0], dacc[nt][1]);
+                *(float2 *)&Dg[(g + 8) * kD + col] = make_float2(dacc[nt][2], dacc[nt][3]);
+            }
         }
         __syncwarp();
         // H1 = diag(e^{G_C}) H0 + Ke^T D on this warp's columns
@@ -293,18 +471,28 @@ bwd_adj_chain_kernel(const BcArgs A) {
     extern __shared__ float sm[];
     float *dH = sm + kA_H, *Kt = sm + kA_Kt, *Kh = sm + kA_Kh, *Qt = sm + kA_Qt, *Ob = sm + kA_O;
     float *Eb = sm + kA_E, *Am = sm + kA_A, *Sm = sm + kA_S, *eg = sm + kA_eg, *bs = sm + kA_b;
-    const int h = blockIdx.x % A.H, n = blockIdx.x / A.H;
+    __shared__ int64_t last;
+    const int h = blockIdx.x % A.H;
+    int n;
+    int64_t s0, s1;
+    if (!segment_of(A, blockIdx.x / A.H, h, n, s0, s1)) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
     const int c0 = 16 * warp;
-    const size_t sbase = ((size_t)n * A.H + h) * kD * kD;
-    copy_state_in(dH, A.dhT ? A.dhT + sbase : nullptr);
     const int64_t s = A.p.seq_start[n], e_end = A.p.seq_start[n + 1], tile0 = A.p.chunk_base[n];
     const int64_t ntiles = A.p.chunk_base[n + 1] - tile0;
-    for (int64_t tt = ntiles - 1; tt >= 0; --tt) {
+    if (warp == 0) {
+        const int64_t e = warm_walk(A.lam, tile0, ntiles, A.H, h, s1, +1);
+        if (lane == 0) last = e;
+    }
+    __syncthreads();
+    const int64_t e0 = last;
+    const size_t sbase = ((size_t)n * A.H + h) * kD * kD;
+    copy_state_in(dH, (e0 == ntiles && A.dhT) ? A.dhT + sbase : nullptr);
+    for (int64_t tt = e0 - 1; tt >= s0; --tt) {
         const int64_t t0 = s + tt * kT, c = tile0 + tt;
         const int len = (int)min((int64_t)kT, e_end - t0);
         __syncthreads();
-        copy_state_out(dH, A.dHst + ((size_t)c * A.H + h) * kD * kD);
+        if (tt < s1) copy_state_out_h(dH, A.dHst + ((size_t)c * A.H + h) * kD * kD);
         stage_tile<VEC>(A, t0, len, h, Kt, Kh, Qt, nullptr, eg, A.dout, Ob, bs);
         __syncthreads();
         if (warp < 2) build_A(Kt, Kh, bs, Am, nullptr, warp, g, t);
@@ -387,46 +575,35 @@ bwd_adj_chain_kernel(const BcArgs A) {
         }
     }
     __syncthreads();
-    if (A.dh0) copy_state_out(dH, A.dh0 + sbase);
+    if (A.dh0 && s0 == 0) copy_state_out(dH, A.dh0 + sbase);
 }
 
 // ---------------------------------------------------------------------------
-// per-tile gradients
+// per-tile gradients.  Buffers are reused by lifetime:
+//   Ob: dO, then dG        Db: D, then dW, then dYw     Eb: dD, then dYu
+//   Ub: V, then U          Wb: W                        Sh: dH1, then H0 (bf16)
 // ---------------------------------------------------------------------------
-constexpr int kG_S = 0;                            // dH1, then H0   [128][kLd]
-constexpr int kG_Kt = kG_S + kD * kLd;             // Kt
-constexpr int kG_Kh = kG_Kt + kTile2;              // Kh
-constexpr int kG_Qt = kG_Kh + kTile2;              // Qt
-constexpr int kG_G = kG_Qt + kTile2;               // G
-constexpr int kG_V = kG_G + kTile2;                // V
-constexpr int kG_O = kG_V + kTile2;                // dO
-constexpr int kG_W = kG_O + kTile2;                // W
-constexpr int kG_U = kG_W + kTile2;                // U
-constexpr int kG_D = kG_U + kTile2;                // D
-constexpr int kG_E = kG_D + kTile2;                // dD
-constexpr int kG_F1 = kG_E + kTile2;               // dW, then dYu
-constexpr int kG_F2 = kG_F1 + kTile2;              // dYw
-constexpr int kG_X = kG_F2 + kTile2;               // dG (per token, channel)
-constexpr int kG_A = kG_X + kTile2;                // A        [16][kPd]
-constexpr int kG_KK = kG_A + kT * kPd;             // Kt Kh^T
-constexpr int kG_Sm = kG_KK + kT * kPd;            // S
-constexpr int kG_dS = kG_Sm + kT * kPd;            // dS
-constexpr int kG_dA = kG_dS + kT * kPd;            // dA
-constexpr int kG_bdA = kG_dA + kT * kPd;           // beta_i dA_ij
-constexpr int kG_eg = kG_bdA + kT * kPd;           // e^{G_C} [128]
-constexpr int kG_rG = kG_eg + kD;                  // extra dG_C [128]
-constexpr int kG_b = kG_rG + kD;                   // beta [16]
-constexpr int kG_total = kG_b + kT;
+template <bool VEC> struct TileLayout {
+    static constexpr int kt = 0, kh = kt + kTile2, qt = kh + kTile2, ob = qt + kTile2,
+                         db = ob + kTile2, ub = db + kTile2, wb = ub + kTile2, eb = wb + kTile2,
+                         am = eb + kTile2, kk = am + kT * kPd, smx = kk + kT * kPd,
+                         ds = smx + kT * kPd, da = ds + kT * kPd, bda = da + kT * kPd,
+                         eg = bda + kT * kPd, rg = eg + kD, bs = rg + kD, rs = bs + kT,
+                         gb = rs + kT, sh = gb + (VEC ? kTile2 : kT), total_f = sh;
+    static constexpr size_t bytes = sizeof(float) * total_f + sizeof(__nv_bfloat16) * kD * kLdh;
+};
 
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads)
 bwd_tile_kernel(const BcArgs A) {
+    using L = TileLayout<VEC>;
     extern __shared__ float sm[];
-    float *Sb = sm + kG_S, *Kt = sm + kG_Kt, *Kh = sm + kG_Kh, *Qt = sm + kG_Qt, *Gb = sm + kG_G;
-    float *Vb = sm + kG_V, *Ob = sm + kG_O, *Wb = sm + kG_W, *Ub = sm + kG_U, *Db = sm + kG_D;
-    float *Eb = sm + kG_E, *F1 = sm + kG_F1, *F2 = sm + kG_F2, *Xb = sm + kG_X;
-    float *Am = sm + kG_A, *KK = sm + kG_KK, *Sm = sm + kG_Sm, *dS = sm + kG_dS, *dA = sm + kG_dA;
-    float *bdA = sm + kG_bdA, *eg = sm + kG_eg, *rG = sm + kG_rG, *bs = sm + kG_b;
+    float *Kt = sm + L::kt, *Kh = sm + L::kh, *Qt = sm + L::qt, *Ob = sm + L::ob, *Db = sm + L::db;
+    float *Ub = sm + L::ub, *Wb = sm + L::wb, *Eb = sm + L::eb;
+    float *Am = sm + L::am, *KK = sm + L::kk, *Sm = sm + L::smx, *dS = sm + L::ds, *dA = sm + L::da;
+    float *bdA = sm + L::bda, *eg = sm + L::eg, *rG = sm + L::rg, *bs = sm + L::bs, *rowsum = sm + L::rs;
+    float *Gb = sm + L::gb;
+    __nv_bfloat16 *Sh = (__nv_bfloat16 *)(sm + L::sh);
     const int64_t c = blockIdx.x;
     const int h = blockIdx.y;
     const int n = find_owner(A.p.chunk_base, A.p.N, c);
@@ -436,16 +613,29 @@ bwd_tile_kernel(const BcArgs A) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
     const int c0 = 16 * warp;
     const size_t st = ((size_t)c * A.H + h) * kD * kD;
-    // ---- stage: factored rows, G, V, dO, beta, D; dH1 into the state buffer
-    stage_tile<VEC>(A, t0, len, h, Kt, Kh, Qt, Gb, eg, A.v, Vb, bs);
+    auto stage_state = [&](const __nv_bfloat16 *src) {
+#pragma unroll
+        for (int e = tid * 8; e < kD * kD; e += kThreads * 8) {
+            const int r = e >> 7, col = e & (kD - 1);
+            *(uint4 *)&Sh[r * kLdh + col] = *(const uint4 *)&src[e];
+        }
+    };
+    // ---- stage: factored rows, G, dO, D, V; dH1 into the state buffer
+    stage_tile<VEC>(A, t0, len, h, Kt, Kh, Qt, VEC ? Gb : nullptr, eg, A.dout, Ob, bs);
+    if (!VEC && tid < kT) {
+        // scalar gate: one cumulative log-decay per token
+        float G = 0.f;
+        for (int i = 0; i <= tid && i < len; ++i)
+            G += gate_logdecay(__bfloat162float(A.a[(t0 + i) * A.H + h]), A.b, GDR_GATE_BOUNDED);
+        Gb[tid] = G;
+    }
+#pragma unroll
     for (int e = tid; e < kT * kD; e += kThreads) {
         const int i = e >> 7, col = e & (kD - 1);
-        const int64_t row = (t0 + i) * A.H + h;
-        Ob[i * kLd + col] = (i < len && A.dout) ? __bfloat162float(A.dout[row * kD + col]) : 0.f;
         Db[i * kLd + col] = A.Dst[((size_t)c * A.H + h) * kT * kD + e];
-        Ub[i * kLd + col] = i < len ? __bfloat162float(A.v[row * kD + col]) : 0.f;   // U built in place
+        Ub[i * kLd + col] = i < len ? __bfloat162float(A.v[((t0 + i) * A.H + h) * kD + col]) : 0.f;
     }
-    copy_state_in(Sb, A.dHst + st);
+    stage_state(A.dHst + st);
     __syncthreads();
     // ---- 16 x 16 products
     if (warp < 2) build_A(Kt, Kh, bs, Am, KK, warp, g, t);
@@ -468,8 +658,7 @@ bwd_tile_kernel(const BcArgs A) {
 #pragma unroll 2
         for (int k0 = 0; k0 < kD; k0 += 8) {
             uint32_t ak[4], ad[4];
-            // Ke = Kh (.) e^{G_C}: scale the A fragment by the channel factors
-            ak[0] = tf32(Kh[g * kLd + k0 + t] * eg[k0 + t]);
+            ak[0] = tf32(Kh[g * kLd + k0 + t] * eg[k0 + t]);   // Ke = Kh (.) e^{G_C}
             ak[1] = tf32(Kh[(g + 8) * kLd + k0 + t] * eg[k0 + t]);
             ak[2] = tf32(Kh[g * kLd + k0 + t + 4] * eg[k0 + t + 4]);
             ak[3] = tf32(Kh[(g + 8) * kLd + k0 + t + 4] * eg[k0 + t + 4]);
@@ -477,9 +666,9 @@ bwd_tile_kernel(const BcArgs A) {
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 uint32_t b0, b1;
-                load_b(b0, b1, Sb, kLd, k0, c0 + 8 * nt, g, t);    // dH1[k][c]
+                load_b_h(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);    // dH1[k][c]
                 mma8(acc[nt], ak, b0, b1);
-                load_bt(b0, b1, Sb, kLd, k0, c0 + 8 * nt, g, t);   // dH1^T[k][d] = dH1[d][k]
+                load_bt_h(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);   // dH1^T[k][d] = dH1[d][k]
                 mma8(dke[nt], ad, b0, b1);
             }
         }
@@ -504,21 +693,25 @@ bwd_tile_kernel(const BcArgs A) {
         }
     }
     __syncthreads();
-    // ---- H0 into the state buffer, and e^{G_C} rowsum(dH1 (.) H0) (dH1 reread from HBM)
+    // ---- H0 into the state buffer, and e^{G_C} rowsum(dH1 (.) H0) from the stored copies
     {
-        const float *H0g = A.Hst + st, *dH1g = A.dHst + st;
+        const __nv_bfloat16 *H0g = A.Hst + st, *dH1g = A.dHst + st;
+#pragma unroll 4
         for (int r = warp; r < kD; r += 8) {
-            const float4 x = *(const float4 *)&H0g[r * kD + 4 * lane];
-            const float4 y = *(const float4 *)&dH1g[r * kD + 4 * lane];
-            *(float4 *)&Sb[r * kLd + 4 * lane] = x;
-            float p = x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
+            const uint2 xh = *(const uint2 *)&H0g[r * kD + 4 * lane];
+            const uint2 yh = *(const uint2 *)&dH1g[r * kD + 4 * lane];
+            *(uint2 *)&Sh[r * kLdh + 4 * lane] = xh;
+            const __nv_bfloat162 *x2 = (const __nv_bfloat162 *)&xh, *y2 = (const __nv_bfloat162 *)&yh;
+            const float2 xa = __bfloat1622float2(x2[0]), xb = __bfloat1622float2(x2[1]);
+            const float2 ya = __bfloat1622float2(y2[0]), yb = __bfloat1622float2(y2[1]);
+            float p = xa.x * ya.x + xa.y * ya.y + xb.x * yb.x + xb.y * yb.y;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
             if (lane == 0) rG[r] = eg[r] * p;
         }
     }
     __syncthreads();
-    // ---- dQt_a = dO H0^T and dW = -dD H0^T (this warp's dk columns)
+    // ---- dQt_a = dO H0^T and dW = -dD H0^T (this warp's dk columns); dW into Db
     float dq[2][4];
     {
         float dw[2][4];
@@ -536,25 +729,24 @@ bwd_tile_kernel(const BcArgs A) {
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 uint32_t b0, b1;
-                load_bt(b0, b1, Sb, kLd, k0, c0 + 8 * nt, g, t);   // H0^T[k][d] = H0[d][k]
+                load_bt_h(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);   // H0^T[k][d] = H0[d][k]
                 mma8(dq[nt], ao, b0, b1);
                 mma8(dw[nt], ae, b0, b1);
             }
         }
+        __syncthreads();   // every warp is done reading D (the dS and dKe products) and dO
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             const int col = c0 + 8 * nt + 2 * t;
-            F1[g * kLd + col] = dw[nt][0];
-            F1[g * kLd + col + 1] = dw[nt][1];
-            F1[(g + 8) * kLd + col] = dw[nt][2];
-            F1[(g + 8) * kLd + col + 1] = dw[nt][3];
+            Db[g * kLd + col] = dw[nt][0];
+            Db[g * kLd + col + 1] = dw[nt][1];
+            Db[(g + 8) * kLd + col] = dw[nt][2];
+            Db[(g + 8) * kLd + col + 1] = dw[nt][3];
         }
     }
     __syncthreads();
-    // ---- dYw = T^T dW (threads 0..127, dk columns); dYu = T^T dD (threads 128..255)
-    if (tid < kD) back_subst(F1, F2, tid, Am);
-    __syncthreads();
-    if (tid >= kD) back_subst(Eb, F1, tid - kD, Am);   // F1 <- dYu (dW no longer needed)
+    // ---- dYw = T^T dW in place (dk columns, threads 0..127); dYu = T^T dD in place
+    back_subst(tid < kD ? Db : Eb, tid < kD ? Db : Eb, tid & (kD - 1), Am);
     __syncthreads();
     // ---- dA = -strict_lower(dYu U^T + dYw W^T) (warps 0-1); dV = diag(beta) dYu
     if (warp < 2) {
@@ -563,10 +755,10 @@ bwd_tile_kernel(const BcArgs A) {
 #pragma unroll 4
         for (int k0 = 0; k0 < kD; k0 += 8) {
             uint32_t af[4], b0, b1;
-            load_a(af, F1, kLd, 0, k0, g, t);
+            load_a(af, Eb, kLd, 0, k0, g, t);
             load_bt(b0, b1, Ub, kLd, k0, j0, g, t);
             mma8(acc, af, b0, b1);
-            load_a(af, F2, kLd, 0, k0, g, t);
+            load_a(af, Db, kLd, 0, k0, g, t);
             load_bt(b0, b1, Wb, kLd, k0, j0, g, t);
             mma8(acc, af, b0, b1);
         }
@@ -584,10 +776,10 @@ bwd_tile_kernel(const BcArgs A) {
     }
     for (int e = tid; e < kT * kD; e += kThreads) {
         const int i = e >> 7, col = e & (kD - 1);
-        if (i < len) A.dv[((t0 + i) * A.H + h) * kD + col] = __float2bfloat16_rn(bs[i] * F1[i * kLd + col]);
+        if (i < len) A.dv[((t0 + i) * A.H + h) * kD + col] = __float2bfloat16_rn(bs[i] * Eb[i * kLd + col]);
     }
     __syncthreads();
-    // ---- dKt, dKh, dQt on this warp's dk columns; dG into Xb
+    // ---- dKt, dKh, dQt on this warp's dk columns; dG into Ob
     {
         float dkt[2][4], dkh[2][4];
 #pragma unroll
@@ -619,20 +811,17 @@ bwd_tile_kernel(const BcArgs A) {
             for (int u = 0; u < 4; ++u) {
                 const int i = g + 8 * (u >> 1), d = c0 + 8 * nt + 2 * t + (u & 1);
                 const float kt = Kt[i * kLd + d], kh = Kh[i * kLd + d], qt = Qt[i * kLd + d];
-                const float dKt = dkt[nt][u] + bs[i] * F2[i * kLd + d];
+                const float dKt = dkt[nt][u] + bs[i] * Db[i * kLd + d];
                 const float dKh = dkh[nt][u] + dke[nt][u] * eg[d];
-                float dG = dq[nt][u] * qt + dKt * kt - dKh * kh;
-                Xb[i * kLd + d] = dG;
-                const float G = Gb[i * kLd + d];
+                Ob[i * kLd + d] = dq[nt][u] * qt + dKt * kt - dKh * kh;
                 if (i < len) {
+                    const float G = VEC ? Gb[i * kLd + d] : Gb[i];
                     const int64_t r = ((t0 + i) * A.H + h) * kD + d;
                     A.dq[r] = __float2bfloat16_rn(dq[nt][u] * expf(G));
                     A.dk[r] = __float2bfloat16_rn(dKt * expf(G) + dKh * expf(-G));
                 }
-                // sum_i dKe (.) Ke, folded into the last token's dG below
-                dke[nt][u] *= kh * eg[d];
+                dke[nt][u] *= kh * eg[d];   // dKe (.) Ke, summed over the tile below
             }
-        // column sums over the 16 rows of dKe (.) Ke: rows g and g+8 of the 8 lane groups
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -647,11 +836,13 @@ bwd_tile_kernel(const BcArgs A) {
     // ---- dbeta (threads 0..15, one token each)
     if (tid < kT && tid < len) {
         const int i = tid;
+        const int64_t row = (t0 + i) * A.H + h;
         float acc = 0.f;
         for (int col = 0; col < kD; ++col)
-            acc = fmaf(F1[i * kLd + col], Vb[i * kLd + col], fmaf(F2[i * kLd + col], Kt[i * kLd + col], acc));
+            acc = fmaf(Eb[i * kLd + col], __bfloat162float(A.v[row * kD + col]),
+                       fmaf(Db[i * kLd + col], Kt[i * kLd + col], acc));
         for (int j = 0; j < i; ++j) acc = fmaf(dA[i * kPd + j], KK[i * kPd + j], acc);
-        A.dbeta[(t0 + i) * A.H + h] = __float2bfloat16_rn(acc);
+        A.dbeta[row] = __float2bfloat16_rn(acc);
     }
     // ---- da: the last token also carries dG_C; reverse cumsum over the tile
     if (VEC) {
@@ -659,7 +850,7 @@ bwd_tile_kernel(const BcArgs A) {
             const int d = tid;
             float acc = 0.f;
             for (int i = len - 1; i >= 0; --i) {
-                acc += Xb[i * kLd + d] + (i == len - 1 ? rG[d] : 0.f);
+                acc += Ob[i * kLd + d] + (i == len - 1 ? rG[d] : 0.f);
                 const int64_t r = ((t0 + i) * A.H + h) * kD + d;
                 const float av = __bfloat162float(A.a[r]);
                 const float sg = 1.f / (1.f + expf(-av));
@@ -667,12 +858,10 @@ bwd_tile_kernel(const BcArgs A) {
             }
         }
     } else {
-        // per-token sums over the channels, then the reverse cumsum (warp 0)
-        __shared__ float rowsum[kT];
         if (warp < 4) {
             for (int i = warp; i < kT; i += 4) {
                 float x = 0.f;
-                for (int d = lane; d < kD; d += 32) x += Xb[i * kLd + d] + (i == len - 1 ? rG[d] : 0.f);
+                for (int d = lane; d < kD; d += 32) x += Ob[i * kLd + d] + (i == len - 1 ? rG[d] : 0.f);
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
                 if (lane == 0) rowsum[i] = x;
@@ -693,31 +882,67 @@ bwd_tile_kernel(const BcArgs A) {
 }
 
 template <bool VEC>
-cudaError_t launch_chunk_bwd_t(const BcArgs &A, int64_t max_tiles) {
+cudaError_t run_chunk_bwd(const BcArgs &A, int64_t max_tiles, int64_t max_segs, float *lam, int *ok,
+                          cudaStream_t stream) {
     cudaError_t err;
-    const int N = A.p.N, H = A.H;
+    const int H = A.H;
     auto kf = bwd_fwd_chain_kernel<VEC>;
     auto ka = bwd_adj_chain_kernel<VEC>;
     auto kt = bwd_tile_kernel<VEC>;
-    const size_t sf = sizeof(float) * kF_total, sa = sizeof(float) * kA_total, sg = sizeof(float) * kG_total;
+    const size_t sf = sizeof(float) * kF_total, sa = sizeof(float) * kA_total, sg = TileLayout<VEC>::bytes;
     if ((err = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sf)) != cudaSuccess) return err;
     if ((err = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sa)) != cudaSuccess) return err;
     if ((err = cudaFuncSetAttribute(kt, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sg)) != cudaSuccess) return err;
+    const int64_t segs = max_segs * H;
+    if (segs > 0x7fffffff) return cudaErrorInvalidValue;
+    if (max_tiles > 0) {
+        ProfScope prof(stream, "bwd_bound_kernel");
+        bwd_bound_kernel<VEC><<<dim3((unsigned)max_tiles, (unsigned)H), 128, 0, stream>>>(A, lam);
+        count_launch();
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    {
+        ProfScope prof(stream, "bwd_decide_kernel");
+        bwd_decide_kernel<<<(unsigned)((int64_t)A.p.N * H), 32, 0, stream>>>(lam, ok, A.p, H);
+        count_launch();
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    {
+        ProfScope prof(stream, "bwd_fwd_chain_kernel");
+        kf<<<(unsigned)segs, kThreads, sf, stream>>>(A);
+        count_launch();
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    {
+        ProfScope prof(stream, "bwd_adj_chain_kernel");
+        ka<<<(unsigned)segs, kThreads, sa, stream>>>(A);
+        count_launch();
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    if (max_tiles > 0) {
+        ProfScope prof(stream, "bwd_tile_kernel");
+        kt<<<dim3((unsigned)max_tiles, (unsigned)H), kThreads, sg, stream>>>(A);
+        count_launch();
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
     return cudaSuccess;
 }
 
 }  // namespace
 
-size_t chunk_bwd_scratch_bytes(int64_t tiles, int H) {
-    return sizeof(float) * (size_t)tiles * H * (2 * (size_t)kD * kD + (size_t)kT * kD) + 3 * 256;
+int chunk_bwd_segment_tiles() { return kSegTiles; }
+
+size_t chunk_bwd_scratch_bytes(int64_t tiles, int N, int H) {
+    return sizeof(__nv_bfloat16) * (size_t)tiles * H * 2 * kD * kD +
+           sizeof(float) * (size_t)tiles * H * (kT * kD + 1) + sizeof(int) * (size_t)N * H + 5 * 256;
 }
 
 cudaError_t launch_chunk_bwd(const void *q, const void *k, const void *v, const void *a,
                              const void *beta, const float *h0, const void *dout, const float *dhT,
                              void *dq, void *dk, void *dv, void *da, void *dbeta, float *dh0,
-                             Plan plan, int H, int64_t max_tiles, float b, bool per_channel,
-                             void *scratch, cudaStream_t stream) {
-    if (plan.C != kT) return cudaErrorInvalidValue;
+                             Plan plan, int H, int64_t max_tiles, int64_t max_segs, float b,
+                             bool per_channel, void *scratch, cudaStream_t stream) {
+    if (plan.C != kT || plan.seg_chunks != kSegTiles) return cudaErrorInvalidValue;
     auto al = [](size_t x) { return (x + 255) / 256 * 256; };
     BcArgs A;
     A.q = (const __nv_bfloat16 *)q;
@@ -735,48 +960,23 @@ cudaError_t launch_chunk_bwd(const void *q, const void *k, const void *v, const 
     A.dbeta = (__nv_bfloat16 *)dbeta;
     A.dh0 = dh0;
     char *p = (char *)scratch;
-    const size_t st = sizeof(float) * (size_t)max_tiles * H * kD * kD;
-    A.Hst = (float *)p;
-    p += al(st);
-    A.dHst = (float *)p;
-    p += al(st);
+    const size_t sth = sizeof(__nv_bfloat16) * (size_t)max_tiles * H * kD * kD;
+    A.Hst = (__nv_bfloat16 *)p;
+    p += al(sth);
+    A.dHst = (__nv_bfloat16 *)p;
+    p += al(sth);
     A.Dst = (float *)p;
+    p += al(sizeof(float) * (size_t)max_tiles * H * kT * kD);
+    float *lam = (float *)p;
+    p += al(sizeof(float) * (size_t)max_tiles * H);
+    int *ok = (int *)p;
+    A.lam = lam;
+    A.seg_ok = ok;
     A.p = plan;
     A.H = H;
     A.b = b;
-    cudaError_t err = per_channel ? launch_chunk_bwd_t<true>(A, max_tiles) : launch_chunk_bwd_t<false>(A, max_tiles);
-    if (err != cudaSuccess) return err;
-    const int64_t chains = (int64_t)plan.N * H;
-    if (chains > 0x7fffffff) return cudaErrorInvalidValue;
-    {
-        ProfScope prof(stream, "bwd_fwd_chain_kernel");
-        if (per_channel)
-            bwd_fwd_chain_kernel<true><<<(unsigned)chains, kThreads, sizeof(float) * kF_total, stream>>>(A);
-        else
-            bwd_fwd_chain_kernel<false><<<(unsigned)chains, kThreads, sizeof(float) * kF_total, stream>>>(A);
-        count_launch();
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    }
-    {
-        ProfScope prof(stream, "bwd_adj_chain_kernel");
-        if (per_channel)
-            bwd_adj_chain_kernel<true><<<(unsigned)chains, kThreads, sizeof(float) * kA_total, stream>>>(A);
-        else
-            bwd_adj_chain_kernel<false><<<(unsigned)chains, kThreads, sizeof(float) * kA_total, stream>>>(A);
-        count_launch();
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    }
-    if (max_tiles > 0) {
-        ProfScope prof(stream, "bwd_tile_kernel");
-        const dim3 grid((unsigned)max_tiles, (unsigned)H);
-        if (per_channel)
-            bwd_tile_kernel<true><<<grid, kThreads, sizeof(float) * kG_total, stream>>>(A);
-        else
-            bwd_tile_kernel<false><<<grid, kThreads, sizeof(float) * kG_total, stream>>>(A);
-        count_launch();
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    }
-    return cudaSuccess;
+    return per_channel ? run_chunk_bwd<true>(A, max_tiles, max_segs, lam, ok, stream)
+                       : run_chunk_bwd<false>(A, max_tiles, max_segs, lam, ok, stream);
 }
 
 }  // namespace gdr

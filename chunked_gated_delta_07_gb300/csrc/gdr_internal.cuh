@@ -132,12 +132,13 @@ cudaError_t launch_vec_mma(const void *q, const void *k, const void *v, const vo
                            cudaStream_t stream);
 
 // backward in the chunked form, bf16 d = 128, bounded gate (gdr_bwd_chunk.cu)
-size_t chunk_bwd_scratch_bytes(int64_t tiles, int H);
+int chunk_bwd_segment_tiles();
+size_t chunk_bwd_scratch_bytes(int64_t tiles, int N, int H);
 cudaError_t launch_chunk_bwd(const void *q, const void *k, const void *v, const void *a,
                              const void *beta, const float *h0, const void *dout, const float *dhT,
                              void *dq, void *dk, void *dv, void *da, void *dbeta, float *dh0,
-                             Plan plan, int H, int64_t max_tiles, float b, bool per_channel,
-                             void *scratch, cudaStream_t stream);
+                             Plan plan, int H, int64_t max_tiles, int64_t max_segs, float b,
+                             bool per_channel, void *scratch, cudaStream_t stream);
 
 // quantile-balancing router-bias update (gdr_router.cu)
 constexpr int kRouterMaxE = 2048;

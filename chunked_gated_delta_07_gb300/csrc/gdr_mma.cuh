@@ -9,6 +9,8 @@
 
 #include <cstdint>
 
+#include <cuda_bf16.h>
+
 namespace gdr {
 
 __device__ __forceinline__ uint32_t tf32(float x) {
@@ -56,6 +58,23 @@ __device__ __forceinline__ void load_bt(uint32_t &b0, uint32_t &b1, const float 
                                         int n0, int g, int t) {
     b0 = tf32(M[(n0 + g) * ld + k0 + t]);
     b1 = tf32(M[(n0 + g) * ld + k0 + t + 4]);
+}
+
+}  // namespace gdr
+
+namespace gdr {
+
+// B fragments from a bf16 row-major matrix (values widened exactly, then tf32)
+__device__ __forceinline__ void load_b_h(uint32_t &b0, uint32_t &b1, const __nv_bfloat16 *M, int ld,
+                                         int k0, int n0, int g, int t) {
+    b0 = tf32(__bfloat162float(M[(k0 + t) * ld + n0 + g]));
+    b1 = tf32(__bfloat162float(M[(k0 + t + 4) * ld + n0 + g]));
+}
+
+__device__ __forceinline__ void load_bt_h(uint32_t &b0, uint32_t &b1, const __nv_bfloat16 *M, int ld,
+                                          int k0, int n0, int g, int t) {
+    b0 = tf32(__bfloat162float(M[(n0 + g) * ld + k0 + t]));
+    b1 = tf32(__bfloat162float(M[(n0 + g) * ld + k0 + t + 4]));
 }
 
 }  // namespace gdr

@@ -28,10 +28,10 @@ def _built():
     torch.cuda.set_device(0)
 
 
-def _inputs(dtype, d, T, gate, seed, N=2, H=3, varlen=False, h0=True):
+def _inputs(dtype, d, T, gate, seed, N=2, H=3, varlen=False, h0=True, a_mean=0.0):
     w = WORKLOADS["b2_t4k"].with_(B=N, H=H, dk=d, dv=d, dtype=dtype, h0_std=0.05 if h0 else 0.0,
                                   gate=gate, a_std=3.0 if gate == "softplus" else 1.0, seed=seed,
-                                  varlen=varlen)
+                                  varlen=varlen, a_mean=a_mean)
     x = make_inputs(w, device="cuda", T=T)
     g = torch.Generator(device="cpu").manual_seed(seed + 1)
     B, Tn = x["q"].shape[:2]
@@ -151,3 +151,13 @@ def test_chunked_and_token_forms_agree(monkeypatch):
         assert r <= 1e-2, f"{name}: chunked vs token rel-L2 {r:.3e}"
     _check(chunked, ref, "bf16")
     _check(token, ref, "bf16")
+
+
+@pytest.mark.parametrize("T,a_mean", [(2500, 0.0), (1500, -6.0), (5500, -6.0)])
+def test_chunked_backward_segments(T, a_mean):
+    """Long sequences: 64-tile segments of both state chains started at warm-up tiles
+    (2500 tokens); a weak decay whose warm-ups run to the sequence ends (1500
+    tokens); a weak decay with no warm-up within 256 tiles, run unsegmented (5500)."""
+    x = _inputs("bf16", 128, T, "bounded", seed=4800 + T, N=1, H=2, a_mean=a_mean)
+    got, ref = _run(x, "bounded")
+    _check(got, ref, "bf16")
