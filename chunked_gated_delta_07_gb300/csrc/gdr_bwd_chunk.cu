@@ -204,8 +204,11 @@ __device__ __forceinline__ void copy_state_out(const float *Hs, float *dst) {
     }
 }
 
-__device__ __forceinline__ void copy_state_out_h(const float *Hs, __nv_bfloat16 *dst) {
-    for (int e = threadIdx.x * 4; e < kD * kD; e += kThreads * 4) {
+// bf16 copy of the fp32 state by threads [first, kThreads)
+__device__ __forceinline__ void copy_state_out_h(const float *Hs, __nv_bfloat16 *dst, int first = 0) {
+    if ((int)threadIdx.x < first) return;
+    const int n = kThreads - first;
+    for (int e = ((int)threadIdx.x - first) * 4; e < kD * kD; e += n * 4) {
         const int r = e >> 7, c = e & (kD - 1);
         const float4 x = *(const float4 *)&Hs[r * kLd + c];
         __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y), hi = __floats2bfloat162_rn(x.z, x.w);
@@ -380,10 +383,10 @@ bwd_fwd_chain_kernel(const BcArgs A) {
         const int len = (int)min((int64_t)kT, e_end - t0);
         const bool keep = tt >= s0;   // warm-up tiles only advance the state
         __syncthreads();
-        if (keep) copy_state_out_h(Hs, A.Hst + ((size_t)c * A.H + h) * kD * kD);
         stage_tile<VEC>(A, t0, len, h, Kt, Kh, nullptr, nullptr, eg, A.v, Ub, bs);
         __syncthreads();
         if (warp < 2) build_A(Kt, Kh, bs, Am, nullptr, warp, g, t);
+        else if (keep) copy_state_out_h(Hs, A.Hst + ((size_t)c * A.H + h) * kD * kD, 64);
         __syncthreads();
         fwd_subst(tid < kD ? Kt : Ub, tid & (kD - 1), Am, bs);   // Kt -> W, V -> U
         if (tid < kD)
@@ -492,11 +495,11 @@ bwd_adj_chain_kernel(const BcArgs A) {
         const int64_t t0 = s + tt * kT, c = tile0 + tt;
         const int len = (int)min((int64_t)kT, e_end - t0);
         __syncthreads();
-        if (tt < s1) copy_state_out_h(dH, A.dHst + ((size_t)c * A.H + h) * kD * kD);
         stage_tile<VEC>(A, t0, len, h, Kt, Kh, Qt, nullptr, eg, A.dout, Ob, bs);
         __syncthreads();
         if (warp < 2) build_A(Kt, Kh, bs, Am, nullptr, warp, g, t);
         else if (warp < 4) build_lower(Qt, Kh, Sm, warp - 2, g, t);
+        else if (tt < s1) copy_state_out_h(dH, A.dHst + ((size_t)c * A.H + h) * kD * kD, 128);
         __syncthreads();
         if (tid < kD) {
             fwd_subst(Kt, tid, Am, bs);   // Kt -> W
@@ -589,7 +592,7 @@ template <bool VEC> struct TileLayout {
                          am = eb + kTile2, kk = am + kT * kPd, smx = kk + kT * kPd,
                          ds = smx + kT * kPd, da = ds + kT * kPd, bda = da + kT * kPd,
                          eg = bda + kT * kPd, rg = eg + kD, bs = rg + kD, rs = bs + kT,
-                         gb = rs + kT, sh = gb + (VEC ? kTile2 : kT), total_f = sh;
+                         gb = rs + 4 * kT, sh = gb + (VEC ? kTile2 : kT), total_f = sh;
     static constexpr size_t bytes = sizeof(float) * total_f + sizeof(__nv_bfloat16) * kD * kLdh;
 };
 
@@ -637,60 +640,56 @@ bwd_tile_kernel(const BcArgs A) {
     }
     stage_state(A.dHst + st);
     __syncthreads();
-    // ---- 16 x 16 products
+    // ---- Ke dH1 (this warp's dv columns) and dKe = D dH1^T (this warp's dk columns),
+    // then the 16 x 16 products
+    float dke[2][4], dd[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dke[nt][u] = dd[nt][u] = 0.f;
+#pragma unroll 2
+    for (int k0 = 0; k0 < kD; k0 += 8) {
+        uint32_t ak[4], ad[4];
+        ak[0] = tf32(Kh[g * kLd + k0 + t] * eg[k0 + t]);   // Ke = Kh (.) e^{G_C}
+        ak[1] = tf32(Kh[(g + 8) * kLd + k0 + t] * eg[k0 + t]);
+        ak[2] = tf32(Kh[g * kLd + k0 + t + 4] * eg[k0 + t + 4]);
+        ak[3] = tf32(Kh[(g + 8) * kLd + k0 + t + 4] * eg[k0 + t + 4]);
+        load_a(ad, Db, kLd, 0, k0, g, t);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            uint32_t b0, b1;
+            load_b_h(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);    // dH1[k][c]
+            mma8(dd[nt], ak, b0, b1);
+            load_bt_h(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);   // dH1^T[k][d] = dH1[d][k]
+            mma8(dke[nt], ad, b0, b1);
+        }
+    }
     if (warp < 2) build_A(Kt, Kh, bs, Am, KK, warp, g, t);
     else if (warp < 4) build_lower(Qt, Kh, Sm, warp - 2, g, t);
     else if (warp < 6) build_lower(Ob, Db, dS, warp - 4, g, t);   // dS = lower(dO D^T)
     if (tid < kD)
         for (int i = 0; i < kT; ++i) Wb[i * kLd + tid] = Kt[i * kLd + tid];
     __syncthreads();
-    // ---- W and U
+    // ---- W and U; dD = Ke dH1 + S^T dO into Eb (this warp's dv columns)
     fwd_subst(tid < kD ? Wb : Ub, tid & (kD - 1), Am, bs);
-    __syncthreads();
-    // ---- dD = S^T dO + Ke dH1 (this warp's dv columns); dKe = D dH1^T (this warp's dk columns)
-    float dke[2][4];
-    {
-        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int u = 0; u < 4; ++u) dke[nt][u] = 0.f;
-#pragma unroll 2
-        for (int k0 = 0; k0 < kD; k0 += 8) {
-            uint32_t ak[4], ad[4];
-            ak[0] = tf32(Kh[g * kLd + k0 + t] * eg[k0 + t]);   // Ke = Kh (.) e^{G_C}
-            ak[1] = tf32(Kh[(g + 8) * kLd + k0 + t] * eg[k0 + t]);
-            ak[2] = tf32(Kh[g * kLd + k0 + t + 4] * eg[k0 + t + 4]);
-            ak[3] = tf32(Kh[(g + 8) * kLd + k0 + t + 4] * eg[k0 + t + 4]);
-            load_a(ad, Db, kLd, 0, k0, g, t);
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                uint32_t b0, b1;
-                load_b_h(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);    // dH1[k][c]
-                mma8(acc[nt], ak, b0, b1);
-                load_bt_h(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);   // dH1^T[k][d] = dH1[d][k]
-                mma8(dke[nt], ad, b0, b1);
-            }
-        }
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-            uint32_t as[4];
-            load_at(as, Sm, kPd, 0, 8 * ks, g, t);
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                uint32_t b0, b1;
-                load_b(b0, b1, Ob, kLd, 8 * ks, c0 + 8 * nt, g, t);
-                mma8(acc[nt], as, b0, b1);
-            }
-        }
+    for (int ks = 0; ks < 2; ++ks) {
+        uint32_t as[4];
+        load_at(as, Sm, kPd, 0, 8 * ks, g, t);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            const int col = c0 + 8 * nt + 2 * t;
-            Eb[g * kLd + col] = acc[nt][0];
-            Eb[g * kLd + col + 1] = acc[nt][1];
-            Eb[(g + 8) * kLd + col] = acc[nt][2];
-            Eb[(g + 8) * kLd + col + 1] = acc[nt][3];
+            uint32_t b0, b1;
+            load_b(b0, b1, Ob, kLd, 8 * ks, c0 + 8 * nt, g, t);
+            mma8(dd[nt], as, b0, b1);
         }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int col = c0 + 8 * nt + 2 * t;
+        Eb[g * kLd + col] = dd[nt][0];
+        Eb[g * kLd + col + 1] = dd[nt][1];
+        Eb[(g + 8) * kLd + col] = dd[nt][2];
+        Eb[(g + 8) * kLd + col + 1] = dd[nt][3];
     }
     __syncthreads();
     // ---- H0 into the state buffer, and e^{G_C} rowsum(dH1 (.) H0) from the stored copies
@@ -774,9 +773,24 @@ bwd_tile_kernel(const BcArgs A) {
         bdA[i1 * kPd + ja] = bs[i1] * v10;
         bdA[i1 * kPd + jb] = bs[i1] * v11;
     }
-    for (int e = tid; e < kT * kD; e += kThreads) {
-        const int i = e >> 7, col = e & (kD - 1);
-        if (i < len) A.dv[((t0 + i) * A.H + h) * kD + col] = __float2bfloat16_rn(bs[i] * Eb[i * kLd + col]);
+    // dV = diag(beta) dYu, and the per-token sums dYu . V + dYw . Kt for dbeta: thread
+    // (tid & 127) takes one column of rows (tid >> 7), (tid >> 7) + 2, ...
+    {
+        const int col = tid & (kD - 1), half = tid >> 7;
+#pragma unroll
+        for (int m = 0; m < kT / 2; ++m) {
+            const int i = half + 2 * m;
+            float x = 0.f;
+            if (i < len) {
+                const int64_t r = ((t0 + i) * A.H + h) * kD + col;
+                const float yu = Eb[i * kLd + col];
+                A.dv[r] = __float2bfloat16_rn(bs[i] * yu);
+                x = fmaf(yu, __bfloat162float(A.v[r]), Db[i * kLd + col] * Kt[i * kLd + col]);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+            if (lane == 0) rowsum[i * 4 + (warp & 3)] = x;   // 4 warps per half
+        }
     }
     __syncthreads();
     // ---- dKt, dKh, dQt on this warp's dk columns; dG into Ob
@@ -836,14 +850,11 @@ bwd_tile_kernel(const BcArgs A) {
     // ---- dbeta (threads 0..15, one token each)
     if (tid < kT && tid < len) {
         const int i = tid;
-        const int64_t row = (t0 + i) * A.H + h;
-        float acc = 0.f;
-        for (int col = 0; col < kD; ++col)
-            acc = fmaf(Eb[i * kLd + col], __bfloat162float(A.v[row * kD + col]),
-                       fmaf(Db[i * kLd + col], Kt[i * kLd + col], acc));
+        float acc = rowsum[i * 4] + rowsum[i * 4 + 1] + rowsum[i * 4 + 2] + rowsum[i * 4 + 3];
         for (int j = 0; j < i; ++j) acc = fmaf(dA[i * kPd + j], KK[i * kPd + j], acc);
-        A.dbeta[row] = __float2bfloat16_rn(acc);
+        A.dbeta[(t0 + i) * A.H + h] = __float2bfloat16_rn(acc);
     }
+    __syncthreads();   // rowsum is reused below
     // ---- da: the last token also carries dG_C; reverse cumsum over the tile
     if (VEC) {
         if (tid < kD) {
