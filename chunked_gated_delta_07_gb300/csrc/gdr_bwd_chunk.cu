@@ -592,7 +592,7 @@ template <bool VEC> struct TileLayout {
                          am = eb + kTile2, kk = am + kT * kPd, smx = kk + kT * kPd,
                          ds = smx + kT * kPd, da = ds + kT * kPd, bda = da + kT * kPd,
                          eg = bda + kT * kPd, rg = eg + kD, bs = rg + kD, rs = bs + kT,
-                         gb = rs + 4 * kT, sh = gb + (VEC ? kTile2 : kT), total_f = sh;
+                         gb = rs + 4 * kT, sh = gb + (VEC ? kTile2 : 2 * kT), total_f = sh;
     static constexpr size_t bytes = sizeof(float) * total_f + sizeof(__nv_bfloat16) * kD * kLdh;
 };
 
@@ -625,12 +625,18 @@ bwd_tile_kernel(const BcArgs A) {
     };
     // ---- stage: factored rows, G, dO, D, V; dH1 into the state buffer
     stage_tile<VEC>(A, t0, len, h, Kt, Kh, Qt, VEC ? Gb : nullptr, eg, A.dout, Ob, bs);
-    if (!VEC && tid < kT) {
-        // scalar gate: one cumulative log-decay per token
-        float G = 0.f;
-        for (int i = 0; i <= tid && i < len; ++i)
-            G += gate_logdecay(__bfloat162float(A.a[(t0 + i) * A.H + h]), A.b, GDR_GATE_BOUNDED);
-        Gb[tid] = G;
+    if (!VEC && tid >= kThreads - kT) {
+        // scalar gate: g and g'(a) per token, one load each (the cumsum follows the barrier)
+        const int i = tid - (kThreads - kT);
+        float gi = 0.f, dgi = 0.f;
+        if (i < len) {
+            const float av = __bfloat162float(A.a[(t0 + i) * A.H + h]);
+            const float sg = 1.f / (1.f + expf(-av));
+            gi = -A.b * sg;
+            dgi = -A.b * sg * (1.f - sg);
+        }
+        Gb[i] = gi;
+        Gb[kT + i] = dgi;
     }
 #pragma unroll
     for (int e = tid; e < kT * kD; e += kThreads) {
@@ -667,6 +673,16 @@ bwd_tile_kernel(const BcArgs A) {
     if (warp < 2) build_A(Kt, Kh, bs, Am, KK, warp, g, t);
     else if (warp < 4) build_lower(Qt, Kh, Sm, warp - 2, g, t);
     else if (warp < 6) build_lower(Ob, Db, dS, warp - 4, g, t);   // dS = lower(dO D^T)
+    else if (!VEC && warp == 7) {
+        // in-tile inclusive cumsum of g (lanes 0..15), in place
+        float x = lane < kT ? Gb[lane] : 0.f;
+#pragma unroll
+        for (int o = 1; o < kT; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane < kT) Gb[lane] = x;
+    }
     if (tid < kD)
         for (int i = 0; i < kT; ++i) Wb[i * kLd + tid] = Kt[i * kLd + tid];
     __syncthreads();
@@ -879,15 +895,15 @@ bwd_tile_kernel(const BcArgs A) {
             }
         }
         __syncthreads();
-        if (tid == 0) {
-            float acc = 0.f;
-            for (int i = len - 1; i >= 0; --i) {
-                acc += rowsum[i];
-                const int64_t r = (t0 + i) * A.H + h;
-                const float av = __bfloat162float(A.a[r]);
-                const float sg = 1.f / (1.f + expf(-av));
-                A.da[r] = __float2bfloat16_rn(acc * (-A.b * sg * (1.f - sg)));
+        if (warp == 0) {
+            // reverse cumsum over the tile's tokens (lanes 0..15), times g'(a)
+            float x = lane < len ? rowsum[lane] : 0.f;
+#pragma unroll
+            for (int o = 1; o < kT; o <<= 1) {
+                const float y = __shfl_down_sync(0xffffffffu, x, o);
+                if (lane + o < kT) x += y;
             }
+            if (lane < len) A.da[(t0 + lane) * A.H + h] = __float2bfloat16_rn(x * Gb[kT + lane]);
         }
     }
 }
