@@ -33,7 +33,7 @@ constexpr int kRtBlocksPerSm = 4;
 // Order-preserving map of a binary32 score onto uint32 (-0 taken as +0).
 __device__ __forceinline__ uint32_t score_key(float s) {
     const uint32_t u = __float_as_uint(s + 0.0f);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);   // negative: ~u, else u | sign
 }
 
 // (key, -index) packed so that a larger value is the better expert.
@@ -61,11 +61,13 @@ template <> struct Vec4<float> {
     }
 };
 
-template <typename T, int NCH>
+// ECT > 0 fixes the expert count at compile time (the bounds checks fold away).
+template <typename T, int NCH, int ECT>
 __global__ void __launch_bounds__(kRtThreads, NCH > 8 ? 1 : 2)
 router_topk_kernel(const T *__restrict__ logits, const float *__restrict__ bias,
                    int32_t *__restrict__ idx, float *__restrict__ sel,
-                   unsigned long long *__restrict__ load, int64_t Tn, int E, int k) {
+                   unsigned long long *__restrict__ load, int64_t Tn, int E_arg, int k) {
+    const int E = ECT > 0 ? ECT : E_arg;
     extern __shared__ unsigned int hist[];                // [E] counts, then [E] bias
     float *bsm = (float *)(hist + E);
     __shared__ uint64_t cand[kRtWarps][kCap];
@@ -261,10 +263,10 @@ router_update_kernel(const long long *__restrict__ load, float *__restrict__ bia
     }
 }
 
-template <typename T, int NCH>
+template <typename T, int NCH, int ECT = 0>
 cudaError_t launch_topk_t(const void *logits, const float *bias, int32_t *idx, float *sel,
                           int64_t *load, int64_t Tn, int E, int k, cudaStream_t stream) {
-    auto kern = router_topk_kernel<T, NCH>;
+    auto kern = router_topk_kernel<T, NCH, ECT>;
     const size_t smem = (sizeof(unsigned int) + sizeof(float)) * (size_t)E;
     int dev = 0, sms = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -287,6 +289,7 @@ cudaError_t launch_topk_dt(const void *logits, const float *bias, int32_t *idx, 
     if (E <= 128) return launch_topk_t<T, 1>(logits, bias, idx, sel, load, Tn, E, k, stream);
     if (E <= 256) return launch_topk_t<T, 2>(logits, bias, idx, sel, load, Tn, E, k, stream);
     if (E <= 512) return launch_topk_t<T, 4>(logits, bias, idx, sel, load, Tn, E, k, stream);
+    if (E == 896) return launch_topk_t<T, 7, 896>(logits, bias, idx, sel, load, Tn, E, k, stream);
     if (E <= 896) return launch_topk_t<T, 7>(logits, bias, idx, sel, load, Tn, E, k, stream);
     if (E <= 1024) return launch_topk_t<T, 8>(logits, bias, idx, sel, load, Tn, E, k, stream);
     return launch_topk_t<T, 16>(logits, bias, idx, sel, load, Tn, E, k, stream);
