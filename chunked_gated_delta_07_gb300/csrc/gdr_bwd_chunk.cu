@@ -238,7 +238,7 @@ bwd_bound_kernel(const BcArgs A, float *lam) {
     const int64_t t0 = A.p.seq_start[n] + (c - A.p.chunk_base[n]) * kT;
     const int len = (int)min((int64_t)kT, A.p.seq_start[n + 1] - t0);
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-#pragma unroll 4
+#pragma unroll
     for (int i = 0; i < kT; ++i) {
         float m = 3.0e38f, kk = 0.f;
         if (i < len) {

@@ -58,51 +58,49 @@ constexpr size_t kSmemBytes = sizeof(float) * kSmemFloats;
 
 // Per (tile, head): the log of a bound on the norm of the tile's transition,
 // sum over its tokens of  max_d g_{t,d} + ln max(1, |1 - beta_t |k_t|^2|),
-// with max_d g = -b sigmoid(min_d a) (the gate is decreasing in a).
-__global__ void __launch_bounds__(128)
+// with max_d g = -b sigmoid(min_d a) (the gate is decreasing in a).  One warp per
+// (tile, head): lane l holds channels 4l..4l+3 of every token.
+constexpr int kBoundWarps = 8;
+
+__global__ void __launch_bounds__(32 * kBoundWarps)
 vec_bound_kernel(const __nv_bfloat16 *__restrict__ a, const __nv_bfloat16 *__restrict__ k,
                  const __nv_bfloat16 *__restrict__ beta, float *__restrict__ lam, Plan p, int H,
-                 float b) {
-    __shared__ float red[2][4][kT];
-    const int64_t c = blockIdx.x;
+                 float b, int64_t max_tiles) {
+    const int lane = threadIdx.x & 31;
+    const int64_t c = (int64_t)blockIdx.x * kBoundWarps + (threadIdx.x >> 5);
     const int h = blockIdx.y;
+    if (c >= max_tiles) return;
     const int n = find_owner(p.chunk_base, p.N, c);
     if (n < 0) return;
     const int64_t t0 = p.seq_start[n] + (c - p.chunk_base[n]) * kT;
     const int len = (int)min((int64_t)kT, p.seq_start[n + 1] - t0);
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-#pragma unroll 4
-    for (int i = 0; i < kT; ++i) {
-        float m = 3.0e38f, kk = 0.f;
+    uint2 ra[kT], rk[kT];
+#pragma unroll
+    for (int i = 0; i < kT; ++i)
         if (i < len) {
-            const int64_t r = ((t0 + i) * H + h) * kD + tid;
-            m = __bfloat162float(a[r]);
-            const float kd = __bfloat162float(k[r]);
-            kk = kd * kd;
+            const int64_t r = ((t0 + i) * H + h) * kD + 4 * lane;
+            ra[i] = *(const uint2 *)&a[r];
+            rk[i] = *(const uint2 *)&k[r];
         }
+    float lam_t = 0.f;
+#pragma unroll
+    for (int i = 0; i < kT; ++i) {
+        if (i >= len) break;
+        const float2 a0 = __bfloat1622float2(*(const __nv_bfloat162 *)&ra[i].x);
+        const float2 a1 = __bfloat1622float2(*(const __nv_bfloat162 *)&ra[i].y);
+        const float2 k0 = __bfloat1622float2(*(const __nv_bfloat162 *)&rk[i].x);
+        const float2 k1 = __bfloat1622float2(*(const __nv_bfloat162 *)&rk[i].y);
+        float m = fminf(fminf(a0.x, a0.y), fminf(a1.x, a1.y));
+        float kk = k0.x * k0.x + k0.y * k0.y + k1.x * k1.x + k1.y * k1.y;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             m = fminf(m, __shfl_xor_sync(0xffffffffu, m, o));
             kk += __shfl_xor_sync(0xffffffffu, kk, o);
         }
-        if (lane == 0) {
-            red[0][w][i] = m;
-            red[1][w][i] = kk;
-        }
+        const float bt = __bfloat162float(beta[(t0 + i) * H + h]);
+        lam_t += gate_logdecay(m, b, GDR_GATE_BOUNDED) + logf(fmaxf(1.f, fabsf(1.f - bt * kk)));
     }
-    __syncthreads();
-    if (tid < 32) {
-        float x = 0.f;
-        if (tid < len) {
-            const float m = fminf(fminf(red[0][0][tid], red[0][1][tid]), fminf(red[0][2][tid], red[0][3][tid]));
-            const float kk = red[1][0][tid] + red[1][1][tid] + red[1][2][tid] + red[1][3][tid];
-            const float bt = __bfloat162float(beta[(t0 + tid) * H + h]);
-            x = gate_logdecay(m, b, GDR_GATE_BOUNDED) + logf(fmaxf(1.f, fabsf(1.f - bt * kk)));
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-        if (tid == 0) lam[c * H + h] = x;
-    }
+    if (lane == 0) lam[c * H + h] = lam_t;
 }
 
 // Per (sequence, head): 1 if every segment start has a bound <= 2^-64 within
@@ -405,9 +403,10 @@ cudaError_t launch_vec_mma(const void *q, const void *k, const void *v, const vo
     cudaError_t err;
     if (max_tiles > 0) {
         ProfScope prof(stream, "vec_bound_kernel");
-        vec_bound_kernel<<<dim3((unsigned)max_tiles, (unsigned)H), 128, 0, stream>>>(
+        vec_bound_kernel<<<dim3((unsigned)((max_tiles + kBoundWarps - 1) / kBoundWarps), (unsigned)H),
+                           32 * kBoundWarps, 0, stream>>>(
             (const __nv_bfloat16 *)a, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)beta, lam,
-            plan, H, b);
+            plan, H, b, max_tiles);
         count_launch();
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
