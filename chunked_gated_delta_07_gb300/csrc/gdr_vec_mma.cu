@@ -13,8 +13,8 @@
 //   H <- diag(exp(G_C)) H + (Kh exp(G_C))^T D                          (tensor cores)
 // Warp w owns the state columns 16w..16w+15 for D, O and the state update, so
 // those three steps need no block barrier between them; a tile takes four.
-// The next tile's inputs are loaded into registers while the current tile is
-// computed.
+// Each tile's loads are issued together before its staging; two blocks share an
+// SM (a next-tile prefetch held ~48 more registers live and ran 1.5x slower).
 //
 // Long sequences are cut into segments of kSegTiles tiles, one block per
 // (segment, head).  A block starts from a zero state at a warm-up tile w before
@@ -122,7 +122,7 @@ vec_decide_kernel(const float *__restrict__ lam, int *__restrict__ ok, Plan p, i
     if (lane == 0) ok[(int64_t)n * H + h] = good;
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ a,
                const __nv_bfloat16 *__restrict__ beta, const float *__restrict__ h0,
@@ -179,7 +179,7 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
         Hs[r * kLd + c] = from_h0 ? h0[hbase + e] : 0.f;
     }
     const int64_t sstart = p.seq_start[n], e_end = p.seq_start[n + 1];
-    // registers holding the next tile's inputs
+    // registers holding one tile's raw inputs
     __nv_bfloat16 ra[kT], rk[kT], rq[kT];
     float rb = 0.f;
     auto fetch = [&](int64_t tt) {
@@ -202,11 +202,11 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
             if (c < len) rb = __bfloat162float(beta[(t0 + c) * H + h]);
         }
     };
-    fetch(w0);
     for (int64_t tt = w0; tt < s1; ++tt) {
         const int64_t t0 = sstart + tt * kT;
         const int len = (int)min((int64_t)kT, e_end - t0);
         const bool emit = tt >= s0;   // warm-up tiles only advance the state
+        fetch(tt);         // every load of the tile, issued together
         __syncthreads();   // the previous tile is done with every staging buffer
         // ---- stage the tile: factored decays per key channel, V and beta
         if (tid < kD) {
@@ -235,7 +235,6 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
             if (c < kT) bs[c] = c < len ? rb : 0.f;
         }
         __syncthreads();
-        fetch(tt + 1);   // in flight while this tile is computed
         // ---- A = beta (.) strict_lower(Kt Kh^T) and P = lower(Qt Kh^T): warps 0-3
         if (warp < 4) {
             const float *Aop = (warp < 2) ? Kt : Qt;
