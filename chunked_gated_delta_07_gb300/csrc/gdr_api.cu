@@ -61,6 +61,7 @@ constexpr int kMaxPieces = 8;   // pieces of a pipelined host-buffer call
 
 struct DeviceCtx {
     int *d_status = nullptr;
+    int sms = 0;         // streaming multiprocessors of the device
     void *ws = nullptr;  // internal workspace cache
     size_t ws_bytes = 0;
     void *io = nullptr;  // device copies for the host-buffer entry point
@@ -84,6 +85,8 @@ DeviceCtx *device_ctx() {
     if (!c.d_status) {
         if (cudaMalloc(&c.d_status, sizeof(int)) != cudaSuccess) return nullptr;
         if (cudaMemset(c.d_status, 0, sizeof(int)) != cudaSuccess) return nullptr;
+        if (cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return nullptr;
     }
     return &c;
 }
@@ -630,7 +633,7 @@ gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const vo
     // factored in-tile decays need exp(16 b) < FLT_MAX); the rest runs token by token
     const bool chunked = dtype == GDR_BF16 && dk == 128 && dv == 128 && gate == GDR_GATE_BOUNDED &&
                          b <= kVecMaxB && !bwd_force_token_path();
-    const int seg = chunked ? chunk_bwd_segment_tiles() : (1 << 30);
+    const int seg = chunked ? chunk_bwd_segment_tiles(tiles, H, ctx->sms) : (1 << 30);
     const int64_t segs = s.varlen ? (tiles + seg - 1) / seg + B : (int64_t)B * ((tiles / B + seg - 1) / seg);
     const size_t need = plan_b + (chunked ? chunk_bwd_scratch_bytes(tiles, B, H)
                                           : bwd_scratch_bytes(tiles, s.T_total, H, dk, dv));
@@ -684,7 +687,7 @@ gdr_status_t gdr_chunk_fwd_vec(const void *q, const void *k, const void *v, cons
     const bool fused = dtype == GDR_BF16 && dk == 128 && dv == 128;   // tensor-core kernel
     const int64_t tiles = tile_bound(s.varlen, B, T, kVecTile);
     const size_t plan_b = align_up(3 * sizeof(int64_t) * (size_t)(B + 1));
-    const int seg = fused ? vec_mma_segment_tiles() : (1 << 30);
+    const int seg = fused ? vec_mma_segment_tiles(tiles, H, ctx->sms) : (1 << 30);
     // segments: at most one partial segment per sequence beyond the full ones
     const int64_t segs = s.varlen ? (tiles + seg - 1) / seg + B : (int64_t)B * ((tiles / B + seg - 1) / seg);
     const size_t need = plan_b + (fused ? vec_mma_scratch_bytes(tiles, B, H)

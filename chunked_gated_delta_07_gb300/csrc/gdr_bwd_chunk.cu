@@ -26,13 +26,14 @@
 //   bwd_tile_kernel       per (tile, head), all tiles at once: every input gradient
 // The scalar-gate form is the per-channel form with every channel's gate equal.
 //
-// The two chains run in 64-tile segments, one block per (segment, head), each
+// The two chains run in segments of S tiles (the plan's seg_chunks: 64 to 256,
+// longer when enough (segment, head) blocks remain), one block per (segment, head), each
 // started at a warm-up tile whose neglected transition is provably below 2^-64:
 // the forward chain from a zero state some tiles before its segment, the adjoint
 // chain from a zero gradient some tiles after it.  Both transitions have norm at
 // most prod_t max(1, |1 - beta_t |k_t|^2|) max_d alpha_{t,d} (the adjoint one is
 // the transpose), summed in log form per tile by bwd_bound_kernel.  A (sequence,
-// head) pair without such a warm-up within kMaxWarm tiles of every segment
+// head) pair without such a warm-up within 4 S tiles of every segment
 // boundary runs as one block, as without segments (bwd_decide_kernel).
 // The stored states are bf16 (they only feed the per-tile products).
 #include "gdr_internal.cuh"
@@ -47,8 +48,8 @@ constexpr int kLd = 132;
 constexpr int kPd = 20;
 constexpr int kThreads = 256;
 constexpr int kTile2 = kT * kLd;   // floats of one [16][kLd] buffer
-constexpr int kSegTiles = 64;
-constexpr int kMaxWarm = 4 * kSegTiles;
+constexpr int kSegMin = 64, kSegMax = 256;   // segment lengths in tiles
+constexpr int kWarmFactor = 4;   // longest warm-up, in segments
 constexpr float kHorizonLog = -46.0f;   // below ln(2^-64) = -44.4, with room for fp32 sums
 constexpr int kLdh = 136;               // row stride (elements) of the bf16 state in shared memory
 
@@ -273,16 +274,17 @@ bwd_bound_kernel(const BcArgs A, float *lam) {
 }
 
 // Per (sequence, head): 1 if every interior segment boundary has a bound <= e^-46
-// within kMaxWarm tiles on both sides (or the sequence's end within reach).
+// within 4 S tiles on both sides (or the sequence's end within reach).
 __global__ void __launch_bounds__(32)
 bwd_decide_kernel(const float *__restrict__ lam, int *__restrict__ ok, Plan p, int H) {
     const int h = blockIdx.x % H, n = blockIdx.x / H;
     const int lane = threadIdx.x;
     const int64_t base = p.chunk_base[n], nt = p.chunk_base[n + 1] - base;
     int good = 1;
-    for (int64_t B = kSegTiles; B < nt && good; B += kSegTiles) {
+    const int seg = p.seg_chunks, max_warm = kWarmFactor * seg;
+    for (int64_t B = seg; B < nt && good; B += seg) {
         float before = 0.f, after = 0.f;
-        for (int i = lane; i < kMaxWarm; i += 32) {
+        for (int i = lane; i < max_warm; i += 32) {
             if (B - 1 - i >= 0) before += lam[(base + B - 1 - i) * H + h];
             if (B + i < nt) after += lam[(base + B + i) * H + h];
         }
@@ -291,7 +293,7 @@ bwd_decide_kernel(const float *__restrict__ lam, int *__restrict__ ok, Plan p, i
             before += __shfl_xor_sync(0xffffffffu, before, o);
             after += __shfl_xor_sync(0xffffffffu, after, o);
         }
-        good = (B <= kMaxWarm || before <= kHorizonLog) && (B + kMaxWarm >= nt || after <= kHorizonLog);
+        good = (B <= max_warm || before <= kHorizonLog) && (B + max_warm >= nt || after <= kHorizonLog);
     }
     if (lane == 0) ok[(int64_t)n * H + h] = good;
 }
@@ -338,8 +340,8 @@ __device__ __forceinline__ bool segment_of(const BcArgs &A, int64_t sg, int h, i
     const int64_t nt = A.p.chunk_base[n + 1] - A.p.chunk_base[n];
     const int64_t j = sg - A.p.seg_base[n];
     if (A.seg_ok[(int64_t)n * A.H + h]) {
-        s0 = j * kSegTiles;
-        s1 = min(nt, s0 + kSegTiles);
+        s0 = j * A.p.seg_chunks;
+        s1 = min(nt, s0 + (int64_t)A.p.seg_chunks);
     } else {
         if (j > 0) return false;
         s0 = 0;
@@ -957,7 +959,13 @@ cudaError_t run_chunk_bwd(const BcArgs &A, int64_t max_tiles, int64_t max_segs, 
 
 }  // namespace
 
-int chunk_bwd_segment_tiles() { return kSegTiles; }
+// Segment length: the longest of 64, 128, 256 tiles that still leaves about eight
+// (segment, head) blocks per resident block (two per SM).
+int chunk_bwd_segment_tiles(int64_t tiles, int H, int sms) {
+    int seg = kSegMin;
+    while (seg < kSegMax && tiles * H / (2 * seg) >= (int64_t)16 * sms) seg *= 2;
+    return seg;
+}
 
 size_t chunk_bwd_scratch_bytes(int64_t tiles, int N, int H) {
     return sizeof(__nv_bfloat16) * (size_t)tiles * H * 2 * kD * kD +
@@ -969,7 +977,7 @@ cudaError_t launch_chunk_bwd(const void *q, const void *k, const void *v, const 
                              void *dq, void *dk, void *dv, void *da, void *dbeta, float *dh0,
                              Plan plan, int H, int64_t max_tiles, int64_t max_segs, float b,
                              bool per_channel, void *scratch, cudaStream_t stream) {
-    if (plan.C != kT || plan.seg_chunks != kSegTiles) return cudaErrorInvalidValue;
+    if (plan.C != kT || plan.seg_chunks < kSegMin || plan.seg_chunks > kSegMax) return cudaErrorInvalidValue;
     auto al = [](size_t x) { return (x + 255) / 256 * 256; };
     BcArgs A;
     A.q = (const __nv_bfloat16 *)q;

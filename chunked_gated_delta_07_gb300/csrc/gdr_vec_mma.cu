@@ -16,7 +16,8 @@
 // Each tile's loads are issued together before its staging; two blocks share an
 // SM (a next-tile prefetch held ~48 more registers live and ran 1.5x slower).
 //
-// Long sequences are cut into segments of kSegTiles tiles, one block per
+// Long sequences are cut into segments of S tiles (the plan's seg_chunks, 64 to 256,
+// larger when there are enough (segment, head) blocks to fill the GPU), one block per
 // (segment, head).  A block starts from a zero state at a warm-up tile w before
 // its segment and runs the state update alone up to the segment start.  The
 // state entering tile w reaches the segment start multiplied by a product of
@@ -26,7 +27,7 @@
 // this bound <= 2^-64 (far below fp32 resolution), or the sequence start,
 // where the block starts from h0 exactly.  vec_bound_kernel sums
 // max_d g per (tile, head); vec_decide_kernel marks the (sequence, head)
-// pairs whose decay is too weak for a warm-up of at most kMaxWarm tiles: those
+// pairs whose decay is too weak for a warm-up of at most 4 S tiles: those
 // run as one block over the whole sequence, exactly as without segments.
 #include "gdr_internal.cuh"
 #include "gdr_mma.cuh"
@@ -39,8 +40,8 @@ constexpr int kD = 128;      // dk = dv
 constexpr int kLd = 132;     // row stride (floats) of 128-wide shared matrices
 constexpr int kPd = 20;      // row stride of 16 x 16 shared matrices
 constexpr int kThreads = 256;
-constexpr int kSegTiles = 64;          // tiles per segment
-constexpr int kMaxWarm = 4 * kSegTiles;  // longest warm-up before a pair runs unsegmented
+constexpr int kSegMin = 64, kSegMax = 256;   // segment lengths in tiles
+constexpr int kWarmFactor = 4;   // longest warm-up, in segments, before a pair runs unsegmented
 constexpr float kHorizonLog = -46.0f;    // below ln(2^-64) = -44.4, with room for fp32 sums
 
 // shared layout, in floats
@@ -104,17 +105,18 @@ vec_bound_kernel(const __nv_bfloat16 *__restrict__ a, const __nv_bfloat16 *__res
 }
 
 // Per (sequence, head): 1 if every segment start has a bound <= 2^-64 within
-// kMaxWarm tiles before it (or the sequence start within reach), else 0.
+// 4 S tiles before it (or the sequence start within reach), else 0.
 __global__ void __launch_bounds__(32)
 vec_decide_kernel(const float *__restrict__ lam, int *__restrict__ ok, Plan p, int H) {
     const int h = blockIdx.x % H, n = blockIdx.x / H;
     const int lane = threadIdx.x;
     const int64_t base = p.chunk_base[n], nt = p.chunk_base[n + 1] - base;
     int good = 1;
-    for (int64_t s0 = kSegTiles; s0 < nt && good; s0 += kSegTiles) {
-        if (s0 <= kMaxWarm) continue;   // the warm-up can always reach the sequence start
+    const int seg = p.seg_chunks, max_warm = kWarmFactor * seg;
+    for (int64_t s0 = seg; s0 < nt && good; s0 += seg) {
+        if (s0 <= max_warm) continue;   // the warm-up can always reach the sequence start
         float acc = 0.f;
-        for (int i = lane; i < kMaxWarm; i += 32) acc += lam[(base + s0 - 1 - i) * H + h];
+        for (int i = lane; i < max_warm; i += 32) acc += lam[(base + s0 - 1 - i) * H + h];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
         good = acc <= kHorizonLog;
@@ -143,8 +145,8 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
     const int64_t j = sg - p.seg_base[n];
     const bool segmented = seg_ok[(int64_t)n * H + h] != 0;
     if (!segmented && j > 0) return;   // one block runs the whole sequence
-    const int64_t s0 = segmented ? j * kSegTiles : 0;
-    const int64_t s1 = segmented ? min(ntiles, s0 + kSegTiles) : ntiles;
+    const int64_t s0 = segmented ? j * p.seg_chunks : 0;
+    const int64_t s1 = segmented ? min(ntiles, s0 + (int64_t)p.seg_chunks) : ntiles;
     // warm-up start: the latest tile w <= s0 whose bound to s0 is <= 2^-64
     if (warp == 0) {
         int64_t w = s0;
@@ -390,13 +392,19 @@ size_t vec_mma_scratch_bytes(int64_t tiles, int N, int H) {
     return sizeof(float) * (size_t)tiles * H + sizeof(int) * (size_t)N * H + 2 * 256;
 }
 
-int vec_mma_segment_tiles() { return kSegTiles; }
+// Segment length: the longest of 64, 128, 256 tiles that still leaves about eight
+// (segment, head) blocks per resident block (two per SM).
+int vec_mma_segment_tiles(int64_t tiles, int H, int sms) {
+    int seg = kSegMin;
+    while (seg < kSegMax && tiles * H / (2 * seg) >= (int64_t)16 * sms) seg *= 2;
+    return seg;
+}
 
 cudaError_t launch_vec_mma(const void *q, const void *k, const void *v, const void *a,
                            const void *beta, const float *h0, void *out, float *hT, Plan plan,
                            int H, float b, int64_t max_tiles, int64_t max_segs, void *scratch,
                            cudaStream_t stream) {
-    if (plan.C != kT || plan.seg_chunks != kSegTiles) return cudaErrorInvalidValue;
+    if (plan.C != kT || plan.seg_chunks < kSegMin || plan.seg_chunks > kSegMax) return cudaErrorInvalidValue;
     float *lam = (float *)scratch;
     int *ok = (int *)((char *)scratch + (sizeof(float) * (size_t)max_tiles * H + 255) / 256 * 256);
     cudaError_t err;
