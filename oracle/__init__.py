@@ -93,6 +93,8 @@ def _bind(path):
         [ctypes.c_void_p] * 5 + [ctypes.c_int] + [ctypes.c_void_p] * 9
         + [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
            ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int])
+    lib.gdr_oracle_bwd_vec.restype = ctypes.c_int
+    lib.gdr_oracle_bwd_vec.argtypes = lib.gdr_oracle_bwd.argtypes
     lib.gdr_oracle_gate.restype = ctypes.c_double
     lib.gdr_oracle_gate.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.c_int]
     lib.gdr_oracle_max_threads.restype = ctypes.c_int
@@ -199,6 +201,21 @@ def oracle_bwd(q, k, v, a, beta, dout=None, dhT=None, h0=None, cu_seqlens=None,
     means zero).  Returns a dict with dq, dk [B,T,H,dk], dv [B,T,H,dv], da, dbeta
     [B,T,H] and dh0 [N,H,dk,dv], all fp64, with respect to the stored input values
     (bf16 inputs widened exactly)."""
+    return _bwd("gdr_oracle_bwd", q, k, v, a, beta, dout, dhT, h0, cu_seqlens, b, gate, nthreads,
+                _lib_path)
+
+
+def oracle_bwd_vec(q, k, v, a, beta, dout=None, dhT=None, h0=None, cu_seqlens=None,
+                   b: float = 2.0, gate: str = "bounded", nthreads: int = 0,
+                   _lib_path: str | None = None):
+    """fp64 gradients of <dout, out> + <dhT, hT> of the per-channel decay forward
+    (``oracle_fwd_vec``): a is [B,T,H,dk] and so is the returned da.  It keeps every
+    state of a sequence, so it is meant for small cases."""
+    return _bwd("gdr_oracle_bwd_vec", q, k, v, a, beta, dout, dhT, h0, cu_seqlens, b, gate,
+                nthreads, _lib_path)
+
+
+def _bwd(fn, q, k, v, a, beta, dout, dhT, h0, cu_seqlens, b, gate, nthreads, _lib_path):
     lib = _load() if _lib_path is None else _bind(_lib_path)
     arrs = [_as_array(x) for x in (q, k, v, a, beta)]
     if len({d for _, d in arrs}) != 1:
@@ -206,6 +223,8 @@ def oracle_bwd(q, k, v, a, beta, dout=None, dhT=None, h0=None, cu_seqlens=None,
     (qa, dt), (ka, _), (va, _), (aa, _), (ba, _) = arrs
     B, T, H, dk = qa.shape
     dv = va.shape[-1]
+    vec = fn == "gdr_oracle_bwd_vec"
+    assert aa.shape == ((B, T, H, dk) if vec else (B, T, H)), aa.shape
     if cu_seqlens is not None:
         cu = np.ascontiguousarray(np.asarray(
             cu_seqlens.cpu().numpy() if hasattr(cu_seqlens, "cpu") else cu_seqlens,
@@ -228,17 +247,17 @@ def oracle_bwd(q, k, v, a, beta, dout=None, dhT=None, h0=None, cu_seqlens=None,
     dout_a = f64(dout, (B, T, H, dv))
     dhT_a = f64(dhT, (N, H, dk, dv))
     g = {"dq": np.zeros((B, T, H, dk)), "dk": np.zeros((B, T, H, dk)),
-         "dv": np.zeros((B, T, H, dv)), "da": np.zeros((B, T, H)),
+         "dv": np.zeros((B, T, H, dv)), "da": np.zeros((B, T, H, dk) if vec else (B, T, H)),
          "dbeta": np.zeros((B, T, H)), "dh0": np.zeros((N, H, dk, dv))}
     ptr = lambda x: None if x is None else x.ctypes.data
-    rc = lib.gdr_oracle_bwd(
+    rc = getattr(lib, fn)(
         qa.ctypes.data, ka.ctypes.data, va.ctypes.data, aa.ctypes.data, ba.ctypes.data, dt,
         ptr(h0a), ptr(dout_a), ptr(dhT_a), g["dq"].ctypes.data, g["dk"].ctypes.data,
         g["dv"].ctypes.data, g["da"].ctypes.data, g["dbeta"].ctypes.data, g["dh0"].ctypes.data,
         None if cu is None else cu.ctypes.data, N, T, H, dk, dv, float(b), GATES[gate],
         int(nthreads))
     if rc != 0:
-        raise ValueError(f"gdr_oracle_bwd rejected its arguments (code {rc})")
+        raise ValueError(f"{fn} rejected its arguments (code {rc})")
     return g
 
 

@@ -456,6 +456,139 @@ int gdr_oracle_bwd(const void *q, const void *k, const void *v, const void *a,
     return rc;
 }
 
+/*
+ * Gradients for the per-channel decay form of gdr_oracle_fwd_vec: row i of the
+ * state decays by al_i = exp(g(a_{t,i})).  With Hb = diag(al) H_{t-1}, the
+ * token's adjoint step is that of gdr_oracle_bwd with alpha replaced row by row:
+ *     dk_i += sum_j al_i H_{t-1}[i][j] dp_j       (from p = Hb^T k)
+ *     dal_i = sum_j H_{t-1}[i][j] dHb[i][j]       dH[i][j] <- al_i dHb[i][j]
+ *     da_{t,i} = dal_i al_i g'(a_{t,i})           (da is [rows, dk])
+ */
+int gdr_oracle_bwd_vec(const void *q, const void *k, const void *v, const void *a,
+                       const void *beta, int in_dtype, const double *h0, const double *dout,
+                       const double *dhT, double *dq, double *dk_out, double *dv_out, double *da,
+                       double *dbeta, double *dh0, const int64_t *cu_seqlens, int B, int64_t T,
+                       int H, int dk, int dv, double b, int gate, int nthreads)
+{
+    if (B < 1 || T < 0 || H < 1 || dk < 1 || dv < 1) return 1;
+    if (in_dtype < OR_BF16 || in_dtype > OR_F64) return 1;
+    const int N = B;
+    if (cu_seqlens) {
+        if (cu_seqlens[0] != 0) return 2;
+        for (int n = 0; n < N; n++)
+            if (cu_seqlens[n + 1] < cu_seqlens[n]) return 2;
+        if (cu_seqlens[N] != T) return 2;
+    }
+    const int64_t S = (int64_t)dk * dv;
+    const int64_t nunit = (int64_t)N * H;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int rc = 0;
+#pragma omp parallel
+    {
+        double *dH = (double *)malloc(sizeof(double) * (size_t)S);
+        double *al = (double *)malloc(sizeof(double) * (size_t)dk);
+        double *kt = (double *)malloc(sizeof(double) * (size_t)dk);
+        double *qt = (double *)malloc(sizeof(double) * (size_t)dk);
+        double *pr = (double *)malloc(sizeof(double) * (size_t)dv);
+        double *de = (double *)malloc(sizeof(double) * (size_t)dv);
+        double *gp = (double *)malloc(sizeof(double) * (size_t)dv);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t u = 0; u < nunit; u++) {
+            const int h = (int)(u % H);
+            const int n = (int)(u / H);
+            const int64_t t_begin = cu_seqlens ? cu_seqlens[n] : (int64_t)n * T;
+            const int64_t len = (cu_seqlens ? cu_seqlens[n + 1] : t_begin + T) - t_begin;
+            /* every state H_0 .. H_len of this (sequence, head): small cases only */
+            double *Hs = (double *)malloc(sizeof(double) * (size_t)(len + 1) * S);
+            if (!Hs) {
+                rc = 3;
+                continue;
+            }
+            for (int64_t e = 0; e < S; e++) Hs[e] = h0 ? h0[u * S + e] : 0.0;
+            for (int64_t t = 0; t < len; t++) {
+                const int64_t row = (t_begin + t) * H + h;
+                const double bt = widen(beta, in_dtype, row);
+                const double *Hp = Hs + t * S;
+                double *Hn = Hs + (t + 1) * S;
+                for (int i = 0; i < dk; i++) {
+                    al[i] = exp(gdr_oracle_gate(widen(a, in_dtype, (row * dk) + i), b, gate));
+                    kt[i] = widen(k, in_dtype, row * dk + i);
+                }
+                for (int j = 0; j < dv; j++) {
+                    double acc = 0.0;
+                    for (int i = 0; i < dk; i++) acc += al[i] * Hp[i * dv + j] * kt[i];
+                    de[j] = bt * (widen(v, in_dtype, row * dv + j) - acc);
+                }
+                for (int i = 0; i < dk; i++)
+                    for (int j = 0; j < dv; j++) Hn[i * dv + j] = al[i] * Hp[i * dv + j] + kt[i] * de[j];
+            }
+            for (int64_t e = 0; e < S; e++) dH[e] = dhT ? dhT[u * S + e] : 0.0;
+            for (int64_t t = len - 1; t >= 0; t--) {
+                const int64_t row = (t_begin + t) * H + h;
+                const double bt = widen(beta, in_dtype, row);
+                const double *Hp = Hs + t * S, *Ht = Hs + (t + 1) * S;
+                for (int i = 0; i < dk; i++) {
+                    al[i] = exp(gdr_oracle_gate(widen(a, in_dtype, (row * dk) + i), b, gate));
+                    kt[i] = widen(k, in_dtype, row * dk + i);
+                    qt[i] = widen(q, in_dtype, row * dk + i);
+                }
+                for (int j = 0; j < dv; j++) {
+                    double acc = 0.0;
+                    for (int i = 0; i < dk; i++) acc += al[i] * Hp[i * dv + j] * kt[i];
+                    pr[j] = acc;
+                    de[j] = bt * (widen(v, in_dtype, row * dv + j) - acc);
+                }
+                /* o = H_t^T q: dq, and dH gains q do^T */
+                for (int i = 0; i < dk; i++) {
+                    double acc = 0.0;
+                    for (int j = 0; j < dv; j++) {
+                        const double go = dout ? dout[row * dv + j] : 0.0;
+                        acc += Ht[i * dv + j] * go;
+                        dH[i * dv + j] += go * qt[i];
+                    }
+                    dq[row * dk + i] = acc;
+                }
+                /* H_t = Hb + k delta^T, delta = beta (v - Hb^T k) */
+                double db = 0.0;
+                for (int j = 0; j < dv; j++) {
+                    double gd = 0.0;
+                    for (int i = 0; i < dk; i++) gd += kt[i] * dH[i * dv + j];
+                    dv_out[row * dv + j] = bt * gd;
+                    db += gd * (widen(v, in_dtype, row * dv + j) - pr[j]);
+                    gp[j] = -bt * gd;
+                }
+                dbeta[row] = db;
+                for (int i = 0; i < dk; i++) {
+                    double gk = 0.0, dal = 0.0;
+                    for (int j = 0; j < dv; j++) {
+                        const double hb_bar = dH[i * dv + j] + kt[i] * gp[j];
+                        gk += dH[i * dv + j] * de[j] + al[i] * Hp[i * dv + j] * gp[j];
+                        dal += Hp[i * dv + j] * hb_bar;
+                        dH[i * dv + j] = al[i] * hb_bar;
+                    }
+                    dk_out[row * dk + i] = gk;
+                    da[row * dk + i] = dal * al[i] * gate_grad(widen(a, in_dtype, (row * dk) + i), b, gate);
+                }
+            }
+            if (dh0)
+                for (int64_t e = 0; e < S; e++) dh0[u * S + e] = dH[e];
+            free(Hs);
+        }
+        free(dH);
+        free(al);
+        free(kt);
+        free(qt);
+        free(pr);
+        free(de);
+        free(gp);
+    }
+    return rc;
+}
+
 /* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
 int gdr_oracle_max_threads(void)
 {

@@ -10,6 +10,8 @@ before the delta-rule write:  H_t = (I - beta_t k_t k_t^T) diag(alpha_t) H_{t-1}
     is dropped;
   - beta = 0 (pure per-channel decay) and one-hot keys (only that row is
     rewritten, every other row only decays).
+Its backward (``oracle_bwd_vec``) is pinned by finite differences of the forward
+and by its reduction to the scalar backward when all channels share a.
 Planted one-token mistakes in copies of the C source must fail the battery.
 """
 import math
@@ -153,3 +155,83 @@ def test_vec_mutant_is_rejected(tmp_path, name):
     ok = np.allclose(out[0, :, 0], ro, rtol=1e-11, atol=1e-12) and \
         np.allclose(hT[0, 0], rh, rtol=1e-11, atol=1e-12)
     assert not ok
+
+
+# --------------------------------------------------------------------------
+# per-channel backward (oracle_bwd_vec)
+# --------------------------------------------------------------------------
+def _vec_loss(x, dout, dhT, b, cu=None):
+    out, hT = oracle.oracle_fwd_vec(x["q"], x["k"], x["v"], x["a"], x["beta"], h0=x["h0"],
+                                    cu_seqlens=cu, b=b)
+    return float((out * dout).sum() + (hT * dhT).sum())
+
+
+@pytest.mark.parametrize("T,dk,dv,varlen", [(6, 3, 4, False), (40, 4, 3, False), (30, 3, 2, True)])
+def test_vec_backward_matches_finite_differences(T, dk, dv, varlen):
+    rng = np.random.default_rng(40 + T)
+    q, k, v, a, beta, h0 = _vec_case(rng, T, H=2, dk=dk, dv=dv)
+    cu = np.array([0, 4, 4, T], dtype=np.int64) if varlen else None
+    N = 3 if varlen else 1
+    h0 = 0.3 * rng.standard_normal((N, 2, dk, dv))
+    x = dict(q=q, k=k, v=v, a=a, beta=beta, h0=h0)
+    dout = rng.standard_normal(v.shape)
+    dhT = rng.standard_normal((N, 2, dk, dv))
+    g = oracle.oracle_bwd_vec(q, k, v, a, beta, dout=dout, dhT=dhT, h0=h0, cu_seqlens=cu, b=2.0)
+    grads = {"q": g["dq"], "k": g["dk"], "v": g["dv"], "a": g["da"], "beta": g["dbeta"],
+             "h0": g["dh0"]}
+    eps = 1e-5
+    for name, grad in grads.items():
+        R = rng.standard_normal(x[name].shape)
+        fd = (_vec_loss(dict(x, **{name: x[name] + eps * R}), dout, dhT, 2.0, cu)
+              - _vec_loss(dict(x, **{name: x[name] - eps * R}), dout, dhT, 2.0, cu)) / (2 * eps)
+        an = float((grad * R).sum())
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(fd)), (name, fd, an)
+
+
+def test_vec_backward_with_equal_channels_is_the_scalar_backward():
+    """All channels sharing a: every gradient equals the scalar backward's, and the
+    per-channel da summed over the channels equals the scalar da."""
+    rng = np.random.default_rng(41)
+    q, k, v, _, beta, h0 = _case(rng, 25, H=2, dk=5, dv=4, B=2)
+    a = rng.standard_normal((2, 25, 2))
+    av = np.repeat(a[..., None], 5, axis=-1)
+    dout = rng.standard_normal(v.shape)
+    dhT = rng.standard_normal(h0.shape)
+    gs = oracle.oracle_bwd(q, k, v, a, beta, dout=dout, dhT=dhT, h0=h0, b=2.0)
+    gv = oracle.oracle_bwd_vec(q, k, v, av, beta, dout=dout, dhT=dhT, h0=h0, b=2.0)
+    for name in ("dq", "dk", "dv", "dbeta", "dh0"):
+        np.testing.assert_allclose(gv[name], gs[name], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(gv["da"].sum(axis=-1), gs["da"], rtol=1e-11, atol=1e-12)
+
+
+VEC_BWD_MUTANTS = {
+    "k_grad_without_row_decay": ("gk += dH[i * dv + j] * de[j] + al[i] * Hp[i * dv + j] * gp[j];",
+                                 "gk += dH[i * dv + j] * de[j] + Hp[i * dv + j] * gp[j];"),
+    "decay_grad_reads_new_state": ("dal += Hp[i * dv + j] * hb_bar;", "dal += Ht[i * dv + j] * hb_bar;"),
+}
+
+
+@pytest.mark.parametrize("name", list(VEC_BWD_MUTANTS))
+def test_vec_backward_mutant_is_rejected(tmp_path, name):
+    old, new = VEC_BWD_MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, name
+    c, so = tmp_path / f"{name}.c", tmp_path / f"{name}.so"
+    c.write_text(src.replace(old, new))
+    subprocess.run(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-o", str(so), str(c),
+                    "-lm"], check=True)
+    rng = np.random.default_rng(42)
+    q, k, v, a, beta, h0 = _vec_case(rng, 8, dk=4, dv=3)
+    x = dict(q=q, k=k, v=v, a=a, beta=beta, h0=h0)
+    dout = rng.standard_normal(v.shape)
+    dhT = rng.standard_normal(h0.shape)
+    g = oracle.oracle_bwd_vec(q, k, v, a, beta, dout=dout, dhT=dhT, h0=h0, b=2.0, _lib_path=str(so))
+    grads = {"q": g["dq"], "k": g["dk"], "v": g["dv"], "a": g["da"], "beta": g["dbeta"],
+             "h0": g["dh0"]}
+    caught = False
+    for xname, grad in grads.items():
+        R = rng.standard_normal(x[xname].shape)
+        fd = (_vec_loss(dict(x, **{xname: x[xname] + 1e-5 * R}), dout, dhT, 2.0)
+              - _vec_loss(dict(x, **{xname: x[xname] - 1e-5 * R}), dout, dhT, 2.0)) / 2e-5
+        caught |= abs(fd - float((grad * R).sum())) > 1e-6 * max(1.0, abs(fd))
+    assert caught
