@@ -241,6 +241,8 @@ def parse_args(argv=None):
     ap.add_argument("--decode-seqs", type=int, default=256)
     ap.add_argument("--bwd-seqs", type=int, default=8)
     ap.add_argument("--bwd-tokens", type=int, default=4096)
+    ap.add_argument("--bwd-per-channel", action="store_true",
+                    help="backward of the per-channel decay form (gdr_chunk_bwd_vec)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     return args
@@ -452,7 +454,11 @@ def bench_backward(args):
     import chunked_gated_delta_07_gb300 as gdr
     from gdr_inputs import WORKLOADS, make_inputs
     N, T, H, d = args.bwd_seqs, args.bwd_tokens, 16, 128
+    from gdr_inputs import make_channel_gate
     x = make_inputs(WORKLOADS["t1m"].with_(B=N, h0_std=0.02, seed=4500), device="cuda", T=T)
+    vec = args.bwd_per_channel
+    if vec:
+        x["a"] = make_channel_gate(x, 4502)
     g = torch.Generator(device="cuda").manual_seed(4501)
     dout = torch.randn(x["v"].shape, generator=g, device="cuda").to(torch.bfloat16)
     dhT = 0.1 * torch.randn((N, H, d, d), generator=g, device="cuda")
@@ -461,9 +467,14 @@ def bench_backward(args):
     stream = torch.cuda.current_stream()
 
     def step():
-        rc = gdr.gdr_chunk_bwd(x["q"], x["k"], x["v"], x["a"], x["beta"], x["h0"], dout, dhT,
-                               *outs, dh0, None, N, T, H, d, d, 16, 2.0, gdr.GDR_BF16,
-                               gdr.GDR_GATE_BOUNDED, stream)
+        if vec:
+            rc = gdr.gdr_chunk_bwd_vec(x["q"], x["k"], x["v"], x["a"], x["beta"], x["h0"], dout,
+                                       dhT, *outs, dh0, None, N, T, H, d, d, 16, 2.0, gdr.GDR_BF16,
+                                       stream)
+        else:
+            rc = gdr.gdr_chunk_bwd(x["q"], x["k"], x["v"], x["a"], x["beta"], x["h0"], dout, dhT,
+                                   *outs, dh0, None, N, T, H, d, d, 16, 2.0, gdr.GDR_BF16,
+                                   gdr.GDR_GATE_BOUNDED, stream)
         if rc != gdr.GDR_OK:
             raise gdr.GdrError(rc, "gdr_chunk_bwd")
 
@@ -495,7 +506,8 @@ def bench_backward(args):
     peak = bf16_tf / 2.0
     achieved = flops / (ms / 1e3) / 1e12
     print(json.dumps({
-        "metric": "backward tokens/s, gated delta rule, 16 heads, d=128, bf16 in/out, fp32 math",
+        "metric": ("backward tokens/s, gated delta rule" + (" with per-channel decay" if vec else "")
+                   + ", 16 heads, d=128, bf16 in/out, fp32 math"),
         "value": N * T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",

@@ -29,7 +29,7 @@ EXPORTS = ("gdr_chunk_fwd", "gdr_chunk_fwd_ex", "gdr_chunk_fwd_workspace_size",
            "gdr_chunk_fwd_host", "gdr_gate_cumsum", "gdr_wy_repr", "gdr_get_status",
            "gdr_status_string", "gdr_release", "gdr_launch_count", "gdr_profile_enable",
            "gdr_profile_read", "gdr_chunk_fwd_noalloc", "gdr_recurrent_fwd", "gdr_chunk_bwd", "gdr_chunk_fwd_vec",
-           "gdr_router_topk", "gdr_router_bias_update")
+           "gdr_router_topk", "gdr_router_bias_update", "gdr_chunk_bwd_vec")
 
 _lock = threading.Lock()
 _lib = None
@@ -54,6 +54,7 @@ _SIGS = {
     "gdr_chunk_fwd_vec": (_I, [_P] * 9 + [_I, _I64, _I, _I, _I, _I, _F, _I, _P]),
     "gdr_router_topk": (_I, [_P] * 5 + [_I64, _I, _I, _I, _P]),
     "gdr_router_bias_update": (_I, [_P] * 3 + [_I, _I, ctypes.c_double, ctypes.c_double, _F, _P]),
+    "gdr_chunk_bwd_vec": (_I, [_P] * 15 + [_I, _I64, _I, _I, _I, _I, _F, _I, _P]),
 }
 
 
@@ -187,6 +188,32 @@ def chunk_fwd_vec(q, k, v, a, beta, h0=None, cu_seqlens=None, b=2.0, want_state=
     if rc != GDR_OK:
         raise GdrError(rc, "gdr_chunk_fwd_vec")
     return out, hT
+
+
+def gdr_chunk_bwd_vec(q, k, v, a, beta, h0, dout, dhT, dq, dk, dv, da, dbeta, dh0, cu_seqlens, B,
+                      T, H, dk_dim, dv_dim, chunk, b, dtype, stream=None) -> int:
+    """Backward of the per-channel decay form (a and da are [..., H, dk])."""
+    return lib().gdr_chunk_bwd_vec(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(beta), _ptr(h0),
+                                   _ptr(dout), _ptr(dhT), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(da),
+                                   _ptr(dbeta), _ptr(dh0), _ptr(cu_seqlens), B, T, H, dk_dim, dv_dim,
+                                   chunk, float(b), dtype, _stream(stream))
+
+
+def chunk_bwd_vec(q, k, v, a, beta, dout=None, dhT=None, h0=None, cu_seqlens=None, b=2.0,
+                  want_dh0=True, stream=None):
+    """Allocate and return (dq, dk, dv, da, dbeta, dh0) of the per-channel form."""
+    import torch
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    dq, dkk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    da, dbeta = torch.empty_like(a), torch.empty_like(beta)
+    dh0 = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device) if want_dh0 else None
+    rc = gdr_chunk_bwd_vec(q, k, v, a, beta, h0, dout, dhT, dq, dkk, dvv, da, dbeta, dh0,
+                           cu_seqlens, N, T, H, dk, dv, 16, b, dtype_code(q), stream)
+    if rc != GDR_OK:
+        raise GdrError(rc, "gdr_chunk_bwd_vec")
+    return dq, dkk, dvv, da, dbeta, dh0
 
 
 GDR_QB_SIGN, GDR_QB_PROPORTIONAL = 0, 1

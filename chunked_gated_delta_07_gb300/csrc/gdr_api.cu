@@ -594,25 +594,31 @@ static bool bwd_force_token_path() {
     return e && e[0] == '1';
 }
 
-gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const void *a,
+static gdr_status_t chunk_bwd_impl(const void *q, const void *k, const void *v, const void *a,
                            const void *beta, const float *h0, const void *dout,
                            const float *dhT, void *dq, void *dk_out, void *dv_out, void *da,
                            void *dbeta, float *dh0, const int32_t *cu_seqlens, int B,
                            int64_t T, int H, int dk, int dv, int chunk, float b,
-                           gdr_dtype_t dtype, gdr_gate_t gate, gdr_stream_t stream_) {
+                           gdr_dtype_t dtype, gdr_gate_t gate, gdr_stream_t stream_,
+                           bool per_channel) {
     Shape s;
     // the forward's checks (with dq standing in for out in the aliasing tests)
     gdr_status_t st = check_args(q, k, v, a, beta, h0, dq, nullptr, cu_seqlens, B, T, H, dk, dv,
                                  chunk, b, dtype, gate, GDR_PATH_SIMT, &s);
     if (st != GDR_OK) return st;
     if (s.T_total > 0 && (!dq || !dk_out || !dv_out || !da || !dbeta)) return GDR_ERR_INVALID_ARG;
+    // the per-channel form exists as the chunked tensor-core form only
+    if (per_channel && (dtype != GDR_BF16 || dk != 128 || dv != 128 || gate != GDR_GATE_BOUNDED ||
+                        b > kVecMaxB || chunk != kBwTile))
+        return GDR_ERR_UNSUPPORTED;
     const size_t es = dtype == GDR_BF16 ? 2 : 4;
     const size_t rows = (size_t)s.T_total * H;
+    const size_t a_b = rows * (per_channel ? dk : 1) * es;   // a and da
     const void *ins[6] = {q, k, v, a, beta, dout};
-    const size_t in_b[6] = {rows * dk * es, rows * dk * es, rows * dv * es, rows * es, rows * es,
+    const size_t in_b[6] = {rows * dk * es, rows * dk * es, rows * dv * es, a_b, rows * es,
                             rows * dv * es};
     void *outs[5] = {dq, dk_out, dv_out, da, dbeta};
-    const size_t out_b[5] = {rows * dk * es, rows * dk * es, rows * dv * es, rows * es, rows * es};
+    const size_t out_b[5] = {rows * dk * es, rows * dk * es, rows * dv * es, a_b, rows * es};
     for (int i = 0; i < 5; ++i)
         for (int j = 0; j < 6; ++j)
             if (overlaps(outs[i], out_b[i], ins[j], in_b[j])) return GDR_ERR_INVALID_ARG;
@@ -631,8 +637,9 @@ gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const vo
     const size_t plan_b = align_up(3 * sizeof(int64_t) * (size_t)(B + 1));
     // the chunked tensor-core form takes bf16, d = 128 and the bounded gate (its
     // factored in-tile decays need exp(16 b) < FLT_MAX); the rest runs token by token
-    const bool chunked = dtype == GDR_BF16 && dk == 128 && dv == 128 && gate == GDR_GATE_BOUNDED &&
-                         b <= kVecMaxB && !bwd_force_token_path();
+    const bool chunked = per_channel || (dtype == GDR_BF16 && dk == 128 && dv == 128 &&
+                                         gate == GDR_GATE_BOUNDED && b <= kVecMaxB &&
+                                         !bwd_force_token_path());
     const int seg = chunked ? chunk_bwd_segment_tiles(tiles, H, ctx->sms) : (1 << 30);
     const int64_t segs = s.varlen ? (tiles + seg - 1) / seg + B : (int64_t)B * ((tiles / B + seg - 1) / seg);
     const size_t need = plan_b + (chunked ? chunk_bwd_scratch_bytes(tiles, B, H)
@@ -651,13 +658,34 @@ gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const vo
         return GDR_ERR_CUDA;
     if (chunked)
         return launch_chunk_bwd(q, k, v, a, beta, h0, dout, dhT, dq, dk_out, dv_out, da, dbeta, dh0,
-                                plan, H, tiles, segs, b, false, ws + plan_b, stream) == cudaSuccess
+                                plan, H, tiles, segs, b, per_channel, ws + plan_b, stream) == cudaSuccess
                    ? GDR_OK
                    : GDR_ERR_CUDA;
     return launch_bwd(q, k, v, a, beta, h0, dout, dhT, dq, dk_out, dv_out, da, dbeta, dh0, dtype,
                       plan, H, dk, dv, s.T_total, tiles, b, gate, ws + plan_b, stream) == cudaSuccess
                ? GDR_OK
                : GDR_ERR_CUDA;
+}
+
+gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const void *a,
+                           const void *beta, const float *h0, const void *dout,
+                           const float *dhT, void *dq, void *dk_out, void *dv_out, void *da,
+                           void *dbeta, float *dh0, const int32_t *cu_seqlens, int B,
+                           int64_t T, int H, int dk, int dv, int chunk, float b,
+                           gdr_dtype_t dtype, gdr_gate_t gate, gdr_stream_t stream) {
+    return chunk_bwd_impl(q, k, v, a, beta, h0, dout, dhT, dq, dk_out, dv_out, da, dbeta, dh0,
+                          cu_seqlens, B, T, H, dk, dv, chunk, b, dtype, gate, stream, false);
+}
+
+gdr_status_t gdr_chunk_bwd_vec(const void *q, const void *k, const void *v, const void *a,
+                               const void *beta, const float *h0, const void *dout,
+                               const float *dhT, void *dq, void *dk_out, void *dv_out, void *da,
+                               void *dbeta, float *dh0, const int32_t *cu_seqlens, int B,
+                               int64_t T, int H, int dk, int dv, int chunk, float b,
+                               gdr_dtype_t dtype, gdr_stream_t stream) {
+    return chunk_bwd_impl(q, k, v, a, beta, h0, dout, dhT, dq, dk_out, dv_out, da, dbeta, dh0,
+                          cu_seqlens, B, T, H, dk, dv, chunk, b, dtype, GDR_GATE_BOUNDED, stream,
+                          true);
 }
 
 gdr_status_t gdr_chunk_fwd_vec(const void *q, const void *k, const void *v, const void *a,

@@ -880,10 +880,10 @@ bwd_tile_kernel(const BcArgs A) {
             float acc = 0.f;
             for (int i = len - 1; i >= 0; --i) {
                 acc += Ob[i * kLd + d] + (i == len - 1 ? rG[d] : 0.f);
+                // g'(a) = -b s (1 - s) with s = -g / b, i.e. g (1 + g / b); g from the cumsum
+                const float gi = Gb[i * kLd + d] - (i > 0 ? Gb[(i - 1) * kLd + d] : 0.f);
                 const int64_t r = ((t0 + i) * A.H + h) * kD + d;
-                const float av = __bfloat162float(A.a[r]);
-                const float sg = 1.f / (1.f + expf(-av));
-                A.da[r] = __float2bfloat16_rn(acc * (-A.b * sg * (1.f - sg)));
+                A.da[r] = __float2bfloat16_rn(acc * gi * (1.f + gi / A.b));
             }
         }
     } else {

@@ -252,6 +252,21 @@ GDR_API gdr_status_t gdr_chunk_fwd_vec(const void *q, const void *k, const void 
                                const int32_t *cu_seqlens, int B, int64_t T, int H, int dk, int dv,
                                int chunk, float b, gdr_dtype_t dtype, gdr_stream_t stream);
 
+/*
+ * Backward of the per-channel decay form (gdr_chunk_fwd_vec): gradients of
+ * <dout, out> + <dhT, hT> with respect to q, k, v, a, beta and h0, as for
+ * gdr_chunk_bwd, except that a and da are [tokens, H, dk] (one gate input and one
+ * gradient per key channel).  It runs the chunked tensor-core form only: bf16,
+ * dk = dv = 128, chunk 16, 0 < b <= 5 (GDR_ERR_UNSUPPORTED otherwise); the
+ * bounded gate is implied.  Errors, ownership and streams as for gdr_chunk_bwd.
+ */
+GDR_API gdr_status_t gdr_chunk_bwd_vec(const void *q, const void *k, const void *v, const void *a,
+                               const void *beta, const float *h0, const void *dout,
+                               const float *dhT, void *dq, void *dk_out, void *dv_out, void *da,
+                               void *dbeta, float *dh0, const int32_t *cu_seqlens, int B,
+                               int64_t T, int H, int dk, int dv, int chunk, float b,
+                               gdr_dtype_t dtype, gdr_stream_t stream);
+
 /* Bias-update rule of the quantile-balancing router (see gdr_router_bias_update). */
 typedef enum { GDR_QB_SIGN = 0, GDR_QB_PROPORTIONAL = 1 } gdr_qb_mode_t;
 
