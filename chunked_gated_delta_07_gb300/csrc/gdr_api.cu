@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <deque>
 #include <mutex>
 #include <vector>
 
@@ -72,7 +73,8 @@ struct DeviceCtx {
 };
 
 std::mutex g_mu;
-std::vector<DeviceCtx> g_ctx;
+// a deque: growing it for a new device keeps every handed-out context in place
+std::deque<DeviceCtx> g_ctx;
 
 // The calling thread's current device context, with its status word
 // allocated.  Returns nullptr on a CUDA failure.
