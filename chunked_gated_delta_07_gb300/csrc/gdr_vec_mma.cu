@@ -181,28 +181,25 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
         Hs[r * kLd + c] = from_h0 ? h0[hbase + e] : 0.f;
     }
     const int64_t sstart = p.seq_start[n], e_end = p.seq_start[n + 1];
-    // registers holding one tile's raw inputs
-    __nv_bfloat16 ra[kT], rk[kT], rq[kT];
+    // Staging is split over all 256 threads: lanes 2d and 2d + 1 of a warp take key
+    // (and value) channel d, tokens 0-7 and 8-15; the second half gets the first
+    // half's cumulative log-decay from its neighbour lane.
+    const int sd = tid >> 1, shalf = tid & 1, si0 = 8 * shalf;
+    __nv_bfloat16 ra[8], rk[8], rq[8], rv[8];
     float rb = 0.f;
     auto fetch = [&](int64_t tt) {
         const int64_t t0 = sstart + tt * kT;
         const int len = tt < s1 ? (int)min((int64_t)kT, e_end - t0) : 0;
-        if (tid < kD) {
 #pragma unroll
-            for (int i = 0; i < kT; ++i)
-                if (i < len) {
-                    const int64_t r = ((t0 + i) * H + h) * kD + tid;
-                    ra[i] = a[r];
-                    rk[i] = k[r];
-                    rq[i] = q[r];
-                }
-        } else {
-            const int c = tid - kD;
-#pragma unroll
-            for (int i = 0; i < kT; ++i)
-                if (i < len) ra[i] = v[((t0 + i) * H + h) * kD + c];
-            if (c < len) rb = __bfloat162float(beta[(t0 + c) * H + h]);
-        }
+        for (int u = 0; u < 8; ++u)
+            if (si0 + u < len) {
+                const int64_t r = ((t0 + si0 + u) * H + h) * kD + sd;
+                ra[u] = a[r];
+                rk[u] = k[r];
+                rq[u] = q[r];
+                rv[u] = v[r];
+            }
+        if (tid < len) rb = __bfloat162float(beta[(t0 + tid) * H + h]);
     };
     for (int64_t tt = w0; tt < s1; ++tt) {
         const int64_t t0 = sstart + tt * kT;
@@ -211,30 +208,38 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
         fetch(tt);         // every load of the tile, issued together
         __syncthreads();   // the previous tile is done with every staging buffer
         // ---- stage the tile: factored decays per key channel, V and beta
-        if (tid < kD) {
-            const int d = tid;
-            float G = 0.f, eGC = 1.f;
+        {
+            float gl[8], G = 0.f;
 #pragma unroll
-            for (int i = 0; i < kT; ++i) {
-                float kt = 0.f, kh = 0.f, qt = 0.f;
+            for (int u = 0; u < 8; ++u) {
+                gl[u] = si0 + u < len ? gate_logdecay(__bfloat162float(ra[u]), b, GDR_GATE_BOUNDED) : 0.f;
+                G += gl[u];
+            }
+            const float Gfirst = __shfl_xor_sync(0xffffffffu, G, 1);   // the other half's total
+            G = shalf ? Gfirst : 0.f;                                    // offset of this half
+            float eGC = 1.f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = si0 + u;
+                float kt = 0.f, kh = 0.f, qt = 0.f, vv = 0.f;
                 if (i < len) {
-                    G += gate_logdecay(__bfloat162float(ra[i]), b, GDR_GATE_BOUNDED);
-                    const float e = expf(G), en = expf(-G), kd = __bfloat162float(rk[i]);
+                    G += gl[u];
+                    const float e = expf(G), en = expf(-G), kd = __bfloat162float(rk[u]);
                     kt = kd * e;
                     kh = kd * en;
-                    qt = __bfloat162float(rq[i]) * e;
+                    qt = __bfloat162float(rq[u]) * e;
+                    vv = __bfloat162float(rv[u]);
                     eGC = e;
                 }
-                Kt[i * kLd + d] = kt;
-                Kh[i * kLd + d] = kh;
-                Qt[i * kLd + d] = qt;
+                Kt[i * kLd + sd] = kt;
+                Kh[i * kLd + sd] = kh;
+                Qt[i * kLd + sd] = qt;
+                Ub[i * kLd + sd] = vv;
             }
-            eg[d] = eGC;
-        } else {
-            const int c = tid - kD;
-#pragma unroll
-            for (int i = 0; i < kT; ++i) Ub[i * kLd + c] = i < len ? __bfloat162float(ra[i]) : 0.f;
-            if (c < kT) bs[c] = c < len ? rb : 0.f;
+            // e^{G_C} of channel d: from the half that holds the tile's last token
+            const float other = __shfl_xor_sync(0xffffffffu, eGC, 1);
+            if (shalf == 0) eg[sd] = len > 8 ? other : eGC;
+            if (tid < kT) bs[tid] = tid < len ? rb : 0.f;
         }
         __syncthreads();
         // ---- A = beta (.) strict_lower(Kt Kh^T) and P = lower(Qt Kh^T): warps 0-3
