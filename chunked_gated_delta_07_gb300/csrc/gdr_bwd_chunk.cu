@@ -72,55 +72,60 @@ __device__ __forceinline__ float gate_in(const __nv_bfloat16 *a, int64_t row, in
     return __bfloat162float(VEC ? a[row * kD + d] : a[row]);
 }
 
-// Stage one tile: per key channel (threads 0..127) the cumulative log-decay and the
-// factored rows; the other 128 threads load one 128-wide input (V or dO) and beta.
+// Stage one tile over all 256 threads: lanes 2d and 2d + 1 of a warp take key channel
+// d (and column d of the 128-wide input `other`, V or dO), tokens 0-7 and 8-15; the
+// second half gets the first half's cumulative log-decay from its neighbour lane.
+// Writes the factored rows, G (if Gb), e^{G_C} per channel and beta.
 template <bool VEC>
 __device__ __forceinline__ void stage_tile(const BcArgs &A, int64_t t0, int len, int h, float *Kt,
                                            float *Kh, float *Qt, float *Gb, float *eg,
                                            const __nv_bfloat16 *other, float *Ob, float *bs) {
     const int tid = threadIdx.x;
-    if (tid < kD) {
-        const int d = tid;
-        // every load of the tile first, then the arithmetic
-        __nv_bfloat16 ra[kT], rk[kT], rq[kT];
+    const int d = tid >> 1, half = tid & 1, i0 = 8 * half;
+    // every load of the tile first, then the arithmetic
+    __nv_bfloat16 ra[8], rk[8], rq[8], ro[8];
 #pragma unroll
-        for (int i = 0; i < kT; ++i)
-            if (i < len) {
-                const int64_t row = (t0 + i) * A.H + h;
-                ra[i] = VEC ? A.a[row * kD + d] : A.a[row];
-                rk[i] = A.k[row * kD + d];
-                if (Qt) rq[i] = A.q[row * kD + d];
-            }
-        float G = 0.f, eGC = 1.f;
-#pragma unroll
-        for (int i = 0; i < kT; ++i) {
-            float kt = 0.f, kh = 0.f, qt = 0.f, gg = 0.f;
-            if (i < len) {
-                G += gate_logdecay(__bfloat162float(ra[i]), A.b, GDR_GATE_BOUNDED);
-                const float e = expf(G), en = expf(-G), kd = __bfloat162float(rk[i]);
-                kt = kd * e;
-                kh = kd * en;
-                if (Qt) qt = __bfloat162float(rq[i]) * e;
-                eGC = e;
-                gg = G;
-            }
-            Kt[i * kLd + d] = kt;
-            Kh[i * kLd + d] = kh;
-            if (Qt) Qt[i * kLd + d] = qt;
-            if (Gb) Gb[i * kLd + d] = gg;
+    for (int u = 0; u < 8; ++u)
+        if (i0 + u < len) {
+            const int64_t row = (t0 + i0 + u) * A.H + h;
+            ra[u] = VEC ? A.a[row * kD + d] : A.a[row];
+            rk[u] = A.k[row * kD + d];
+            if (Qt) rq[u] = A.q[row * kD + d];
+            if (other) ro[u] = other[row * kD + d];
         }
-        eg[d] = eGC;
-    } else {
-        const int c = tid - kD;
-        __nv_bfloat16 ro[kT];
+    const float bt = tid < len ? __bfloat162float(A.beta[(t0 + tid) * A.H + h]) : 0.f;
+    float gl[8], G = 0.f;
 #pragma unroll
-        for (int i = 0; i < kT; ++i)
-            if (i < len && other) ro[i] = other[((t0 + i) * A.H + h) * kD + c];
-        const float bt = c < len ? __bfloat162float(A.beta[(t0 + c) * A.H + h]) : 0.f;
-#pragma unroll
-        for (int i = 0; i < kT; ++i) Ob[i * kLd + c] = (i < len && other) ? __bfloat162float(ro[i]) : 0.f;
-        if (c < kT) bs[c] = bt;
+    for (int u = 0; u < 8; ++u) {
+        gl[u] = i0 + u < len ? gate_logdecay(__bfloat162float(ra[u]), A.b, GDR_GATE_BOUNDED) : 0.f;
+        G += gl[u];
     }
+    const float Gfirst = __shfl_xor_sync(0xffffffffu, G, 1);
+    G = half ? Gfirst : 0.f;
+    float eGC = 1.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u;
+        float kt = 0.f, kh = 0.f, qt = 0.f, gg = 0.f, ov = 0.f;
+        if (i < len) {
+            G += gl[u];
+            const float e = expf(G), en = expf(-G), kd = __bfloat162float(rk[u]);
+            kt = kd * e;
+            kh = kd * en;
+            if (Qt) qt = __bfloat162float(rq[u]) * e;
+            if (other) ov = __bfloat162float(ro[u]);
+            eGC = e;
+            gg = G;
+        }
+        Kt[i * kLd + d] = kt;
+        Kh[i * kLd + d] = kh;
+        if (Qt) Qt[i * kLd + d] = qt;
+        if (Gb) Gb[i * kLd + d] = gg;
+        Ob[i * kLd + d] = ov;
+    }
+    const float eo = __shfl_xor_sync(0xffffffffu, eGC, 1);
+    if (half == 0) eg[d] = len > 8 ? eo : eGC;
+    if (tid < kT) bs[tid] = bt;
 }
 
 // 16 x 16 product X Y^T over K = 128 (one 8-column half of the output per warp):
