@@ -623,14 +623,25 @@ bwd_tile_kernel(const BcArgs A) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
     const int c0 = 16 * warp;
     const size_t st = ((size_t)c * A.H + h) * kD * kD;
+    // a bf16 state into Sh and, asynchronously, without registers
     auto stage_state = [&](const __nv_bfloat16 *src) {
 #pragma unroll
         for (int e = tid * 8; e < kD * kD; e += kThreads * 8) {
             const int r = e >> 7, col = e & (kD - 1);
-            *(uint4 *)&Sh[r * kLdh + col] = *(const uint4 *)&src[e];
+            cp_async16(&Sh[r * kLdh + col], &src[e]);
         }
     };
-    // ---- stage: factored rows, G, dO, D, V; dH1 into the state buffer
+    // ---- stage: dH1 and D by asynchronous copies, then the factored rows, G, dO, V
+    stage_state(A.dHst + st);
+    {
+        const float *Dg = A.Dst + ((size_t)c * A.H + h) * kT * kD;
+#pragma unroll
+        for (int e = tid * 4; e < kT * kD; e += kThreads * 4) {
+            const int i = e >> 7, col = e & (kD - 1);
+            cp_async16(&Db[i * kLd + col], &Dg[e]);
+        }
+    }
+    cp_async_commit();
     stage_tile<VEC>(A, t0, len, h, Kt, Kh, Qt, VEC ? Gb : nullptr, eg, A.dout, Ob, bs);
     if (!VEC && tid >= kThreads - kT) {
         // scalar gate: g and g'(a) per token, one load each (the cumsum follows the barrier)
@@ -648,10 +659,9 @@ bwd_tile_kernel(const BcArgs A) {
 #pragma unroll
     for (int e = tid; e < kT * kD; e += kThreads) {
         const int i = e >> 7, col = e & (kD - 1);
-        Db[i * kLd + col] = A.Dst[((size_t)c * A.H + h) * kT * kD + e];
         Ub[i * kLd + col] = i < len ? __bfloat162float(A.v[((t0 + i) * A.H + h) * kD + col]) : 0.f;
     }
-    stage_state(A.dHst + st);
+    cp_async_wait_all();
     __syncthreads();
     // ---- Ke dH1 (this warp's dv columns) and dKe = D dH1^T (this warp's dk columns),
     // then the 16 x 16 products
@@ -677,6 +687,25 @@ bwd_tile_kernel(const BcArgs A) {
             mma8(dke[nt], ad, b0, b1);
         }
     }
+    // e^{G_C} rowsum(dH1 (.) H0): dH1 from shared memory, H0 rows from the stored copy
+    {
+        const __nv_bfloat16 *H0g = A.Hst + st;
+        uint2 xh[kD / 8];
+#pragma unroll
+        for (int m = 0; m < kD / 8; ++m) xh[m] = *(const uint2 *)&H0g[(warp + 8 * m) * kD + 4 * lane];
+#pragma unroll
+        for (int m = 0; m < kD / 8; ++m) {
+            const int r = warp + 8 * m;
+            const uint2 yh = *(const uint2 *)&Sh[r * kLdh + 4 * lane];
+            const __nv_bfloat162 *x2 = (const __nv_bfloat162 *)&xh[m], *y2 = (const __nv_bfloat162 *)&yh;
+            const float2 xa = __bfloat1622float2(x2[0]), xb = __bfloat1622float2(x2[1]);
+            const float2 ya = __bfloat1622float2(y2[0]), yb = __bfloat1622float2(y2[1]);
+            float pr = xa.x * ya.x + xa.y * ya.y + xb.x * yb.x + xb.y * yb.y;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) pr += __shfl_xor_sync(0xffffffffu, pr, o);
+            if (lane == 0) rG[r] = eg[r] * pr;
+        }
+    }
     if (warp < 2) build_A(Kt, Kh, bs, Am, KK, warp, g, t);
     else if (warp < 4) build_lower(Qt, Kh, Sm, warp - 2, g, t);
     else if (warp < 6) build_lower(Ob, Db, dS, warp - 4, g, t);   // dS = lower(dO D^T)
@@ -693,6 +722,9 @@ bwd_tile_kernel(const BcArgs A) {
     if (tid < kD)
         for (int i = 0; i < kT; ++i) Wb[i * kLd + tid] = Kt[i * kLd + tid];
     __syncthreads();
+    // ---- H0 into the state buffer (asynchronous: dH1 is no longer needed)
+    stage_state(A.Hst + st);
+    cp_async_commit();
     // ---- W and U; dD = Ke dH1 + S^T dO into Eb (this warp's dv columns)
     fwd_subst(tid < kD ? Wb : Ub, tid & (kD - 1), Am, bs);
 #pragma unroll
@@ -714,24 +746,7 @@ bwd_tile_kernel(const BcArgs A) {
         Eb[(g + 8) * kLd + col] = dd[nt][2];
         Eb[(g + 8) * kLd + col + 1] = dd[nt][3];
     }
-    __syncthreads();
-    // ---- H0 into the state buffer, and e^{G_C} rowsum(dH1 (.) H0) from the stored copies
-    {
-        const __nv_bfloat16 *H0g = A.Hst + st, *dH1g = A.dHst + st;
-#pragma unroll 4
-        for (int r = warp; r < kD; r += 8) {
-            const uint2 xh = *(const uint2 *)&H0g[r * kD + 4 * lane];
-            const uint2 yh = *(const uint2 *)&dH1g[r * kD + 4 * lane];
-            *(uint2 *)&Sh[r * kLdh + 4 * lane] = xh;
-            const __nv_bfloat162 *x2 = (const __nv_bfloat162 *)&xh, *y2 = (const __nv_bfloat162 *)&yh;
-            const float2 xa = __bfloat1622float2(x2[0]), xb = __bfloat1622float2(x2[1]);
-            const float2 ya = __bfloat1622float2(y2[0]), yb = __bfloat1622float2(y2[1]);
-            float p = xa.x * ya.x + xa.y * ya.y + xb.x * yb.x + xb.y * yb.y;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
-            if (lane == 0) rG[r] = eg[r] * p;
-        }
-    }
+    cp_async_wait_all();   // H0 landed (own copies); the barrier publishes them and dD
     __syncthreads();
     // ---- dQt_a = dO H0^T and dW = -dD H0^T (this warp's dk columns); dW into Db
     float dq[2][4];

@@ -78,3 +78,15 @@ __device__ __forceinline__ void load_bt_h(uint32_t &b0, uint32_t &b1, const __nv
 }
 
 }  // namespace gdr
+
+namespace gdr {
+
+// 16-byte asynchronous copy global -> shared (completion: cp_async_wait_all)
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+}  // namespace gdr
