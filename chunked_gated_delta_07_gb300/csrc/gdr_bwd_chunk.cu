@@ -656,10 +656,13 @@ bwd_tile_kernel(const BcArgs A) {
         Gb[i] = gi;
         Gb[kT + i] = dgi;
     }
+    // V, kept in registers for the dV / dbeta pass (same element per thread there)
+    __nv_bfloat16 rv[kT / 2];
 #pragma unroll
-    for (int e = tid; e < kT * kD; e += kThreads) {
-        const int i = e >> 7, col = e & (kD - 1);
-        Ub[i * kLd + col] = i < len ? __bfloat162float(A.v[((t0 + i) * A.H + h) * kD + col]) : 0.f;
+    for (int m = 0; m < kT / 2; ++m) {
+        const int i = (tid >> 7) + 2 * m, col = tid & (kD - 1);
+        rv[m] = i < len ? A.v[((t0 + i) * A.H + h) * kD + col] : __float2bfloat16_rn(0.f);
+        Ub[i * kLd + col] = __bfloat162float(rv[m]);
     }
     cp_async_wait_all();
     __syncthreads();
@@ -823,7 +826,7 @@ bwd_tile_kernel(const BcArgs A) {
                 const int64_t r = ((t0 + i) * A.H + h) * kD + col;
                 const float yu = Eb[i * kLd + col];
                 A.dv[r] = __float2bfloat16_rn(bs[i] * yu);
-                x = fmaf(yu, __bfloat162float(A.v[r]), Db[i * kLd + col] * Kt[i * kLd + col]);
+                x = fmaf(yu, __bfloat162float(rv[m]), Db[i * kLd + col] * Kt[i * kLd + col]);
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
