@@ -13,11 +13,9 @@
 
 namespace gdr {
 
-__device__ __forceinline__ uint32_t tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
+// The tensor cores read the top 19 bits of an fp32 operand (sign, exponent and 10
+// mantissa bits); the low bits are ignored, which truncates rather than rounds.
+__device__ __forceinline__ uint32_t tf32(float x) { return __float_as_uint(x); }
 
 // d += a * b
 __device__ __forceinline__ void mma8(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
