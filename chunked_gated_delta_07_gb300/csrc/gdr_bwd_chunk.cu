@@ -72,32 +72,42 @@ __device__ __forceinline__ float gate_in(const __nv_bfloat16 *a, int64_t row, in
     return __bfloat162float(VEC ? a[row * kD + d] : a[row]);
 }
 
-// Stage one tile over all 256 threads: lanes 2d and 2d + 1 of a warp take key channel
-// d (and column d of the 128-wide input `other`, V or dO), tokens 0-7 and 8-15; the
-// second half gets the first half's cumulative log-decay from its neighbour lane.
-// Writes the factored rows, G (if Gb), e^{G_C} per channel and beta.
-template <bool VEC>
-__device__ __forceinline__ void stage_tile(const BcArgs &A, int64_t t0, int len, int h, float *Kt,
-                                           float *Kh, float *Qt, float *Gb, float *eg,
-                                           const __nv_bfloat16 *other, float *Ob, float *bs) {
-    const int tid = threadIdx.x;
-    const int d = tid >> 1, half = tid & 1, i0 = 8 * half;
-    // every load of the tile first, then the arithmetic
+// Staging of one tile over all 256 threads: lanes 2d and 2d + 1 of a warp take key
+// channel d (and column d of the 128-wide input `other`, V or dO), tokens 0-7 and 8-15;
+// the second half gets the first half's cumulative log-decay from its neighbour lane.
+// stage_fetch issues every global load of the tile into registers; stage_compute
+// writes the factored rows, G (if Gb), e^{G_C} per channel and beta.
+struct StageRegs {
     __nv_bfloat16 ra[8], rk[8], rq[8], ro[8];
+    float bt;
+};
+
+template <bool VEC>
+__device__ __forceinline__ void stage_fetch(const BcArgs &A, int64_t t0, int len, int h, bool with_q,
+                                            const __nv_bfloat16 *other, StageRegs &R) {
+    const int tid = threadIdx.x;
+    const int d = tid >> 1, i0 = 8 * (tid & 1);
 #pragma unroll
     for (int u = 0; u < 8; ++u)
         if (i0 + u < len) {
             const int64_t row = (t0 + i0 + u) * A.H + h;
-            ra[u] = VEC ? A.a[row * kD + d] : A.a[row];
-            rk[u] = A.k[row * kD + d];
-            if (Qt) rq[u] = A.q[row * kD + d];
-            if (other) ro[u] = other[row * kD + d];
+            R.ra[u] = VEC ? A.a[row * kD + d] : A.a[row];
+            R.rk[u] = A.k[row * kD + d];
+            if (with_q) R.rq[u] = A.q[row * kD + d];
+            if (other) R.ro[u] = other[row * kD + d];
         }
-    const float bt = tid < len ? __bfloat162float(A.beta[(t0 + tid) * A.H + h]) : 0.f;
+    R.bt = tid < len ? __bfloat162float(A.beta[(t0 + tid) * A.H + h]) : 0.f;
+}
+
+__device__ __forceinline__ void stage_compute(const BcArgs &A, int len, const StageRegs &R, float *Kt,
+                                              float *Kh, float *Qt, float *Gb, float *eg, bool has_other,
+                                              float *Ob, float *bs) {
+    const int tid = threadIdx.x;
+    const int d = tid >> 1, half = tid & 1, i0 = 8 * half;
     float gl[8], G = 0.f;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-        gl[u] = i0 + u < len ? gate_logdecay(__bfloat162float(ra[u]), A.b, GDR_GATE_BOUNDED) : 0.f;
+        gl[u] = i0 + u < len ? gate_logdecay(__bfloat162float(R.ra[u]), A.b, GDR_GATE_BOUNDED) : 0.f;
         G += gl[u];
     }
     const float Gfirst = __shfl_xor_sync(0xffffffffu, G, 1);
@@ -109,11 +119,11 @@ __device__ __forceinline__ void stage_tile(const BcArgs &A, int64_t t0, int len,
         float kt = 0.f, kh = 0.f, qt = 0.f, gg = 0.f, ov = 0.f;
         if (i < len) {
             G += gl[u];
-            const float e = expf(G), en = expf(-G), kd = __bfloat162float(rk[u]);
+            const float e = expf(G), en = expf(-G), kd = __bfloat162float(R.rk[u]);
             kt = kd * e;
             kh = kd * en;
-            if (Qt) qt = __bfloat162float(rq[u]) * e;
-            if (other) ov = __bfloat162float(ro[u]);
+            if (Qt) qt = __bfloat162float(R.rq[u]) * e;
+            if (has_other) ov = __bfloat162float(R.ro[u]);
             eGC = e;
             gg = G;
         }
@@ -125,7 +135,16 @@ __device__ __forceinline__ void stage_tile(const BcArgs &A, int64_t t0, int len,
     }
     const float eo = __shfl_xor_sync(0xffffffffu, eGC, 1);
     if (half == 0) eg[d] = len > 8 ? eo : eGC;
-    if (tid < kT) bs[tid] = bt;
+    if (tid < kT) bs[tid] = R.bt;
+}
+
+template <bool VEC>
+__device__ __forceinline__ void stage_tile(const BcArgs &A, int64_t t0, int len, int h, float *Kt,
+                                           float *Kh, float *Qt, float *Gb, float *eg,
+                                           const __nv_bfloat16 *other, float *Ob, float *bs) {
+    StageRegs R;
+    stage_fetch<VEC>(A, t0, len, h, Qt != nullptr, other, R);
+    stage_compute(A, len, R, Kt, Kh, Qt, Gb, eg, other != nullptr, Ob, bs);
 }
 
 // 16 x 16 product X Y^T over K = 128 (one 8-column half of the output per warp):
