@@ -714,7 +714,9 @@ gdr_status_t gdr_chunk_fwd_vec(const void *q, const void *k, const void *v, cons
     }
     DeviceCtx *ctx = device_ctx();
     if (!ctx) return GDR_ERR_CUDA;
-    const bool fused = dtype == GDR_BF16 && dk == 128 && dv == 128;   // tensor-core kernel
+    // tensor-core kernel; it writes out in 16-byte pieces, so an unaligned out takes
+    // the CUDA-core kernels
+    const bool fused = dtype == GDR_BF16 && dk == 128 && dv == 128 && (uintptr_t)out % 16 == 0;
     const int64_t tiles = tile_bound(s.varlen, B, T, kVecTile);
     const size_t plan_b = align_up(3 * sizeof(int64_t) * (size_t)(B + 1));
     const int seg = fused ? vec_mma_segment_tiles(tiles, H, ctx->sms) : (1 << 30);

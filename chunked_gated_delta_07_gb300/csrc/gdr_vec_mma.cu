@@ -1,7 +1,15 @@
 // gdr_vec_mma.cu -- per-channel decay forward, bf16 inputs, dk = dv = 128:
-// one fused kernel per (sequence, head) that keeps the 128 x 128 fp32 state in
-// shared memory and runs every dense product of a 16-token tile on the tensor
-// cores (mma.sync m16n8k8, tf32 operands, fp32 accumulation).
+// one fused kernel per (segment, head) that keeps the 128 x 128 fp32 state in
+// registers and runs every dense product of a 16-token tile on the tensor cores
+// (mma.sync m16n8k8, tf32 operands, fp32 accumulation).
+//
+// The state is held transposed, H^T (value channel x key channel), as accumulator
+// fragments: warp w owns value channels 16w..16w+15, every thread 64 values.  A
+// thread's accumulator holds key channels 2t and 2t + 1 of each 8-wide block, which
+// is exactly what an A-operand fragment needs if the reduction index inside the
+// block is read in the order (2t, 2t + 1) <-> slots (t, t + 4); the B operand is
+// loaded from shared memory in the same order, so the sum is unchanged and the
+// state never leaves the registers.
 //
 // Per tile, with per-channel cumulative log-decay G (resetting each tile) and
 // the factored decays Kt = K (.) exp(G), Kh = K (.) exp(-G), Qt = Q (.) exp(G)
@@ -11,8 +19,9 @@
 //        substitution, one column per thread: no explicit inverse)
 //   D = U - W H,  O = Qt H + P D                                       (tensor cores)
 //   H <- diag(exp(G_C)) H + (Kh exp(G_C))^T D                          (tensor cores)
-// Warp w owns the state columns 16w..16w+15 for D, O and the state update, so
-// those three steps need no block barrier between them; a tile takes four.
+// In the transposed form D^T = U^T - H^T W^T, O^T = H^T Qt^T + D^T P^T and
+// H^T <- H^T diag(exp(G_C)) + D^T (Kh exp(G_C)) are per-warp; a tile takes four
+// block barriers (staging, the Gram products, the substitutions, reuse).
 // Each tile's loads are issued together before its staging; two blocks share an
 // SM (a next-tile prefetch held ~48 more registers live and ran 1.5x slower).
 //
@@ -45,8 +54,7 @@ constexpr int kWarmFactor = 4;   // longest warm-up, in segments, before a pair 
 constexpr float kHorizonLog = -46.0f;    // below ln(2^-64) = -44.4, with room for fp32 sums
 
 // shared layout, in floats
-constexpr int kOffH = 0;                      // H   [128][kLd]
-constexpr int kOffKt = kOffH + kD * kLd;      // Kt, then -W   [16][kLd]
+constexpr int kOffKt = 0;                     // Kt, then -W   [16][kLd]
 constexpr int kOffKh = kOffKt + kT * kLd;     // Kh, then Kh exp(G_C)
 constexpr int kOffQt = kOffKh + kT * kLd;     // Qt
 constexpr int kOffU = kOffQt + kT * kLd;      // V, then U, then D
@@ -54,7 +62,8 @@ constexpr int kOffA = kOffU + kT * kLd;       // A [16][kPd]
 constexpr int kOffP = kOffA + kT * kPd;       // P [16][kPd]
 constexpr int kOffEg = kOffP + kT * kPd;      // exp(G_C) [128]
 constexpr int kOffB = kOffEg + kD;            // beta [16]
-constexpr int kSmemFloats = kOffB + kT;
+constexpr int kOffO = kOffB + kT;             // the tile's outputs, bf16 [16][128]
+constexpr int kSmemFloats = kOffO + kT * kD / 2;
 constexpr size_t kSmemBytes = sizeof(float) * kSmemFloats;
 
 // Per (tile, head): the log of a bound on the norm of the tile's transition,
@@ -131,8 +140,9 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
                __nv_bfloat16 *__restrict__ out, float *__restrict__ hT, Plan p, int H, float b,
                const float *__restrict__ lam, const int *__restrict__ seg_ok) {
     extern __shared__ float sm[];
-    float *Hs = sm + kOffH, *Kt = sm + kOffKt, *Kh = sm + kOffKh, *Qt = sm + kOffQt;
+    float *Kt = sm + kOffKt, *Kh = sm + kOffKh, *Qt = sm + kOffQt;
     float *Ub = sm + kOffU, *Am = sm + kOffA, *Pm = sm + kOffP, *eg = sm + kOffEg, *bs = sm + kOffB;
+    __nv_bfloat16 *Os = (__nv_bfloat16 *)(sm + kOffO);
     __shared__ int warm_start;
     const int h = blockIdx.x % H;
     const int64_t sg = blockIdx.x / H;   // global segment
@@ -140,7 +150,7 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
     if (n < 0) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
-    const int c0 = 16 * warp;   // this warp's 16 state columns
+    const int c0 = 16 * warp;   // this warp's 16 value channels
     const int64_t tile0 = p.chunk_base[n], ntiles = p.chunk_base[n + 1] - tile0;
     const int64_t j = sg - p.seg_base[n];
     const bool segmented = seg_ok[(int64_t)n * H + h] != 0;
@@ -176,30 +186,56 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
     const int64_t w0 = s0 - warm_start;   // first tile run
     const size_t hbase = ((size_t)n * H + h) * kD * kD;
     const bool from_h0 = w0 == 0 && h0;
-    for (int e = tid; e < kD * kD; e += kThreads) {
-        const int r = e >> 7, c = e & (kD - 1);
-        Hs[r * kLd + c] = from_h0 ? h0[hbase + e] : 0.f;
-    }
+    // H^T fragments: hs[nd][u] = H[d][c], c = c0 + g + 8 (u >> 1), d = 8 nd + 2t + (u & 1)
+    float hs[kD / 8][4];
+#pragma unroll
+    for (int nd = 0; nd < kD / 8; ++nd)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c = c0 + g + 8 * (u >> 1), d = 8 * nd + 2 * t + (u & 1);
+            hs[nd][u] = from_h0 ? h0[hbase + (size_t)d * kD + c] : 0.f;
+        }
     const int64_t sstart = p.seq_start[n], e_end = p.seq_start[n + 1];
     // Staging is split over all 256 threads: lanes 2d and 2d + 1 of a warp take key
     // (and value) channel d, tokens 0-7 and 8-15; the second half gets the first
     // half's cumulative log-decay from its neighbour lane.
     const int sd = tid >> 1, shalf = tid & 1, si0 = 8 * shalf;
-    __nv_bfloat16 ra[8], rk[8], rq[8], rv[8];
+    uint32_t pa[4], pk[4], pq[4], pv[4];   // two bf16 per register: tokens 2m, 2m + 1 of the half
     float rb = 0.f;
     auto fetch = [&](int64_t tt) {
         const int64_t t0 = sstart + tt * kT;
         const int len = tt < s1 ? (int)min((int64_t)kT, e_end - t0) : 0;
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-            if (si0 + u < len) {
-                const int64_t r = ((t0 + si0 + u) * H + h) * kD + sd;
-                ra[u] = a[r];
-                rk[u] = k[r];
-                rq[u] = q[r];
-                rv[u] = v[r];
+        for (int m = 0; m < 4; ++m) {
+            uint32_t xa = 0, xk = 0, xq = 0, xv = 0;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int i = si0 + 2 * m + u;
+                if (i < len) {
+                    const int64_t r = ((t0 + i) * H + h) * kD + sd;
+                    xa |= (uint32_t)__bfloat16_as_ushort(a[r]) << (16 * u);
+                    xk |= (uint32_t)__bfloat16_as_ushort(k[r]) << (16 * u);
+                    xq |= (uint32_t)__bfloat16_as_ushort(q[r]) << (16 * u);
+                    xv |= (uint32_t)__bfloat16_as_ushort(v[r]) << (16 * u);
+                }
             }
+            pa[m] = xa;
+            pk[m] = xk;
+            pq[m] = xq;
+            pv[m] = xv;
+        }
         if (tid < len) rb = __bfloat162float(beta[(t0 + tid) * H + h]);
+    };
+    auto half_f = [](uint32_t x, int u) { return __uint_as_float(u ? (x & 0xffff0000u) : (x << 16)); };
+    // outputs of a tile wait in Os until the next barrier, then go out as 256-byte rows
+    int64_t o_t0 = 0;
+    int o_len = 0;
+    auto flush_out = [&]() {
+        for (int e = tid; e < o_len * (kD / 8); e += kThreads) {
+            const int i = e / (kD / 8), c8 = e % (kD / 8);
+            *(uint4 *)&out[((o_t0 + i) * H + h) * kD + 8 * c8] = *(const uint4 *)&Os[i * kD + 8 * c8];
+        }
+        o_len = 0;
     };
     for (int64_t tt = w0; tt < s1; ++tt) {
         const int64_t t0 = sstart + tt * kT;
@@ -207,12 +243,13 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
         const bool emit = tt >= s0;   // warm-up tiles only advance the state
         fetch(tt);         // every load of the tile, issued together
         __syncthreads();   // the previous tile is done with every staging buffer
+        flush_out();       // the previous tile's outputs, whole rows
         // ---- stage the tile: factored decays per key channel, V and beta
         {
             float gl[8], G = 0.f;
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                gl[u] = si0 + u < len ? gate_logdecay(__bfloat162float(ra[u]), b, GDR_GATE_BOUNDED) : 0.f;
+                gl[u] = si0 + u < len ? gate_logdecay(half_f(pa[u >> 1], u & 1), b, GDR_GATE_BOUNDED) : 0.f;
                 G += gl[u];
             }
             const float Gfirst = __shfl_xor_sync(0xffffffffu, G, 1);   // the other half's total
@@ -224,11 +261,11 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
                 float kt = 0.f, kh = 0.f, qt = 0.f, vv = 0.f;
                 if (i < len) {
                     G += gl[u];
-                    const float e = expf(G), en = expf(-G), kd = __bfloat162float(rk[u]);
+                    const float e = expf(G), en = expf(-G), kd = half_f(pk[u >> 1], u & 1);
                     kt = kd * e;
                     kh = kd * en;
-                    qt = __bfloat162float(rq[u]) * e;
-                    vv = __bfloat162float(rv[u]);
+                    qt = half_f(pq[u >> 1], u & 1) * e;
+                    vv = half_f(pv[u >> 1], u & 1);
                     eGC = e;
                 }
                 Kt[i * kLd + sd] = kt;
@@ -236,7 +273,7 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
                 Qt[i * kLd + sd] = qt;
                 Ub[i * kLd + sd] = vv;
             }
-            // e^{G_C} of channel d: from the half that holds the tile's last token
+        // e^{G_C} of channel d: from the half that holds the tile's last token
             const float other = __shfl_xor_sync(0xffffffffu, eGC, 1);
             if (shalf == 0) eg[sd] = len > 8 ? other : eGC;
             if (tid < kT) bs[tid] = tid < len ? rb : 0.f;
@@ -292,103 +329,80 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
             }
         }
         __syncthreads();
-        // ---- D = U - W H and O = Qt H on this warp's 16 columns
-        float dacc[2][4], oacc[2][4];
+        // ---- D^T = U^T - H^T W^T and O^T = H^T Qt^T (value channels c0..c0+15)
+        float dt[2][4], ot[2][4];   // [token tile][fragment]: (c, i = 8 it + 2t + (u & 1))
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int n0 = c0 + 8 * nt;
-            dacc[nt][0] = Ub[g * kLd + n0 + 2 * t];
-            dacc[nt][1] = Ub[g * kLd + n0 + 2 * t + 1];
-            dacc[nt][2] = Ub[(g + 8) * kLd + n0 + 2 * t];
-            dacc[nt][3] = Ub[(g + 8) * kLd + n0 + 2 * t + 1];
+        for (int it = 0; it < 2; ++it)
 #pragma unroll
-            for (int u = 0; u < 4; ++u) oacc[nt][u] = 0.f;
-        }
-#pragma unroll 2
-        for (int k0 = 0; k0 < kD; k0 += 8) {
-            uint32_t aw[4], aq[4];
-            load_a(aw, Kt, kLd, 0, k0, g, t);
-            load_a(aq, Qt, kLd, 0, k0, g, t);
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int n0 = c0 + 8 * nt;
-                const uint32_t b0 = tf32(Hs[(k0 + t) * kLd + n0 + g]);
-                const uint32_t b1 = tf32(Hs[(k0 + t + 4) * kLd + n0 + g]);
-                mma8(dacc[nt], aw, b0, b1);
-                mma8(oacc[nt], aq, b0, b1);
-            }
-        }
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int n0 = c0 + 8 * nt;
-            Ub[g * kLd + n0 + 2 * t] = dacc[nt][0];
-            Ub[g * kLd + n0 + 2 * t + 1] = dacc[nt][1];
-            Ub[(g + 8) * kLd + n0 + 2 * t] = dacc[nt][2];
-            Ub[(g + 8) * kLd + n0 + 2 * t + 1] = dacc[nt][3];
-        }
-        __syncwarp();
-        // ---- O += P D, then the outputs
-        uint32_t bd[2][2][2];   // D fragments [k-step][n-tile][2]
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks)
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int n0 = c0 + 8 * nt;
-                bd[ks][nt][0] = tf32(Ub[(8 * ks + t) * kLd + n0 + g]);
-                bd[ks][nt][1] = tf32(Ub[(8 * ks + t + 4) * kLd + n0 + g]);
+            for (int u = 0; u < 4; ++u) {
+                dt[it][u] = Ub[(8 * it + 2 * t + (u & 1)) * kLd + c0 + g + 8 * (u >> 1)];
+                ot[it][u] = 0.f;
             }
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-            uint32_t ap[4];
-            load_a(ap, Pm, kPd, 0, 8 * ks, g, t);
+        for (int nd = 0; nd < kD / 8; ++nd) {
+            const uint32_t ah[4] = {tf32(hs[nd][0]), tf32(hs[nd][2]), tf32(hs[nd][1]), tf32(hs[nd][3])};
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) mma8(oacc[nt], ap, bd[ks][nt][0], bd[ks][nt][1]);
-        }
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int col = c0 + 8 * nt + 2 * t;
-            if (!emit) break;
-            if (g < len)
-                *(__nv_bfloat162 *)&out[((t0 + g) * H + h) * kD + col] =
-                    __floats2bfloat162_rn(oacc[nt][0], oacc[nt][1]);
-            if (g + 8 < len)
-                *(__nv_bfloat162 *)&out[((t0 + g + 8) * H + h) * kD + col] =
-                    __floats2bfloat162_rn(oacc[nt][2], oacc[nt][3]);
-        }
-        // ---- H <- diag(exp(G_C)) H + (Kh exp(G_C))^T D on this warp's columns
-#pragma unroll 2
-        for (int mt = 0; mt < kD / 16; ++mt) {
-            const int r0 = 16 * mt;
-            const float e0 = eg[r0 + g], e1 = eg[r0 + g + 8];
-            uint32_t ak[2][4];
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                const int k0 = 8 * ks;
-                ak[ks][0] = tf32(Kh[(k0 + t) * kLd + r0 + g]);
-                ak[ks][1] = tf32(Kh[(k0 + t) * kLd + r0 + g + 8]);
-                ak[ks][2] = tf32(Kh[(k0 + t + 4) * kLd + r0 + g]);
-                ak[ks][3] = tf32(Kh[(k0 + t + 4) * kLd + r0 + g + 8]);
+            for (int it = 0; it < 2; ++it) {
+                const float2 w2 = *(const float2 *)&Kt[(8 * it + g) * kLd + 8 * nd + 2 * t];   // -W
+                const float2 q2 = *(const float2 *)&Qt[(8 * it + g) * kLd + 8 * nd + 2 * t];
+                mma8(dt[it], ah, tf32(w2.x), tf32(w2.y));
+                mma8(ot[it], ah, tf32(q2.x), tf32(q2.y));
             }
+        }
+        // D^T as A operands over the tokens (reduction order 2t, 2t + 1 as above)
+        uint32_t ad[2][4];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int col = c0 + 8 * nt + 2 * t;
-                float *h0p = &Hs[(r0 + g) * kLd + col], *h1p = &Hs[(r0 + g + 8) * kLd + col];
-                float acc[4] = {e0 * h0p[0], e0 * h0p[1], e1 * h1p[0], e1 * h1p[1]};
+        for (int kk = 0; kk < 2; ++kk) {
+            ad[kk][0] = tf32(dt[kk][0]);
+            ad[kk][1] = tf32(dt[kk][2]);
+            ad[kk][2] = tf32(dt[kk][1]);
+            ad[kk][3] = tf32(dt[kk][3]);
+        }
+        // ---- O^T += D^T P^T, then the outputs
 #pragma unroll
-                for (int ks = 0; ks < 2; ++ks) mma8(acc, ak[ks], bd[ks][nt][0], bd[ks][nt][1]);
-                h0p[0] = acc[0];
-                h0p[1] = acc[1];
-                h1p[0] = acc[2];
-                h1p[1] = acc[3];
+        for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+            for (int it = 0; it < 2; ++it) {
+                const float2 p2 = *(const float2 *)&Pm[(8 * it + g) * kPd + 8 * kk + 2 * t];
+                mma8(ot[it], ad[kk], tf32(p2.x), tf32(p2.y));
+            }
+        if (emit) {
+#pragma unroll
+            for (int it = 0; it < 2; ++it)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = 8 * it + 2 * t + (u & 1), c = c0 + g + 8 * (u >> 1);
+                    Os[i * kD + c] = __float2bfloat16_rn(ot[it][u]);
+                }
+            o_t0 = t0;
+            o_len = len;
+        }
+        // ---- H^T <- H^T diag(exp(G_C)) + D^T (Kh exp(G_C))
+#pragma unroll
+        for (int nd = 0; nd < kD / 8; ++nd) {
+            const float e0 = eg[8 * nd + 2 * t], e1 = eg[8 * nd + 2 * t + 1];
+            hs[nd][0] *= e0;
+            hs[nd][1] *= e1;
+            hs[nd][2] *= e0;
+            hs[nd][3] *= e1;
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                const uint32_t b0 = tf32(Kh[(8 * kk + 2 * t) * kLd + 8 * nd + g]);
+                const uint32_t b1 = tf32(Kh[(8 * kk + 2 * t + 1) * kLd + 8 * nd + g]);
+                mma8(hs[nd], ad[kk], b0, b1);
             }
         }
     }
     __syncthreads();
+    flush_out();
     if (hT && s1 == ntiles)
-        for (int e = tid; e < kD * kD; e += kThreads) {
-            const int r = e >> 7, c = e & (kD - 1);
-            hT[hbase + e] = Hs[r * kLd + c];
-        }
+#pragma unroll
+        for (int nd = 0; nd < kD / 8; ++nd)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int c = c0 + g + 8 * (u >> 1), d = 8 * nd + 2 * t + (u & 1);
+                hT[hbase + (size_t)d * kD + c] = hs[nd][u];
+            }
 }
 
 }  // namespace
