@@ -138,6 +138,83 @@ __device__ __forceinline__ void stage_compute(const BcArgs &A, int len, const St
     if (tid < kT) bs[tid] = R.bt;
 }
 
+// The same staging with the raw values packed two bf16 per register (for a kernel
+// whose state takes most of its registers).
+struct StageRegsPacked {
+    uint32_t pa[4], pk[4], pq[4], po[4];   // two bf16 per register: tokens i0 + 2m, i0 + 2m + 1
+    float bt;
+};
+
+__device__ __forceinline__ float bf_half(uint32_t x, int u) {
+    return __uint_as_float(u ? (x & 0xffff0000u) : (x << 16));
+}
+
+template <bool VEC>
+__device__ __forceinline__ void stage_fetch_packed(const BcArgs &A, int64_t t0, int len, int h, bool with_q,
+                                            const __nv_bfloat16 *other, StageRegsPacked &R) {
+    const int tid = threadIdx.x;
+    const int d = tid >> 1, i0 = 8 * (tid & 1);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        uint32_t xa = 0, xk = 0, xq = 0, xo = 0;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int i = i0 + 2 * m + u;
+            if (i < len) {
+                const int64_t row = (t0 + i) * A.H + h;
+                xa |= (uint32_t)__bfloat16_as_ushort(VEC ? A.a[row * kD + d] : A.a[row]) << (16 * u);
+                xk |= (uint32_t)__bfloat16_as_ushort(A.k[row * kD + d]) << (16 * u);
+                if (with_q) xq |= (uint32_t)__bfloat16_as_ushort(A.q[row * kD + d]) << (16 * u);
+                if (other) xo |= (uint32_t)__bfloat16_as_ushort(other[row * kD + d]) << (16 * u);
+            }
+        }
+        R.pa[m] = xa;
+        R.pk[m] = xk;
+        R.pq[m] = xq;
+        R.po[m] = xo;
+    }
+    R.bt = tid < len ? __bfloat162float(A.beta[(t0 + tid) * A.H + h]) : 0.f;
+}
+
+__device__ __forceinline__ void stage_compute_packed(const BcArgs &A, int len, const StageRegsPacked &R, float *Kt,
+                                              float *Kh, float *Qt, float *Gb, float *eg, bool has_other,
+                                              float *Ob, float *bs) {
+    const int tid = threadIdx.x;
+    const int d = tid >> 1, half = tid & 1, i0 = 8 * half;
+    float gl[8], G = 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        gl[u] = i0 + u < len ? gate_logdecay(bf_half(R.pa[u >> 1], u & 1), A.b, GDR_GATE_BOUNDED) : 0.f;
+        G += gl[u];
+    }
+    const float Gfirst = __shfl_xor_sync(0xffffffffu, G, 1);
+    G = half ? Gfirst : 0.f;
+    float eGC = 1.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u;
+        float kt = 0.f, kh = 0.f, qt = 0.f, gg = 0.f, ov = 0.f;
+        if (i < len) {
+            G += gl[u];
+            const float e = expf(G), en = expf(-G), kd = bf_half(R.pk[u >> 1], u & 1);
+            kt = kd * e;
+            kh = kd * en;
+            if (Qt) qt = bf_half(R.pq[u >> 1], u & 1) * e;
+            if (has_other) ov = bf_half(R.po[u >> 1], u & 1);
+            eGC = e;
+            gg = G;
+        }
+        Kt[i * kLd + d] = kt;
+        Kh[i * kLd + d] = kh;
+        if (Qt) Qt[i * kLd + d] = qt;
+        if (Gb) Gb[i * kLd + d] = gg;
+        Ob[i * kLd + d] = ov;
+    }
+    const float eo = __shfl_xor_sync(0xffffffffu, eGC, 1);
+    if (half == 0) eg[d] = len > 8 ? eo : eGC;
+    if (tid < kT) bs[tid] = R.bt;
+}
+
 template <bool VEC>
 __device__ __forceinline__ void stage_tile(const BcArgs &A, int64_t t0, int len, int h, float *Kt,
                                            float *Kh, float *Qt, float *Gb, float *eg,
@@ -377,16 +454,25 @@ __device__ __forceinline__ bool segment_of(const BcArgs &A, int64_t sg, int h, i
 // ---------------------------------------------------------------------------
 // forward state chain: stores H0 and D of every tile
 // ---------------------------------------------------------------------------
-constexpr int kF_H = 0, kF_Kt = kF_H + kD * kLd, kF_Kh = kF_Kt + kTile2, kF_U = kF_Kh + kTile2,
-              kF_A = kF_U + kTile2, kF_eg = kF_A + kT * kPd, kF_b = kF_eg + kD,
-              kF_total = kF_b + kT;
+// The state is held in registers as transposed accumulator fragments (as in the
+// per-channel forward): warp w owns value channels 16w..16w+15; hs[nd][u] = H[d][c]
+// with c = c0 + g + 8 (u >> 1), d = 8 nd + 2t + (u & 1).  An 8-wide block of a
+// thread's fragments is an A operand if the reduction order inside the block is
+// (2t, 2t + 1) <-> slots (t, t + 4), and the shared-memory B operand is read in that
+// order too.  Each tile's entering state goes out in bf16 through Hb, its D through
+// Db, both written by the warps idle during the Gram products one step later.
+constexpr int kF_Kt = 0, kF_Kh = kF_Kt + kTile2, kF_U = kF_Kh + kTile2, kF_D = kF_U + kTile2,
+              kF_A = kF_D + kTile2, kF_eg = kF_A + kT * kPd, kF_b = kF_eg + kD,
+              kF_Hb = kF_b + kT,                                   // bf16 [128][kLdh]
+              kF_total = kF_Hb + kD * kLdh / 2;
 
 template <bool VEC>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 bwd_fwd_chain_kernel(const BcArgs A) {
     extern __shared__ float sm[];
-    float *Hs = sm + kF_H, *Kt = sm + kF_Kt, *Kh = sm + kF_Kh, *Ub = sm + kF_U, *Am = sm + kF_A;
+    float *Kt = sm + kF_Kt, *Kh = sm + kF_Kh, *Ub = sm + kF_U, *Db = sm + kF_D, *Am = sm + kF_A;
     float *eg = sm + kF_eg, *bs = sm + kF_b;
+    __nv_bfloat16 *Hb = (__nv_bfloat16 *)(sm + kF_Hb);
     __shared__ int64_t first;
     const int h = blockIdx.x % A.H;
     int n;
@@ -403,87 +489,107 @@ bwd_fwd_chain_kernel(const BcArgs A) {
     __syncthreads();
     const int64_t w0 = first;
     const size_t sbase = ((size_t)n * A.H + h) * kD * kD;
-    copy_state_in(Hs, (w0 == 0 && A.h0) ? A.h0 + sbase : nullptr);
+    const bool from_h0 = w0 == 0 && A.h0;
+    float hs[kD / 8][4];
+#pragma unroll
+    for (int nd = 0; nd < kD / 8; ++nd)
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            hs[nd][u] = from_h0 ? A.h0[sbase + (size_t)(8 * nd + 2 * t + (u & 1)) * kD + c0 + g + 8 * (u >> 1)] : 0.f;
+    int64_t d_tile = -1;   // tile whose D waits in Db
+    // bf16 state in Hb and D in Db go out as whole rows (threads [64, 256))
+    auto copy_out = [&](int64_t c_state, int64_t c_d) {
+        if (tid < 64) return;
+        const int q = tid - 64;
+        if (c_state >= 0) {
+            __nv_bfloat16 *dst = A.Hst + ((size_t)c_state * A.H + h) * kD * kD;
+            for (int e = q; e < kD * kD / 8; e += kThreads - 64) {
+                const int r = e >> 4, c8 = e & 15;
+                *(uint4 *)&dst[r * kD + 8 * c8] = *(const uint4 *)&Hb[r * kLdh + 8 * c8];
+            }
+        }
+        if (c_d >= 0) {
+            float *dst = A.Dst + ((size_t)c_d * A.H + h) * kT * kD;
+            for (int e = q; e < kT * kD / 4; e += kThreads - 64) {
+                const int i = e >> 5, c4 = e & 31;
+                *(float4 *)&dst[i * kD + 4 * c4] = *(const float4 *)&Db[i * kLd + 4 * c4];
+            }
+        }
+    };
     for (int64_t tt = w0; tt < s1; ++tt) {
         const int64_t t0 = s + tt * kT, c = tile0 + tt;
         const int len = (int)min((int64_t)kT, e_end - t0);
         const bool keep = tt >= s0;   // warm-up tiles only advance the state
         __syncthreads();
-        stage_tile<VEC>(A, t0, len, h, Kt, Kh, nullptr, nullptr, eg, A.v, Ub, bs);
+        {
+            StageRegsPacked R;
+            stage_fetch_packed<VEC>(A, t0, len, h, false, A.v, R);
+            stage_compute_packed(A, len, R, Kt, Kh, nullptr, nullptr, eg, true, Ub, bs);
+        }
+        if (keep)
+#pragma unroll
+            for (int nd = 0; nd < kD / 8; ++nd)
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    Hb[(8 * nd + 2 * t + (u & 1)) * kLdh + c0 + g + 8 * (u >> 1)] = __float2bfloat16_rn(hs[nd][u]);
         __syncthreads();
         if (warp < 2) build_A(Kt, Kh, bs, Am, nullptr, warp, g, t);
-        else if (keep) copy_state_out_h(Hs, A.Hst + ((size_t)c * A.H + h) * kD * kD, 64);
+        else copy_out(keep ? c : -1, d_tile);
         __syncthreads();
         fwd_subst(tid < kD ? Kt : Ub, tid & (kD - 1), Am, bs);   // Kt -> W, V -> U
         if (tid < kD)
             for (int i = 0; i < kT; ++i) Kh[i * kLd + tid] *= eg[tid];   // Ke
         __syncthreads();
-        // D = U - W H0 on this warp's columns; stored for the tile-gradient kernel
-        float dacc[2][4];
+        // D^T = U^T - H^T W^T (this warp's value channels)
+        float dt[2][4];   // (c, i = 8 it + 2t + (u & 1))
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int n0 = c0 + 8 * nt;
-            dacc[nt][0] = Ub[g * kLd + n0 + 2 * t];
-            dacc[nt][1] = Ub[g * kLd + n0 + 2 * t + 1];
-            dacc[nt][2] = Ub[(g + 8) * kLd + n0 + 2 * t];
-            dacc[nt][3] = Ub[(g + 8) * kLd + n0 + 2 * t + 1];
-        }
-#pragma unroll 2
-        for (int k0 = 0; k0 < kD; k0 += 8) {
-            uint32_t aw[4];
-            load_a(aw, Kt, kLd, 0, k0, g, t);
-            aw[0] ^= 0x80000000u;   // -W: flip the sign bits
-            aw[1] ^= 0x80000000u;
-            aw[2] ^= 0x80000000u;
-            aw[3] ^= 0x80000000u;
+        for (int it = 0; it < 2; ++it)
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                uint32_t b0, b1;
-                load_b(b0, b1, Hs, kLd, k0, c0 + 8 * nt, g, t);
-                mma8(dacc[nt], aw, b0, b1);
+            for (int u = 0; u < 4; ++u) dt[it][u] = Ub[(8 * it + 2 * t + (u & 1)) * kLd + c0 + g + 8 * (u >> 1)];
+#pragma unroll
+        for (int nd = 0; nd < kD / 8; ++nd) {
+            const uint32_t ah[4] = {tf32(hs[nd][0]), tf32(hs[nd][2]), tf32(hs[nd][1]), tf32(hs[nd][3])};
+#pragma unroll
+            for (int it = 0; it < 2; ++it) {
+                const float2 w2 = *(const float2 *)&Kt[(8 * it + g) * kLd + 8 * nd + 2 * t];
+                mma8(dt[it], ah, tf32(-w2.x), tf32(-w2.y));
             }
         }
-        float *Dg = A.Dst + ((size_t)c * A.H + h) * kT * kD;
+        if (keep) {
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int col = c0 + 8 * nt + 2 * t;
-            Ub[g * kLd + col] = dacc[nt][0];
-            Ub[g * kLd + col + 1] = dacc[nt][1];
-            Ub[(g + 8) * kLd + col] = dacc[nt][2];
-            Ub[(g + 8) * kLd + col + 1] = dacc[nt][3];
-            if (keep) {
-                *(float2 *)&Dg[g * kD + col] = make_float2(dacc[nt][0], dacc[nt][1]);
-                *(float2 *)&Dg[(g + 8) * kD + col] = make_float2(dacc[nt][2], dacc[nt][3]);
-            }
+            for (int it = 0; it < 2; ++it)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) Db[(8 * it + 2 * t + (u & 1)) * kLd + c0 + g + 8 * (u >> 1)] = dt[it][u];
+            d_tile = c;
+        } else {
+            d_tile = -1;
         }
-        __syncwarp();
-        // H1 = diag(e^{G_C}) H0 + Ke^T D on this warp's columns
-        uint32_t bd[2][2][2];
+        // H1^T = H0^T diag(e^{G_C}) + D^T Ke
+        uint32_t ad[2][4];
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks)
+        for (int kk = 0; kk < 2; ++kk) {
+            ad[kk][0] = tf32(dt[kk][0]);
+            ad[kk][1] = tf32(dt[kk][2]);
+            ad[kk][2] = tf32(dt[kk][1]);
+            ad[kk][3] = tf32(dt[kk][3]);
+        }
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) load_b(bd[ks][nt][0], bd[ks][nt][1], Ub, kLd, 8 * ks, c0 + 8 * nt, g, t);
-#pragma unroll 2
-        for (int mt = 0; mt < kD / 16; ++mt) {
-            const int r0 = 16 * mt;
-            const float e0 = eg[r0 + g], e1 = eg[r0 + g + 8];
-            uint32_t ak[2][4];
+        for (int nd = 0; nd < kD / 8; ++nd) {
+            const float e0 = eg[8 * nd + 2 * t], e1 = eg[8 * nd + 2 * t + 1];
+            hs[nd][0] *= e0;
+            hs[nd][1] *= e1;
+            hs[nd][2] *= e0;
+            hs[nd][3] *= e1;
 #pragma unroll
-            for (int ks = 0; ks < 2; ++ks) load_at(ak[ks], Kh, kLd, r0, 8 * ks, g, t);
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int col = c0 + 8 * nt + 2 * t;
-                float *p0 = &Hs[(r0 + g) * kLd + col], *p1 = &Hs[(r0 + g + 8) * kLd + col];
-                float acc[4] = {e0 * p0[0], e0 * p0[1], e1 * p1[0], e1 * p1[1]};
-#pragma unroll
-                for (int ks = 0; ks < 2; ++ks) mma8(acc, ak[ks], bd[ks][nt][0], bd[ks][nt][1]);
-                p0[0] = acc[0];
-                p0[1] = acc[1];
-                p1[0] = acc[2];
-                p1[1] = acc[3];
+            for (int kk = 0; kk < 2; ++kk) {
+                const uint32_t b0 = tf32(Kh[(8 * kk + 2 * t) * kLd + 8 * nd + g]);
+                const uint32_t b1 = tf32(Kh[(8 * kk + 2 * t + 1) * kLd + 8 * nd + g]);
+                mma8(hs[nd], ad[kk], b0, b1);
             }
         }
     }
+    __syncthreads();
+    copy_out(-1, d_tile);   // the last tile's D
 }
 
 // ---------------------------------------------------------------------------
