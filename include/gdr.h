@@ -244,7 +244,9 @@ GDR_API gdr_status_t gdr_recurrent_fwd(const void *q, const void *k, const void 
  *        for gdr_chunk_fwd_ex.
  * chunk must be 16 and 0 < b <= 5 (exp(16 b) must stay below FLT_MAX):
  * GDR_ERR_UNSUPPORTED otherwise; b <= 0 is GDR_ERR_INVALID_ARG.  Only the
- * bounded gate is taken (an unbounded one can overflow exp(-G)).  Scratch
+ * bounded gate is taken (an unbounded one can overflow exp(-G)).  bf16 with
+ * dk = dv = 128 runs a fused tensor-core kernel when `out` is 16-byte aligned;
+ * other shapes, fp32 and unaligned `out` run the CUDA-core kernels.  Scratch
  * comes from the internal per-device cache; asynchronous on `stream`.
  */
 GDR_API gdr_status_t gdr_chunk_fwd_vec(const void *q, const void *k, const void *v, const void *a,
