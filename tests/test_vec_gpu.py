@@ -124,3 +124,20 @@ def test_vec_packed_long_and_short_sequences():
     g = torch.Generator(device="cpu").manual_seed(5801)
     x["h0"] = (0.05 * torch.randn((5, 2, 128, 128), generator=g)).cuda()
     _check(x, "bf16")
+
+
+def test_vec_unaligned_output_takes_the_cuda_core_kernels():
+    """bf16 d = 128 with `out` not 16-byte aligned: the fused kernel writes 16-byte
+    pieces, so the call runs the CUDA-core kernels; the result is the same."""
+    x = _inputs("bf16", 128, 40, seed=5900, N=1, H=2)
+    buf = torch.empty(x["v"].numel() + 8, dtype=torch.bfloat16, device="cuda")
+    out = buf[1:1 + x["v"].numel()].view(x["v"].shape)          # 2 bytes past an aligned start
+    hT = torch.empty((1, 2, 128, 128), dtype=torch.float32, device="cuda")
+    rc = gdr.gdr_chunk_fwd_vec(x["q"], x["k"], x["v"], x["av"], x["beta"], x["h0"], out, hT, None,
+                               1, 40, 2, 128, 128, 16, 2.0, gdr.GDR_BF16)
+    assert rc == gdr.GDR_OK
+    torch.cuda.synchronize()
+    assert gdr.gdr_get_status() == gdr.GDR_OK
+    ro, rh = oracle.oracle_fwd_vec(x["q"], x["k"], x["v"], x["av"], x["beta"], h0=x["h0"], b=2.0)
+    assert_close(to64(out), ro, "bf16", "out")
+    assert_close(to64(hT), rh, "bf16", "hT")
