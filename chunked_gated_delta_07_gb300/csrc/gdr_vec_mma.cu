@@ -22,20 +22,22 @@
 // In the transposed form D^T = U^T - H^T W^T, O^T = H^T Qt^T + D^T P^T and
 // H^T <- H^T diag(exp(G_C)) + D^T (Kh exp(G_C)) are per-warp; a tile takes four
 // block barriers (staging, the Gram products, the substitutions, reuse).
-// Each tile's loads are issued together before its staging; two blocks share an
-// SM (a next-tile prefetch held ~48 more registers live and ran 1.5x slower).
+// Each tile's loads are issued together before its staging (two bf16 per register);
+// two blocks share an SM (holding the next tile's inputs in registers during the
+// current tile measured slower).  The outputs of a tile wait in shared memory and go
+// out as whole rows after the next barrier.
 //
 // Long sequences are cut into segments of S tiles (the plan's seg_chunks, 64 to 256,
 // larger when there are enough (segment, head) blocks to fill the GPU), one block per
 // (segment, head).  A block starts from a zero state at a warm-up tile w before
 // its segment and runs the state update alone up to the segment start.  The
 // state entering tile w reaches the segment start multiplied by a product of
-// (I - beta k k^T) diag(alpha_t); with beta |k|^2 in [0, 2] each factor has
-// norm <= max_d alpha_{t,d}, so the neglected term is at most
-// exp(sum_t max_d g_{t,d}) times that state.  w is the latest tile that makes
-// this bound <= 2^-64 (far below fp32 resolution), or the sequence start,
-// where the block starts from h0 exactly.  vec_bound_kernel sums
-// max_d g per (tile, head); vec_decide_kernel marks the (sequence, head)
+// (I - beta k k^T) diag(alpha_t); each factor has norm at most
+// max(1, |1 - beta |k|^2|) max_d alpha_{t,d}, so the neglected term is at most
+// the product of those times that state.  w is the latest tile that makes this
+// bound <= e^-46 < 2^-64 (far below fp32 resolution), or the sequence start,
+// where the block starts from h0 exactly.  vec_bound_kernel sums the bound's log
+// per (tile, head); vec_decide_kernel marks the (sequence, head)
 // pairs whose decay is too weak for a warm-up of at most 4 S tiles: those
 // run as one block over the whole sequence, exactly as without segments.
 #include "gdr_internal.cuh"
@@ -57,7 +59,7 @@ constexpr float kHorizonLog = -46.0f;    // below ln(2^-64) = -44.4, with room f
 constexpr int kOffKt = 0;                     // Kt, then -W   [16][kLd]
 constexpr int kOffKh = kOffKt + kT * kLd;     // Kh, then Kh exp(G_C)
 constexpr int kOffQt = kOffKh + kT * kLd;     // Qt
-constexpr int kOffU = kOffQt + kT * kLd;      // V, then U, then D
+constexpr int kOffU = kOffQt + kT * kLd;      // V, then U
 constexpr int kOffA = kOffU + kT * kLd;       // A [16][kPd]
 constexpr int kOffP = kOffA + kT * kPd;       // P [16][kPd]
 constexpr int kOffEg = kOffP + kT * kPd;      // exp(G_C) [128]
