@@ -19,10 +19,10 @@
 //        sum_i dKe (.) Ke + e^{G_C} (.) rowsum(dH1 (.) H0);  dg = reverse cumsum of dG
 //   dq = dQt (.) e^G,  dk = dKt (.) e^G + dKh (.) e^-G,  da = dg g'(a)
 // Three kernels:
-//   bwd_fwd_chain_kernel  per (sequence, head): the state chain; stores H0 and D of
-//                         every tile
-//   bwd_adj_chain_kernel  per (sequence, head), tiles in reverse: the dH chain; stores
-//                         dH1 of every tile and writes dh0
+//   bwd_fwd_chain_kernel  per (segment, head): the state chain (state in registers);
+//                         stores H0 and D of every tile
+//   bwd_adj_chain_kernel  per (segment, head), tiles in reverse: the dH chain (state in
+//                         shared memory); stores dH1 of every tile, and dh0
 //   bwd_tile_kernel       per (tile, head), all tiles at once: every input gradient
 // The scalar-gate form is the per-channel form with every channel's gate equal.
 //
