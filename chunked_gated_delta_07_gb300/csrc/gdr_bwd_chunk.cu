@@ -724,7 +724,7 @@ template <bool VEC> struct TileLayout {
                          am = eb + kTile2, kk = am + kT * kPd, smx = kk + kT * kPd,
                          ds = smx + kT * kPd, da = ds + kT * kPd, bda = da + kT * kPd,
                          eg = bda + kT * kPd, rg = eg + kD, bs = rg + kD, rs = bs + kT,
-                         gb = rs + 4 * kT, sh = gb + (VEC ? kTile2 : 2 * kT), total_f = sh;
+                         rs2 = rs + 4 * kT, gb = rs2 + kT, sh = gb + (VEC ? kTile2 : 2 * kT), total_f = sh;
     static constexpr size_t bytes = sizeof(float) * total_f + sizeof(__nv_bfloat16) * kD * kLdh;
 };
 
@@ -737,6 +737,7 @@ bwd_tile_kernel(const BcArgs A) {
     float *Ub = sm + L::ub, *Wb = sm + L::wb, *Eb = sm + L::eb;
     float *Am = sm + L::am, *KK = sm + L::kk, *Sm = sm + L::smx, *dS = sm + L::ds, *dA = sm + L::da;
     float *bdA = sm + L::bda, *eg = sm + L::eg, *rG = sm + L::rg, *bs = sm + L::bs, *rowsum = sm + L::rs;
+    float *rowsum2 = sm + L::rs2;   // per-token dG sums for da
     float *Gb = sm + L::gb;
     __nv_bfloat16 *Sh = (__nv_bfloat16 *)(sm + L::sh);
     const int64_t c = blockIdx.x;
@@ -899,7 +900,7 @@ bwd_tile_kernel(const BcArgs A) {
                 mma8(dw[nt], ae, b0, b1);
             }
         }
-        __syncthreads();   // every warp is done reading D (the dS and dKe products) and dO
+        // D's last readers (dS and dKe) finished two barriers ago: dW can take its place
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             const int col = c0 + 8 * nt + 2 * t;
@@ -915,7 +916,7 @@ bwd_tile_kernel(const BcArgs A) {
     __syncthreads();
     // ---- dA = -strict_lower(dYu U^T + dYw W^T) (warps 0-1); dV = diag(beta) dYu
     if (warp < 2) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};   // two chains
         const int j0 = 8 * warp;
 #pragma unroll 4
         for (int k0 = 0; k0 < kD; k0 += 8) {
@@ -925,8 +926,10 @@ bwd_tile_kernel(const BcArgs A) {
             mma8(acc, af, b0, b1);
             load_a(af, Db, kLd, 0, k0, g, t);
             load_bt(b0, b1, Wb, kLd, k0, j0, g, t);
-            mma8(acc, af, b0, b1);
+            mma8(acc2, af, b0, b1);
         }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) acc[u] += acc2[u];
         const int i0 = g, i1 = g + 8, ja = j0 + 2 * t, jb = ja + 1;
         const float v00 = ja < i0 ? -acc[0] : 0.f, v01 = jb < i0 ? -acc[1] : 0.f;
         const float v10 = ja < i1 ? -acc[2] : 0.f, v11 = jb < i1 ? -acc[3] : 0.f;
@@ -1020,7 +1023,6 @@ bwd_tile_kernel(const BcArgs A) {
         for (int j = 0; j < i; ++j) acc = fmaf(dA[i * kPd + j], KK[i * kPd + j], acc);
         A.dbeta[(t0 + i) * A.H + h] = __float2bfloat16_rn(acc);
     }
-    __syncthreads();   // rowsum is reused below
     // ---- da: the last token also carries dG_C; reverse cumsum over the tile
     if (VEC) {
         if (tid < kD) {
@@ -1041,13 +1043,13 @@ bwd_tile_kernel(const BcArgs A) {
                 for (int d = lane; d < kD; d += 32) x += Ob[i * kLd + d] + (i == len - 1 ? rG[d] : 0.f);
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-                if (lane == 0) rowsum[i] = x;
+                if (lane == 0) rowsum2[i] = x;
             }
         }
         __syncthreads();
         if (warp == 0) {
             // reverse cumsum over the tile's tokens (lanes 0..15), times g'(a)
-            float x = lane < len ? rowsum[lane] : 0.f;
+            float x = lane < len ? rowsum2[lane] : 0.f;
 #pragma unroll
             for (int o = 1; o < kT; o <<= 1) {
                 const float y = __shfl_down_sync(0xffffffffu, x, o);
