@@ -160,6 +160,10 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     return pa < pb + nb && pb < pa + na;
 }
 
+// 16-byte alignment (a null pointer counts as aligned): TMA tiles, cp.async and
+// the float4 state copies need it.
+inline bool al16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
 // Checks shared by every forward entry point.  Fills `s` on success.
 gdr_status_t check_args(const void *q, const void *k, const void *v, const void *a,
                         const void *beta, const float *h0, const void *out, const float *hT,
@@ -468,6 +472,11 @@ gdr_status_t gdr_chunk_fwd_ex(const void *q, const void *k, const void *v, const
     gdr_status_t st = check_args(q, k, v, a, beta, h0, out, hT, cu_seqlens, B, T, H, dk, dv,
                                  chunk, b, dtype, gate, path, &s);
     if (st != GDR_OK) return st;
+    // the tensor-core path reads q, k, v as TMA tiles, which start on 16-byte boundaries
+    if (!(al16(q) && al16(k) && al16(v))) {
+        if (path == GDR_PATH_TC) return GDR_ERR_UNSUPPORTED;
+        path = GDR_PATH_SIMT;
+    }
     path = resolve_path(path, dtype, dk, dv, chunk);
     return run_forward(q, k, v, a, beta, h0, out, hT, cu_seqlens, s, b, dtype, gate, path,
                        workspace, workspace_bytes, (cudaStream_t)stream);
@@ -486,23 +495,27 @@ size_t gdr_chunk_fwd_workspace_size(int B, int64_t T, int H, int dk, int dv, int
     if (B < 1 || H < 1 || T < 0 || (dk != 64 && dk != 128) || (dv != 64 && dv != 128) ||
         (chunk != 16 && chunk != 32 && chunk != 64) || (dtype != GDR_BF16 && dtype != GDR_F32))
         return 0;
-    path = resolve_path(path, dtype, dk, dv, chunk);
     if (path == GDR_PATH_TC && !tc_supported(dtype, dk, dv, chunk)) return 0;
-    // the larger of the dense (B*T tokens) and varlen (T tokens) readings of (B, T)
+    // AUTO may run either path (unaligned q, k, v take the CUDA-core one): the larger
+    // of the two, and of the dense (B*T tokens) and varlen (T tokens) readings of (B, T)
+    const gdr_path_t resolved = resolve_path(path, dtype, dk, dv, chunk);
+    const gdr_path_t paths[2] = {resolved, path == GDR_PATH_AUTO ? GDR_PATH_SIMT : resolved};
     size_t best = 0;
-    for (int varlen = 0; varlen < 2; ++varlen) {
-        Shape s;
-        s.N = B;
-        s.H = H;
-        s.dk = dk;
-        s.dv = dv;
-        s.C = chunk;
-        s.T_total = varlen ? T : (int64_t)B * T;
-        s.T_per = varlen ? 0 : T;
-        s.varlen = varlen != 0;
-        s.max_chunks = tile_bound(s.varlen, B, T, chunk);
-        const size_t n = layout_for(s, path).total;
-        if (n > best) best = n;
+    for (int pi = 0; pi < 2; ++pi) {
+        for (int varlen = 0; varlen < 2; ++varlen) {
+            Shape s;
+            s.N = B;
+            s.H = H;
+            s.dk = dk;
+            s.dv = dv;
+            s.C = chunk;
+            s.T_total = varlen ? T : (int64_t)B * T;
+            s.T_per = varlen ? 0 : T;
+            s.varlen = varlen != 0;
+            s.max_chunks = tile_bound(s.varlen, B, T, chunk);
+            const size_t n = layout_for(s, paths[pi]).total;
+            if (n > best) best = n;
+        }
     }
     return best;
 }
@@ -574,6 +587,7 @@ gdr_status_t gdr_recurrent_fwd(const void *q, const void *k, const void *v, cons
     if (T > ((int64_t)1 << 40) || (int64_t)N * T > ((int64_t)1 << 40)) return GDR_ERR_UNSUPPORTED;
     if (T == 0) return GDR_OK;
     if (!q || !k || !v || !a || !beta || !state || !out) return GDR_ERR_INVALID_ARG;
+    if (!al16(state)) return GDR_ERR_INVALID_ARG;   // read and written as float4
     const size_t es = dtype == GDR_BF16 ? 2 : 4;
     const size_t rows = (size_t)N * T * H;
     const size_t out_bytes = rows * dv * es, n_state = (size_t)N * H * dk * dv * sizeof(float);
@@ -626,6 +640,7 @@ static gdr_status_t chunk_bwd_impl(const void *q, const void *k, const void *v, 
             if (overlaps(outs[i], out_b[i], ins[j], in_b[j])) return GDR_ERR_INVALID_ARG;
     const size_t nst = (size_t)B * H * dk * dv * sizeof(float);
     if (dh0 && (overlaps(dh0, nst, h0, nst) || overlaps(dh0, nst, dhT, nst))) return GDR_ERR_INVALID_ARG;
+    if (!al16(dhT) || !al16(dh0)) return GDR_ERR_INVALID_ARG;   // copied as float4
     if (s.T_total == 0) {   // no tokens: dh0 = dhT
         if (!dh0) return GDR_OK;
         cudaStream_t stream = (cudaStream_t)stream_;
@@ -714,9 +729,11 @@ gdr_status_t gdr_chunk_fwd_vec(const void *q, const void *k, const void *v, cons
     }
     DeviceCtx *ctx = device_ctx();
     if (!ctx) return GDR_ERR_CUDA;
-    // tensor-core kernel; it writes out in 16-byte pieces, so an unaligned out takes
-    // the CUDA-core kernels
-    const bool fused = dtype == GDR_BF16 && dk == 128 && dv == 128 && (uintptr_t)out % 16 == 0;
+    // tensor-core kernel; it reads q, k, v, a and writes out in 16-byte pieces, so an
+    // unaligned one of those takes the CUDA-core kernels
+    const bool aligned16 = ((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)a |
+                            (uintptr_t)out) % 16 == 0;
+    const bool fused = dtype == GDR_BF16 && dk == 128 && dv == 128 && aligned16;
     const int64_t tiles = tile_bound(s.varlen, B, T, kVecTile);
     const size_t plan_b = align_up(3 * sizeof(int64_t) * (size_t)(B + 1));
     const int seg = fused ? vec_mma_segment_tiles(tiles, H, ctx->sms) : (1 << 30);

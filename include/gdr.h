@@ -91,9 +91,11 @@ typedef enum {
 } gdr_gate_t;
 
 typedef enum {
-    GDR_PATH_AUTO = 0, /* tensor-core path where supported, else SIMT            */
+    GDR_PATH_AUTO = 0, /* tensor-core path where supported and q, k, v are 16-byte
+                          aligned (TMA tiles), else SIMT                            */
     GDR_PATH_SIMT = 1, /* fp32 CUDA-core path (any supported shape and dtype)     */
-    GDR_PATH_TC = 2    /* tcgen05 path; GDR_ERR_UNSUPPORTED where it does not apply */
+    GDR_PATH_TC = 2    /* tcgen05 path; GDR_ERR_UNSUPPORTED where it does not apply
+                          (shape, dtype, or q, k, v not 16-byte aligned)            */
 } gdr_path_t;
 
 /*
@@ -131,7 +133,8 @@ GDR_API gdr_status_t gdr_chunk_fwd_ex(const void *q, const void *k, const void *
                               gdr_stream_t stream);
 
 /* Scratch bytes gdr_chunk_fwd_ex needs for these sizes (0 on invalid sizes).
- * B is N (the sequence count) for varlen input. */
+ * B is N (the sequence count) for varlen input.  For GDR_PATH_AUTO it covers
+ * both paths, since the pointers' alignment decides between them. */
 GDR_API size_t gdr_chunk_fwd_workspace_size(int B, int64_t T, int H, int dk, int dv, int chunk,
                                     gdr_dtype_t dtype, gdr_path_t path);
 
@@ -220,7 +223,8 @@ GDR_API gdr_status_t gdr_wy_repr(const void *k, const void *v, const void *beta,
  * o = H^T q (the same recurrence as gdr_chunk_fwd_ex, computed without tiles).
  * Device pointers owned by the caller; nothing is retained or allocated.
  * dk, dv in {64, 128}; N, H >= 1; T >= 0 (T = 0 leaves state untouched).
- * out must not alias any input or state.  Returns GDR_ERR_INVALID_ARG or
+ * out must not alias any input or state; state must be 16-byte aligned (it
+ * is read and written as float4).  Returns GDR_ERR_INVALID_ARG or
  * GDR_ERR_UNSUPPORTED before any launch, GDR_ERR_CUDA on a launch failure;
  * the call is asynchronous on `stream`.
  */
@@ -245,8 +249,9 @@ GDR_API gdr_status_t gdr_recurrent_fwd(const void *q, const void *k, const void 
  * chunk must be 16 and 0 < b <= 5 (exp(16 b) must stay below FLT_MAX):
  * GDR_ERR_UNSUPPORTED otherwise; b <= 0 is GDR_ERR_INVALID_ARG.  Only the
  * bounded gate is taken (an unbounded one can overflow exp(-G)).  bf16 with
- * dk = dv = 128 runs a fused tensor-core kernel when `out` is 16-byte aligned;
- * other shapes, fp32 and unaligned `out` run the CUDA-core kernels.  Scratch
+ * dk = dv = 128 runs a fused tensor-core kernel when q, k, v, a and `out` are
+ * 16-byte aligned; other shapes, fp32 and unaligned pointers run the CUDA-core
+ * kernels (same results within the stated tolerances).  Scratch
  * comes from the internal per-device cache; asynchronous on `stream`.
  */
 GDR_API gdr_status_t gdr_chunk_fwd_vec(const void *q, const void *k, const void *v, const void *a,
@@ -326,11 +331,16 @@ GDR_API gdr_status_t gdr_router_bias_update(const int64_t *load, float *bias, do
  *   dout [tokens, H, dv] (dtype) or NULL (zero);  dhT [N, H, dk, dv] fp32 or NULL
  *   dq, dk [tokens, H, dk], dv [tokens, H, dv], da, dbeta [tokens, H]  (dtype, all
  *   written);  dh0 [N, H, dk, dv] fp32 (written when not NULL)
- * `chunk` is validated like the forward's; the pass keeps checkpoints of the
- * state every 16 tokens and recomputes between them.  Device pointers owned
+ * `chunk` is validated like the forward's; the pass works on 16-token tiles
+ * either way.  bf16 with dk = dv = 128 and the bounded gate with b <= 5 runs
+ * the chunked tensor-core form: the states at tile boundaries are stored in
+ * bf16, and each tile's gradients come from dense products.  Every other case
+ * runs token by token, from fp32 checkpoints every 16 tokens with the tokens
+ * between them recomputed.  Device pointers owned
  * by the caller; scratch comes from the internal per-device cache.  Outputs
- * must not alias inputs.  The result is deterministic (no atomics).  Errors as
- * for gdr_chunk_fwd_ex; asynchronous on `stream`.
+ * must not alias inputs; dhT and dh0 must be 16-byte aligned (copied as
+ * float4), GDR_ERR_INVALID_ARG otherwise.  The result is deterministic (no
+ * atomics).  Errors as for gdr_chunk_fwd_ex; asynchronous on `stream`.
  */
 GDR_API gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const void *a,
                            const void *beta, const float *h0, const void *dout,

@@ -89,3 +89,36 @@ def test_workspace_size(lib):
 
 def test_launch_count_starts_at_zero_without_calls(lib):
     assert gdr.gdr_launch_count() >= 0
+
+
+def test_tc_path_needs_aligned_q_k_v(lib):
+    # the tensor-core path reads q, k, v as TMA tiles: an explicit request with an
+    # unaligned one is unsupported (AUTO runs the CUDA-core kernels instead)
+    for name in ("q", "k", "v"):
+        bad = {name: dict(q=1 << 20, k=2 << 20, v=3 << 20)[name] + 2}
+        assert _call(path=gdr.GDR_PATH_TC, **bad) == gdr.GDR_ERR_UNSUPPORTED, name
+
+
+def test_workspace_size_auto_covers_both_paths(lib):
+    args = (2, 4096, 16, 128, 128, 16, gdr.GDR_BF16)
+    auto = gdr.gdr_chunk_fwd_workspace_size(*args, gdr.GDR_PATH_AUTO)
+    assert auto >= gdr.gdr_chunk_fwd_workspace_size(*args, gdr.GDR_PATH_TC) > 0
+    assert auto >= gdr.gdr_chunk_fwd_workspace_size(*args, gdr.GDR_PATH_SIMT) > 0
+
+
+def test_recurrent_state_must_be_aligned(lib):
+    base = [1 << 20, 2 << 20, 3 << 20, 4 << 20, 5 << 20]
+    args = (1, 1, 2, 128, 128, 2.0, gdr.GDR_BF16, gdr.GDR_GATE_BOUNDED, 0)
+    assert gdr.gdr_recurrent_fwd(*base, (7 << 20) + 4, 6 << 20, *args) == gdr.GDR_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("which", ["dhT", "dh0"])
+def test_backward_state_gradients_must_be_aligned(lib, which):
+    # T = 0: the call would only copy dhT to dh0, but the check comes first
+    ptr = {"dhT": 8 << 20, "dh0": 9 << 20}
+    ptr[which] += 8
+    ins = [1 << 20, 2 << 20, 3 << 20, 4 << 20, 5 << 20, None, 6 << 20, ptr["dhT"]]
+    outs = [10 << 20, 11 << 20, 12 << 20, 13 << 20, 14 << 20, ptr["dh0"]]
+    rc = gdr.gdr_chunk_bwd(*ins, *outs, None, 1, 0, 2, 128, 128, 16, 2.0, gdr.GDR_BF16,
+                           gdr.GDR_GATE_BOUNDED, 0)
+    assert rc == gdr.GDR_ERR_INVALID_ARG

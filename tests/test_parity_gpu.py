@@ -202,6 +202,29 @@ def test_in_place_state_carry():
         assert_close(to64(h), rh, "bf16", f"hT[{path}]")
 
 
+def test_unaligned_q_runs_the_cuda_core_path():
+    """q 2 bytes past an aligned address: the tensor-core path (TMA tiles) cannot
+    take it, so AUTO runs the CUDA-core kernels and an explicit TC request is
+    unsupported; the result matches the oracle."""
+    w = WORKLOADS["b2_t4k"].with_(H=2)
+    x = make_inputs(w, device="cuda", T=100)
+    buf = torch.empty(x["q"].numel() + 8, dtype=x["q"].dtype, device="cuda")
+    q = buf[1:1 + x["q"].numel()].view(x["q"].shape)
+    q.copy_(x["q"])
+    out = torch.empty_like(x["v"])
+    hT = torch.empty((x["B"], 2, 128, 128), dtype=torch.float32, device="cuda")
+    args = (q, x["k"], x["v"], x["a"], x["beta"], x["h0"], out, hT, None, x["B"], x["T"], 2, 128,
+            128, 16, 2.0, gdr.GDR_BF16, gdr.GDR_GATE_BOUNDED)
+    assert gdr.gdr_chunk_fwd_ex(*args, gdr.GDR_PATH_AUTO, None, 0, None) == gdr.GDR_OK
+    torch.cuda.synchronize()
+    assert gdr.gdr_get_status() == gdr.GDR_OK
+    ro, rh = run_oracle(x)
+    assert_close(to64(out), ro, "bf16", "out")
+    assert_close(to64(hT), rh, "bf16", "hT")
+    if _tc_available():
+        assert gdr.gdr_chunk_fwd_ex(*args, gdr.GDR_PATH_TC, None, 0, None) == gdr.GDR_ERR_UNSUPPORTED
+
+
 def test_bad_cu_seqlens_sets_status():
     w = WORKLOADS["varlen_1m"]
     x = make_inputs(w, device="cuda", T=256)

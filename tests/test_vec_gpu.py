@@ -126,12 +126,24 @@ def test_vec_packed_long_and_short_sequences():
     _check(x, "bf16")
 
 
-def test_vec_unaligned_output_takes_the_cuda_core_kernels():
-    """bf16 d = 128 with `out` not 16-byte aligned: the fused kernel writes 16-byte
-    pieces, so the call runs the CUDA-core kernels; the result is the same."""
+@pytest.mark.parametrize("which", ["out", "q", "av"])
+def test_vec_unaligned_pointer_takes_the_cuda_core_kernels(which):
+    """bf16 d = 128 with `out`, or an input, not 16-byte aligned: the fused kernel
+    reads and writes 16-byte pieces, so the call runs the CUDA-core kernels; the
+    result is the same."""
     x = _inputs("bf16", 128, 40, seed=5900, N=1, H=2)
-    buf = torch.empty(x["v"].numel() + 8, dtype=torch.bfloat16, device="cuda")
-    out = buf[1:1 + x["v"].numel()].view(x["v"].shape)          # 2 bytes past an aligned start
+
+    def shifted(t):   # a copy of t that starts 2 bytes past an aligned address
+        buf = torch.empty(t.numel() + 8, dtype=t.dtype, device="cuda")
+        u = buf[1:1 + t.numel()].view(t.shape)
+        u.copy_(t)
+        return u
+
+    out = torch.empty_like(x["v"])
+    if which == "out":
+        out = shifted(out)
+    else:
+        x[which] = shifted(x[which])
     hT = torch.empty((1, 2, 128, 128), dtype=torch.float32, device="cuda")
     rc = gdr.gdr_chunk_fwd_vec(x["q"], x["k"], x["v"], x["av"], x["beta"], x["h0"], out, hT, None,
                                1, 40, 2, 128, 128, 16, 2.0, gdr.GDR_BF16)
