@@ -22,10 +22,11 @@
 // In the transposed form D^T = U^T - H^T W^T, O^T = H^T Qt^T + D^T P^T and
 // H^T <- H^T diag(exp(G_C)) + D^T (Kh exp(G_C)) are per-warp; a tile takes four
 // block barriers (staging, the Gram products, the substitutions, reuse).
-// Each tile's loads are issued together before its staging (two bf16 per register);
-// two blocks share an SM (holding the next tile's inputs in registers during the
-// current tile measured slower).  The outputs of a tile wait in shared memory and go
-// out as whole rows after the next barrier.
+// The next tile's q, k, v and a rows are copied into shared memory (16-byte cp.async,
+// bf16 as stored) while the current tile runs its products, so the staging reads
+// shared memory instead of waiting on global loads; two blocks share an SM.  The
+// outputs of a tile wait in shared memory and go out as whole rows after the next
+// barrier.
 //
 // Long sequences are cut into segments of S tiles (the plan's seg_chunks, 64 to 256,
 // larger when there are enough (segment, head) blocks to fill the GPU), one block per
@@ -65,7 +66,12 @@ constexpr int kOffP = kOffA + kT * kPd;       // P [16][kPd]
 constexpr int kOffEg = kOffP + kT * kPd;      // exp(G_C) [128]
 constexpr int kOffB = kOffEg + kD;            // beta [16]
 constexpr int kOffO = kOffB + kT;             // the tile's outputs, bf16 [16][128]
-constexpr int kSmemFloats = kOffO + kT * kD / 2;
+constexpr int kOffRaw = kOffO + kT * kD / 2;  // next tile's q, k, v, a as stored: bf16 [4][16][128]
+constexpr int kSmemFloats = kOffRaw + 4 * kT * kD / 2;
+static_assert(kOffO % 4 == 0 && kOffRaw % 4 == 0, "16-byte aligned bf16 tiles");
+// Rows 8-15 of a raw tile keep their 16-byte pieces in the order c ^ 2, so that the
+// two staging lanes of a channel (tokens i and i + 8) read different banks.
+__device__ __forceinline__ int raw_slot(int i, int c16) { return i * kD + 8 * (c16 ^ ((i >> 3) << 1)); }
 constexpr size_t kSmemBytes = sizeof(float) * kSmemFloats;
 
 // Per (tile, head): the log of a bound on the norm of the tile's transition,
@@ -202,33 +208,29 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
     // (and value) channel d, tokens 0-7 and 8-15; the second half gets the first
     // half's cumulative log-decay from its neighbour lane.
     const int sd = tid >> 1, shalf = tid & 1, si0 = 8 * shalf;
-    uint32_t pa[4], pk[4], pq[4], pv[4];   // two bf16 per register: tokens 2m, 2m + 1 of the half
-    float rb = 0.f;
-    auto fetch = [&](int64_t tt) {
+    __nv_bfloat16 *Raw = (__nv_bfloat16 *)(sm + kOffRaw);
+    float rb = 0.f;   // beta of token tid of the fetched tile
+    // Copies of a tile's rows into Raw: thread tid takes row tid / 16, 16-byte piece
+    // tid % 16, of q, k, v and a; rows past the sequence end are not copied (staging
+    // masks them).  Waited for by cp_async_wait_all before the next barrier.
+    auto prefetch = [&](int64_t tt) {
         const int64_t t0 = sstart + tt * kT;
-        const int len = tt < s1 ? (int)min((int64_t)kT, e_end - t0) : 0;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            uint32_t xa = 0, xk = 0, xq = 0, xv = 0;
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int i = si0 + 2 * m + u;
-                if (i < len) {
-                    const int64_t r = ((t0 + i) * H + h) * kD + sd;
-                    xa |= (uint32_t)__bfloat16_as_ushort(a[r]) << (16 * u);
-                    xk |= (uint32_t)__bfloat16_as_ushort(k[r]) << (16 * u);
-                    xq |= (uint32_t)__bfloat16_as_ushort(q[r]) << (16 * u);
-                    xv |= (uint32_t)__bfloat16_as_ushort(v[r]) << (16 * u);
-                }
-            }
-            pa[m] = xa;
-            pk[m] = xk;
-            pq[m] = xq;
-            pv[m] = xv;
+        const int len = (int)min((int64_t)kT, e_end - t0);
+        const int i = tid >> 4, c16 = tid & 15;
+        if (i < len) {
+            const int64_t r = ((t0 + i) * H + h) * kD + 8 * c16;
+            const int dst = raw_slot(i, c16);
+            cp_async16(&Raw[0 * kT * kD + dst], &q[r]);
+            cp_async16(&Raw[1 * kT * kD + dst], &k[r]);
+            cp_async16(&Raw[2 * kT * kD + dst], &v[r]);
+            cp_async16(&Raw[3 * kT * kD + dst], &a[r]);
         }
+        cp_async_commit();
         if (tid < len) rb = __bfloat162float(beta[(t0 + tid) * H + h]);
     };
-    auto half_f = [](uint32_t x, int u) { return __uint_as_float(u ? (x & 0xffff0000u) : (x << 16)); };
+    // channel sd of token si0 + u of raw tile X (0 q, 1 k, 2 v, 3 a)
+    const int rs0 = raw_slot(si0, sd >> 3) + (sd & 7);
+    auto raw = [&](int X, int u) { return __bfloat162float(Raw[X * kT * kD + rs0 + u * kD]); };
     // outputs of a tile wait in Os until the next barrier, then go out as 256-byte rows
     int64_t o_t0 = 0;
     int o_len = 0;
@@ -239,19 +241,20 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
         }
         o_len = 0;
     };
+    if (w0 < s1) prefetch(w0);
     for (int64_t tt = w0; tt < s1; ++tt) {
         const int64_t t0 = sstart + tt * kT;
         const int len = (int)min((int64_t)kT, e_end - t0);
         const bool emit = tt >= s0;   // warm-up tiles only advance the state
-        fetch(tt);         // every load of the tile, issued together
-        __syncthreads();   // the previous tile is done with every staging buffer
-        flush_out();       // the previous tile's outputs, whole rows
+        cp_async_wait_all();   // this thread's copies of the tile have landed
+        __syncthreads();       // all copies visible; the previous tile is done with every buffer
+        flush_out();           // the previous tile's outputs, whole rows
         // ---- stage the tile: factored decays per key channel, V and beta
         {
             float gl[8], G = 0.f;
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                gl[u] = si0 + u < len ? gate_logdecay(half_f(pa[u >> 1], u & 1), b, GDR_GATE_BOUNDED) : 0.f;
+                gl[u] = si0 + u < len ? gate_logdecay(raw(3, u), b, GDR_GATE_BOUNDED) : 0.f;
                 G += gl[u];
             }
             const float Gfirst = __shfl_xor_sync(0xffffffffu, G, 1);   // the other half's total
@@ -263,11 +266,11 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
                 float kt = 0.f, kh = 0.f, qt = 0.f, vv = 0.f;
                 if (i < len) {
                     G += gl[u];
-                    const float e = expf(G), en = expf(-G), kd = half_f(pk[u >> 1], u & 1);
+                    const float e = expf(G), en = expf(-G), kd = raw(1, u);
                     kt = kd * e;
                     kh = kd * en;
-                    qt = half_f(pq[u >> 1], u & 1) * e;
-                    vv = half_f(pv[u >> 1], u & 1);
+                    qt = raw(0, u) * e;
+                    vv = raw(2, u);
                     eGC = e;
                 }
                 Kt[i * kLd + sd] = kt;
@@ -281,6 +284,7 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
             if (tid < kT) bs[tid] = tid < len ? rb : 0.f;
         }
         __syncthreads();
+        if (tt + 1 < s1) prefetch(tt + 1);   // Raw and rb are free until the next staging
         // ---- A = beta (.) strict_lower(Kt Kh^T) and P = lower(Qt Kh^T): warps 0-3
         if (warp < 4) {
             const float *Aop = (warp < 2) ? Kt : Qt;
