@@ -69,6 +69,7 @@ constexpr int kOffO = kOffB + kT;             // the tile's outputs, bf16 [16][1
 constexpr int kOffRaw = kOffO + kT * kD / 2;  // next tile's q, k, v, a as stored: bf16 [4][16][128]
 constexpr int kSmemFloats = kOffRaw + 4 * kT * kD / 2;
 static_assert(kOffO % 4 == 0 && kOffRaw % 4 == 0, "16-byte aligned bf16 tiles");
+static_assert(kOffA % 4 == 0 && kPd % 4 == 0, "A rows read in 16-byte pieces");
 // Rows 8-15 of a raw tile keep their 16-byte pieces in the order c ^ 2, so that the
 // two staging lanes of a channel (tokens i and i + 8) read different banks.
 __device__ __forceinline__ int raw_slot(int i, int c16) { return i * kD + 8 * (c16 ^ ((i >> 3) << 1)); }
@@ -77,16 +78,35 @@ constexpr size_t kSmemBytes = sizeof(float) * kSmemFloats;
 // Per (tile, head): the log of a bound on the norm of the tile's transition,
 // sum over its tokens of  max_d g_{t,d} + ln max(1, |1 - beta_t |k_t|^2|),
 // with max_d g = -b sigmoid(min_d a) (the gate is decreasing in a).  One warp per
-// (tile, head): lane l holds channels 4l..4l+3 of every token.
+// (tile, head), the head fastest across warps (so the warps running together read
+// whole token rows): lane l loads channels 4l..4l+3 of every token.  The 16
+// per-token reductions over the lanes run as one butterfly that halves the tokens
+// a lane keeps at each step: afterwards lanes 2j and 2j + 1 hold the complete
+// minimum and squared norm of token j (in a lane-bit order), and each evaluates
+// that token's term once.
 constexpr int kBoundWarps = 8;
+
+// One butterfly step over n tokens: lanes whose bit `o` is clear keep the first
+// n/2, the others the last n/2, each combining its kept half with its partner's.
+template <int N, bool MIN>
+__device__ __forceinline__ void bound_step(float (&x)[kT], int o, bool upper) {
+#pragma unroll
+    for (int j = 0; j < N / 2; ++j) {
+        const float keep = upper ? x[j + N / 2] : x[j];
+        const float give = upper ? x[j] : x[j + N / 2];
+        const float got = __shfl_xor_sync(0xffffffffu, give, o);
+        x[j] = MIN ? fminf(keep, got) : keep + got;
+    }
+}
 
 __global__ void __launch_bounds__(32 * kBoundWarps)
 vec_bound_kernel(const __nv_bfloat16 *__restrict__ a, const __nv_bfloat16 *__restrict__ k,
                  const __nv_bfloat16 *__restrict__ beta, float *__restrict__ lam, Plan p, int H,
                  float b, int64_t max_tiles) {
     const int lane = threadIdx.x & 31;
-    const int64_t c = (int64_t)blockIdx.x * kBoundWarps + (threadIdx.x >> 5);
-    const int h = blockIdx.y;
+    const int64_t idx = (int64_t)blockIdx.x * kBoundWarps + (threadIdx.x >> 5);
+    const int64_t c = idx / H;
+    const int h = (int)(idx - c * H);
     if (c >= max_tiles) return;
     const int n = find_owner(p.chunk_base, p.N, c);
     if (n < 0) return;
@@ -94,31 +114,45 @@ vec_bound_kernel(const __nv_bfloat16 *__restrict__ a, const __nv_bfloat16 *__res
     const int len = (int)min((int64_t)kT, p.seq_start[n + 1] - t0);
     uint2 ra[kT], rk[kT];
 #pragma unroll
-    for (int i = 0; i < kT; ++i)
+    for (int i = 0; i < kT; ++i) {
+        ra[i] = make_uint2(0u, 0u);
+        rk[i] = make_uint2(0u, 0u);
         if (i < len) {
             const int64_t r = ((t0 + i) * H + h) * kD + 4 * lane;
             ra[i] = *(const uint2 *)&a[r];
             rk[i] = *(const uint2 *)&k[r];
         }
-    float lam_t = 0.f;
+    }
+    // the token this lane ends up holding: bits 4, 3, 2, 1 of the lane, high to low
+    const int tk = 8 * ((lane >> 4) & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) + ((lane >> 1) & 1);
+    const float bt = tk < len ? __bfloat162float(beta[(t0 + tk) * H + h]) : 0.f;
+    float m[kT], kk[kT];
 #pragma unroll
     for (int i = 0; i < kT; ++i) {
-        if (i >= len) break;
         const float2 a0 = __bfloat1622float2(*(const __nv_bfloat162 *)&ra[i].x);
         const float2 a1 = __bfloat1622float2(*(const __nv_bfloat162 *)&ra[i].y);
         const float2 k0 = __bfloat1622float2(*(const __nv_bfloat162 *)&rk[i].x);
         const float2 k1 = __bfloat1622float2(*(const __nv_bfloat162 *)&rk[i].y);
-        float m = fminf(fminf(a0.x, a0.y), fminf(a1.x, a1.y));
-        float kk = k0.x * k0.x + k0.y * k0.y + k1.x * k1.x + k1.y * k1.y;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            m = fminf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            kk += __shfl_xor_sync(0xffffffffu, kk, o);
-        }
-        const float bt = __bfloat162float(beta[(t0 + i) * H + h]);
-        lam_t += gate_logdecay(m, b, GDR_GATE_BOUNDED) + logf(fmaxf(1.f, fabsf(1.f - bt * kk)));
+        m[i] = fminf(fminf(a0.x, a0.y), fminf(a1.x, a1.y));
+        kk[i] = k0.x * k0.x + k0.y * k0.y + k1.x * k1.x + k1.y * k1.y;
     }
-    if (lane == 0) lam[c * H + h] = lam_t;
+    bound_step<16, true>(m, 16, (lane >> 4) & 1);
+    bound_step<16, false>(kk, 16, (lane >> 4) & 1);
+    bound_step<8, true>(m, 8, (lane >> 3) & 1);
+    bound_step<8, false>(kk, 8, (lane >> 3) & 1);
+    bound_step<4, true>(m, 4, (lane >> 2) & 1);
+    bound_step<4, false>(kk, 4, (lane >> 2) & 1);
+    bound_step<2, true>(m, 2, (lane >> 1) & 1);
+    bound_step<2, false>(kk, 2, (lane >> 1) & 1);
+    const float mt = fminf(m[0], __shfl_xor_sync(0xffffffffu, m[0], 1));
+    const float kt = kk[0] + __shfl_xor_sync(0xffffffffu, kk[0], 1);
+    // token tk's term, counted once (by the even lane of the pair)
+    float x = 0.f;
+    if (tk < len && (lane & 1) == 0)
+        x = gate_logdecay(mt, b, GDR_GATE_BOUNDED) + logf(fmaxf(1.f, fabsf(1.f - bt * kt)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (lane == 0) lam[c * H + h] = x;
 }
 
 // Per (sequence, head): 1 if every segment start has a bound <= 2^-64 within
@@ -209,7 +243,7 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
     // half's cumulative log-decay from its neighbour lane.
     const int sd = tid >> 1, shalf = tid & 1, si0 = 8 * shalf;
     __nv_bfloat16 *Raw = (__nv_bfloat16 *)(sm + kOffRaw);
-    float rb = 0.f;   // beta of token tid of the fetched tile
+    unsigned short rb = 0;   // beta of token tid of the fetched tile, as stored (converted at staging)
     // Copies of a tile's rows into Raw: thread tid takes row tid / 16, 16-byte piece
     // tid % 16, of q, k, v and a; rows past the sequence end are not copied (staging
     // masks them).  Waited for by cp_async_wait_all before the next barrier.
@@ -226,7 +260,7 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
             cp_async16(&Raw[3 * kT * kD + dst], &a[r]);
         }
         cp_async_commit();
-        if (tid < len) rb = __bfloat162float(beta[(t0 + tid) * H + h]);
+        if (tid < len) rb = __bfloat16_as_ushort(beta[(t0 + tid) * H + h]);
     };
     // channel sd of token si0 + u of raw tile X (0 q, 1 k, 2 v, 3 a)
     const int rs0 = raw_slot(si0, sd >> 3) + (sd & 7);
@@ -281,7 +315,7 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
         // e^{G_C} of channel d: from the half that holds the tile's last token
             const float other = __shfl_xor_sync(0xffffffffu, eGC, 1);
             if (shalf == 0) eg[sd] = len > 8 ? other : eGC;
-            if (tid < kT) bs[tid] = tid < len ? rb : 0.f;
+            if (tid < kT) bs[tid] = tid < len ? __bfloat162float(__ushort_as_bfloat16(rb)) : 0.f;
         }
         __syncthreads();
         if (tt + 1 < s1) prefetch(tt + 1);   // Raw and rb are free until the next staging
@@ -318,8 +352,15 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
 #pragma unroll
             for (int i = 0; i < kT; ++i) {
                 float acc = bs[i] * X[i * kLd + col];
+                // row i of A in 16-byte pieces (entries j >= i are zero and unused)
 #pragma unroll
-                for (int j = 0; j < i; ++j) acc = fmaf(-Am[i * kPd + j], x[j], acc);
+                for (int j4 = 0; j4 < i; j4 += 4) {
+                    const float4 a4 = *(const float4 *)&Am[i * kPd + j4];
+                    const float ar[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (j4 + u < i) acc = fmaf(-ar[u], x[j4 + u], acc);
+                }
                 x[i] = acc;
             }
             if (tid < kD) {
@@ -435,8 +476,10 @@ cudaError_t launch_vec_mma(const void *q, const void *k, const void *v, const vo
     cudaError_t err;
     if (max_tiles > 0) {
         ProfScope prof(stream, "vec_bound_kernel");
-        vec_bound_kernel<<<dim3((unsigned)((max_tiles + kBoundWarps - 1) / kBoundWarps), (unsigned)H),
-                           32 * kBoundWarps, 0, stream>>>(
+        const int64_t warps = max_tiles * H;
+        if ((warps + kBoundWarps - 1) / kBoundWarps > 0x7fffffff) return cudaErrorInvalidValue;
+        vec_bound_kernel<<<(unsigned)((warps + kBoundWarps - 1) / kBoundWarps), 32 * kBoundWarps, 0,
+                           stream>>>(
             (const __nv_bfloat16 *)a, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)beta, lam,
             plan, H, b, max_tiles);
         count_launch();
