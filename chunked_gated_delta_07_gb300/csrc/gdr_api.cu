@@ -739,7 +739,7 @@ gdr_status_t gdr_chunk_fwd_vec(const void *q, const void *k, const void *v, cons
     const int seg = fused ? vec_mma_segment_tiles(tiles, H, ctx->sms) : (1 << 30);
     // segments: at most one partial segment per sequence beyond the full ones
     const int64_t segs = s.varlen ? (tiles + seg - 1) / seg + B : (int64_t)B * ((tiles / B + seg - 1) / seg);
-    const size_t need = plan_b + (fused ? vec_mma_scratch_bytes(tiles, B, H)
+    const size_t need = plan_b + (fused ? vec_mma_scratch_bytes(segs, H)
                                         : vec_scratch_bytes(tiles, s.T_total, H, dk, dv));
     char *ws;
     {
@@ -753,8 +753,8 @@ gdr_status_t gdr_chunk_fwd_vec(const void *q, const void *k, const void *v, cons
                     seq_start + (B + 1), seq_start + 2 * (B + 1), ctx->d_status, stream) != cudaSuccess)
         return GDR_ERR_CUDA;
     if (fused)
-        return launch_vec_mma(q, k, v, a, beta, h0, out, hT, plan, H, b, tiles, segs, ws + plan_b,
-                              stream) == cudaSuccess
+        return launch_vec_mma(q, k, v, a, beta, h0, out, hT, plan, H, b, segs, ws + plan_b, stream) ==
+                       cudaSuccess
                    ? GDR_OK
                    : GDR_ERR_CUDA;
     return launch_vec_forward(q, k, v, a, beta, h0, out, hT, dtype, plan, H, dk, dv, s.T_total, tiles,

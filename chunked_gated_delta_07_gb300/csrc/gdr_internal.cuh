@@ -124,12 +124,11 @@ cudaError_t launch_vec_forward(const void *q, const void *k, const void *v, cons
                                cudaStream_t stream);
 
 // per-channel decay, bf16 and dk = dv = 128: fused tensor-core kernel (gdr_vec_mma.cu)
-size_t vec_mma_scratch_bytes(int64_t tiles, int N, int H);
+size_t vec_mma_scratch_bytes(int64_t max_segs, int H);
 int vec_mma_segment_tiles(int64_t tiles, int H, int sms);
 cudaError_t launch_vec_mma(const void *q, const void *k, const void *v, const void *a,
                            const void *beta, const float *h0, void *out, float *hT, Plan plan,
-                           int H, float b, int64_t max_tiles, int64_t max_segs, void *scratch,
-                           cudaStream_t stream);
+                           int H, float b, int64_t max_segs, void *scratch, cudaStream_t stream);
 
 // backward in the chunked form, bf16 d = 128, bounded gate (gdr_bwd_chunk.cu)
 int chunk_bwd_segment_tiles(int64_t tiles, int H, int sms);

@@ -37,10 +37,12 @@
 // max(1, |1 - beta |k|^2|) max_d alpha_{t,d}, so the neglected term is at most
 // the product of those times that state.  w is the latest tile that makes this
 // bound <= e^-46 < 2^-64 (far below fp32 resolution), or the sequence start,
-// where the block starts from h0 exactly.  vec_bound_kernel sums the bound's log
-// per (tile, head); vec_decide_kernel marks the (sequence, head)
-// pairs whose decay is too weak for a warm-up of at most 4 S tiles: those
-// run as one block over the whole sequence, exactly as without segments.
+// where the block starts from h0 exactly.  vec_warm_kernel finds w for every
+// (segment, head) before the main kernel runs: it walks back from the segment
+// start eight tiles at a time, bounding each tile from its a, k and beta, so it
+// reads only the tiles its warm-up spans.  A (sequence, head) pair with a segment
+// start that has no such w within 4 S tiles runs as one block over the whole
+// sequence, exactly as without segments.
 #include "gdr_internal.cuh"
 #include "gdr_mma.cuh"
 
@@ -75,16 +77,14 @@ static_assert(kOffA % 4 == 0 && kPd % 4 == 0, "A rows read in 16-byte pieces");
 __device__ __forceinline__ int raw_slot(int i, int c16) { return i * kD + 8 * (c16 ^ ((i >> 3) << 1)); }
 constexpr size_t kSmemBytes = sizeof(float) * kSmemFloats;
 
-// Per (tile, head): the log of a bound on the norm of the tile's transition,
-// sum over its tokens of  max_d g_{t,d} + ln max(1, |1 - beta_t |k_t|^2|),
+// The log of a bound on the norm of a tile's transition, sum over its tokens of
+//   max_d g_{t,d} + ln max(1, |1 - beta_t |k_t|^2|),
 // with max_d g = -b sigmoid(min_d a) (the gate is decreasing in a).  One warp per
-// (tile, head), the head fastest across warps (so the warps running together read
-// whole token rows): lane l loads channels 4l..4l+3 of every token.  The 16
-// per-token reductions over the lanes run as one butterfly that halves the tokens
-// a lane keeps at each step: afterwards lanes 2j and 2j + 1 hold the complete
-// minimum and squared norm of token j (in a lane-bit order), and each evaluates
-// that token's term once.
-constexpr int kBoundWarps = 8;
+// tile: lane l loads channels 4l..4l+3 of every token.  The 16 per-token reductions
+// over the lanes run as one butterfly that halves the tokens a lane keeps at each
+// step: afterwards lanes 2j and 2j + 1 hold the complete minimum and squared norm
+// of token j (in a lane-bit order), and each token's term is evaluated once.
+// Returns the sum in every lane.
 
 // One butterfly step over n tokens: lanes whose bit `o` is clear keep the first
 // n/2, the others the last n/2, each combining its kept half with its partner's.
@@ -99,19 +99,10 @@ __device__ __forceinline__ void bound_step(float (&x)[kT], int o, bool upper) {
     }
 }
 
-__global__ void __launch_bounds__(32 * kBoundWarps)
-vec_bound_kernel(const __nv_bfloat16 *__restrict__ a, const __nv_bfloat16 *__restrict__ k,
-                 const __nv_bfloat16 *__restrict__ beta, float *__restrict__ lam, Plan p, int H,
-                 float b, int64_t max_tiles) {
-    const int lane = threadIdx.x & 31;
-    const int64_t idx = (int64_t)blockIdx.x * kBoundWarps + (threadIdx.x >> 5);
-    const int64_t c = idx / H;
-    const int h = (int)(idx - c * H);
-    if (c >= max_tiles) return;
-    const int n = find_owner(p.chunk_base, p.N, c);
-    if (n < 0) return;
-    const int64_t t0 = p.seq_start[n] + (c - p.chunk_base[n]) * kT;
-    const int len = (int)min((int64_t)kT, p.seq_start[n + 1] - t0);
+__device__ __forceinline__ float tile_bound_log(const __nv_bfloat16 *__restrict__ a,
+                                                const __nv_bfloat16 *__restrict__ k,
+                                                const __nv_bfloat16 *__restrict__ beta, int64_t t0,
+                                                int len, int H, int h, float b, int lane) {
     uint2 ra[kT], rk[kT];
 #pragma unroll
     for (int i = 0; i < kT; ++i) {
@@ -152,27 +143,71 @@ vec_bound_kernel(const __nv_bfloat16 *__restrict__ a, const __nv_bfloat16 *__res
         x = gate_logdecay(mt, b, GDR_GATE_BOUNDED) + logf(fmaxf(1.f, fabsf(1.f - bt * kt)));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    if (lane == 0) lam[c * H + h] = x;
+    return x;
 }
 
-// Per (sequence, head): 1 if every segment start has a bound <= 2^-64 within
-// 4 S tiles before it (or the sequence start within reach), else 0.
-__global__ void __launch_bounds__(32)
-vec_decide_kernel(const float *__restrict__ lam, int *__restrict__ ok, Plan p, int H) {
-    const int h = blockIdx.x % H, n = blockIdx.x / H;
-    const int lane = threadIdx.x;
-    const int64_t base = p.chunk_base[n], nt = p.chunk_base[n + 1] - base;
-    int good = 1;
-    const int seg = p.seg_chunks, max_warm = kWarmFactor * seg;
-    for (int64_t s0 = seg; s0 < nt && good; s0 += seg) {
-        if (s0 <= max_warm) continue;   // the warm-up can always reach the sequence start
-        float acc = 0.f;
-        for (int i = lane; i < max_warm; i += 32) acc += lam[(base + s0 - 1 - i) * H + h];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        good = acc <= kHorizonLog;
+// Per (segment, head): the warm-up length s0 - w, where w is the latest tile
+// <= s0 (the segment start) whose bound to s0 is <= e^-46, or the sequence start
+// when none is; -1 when s0 > 4 S and no w >= s0 - 4 S exists.  Segment 0 writes 0.
+// Warp i bounds tile top - 1 - i; warp 0 scans the eight sums from the top down.
+// The walk ends after at most 4 S / 8 steps.
+constexpr int kWarmWarps = 8;
+constexpr int64_t kWalking = -2;
+
+__global__ void __launch_bounds__(32 * kWarmWarps)
+vec_warm_kernel(const __nv_bfloat16 *__restrict__ a, const __nv_bfloat16 *__restrict__ k,
+                const __nv_bfloat16 *__restrict__ beta, int *__restrict__ warm, Plan p, int H,
+                float b) {
+    __shared__ float lam_s[kWarmWarps];
+    __shared__ long long res;
+    const int h = blockIdx.x % H;
+    const int64_t sg = blockIdx.x / H;
+    const int n = find_owner(p.seg_base, p.N, sg);
+    if (n < 0) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t s0 = (sg - p.seg_base[n]) * p.seg_chunks;
+    if (s0 == 0) {
+        if (threadIdx.x == 0) warm[sg * H + h] = 0;
+        return;
     }
-    if (lane == 0) ok[(int64_t)n * H + h] = good;
+    const int64_t sstart = p.seq_start[n], send = p.seq_start[n + 1];
+    const int64_t max_warm = (int64_t)kWarmFactor * p.seg_chunks;
+    const int64_t floor_w = s0 > max_warm ? s0 - max_warm : 0;   // lowest tile the walk visits
+    if (threadIdx.x == 0) res = kWalking;
+    float acc = 0.f;   // warp 0: the bound's log over [top, s0)
+    for (int64_t top = s0;; top -= kWarmWarps) {
+        const int64_t c = top - 1 - warp;
+        float lw = 0.f;
+        if (c >= floor_w) {
+            const int64_t t0 = sstart + c * kT;
+            lw = tile_bound_log(a, k, beta, t0, (int)min((int64_t)kT, send - t0), H, h, b, lane);
+        }
+        if (lane == 0) lam_s[warp] = lw;
+        __syncthreads();
+        if (warp == 0) {
+            const bool valid = lane < kWarmWarps && top - 1 - lane >= floor_w;
+            float x = valid ? lam_s[lane] : 0.f;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, valid && acc + x <= kHorizonLog);
+            if (lane == 0) {
+                if (hit)
+                    res = s0 - (top - 1 - (__ffs(hit) - 1));
+                else if (top - kWarmWarps <= floor_w)
+                    res = floor_w == 0 ? s0 : -1;   // from h0 at the sequence start, or none
+            }
+            acc += __shfl_sync(0xffffffffu, x, 31);
+        }
+        __syncthreads();
+        const long long r = res;   // written again only after the next first barrier
+        if (r != kWalking) {
+            if (threadIdx.x == 0) warm[sg * H + h] = (int)r;
+            return;
+        }
+    }
 }
 
 __global__ void __launch_bounds__(kThreads, 2)
@@ -180,12 +215,12 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
                const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ a,
                const __nv_bfloat16 *__restrict__ beta, const float *__restrict__ h0,
                __nv_bfloat16 *__restrict__ out, float *__restrict__ hT, Plan p, int H, float b,
-               const float *__restrict__ lam, const int *__restrict__ seg_ok) {
+               const int *__restrict__ warm) {
     extern __shared__ float sm[];
     float *Kt = sm + kOffKt, *Kh = sm + kOffKh, *Qt = sm + kOffQt;
     float *Ub = sm + kOffU, *Am = sm + kOffA, *Pm = sm + kOffP, *eg = sm + kOffEg, *bs = sm + kOffB;
     __nv_bfloat16 *Os = (__nv_bfloat16 *)(sm + kOffO);
-    __shared__ int warm_start;
+    __shared__ int warm_start, seg_all;
     const int h = blockIdx.x % H;
     const int64_t sg = blockIdx.x / H;   // global segment
     const int n = find_owner(p.seg_base, p.N, sg);
@@ -195,36 +230,22 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
     const int c0 = 16 * warp;   // this warp's 16 value channels
     const int64_t tile0 = p.chunk_base[n], ntiles = p.chunk_base[n + 1] - tile0;
     const int64_t j = sg - p.seg_base[n];
-    const bool segmented = seg_ok[(int64_t)n * H + h] != 0;
+    // the pair runs in segments only if every segment start found its warm-up
+    if (warp == 0) {
+        const int64_t first = p.seg_base[n], nseg = p.seg_base[n + 1] - first;
+        bool ok = true;
+        for (int64_t i = lane; i < nseg; i += 32) ok = ok && warm[(first + i) * H + h] >= 0;
+        ok = __all_sync(0xffffffffu, ok);
+        if (lane == 0) {
+            seg_all = ok;
+            warm_start = ok ? warm[sg * H + h] : 0;
+        }
+    }
+    __syncthreads();
+    const bool segmented = seg_all != 0;
     if (!segmented && j > 0) return;   // one block runs the whole sequence
     const int64_t s0 = segmented ? j * p.seg_chunks : 0;
     const int64_t s1 = segmented ? min(ntiles, s0 + (int64_t)p.seg_chunks) : ntiles;
-    // warm-up start: the latest tile w <= s0 whose bound to s0 is <= 2^-64
-    if (warp == 0) {
-        int64_t w = s0;
-        float acc = 0.f;
-        bool done = s0 == 0;
-        while (!done) {
-            const int64_t i = w - 1 - lane;
-            float x = i >= 0 ? lam[(tile0 + i) * H + h] : 0.f;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
-            }
-            const unsigned hit = __ballot_sync(0xffffffffu, i >= 0 && acc + x <= kHorizonLog);
-            if (hit) {
-                w = w - 1 - (__ffs(hit) - 1);
-                done = true;
-            } else {
-                acc += __shfl_sync(0xffffffffu, x, 31);
-                w = max(w - 32, (int64_t)0);
-                done = w == 0;
-            }
-        }
-        if (lane == 0) warm_start = (int)(s0 - w);
-    }
-    __syncthreads();
     const int64_t w0 = s0 - warm_start;   // first tile run
     const size_t hbase = ((size_t)n * H + h) * kD * kD;
     const bool from_h0 = w0 == 0 && h0;
@@ -454,8 +475,8 @@ vec_mma_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
 
 }  // namespace
 
-size_t vec_mma_scratch_bytes(int64_t tiles, int N, int H) {
-    return sizeof(float) * (size_t)tiles * H + sizeof(int) * (size_t)N * H + 2 * 256;
+size_t vec_mma_scratch_bytes(int64_t max_segs, int H) {
+    return sizeof(int) * (size_t)max_segs * H + 256;
 }
 
 // Segment length: the longest of 64, 128, 256 tiles that still leaves about eight
@@ -468,39 +489,29 @@ int vec_mma_segment_tiles(int64_t tiles, int H, int sms) {
 
 cudaError_t launch_vec_mma(const void *q, const void *k, const void *v, const void *a,
                            const void *beta, const float *h0, void *out, float *hT, Plan plan,
-                           int H, float b, int64_t max_tiles, int64_t max_segs, void *scratch,
-                           cudaStream_t stream) {
+                           int H, float b, int64_t max_segs, void *scratch, cudaStream_t stream) {
     if (plan.C != kT || plan.seg_chunks < kSegMin || plan.seg_chunks > kSegMax) return cudaErrorInvalidValue;
-    float *lam = (float *)scratch;
-    int *ok = (int *)((char *)scratch + (sizeof(float) * (size_t)max_tiles * H + 255) / 256 * 256);
+    const int64_t blocks = max_segs * H;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+    if (blocks == 0) return cudaSuccess;
+    int *warm = (int *)scratch;
     cudaError_t err;
-    if (max_tiles > 0) {
-        ProfScope prof(stream, "vec_bound_kernel");
-        const int64_t warps = max_tiles * H;
-        if ((warps + kBoundWarps - 1) / kBoundWarps > 0x7fffffff) return cudaErrorInvalidValue;
-        vec_bound_kernel<<<(unsigned)((warps + kBoundWarps - 1) / kBoundWarps), 32 * kBoundWarps, 0,
-                           stream>>>(
-            (const __nv_bfloat16 *)a, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)beta, lam,
-            plan, H, b, max_tiles);
-        count_launch();
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    }
     {
-        ProfScope prof(stream, "vec_decide_kernel");
-        vec_decide_kernel<<<(unsigned)((int64_t)plan.N * H), 32, 0, stream>>>(lam, ok, plan, H);
+        ProfScope prof(stream, "vec_warm_kernel");
+        vec_warm_kernel<<<(unsigned)blocks, 32 * kWarmWarps, 0, stream>>>(
+            (const __nv_bfloat16 *)a, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)beta, warm,
+            plan, H, b);
         count_launch();
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     err = cudaFuncSetAttribute(vec_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)kSmemBytes);
     if (err != cudaSuccess) return err;
-    const int64_t blocks = max_segs * H;
-    if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
     ProfScope prof(stream, "vec_mma_kernel");
     vec_mma_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(
         (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v,
         (const __nv_bfloat16 *)a, (const __nv_bfloat16 *)beta, h0, (__nv_bfloat16 *)out, hT, plan,
-        H, b, lam, ok);
+        H, b, warm);
     count_launch();
     return cudaGetLastError();
 }
