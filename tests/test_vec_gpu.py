@@ -110,6 +110,17 @@ def test_vec_weak_decay_runs_unsegmented():
     _check(_inputs("bf16", 128, 5000, seed=5600, N=1, H=2, a_mean=-6.0), "bf16")
 
 
+def test_vec_one_failed_warm_up_runs_the_pair_unsegmented():
+    """6000 tokens = 375 tiles in 64-tile segments.  Head 0 has a weak decay on tokens
+    1024-5119 (tiles 64-319), so the walk back from the segment start at tile 320 finds
+    no warm-up within 256 tiles: head 0 runs as one block.  Its other segment starts
+    (tiles 64-256) could reach the sequence start, and head 1 decays strongly
+    everywhere, so head 1 runs in segments."""
+    x = _inputs("bf16", 128, 6000, seed=5650, N=1, H=2)
+    x["av"][:, 1024:5120, 0, :] -= 8.0
+    _check(x, "bf16")
+
+
 def test_vec_unnormalised_keys_lengthen_the_warm_up():
     """|k| = 2: each token's erase factor I - beta k k^T can stretch the state by
     |1 - 4 beta|, which the warm-up bound includes."""
