@@ -12,6 +12,10 @@ before the delta-rule write:  H_t = (I - beta_t k_t k_t^T) diag(alpha_t) H_{t-1}
     rewritten, every other row only decays).
 Its backward (``oracle_bwd_vec``) is pinned by finite differences of the forward
 and by its reduction to the scalar backward when all channels share a.
+The bound that places the segmented kernels' warm-up tiles is checked on the
+oracle's trajectories: the norm identity of the erase factor, the per-token maximum
+decay, and that the bound's product dominates the effect of a dropped entering
+state (and that its erase-factor term cannot be left out).
 Planted one-token mistakes in copies of the C source must fail the battery.
 """
 import math
@@ -235,3 +239,85 @@ def test_vec_backward_mutant_is_rejected(tmp_path, name):
               - _vec_loss(dict(x, **{xname: x[xname] - 1e-5 * R}), dout, dhT, 2.0)) / 2e-5
         caught |= abs(fd - float((grad * R).sum())) > 1e-6 * max(1.0, abs(fd))
     assert caught
+
+
+# --------------------------------------------------------------------------
+# the bound behind the segmented per-channel kernels' warm-up tiles
+# --------------------------------------------------------------------------
+def test_erase_factor_norm_identity():
+    """||I - beta k k^T||_2 = max(1, |1 - beta |k|^2|): its eigenvalues are 1 (dk - 1
+    times, on the complement of k) and 1 - beta |k|^2 (on k).  Checked against the
+    matrix 2-norm for unit and unnormalised keys and beta outside [0, 1]."""
+    rng = np.random.default_rng(41)
+    for _ in range(300):
+        dk = int(rng.integers(2, 10))
+        k = rng.standard_normal(dk) * rng.choice([0.3, 1.0, 2.0])
+        beta = rng.uniform(-0.5, 2.0)
+        want = max(1.0, abs(1.0 - beta * float(k @ k)))
+        got = np.linalg.norm(np.eye(dk) - beta * np.outer(k, k), 2)
+        assert abs(got - want) <= 1e-12 * want
+
+
+def test_channel_decay_maximum_is_the_gate_at_the_smallest_input():
+    """max_d exp(g(a_d)) = exp(g(min_d a)) for the bounded gate (g is decreasing in
+    a), so the bound needs one minimum per token, not dk exponentials."""
+    rng = np.random.default_rng(42)
+    for b in (0.5, 2.0, 5.0):
+        a = 3.0 * rng.standard_normal((100, 16))
+        full = np.exp(_g(a, b)).max(axis=1)
+        short = np.exp(_g(a.min(axis=1), b))
+        np.testing.assert_array_equal(full, short)
+
+
+@pytest.mark.parametrize("key_scale,beta_hi", [(1.0, 1.0), (2.0, 1.0), (1.0, 2.0)])
+def test_warm_up_bound_dominates_the_dropped_state(key_scale, beta_hi):
+    """Two runs over the same tokens from different entering states differ by the
+    transitions applied to the difference (the recurrence is affine in the state).
+    After every token the difference stays within
+        prod_t max(1, |1 - beta_t |k_t|^2|) max_d alpha_{t,d}
+    times the entering one: the bound that places the warm-up tiles.  Each run is
+    taken one token at a time by chaining hT into h0; unnormalised keys and beta > 1
+    make some tokens' erase factors expansive."""
+    rng = np.random.default_rng(43)
+    T, dk, dv, b = 64, 8, 6, 2.0
+    q, k, v, a, beta, h0 = _vec_case(rng, T, dk=dk, dv=dv)
+    k = k * key_scale
+    beta = rng.uniform(0.0, beta_hi, beta.shape)
+    h1 = rng.standard_normal(h0.shape)
+    d0 = np.linalg.norm(h1 - h0)
+    Ha, Hb = h0.copy(), h1.copy()
+    log_bound = 0.0
+    for t in range(T):
+        sl = slice(t, t + 1)
+        _, Ha = oracle.oracle_fwd_vec(q[:, sl], k[:, sl], v[:, sl], a[:, sl], beta[:, sl], h0=Ha, b=b)
+        _, Hb = oracle.oracle_fwd_vec(q[:, sl], k[:, sl], v[:, sl], a[:, sl], beta[:, sl], h0=Hb, b=b)
+        kt, bt = k[0, t, 0], beta[0, t, 0]
+        log_alpha_max = float(_g(a[0, t, 0].min(), b))
+        log_bound += log_alpha_max + math.log(max(1.0, abs(1.0 - bt * float(kt @ kt))))
+        dt = np.linalg.norm(Hb - Ha)
+        assert dt <= math.exp(log_bound) * d0 * (1 + 1e-9), (t, dt, math.exp(log_bound) * d0)
+
+
+def test_erase_factor_term_is_needed():
+    """Every key 2 e_1 with beta = 1 and an almost undamped gate (a = -8): each token
+    multiplies the e_1 row of the state difference by 1 - 4 = -3.  The decay-only
+    product prod_t max_d alpha_{t,d} (about 1) is exceeded, while the bound with
+    the erase factor's term (3 alpha per token) holds, here with equality."""
+    T, dk, dv, b = 6, 4, 3, 2.0
+    rng = np.random.default_rng(44)
+    q = rng.standard_normal((1, T, 1, dk))
+    k = np.zeros((1, T, 1, dk))
+    k[..., 0] = 2.0
+    v = rng.standard_normal((1, T, 1, dv))
+    a = np.full((1, T, 1, dk), -8.0)
+    beta = np.ones((1, T, 1))
+    h0 = np.zeros((1, 1, dk, dv))
+    h1 = h0.copy()
+    h1[0, 0, 0] = rng.standard_normal(dv)        # the difference lies in the e_1 row
+    d0 = np.linalg.norm(h1 - h0)
+    _, Ha = oracle.oracle_fwd_vec(q, k, v, a, beta, h0=h0, b=b)
+    _, Hb = oracle.oracle_fwd_vec(q, k, v, a, beta, h0=h1, b=b)
+    dT = np.linalg.norm(Hb - Ha)
+    alpha = math.exp(float(_g(-8.0, b)))
+    assert dT > 100 * alpha ** T * d0                  # decay-only bound: far exceeded
+    np.testing.assert_allclose(dT, (3.0 * alpha) ** T * d0, rtol=1e-12)
