@@ -39,6 +39,15 @@
  *   beta is a probability (used as given, not passed through a sigmoid).
  *   q and k are used as given: no scaling, no normalisation.
  *
+ * Precondition of the tensor-core path (GDR_PATH_TC, and GDR_PATH_AUTO where it
+ * picks that path): 0 <= beta_t |k_t|^2 <= 2 for every token, e.g. unit-norm
+ * keys with beta in [0, 1], as the layer produces them.  Then every erase
+ * factor I - beta k k^T has norm <= 1, and the path's segment scan may drop
+ * what enters a segment more than 64 ln 2 of accumulated log-decay before its
+ * end (attenuated below 2^-64).  For other inputs set the environment variable
+ * GDR_TC_EXACT=1 (no truncation) or use GDR_PATH_SIMT; the CUDA-core,
+ * per-channel, decode and backward calls hold for any input.
+ *
  * Ownership and concurrency.  All tensor pointers of gdr_chunk_fwd* and of
  * the stage calls are DEVICE pointers owned by the caller; the library
  * retains none of them.  Calls are asynchronous on `stream` (NULL = the
