@@ -249,6 +249,36 @@ def test_state_norm_bound_along_trajectory():
         H = Hn
 
 
+def test_dropped_state_decays_with_the_gate_for_unit_keys():
+    """The tensor-core path's segment truncation: for unit keys and beta in [0, 1] the
+    erase factors have norm <= 1, so two runs over the same tokens from different
+    entering states stay within prod_t alpha_t of their entering difference.
+    Outside that precondition (beta |k|^2 = 3, an erase factor of norm 2) the
+    decay-only product is exceeded."""
+    rng = np.random.default_rng(9)
+    T, dk, dv = 12, 8, 6   # the product of decays stays far above fp64 rounding of the states
+    q, k, v, a, beta, h0 = _case(rng, T, dk=dk, dv=dv, h0_std=1.0)
+    h1 = rng.standard_normal(h0.shape)
+    _, Ha = oracle.oracle_fwd(q, k, v, a, beta, h0=h0, b=2.0)
+    _, Hb = oracle.oracle_fwd(q, k, v, a, beta, h0=h1, b=2.0)
+    decay = math.exp(sum(oracle.gate(x, 2.0) for x in a[0, :, 0]))
+    assert decay > 1e-8
+    slack = 1e-14 * max(np.linalg.norm(Ha), np.linalg.norm(Hb))
+    assert np.linalg.norm(Hb - Ha) <= decay * np.linalg.norm(h1 - h0) * (1 + 1e-9) + slack
+    # every key e_1 scaled to |k|^2 = 3, beta = 1: the e_1 row is multiplied by -2 alpha
+    k3 = np.zeros_like(k)
+    k3[..., 0] = math.sqrt(3.0)
+    ones = np.ones_like(beta)
+    a8 = np.full_like(a, -8.0)
+    d = np.zeros_like(h0)
+    d[0, 0, 0] = rng.standard_normal(dv)
+    _, Ha = oracle.oracle_fwd(q, k3, v, a8, ones, h0=h0, b=2.0)
+    _, Hb = oracle.oracle_fwd(q, k3, v, a8, ones, h0=h0 + d, b=2.0)
+    alpha = math.exp(oracle.gate(-8.0, 2.0))
+    np.testing.assert_allclose(np.linalg.norm(Hb - Ha), (2 * alpha) ** T * np.linalg.norm(d), rtol=1e-9)
+    assert np.linalg.norm(Hb - Ha) > 1e3 * alpha ** T * np.linalg.norm(d)   # 2^12 = 4096
+
+
 def test_chaining_and_varlen_equal_separate_calls():
     """fwd(x[0:T]) == fwd(x[s:T], h0 = fwd(x[0:s]).hT), and a packed varlen call
     equals one call per sequence."""
