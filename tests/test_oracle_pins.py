@@ -93,6 +93,37 @@ def test_gate_tile_reciprocal_fits_bf16_only_when_bounded():
     assert worst_softplus > math.log(bf16_max)
 
 
+@pytest.mark.parametrize("C,b,overflows", [(16, 2.0, False), (16, 8.0, True), (32, 2.0, False),
+                                             (32, 8.0, True), (64, 2.0, False), (64, 8.0, True)])
+def test_factored_tile_form_breaks_where_the_tile_decay_leaves_fp32(C, b, overflows):
+    """Where the factored in-tile form (Q (.) e^G)(K (.) e^-G)^T breaks, on the gate
+    recipe of the 32-head, 65,536-token workload (a ~ N(0, 2)).  The form needs
+    e^{-G} inside fp32, i.e. an in-tile |G| below ln(FLT_MAX) = 88.7.  Over 65,536
+    tokens the largest in-tile |G| stays below that for b = 2 at C = 16, 32 and 64
+    (at most b C = 32, 64, 128; 78.8 reached at C = 64).  It exceeds that for b = 8 at
+    every C.  In the worst tile the factored fp32 Gram then has non-finite entries on
+    and below the diagonal, while the pairwise form (e^{G_i - G_j} <= 1, the one the
+    scalar kernels use) stays finite for every case."""
+    rng = np.random.default_rng(1002)
+    a = 2.0 * rng.standard_normal(65536)
+    g = -b / (1.0 + np.exp(-a))                     # the bounded gate, restated in numpy
+    np.testing.assert_allclose(g[:64], _g(a[:64], b), rtol=1e-15, atol=0)
+    n = len(g) // C
+    G = np.cumsum(g[: n * C].reshape(n, C), axis=1)
+    worst = int(np.argmin(G[:, -1]))
+    f32_max_log = math.log(float(np.finfo(np.float32).max))
+    assert (-G[worst, -1] > f32_max_log) == overflows
+    Gt = G[worst].astype(np.float32)
+    q = _rand_unit(rng, C, 16).astype(np.float32)
+    k = _rand_unit(rng, C, 16).astype(np.float32)
+    lower = np.tril(np.ones((C, C), dtype=bool))
+    with np.errstate(over="ignore", invalid="ignore"):
+        factored = (q * np.exp(Gt)[:, None]) @ (k * np.exp(-Gt)[:, None]).T
+    pairwise = (q @ k.T) * np.exp(np.where(lower, Gt[:, None] - Gt[None, :], np.float32(-np.inf)))
+    assert np.isfinite(pairwise).all()
+    assert bool(np.isfinite(factored[lower]).all()) == (not overflows)
+
+
 def test_gate_symmetry_and_softplus():
     rng = np.random.default_rng(1)
     for b in (2.0, 5.0, 8.0):
