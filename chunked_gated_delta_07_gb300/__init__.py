@@ -146,8 +146,10 @@ def recurrent_fwd(q, k, v, a, beta, state, b=2.0, gate="bounded", out=None, stre
     """Decode T tokens: q,k [N,T,H,dk], v [N,T,H,dv], a,beta [N,T,H] on one device, state
     [N,H,dk,dv] fp32 updated in place; returns out [N,T,H,dv] (raises GdrError on failure)."""
     import torch
-    N, T, H, dk = q.shape
-    dv = v.shape[-1]
+    if state is None:
+        raise ValueError("state is required")
+    N, T, H, dk, dv, _ = check_sequence_inputs(q, k, v, a, beta, h0=state, out=out)
+    _require_cuda(q)
     if out is None:
         out = torch.empty((N, T, H, dv), dtype=q.dtype, device=q.device)
     rc = gdr_recurrent_fwd(q, k, v, a, beta, state, out, N, T, H, dk, dv, b, dtype_code(q),
@@ -178,9 +180,8 @@ def chunk_fwd_vec(q, k, v, a, beta, h0=None, cu_seqlens=None, b=2.0, want_state=
                   stream=None):
     """Allocate and return (out, hT) of the per-channel decay form."""
     import torch
-    B, T, H, dk = q.shape
-    dv = v.shape[-1]
-    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    B, T, H, dk, dv, N = check_sequence_inputs(q, k, v, a, beta, h0, cu_seqlens, per_channel=True)
+    _require_cuda(q)
     out = torch.empty_like(v)
     hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device) if want_state else None
     rc = gdr_chunk_fwd_vec(q, k, v, a, beta, h0, out, hT, cu_seqlens, N, T, H, dk, dv, 16, b,
@@ -203,9 +204,9 @@ def chunk_bwd_vec(q, k, v, a, beta, dout=None, dhT=None, h0=None, cu_seqlens=Non
                   want_dh0=True, stream=None):
     """Allocate and return (dq, dk, dv, da, dbeta, dh0) of the per-channel form."""
     import torch
-    B, T, H, dk = q.shape
-    dv = v.shape[-1]
-    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    B, T, H, dk, dv, N = check_sequence_inputs(q, k, v, a, beta, h0, cu_seqlens, per_channel=True,
+                                               dout=dout, dhT=dhT)
+    _require_cuda(q)
     dq, dkk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     da, dbeta = torch.empty_like(a), torch.empty_like(beta)
     dh0 = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device) if want_dh0 else None
@@ -235,7 +236,16 @@ def gdr_router_bias_update(load, bias, thresholds, E, mode, q_lo, q_hi, eta, str
 def router_topk(logits, bias, k, load=None, want_logits=True, stream=None):
     """Return (idx [T, k] int32, picked logits [T, k] fp32 or None); counts go to load."""
     import torch
+    if logits is None or logits.dim() != 2:
+        raise ValueError("logits must be [T, E]")
+    if logits.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError(f"logits: dtype {logits.dtype}, expected bfloat16 or float32")
     T, E = logits.shape
+    _expect("logits", logits, (T, E), logits.dtype, logits.device)
+    _expect("bias", bias, (E,), torch.float32, logits.device)
+    if load is not None:
+        _expect("load", load, (E,), torch.int64, logits.device)
+    _require_cuda(logits, "logits")
     idx = torch.empty((T, k), dtype=torch.int32, device=logits.device)
     sel = torch.empty((T, k), dtype=torch.float32, device=logits.device) if want_logits else None
     rc = gdr_router_topk(logits, bias, idx, sel, load, T, E, k, dtype_code(logits), stream)
@@ -247,6 +257,13 @@ def router_topk(logits, bias, k, load=None, want_logits=True, stream=None):
 def router_bias_update(load, bias, mode="sign", q_lo=0.1, q_hi=0.9, eta=1e-3, stream=None):
     """Update bias in place; returns the fp64 thresholds (Q(q_lo), Q(q_hi)) on the device."""
     import torch
+    if bias is None or bias.dim() != 1:
+        raise ValueError("bias must be [E]")
+    _expect("bias", bias, bias.shape, torch.float32, bias.device)
+    _expect("load", load, bias.shape, torch.int64, bias.device)
+    _require_cuda(bias, "bias")
+    if mode not in _QB:
+        raise ValueError(f"mode must be one of {sorted(_QB)}")
     thr = torch.empty(2, dtype=torch.float64, device=bias.device)
     rc = gdr_router_bias_update(load, bias, thr, bias.numel(), _QB[mode], q_lo, q_hi, eta, stream)
     if rc != GDR_OK:
@@ -258,9 +275,8 @@ def chunk_bwd(q, k, v, a, beta, dout=None, dhT=None, h0=None, cu_seqlens=None, c
               gate="bounded", want_dh0=True, stream=None):
     """Allocate and return (dq, dk, dv, da, dbeta, dh0) for tensors laid out as in chunk_fwd."""
     import torch
-    B, T, H, dk = q.shape
-    dv = v.shape[-1]
-    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    B, T, H, dk, dv, N = check_sequence_inputs(q, k, v, a, beta, h0, cu_seqlens, dout=dout, dhT=dhT)
+    _require_cuda(q)
     dq, dkk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     da, dbeta = torch.empty_like(a), torch.empty_like(beta)
     dh0 = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device) if want_dh0 else None
@@ -333,6 +349,70 @@ def dtype_code(t) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
+# ---- argument checks of the tensor-level calls ------------------------------------------
+# The C entry points take pointers and sizes only.  The calls below take the sizes from q
+# (or logits) and check every other tensor against them before the C call, so that a
+# mismatched tensor raises ValueError here instead of being read out of bounds on the
+# device.  Nothing here computes any part of the method.
+
+def _expect(name, t, shape, dtype, device):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device} (the device of the first input)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _require_cuda(t, name="q"):
+    if not t.is_cuda:
+        raise ValueError(f"{name} is on {t.device}: the library runs on CUDA devices only")
+
+
+def check_sequence_inputs(q, k, v, a, beta, h0=None, cu_seqlens=None, per_channel=False,
+                          dout=None, dhT=None, out=None, hT=None):
+    """Check the tensors of a forward or backward call against q [B, T, H, dk]:
+    k [B,T,H,dk], v [B,T,H,dv], a [B,T,H] (or [B,T,H,dk] per channel), beta [B,T,H],
+    all of q's dtype (bf16 or fp32) and device, contiguous; cu_seqlens int32 [N+1] with
+    B = 1; h0, hT, dhT fp32 [N,H,dk,dv]; out, dout like v.  Returns (B, T, H, dk, dv, N).
+    Raises ValueError on the first mismatch (the device kind is checked by the callers)."""
+    import torch
+    if q is None or q.dim() != 4:
+        raise ValueError("q must be [B, T, H, dk]")
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError(f"q: dtype {q.dtype}, expected bfloat16 or float32")
+    B, T, H, dk = q.shape
+    dev, dt = q.device, q.dtype
+    _expect("q", q, (B, T, H, dk), dt, dev)
+    _expect("k", k, (B, T, H, dk), dt, dev)
+    if v is None or v.dim() != 4:
+        raise ValueError("v must be [B, T, H, dv]")
+    dv = v.shape[-1]
+    _expect("v", v, (B, T, H, dv), dt, dev)
+    _expect("a", a, (B, T, H, dk) if per_channel else (B, T, H), dt, dev)
+    _expect("beta", beta, (B, T, H), dt, dev)
+    if cu_seqlens is None:
+        N = B
+    else:
+        if B != 1:
+            raise ValueError("with cu_seqlens the token tensors are [1, T_total, H, *]")
+        if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+            raise ValueError("cu_seqlens must be [N + 1] with N >= 1")
+        _expect("cu_seqlens", cu_seqlens, cu_seqlens.shape, torch.int32, dev)
+        N = cu_seqlens.numel() - 1
+    for name, t in (("h0", h0), ("hT", hT), ("dhT", dhT)):
+        if t is not None:
+            _expect(name, t, (N, H, dk, dv), torch.float32, dev)
+    for name, t in (("out", out), ("dout", dout)):
+        if t is not None:
+            _expect(name, t, (B, T, H, dv), dt, dev)
+    return B, T, H, dk, dv, N
+
+
 def chunk_fwd(q, k, v, a, beta, h0=None, cu_seqlens=None, chunk=16, b=2.0, gate="bounded",
               path="auto", out=None, hT=None, want_state=True, stream=None, workspace=None):
     """Allocate out (and hT), run gdr_chunk_fwd_ex, raise GdrError on a failing status.
@@ -340,9 +420,12 @@ def chunk_fwd(q, k, v, a, beta, h0=None, cu_seqlens=None, chunk=16, b=2.0, gate=
     q,k [B,T,H,dk], v [B,T,H,dv], a,beta [B,T,H] on one CUDA device, all of one
     dtype (bf16 or fp32); with cu_seqlens (int32, N+1) B must be 1."""
     import torch
-    B, T, H, dk = q.shape
-    dv = v.shape[-1]
-    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    B, T, H, dk, dv, N = check_sequence_inputs(q, k, v, a, beta, h0, cu_seqlens, out=out, hT=hT)
+    _require_cuda(q)
+    if workspace is not None:
+        _require_cuda(workspace, "workspace")
+        if workspace.device != q.device or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous tensor on q's device")
     if out is None:
         out = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
     if hT is None and want_state:
