@@ -22,7 +22,9 @@ Independent references live here:
   load counts, linear-interpolation quantiles and the sign or proportional
   bias step, pinned by numpy's stable argsort and quantile and by closed forms.
 * ``chunk_ref`` -- the chunk-parallel (WY / UT) form in fp64 numpy, used only
-  to check the GPU's intermediate stages (gate cumsum, W, U) one by one.
+  to check the GPU's intermediate stages (gate cumsum, W, U) one by one, and the
+  chunked backward's per-tile formulas, checked against ``oracle_bwd`` and
+  ``oracle_bwd_vec``.
 
 Citation keys used in this package (page title, section):
   P1 = "Deep Dive: The Next Generation of Ultra-Long Context Sparse MoE LLMs"

@@ -1,0 +1,107 @@
+"""The chunked backward formulas against the token-by-token adjoint (CPU only).
+
+``oracle.chunk_ref.bwd`` states the backward pass in the chunked, factored form
+the GPU's chunked backward computes (per tile: the two state chains' quantities,
+the triangular solves by back substitution, the gradients of every input).  The
+pages print no backward; this form is the adjoint of the tile algebra.  In fp64 it
+must equal the C oracle's token-by-token adjoint recurrence, itself pinned by
+finite differences of the forward, to rounding: the chunked form is exact, not an
+approximation, so the GPU's tolerance only has to cover its own rounding.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import chunk_ref
+from test_oracle_pins import _case
+
+NAMES = ("dq", "dk", "dv", "da", "dbeta", "dh0")
+
+
+def _grads(rng, B, T, H, dk, dv, per_channel):
+    q, k, v, a, beta, h0 = _case(rng, T, H=H, dk=dk, dv=dv, B=B)
+    if per_channel:
+        a = rng.standard_normal((B, T, H, dk))
+    dout = rng.standard_normal(v.shape)
+    dhT = 0.1 * rng.standard_normal(h0.shape)
+    return q, k, v, a, beta, h0, dout, dhT
+
+
+def _close(got, ref, rtol=1e-9):
+    for n in NAMES:
+        scale = max(1.0, float(np.abs(ref[n]).max()))
+        err = float(np.abs(got[n] - ref[n]).max())
+        assert err <= rtol * scale, f"{n}: max error {err:.3e} (scale {scale:.3e})"
+
+
+@pytest.mark.parametrize("T,chunk", [(1, 16), (16, 16), (37, 16), (50, 8)])
+@pytest.mark.parametrize("per_channel", [False, True])
+def test_chunked_backward_equals_token_adjoint(T, chunk, per_channel):
+    rng = np.random.default_rng(100 + T + chunk + per_channel)
+    q, k, v, a, beta, h0, dout, dhT = _grads(rng, 2, T, 2, 6, 5, per_channel)
+    got = chunk_ref.bwd(q, k, v, a, beta, dout=dout, dhT=dhT, h0=h0, chunk=chunk,
+                        per_channel=per_channel)
+    fn = oracle.oracle_bwd_vec if per_channel else oracle.oracle_bwd
+    ref = fn(q, k, v, a, beta, dout=dout, dhT=dhT, h0=h0, b=2.0)
+    _close(got, ref)
+
+
+def test_chunked_backward_packed_sequences_and_large_bound():
+    """Packed sequences (one empty) and b = 5, the largest bound the factored
+    in-tile form takes at 16-token tiles (e^{-G} up to e^{80})."""
+    rng = np.random.default_rng(7)
+    q, k, v, a, beta, h0, dout, dhT = _grads(rng, 1, 70, 2, 6, 5, True)
+    cu = np.array([0, 9, 9, 40, 70])
+    h0 = 0.1 * rng.standard_normal((4, 2, 6, 5))
+    dhT = 0.1 * rng.standard_normal((4, 2, 6, 5))
+    a = 3.0 * a
+    got = chunk_ref.bwd(q, k, v, a, beta, dout=dout, dhT=dhT, h0=h0, cu_seqlens=cu, b=5.0,
+                        per_channel=True)
+    ref = oracle.oracle_bwd_vec(q, k, v, a, beta, dout=dout, dhT=dhT, h0=h0, cu_seqlens=cu, b=5.0)
+    _close(got, ref)
+    np.testing.assert_array_equal(got["dh0"][1], dhT[1])   # the empty sequence
+
+
+def test_chunked_backward_without_optional_inputs():
+    rng = np.random.default_rng(8)
+    q, k, v, a, beta, _, dout, _ = _grads(rng, 1, 30, 1, 4, 3, False)
+    got = chunk_ref.bwd(q, k, v, a, beta, dout=dout)
+    ref = oracle.oracle_bwd(q, k, v, a, beta, dout=dout, b=2.0)
+    _close(got, ref)
+
+
+def test_a_wrong_tile_term_is_caught():
+    """Dropping the last token's e^{G_C} rowsum(dH1 (.) H0) term from dG, the one that
+    is easiest to miss, moves da well outside the tolerance."""
+    rng = np.random.default_rng(9)
+    q, k, v, a, beta, h0, dout, dhT = _grads(rng, 1, 33, 1, 6, 5, True)
+    ref = oracle.oracle_bwd_vec(q, k, v, a, beta, dout=dout, dhT=dhT, h0=h0, b=2.0)
+    saved = chunk_ref.unit_bwd_channels
+
+    def without_state_term(q_, k_, v_, g_, b_, h0_, do_, dh_, chunk):
+        out = list(saved(q_, k_, v_, g_, b_, h0_, do_, dh_, chunk))
+        # recompute dg with the state term of every tile removed
+        L = k_.shape[0]
+        H = np.array(h0_, copy=True)
+        tiles = []
+        for s in range(0, L, chunk):
+            t = chunk_ref._tile_channels(q_[s:s + chunk], k_[s:s + chunk], v_[s:s + chunk],
+                                         g_[s:s + chunk], b_[s:s + chunk], H)
+            tiles.append((s, t))
+            H = t["H1"]
+        dH = np.array(dh_, copy=True)
+        for s, t in reversed(tiles):
+            e = min(s + chunk, L)
+            dO = do_[s:e]
+            dD = t["S"].T @ dO + t["Ke"] @ dH
+            out[3][s:e] -= t["eGC"] * (dH * t["H0"]).sum(1)   # the term reaches every dg of the tile
+            dH = t["eGC"][:, None] * dH + t["Qt"].T @ dO - t["W"].T @ dD
+        return tuple(out)
+
+    chunk_ref.unit_bwd_channels = without_state_term
+    try:
+        bad = chunk_ref.bwd(q, k, v, a, beta, dout=dout, dhT=dhT, h0=h0, per_channel=True)
+    finally:
+        chunk_ref.unit_bwd_channels = saved
+    err = float(np.abs(bad["da"] - ref["da"]).max())
+    assert err > 1e-3 * max(1.0, float(np.abs(ref["da"]).max()))
