@@ -185,8 +185,41 @@ def _tile_channels(q, k, v, g, beta, H0):
     U = T @ (beta[:, None] * v)
     D = U - W @ H0
     H1 = eGC[:, None] * H0 + Ke.T @ D
+    O = Qt @ H0 + S @ D
     return dict(G=G, eG=eG, enG=enG, Kt=Kt, Kh=Kh, Qt=Qt, eGC=eGC, Ke=Ke, A=A, S=S, T=T, W=W,
-                U=U, D=D, H0=H0, H1=H1)
+                U=U, D=D, H0=H0, H1=H1, O=O)
+
+
+def fwd_channels(q, k, v, a, beta, h0=None, cu_seqlens=None, chunk: int = 16, b: float = 2.0,
+                 mode: str = "bounded"):
+    """Chunked fp64 forward with a log-decay per key channel (a [B,T,H,dk]), tile by
+    tile in the factored form above: O = Qt H0 + S D, H1 = diag(e^{G_C}) H0 + Ke^T D.
+    Returns (out [B,T,H,dv], hT [N,H,dk,dv]); small sizes only."""
+    q, k, v, a, beta = (np.asarray(x, np.float64) for x in (q, k, v, a, beta))
+    B, T, Hh, dk = q.shape
+    dv = v.shape[-1]
+    if cu_seqlens is None:
+        spans = [(n, n * T, (n + 1) * T) for n in range(B)]
+        flat = lambda x: x.reshape((B * T,) + x.shape[2:])  # noqa: E731
+    else:
+        cu = np.asarray(cu_seqlens, dtype=np.int64)
+        spans = [(n, int(cu[n]), int(cu[n + 1])) for n in range(len(cu) - 1)]
+        flat = lambda x: x.reshape((T,) + x.shape[2:])  # noqa: E731
+    qf, kf, vf, af, bf = (flat(x) for x in (q, k, v, a, beta))
+    out = np.zeros((qf.shape[0], Hh, dv))
+    hT = np.zeros((len(spans), Hh, dk, dv))
+    for n, s, e in spans:
+        for h in range(Hh):
+            H = np.zeros((dk, dv)) if h0 is None else np.array(h0, np.float64)[n, h]
+            g = gate(af[s:e, h], b, mode)
+            for t0 in range(s, e, chunk):
+                t1 = min(t0 + chunk, e)
+                t = _tile_channels(qf[t0:t1, h], kf[t0:t1, h], vf[t0:t1, h], g[t0 - s:t1 - s],
+                                   bf[t0:t1, h], H)
+                out[t0:t1, h] = t["O"]
+                H = t["H1"]
+            hT[n, h] = H
+    return out.reshape(q.shape[:3] + (dv,)), hT
 
 
 def unit_bwd_channels(q, k, v, g, beta, h0, dout, dhT, chunk: int):

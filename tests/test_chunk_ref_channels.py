@@ -1,4 +1,5 @@
-"""The chunked backward formulas against the token-by-token adjoint (CPU only).
+"""The chunked per-channel forward and backward formulas against the token-by-token
+oracle (CPU only).
 
 ``oracle.chunk_ref.bwd`` states the backward pass in the chunked, factored form
 the GPU's chunked backward computes (per tile: the two state chains' quantities,
@@ -105,3 +106,27 @@ def test_a_wrong_tile_term_is_caught():
         chunk_ref.unit_bwd_channels = saved
     err = float(np.abs(bad["da"] - ref["da"]).max())
     assert err > 1e-3 * max(1.0, float(np.abs(ref["da"]).max()))
+
+
+@pytest.mark.parametrize("T,chunk,b", [(1, 16, 2.0), (37, 16, 2.0), (64, 16, 5.0), (45, 8, 2.0)])
+def test_chunked_per_channel_forward_equals_token_recurrence(T, chunk, b):
+    """The factored per-channel tile form of the GPU's per-channel forward (Kt, Kh, Qt,
+    Ke, A, S, W, U, D per tile) equals the per-channel oracle to rounding."""
+    rng = np.random.default_rng(200 + T + chunk)
+    q, k, v, a, beta, h0, _, _ = _grads(rng, 2, T, 2, 6, 5, True)
+    o, hT = chunk_ref.fwd_channels(q, k, v, a, beta, h0=h0, chunk=chunk, b=b)
+    ro, rh = oracle.oracle_fwd_vec(q, k, v, a, beta, h0=h0, b=b)
+    np.testing.assert_allclose(o, ro, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(hT, rh, rtol=1e-10, atol=1e-12)
+
+
+def test_chunked_per_channel_forward_packed_sequences():
+    rng = np.random.default_rng(11)
+    q, k, v, a, beta, _, _, _ = _grads(rng, 1, 70, 2, 6, 5, True)
+    cu = np.array([0, 9, 9, 40, 70])
+    h0 = 0.1 * rng.standard_normal((4, 2, 6, 5))
+    o, hT = chunk_ref.fwd_channels(q, k, v, a, beta, h0=h0, cu_seqlens=cu)
+    ro, rh = oracle.oracle_fwd_vec(q, k, v, a, beta, h0=h0, cu_seqlens=cu, b=2.0)
+    np.testing.assert_allclose(o, ro, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(hT, rh, rtol=1e-10, atol=1e-12)
+    np.testing.assert_array_equal(hT[1], h0[1])
