@@ -130,3 +130,93 @@ def test_chunked_per_channel_forward_packed_sequences():
     np.testing.assert_allclose(o, ro, rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(hT, rh, rtol=1e-10, atol=1e-12)
     np.testing.assert_array_equal(hT[1], h0[1])
+
+
+# ---- the segment scheme of the per-channel kernels, in fp64 -----------------------------
+def _segmented(q, k, v, a, beta, h0, S, b=2.0, erase_term=True, horizon=-46.0, chunk=16):
+    """One (sequence, head): q, k [L,dk], v [L,dv], a [L,dk], beta [L].  Tiles are cut
+    into segments of S tiles.  Segment j > 0 starts from a zero state at the latest tile
+    w <= j S whose bound to j S, sum over its tokens of max_d g + ln max(1, |1 - beta |k|^2|),
+    is <= horizon.  w = 0 starts from h0.  If some segment start has no such w within
+    4 S tiles, the whole sequence runs as one segment.  Returns (out, hT, warm-ups)."""
+    L = q.shape[0]
+    g = chunk_ref.gate(a, b)
+    n_t = (L + chunk - 1) // chunk
+    lam = np.zeros(n_t)
+    for c in range(n_t):
+        s, e = c * chunk, min(L, (c + 1) * chunk)
+        erase = np.log(np.maximum(1.0, np.abs(1.0 - beta[s:e] * (k[s:e] ** 2).sum(1))))
+        lam[c] = g[s:e].max(axis=1).sum() + (erase.sum() if erase_term else 0.0)
+    starts = list(range(0, n_t, S))
+    warm = {}
+    for s0 in starts[1:]:
+        acc, w = 0.0, None
+        for c in range(s0 - 1, max(-1, s0 - 4 * S - 1), -1):
+            acc += lam[c]
+            if acc <= horizon:
+                w = c
+                break
+        if w is None and s0 > 4 * S:
+            starts, warm = [0], {}           # no warm-up: one segment
+            break
+        warm[s0] = 0 if w is None else w
+    out = np.zeros((L, v.shape[1]))
+    hT = None
+    for j, s0 in enumerate(starts):
+        s1 = starts[j + 1] if j + 1 < len(starts) else n_t
+        w = warm.get(s0, 0)
+        H = h0.copy() if w == 0 else np.zeros_like(h0)
+        for c in range(w, s1):
+            ts, te = c * chunk, min(L, (c + 1) * chunk)
+            t = chunk_ref._tile_channels(q[ts:te], k[ts:te], v[ts:te], g[ts:te], beta[ts:te], H)
+            if c >= s0:
+                out[ts:te] = t["O"]
+            H = t["H1"]
+        hT = H
+    return out, hT, warm
+
+
+def _unit(rng, L, dk=8, dv=6, key_scale=1.0):
+    q, k, v, _, beta, h0 = _case(rng, L, dk=dk, dv=dv, h0_std=1.0)
+    a = rng.standard_normal((1, L, 1, dk))
+    return (q[0, :, 0], key_scale * k[0, :, 0], v[0, :, 0], a[0, :, 0], beta[0, :, 0], h0[0, 0])
+
+
+def test_segments_from_warm_up_tiles_reproduce_the_sequence():
+    """Unit keys, a ~ N(0, 1): every segment start finds a warm-up tile after the
+    sequence start (7 or 8 tiles back with 8 channels), so every later segment drops its
+    earlier history.  The segmented outputs and final state still equal the unsegmented
+    oracle to fp64 rounding: the dropped parts are below e^-46 of the state."""
+    rng = np.random.default_rng(300)
+    q, k, v, a, beta, h0 = _unit(rng, 16 * 48)
+    out, hT, warm = _segmented(q, k, v, a, beta, h0, S=8)
+    assert len(warm) == 5 and all(0 < w and s0 - w <= 4 * 8 for s0, w in warm.items())   # all truncate
+    ro, rh = oracle.oracle_fwd_vec(*(x[None, :, None] for x in (q, k, v, a, beta)), h0=h0[None, None],
+                                   b=2.0)
+    np.testing.assert_allclose(out, ro[0, :, 0], rtol=0, atol=1e-12 * np.abs(ro).max())
+    np.testing.assert_allclose(hT, rh[0, 0], rtol=0, atol=1e-12 * np.abs(rh).max())
+
+
+def test_the_walk_needs_the_erase_term():
+    """Keys 2 e_1 with beta = 1 on every token: each token multiplies the e_1 row of a
+    dropped state by -3 alpha.  The walk with the erase term finds no warm-up within
+    4 S tiles, so the sequence runs as one segment and matches the oracle.  A walk
+    on the decay alone picks short warm-ups, and its outputs are visibly wrong."""
+    rng = np.random.default_rng(301)
+    L, dk, dv = 16 * 48, 4, 3
+    q = rng.standard_normal((L, dk))
+    k = np.zeros((L, dk))
+    k[:, 0] = 2.0
+    v = rng.standard_normal((L, dv))
+    a = np.full((L, dk), -1.0)                    # alpha = e^{-2 sigmoid(-1)} = 0.58 per token
+    beta = np.ones(L)
+    h0 = rng.standard_normal((dk, dv))
+    ro, _ = oracle.oracle_fwd_vec(*(x[None, :, None] for x in (q, k, v, a, beta)), h0=h0[None, None],
+                                  b=2.0)
+    ro = ro[0, :, 0]
+    out, _, warm = _segmented(q, k, v, a, beta, h0, S=4)
+    assert warm == {}                               # one segment
+    np.testing.assert_allclose(out, ro, rtol=0, atol=1e-12 * np.abs(ro).max())
+    bad, _, warm_bad = _segmented(q, k, v, a, beta, h0, S=4, erase_term=False)
+    assert warm_bad and max(s0 - w for s0, w in warm_bad.items()) < 8
+    assert np.abs(bad - ro).max() > 1e-3 * np.abs(ro).max()
