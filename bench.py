@@ -171,6 +171,91 @@ def cpu_oracle_rate(x, w, budget_s, max_tokens):
     return n / dt, n, threads, dt
 
 
+def _grow_to_budget(run, n_min, budget_s, n_max):
+    """Time run(n) on n_min units, then on as many as fit the budget (at most n_max);
+    returns (units/s, units, seconds)."""
+    n = n_min
+    dt = run(n)
+    n = int(min(n_max, max(n_min, n * budget_s / max(dt, 1e-6))))
+    dt = run(n)
+    return n / dt, n, dt
+
+
+def cpu_rate_vec(x, av, b, budget_s):
+    """The per-channel oracle on the first n tokens of every head (packed tokens taken
+    as one sequence); returns (tokens/s, tokens, threads, seconds)."""
+    import oracle
+    threads = oracle.max_threads()
+
+    def run(n):
+        sl = [t[:, :n].cpu() for t in (x["q"], x["k"], x["v"], av, x["beta"])]
+        t0 = time.perf_counter()
+        oracle.oracle_fwd_vec(*sl, h0=None, b=b, nthreads=threads)
+        return time.perf_counter() - t0
+
+    rate, n, dt = _grow_to_budget(run, 64, budget_s, x["q"].shape[1])
+    return rate, n, threads, dt
+
+
+def cpu_rate_bwd(x, dout, dhT, b, per_channel, budget_s):
+    """The oracle backward on the first n tokens of sequence 0, every head (the
+    per-channel oracle keeps every state, so n <= 1024 there); returns
+    (tokens/s, tokens, threads, seconds)."""
+    import oracle
+    threads = oracle.max_threads()
+    fn = oracle.oracle_bwd_vec if per_channel else oracle.oracle_bwd
+
+    def run(n):
+        sl = [t[:1, :n].cpu() for t in (x["q"], x["k"], x["v"], x["a"], x["beta"], dout)]
+        h0 = None if x["h0"] is None else x["h0"][:1].cpu()
+        d_t = dhT[:1].cpu()
+        t0 = time.perf_counter()
+        fn(*sl[:5], dout=sl[5], dhT=d_t, h0=h0, b=b, nthreads=threads)
+        return time.perf_counter() - t0
+
+    cap = min(x["q"].shape[1], 1024 if per_channel else x["q"].shape[1])
+    rate, n, dt = _grow_to_budget(run, 32, budget_s, cap)
+    return rate, n, threads, dt
+
+
+def cpu_rate_router(logits, bias, k, budget_s):
+    """The router oracle (top-k of logit + bias, counts) on the first n tokens of the
+    window; returns (tokens/s, tokens, threads, seconds)."""
+    import oracle
+
+    def run(n):
+        sl = logits[:n].cpu()
+        bz = bias.cpu()
+        t0 = time.perf_counter()
+        oracle.router_topk(sl, bz, k)
+        return time.perf_counter() - t0
+
+    rate, n, dt = _grow_to_budget(run, 256, budget_s, logits.shape[0])
+    return rate, n, 1, dt
+
+
+def cpu_rate_decode(x, state, b, budget_s):
+    """The oracle on one decode step of the first n sequences, every head; returns
+    (tokens/s, tokens, threads, seconds)."""
+    import oracle
+    threads = oracle.max_threads()
+
+    def run(n):
+        sl = [t[:n].cpu() for t in (x["q"], x["k"], x["v"], x["a"], x["beta"])]
+        h = state[:n].cpu()
+        t0 = time.perf_counter()
+        oracle.oracle_fwd(*sl, h0=h, b=b, nthreads=threads)
+        return time.perf_counter() - t0
+
+    rate, n, dt = _grow_to_budget(run, 1, budget_s, x["q"].shape[0])
+    return rate, n, threads, dt
+
+
+def _cpu_line(rate, n, threads, dt, what):
+    return {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{what}: {n} tokens, fp64 oracle, {dt:.1f} s"}
+
+
 def bench_reference(args, w):
     """The oracle arm: fp64 CPU oracle, a bounded prefix of the workload per step."""
     ws, rank, _ = dist_env()
@@ -428,6 +513,8 @@ def bench_decode(args):
     hbm, _, _, peak_src = peaks()
     byt = 2 * N * H * d * d * 4 + N * H * (4 * d * 2 + 2 * 2)   # state in + out, q k v out, a beta
     achieved = byt / (ms / 1e3) / 1e9
+    cpu = None if args.no_cpu else _cpu_line(*cpu_rate_decode(x, state, 2.0, args.cpu_budget),
+                                             "one decode step of the first sequences x 16 heads")
     print(json.dumps({
         "metric": "decode tokens/s, one recurrent step, 16 heads, d=128, bf16, fp32 state",
         "value": N / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": steps,
@@ -438,6 +525,7 @@ def bench_decode(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": None, "kernel": "recurrent_kernel",
                      "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_step": byt},
+        "cpu_baseline": cpu,
         "gpu_launches": n_launch, "clocks": clk.summary(),
     }), flush=True)
 
@@ -505,6 +593,8 @@ def bench_backward(args):
     _, bf16_tf, _, peak_src = peaks()
     peak = bf16_tf / 2.0
     achieved = flops / (ms / 1e3) / 1e12
+    cpu = None if args.no_cpu else _cpu_line(*cpu_rate_bwd(x, dout, dhT, 2.0, vec, args.cpu_budget),
+                                             "sequence 0, its first tokens x 16 heads, with dout and dhT")
     print(json.dumps({
         "metric": ("backward tokens/s, gated delta rule" + (" with per-channel decay" if vec else "")
                    + ", 16 heads, d=128, bf16 in/out, fp32 math"),
@@ -519,7 +609,7 @@ def bench_backward(args):
                      "algorithmic_flops_per_step": flops, "dominant_kernel": dom_name,
                      "dominant_share": dom_ms / sum(v[0] for v in prof.values()) if prof else None},
         "kernels": {k: {"ms_total": v[0], "launches": v[1]} for k, v in prof.items()},
-        "gpu_launches": n_launch, "clocks": summ or None,
+        "cpu_baseline": cpu, "gpu_launches": n_launch, "clocks": summ or None,
     }), flush=True)
 
 
@@ -572,6 +662,8 @@ def bench_vec(args, w):
     hbm, _, _, peak_src = peaks()
     dom_name, (dom_ms, dom_n) = max(prof.items(), key=lambda kv: kv[1][0]) if prof else ("?", (0.0, 1))
     achieved = byt / (ms / 1e3) / 1e9
+    cpu = None if args.no_cpu else _cpu_line(*cpu_rate_vec(x, av, w.b, args.cpu_budget),
+                                             "the first packed tokens x 16 heads, as one sequence")
     print(json.dumps({
         "metric": "per-channel decay forward tokens/s, bounded gate, bf16 in/out, fp32 state",
         "value": n_tok / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": steps,
@@ -586,7 +678,7 @@ def bench_vec(args, w):
                      "dominant_kernel": dom_name, "dominant_share":
                          dom_ms / sum(v[0] for v in prof.values()) if prof else None},
         "kernels": {k: {"ms_total": v[0], "launches": v[1]} for k, v in prof.items()},
-        "gpu_launches": n_launch, "clocks": clk.summary(),
+        "cpu_baseline": cpu, "gpu_launches": n_launch, "clocks": clk.summary(),
     }), flush=True)
 
 
@@ -638,6 +730,8 @@ def bench_router(args):
     byt = T * E * 2 + T * k * 8 + E * (4 + 8)
     hbm, _, _, peak_src = peaks()
     achieved = byt / (kern_ms / 1e3) / 1e9 if kern_ms > 0 else 0.0
+    cpu = None if args.no_cpu else _cpu_line(*cpu_rate_router(x, bias, k, args.cpu_budget),
+                                             "top-k of the window's first tokens")
     print(json.dumps({
         "metric": "router tokens/s, quantile-balancing window (top-8 of 896 experts + bias step)",
         "value": T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": steps,
@@ -651,7 +745,7 @@ def bench_router(args):
                      "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": byt,
                      "kernel_ms": kern_ms},
         "kernels": {kk: {"ms_total": v[0], "launches": v[1]} for kk, v in prof.items()},
-        "gpu_launches": n_launch, "clocks": clk.summary(),
+        "cpu_baseline": cpu, "gpu_launches": n_launch, "clocks": clk.summary(),
     }), flush=True)
 
 

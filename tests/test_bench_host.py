@@ -95,3 +95,49 @@ def test_reference_arm_line(monkeypatch, capsys):
     assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
     assert line["config"]["workload"].startswith("b2_t4k")
+
+
+# ---- the oracle timed beside the next rows' benchmark modes (CPU tensors, tiny budgets) --
+def _small_inputs(T=48, B=2, H=2):
+    from gdr_inputs import make_inputs
+    return make_inputs(WORKLOADS["b2_t4k"].with_(B=B, H=H), device="cpu", T=T)
+
+
+def _check_rate(res, cap):
+    rate, n, threads, dt = res
+    assert rate > 0 and dt > 0 and threads >= 1
+    assert 1 <= n <= cap
+    line = bench._cpu_line(rate, n, threads, dt, "sample")
+    assert line["kind"] == "oracle" and line["unit"] == "tokens/s" and line["cores"] == threads
+    assert str(n) in line["sample"]
+
+
+def test_cpu_rate_of_the_per_channel_forward():
+    from gdr_inputs import make_channel_gate
+    x = _small_inputs(B=1)
+    av = make_channel_gate(x, 3)
+    _check_rate(bench.cpu_rate_vec(x, av, 2.0, 0.05), x["q"].shape[1])
+
+
+@pytest.mark.parametrize("per_channel", [False, True])
+def test_cpu_rate_of_the_backward(per_channel):
+    from gdr_inputs import make_channel_gate
+    x = _small_inputs()
+    if per_channel:
+        x["a"] = make_channel_gate(x, 4)
+    dout = torch.randn(x["v"].shape).to(x["v"].dtype)
+    dhT = 0.1 * torch.randn(x["h0"].shape)
+    _check_rate(bench.cpu_rate_bwd(x, dout, dhT, 2.0, per_channel, 0.05), x["q"].shape[1])
+
+
+def test_cpu_rate_of_the_router():
+    from gdr_inputs import make_router_logits
+    logits, bias = make_router_logits(512, 64, 9, "bf16", device="cpu")
+    res = bench.cpu_rate_router(logits, bias, 8, 0.05)
+    _check_rate(res, 512)
+    assert res[2] == 1                                # the router oracle is single-threaded
+
+
+def test_cpu_rate_of_one_decode_step():
+    x = _small_inputs(T=1, B=4)
+    _check_rate(bench.cpu_rate_decode(x, x["h0"].clone(), 2.0, 0.05), 4)
