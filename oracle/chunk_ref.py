@@ -222,6 +222,30 @@ def fwd_channels(q, k, v, a, beta, h0=None, cu_seqlens=None, chunk: int = 16, b:
     return out.reshape(q.shape[:3] + (dv,)), hT
 
 
+def tile_grads(t, v, beta, dO, dH1):
+    """The gradients of one tile from its forward quantities t (``_tile_channels``),
+    its V and beta, the output gradient dO and the gradient dH1 at the tile's end.
+    Returns dq, dk [C,dk], dv [C,dv], dg [C,dk], dbeta [C] and dH0 [dk,dv]."""
+    dD = t["S"].T @ dO + t["Ke"] @ dH1
+    dH0 = t["eGC"][:, None] * dH1 + t["Qt"].T @ dO - t["W"].T @ dD
+    dS = np.tril(dO @ t["D"].T)
+    dKe = t["D"] @ dH1.T
+    dW = -dD @ t["H0"].T
+    dQt = dO @ t["H0"].T + dS @ t["Kh"]
+    dYu = t["T"].T @ dD
+    dYw = t["T"].T @ dW
+    dA = -np.tril(dYu @ t["U"].T + dYw @ t["W"].T, -1)
+    bdA = beta[:, None] * dA
+    dKt = beta[:, None] * dYw + bdA @ t["Kh"]
+    dKh = bdA.T @ t["Kt"] + dS.T @ t["Qt"] + dKe * t["eGC"]
+    dv = beta[:, None] * dYu
+    dbeta = (dYu * v).sum(1) + (dYw * t["Kt"]).sum(1) + (dA * (t["Kt"] @ t["Kh"].T)).sum(1)
+    dG = dQt * t["Qt"] + dKt * t["Kt"] - dKh * t["Kh"]
+    dG[-1] += (dKe * t["Ke"]).sum(0) + t["eGC"] * (dH1 * t["H0"]).sum(1)
+    dg = np.cumsum(dG[::-1], axis=0)[::-1]
+    return dQt * t["eG"], dKt * t["eG"] + dKh * t["enG"], dv, dg, dbeta, dH0
+
+
 def unit_bwd_channels(q, k, v, g, beta, h0, dout, dhT, chunk: int):
     """Chunked backward of one unit: q, k [L,dk], v [L,dv], g [L,dk], beta [L], h0 and
     dhT [dk,dv], dout [L,dv].  Returns dq, dk [L,dk], dv [L,dv], dg [L,dk], dbeta [L]
@@ -239,28 +263,8 @@ def unit_bwd_channels(q, k, v, g, beta, h0, dout, dhT, chunk: int):
     dH = np.array(dhT, dtype=np.float64, copy=True)
     for s, t in zip(reversed(starts), reversed(tiles)):
         e = min(s + chunk, L)
-        dO, dH1, bt = dout[s:e], dH, beta[s:e]
-        dD = t["S"].T @ dO + t["Ke"] @ dH1
-        dH0 = t["eGC"][:, None] * dH1 + t["Qt"].T @ dO - t["W"].T @ dD
-        dS = np.tril(dO @ t["D"].T)
-        dKe = t["D"] @ dH1.T
-        dW = -dD @ t["H0"].T
-        dQt = dO @ t["H0"].T + dS @ t["Kh"]
-        dYu = t["T"].T @ dD
-        dYw = t["T"].T @ dW
-        dA = -np.tril(dYu @ t["U"].T + dYw @ t["W"].T, -1)
-        bdA = bt[:, None] * dA
-        dKt = bt[:, None] * dYw + bdA @ t["Kh"]
-        dKh = bdA.T @ t["Kt"] + dS.T @ t["Qt"] + dKe * t["eGC"]
-        dv_[s:e] = bt[:, None] * dYu
-        dbeta[s:e] = ((dYu * v[s:e]).sum(1) + (dYw * t["Kt"]).sum(1)
-                      + (dA * (t["Kt"] @ t["Kh"].T)).sum(1))
-        dG = dQt * t["Qt"] + dKt * t["Kt"] - dKh * t["Kh"]
-        dG[-1] += (dKe * t["Ke"]).sum(0) + t["eGC"] * (dH1 * t["H0"]).sum(1)
-        dg[s:e] = np.cumsum(dG[::-1], axis=0)[::-1]
-        dq[s:e] = dQt * t["eG"]
-        dk_[s:e] = dKt * t["eG"] + dKh * t["enG"]
-        dH = dH0
+        dq[s:e], dk_[s:e], dv_[s:e], dg[s:e], dbeta[s:e], dH = tile_grads(t, v[s:e], beta[s:e],
+                                                                          dout[s:e], dH)
     return dq, dk_, dv_, dg, dbeta, dH
 
 

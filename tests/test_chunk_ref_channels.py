@@ -220,3 +220,115 @@ def test_the_walk_needs_the_erase_term():
     bad, _, warm_bad = _segmented(q, k, v, a, beta, h0, S=4, erase_term=False)
     assert warm_bad and max(s0 - w for s0, w in warm_bad.items()) < 8
     assert np.abs(bad - ro).max() > 1e-3 * np.abs(ro).max()
+
+
+# ---- the chunked backward's two-sided segments, in fp64 ----------------------------------
+def _segmented_bwd(q, k, v, a, beta, h0, dout, dhT, S, b=2.0, horizon=-46.0, chunk=16):
+    """One unit, per-channel gate.  The forward chain of each segment starts from a
+    zero state at a warm-up tile before it (the sequence start: h0); the adjoint chain
+    of each segment starts from a zero gradient at a warm-up tile after its end (the
+    sequence end: dhT).  Both warm-ups use the same per-tile bound, sum over the tokens
+    of max_d g + ln max(1, |1 - beta |k|^2|) (the adjoint transition is the transpose).
+    If a boundary has no warm-up within 4 S tiles on either side, one segment.  Every
+    tile's gradients then come from its stored entering state and end gradient.
+    Returns (dict of the unit's gradients, number of segments)."""
+    L, dk = k.shape
+    g = chunk_ref.gate(a, b)
+    n_t = (L + chunk - 1) // chunk
+    tl = [(c * chunk, min(L, (c + 1) * chunk)) for c in range(n_t)]
+    lam = np.array([g[s:e].max(axis=1).sum()
+                    + np.log(np.maximum(1.0, np.abs(1.0 - beta[s:e] * (k[s:e] ** 2).sum(1)))).sum()
+                    for s, e in tl])
+    starts = list(range(0, n_t, S))
+    ends = starts[1:] + [n_t]
+    fw, aw = {0: 0}, {n_t: n_t}
+    for s1 in starts[1:]:
+        acc, w = 0.0, None                       # forward chain of the segment starting at s1
+        for c in range(s1 - 1, max(-1, s1 - 4 * S - 1), -1):
+            acc += lam[c]
+            if acc <= horizon:
+                w = c
+                break
+        acc, e = 0.0, None                       # adjoint chain of the segment ending at s1
+        for c in range(s1, min(n_t, s1 + 4 * S)):
+            acc += lam[c]
+            if acc <= horizon:
+                e = c + 1
+                break
+        if (w is None and s1 > 4 * S) or (e is None and s1 + 4 * S < n_t):
+            starts, ends, fw, aw = [0], [n_t], {0: 0}, {n_t: n_t}
+            break
+        fw[s1] = 0 if w is None else w
+        aw[s1] = n_t if e is None else e
+    H0s, tiles = {}, {}
+    for s0, s1 in zip(starts, ends):             # forward chains: entering states of their tiles
+        w = fw[s0]
+        H = h0.copy() if w == 0 else np.zeros_like(h0)
+        for c in range(w, s1):
+            s, e = tl[c]
+            t = chunk_ref._tile_channels(q[s:e], k[s:e], v[s:e], g[s:e], beta[s:e], H)
+            if c >= s0:
+                H0s[c], tiles[c] = H, t
+            H = t["H1"]
+    res = {n: np.zeros_like(x) for n, x in (("dq", k), ("dk", k), ("dv", v), ("da", a),
+                                            ("dbeta", beta))}
+    dh0 = None
+    for s0, s1 in zip(starts, ends):             # adjoint chains: end gradients, then tile gradients
+        e_w = aw[s1]
+        dH = dhT.copy() if e_w == n_t else np.zeros_like(dhT)
+        for c in range(e_w - 1, s0 - 1, -1):
+            s, e = tl[c]
+            gq, gk, gv, gg, gb, dH0 = chunk_ref.tile_grads(tiles[c], v[s:e], beta[s:e], dout[s:e], dH)
+            if c < s1:
+                res["dq"][s:e], res["dk"][s:e], res["dv"][s:e], res["dbeta"][s:e] = gq, gk, gv, gb
+                res["da"][s:e] = gg * chunk_ref.gate_grad(a[s:e], b)
+            dH = dH0
+        if s0 == 0:
+            dh0 = dH
+    res["dh0"] = dh0
+    return res, len(starts)
+
+
+def test_backward_segments_from_two_sided_warm_ups_reproduce_the_gradients():
+    """Unit keys, a ~ N(0, 1), 6 segments of 8 tiles: both chains of every interior
+    boundary find warm-ups, and the gradients equal the unsegmented oracle's to
+    fp64 rounding."""
+    rng = np.random.default_rng(500)
+    L, dk, dv = 16 * 48, 8, 6
+    q, k, v, _, beta, h0 = _case(rng, L, dk=dk, dv=dv, h0_std=1.0)
+    a = rng.standard_normal((1, L, 1, dk))
+    dout = rng.standard_normal(v.shape)
+    dhT = rng.standard_normal(h0.shape)
+    got, nseg = _segmented_bwd(q[0, :, 0], k[0, :, 0], v[0, :, 0], a[0, :, 0], beta[0, :, 0],
+                               h0[0, 0], dout[0, :, 0], dhT[0, 0], S=8)
+    assert nseg == 6
+    ref = oracle.oracle_bwd_vec(q, k, v, a, beta, dout=dout, dhT=dhT, h0=h0, b=2.0)
+    for n in ("dq", "dk", "dv", "da", "dbeta"):
+        r = ref[n][0, :, 0]
+        np.testing.assert_allclose(got[n], r, rtol=0, atol=1e-11 * max(1.0, np.abs(r).max()), err_msg=n)
+    np.testing.assert_allclose(got["dh0"], ref["dh0"][0, 0], rtol=0,
+                               atol=1e-11 * max(1.0, np.abs(ref["dh0"]).max()))
+
+
+def test_backward_segments_with_a_short_horizon_are_visible():
+    """Where the bound is tight, a short horizon shows.  Every channel shares one gate
+    (a ~ N(-2, 1)) and beta = 1e-3, so a dropped state or gradient shrinks almost
+    exactly by the bound.  With the horizon at -46 the segmented gradients equal the
+    oracle's to rounding.  At -3 the dropped parts (about e^-3) show in dk and dv."""
+    rng = np.random.default_rng(501)
+    L, dk, dv = 16 * 48, 8, 6
+    q, k, v, _, beta, h0 = _case(rng, L, dk=dk, dv=dv, h0_std=1.0)
+    a = np.repeat((rng.standard_normal((1, L, 1)) - 2.0)[..., None], dk, axis=-1)
+    beta = np.full(beta.shape, 1e-3)
+    dout = rng.standard_normal(v.shape)
+    dhT = rng.standard_normal(h0.shape)
+    ref = oracle.oracle_bwd_vec(q, k, v, a, beta, dout=dout, dhT=dhT, h0=h0, b=2.0)
+    args = (q[0, :, 0], k[0, :, 0], v[0, :, 0], a[0, :, 0], beta[0, :, 0], h0[0, 0], dout[0, :, 0],
+            dhT[0, 0])
+    exact, nseg = _segmented_bwd(*args, S=8)
+    short, nseg_s = _segmented_bwd(*args, S=8, horizon=-3.0)
+    assert nseg == nseg_s == 6
+    for n in ("dk", "dv"):
+        scale = np.abs(ref[n]).max()
+        assert np.abs(exact[n] - ref[n][0, :, 0]).max() <= 1e-12 * scale
+        assert np.abs(short[n] - ref[n][0, :, 0]).max() > 1e-3 * scale
