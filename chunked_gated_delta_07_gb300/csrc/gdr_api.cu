@@ -181,6 +181,8 @@ gdr_status_t check_args(const void *q, const void *k, const void *v, const void 
     if (T > ((int64_t)1 << 40) || (int64_t)B * T > ((int64_t)1 << 40)) return GDR_ERR_UNSUPPORTED;
     const bool varlen = cu != nullptr;
     const int64_t T_total = varlen ? T : (int64_t)B * T;
+    // at most 2^40 (token, head) rows, so that no byte count below wraps
+    if (T_total > 0 && (int64_t)H > ((int64_t)1 << 40) / T_total) return GDR_ERR_UNSUPPORTED;
     if (T_total > 0 && (!q || !k || !v || !a || !beta || !out)) return GDR_ERR_INVALID_ARG;
     const size_t es = dtype == GDR_BF16 ? 2 : 4;
     const size_t rows = (size_t)T_total * H;
@@ -456,6 +458,17 @@ gdr_status_t fwd_host_pipelined(const void *q, const void *k, const void *v, con
 }
 
 }  // namespace
+
+gdr_status_t validate_forward(const void *q, const void *k, const void *v, const void *a,
+                              const void *beta, const float *h0, const void *out, const float *hT,
+                              const int32_t *cu, int B, int64_t T, int H, int dk, int dv,
+                              int chunk, float b, gdr_dtype_t dtype, gdr_gate_t gate,
+                              gdr_path_t path) {
+    Shape s;
+    return check_args(q, k, v, a, beta, h0, out, hT, cu, B, T, H, dk, dv, chunk, b, dtype, gate,
+                      path, &s);
+}
+
 }  // namespace gdr
 
 using namespace gdr;

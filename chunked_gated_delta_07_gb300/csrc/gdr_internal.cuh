@@ -71,6 +71,14 @@ __device__ __forceinline__ float gate_logdecay(float a, float b, int gate) {
     return -b / (1.f + expf(-a));
 }
 
+// The argument checks of gdr_chunk_fwd_ex (sizes, dtypes, gate, path, null and
+// overlapping buffers), for entry points that take the same arguments.
+gdr_status_t validate_forward(const void *q, const void *k, const void *v, const void *a,
+                              const void *beta, const float *h0, const void *out, const float *hT,
+                              const int32_t *cu, int B, int64_t T, int H, int dk, int dv,
+                              int chunk, float b, gdr_dtype_t dtype, gdr_gate_t gate,
+                              gdr_path_t path);
+
 // ---- launchers (host side; each returns the launch error) -------------------
 
 // Builds the plan arrays (seq_start, chunk_base, seg_base; N+1 each) and

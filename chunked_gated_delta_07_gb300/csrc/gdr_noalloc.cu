@@ -61,17 +61,20 @@ extern "C" gdr_status_t gdr_chunk_fwd_noalloc(const void *q, const void *k, cons
                                               int dk, int dv, int chunk, float b,
                                               gdr_dtype_t dtype, gdr_gate_t gate,
                                               gdr_stream_t stream) {
-    if (dtype != GDR_BF16 && dtype != GDR_F32) return GDR_ERR_INVALID_ARG;
-    if (gate != GDR_GATE_BOUNDED && gate != GDR_GATE_SOFTPLUS) return GDR_ERR_INVALID_ARG;
-    if (B < 1 || H < 1 || T < 0 || dk < 1 || dv < 1 || chunk < 1) return GDR_ERR_INVALID_ARG;
-    if (gate == GDR_GATE_BOUNDED && !(b > 0.f && b < 3.4e38f)) return GDR_ERR_INVALID_ARG;
-    if ((dk != 64 && dk != 128) || (dv != 64 && dv != 128)) return GDR_ERR_UNSUPPORTED;
-    if (chunk != 16 && chunk != 32 && chunk != 64) return GDR_ERR_UNSUPPORTED;
-    if (T > ((int64_t)1 << 40) || (int64_t)B * T > ((int64_t)1 << 40)) return GDR_ERR_NO_WORKSPACE;
-    const int64_t T_total = (int64_t)B * T;
-    if (T_total > 0 && (!q || !k || !v || !a || !beta || !out)) return GDR_ERR_INVALID_ARG;
+    // the same checks as gdr_chunk_fwd_ex (dense input, CUDA-core path)
+    const gdr_status_t chk = validate_forward(q, k, v, a, beta, h0, out, hT, nullptr, B, T, H, dk,
+                                              dv, chunk, b, dtype, gate, GDR_PATH_SIMT);
+    if (chk != GDR_OK) return chk;
+    const int64_t T_total = (int64_t)B * T;   // <= 2^40 after the checks
 
-    // scratch layout: plan arrays, G [H, B*T], W [B*T, H, dk], U [B*T, H, dv]
+    // scratch layout: plan arrays, G [H, B*T], W [B*T, H, dk], U [B*T, H, dv].
+    // The (token, head) rows are bounded first, by division, so that no byte
+    // count below can wrap whatever H is.
+    const int64_t row_bytes = 4 * (int64_t)(1 + dk + dv);
+    const int64_t max_rows = (int64_t)kNoAllocScratchBytes / row_bytes;
+    if (T_total > max_rows / H) return GDR_ERR_NO_WORKSPACE;
+    if ((int64_t)B > (int64_t)kNoAllocScratchBytes / (3 * (int64_t)sizeof(int64_t)))
+        return GDR_ERR_NO_WORKSPACE;
     const size_t plan_b = round256(3 * sizeof(int64_t) * (size_t)(B + 1));
     const size_t g_b = round256(sizeof(float) * (size_t)H * T_total);
     const size_t w_b = round256(sizeof(float) * (size_t)T_total * H * dk);

@@ -50,7 +50,12 @@ constexpr int kD = 128;          // dk = dv
 constexpr int kC = 16;           // tile length on this path
 constexpr int kNS = 4;           // pipeline stages, one per prep warp
 constexpr int kThreads = 32 * (4 + kNS + 1);   // 4 state warps, kNS prep warps, 1 MMA issuer
-constexpr uint64_t kWaitNs = 2000000000ull;  // bounded waits: 2 s
+// Every wait is bounded.  The pipeline waits use the launch's limit (TcArgs::wait_ns,
+// 2 s unless GDR_TC_WAIT_NS is set, which the tests use to make waits run out); the
+// drains before exit -- a tile copy still in flight, the CTA's last MMAs -- always
+// allow kDrainNs, since the CTA may not leave while either is pending.
+constexpr uint64_t kWaitNs = 2000000000ull;   // default pipeline limit: 2 s
+constexpr uint64_t kDrainNs = 2000000000ull;  // drain limit: 2 s
 // The state is kept as H = Gamma * H^.  Gamma runs down by each tile's decay and
 // is folded into H^ (Gamma reset to 1) before it would drop below kGammaMin, so
 // H^ stays within |H| / kGammaMin and the scaled writes within |Delta| /
@@ -123,6 +128,7 @@ struct TcArgs {
     int64_t T_total;
     int mode;
     int *status;
+    uint64_t wait_ns;   // limit of every pipeline wait
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -312,7 +318,7 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 g_i = args.G[(int64_t)h * args.T_total + t0 + i];
                 b_i = lane < len ? args.Bt[(int64_t)h * args.T_total + t0 + lane] : 0.f;
             }
-            if (c >= kNS && !__all_sync(kFull, mbar_wait(&bar_free[st], ph ^ 1u, kWaitNs))) {
+            if (c >= kNS && !__all_sync(kFull, mbar_wait(&bar_free[st], ph ^ 1u, args.wait_ns))) {
                 if (lane == 0) set_status(args.status, GDR_ERR_TIMEOUT);
                 *abort_prep = 1;
                 break;
@@ -345,7 +351,7 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     hdr->gam = __expf(g_last);
                 }
             }
-            if (!__all_sync(kFull, mbar_wait(&bar_full[st], ph, kWaitNs))) {
+            if (!__all_sync(kFull, mbar_wait(&bar_full[st], ph, args.wait_ns))) {
                 if (lane == 0) set_status(args.status, GDR_ERR_TIMEOUT);
                 *abort_prep = 1;
                 break;
@@ -522,7 +528,8 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         // never leave with a tile copy still in flight
         if (pend_st >= 0) {
-            mbar_wait(&bar_full[pend_st], pend_ph, kWaitNs);
+            if (!__all_sync(kFull, mbar_wait(&bar_full[pend_st], pend_ph, kDrainNs)) && lane == 0)
+                set_status(args.status, GDR_ERR_TIMEOUT);
             __syncwarp();
         }
     } else if (warp == 4 + kNS) {
@@ -545,7 +552,7 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const uint64_t dBU = smem_desc(s0 + kOffBU, 128, (kC / 8) * 128, kSwNone);
             const uint64_t dP = smem_desc(s0 + kOffP, 128, (kC / 8) * 128, kSwNone);
             const uint64_t dWQ = smem_desc(s0 + kOffWQ, 16, 1024, kSw128);
-            bool ok = nch == 0 || __all_sync(kFull, mbar_wait(&bar_init[0], 0, kWaitNs));
+            bool ok = nch == 0 || __all_sync(kFull, mbar_wait(&bar_init[0], 0, args.wait_ns));
             for (int c = 0; c < nch && ok; ++c) {
                 if (__any_sync(kFull, *abort_state != 0 || *abort_prep != 0)) {
                     ok = false;
@@ -554,7 +561,7 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const int st = c % kNS, buf = c & 1;
                 const uint64_t so = (uint64_t)((st * kStage) >> 4);   // stage offset in descriptor units
                 const uint32_t cb = kColB + buf * kColBuf;
-                if (!__all_sync(kFull, mbar_wait(&bar_prep[st], (uint32_t)(c / kNS) & 1u, kWaitNs))) {
+                if (!__all_sync(kFull, mbar_wait(&bar_prep[st], (uint32_t)(c / kNS) & 1u, args.wait_ns))) {
                     ok = false;
                     break;
                 }
@@ -578,7 +585,7 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (lane == 0) TC_TRACE(c, 15);
                 // back: the state update and the in-tile output term, once the
                 // state warps have written this tile's A operands
-                if (!__all_sync(kFull, mbar_wait(&bar_a[0], (uint32_t)c & 1u, kWaitNs))) {
+                if (!__all_sync(kFull, mbar_wait(&bar_a[0], (uint32_t)c & 1u, args.wait_ns))) {
                     ok = false;
                     break;
                 }
@@ -605,7 +612,7 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (lane == 0) set_status(args.status, GDR_ERR_TIMEOUT);
                 *abort_state = 1;
             }
-            __all_sync(kFull, mbar_wait(&bar_fin[0], 0, kWaitNs));
+            __all_sync(kFull, mbar_wait(&bar_fin[0], 0, kDrainNs));
         }
         __syncwarp();
     } else {
@@ -657,8 +664,8 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const uint32_t cb = kColB + buf * kColBuf;
             if (lane == 0) TC_TRACE(c, 8);
             // the tile's header and its front MMAs (a missing result times out)
-            const bool okw = mbar_wait(&bar_prep[st], ph, kWaitNs) &&
-                             mbar_wait(&bar_x[buf], (uint32_t)(c >> 1) & 1u, kWaitNs);
+            const bool okw = mbar_wait(&bar_prep[st], ph, args.wait_ns) &&
+                             mbar_wait(&bar_x[buf], (uint32_t)(c >> 1) & 1u, args.wait_ns);
             if (!__all_sync(kFull, okw)) {
                 if (lane == 0) set_status(args.status, GDR_ERR_TIMEOUT);
                 *abort_state = 1;
@@ -726,7 +733,7 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         // drain: the last tile's output, then the final state
         bool ok = done == nch;
-        if (ok && nch > 0) ok = __all_sync(kFull, mbar_wait(&bar_h[0], 0, kWaitNs));
+        if (ok && nch > 0) ok = __all_sync(kFull, mbar_wait(&bar_h[0], 0, args.wait_ns));
         ok = __all_sync(kFull, ok && *abort_state == 0);
         tc_fence_after();
         if (ok && use_q && nch > 0) {
@@ -755,21 +762,72 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
 // ---------------------------------------------------------------------------
 // transition truncation: for each non-last segment, the first tile r such that
-// the accumulated log-decay from the start of tile r to the segment's end is at
-// most -kTruncLog.  Everything that enters the recurrence before tile r reaches
-// the segment's end attenuated by at least exp(-kTruncLog) = 2^-64 (the state
-// norm bound: each step contracts by its decay), so the segment's offset B is
-// computed from a zero state at r, and its transition matrix M, whose norm is
-// bounded by the same product of decays, is taken as zero.  When no such r
-// exists the full transition is computed.
+// the bound on the state transition from the start of tile r to the segment's
+// end is at most exp(-kTruncLog) = 2^-64.  One token multiplies the state by
+// Phi_t = alpha_t (I - beta_t k_t k_t^T), whose norm is
+// alpha_t max(1, |1 - beta_t |k_t|^2|) (the erase factor's eigenvalues are 1
+// and 1 - beta |k|^2), so the log of the bound over a tile is its summed
+// log-decay plus the tokens' log max(1, |1 - beta |k|^2|).  Everything that
+// enters the recurrence before tile r then reaches the segment's end
+// attenuated by at least 2^-64 relative to the state at tile r, so the
+// segment's offset B is computed from a zero state at r and its transition
+// matrix M is taken as zero.  When no such r exists the full transition is
+// computed.  [P3 §3.1-3.2: the state passed from chunk to chunk]
+//
+// One warp per (segment, head), walking back from the segment's end 32 tiles
+// at a time (lane j takes the j-th tile back; a warp scan accumulates).  The
+// decay alone gives a weaker bound (erase factors are >= 1), so a first walk
+// over G only finds whether the horizon can fall inside the segment at all;
+// only then are the tiles' keys read, and only back to that horizon or past it.
 // ---------------------------------------------------------------------------
 constexpr float kTruncLog = 44.3614195558365f;   // 64 ln 2
 
+// Inclusive scan of x over the lanes of a warp.
+__device__ __forceinline__ float warp_scan(float x, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    return x;
+}
+
+// log of the norm bound of one tile's transition: its summed log-decay, plus
+// (with_erase) the log erase-factor norm of each of its tokens.
+__device__ __forceinline__ float tile_log_bound(const float *G, const float *Bt,
+                                                const __nv_bfloat16 *k, const SegInfo &si,
+                                                int64_t c, int h, int H, int64_t T_total,
+                                                bool with_erase) {
+    const int len = (int)min((int64_t)kC, si.len - c * kC);
+    const int64_t row0 = si.tok0 + c * kC;
+    float lb = G[(int64_t)h * T_total + row0 + len - 1];
+    if (with_erase) {
+        for (int i = 0; i < len; ++i) {
+            const uint4 *kp = (const uint4 *)(k + ((row0 + i) * H + h) * kD);
+            float kk = 0.f;
+#pragma unroll
+            for (int u = 0; u < kD / 8; ++u) {
+                const uint4 w = kp[u];
+                const __nv_bfloat162 *p2 = (const __nv_bfloat162 *)&w;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const float2 f = __bfloat1622float2(p2[m]);
+                    kk = fmaf(f.x, f.x, fmaf(f.y, f.y, kk));
+                }
+            }
+            const float e = fabsf(1.f - Bt[(int64_t)h * T_total + row0 + i] * kk);
+            if (e > 1.f) lb += logf(e);
+        }
+    }
+    return lb;
+}
+
 __global__ void __launch_bounds__(128)
-tc_horizon_kernel(const float *G, Plan p, int H, int64_t T_total, int64_t nslots, int *first,
-                  int *mneed, int truncate) {
-    const int64_t slot = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (slot >= nslots) return;
+tc_horizon_kernel(const float *G, const float *Bt, const __nv_bfloat16 *k, Plan p, int H,
+                  int64_t T_total, int64_t nslots, int *first, int *mneed, int truncate) {
+    const int64_t slot = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (slot >= nslots) return;   // warp-uniform
     const int64_t gseg = slot / H;
     const int h = (int)(slot % H);
     SegInfo si;
@@ -777,19 +835,34 @@ tc_horizon_kernel(const float *G, Plan p, int H, int64_t T_total, int64_t nslots
     int r = (int)si.c0;
     int need = 1;
     if (truncate) {
-        float acc = 0.f;
-        for (int64_t c = si.c1 - 1; c >= si.c0; --c) {
-            const int64_t last = min((int64_t)kC, si.len - c * kC) - 1;
-            acc += G[(int64_t)h * T_total + si.tok0 + c * kC + last];
-            if (acc <= -kTruncLog) {
-                r = (int)c;
-                need = 0;
-                break;
+        // pass 0: decay only (is there a horizon inside the segment at all?);
+        // pass 1: with the erase factors (its horizon lies at or before pass 0's)
+        for (int pass = 0; pass < 2 && need; ++pass) {
+            float acc = 0.f;
+            bool found = false;
+            for (int64_t cs = si.c1 - 1; cs >= si.c0 && !found; cs -= 32) {
+                const int64_t c = cs - lane;
+                const bool valid = c >= si.c0;
+                const float lb = valid ? tile_log_bound(G, Bt, k, si, c, h, H, T_total, pass == 1) : 0.f;
+                const float run = acc + warp_scan(lb, lane);
+                const unsigned hit = __ballot_sync(0xffffffffu, valid && run <= -kTruncLog);
+                if (hit) {
+                    const int j = __ffs(hit) - 1;
+                    found = true;
+                    if (pass == 1) {
+                        r = (int)(cs - j);
+                        need = 0;
+                    }
+                }
+                acc = __shfl_sync(0xffffffffu, run, 31);
             }
+            if (!found) break;   // no horizon inside the segment: full transition
         }
     }
-    first[slot] = r;
-    mneed[slot] = need;
+    if (lane == 0) {
+        first[slot] = r;
+        mneed[slot] = need;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -967,11 +1040,16 @@ cudaError_t launch_tc_forward(const void *q, const void *k, const void *v, const
     a.status = status;
     const char *exact = std::getenv("GDR_TC_EXACT");
     const int truncate = (exact && std::atoi(exact) != 0) ? 0 : 1;
+    a.wait_ns = kWaitNs;
+    if (const char *w = std::getenv("GDR_TC_WAIT_NS")) {   // test hook: shorter pipeline waits
+        const long long v = std::atoll(w);
+        if (v > 0 && (uint64_t)v < kWaitNs) a.wait_ns = (uint64_t)v;
+    }
     {
         ProfScope prof(stream, "tc_horizon_kernel");
-        const int64_t nslots = nseg * H;
-        tc_horizon_kernel<<<(unsigned)((nslots + 127) / 128), 128, 0, stream>>>(
-            G, plan, H, T_total, nslots, first, mneed, truncate);
+        const int64_t nslots = nseg * H;   // one warp each
+        tc_horizon_kernel<<<(unsigned)((nslots + 3) / 4), 128, 0, stream>>>(
+            G, Bt, (const __nv_bfloat16 *)k, plan, H, T_total, nslots, first, mneed, truncate);
         count_launch();
     }
     cudaError_t err = cudaFuncSetAttribute(tc_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

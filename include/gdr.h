@@ -39,14 +39,15 @@
  *   beta is a probability (used as given, not passed through a sigmoid).
  *   q and k are used as given: no scaling, no normalisation.
  *
- * Precondition of the tensor-core path (GDR_PATH_TC, and GDR_PATH_AUTO where it
- * picks that path): 0 <= beta_t |k_t|^2 <= 2 for every token, e.g. unit-norm
- * keys with beta in [0, 1], as the layer produces them.  Then every erase
- * factor I - beta k k^T has norm <= 1, and the path's segment scan may drop
- * what enters a segment more than 64 ln 2 of accumulated log-decay before its
- * end (attenuated below 2^-64).  For other inputs set the environment variable
- * GDR_TC_EXACT=1 (no truncation) or use GDR_PATH_SIMT; the CUDA-core,
- * per-channel, decode and backward calls hold for any input.
+ * Segments of the tensor-core path.  A long sequence is cut into segments
+ * whose state transitions are computed in parallel and chained.  A transition
+ * skips what enters its segment so early that it reaches the segment's end
+ * attenuated below 2^-64 of the state: the bound multiplies, per token, the
+ * decay exp(g_t) by the erase factor's norm max(1, |1 - beta_t |k_t|^2|), so
+ * it holds for any keys and write strengths (with unit keys and beta in
+ * [0, 1] the erase factors are 1 and the decay alone sets it).  Where no such
+ * point lies inside a segment the full transition is used.  The environment
+ * variable GDR_TC_EXACT=1 turns the skipping off.
  *
  * Ownership and concurrency.  All tensor pointers of gdr_chunk_fwd* and of
  * the stage calls are DEVICE pointers owned by the caller; the library

@@ -68,6 +68,8 @@ def _call(**kw):
     (dict(out=1 << 20), gdr.GDR_ERR_INVALID_ARG),          # out aliases q
     (dict(hT=(5 << 20) + 8), gdr.GDR_ERR_INVALID_ARG),     # hT overlaps beta
     (dict(h0=7 << 20, hT=(7 << 20) + 4), gdr.GDR_ERR_INVALID_ARG),  # partial h0/hT overlap
+    (dict(q=1 << 52, k=2 << 52, v=3 << 52, a=4 << 52, beta=5 << 52, out=6 << 52, T=1 << 40,
+          H=1 << 22), gdr.GDR_ERR_UNSUPPORTED),                 # > 2^40 (token, head) rows
 ])
 def test_bad_arguments_are_rejected_before_launch(lib, kw, code):
     assert _call(**kw) == code
@@ -122,3 +124,45 @@ def test_backward_state_gradients_must_be_aligned(lib, which):
     rc = gdr.gdr_chunk_bwd(*ins, *outs, None, 1, 0, 2, 128, 128, 16, 2.0, gdr.GDR_BF16,
                            gdr.GDR_GATE_BOUNDED, 0)
     assert rc == gdr.GDR_ERR_INVALID_ARG
+
+
+def _noalloc(**kw):
+    base = dict(q=1 << 20, k=2 << 20, v=3 << 20, a=4 << 20, beta=5 << 20, h0=None, out=6 << 20,
+                hT=None, B=1, T=64, H=2, dk=128, dv=128, chunk=16, b=2.0, dtype=gdr.GDR_BF16,
+                gate=gdr.GDR_GATE_BOUNDED, stream=0)
+    base.update(kw)
+    return gdr.gdr_chunk_fwd_noalloc(*base.values())
+
+
+# fake addresses 2^52 apart, so that large sizes do not make the buffers overlap
+_FAR = dict(q=1 << 52, k=2 << 52, v=3 << 52, a=4 << 52, beta=5 << 52, out=6 << 52)
+
+
+@pytest.mark.parametrize("kw,code", [
+    # sizes whose scratch exceeds the static array
+    (dict(_FAR, T=1 << 20, H=16), gdr.GDR_ERR_NO_WORKSPACE),
+    (dict(_FAR, T=1 << 20, H=1 << 20), gdr.GDR_ERR_NO_WORKSPACE),
+    (dict(_FAR, B=1 << 20, T=1 << 20, H=1), gdr.GDR_ERR_NO_WORKSPACE),
+    # more than 2^40 (token, head) rows, whose byte counts would wrap 64 bits
+    # (2^40 tokens x 2^22 heads): refused as by the regular entry point
+    (dict(_FAR, T=1 << 40, H=1 << 22), gdr.GDR_ERR_UNSUPPORTED),
+    (dict(_FAR, B=1 << 20, T=1 << 20, H=1 << 30), gdr.GDR_ERR_UNSUPPORTED),
+    (dict(B=1 << 30, T=0), gdr.GDR_ERR_NO_WORKSPACE),
+    # the regular entry point's refusals, reached the same way
+    (dict(T=(1 << 40) + 1), gdr.GDR_ERR_UNSUPPORTED),
+    (dict(out=1 << 20), gdr.GDR_ERR_INVALID_ARG),                   # out aliases q
+    (dict(hT=(5 << 20) + 8), gdr.GDR_ERR_INVALID_ARG),              # hT overlaps beta
+    (dict(h0=7 << 20, hT=(7 << 20) + 4), gdr.GDR_ERR_INVALID_ARG),  # partial h0/hT overlap
+    (dict(b=float("inf")), gdr.GDR_ERR_INVALID_ARG),
+    (dict(chunk=8), gdr.GDR_ERR_UNSUPPORTED),
+    (dict(q=None), gdr.GDR_ERR_INVALID_ARG),
+])
+def test_noalloc_refuses_before_launch(lib, kw, code):
+    # fake addresses: every case is refused by the host checks, nothing is launched
+    assert _noalloc(**kw) == code
+
+
+def test_noalloc_refuses_what_the_regular_entry_point_refuses(lib):
+    for kw in (dict(out=1 << 20), dict(hT=(5 << 20) + 8), dict(h0=7 << 20, hT=(7 << 20) + 4),
+               dict(B=0), dict(dk=96), dict(b=float("nan"))):
+        assert _noalloc(**kw) == _call(**kw) != gdr.GDR_OK, kw

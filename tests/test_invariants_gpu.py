@@ -36,8 +36,11 @@ def test_chaining(path):
     assert_close(to64(torch.cat([o1, o2], 1)), to64(out), "bf16", "out")
     if path == "simt":   # same tiles, same fp32 operations on both sides of the split
         assert rel_l2(to64(h2), to64(hT)) < 1e-5
-    else:                # the segment split moves: equal within the bf16 tolerance
-        assert_close(to64(h2), to64(hT), "bf16", "hT")
+    else:
+        # the tensor-core path's segments move with the split, which changes only the
+        # rounding (bf16 operands of the tile products): measured 2.3e-3 on out and hT
+        assert rel_l2(to64(torch.cat([o1, o2], 1)), to64(out)) < 3e-3
+        assert rel_l2(to64(h2), to64(hT)) < 3e-3
 
 
 @pytest.mark.parametrize("path", _paths())
@@ -61,12 +64,10 @@ def test_varlen_equals_separate_calls(path):
         y = _slice(x, cu[n], cu[n + 1])
         y.update(cu_seqlens=None, B=1, N=1, h0=x["h0"][n:n + 1])
         o, h = run_gpu(y, path=path)
-        if path == "simt":
-            assert rel_l2(to64(o), to64(out[:, cu[n]:cu[n + 1]])) < 1e-5
-            assert rel_l2(to64(h), to64(hT[n:n + 1])) < 1e-5
-        else:
-            assert_close(to64(o), to64(out[:, cu[n]:cu[n + 1]]), "bf16", "out")
-            assert_close(to64(h), to64(hT[n:n + 1]), "bf16", "hT")
+        # both paths run the same tiles and segments either way (these sequences are
+        # shorter than a tensor-core segment): equal up to fp32 reordering
+        assert rel_l2(to64(o), to64(out[:, cu[n]:cu[n + 1]])) < 1e-5
+        assert rel_l2(to64(h), to64(hT[n:n + 1])) < 1e-5
 
 
 @pytest.mark.parametrize("path", _paths())

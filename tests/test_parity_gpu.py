@@ -290,3 +290,55 @@ def test_tc_varlen_softplus_segments(monkeypatch):
     out, hT = run_gpu(x, path="tc")
     assert_close(to64(out), ro, "bf16", "out")
     assert_close(to64(hT), rh, "bf16", "hT")
+
+
+# ---------------------------------------------------------------------------
+# the segment truncation with non-unit keys: the horizon carries each token's
+# erase-factor norm max(1, |1 - beta |k|^2|), so AUTO holds for any keys
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("a_mean", [0.0, -6.0])
+def test_auto_path_non_unit_keys_short_segments(monkeypatch, a_mean):
+    """Keys scaled to |k| = 1.5 with beta = sigmoid(N(0, 1)) in (0, 1), so beta |k|^2
+    reaches 2.25 (erase factors up to 1.25 in norm); 4-tile segments put every
+    sequence through the transition pass, the horizon and the combine."""
+    monkeypatch.setenv("GDR_TC_SEG_CHUNKS", "4")
+    w = WORKLOADS["b2_t4k"].with_(H=4, a_mean=a_mean, h0_std=0.05, seed=1010)
+    x = make_inputs(w, device="cuda", T=1000)
+    x["k"] = (x["k"].float() * 1.5).to(x["k"].dtype)
+    ro, rh = run_oracle(x)
+    out, hT = run_gpu(x, path="auto")
+    assert_close(to64(out), ro, "bf16", "out")
+    assert_close(to64(hT), rh, "bf16", "hT")
+
+
+def test_auto_path_expansive_aligned_keys(monkeypatch):
+    """Every key is sqrt(3) e_1 with beta = 1 (erase-factor norm 2) and the gate logits
+    sit near -0.59 (alpha about 0.49), so the state's e_1 row shrinks by only ~0.98
+    per token.  The decay alone would put the truncation horizon ~62 tokens before each
+    16-tile segment's end and drop a state still ~0.3 of its size (the fp64 restatement
+    of the scan shows an output error of 7.7 % that way); with the erase term no
+    transition may be truncated.  Checked bit for bit against the untruncated scan
+    (GDR_TC_EXACT=1), and against the oracle.  This input is badly conditioned for
+    bf16 operands: the e_1 row remembers ~1 / (1 - 0.98) = 50 tokens, so the bf16
+    rounding of each tile's delta values (2^-9 relative) accumulates to about
+    2^-9 sqrt(50) = 1.4e-2 of the state (measured 1.0e-2 on out, 1.4e-2 on hT).  The
+    oracle check therefore takes rel-L2 <= 3e-2, still well below the 7.7e-2 error a
+    decay-only horizon leaves; the outputs reach ~25, so no max-abs bound is used."""
+    monkeypatch.setenv("GDR_TC_SEG_CHUNKS", "16")
+    w = WORKLOADS["b2_t4k"].with_(B=1, H=2, h0_std=0.05, seed=1011)
+    T = 16 * 16 * 5
+    x = make_inputs(w, device="cuda", T=T)
+    g = torch.Generator(device="cuda").manual_seed(1012)
+    k = torch.zeros_like(x["k"])
+    k[..., 0] = 3.0 ** 0.5
+    x["k"] = k
+    x["beta"] = torch.ones_like(x["beta"])
+    x["a"] = (-0.59 + 0.02 * torch.randn(x["a"].shape, generator=g, device="cuda")).to(x["a"].dtype)
+    ro, rh = run_oracle(x)
+    out, hT = run_gpu(x, path="auto")
+    r_o = rel_l2(to64(out), ro)
+    r_h = rel_l2(to64(hT), rh)
+    assert r_o <= 3e-2 and r_h <= 3e-2, (r_o, r_h)
+    monkeypatch.setenv("GDR_TC_EXACT", "1")
+    out_x, hT_x = run_gpu(x, path="auto")
+    assert torch.equal(out, out_x) and torch.equal(hT, hT_x)   # nothing was truncated

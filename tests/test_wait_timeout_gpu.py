@@ -1,0 +1,55 @@
+"""Bounded device waits of the tensor-core forward, made to run out (GPU).
+
+Every wait in tc_chunk_kernel gives up after a limit (2 s), records
+GDR_ERR_TIMEOUT in the status word and unwinds: the CTA drains its tile copies
+and tensor-core operations and frees its tensor memory before it returns.  The
+test hook GDR_TC_WAIT_NS shortens the pipeline waits' limit so that they run
+out on a small case; the call must return, report the timeout, and leave the
+device usable: the next call at the default limit matches the oracle (it could
+not allocate tensor memory, or would read stale tiles, if the unwind had leaked
+either).  No fault, trap or endless loop is involved.
+"""
+import pytest
+import torch
+
+import chunked_gated_delta_07_gb300 as gdr
+from gdr_inputs import WORKLOADS, make_inputs
+from gpu_helpers import assert_close, run_gpu, run_oracle, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from chunked_gated_delta_07_gb300 import _build
+    _build.build()
+    torch.cuda.set_device(0)
+
+
+def _tc_available():
+    return gdr.gdr_chunk_fwd_workspace_size(1, 64, 1, 128, 128, 16, gdr.GDR_BF16,
+                                            gdr.GDR_PATH_TC) > 0
+
+
+@pytest.mark.parametrize("limit_ns", [1, 1500, 20000])
+def test_waits_that_run_out_report_a_timeout_and_unwind(monkeypatch, limit_ns):
+    if not _tc_available():
+        pytest.skip("tensor-core path unavailable")
+    w = WORKLOADS["b2_t4k"].with_(H=3, seed=1020)
+    x = make_inputs(w, device="cuda", T=600)
+    assert gdr.gdr_get_status() == gdr.GDR_OK
+    monkeypatch.setenv("GDR_TC_WAIT_NS", str(limit_ns))
+    monkeypatch.setenv("GDR_TC_SEG_CHUNKS", "8")   # transitions, combine and output passes
+    gdr.chunk_fwd(x["q"], x["k"], x["v"], x["a"], x["beta"], h0=x["h0"], chunk=16, b=w.b,
+                  path="tc")
+    st = gdr.gdr_get_status()   # synchronises: the call has returned
+    if limit_ns == 1:
+        assert st == gdr.GDR_ERR_TIMEOUT, gdr.gdr_status_string(st)
+    else:   # a longer limit may or may not run out, depending on where the waits fall
+        assert st in (gdr.GDR_OK, gdr.GDR_ERR_TIMEOUT), gdr.gdr_status_string(st)
+    monkeypatch.delenv("GDR_TC_WAIT_NS")
+    ro, rh = run_oracle(x)
+    for _ in range(2):
+        out, hT = run_gpu(x, path="tc")   # asserts a clean status
+        assert_close(to64(out), ro, "bf16", "out")
+        assert_close(to64(hT), rh, "bf16", "hT")
