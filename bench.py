@@ -164,11 +164,12 @@ def cpu_oracle_rate(x, w, budget_s, max_tokens):
                           gate=w.gate, nthreads=threads)
         return time.perf_counter() - t0
 
+    nseq = x["q"].shape[0]   # dense input: the prefix of every sequence
     n = 256
     dt = run(n)
-    n = int(min(max_tokens, max(256, n * budget_s / max(dt, 1e-6))))
+    n = int(min(max_tokens // nseq, x["q"].shape[1], max(256, n * budget_s / max(dt, 1e-6) / nseq)))
     dt = run(n)
-    return n / dt, n, threads, dt
+    return nseq * n / dt, nseq * n, threads, dt
 
 
 def _grow_to_budget(run, n_min, budget_s, n_max):
@@ -294,10 +295,13 @@ def bench_reference(args, w):
 
 def workload_config(w):
     shape = (f"varlen total={w.T}" if w.varlen else f"B={w.B} T={w.T}")
+    es = 2 if w.dtype == "bf16" else 4
+    in_bytes = w.T * (1 if w.varlen else w.B) * w.H * es * (2 * w.dk + w.dv + 2)
     return {"workload": f"{w.name}: {shape} H={w.H} dk={w.dk} dv={w.dv} chunk={w.chunk} "
                         f"{w.dtype} gate={w.gate} b={w.b}",
             "tokens_per_step": w.T * (1 if w.varlen else w.B), "heads": w.H,
-            "l2_policy": "inputs larger than L2 (no flush)"}
+            "l2_policy": ("inputs larger than L2 (no flush)" if in_bytes >= 2 * L2_BYTES else
+                          "L2 flushed between steps (each step timed alone)")}
 
 
 def parse_args(argv=None):
@@ -333,11 +337,27 @@ def parse_args(argv=None):
     return args
 
 
+def resolve_workload(name):
+    """A workload by name: the five named ones, h32_t64k_c{16,32,64}_b{2,8} (the chunk and
+    gate-bound sweep of the 32-head workload) and <name>_softplus (the unbounded gate)."""
+    from gdr_inputs import WORKLOADS, h32_variant, softplus_variant
+    if name in WORKLOADS:
+        return WORKLOADS[name]
+    if name.endswith("_softplus"):
+        return softplus_variant(resolve_workload(name[:-len("_softplus")]))
+    if name.startswith("h32_t64k_c"):
+        c, b = name[len("h32_t64k_c"):].split("_b")
+        return h32_variant(int(c), float(b))
+    raise SystemExit(f"unknown workload {name}")
+
+
+L2_BYTES = 129 * 2 ** 20
+
+
 def main(argv=None):
     args = parse_args(argv)
 
-    from gdr_inputs import WORKLOADS
-    w = WORKLOADS[args.workload]
+    w = resolve_workload(args.workload)
     if args.tokens > 0:
         w = w.with_(T=args.tokens)
     if args.impl == "reference":
@@ -395,23 +415,34 @@ def main(argv=None):
         raise gdr.GdrError(st, "device status after warm-up")
 
     # ---- timed region ----
+    # Inputs smaller than twice the L2 are timed step by step, with the L2 flushed
+    # (a buffer of twice its size written) between steps, outside the timed steps.
+    in_bytes = sum(t.numel() * t.element_size() for t in (x["q"], x["k"], x["v"], x["a"], x["beta"]))
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if in_bytes < 2 * L2_BYTES else None
     gdr.gdr_profile_read()           # drop anything recorded so far
     gdr.gdr_profile_enable(True)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps if flush is not None else 1)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         n_launch0 = gdr.gdr_launch_count()
-        ev0.record(stream)
-        for _ in range(args.steps):
-            step()
-        ev1.record(stream)
+        if flush is None:
+            evs[0][0].record(stream)
+            for _ in range(args.steps):
+                step()
+            evs[0][1].record(stream)
+        else:
+            for e0, e1 in evs:
+                flush.fill_(1.0)
+                e0.record(stream)
+                step()
+                e1.record(stream)
         torch.cuda.synchronize()
         n_launch = gdr.gdr_launch_count() - n_launch0
     gdr.gdr_profile_enable(False)
-    ms = ev0.elapsed_time(ev1)
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in evs)
     ms = max_over_ranks(ms, dist, dev)
     if dist:
         dist.barrier()
@@ -454,7 +485,7 @@ def main(argv=None):
     if not args.no_cpu and rank == 0 and ws == 1:
         rate, ntok, threads, secs = cpu_oracle_rate(x, w, args.cpu_budget, n_tokens)
         cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"first {ntok} tokens x {H} heads of workload {w.name}, fp64 oracle, "
+               "sample": f"first {ntok // x['q'].shape[0]} tokens of each of {x['q'].shape[0]} sequence(s) x {H} heads of workload {w.name}, fp64 oracle, "
                          f"{secs:.1f} s"}
 
     if rank == 0:

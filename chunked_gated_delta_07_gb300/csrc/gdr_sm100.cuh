@@ -48,10 +48,24 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
     return t;
 }
+// Non-blocking: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Waits for the phase with the given parity to complete.  Gives up after
 // `limit_ns` of wall time and returns false (the caller records a timeout
-// and unwinds); never spins forever.
+// and unwinds); never spins forever.  (try_wait may itself suspend the thread
+// for a while before it reports an incomplete phase.)  A limit of 0 only looks
+// once, without suspending: a test hook that makes any wait not already
+// satisfied run out.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+    if (limit_ns == 0) return mbar_test_wait(bar, parity);
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
@@ -77,6 +91,12 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
         "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
+}
+// Bring a 3-D tile of a tensor into L2 ahead of its load (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"((uint64_t)map),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
 }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
@@ -137,6 +157,40 @@ __device__ __forceinline__ void mma_tf32_ts(uint32_t d, uint32_t a, uint64_t b, 
         " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p; }" ::"r"(d),
         "r"(a), "l"(b), "r"(idesc), "r"(accum)
         : "memory");
+}
+// D[tmem] = A[tmem] * B[smem] + 2^-S * D[tmem] (kind::tf32; S in [0, 15] is an
+// immediate of the instruction: the accumulator is scaled by an exact power of two
+// as it is read).
+template <int S>
+__device__ __forceinline__ void mma_tf32_ts_scale(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc) {
+    static_assert(S >= 0 && S <= 15, "scale-input-d range");
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, 1, 0;"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p, %4; }" ::"r"(d),
+        "r"(a), "l"(b), "r"(idesc), "n"(S)
+        : "memory");
+}
+// The same with a run-time S in [0, 15] (one branch per value).
+__device__ __forceinline__ void mma_tf32_ts_scaled(uint32_t d, uint32_t a, uint64_t b,
+                                                   uint32_t idesc, int s) {
+    switch (s) {
+        case 0: mma_tf32_ts_scale<0>(d, a, b, idesc); break;
+        case 1: mma_tf32_ts_scale<1>(d, a, b, idesc); break;
+        case 2: mma_tf32_ts_scale<2>(d, a, b, idesc); break;
+        case 3: mma_tf32_ts_scale<3>(d, a, b, idesc); break;
+        case 4: mma_tf32_ts_scale<4>(d, a, b, idesc); break;
+        case 5: mma_tf32_ts_scale<5>(d, a, b, idesc); break;
+        case 6: mma_tf32_ts_scale<6>(d, a, b, idesc); break;
+        case 7: mma_tf32_ts_scale<7>(d, a, b, idesc); break;
+        case 8: mma_tf32_ts_scale<8>(d, a, b, idesc); break;
+        case 9: mma_tf32_ts_scale<9>(d, a, b, idesc); break;
+        case 10: mma_tf32_ts_scale<10>(d, a, b, idesc); break;
+        case 11: mma_tf32_ts_scale<11>(d, a, b, idesc); break;
+        case 12: mma_tf32_ts_scale<12>(d, a, b, idesc); break;
+        case 13: mma_tf32_ts_scale<13>(d, a, b, idesc); break;
+        case 14: mma_tf32_ts_scale<14>(d, a, b, idesc); break;
+        default: mma_tf32_ts_scale<15>(d, a, b, idesc); break;
+    }
 }
 // True in exactly one lane of a converged warp (the warp stays converged around it).
 __device__ __forceinline__ bool elect_one() {

@@ -1042,8 +1042,8 @@ cudaError_t launch_tc_forward(const void *q, const void *k, const void *v, const
     const int truncate = (exact && std::atoi(exact) != 0) ? 0 : 1;
     a.wait_ns = kWaitNs;
     if (const char *w = std::getenv("GDR_TC_WAIT_NS")) {   // test hook: shorter pipeline waits
-        const long long v = std::atoll(w);
-        if (v > 0 && (uint64_t)v < kWaitNs) a.wait_ns = (uint64_t)v;
+        const long long v = std::atoll(w);                  // (0: look once, never wait)
+        if (v >= 0 && (uint64_t)v < kWaitNs) a.wait_ns = (uint64_t)v;
     }
     {
         ProfScope prof(stream, "tc_horizon_kernel");
