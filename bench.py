@@ -624,6 +624,21 @@ def bench_backward(args):
     _, bf16_tf, _, peak_src = peaks()
     peak = bf16_tf / 2.0
     achieved = flops / (ms / 1e3) / 1e12
+    # bytes: per (token, head) the inputs q, k, v, dout and a, beta, the gradients dq, dk, dv,
+    # da, dbeta (a and da carry dk entries with the per-channel gate); per (sequence, head)
+    # h0, dhT and dh0.  The chunked form also writes and reads back, per (16-token tile,
+    # head), the entering state and the end gradient (bf16) and the tile's delta (fp32):
+    # scratch, not algorithmic, reported beside it.
+    hbm, _, _, _ = peaks()
+    ga = 2 * d if vec else 2
+    alg_bytes = (2 * (3 * d + d) + ga + 2 + 2 * 3 * d + ga + 2) * N * T * H + 3 * 4 * d * d * N * H
+    tiles = N * ((T + 15) // 16)
+    scratch_bytes = 2 * tiles * H * (2 * 2 * d * d + 4 * 16 * d)
+    bytes_roof = {"bound": "hbm", "algorithmic_bytes": alg_bytes, "scratch_bytes": scratch_bytes,
+                  "achieved": alg_bytes / (ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                  "frac": alg_bytes / (ms / 1e3) / 1e9 / hbm,
+                  "frac_with_scratch": (alg_bytes + scratch_bytes) / (ms / 1e3) / 1e9 / hbm,
+                  "t_hbm_ms_with_scratch": (alg_bytes + scratch_bytes) / (hbm * 1e9) * 1e3}
     cpu = None if args.no_cpu else _cpu_line(*cpu_rate_bwd(x, dout, dhT, 2.0, vec, args.cpu_budget),
                                              "sequence 0, its first tokens x 16 heads, with dout and dhT")
     print(json.dumps({
@@ -639,6 +654,7 @@ def bench_backward(args):
                      "peak_source": f"{peak_src} bf16_tflops x 0.5 (tf32)",
                      "algorithmic_flops_per_step": flops, "dominant_kernel": dom_name,
                      "dominant_share": dom_ms / sum(v[0] for v in prof.values()) if prof else None},
+        "roofline_bytes": bytes_roof,
         "kernels": {k: {"ms_total": v[0], "launches": v[1]} for k, v in prof.items()},
         "cpu_baseline": cpu, "gpu_launches": n_launch, "clocks": summ or None,
     }), flush=True)

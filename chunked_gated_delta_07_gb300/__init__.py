@@ -17,10 +17,11 @@ import os
 import threading
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libgdr.so")
+# GDR_LIB selects another build of the library (the checking builds of _build.py)
+LIB_PATH = os.environ.get("GDR_LIB") or os.path.join(HERE, "libgdr.so")
 
 GDR_OK, GDR_ERR_INVALID_ARG, GDR_ERR_UNSUPPORTED, GDR_ERR_CUDA = 0, 1, 2, 3
-GDR_ERR_TIMEOUT, GDR_ERR_NO_WORKSPACE, GDR_ERR_BAD_SEQLENS = 4, 5, 6
+GDR_ERR_TIMEOUT, GDR_ERR_NO_WORKSPACE, GDR_ERR_BAD_SEQLENS, GDR_ERR_BOUNDS = 4, 5, 6, 7
 GDR_BF16, GDR_F32 = 0, 1
 GDR_GATE_BOUNDED, GDR_GATE_SOFTPLUS = 0, 1
 GDR_PATH_AUTO, GDR_PATH_SIMT, GDR_PATH_TC = 0, 1, 2

@@ -34,17 +34,42 @@ def _headers():
     return glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def build(verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+# Checking builds, each into its own directory and library:
+#   debug: device-side index checks (GDR_DEBUG); a failed one is reported by
+#          gdr_get_status as GDR_ERR_BOUNDS instead of touching memory
+#   asan:  the host code under AddressSanitizer and UndefinedBehaviorSanitizer (load
+#          it in a process that preloads the sanitizer runtimes)
+VARIANTS = {
+    "debug": ["-DGDR_DEBUG"],
+    "asan": ["-Xcompiler", "-fsanitize=address", "-Xcompiler", "-fsanitize=undefined",
+             "-Xcompiler", "-fno-omit-frame-pointer", "-Xcompiler", "-fno-sanitize-recover=undefined", "-g"],
+}
+
+
+def variant_lib(variant: str) -> str:
+    return os.path.join(HERE, f"libgdr_{variant}.so")
+
+
+def build(verbose: bool = False, extra_flags: list[str] | None = None,
+          variant: str | None = None) -> str:
+    if variant is not None:
+        return _build_into(os.path.join(ROOT, "_build", f"gdr_{variant}"), variant_lib(variant),
+                           VARIANTS[variant], ["-Xcompiler", "-fsanitize=address", "-Xcompiler", "-fsanitize=undefined"]
+                           if variant == "asan" else [], verbose)
+    return _build_into(BUILD, LIB, list(extra_flags or []), [], verbose, force=bool(extra_flags))
+
+
+def _build_into(build_dir, lib, extra, link_extra, verbose, force=False):
+    os.makedirs(build_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     hdr_mtime = max([os.path.getmtime(h) for h in _headers()] + [0.0])
-    flags = NVCC_FLAGS + ARCH + list(extra_flags or [])
+    flags = NVCC_FLAGS + ARCH + extra
     procs, objs = [], []
     for src in srcs:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if (os.path.exists(obj) and os.path.getmtime(obj) >= os.path.getmtime(src)
-                and os.path.getmtime(obj) >= hdr_mtime and not extra_flags):
+                and os.path.getmtime(obj) >= hdr_mtime and not force):
             continue
         cmd = [nvcc(), "-c", src, "-o", obj] + flags
         if verbose:
@@ -60,15 +85,15 @@ def build(verbose: bool = False, extra_flags: list[str] | None = None) -> str:
     if failed:
         msg = "\n".join(f"--- {s}\n{o}" for s, o in failed)
         raise RuntimeError(f"nvcc failed:\n{msg}")
-    if (procs or not os.path.exists(LIB)
-            or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs)):
-        tmp = LIB + f".tmp{os.getpid()}"
-        cmd = [nvcc(), "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static"]
+    if (procs or not os.path.exists(lib)
+            or os.path.getmtime(lib) < max(os.path.getmtime(o) for o in objs)):
+        tmp = lib + f".tmp{os.getpid()}"
+        cmd = [nvcc(), "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static"] + link_extra
         if verbose:
             print(" ".join(cmd), flush=True)
         subprocess.run(cmd, check=True)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

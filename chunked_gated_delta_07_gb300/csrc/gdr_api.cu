@@ -17,6 +17,24 @@ namespace gdr {
 static std::atomic<uint64_t> g_launches{0};
 void count_launch(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
+#ifdef GDR_DEBUG
+namespace {
+std::vector<DebugFlagReader> &debug_readers() {
+    static std::vector<DebugFlagReader> v;
+    return v;
+}
+std::mutex &debug_mu() {
+    static std::mutex m;
+    return m;
+}
+}  // namespace
+bool register_debug_flag(DebugFlagReader fn) {
+    std::lock_guard<std::mutex> lk(debug_mu());
+    debug_readers().push_back(fn);
+    return true;
+}
+#endif
+
 // ---- per-kernel event timing ------------------------------------------------
 namespace {
 struct ProfRec {
@@ -143,7 +161,7 @@ Layout layout_for(const Shape &s, gdr_path_t path) {
         L.Bt = off;
         off += align_up(sizeof(float) * (size_t)s.H * s.T_total);
         L.tc = off;
-        off += align_up(tc_workspace_bytes(s.N, s.H, s.T_total, s.C));
+        off += align_up(tc_workspace_bytes(s.N, s.H, s.T_total, s.C, s.varlen));
     } else {
         L.W = off;
         off += align_up(sizeof(float) * (size_t)s.T_total * s.H * s.dk);
@@ -236,7 +254,7 @@ gdr_status_t run_forward(const void *q, const void *k, const void *v, const void
     int64_t *chunk_base = seq_start + (s.N + 1);
     int64_t *seg_base = chunk_base + (s.N + 1);
     float *G = (float *)(ws + L.G);
-    const int seg_chunks = path == GDR_PATH_TC ? tc_segment_chunks(s.N, s.H, s.T_total, s.C) : (1 << 30);
+    const int seg_chunks = path == GDR_PATH_TC ? tc_segment_chunks(s.N, s.H, s.T_total, s.C, s.varlen) : (1 << 30);
     Plan plan{s.N, s.C, seg_chunks, seq_start, chunk_base, seg_base};
 
     cudaError_t err = launch_plan(cu, s.N, s.T_per, s.T_total, s.C, seg_chunks, seq_start,
@@ -890,6 +908,13 @@ gdr_status_t gdr_get_status(gdr_stream_t stream) {
     if (cudaMemcpy(&code, ctx->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
         return GDR_ERR_CUDA;
     if (code != 0 && cudaMemset(ctx->d_status, 0, sizeof(int)) != cudaSuccess) return GDR_ERR_CUDA;
+#ifdef GDR_DEBUG
+    {
+        std::lock_guard<std::mutex> lk(debug_mu());
+        for (DebugFlagReader fn : debug_readers())
+            if (fn() && code == 0) code = GDR_ERR_BOUNDS;
+    }
+#endif
     return (gdr_status_t)code;
 }
 
@@ -902,6 +927,7 @@ const char *gdr_status_string(gdr_status_t status) {
         case GDR_ERR_TIMEOUT: return "device-side wait timed out";
         case GDR_ERR_NO_WORKSPACE: return "workspace too small";
         case GDR_ERR_BAD_SEQLENS: return "cu_seqlens is not a valid offset list";
+        case GDR_ERR_BOUNDS: return "device-side index check failed (checking build)";
     }
     return "unknown status";
 }

@@ -31,6 +31,31 @@ struct Plan {
 // Device status word codes (a subset of gdr_status_t).
 constexpr int kStatusOk = 0;
 
+// Checking build (-DGDR_DEBUG).  Each translation unit with kernels that check their
+// indexes declares GDR_DEBUG_TU() once at namespace scope: a failed GDR_INBOUNDS(cond)
+// sets that unit's device flag and the caller skips the access; gdr_get_status reads
+// and clears every unit's flag and reports GDR_ERR_BOUNDS.  In regular builds both
+// macros compile to nothing.
+#ifdef GDR_DEBUG
+using DebugFlagReader = int (*)();
+bool register_debug_flag(DebugFlagReader fn);
+#define GDR_DEBUG_TU()                                                                  \
+    namespace {                                                                         \
+    __device__ int g_debug_flag = 0;                                                    \
+    int read_debug_flag() {                                                             \
+        int v = 0, z = 0;                                                               \
+        if (cudaMemcpyFromSymbol(&v, g_debug_flag, sizeof(int)) != cudaSuccess) return 0; \
+        if (v) cudaMemcpyToSymbol(g_debug_flag, &z, sizeof(int));                       \
+        return v;                                                                       \
+    }                                                                                   \
+    [[maybe_unused]] const bool g_debug_registered = register_debug_flag(&read_debug_flag); \
+    }
+#define GDR_INBOUNDS(cond) ((cond) ? true : (atomicExch(&g_debug_flag, 1), false))
+#else
+#define GDR_DEBUG_TU()
+#define GDR_INBOUNDS(cond) true
+#endif
+
 // First error wins; later ones are dropped.
 __device__ __forceinline__ void set_status(int *status, int code) {
     if (status) atomicCAS(status, 0, code);

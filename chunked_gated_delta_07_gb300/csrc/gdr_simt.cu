@@ -18,6 +18,8 @@
 
 namespace gdr {
 
+GDR_DEBUG_TU()
+
 // ---------------------------------------------------------------------------
 // plan: sequence starts, tile bases and segment bases (exclusive prefix sums)
 // ---------------------------------------------------------------------------
@@ -151,8 +153,11 @@ gate_cumsum_kernel(const T *__restrict__ a, const T *__restrict__ beta, float *_
         for (int r = 0; r < kRows; ++r) {
             const int t = warp + 8 * r;
             const int64_t src = (Tb + min(t, ntok - 1)) * H + h0 + lane;
-            av[r] = to_f32(a[src]);
-            bv[r] = Bt ? to_f32(beta[src]) : 0.f;
+            av[r] = bv[r] = 0.f;
+            if (GDR_INBOUNDS(Tb + min(t, ntok - 1) < T_total && h0 + lane < H)) {
+                av[r] = to_f32(a[src]);
+                bv[r] = Bt ? to_f32(beta[src]) : 0.f;
+            }
         }
 #pragma unroll
         for (int r = 0; r < kRows; ++r) {
@@ -179,6 +184,7 @@ gate_cumsum_kernel(const T *__restrict__ a, const T *__restrict__ beta, float *_
     for (int hh = warp; hh < nh; hh += 8) {   // warp per head row, lane per token
         const int64_t dst = (int64_t)(h0 + hh) * T_total + Tb;
         for (int t = lane; t < ntok; t += 32) {
+            if (!GDR_INBOUNDS(Tb + t < T_total)) continue;
             G[dst + t] = sg[hh * ld + t];
             if (Bt) Bt[dst + t] = sb[hh * ld + t];
         }
@@ -225,6 +231,7 @@ wy_simt_kernel(const T *__restrict__ k, const T *__restrict__ v, const T *__rest
     if (n < 0) return;
     const int64_t t0 = p.seq_start[n] + (c - p.chunk_base[n]) * C;
     const int len = (int)min((int64_t)C, p.seq_start[n + 1] - t0);
+    if (!GDR_INBOUNDS(h < H && t0 >= 0 && t0 + len <= T_total)) return;
     float *Ks = sm;                  // [C][dk]
     float *Vs = Ks + C * dk;         // [C][dv]
     float *A = Vs + C * dv;          // [C][C+1]
@@ -346,12 +353,14 @@ state_out_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
     float *eG = Gs + C;                  // exp(G_i)
     float *eR = eG + C;                  // exp(G_C - G_i)
 
+    if (!GDR_INBOUNDS(n < p.N)) return;
     const size_t hbase = ((size_t)n * H + h) * dk * dv;
     for (int e = tid; e < dk * kSimtCols; e += 256) {
         const int d = e / kSimtCols, j = e % kSimtCols;
         Hs[e] = h0 ? h0[hbase + (size_t)d * dv + j0 + j] : 0.f;
     }
     const int64_t s = p.seq_start[n], e_end = p.seq_start[n + 1];
+    if (!GDR_INBOUNDS(s >= 0 && e_end <= T_total)) return;
     for (int64_t t0 = s; t0 < e_end; t0 += C) {
         const int len = (int)min((int64_t)C, e_end - t0);
         __syncthreads();  // previous tile done with Ws/Ks/Qs/Ds/P

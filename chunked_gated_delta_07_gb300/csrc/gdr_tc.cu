@@ -35,6 +35,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
 #include <mutex>
 
@@ -42,6 +43,9 @@
 #include "gdr_tc.cuh"
 
 namespace gdr {
+
+GDR_DEBUG_TU()
+
 namespace {
 
 using namespace sm100;
@@ -258,6 +262,11 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const bool use_v = mode != kModeM, use_q = mode == kModeOut;
     const int nch = (int)(si.c1 - si.c0);
     constexpr unsigned kFull = 0xffffffffu;
+    // (checking build) the segment's tokens and its sequence lie inside the tensors; a
+    // failed check leaves the CTA's work undone (block-uniform, before any barrier)
+    if (!GDR_INBOUNDS(si.n < args.plan.N && h < H && si.tok0 >= 0 && si.tok0 + si.len <= args.T_total &&
+                      si.c0 >= 0 && si.c1 * kC <= si.len + kC - 1))
+        return;
 
     if (tid == 0) {
         for (int i = 0; i < kNS; ++i) {
@@ -313,7 +322,7 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const int len = (int)min((int64_t)kC, si.len - tc * kC);
             // gates of the tile (issued before the waits)
             float g_i = 0.f, b_i = 0.f;
-            if (lane < kC) {
+            if (lane < kC && GDR_INBOUNDS(t0 >= 0 && t0 + len <= args.T_total && len >= 1)) {
                 const int i = min(lane, len - 1);
                 g_i = args.G[(int64_t)h * args.T_total + t0 + i];
                 b_i = lane < len ? args.Bt[(int64_t)h * args.T_total + t0 + lane] : 0.f;
@@ -640,6 +649,7 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // warp writes 64 contiguous bytes.
         const int64_t orow = (int64_t)H * kD;   // elements between token rows
         auto store_out = [&](const uint32_t (&o)[kC], int len, int64_t t0, float scale) {
+            if (!GDR_INBOUNDS(t0 >= 0 && t0 + len <= args.T_total)) return;
             __nv_bfloat16 *out = (__nv_bfloat16 *)args.out + (t0 * H + h) * kD + e;
             if (len == kC) {
 #pragma unroll
@@ -774,11 +784,13 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 // matrix M is taken as zero.  When no such r exists the full transition is
 // computed.  [P3 §3.1-3.2: the state passed from chunk to chunk]
 //
-// One warp per (segment, head), walking back from the segment's end 32 tiles
-// at a time (lane j takes the j-th tile back; a warp scan accumulates).  The
-// decay alone gives a weaker bound (erase factors are >= 1), so a first walk
-// over G only finds whether the horizon can fall inside the segment at all;
-// only then are the tiles' keys read, and only back to that horizon or past it.
+// One warp per (segment, head), walking back from the segment's end.  The decay
+// alone gives a weaker bound (erase factors are >= 1), so a first walk over G
+// (32 tiles per step) finds whether the horizon can fall inside the segment at
+// all, and where; only then are keys read, from the segment's end back to that
+// horizon or a little past it (two tiles per step, a lane per token).  A walk that
+// does not cross within a few times the first horizon's distance gives up and the
+// full transition is used, which is always exact.
 // ---------------------------------------------------------------------------
 constexpr float kTruncLog = 44.3614195558365f;   // 64 ln 2
 
@@ -792,34 +804,13 @@ __device__ __forceinline__ float warp_scan(float x, int lane) {
     return x;
 }
 
-// log of the norm bound of one tile's transition: its summed log-decay, plus
-// (with_erase) the log erase-factor norm of each of its tokens.
-__device__ __forceinline__ float tile_log_bound(const float *G, const float *Bt,
-                                                const __nv_bfloat16 *k, const SegInfo &si,
-                                                int64_t c, int h, int H, int64_t T_total,
-                                                bool with_erase) {
+// log of the decay of one tile (its summed log-decay, the last in-tile cumsum)
+__device__ __forceinline__ float tile_log_decay(const float *G, const SegInfo &si, int64_t c, int h,
+                                                int64_t T_total) {
     const int len = (int)min((int64_t)kC, si.len - c * kC);
     const int64_t row0 = si.tok0 + c * kC;
-    float lb = G[(int64_t)h * T_total + row0 + len - 1];
-    if (with_erase) {
-        for (int i = 0; i < len; ++i) {
-            const uint4 *kp = (const uint4 *)(k + ((row0 + i) * H + h) * kD);
-            float kk = 0.f;
-#pragma unroll
-            for (int u = 0; u < kD / 8; ++u) {
-                const uint4 w = kp[u];
-                const __nv_bfloat162 *p2 = (const __nv_bfloat162 *)&w;
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const float2 f = __bfloat1622float2(p2[m]);
-                    kk = fmaf(f.x, f.x, fmaf(f.y, f.y, kk));
-                }
-            }
-            const float e = fabsf(1.f - Bt[(int64_t)h * T_total + row0 + i] * kk);
-            if (e > 1.f) lb += logf(e);
-        }
-    }
-    return lb;
+    if (!GDR_INBOUNDS(len >= 1 && row0 >= 0 && row0 + len <= T_total)) return 0.f;
+    return G[(int64_t)h * T_total + row0 + len - 1];
 }
 
 __global__ void __launch_bounds__(128)
@@ -827,6 +818,7 @@ tc_horizon_kernel(const float *G, const float *Bt, const __nv_bfloat16 *k, Plan 
                   int64_t T_total, int64_t nslots, int *first, int *mneed, int truncate) {
     const int64_t slot = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
+    constexpr unsigned kFull = 0xffffffffu;
     if (slot >= nslots) return;   // warp-uniform
     const int64_t gseg = slot / H;
     const int h = (int)(slot % H);
@@ -835,28 +827,67 @@ tc_horizon_kernel(const float *G, const float *Bt, const __nv_bfloat16 *k, Plan 
     int r = (int)si.c0;
     int need = 1;
     if (truncate) {
-        // pass 0: decay only (is there a horizon inside the segment at all?);
-        // pass 1: with the erase factors (its horizon lies at or before pass 0's)
-        for (int pass = 0; pass < 2 && need; ++pass) {
+        // pass 0, the decay alone, 32 tiles per step (lane j: the j-th tile back): is
+        // there a horizon inside the segment at all, and where (r0)?
+        int64_t r0 = -1;
+        {
             float acc = 0.f;
-            bool found = false;
-            for (int64_t cs = si.c1 - 1; cs >= si.c0 && !found; cs -= 32) {
+            for (int64_t cs = si.c1 - 1; cs >= si.c0 && r0 < 0; cs -= 32) {
                 const int64_t c = cs - lane;
                 const bool valid = c >= si.c0;
-                const float lb = valid ? tile_log_bound(G, Bt, k, si, c, h, H, T_total, pass == 1) : 0.f;
-                const float run = acc + warp_scan(lb, lane);
-                const unsigned hit = __ballot_sync(0xffffffffu, valid && run <= -kTruncLog);
-                if (hit) {
-                    const int j = __ffs(hit) - 1;
-                    found = true;
-                    if (pass == 1) {
-                        r = (int)(cs - j);
-                        need = 0;
-                    }
-                }
-                acc = __shfl_sync(0xffffffffu, run, 31);
+                const float run = acc + warp_scan(valid ? tile_log_decay(G, si, c, h, T_total) : 0.f, lane);
+                const unsigned hit = __ballot_sync(kFull, valid && run <= -kTruncLog);
+                if (hit) r0 = cs - (__ffs(hit) - 1);
+                acc = __shfl_sync(kFull, run, 31);
             }
-            if (!found) break;   // no horizon inside the segment: full transition
+        }
+        // pass 1, with the erase factors (its horizon lies at or before r0), two tiles
+        // per step, lane = token (tile cs - lane / 16, token lane % 16); a walk that has
+        // not crossed a few segment-end distances past r0 gives up (full transition)
+        if (r0 >= 0) {
+            const int64_t limit = max(si.c0, r0 - 4 * (si.c1 - r0) - 64);
+            float acc = 0.f;
+            for (int64_t cs = si.c1 - 1; cs >= limit; cs -= 2) {
+                const int64_t c = cs - (lane >> 4);
+                const int i = lane & 15;
+                float part = 0.f;
+                if (c >= limit) {
+                    const int len = (int)min((int64_t)kC, si.len - c * kC);
+                    const int64_t row = si.tok0 + c * kC + i;
+                    if (i < len && GDR_INBOUNDS(row < T_total)) {
+                        const uint4 *kp = (const uint4 *)(k + (row * H + h) * kD);
+                        float kk = 0.f;
+#pragma unroll
+                        for (int u = 0; u < kD / 8; ++u) {
+                            const uint4 w = kp[u];
+                            const __nv_bfloat162 *p2 = (const __nv_bfloat162 *)&w;
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) {
+                                const float2 f = __bfloat1622float2(p2[m]);
+                                kk = fmaf(f.x, f.x, fmaf(f.y, f.y, kk));
+                            }
+                        }
+                        const float e = fabsf(1.f - Bt[(int64_t)h * T_total + row] * kk);
+                        if (e > 1.f) part = logf(e);
+                    }
+                    if (i == 0) part += tile_log_decay(G, si, c, h, T_total);
+                }
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) part += __shfl_xor_sync(kFull, part, o);   // per half
+                const float t_hi = __shfl_sync(kFull, part, 0), t_lo = __shfl_sync(kFull, part, 16);
+                acc += t_hi;
+                if (acc <= -kTruncLog) {
+                    r = (int)cs;
+                    need = 0;
+                    break;
+                }
+                acc += t_lo;
+                if (cs - 1 >= limit && acc <= -kTruncLog) {
+                    r = (int)(cs - 1);
+                    need = 0;
+                    break;
+                }
+            }
         }
     }
     if (lane == 0) {
@@ -889,6 +920,7 @@ tc_combine_kernel(float *Hin, const float *Bs, const float *Ms, const int *mneed
     const float *pending = nullptr;
     for (int s = 1; s < nseg; ++s) {
         const int64_t prev = (g0 + s - 1) * H + h, cur = (g0 + s) * H + h;
+        if (!GDR_INBOUNDS(cur < p.seg_base[p.N] * H)) return;   // (block-uniform)
         const float *B = Bs + prev * kD * kD;
         float *Hc = Hin + cur * kD * kD;
         if (s == 1 || mneed[prev] == 0) {
@@ -968,14 +1000,21 @@ bool make_map(CUtensorMap *map, const void *base, int H, int64_t rows) {
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Streaming multiprocessors of the current device, looked up once per device (a
+// benign race: concurrent first calls store the same value).
 int sm_count() {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-            n = 148;
+    constexpr int kMaxDev = 64;
+    static std::atomic<int> cache[kMaxDev];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+    if (dev >= 0 && dev < kMaxDev) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
     }
+    int n = 0;
+    if (dev < 0 || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        n = 148;
+    if (dev >= 0 && dev < kMaxDev) cache[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
@@ -990,20 +1029,45 @@ bool tc_supported(gdr_dtype_t dtype, int dk, int dv, int chunk) {
     return dtype == GDR_BF16 && dk == kD && dv == kD && chunk == kC;
 }
 
-int tc_segment_chunks(int N, int H, int64_t T_total, int C) {
+// Tiles per segment.  The output pass runs one CTA per (segment, head), two per SM,
+// and takes as long as its slowest wave.
+//   Dense input (N sequences of equal length): the segments per sequence s that
+//   minimise waves(s) x tiles per segment, with waves(s) = ceil(N H s / slots), plus a
+//   small charge per extra segment (its transition pass and start-up).
+//   Packed input (lengths unknown on the host): segments of a quarter of an even share
+//   of the tiles, so that the block scheduler balances the many unequal CTAs.
+int tc_segment_chunks(int N, int H, int64_t T_total, int C, bool varlen) {
     if (const char *env = std::getenv("GDR_TC_SEG_CHUNKS")) {
         const int v = std::atoi(env);
         if (v > 0) return v;
     }
-    // about two resident streams per SM in the output pass
-    const int64_t target = 2 * (int64_t)sm_count();
-    const int64_t tiles = (T_total + C - 1) / C + N;
-    int64_t sc = (tiles * H + target - 1) / target;
-    return (int)std::max<int64_t>(32, std::min<int64_t>(sc, 1 << 30));
+    constexpr int64_t kMinTiles = 32;
+    const int64_t slots = 2 * (int64_t)sm_count();
+    if (varlen) {
+        const int64_t tiles = (T_total + C - 1) / C + N;
+        const int64_t sc = (tiles * H + 4 * slots - 1) / (4 * slots);
+        return (int)std::max<int64_t>(kMinTiles, std::min<int64_t>(sc, 1 << 30));
+    }
+    const int64_t L = (T_total / std::max(N, 1) + C - 1) / C;   // tiles per sequence
+    if (L <= kMinTiles) return (int)kMinTiles;
+    int64_t best_s = 1;
+    double best = 1e300;
+    const int64_t s_max = std::min<int64_t>(L / kMinTiles, 4096);
+    for (int64_t s = 1; s <= s_max; ++s) {
+        const int64_t ctas = (int64_t)N * H * s;
+        const int64_t waves = (ctas + slots - 1) / slots;
+        const int64_t per = (L + s - 1) / s;
+        const double cost = (double)waves * (double)per + 4.0 * (double)waves * (double)(s > 1);
+        if (cost < best) {
+            best = cost;
+            best_s = s;
+        }
+    }
+    return (int)((L + best_s - 1) / best_s);
 }
 
-size_t tc_workspace_bytes(int N, int H, int64_t T_total, int C) {
-    const int sc = tc_segment_chunks(N, H, T_total, C);
+size_t tc_workspace_bytes(int N, int H, int64_t T_total, int C, bool varlen) {
+    const int sc = tc_segment_chunks(N, H, T_total, C, varlen);
     const int64_t nseg = max_segments(N, T_total, sc);
     const size_t per = (size_t)nseg * H * kD * kD * sizeof(float);
     const size_t flags = (size_t)nseg * H * sizeof(int);

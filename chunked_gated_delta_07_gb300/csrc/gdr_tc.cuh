@@ -9,10 +9,10 @@ namespace gdr {
 bool tc_supported(gdr_dtype_t dtype, int dk, int dv, int chunk);
 
 // Tiles per segment for the segment-parallel state pass.
-int tc_segment_chunks(int N, int H, int64_t T_total, int C);
+int tc_segment_chunks(int N, int H, int64_t T_total, int C, bool varlen);
 
 // Scratch bytes of the tensor-core path beyond the plan, G and Bt.
-size_t tc_workspace_bytes(int N, int H, int64_t T_total, int C);
+size_t tc_workspace_bytes(int N, int H, int64_t T_total, int C, bool varlen);
 
 // Stages 2-4 on the tensor cores (stage 1, plan and G/Bt already enqueued).
 cudaError_t launch_tc_forward(const void *q, const void *k, const void *v, const float *G,

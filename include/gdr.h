@@ -90,7 +90,9 @@ typedef enum {
     GDR_ERR_CUDA = 3,         /* a CUDA runtime call failed                      */
     GDR_ERR_TIMEOUT = 4,      /* a bounded device-side wait ran out              */
     GDR_ERR_NO_WORKSPACE = 5, /* caller workspace smaller than required          */
-    GDR_ERR_BAD_SEQLENS = 6   /* cu_seqlens is not 0 = c0 <= c1 <= ... <= cN = T */
+    GDR_ERR_BAD_SEQLENS = 6,  /* cu_seqlens is not 0 = c0 <= c1 <= ... <= cN = T */
+    GDR_ERR_BOUNDS = 7        /* checking build (GDR_DEBUG) only: a device-side index
+                                 check failed and its access was skipped           */
 } gdr_status_t;
 
 typedef enum { GDR_BF16 = 0, GDR_F32 = 1 } gdr_dtype_t;

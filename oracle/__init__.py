@@ -67,6 +67,23 @@ def _compile(src, lib, force):
     return lib
 
 
+def build_sanitized(out_dir: str, gdr_src: str | None = None) -> tuple[str, str]:
+    """Compile both C files with AddressSanitizer and UndefinedBehaviorSanitizer into
+    out_dir (for the sanitizer tests, which load them in a process that preloads the
+    sanitizer runtimes); ``gdr_src`` replaces gdr_oracle.c (a planted fault).  Returns
+    (libgdr_oracle, librouter_oracle) paths."""
+    os.makedirs(out_dir, exist_ok=True)
+    outs = []
+    for src, name in ((gdr_src or _SRC, "libgdr_oracle.so"), (_RSRC, "librouter_oracle.so")):
+        lib = os.path.join(out_dir, name)
+        cmd = ["gcc", "-O1", "-g", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+               "-fsanitize=address,undefined", "-fno-sanitize-recover=undefined",
+               "-fno-omit-frame-pointer", "-o", lib, src, "-lm"]
+        subprocess.run(cmd, check=True)
+        outs.append(lib)
+    return outs[0], outs[1]
+
+
 def build(force: bool = False) -> str:
     """Compile gdr_oracle.c into libgdr_oracle.so and router_oracle.c into
     librouter_oracle.so next to them (gcc, OpenMP, ISO C11: no FMA contraction)."""

@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(7):
+    for code in range(8):
         assert gdr.gdr_status_string(code)
     assert gdr.gdr_status_string(99) == "unknown status"
 

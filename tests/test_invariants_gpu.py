@@ -64,10 +64,14 @@ def test_varlen_equals_separate_calls(path):
         y = _slice(x, cu[n], cu[n + 1])
         y.update(cu_seqlens=None, B=1, N=1, h0=x["h0"][n:n + 1])
         o, h = run_gpu(y, path=path)
-        # both paths run the same tiles and segments either way (these sequences are
-        # shorter than a tensor-core segment): equal up to fp32 reordering
-        assert rel_l2(to64(o), to64(out[:, cu[n]:cu[n + 1]])) < 1e-5
-        assert rel_l2(to64(h), to64(hT[n:n + 1])) < 1e-5
+        if path == "simt":   # the same tiles and fp32 operations either way
+            assert rel_l2(to64(o), to64(out[:, cu[n]:cu[n + 1]])) < 1e-5
+            assert rel_l2(to64(h), to64(hT[n:n + 1])) < 1e-5
+        else:
+            # the tensor-core path cuts packed and single sequences into segments
+            # differently, which changes only the rounding (as in test_chaining)
+            assert rel_l2(to64(o), to64(out[:, cu[n]:cu[n + 1]])) < 3e-3
+            assert rel_l2(to64(h), to64(hT[n:n + 1])) < 3e-3
 
 
 @pytest.mark.parametrize("path", _paths())
