@@ -641,6 +641,13 @@ static bool bwd_force_token_path() {
     return e && e[0] == '1';
 }
 
+// GDR_VEC_MMA=1 runs the per-channel forward on the earlier mma.sync kernel instead
+// of the tcgen05 one (for comparisons).
+static bool vec_use_mma_sync() {
+    const char *e = std::getenv("GDR_VEC_MMA");
+    return e && e[0] == '1';
+}
+
 static gdr_status_t chunk_bwd_impl(const void *q, const void *k, const void *v, const void *a,
                            const void *beta, const float *h0, const void *dout,
                            const float *dhT, void *dq, void *dk_out, void *dv_out, void *da,
@@ -783,11 +790,19 @@ gdr_status_t gdr_chunk_fwd_vec(const void *q, const void *k, const void *v, cons
     if (launch_plan(cu_seqlens, B, s.T_per, s.T_total, kVecTile, seg, seq_start,
                     seq_start + (B + 1), seq_start + 2 * (B + 1), ctx->d_status, stream) != cudaSuccess)
         return GDR_ERR_CUDA;
-    if (fused)
+    if (fused && vec_use_mma_sync())
         return launch_vec_mma(q, k, v, a, beta, h0, out, hT, plan, H, b, segs, ws + plan_b, stream) ==
                        cudaSuccess
                    ? GDR_OK
                    : GDR_ERR_CUDA;
+    if (fused) {   // tcgen05 kernel after the warm-up search
+        int *warm = (int *)(ws + plan_b);
+        if (launch_vec_warm(a, k, beta, warm, plan, H, b, segs, stream) != cudaSuccess) return GDR_ERR_CUDA;
+        return launch_tc_vec(q, k, v, a, beta, h0, out, hT, plan, H, s.T_total, b, segs, warm,
+                             ctx->d_status, stream) == cudaSuccess
+                   ? GDR_OK
+                   : GDR_ERR_CUDA;
+    }
     return launch_vec_forward(q, k, v, a, beta, h0, out, hT, dtype, plan, H, dk, dv, s.T_total, tiles,
                               b, ws + plan_b, stream) == cudaSuccess
                ? GDR_OK

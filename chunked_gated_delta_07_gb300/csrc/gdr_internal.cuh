@@ -162,6 +162,11 @@ int vec_mma_segment_tiles(int64_t tiles, int H, int sms);
 cudaError_t launch_vec_mma(const void *q, const void *k, const void *v, const void *a,
                            const void *beta, const float *h0, void *out, float *hT, Plan plan,
                            int H, float b, int64_t max_segs, void *scratch, cudaStream_t stream);
+// The warm-up of every (segment, head) of the plan (int [max_segs][H] in `warm`):
+// tiles to run from a zero state before the segment start, 0 at a sequence start,
+// -1 when no warm-up within 4 segments bounds the dropped state below 2^-64.
+cudaError_t launch_vec_warm(const void *a, const void *k, const void *beta, int *warm, Plan plan,
+                            int H, float b, int64_t max_segs, cudaStream_t stream);
 
 // backward in the chunked form, bf16 d = 128, bounded gate (gdr_bwd_chunk.cu)
 int chunk_bwd_segment_tiles(int64_t tiles, int H, int sms);

@@ -1025,6 +1025,10 @@ int64_t max_segments(int N, int64_t T_total, int seg_chunks) {
 
 }  // namespace
 
+bool tc_make_map(CUtensorMap *map, const void *base, int H, int64_t rows) {
+    return make_map(map, base, H, rows);
+}
+
 bool tc_supported(gdr_dtype_t dtype, int dk, int dv, int chunk) {
     return dtype == GDR_BF16 && dk == kD && dv == kD && chunk == kC;
 }

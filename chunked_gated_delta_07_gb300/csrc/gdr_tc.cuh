@@ -1,6 +1,8 @@
 // gdr_tc.cuh -- the tcgen05 (5th-generation tensor core) path: host-side entry points.
 #pragma once
 
+#include <cuda.h>
+
 #include "gdr_internal.cuh"
 
 namespace gdr {
@@ -19,5 +21,18 @@ cudaError_t launch_tc_forward(const void *q, const void *k, const void *v, const
                               const float *Bt, const float *h0, void *out, float *hT, Plan plan,
                               int H, int64_t T_total, int64_t max_chunks, void *scratch,
                               int *status, cudaStream_t stream);
+
+// Tensor map of a [rows][H][128] bf16 tensor for 64-column x C-row tile loads
+// (128-byte swizzle); false when the driver entry point is missing or the base is
+// not 16-byte aligned.
+bool tc_make_map(CUtensorMap *map, const void *base, int H, int64_t rows);
+
+// The per-channel decay forward on the tensor cores (gdr_tc_vec.cu): bf16, d = 128,
+// tiles of 16, bounded gate.  `warm` holds the warm-up of every (segment, head),
+// written by launch_vec_warm on the same plan.
+cudaError_t launch_tc_vec(const void *q, const void *k, const void *v, const void *a,
+                          const void *beta, const float *h0, void *out, float *hT, Plan plan,
+                          int H, int64_t T_total, float b, int64_t max_segs, const int *warm,
+                          int *status, cudaStream_t stream);
 
 }  // namespace gdr

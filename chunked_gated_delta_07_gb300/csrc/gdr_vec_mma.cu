@@ -487,6 +487,20 @@ int vec_mma_segment_tiles(int64_t tiles, int H, int sms) {
     return seg;
 }
 
+cudaError_t launch_vec_warm(const void *a, const void *k, const void *beta, int *warm, Plan plan,
+                            int H, float b, int64_t max_segs, cudaStream_t stream) {
+    if (plan.C != kT || plan.seg_chunks < kSegMin || plan.seg_chunks > kSegMax) return cudaErrorInvalidValue;
+    const int64_t blocks = max_segs * H;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+    if (blocks == 0) return cudaSuccess;
+    ProfScope prof(stream, "vec_warm_kernel");
+    vec_warm_kernel<<<(unsigned)blocks, 32 * kWarmWarps, 0, stream>>>(
+        (const __nv_bfloat16 *)a, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)beta, warm,
+        plan, H, b);
+    count_launch();
+    return cudaGetLastError();
+}
+
 cudaError_t launch_vec_mma(const void *q, const void *k, const void *v, const void *a,
                            const void *beta, const float *h0, void *out, float *hT, Plan plan,
                            int H, float b, int64_t max_segs, void *scratch, cudaStream_t stream) {
@@ -495,15 +509,8 @@ cudaError_t launch_vec_mma(const void *q, const void *k, const void *v, const vo
     if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
     if (blocks == 0) return cudaSuccess;
     int *warm = (int *)scratch;
-    cudaError_t err;
-    {
-        ProfScope prof(stream, "vec_warm_kernel");
-        vec_warm_kernel<<<(unsigned)blocks, 32 * kWarmWarps, 0, stream>>>(
-            (const __nv_bfloat16 *)a, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)beta, warm,
-            plan, H, b);
-        count_launch();
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    }
+    cudaError_t err = launch_vec_warm(a, k, beta, warm, plan, H, b, max_segs, stream);
+    if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(vec_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)kSmemBytes);
     if (err != cudaSuccess) return err;
