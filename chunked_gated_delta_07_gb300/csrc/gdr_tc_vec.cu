@@ -81,8 +81,8 @@ constexpr uint32_t kOffA0 = kOffWQ;                  // raw gate inputs, columns
 constexpr uint32_t kOffA1 = kOffWQ + kWQBlock;       // raw gate inputs, columns 64..127
 constexpr uint32_t kOffQ0 = kOffWQ + 2 * kWQBlock;   // raw Q, columns 0..63
 constexpr uint32_t kOffQ1 = kOffWQ + 3 * kWQBlock;   // raw Q, columns 64..127
-constexpr uint32_t kOffBT = kOffWQ + 4 * kWQBlock;   // A (fp32 [C][C]), then Bu in tf32
-constexpr uint32_t kOffBU = kOffBT + kC * kC * 4;    // Bu in bf16
+constexpr uint32_t kOffBT = kOffWQ + 4 * kWQBlock;   // Gram scratch (Kt, Kh bf16), A (fp32 [C][C]), then Bu in tf32
+constexpr uint32_t kOffBU = kOffBT + kC * kC * 4;    // Gram scratch (Qt bf16), then Bu in bf16
 constexpr uint32_t kOffP = kOffBU + kC * kC * 2;     // P in bf16
 constexpr uint32_t kOffHdr = kOffP + kC * kC * 2;
 constexpr uint32_t kStage = 27648;
@@ -112,11 +112,6 @@ __device__ __forceinline__ uint32_t cc_off_tf32(int n, int k) {
 __device__ __forceinline__ uint32_t wq_off(int row, int d) {
     return kOffWQ + (uint32_t)(d >> 5) * kWQBlock + sw128_off((uint32_t)row, (uint32_t)(d & 31) * 4u);
 }
-// byte offset of element (row, d) of a raw [C][128] bf16 tile stored as two 64-column boxes
-__device__ __forceinline__ uint32_t box_off(int row, int d) {
-    return (uint32_t)(d >> 6) * kBox + sw128_off((uint32_t)row, (uint32_t)(d & 63) * 2u);
-}
-
 struct TvArgs {
     const __nv_bfloat16 *beta;
     const float *h0;
@@ -342,61 +337,78 @@ tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 *(float4 *)&hdr->gam[d] = make_float4(__expf(G0), __expf(G1), __expf(G2), __expf(G3));
             }
             __syncwarp();
-            // ---- per quarter of the columns: the factored tiles at this lane's
-            // fragment positions (rows g, g + 8; columns 16 s + 2t, +1, +8, +9 of each
-            // 16-column slab s), the Gram products, K'' over the raw K, -Kt and Qt in tf32.
-            // Quarter qd writes -Kt over raw data that quarters <= qd have read: raw gate
-            // inputs (quarters 0, 1), raw Q columns 0..63 (quarter 2) and 64..127
-            // (quarter 3, after its own reads).
+            // ---- per 16-column slab s: lane (row i = lane / 2, 8 columns of half lane & 1)
+            // forms Kt, Kh, Qt, K'' = Kh (.) gamma from the raw tiles and exp(G); writes K''
+            // over the raw K, -Kt (tf32) over the raw gate inputs / raw Q, Qt (tf32) over
+            // exp(G), and Kt, Kh, Qt in bf16 to a 16 x 16 scratch from which the Gram
+            // products take their fragments.  Slab s writes -Kt over raw data that slabs
+            // <= s have read: raw gate inputs (slabs 0-3), raw Q columns 0..63 (slabs 4, 5)
+            // and 64..127 (slabs 6, 7, after their own reads).
             float skk[2][4] = {}, sqk[2][4] = {};
-#pragma unroll 1
-            for (int qd = 0; qd < 4; ++qd) {
-                const int box = qd >> 1;
-                uint32_t kf[2][4], qf[2][4];
+            {
+                const int i = lane >> 1, hw = lane & 1;
+                const uint32_t srow = (uint32_t)i * 32u + 16u * (uint32_t)(hw ^ ((i >> 2) & 1));
+                const uint32_t lrow = (uint32_t)(lane & 15) * 32u +
+                                      16u * (uint32_t)((lane >> 4) ^ (((lane & 15) >> 2) & 1));
+#pragma unroll 2
+                for (int sl = 0; sl < kD / 16; ++sl) {
+                    const int d0 = 16 * sl + 8 * hw;
+                    const uint32_t kq_off = sw128_off((uint32_t)i, (uint32_t)(d0 & 63) * 2u);
+                    const uint4 kr = *(const uint4 *)(stg + kOffK + (d0 >> 6) * kBox + kq_off);
+                    uint4 qr = make_uint4(0, 0, 0, 0);
+                    if (use_q) qr = *(const uint4 *)(stg + q_box(d0 >> 6) + kq_off);
+                    const float4 ea = *(const float4 *)(stg + wq_off(kC + i, d0));
+                    const float4 eb = *(const float4 *)(stg + wq_off(kC + i, d0 + 4));
+                    const float4 ga = *(const float4 *)&hdr->gam[d0];
+                    const float4 gb = *(const float4 *)&hdr->gam[d0 + 4];
+                    __syncwarp();   // the slab's raw data is read before anything overwrites it
+                    const float E[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
+                    const float gmv[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+                    const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
+                    const uint32_t qw[4] = {qr.x, qr.y, qr.z, qr.w};
+                    float kt[8], kh[8], qt[8], kp[8];
 #pragma unroll
-                for (int s = 0; s < 2; ++s) {
-                    const int ks = 2 * qd + s;
-                    const uint32_t off = sw128_off(lane & 15, 32 * (ks & 3) + 16 * (lane >> 4));
-                    ldsm_x4(smem_u32(stg + kOffK + box * kBox + off), kf[s]);
-                    if (use_q) ldsm_x4(smem_u32(stg + q_box(box) + off), qf[s]);
-                }
-                __syncwarp();   // the quarter's raw K and Q are read before anything overwrites them
-#pragma unroll
-                for (int s = 0; s < 2; ++s) {
-                    const int dlo = 32 * qd + 16 * s + 2 * t;   // columns dlo, dlo + 1 (regs 0, 1)
-                    uint32_t kt[4], kh[4], qt[4];
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const int i = g + 8 * (r & 1);
-                        const int d = dlo + 8 * (r >> 1);
-                        const float2 eg = *(const float2 *)(stg + wq_off(kC + i, d));   // exp(G)
-                        const float2 gm = *(const float2 *)&hdr->gam[d];
-                        const float e0 = eg.x, e1 = eg.y;
-                        const float n0 = __fdividef(1.f, e0), n1 = __fdividef(1.f, e1);
-                        const float2 kv = unpack_bf16(kf[s][r]);
-                        const float kt0 = kv.x * e0, kt1 = kv.y * e1;
-                        const float kh0 = kv.x * n0, kh1 = kv.y * n1;
-                        kt[r] = pack_bf16(kt0, kt1);
-                        kh[r] = pack_bf16(kh0, kh1);
-                        // K'' = K e^{G_C - G} (the update's operand) over the raw K
-                        *(uint32_t *)(stg + kOffK + box_off(i, d)) = pack_bf16(kh0 * gm.x, kh1 * gm.y);
-                        // -Kt in tf32 over the raw gate inputs / raw Q
-                        *(float2 *)(stg + wq_off(i, d)) = make_float2(-kt0, -kt1);
-                        if (use_q) {
-                            const float2 qv = unpack_bf16(qf[s][r]);
-                            const float qt0 = qv.x * e0, qt1 = qv.y * e1;
-                            qt[r] = pack_bf16(qt0, qt1);
-                            *(float2 *)(stg + wq_off(kC + i, d)) = make_float2(qt0, qt1);   // over exp(G)
-                        }
+                    for (int u = 0; u < 8; ++u) {
+                        const float kv = __uint_as_float(u & 1 ? kw[u / 2] & 0xffff0000u : kw[u / 2] << 16);
+                        const float qv = __uint_as_float(u & 1 ? qw[u / 2] & 0xffff0000u : qw[u / 2] << 16);
+                        const float n = __fdividef(1.f, E[u]);
+                        kt[u] = kv * E[u];
+                        kh[u] = kv * n;
+                        kp[u] = kh[u] * gmv[u];
+                        qt[u] = qv * E[u];
                     }
-                    mma16816(skk[0], kt, kh[0], kh[2]);
-                    mma16816(skk[1], kt, kh[1], kh[3]);
+                    *(uint4 *)(stg + kOffK + (d0 >> 6) * kBox + kq_off) =
+                        make_uint4(pack_bf16(kp[0], kp[1]), pack_bf16(kp[2], kp[3]), pack_bf16(kp[4], kp[5]),
+                                   pack_bf16(kp[6], kp[7]));
+                    *(float4 *)(stg + wq_off(i, d0)) = make_float4(-kt[0], -kt[1], -kt[2], -kt[3]);
+                    *(float4 *)(stg + wq_off(i, d0 + 4)) = make_float4(-kt[4], -kt[5], -kt[6], -kt[7]);
+                    *(uint4 *)(stg + kOffBT + srow) =
+                        make_uint4(pack_bf16(kt[0], kt[1]), pack_bf16(kt[2], kt[3]), pack_bf16(kt[4], kt[5]),
+                                   pack_bf16(kt[6], kt[7]));
+                    *(uint4 *)(stg + kOffBT + 512 + srow) =
+                        make_uint4(pack_bf16(kh[0], kh[1]), pack_bf16(kh[2], kh[3]), pack_bf16(kh[4], kh[5]),
+                                   pack_bf16(kh[6], kh[7]));
                     if (use_q) {
-                        mma16816(sqk[0], qt, kh[0], kh[2]);
-                        mma16816(sqk[1], qt, kh[1], kh[3]);
+                        *(float4 *)(stg + wq_off(kC + i, d0)) = make_float4(qt[0], qt[1], qt[2], qt[3]);
+                        *(float4 *)(stg + wq_off(kC + i, d0 + 4)) = make_float4(qt[4], qt[5], qt[6], qt[7]);
+                        *(uint4 *)(stg + kOffBU + srow) =
+                            make_uint4(pack_bf16(qt[0], qt[1]), pack_bf16(qt[2], qt[3]),
+                                       pack_bf16(qt[4], qt[5]), pack_bf16(qt[6], qt[7]));
+                    }
+                    __syncwarp();   // the scratch is written before the fragments are read
+                    uint32_t ktf[4], khf[4], qtf[4];
+                    ldsm_x4(smem_u32(stg + kOffBT + lrow), ktf);
+                    ldsm_x4(smem_u32(stg + kOffBT + 512 + lrow), khf);
+                    mma16816(skk[0], ktf, khf[0], khf[2]);
+                    mma16816(skk[1], ktf, khf[1], khf[3]);
+                    if (use_q) {
+                        ldsm_x4(smem_u32(stg + kOffBU + lrow), qtf);
+                        mma16816(sqk[0], qtf, khf[0], khf[2]);
+                        mma16816(sqk[1], qtf, khf[1], khf[3]);
                     }
                 }
             }
+            __syncwarp();   // the last fragments are read before A and P overwrite the scratch
             // ---- A = beta (.) strict_lower(Skk) (fp32, for the substitution) and
             // P = lower(Sqk) (bf16, the output term's operand), from the accumulators:
             // skk[nt][r] is (row g + 8 (r >> 1), column 8 nt + 2t + (r & 1))
@@ -625,12 +637,16 @@ tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     tmem_ld_wait();
                     if (q + 1 < kD / 16) tmem_ld16(tm + lane_base + kColH + 16 * (q + 1), nxt);
 #pragma unroll
-                    for (int j2 = 0; j2 < 8; ++j2) {
-                        const uint64_t g2 = *(const uint64_t *)&hdr->gam[16 * q + 2 * j2];
-                        const uint64_t x2 = ((uint64_t)cur[2 * j2 + 1] << 32) | cur[2 * j2];
-                        const uint64_t y2 = mul_f32x2(x2, g2);
-                        cur[2 * j2] = (uint32_t)y2;
-                        cur[2 * j2 + 1] = (uint32_t)(y2 >> 32);
+                    for (int j4 = 0; j4 < 4; ++j4) {
+                        const uint4 g4 = *(const uint4 *)&hdr->gam[16 * q + 4 * j4];
+                        const uint64_t y0 = mul_f32x2(((uint64_t)cur[4 * j4 + 1] << 32) | cur[4 * j4],
+                                                      ((uint64_t)g4.y << 32) | g4.x);
+                        const uint64_t y1 = mul_f32x2(((uint64_t)cur[4 * j4 + 3] << 32) | cur[4 * j4 + 2],
+                                                      ((uint64_t)g4.w << 32) | g4.z);
+                        cur[4 * j4] = (uint32_t)y0;
+                        cur[4 * j4 + 1] = (uint32_t)(y0 >> 32);
+                        cur[4 * j4 + 2] = (uint32_t)y1;
+                        cur[4 * j4 + 3] = (uint32_t)(y1 >> 32);
                     }
                     tmem_st16(tm + lane_base + kColH + 16 * q, cur);
                 }
