@@ -164,3 +164,35 @@ def test_vec_unaligned_pointer_takes_the_cuda_core_kernels(which):
     ro, rh = oracle.oracle_fwd_vec(x["q"], x["k"], x["v"], x["av"], x["beta"], h0=x["h0"], b=2.0)
     assert_close(to64(out), ro, "bf16", "out")
     assert_close(to64(hT), rh, "bf16", "hT")
+
+
+@pytest.mark.parametrize("case", ["segments", "weak_decay", "packed"])
+def test_vec_mma_sync_kernel_still_matches_the_oracle(case, monkeypatch):
+    """GDR_VEC_MMA=1 runs the earlier per-channel kernel (mma.sync, the state in
+    registers) instead of the tcgen05 one; it stays correct on the shapes that
+    exercise its segments, its unsegmented fallback and packed sequences."""
+    monkeypatch.setenv("GDR_VEC_MMA", "1")
+    if case == "segments":
+        x = _inputs("bf16", 128, 3000, seed=5950, N=1, H=2)
+    elif case == "weak_decay":
+        x = _inputs("bf16", 128, 2000, seed=5951, N=1, H=2, a_mean=-6.0)
+    else:
+        x = _inputs("bf16", 128, 3000, seed=5952, N=3, H=2, varlen=True)
+    _check(x, "bf16")
+
+
+def test_vec_tensor_core_kernels_agree():
+    """The tcgen05 kernel and the mma.sync kernel on the same inputs agree within the
+    bf16 tolerance of each against the oracle (both are checked there too)."""
+    import os
+    x = _inputs("bf16", 128, 2500, seed=5960, N=2, H=3)
+    out_tc, hT_tc = gdr.chunk_fwd_vec(x["q"], x["k"], x["v"], x["av"], x["beta"], h0=x["h0"], b=2.0)
+    os.environ["GDR_VEC_MMA"] = "1"
+    try:
+        out_ms, hT_ms = gdr.chunk_fwd_vec(x["q"], x["k"], x["v"], x["av"], x["beta"], h0=x["h0"], b=2.0)
+    finally:
+        del os.environ["GDR_VEC_MMA"]
+    torch.cuda.synchronize()
+    assert gdr.gdr_get_status() == gdr.GDR_OK
+    assert_close(to64(out_tc), to64(out_ms), "bf16", "out, tcgen05 vs mma.sync")
+    assert_close(to64(hT_tc), to64(hT_ms), "bf16", "hT, tcgen05 vs mma.sync")
