@@ -44,6 +44,23 @@ def main():
             out, hT = run(x, path)
             assert_close(to64(out), ro.reshape(out.shape), tol, f"{w.name} out [{path}]")
             assert_close(to64(hT), rh.reshape(hT.shape), tol, f"{w.name} hT [{path}]")
+    # the per-channel decay forward (tcgen05 kernel): segments with warm-up tiles, packed
+    # sequences with a ragged end
+    import oracle
+    from gdr_inputs import make_channel_gate
+    for w, T in [(WORKLOADS["b2_t4k"].with_(B=1, H=2, seed=1035, h0_std=0.05), 3000),
+                 (WORKLOADS["varlen_1m"].with_(H=2, len_min=30, len_max=1500, seed=1036), 3001)]:
+        x = make_inputs(w, device="cuda", T=T)
+        av = make_channel_gate(x, 1037)
+        out, hT = gdr.chunk_fwd_vec(x["q"], x["k"], x["v"], av, x["beta"], h0=x["h0"],
+                                    cu_seqlens=x["cu_seqlens"], b=w.b)
+        st = gdr.gdr_get_status()
+        assert st == gdr.GDR_OK, gdr.gdr_status_string(st)
+        cu = None if x["cu_seqlens"] is None else x["cu_seqlens"].cpu().numpy()
+        ro, rh = oracle.oracle_fwd_vec(x["q"], x["k"], x["v"], av, x["beta"], h0=x["h0"], cu_seqlens=cu,
+                                       b=w.b)
+        assert_close(to64(out), ro, "bf16", f"{w.name} per-channel out")
+        assert_close(to64(hT), rh, "bf16", f"{w.name} per-channel hT")
     # zero tokens
     x = make_inputs(WORKLOADS["b2_t4k"].with_(H=2, seed=1034), device="cuda", T=0)
     for path in ("simt", "tc"):

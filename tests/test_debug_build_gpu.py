@@ -1,6 +1,7 @@
 """The checking build (GDR_DEBUG: device-side index checks on the forward pass's global
 accesses, a failed one recorded as GDR_ERR_BOUNDS and its access skipped) on small
-parity cases, dense and packed, both gates, both paths, with many segments: results
+parity cases, dense and packed, both gates, both paths, with many segments, and the
+per-channel decay forward with warm-up segments and packed sequences: results
 equal the oracle's within the usual tolerances and no check fails (GPU).  It runs in a
 child process, since this one has the regular build loaded."""
 import os

@@ -1,4 +1,5 @@
-"""Bounded device waits of the tensor-core forward, made to run out (GPU).
+"""Bounded device waits of the tensor-core forward kernels (scalar and per-channel
+gate), made to run out (GPU).
 
 Every wait in tc_chunk_kernel gives up after a limit (2 s), records
 GDR_ERR_TIMEOUT in the status word and unwinds: the CTA drains its tile copies
@@ -52,5 +53,33 @@ def test_waits_that_run_out_report_a_timeout_and_unwind(monkeypatch, limit_ns):
     ro, rh = run_oracle(x)
     for _ in range(2):
         out, hT = run_gpu(x, path="tc")   # asserts a clean status
+        assert_close(to64(out), ro, "bf16", "out")
+        assert_close(to64(hT), rh, "bf16", "hT")
+
+
+@pytest.mark.parametrize("limit_ns", [0, 1500])
+def test_per_channel_kernel_waits_that_run_out_unwind(monkeypatch, limit_ns):
+    """The same for the per-channel tcgen05 kernel (gdr_chunk_fwd_vec, bf16 d = 128),
+    with segments and warm-up tiles: the timed-out call reports GDR_ERR_TIMEOUT (limit
+    0), and the next two calls match the oracle."""
+    import oracle
+    from gdr_inputs import make_channel_gate
+    w = WORKLOADS["b2_t4k"].with_(B=1, H=2, seed=1025, h0_std=0.05)
+    x = make_inputs(w, device="cuda", T=2000)
+    av = make_channel_gate(x, 1026)
+    assert gdr.gdr_get_status() == gdr.GDR_OK
+    monkeypatch.setenv("GDR_TC_WAIT_NS", str(limit_ns))
+    gdr.chunk_fwd_vec(x["q"], x["k"], x["v"], av, x["beta"], h0=x["h0"], b=w.b)
+    st = gdr.gdr_get_status()
+    if limit_ns == 0:
+        assert st == gdr.GDR_ERR_TIMEOUT, gdr.gdr_status_string(st)
+    else:
+        assert st in (gdr.GDR_OK, gdr.GDR_ERR_TIMEOUT), gdr.gdr_status_string(st)
+    monkeypatch.delenv("GDR_TC_WAIT_NS")
+    ro, rh = oracle.oracle_fwd_vec(x["q"], x["k"], x["v"], av, x["beta"], h0=x["h0"], b=w.b)
+    for _ in range(2):
+        out, hT = gdr.chunk_fwd_vec(x["q"], x["k"], x["v"], av, x["beta"], h0=x["h0"], b=w.b)
+        torch.cuda.synchronize()
+        assert gdr.gdr_get_status() == gdr.GDR_OK
         assert_close(to64(out), ro, "bf16", "out")
         assert_close(to64(hT), rh, "bf16", "hT")
