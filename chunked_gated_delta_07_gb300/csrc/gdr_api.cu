@@ -78,6 +78,11 @@ namespace {
 
 constexpr int kMaxPieces = 8;   // pieces of a pipelined host-buffer call
 
+std::mutex &g_mu_aux() {
+    static std::mutex m;
+    return m;
+}
+
 struct DeviceCtx {
     int *d_status = nullptr;
     int sms = 0;         // streaming multiprocessors of the device
@@ -88,7 +93,27 @@ struct DeviceCtx {
     // copy streams and per-piece events of the pipelined host-buffer entry point
     cudaStream_t s_in = nullptr, s_out = nullptr;
     cudaEvent_t ev_in[kMaxPieces] = {}, ev_comp[kMaxPieces] = {}, ev_out[kMaxPieces] = {};
+    // the backward's second stream (its two state chains run concurrently)
+    AuxStream aux;
 };
+
+// The device's auxiliary stream and fork/join events, created on first use (an
+// empty AuxStream, i.e. one stream for everything, if that fails).
+AuxStream aux_stream(DeviceCtx *c) {
+    std::lock_guard<std::mutex> lk(g_mu_aux());
+    if (!c->aux.stream) {
+        AuxStream a;
+        if (cudaStreamCreateWithFlags(&a.stream, cudaStreamNonBlocking) != cudaSuccess) return AuxStream{};
+        if (cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming) != cudaSuccess) {
+            if (a.fork) cudaEventDestroy(a.fork);
+            cudaStreamDestroy(a.stream);
+            return AuxStream{};
+        }
+        c->aux = a;
+    }
+    return c->aux;
+}
 
 std::mutex g_mu;
 // a deque: growing it for a new device keeps every handed-out context in place
@@ -713,7 +738,8 @@ static gdr_status_t chunk_bwd_impl(const void *q, const void *k, const void *v, 
         return GDR_ERR_CUDA;
     if (chunked)
         return launch_chunk_bwd(q, k, v, a, beta, h0, dout, dhT, dq, dk_out, dv_out, da, dbeta, dh0,
-                                plan, H, tiles, segs, b, per_channel, ws + plan_b, stream) == cudaSuccess
+                                plan, H, tiles, segs, b, per_channel, ws + plan_b, stream,
+                                aux_stream(ctx)) == cudaSuccess
                    ? GDR_OK
                    : GDR_ERR_CUDA;
     return launch_bwd(q, k, v, a, beta, h0, dout, dhT, dq, dk_out, dv_out, da, dbeta, dh0, dtype,
@@ -953,7 +979,7 @@ void gdr_release(void) {
     cudaGetDevice(&cur);
     for (size_t d = 0; d < g_ctx.size(); ++d) {
         DeviceCtx &c = g_ctx[d];
-        if (!c.ws && !c.io && !c.d_status && !c.s_in) continue;
+        if (!c.ws && !c.io && !c.d_status && !c.s_in && !c.aux.stream) continue;
         cudaSetDevice((int)d);
         cudaDeviceSynchronize();
         if (c.ws) cudaFree(c.ws);
@@ -961,6 +987,9 @@ void gdr_release(void) {
         if (c.d_status) cudaFree(c.d_status);
         if (c.s_in) cudaStreamDestroy(c.s_in);
         if (c.s_out) cudaStreamDestroy(c.s_out);
+        if (c.aux.stream) cudaStreamDestroy(c.aux.stream);
+        if (c.aux.fork) cudaEventDestroy(c.aux.fork);
+        if (c.aux.join) cudaEventDestroy(c.aux.join);
         for (int i = 0; i < kMaxPieces; ++i) {
             if (c.ev_in[i]) cudaEventDestroy(c.ev_in[i]);
             if (c.ev_comp[i]) cudaEventDestroy(c.ev_comp[i]);

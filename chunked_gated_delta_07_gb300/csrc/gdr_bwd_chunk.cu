@@ -1062,7 +1062,7 @@ bwd_tile_kernel(const BcArgs A) {
 
 template <bool VEC>
 cudaError_t run_chunk_bwd(const BcArgs &A, int64_t max_tiles, int64_t max_segs, float *lam, int *ok,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, const AuxStream &aux) {
     cudaError_t err;
     const int H = A.H;
     auto kf = bwd_fwd_chain_kernel<VEC>;
@@ -1086,18 +1086,29 @@ cudaError_t run_chunk_bwd(const BcArgs &A, int64_t max_tiles, int64_t max_segs, 
         count_launch();
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
+    // The two chains are independent (the adjoint recurrence needs no forward state):
+    // with an auxiliary stream the adjoint chain runs beside the forward chain, and the
+    // tile kernel waits for both.
+    const bool fork = aux.stream != nullptr;
+    if (fork) {
+        if ((err = cudaEventRecord(aux.fork, stream)) != cudaSuccess) return err;
+        if ((err = cudaStreamWaitEvent(aux.stream, aux.fork, 0)) != cudaSuccess) return err;
+    }
+    {
+        cudaStream_t sa_stream = fork ? aux.stream : stream;
+        ProfScope prof(sa_stream, "bwd_adj_chain_kernel");
+        ka<<<(unsigned)segs, kThreads, sa, sa_stream>>>(A);
+        count_launch();
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    if (fork && (err = cudaEventRecord(aux.join, aux.stream)) != cudaSuccess) return err;
     {
         ProfScope prof(stream, "bwd_fwd_chain_kernel");
         kf<<<(unsigned)segs, kThreads, sf, stream>>>(A);
         count_launch();
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
-    {
-        ProfScope prof(stream, "bwd_adj_chain_kernel");
-        ka<<<(unsigned)segs, kThreads, sa, stream>>>(A);
-        count_launch();
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    }
+    if (fork && (err = cudaStreamWaitEvent(stream, aux.join, 0)) != cudaSuccess) return err;
     if (max_tiles > 0) {
         ProfScope prof(stream, "bwd_tile_kernel");
         kt<<<dim3((unsigned)max_tiles, (unsigned)H), kThreads, sg, stream>>>(A);
@@ -1126,7 +1137,8 @@ cudaError_t launch_chunk_bwd(const void *q, const void *k, const void *v, const 
                              const void *beta, const float *h0, const void *dout, const float *dhT,
                              void *dq, void *dk, void *dv, void *da, void *dbeta, float *dh0,
                              Plan plan, int H, int64_t max_tiles, int64_t max_segs, float b,
-                             bool per_channel, void *scratch, cudaStream_t stream) {
+                             bool per_channel, void *scratch, cudaStream_t stream,
+                             const AuxStream &aux) {
     if (plan.C != kT || plan.seg_chunks < kSegMin || plan.seg_chunks > kSegMax) return cudaErrorInvalidValue;
     auto al = [](size_t x) { return (x + 255) / 256 * 256; };
     BcArgs A;
@@ -1160,8 +1172,8 @@ cudaError_t launch_chunk_bwd(const void *q, const void *k, const void *v, const 
     A.p = plan;
     A.H = H;
     A.b = b;
-    return per_channel ? run_chunk_bwd<true>(A, max_tiles, max_segs, lam, ok, stream)
-                       : run_chunk_bwd<false>(A, max_tiles, max_segs, lam, ok, stream);
+    return per_channel ? run_chunk_bwd<true>(A, max_tiles, max_segs, lam, ok, stream, aux)
+                       : run_chunk_bwd<false>(A, max_tiles, max_segs, lam, ok, stream, aux);
 }
 
 }  // namespace gdr

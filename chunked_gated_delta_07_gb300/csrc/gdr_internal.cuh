@@ -168,6 +168,13 @@ cudaError_t launch_vec_mma(const void *q, const void *k, const void *v, const vo
 cudaError_t launch_vec_warm(const void *a, const void *k, const void *beta, int *warm, Plan plan,
                             int H, float b, int64_t max_segs, cudaStream_t stream);
 
+// An internal stream and the two events that fork work onto it from the caller's
+// stream and join it back (stream = nullptr: run everything on the caller's stream).
+struct AuxStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+
 // backward in the chunked form, bf16 d = 128, bounded gate (gdr_bwd_chunk.cu)
 int chunk_bwd_segment_tiles(int64_t tiles, int H, int sms);
 size_t chunk_bwd_scratch_bytes(int64_t tiles, int N, int H);
@@ -175,7 +182,8 @@ cudaError_t launch_chunk_bwd(const void *q, const void *k, const void *v, const 
                              const void *beta, const float *h0, const void *dout, const float *dhT,
                              void *dq, void *dk, void *dv, void *da, void *dbeta, float *dh0,
                              Plan plan, int H, int64_t max_tiles, int64_t max_segs, float b,
-                             bool per_channel, void *scratch, cudaStream_t stream);
+                             bool per_channel, void *scratch, cudaStream_t stream,
+                             const AuxStream &aux);
 
 // quantile-balancing router-bias update (gdr_router.cu)
 constexpr int kRouterMaxE = 2048;

@@ -352,7 +352,11 @@ GDR_API gdr_status_t gdr_router_bias_update(const int64_t *load, float *bias, do
  * by the caller; scratch comes from the internal per-device cache.  Outputs
  * must not alias inputs; dhT and dh0 must be 16-byte aligned (copied as
  * float4), GDR_ERR_INVALID_ARG otherwise.  The result is deterministic (no
- * atomics).  Errors as for gdr_chunk_fwd_ex; asynchronous on `stream`.
+ * atomics).  Errors as for gdr_chunk_fwd_ex; asynchronous on `stream`.  The
+ * chunked form runs its two state chains (forward and adjoint, independent of
+ * each other) concurrently: the adjoint chain on a second stream the library
+ * keeps per device (freed by gdr_release), forked from and joined back to
+ * `stream` with events, so the call is ordered on `stream` as a whole.
  */
 GDR_API gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const void *a,
                            const void *beta, const float *h0, const void *dout,
