@@ -172,7 +172,7 @@ struct Shape {
 
 // Scratch layout of one call.  Every region is 256-byte aligned.
 struct Layout {
-    size_t plan = 0, G = 0, Bt = 0, W = 0, U = 0, tc = 0, total = 0;
+    size_t plan = 0, G = 0, W = 0, U = 0, tc = 0, total = 0;
 };
 
 Layout layout_for(const Shape &s, gdr_path_t path) {
@@ -183,8 +183,6 @@ Layout layout_for(const Shape &s, gdr_path_t path) {
     L.G = off;
     off += align_up(sizeof(float) * (size_t)s.H * s.T_total);
     if (path == GDR_PATH_TC) {
-        L.Bt = off;
-        off += align_up(sizeof(float) * (size_t)s.H * s.T_total);
         L.tc = off;
         off += align_up(tc_workspace_bytes(s.N, s.H, s.T_total, s.C, s.varlen));
     } else {
@@ -285,12 +283,11 @@ gdr_status_t run_forward(const void *q, const void *k, const void *v, const void
     cudaError_t err = launch_plan(cu, s.N, s.T_per, s.T_total, s.C, seg_chunks, seq_start,
                                   chunk_base, seg_base, ctx->d_status, stream);
     if (err != cudaSuccess) return GDR_ERR_CUDA;
-    float *Bt = path == GDR_PATH_TC ? (float *)(ws + L.Bt) : nullptr;
-    err = launch_gate_cumsum(a, beta, dtype, G, Bt, plan, s.H, s.T_total, s.max_chunks, b, gate,
+    err = launch_gate_cumsum(a, beta, dtype, G, nullptr, plan, s.H, s.T_total, s.max_chunks, b, gate,
                              stream);
     if (err != cudaSuccess) return GDR_ERR_CUDA;
     if (path == GDR_PATH_TC) {
-        err = launch_tc_forward(q, k, v, G, Bt, h0, out, hT, plan, s.H, s.T_total, s.max_chunks,
+        err = launch_tc_forward(q, k, v, G, beta, h0, out, hT, plan, s.H, s.T_total, s.max_chunks,
                                 ws + L.tc, ctx->d_status, stream);
     } else {
         float *W = (float *)(ws + L.W);

@@ -147,7 +147,27 @@ gate_cumsum_kernel(const T *__restrict__ a, const T *__restrict__ beta, float *_
     float *sb = gsm + kGateHeads * ld;
     const int warp = tid >> 5, lane = tid & 31;
     constexpr int kRows = kGateTok / 8;   // token rows per warp (8 warps)
-    if (lane < nh) {   // warp per token row, lane per head; all loads in flight at once
+    const int64_t base = Tb * H + h0;
+    if (nh == H && ntok * H % 8 == 0 && ((uintptr_t)(a + base) | (uintptr_t)(beta + base)) % (8 * sizeof(T)) == 0 &&
+        GDR_INBOUNDS(Te <= T_total)) {
+        // every head of the block's tokens: one contiguous [ntok][H] region, read 8
+        // elements (16 or 32 bytes) per thread and load
+        for (int e0 = 8 * tid; e0 < ntok * H; e0 += 8 * 256) {
+            T av[8], bv[8];
+            *(uint4 *)av = *(const uint4 *)(a + base + e0);
+            if (sizeof(T) == 4) *((uint4 *)av + 1) = *((const uint4 *)(a + base + e0) + 1);
+            if (Bt) {
+                *(uint4 *)bv = *(const uint4 *)(beta + base + e0);
+                if (sizeof(T) == 4) *((uint4 *)bv + 1) = *((const uint4 *)(beta + base + e0) + 1);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int t = (e0 + u) / H, hh = (e0 + u) - t * H;
+                sg[hh * ld + t] = gate_logdecay(to_f32(av[u]), b, gate);
+                sb[hh * ld + t] = Bt ? to_f32(bv[u]) : 0.f;
+            }
+        }
+    } else if (lane < nh) {   // warp per token row, lane per head; all loads in flight at once
         float av[kRows], bv[kRows];
 #pragma unroll
         for (int r = 0; r < kRows; ++r) {

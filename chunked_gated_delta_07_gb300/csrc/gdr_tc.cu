@@ -118,7 +118,7 @@ enum Mode : int { kModeOut = 0, kModeB = 1, kModeM = 2 };
 
 struct TcArgs {
     const float *G;
-    const float *Bt;
+    const __nv_bfloat16 *beta;   // [rows][H] write strengths
     const float *h0;
     void *out;
     float *hT;
@@ -325,7 +325,7 @@ tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             if (lane < kC && GDR_INBOUNDS(t0 >= 0 && t0 + len <= args.T_total && len >= 1)) {
                 const int i = min(lane, len - 1);
                 g_i = args.G[(int64_t)h * args.T_total + t0 + i];
-                b_i = lane < len ? args.Bt[(int64_t)h * args.T_total + t0 + lane] : 0.f;
+                b_i = lane < len ? __bfloat162float(args.beta[(t0 + lane) * H + h]) : 0.f;
             }
             if (c >= kNS && !__all_sync(kFull, mbar_wait(&bar_free[st], ph ^ 1u, args.wait_ns))) {
                 if (lane == 0) set_status(args.status, GDR_ERR_TIMEOUT);
@@ -814,7 +814,7 @@ __device__ __forceinline__ float tile_log_decay(const float *G, const SegInfo &s
 }
 
 __global__ void __launch_bounds__(128)
-tc_horizon_kernel(const float *G, const float *Bt, const __nv_bfloat16 *k, Plan p, int H,
+tc_horizon_kernel(const float *G, const __nv_bfloat16 *beta, const __nv_bfloat16 *k, Plan p, int H,
                   int64_t T_total, int64_t nslots, int *first, int *mneed, int truncate) {
     const int64_t slot = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -867,7 +867,7 @@ tc_horizon_kernel(const float *G, const float *Bt, const __nv_bfloat16 *k, Plan 
                                 kk = fmaf(f.x, f.x, fmaf(f.y, f.y, kk));
                             }
                         }
-                        const float e = fabsf(1.f - Bt[(int64_t)h * T_total + row] * kk);
+                        const float e = fabsf(1.f - __bfloat162float(beta[row * H + h]) * kk);
                         if (e > 1.f) part = logf(e);
                     }
                     if (i == 0) part += tile_log_decay(G, si, c, h, T_total);
@@ -1079,7 +1079,7 @@ size_t tc_workspace_bytes(int N, int H, int64_t T_total, int C, bool varlen) {
 }
 
 cudaError_t launch_tc_forward(const void *q, const void *k, const void *v, const float *G,
-                              const float *Bt, const float *h0, void *out, float *hT, Plan plan,
+                              const void *beta, const float *h0, void *out, float *hT, Plan plan,
                               int H, int64_t T_total, int64_t max_chunks, void *scratch,
                               int *status, cudaStream_t stream) {
     (void)max_chunks;
@@ -1090,7 +1090,7 @@ cudaError_t launch_tc_forward(const void *q, const void *k, const void *v, const
     const size_t per = ((size_t)nseg * H * kD * kD * sizeof(float) + 255) / 256 * 256;
     TcArgs a{};
     a.G = G;
-    a.Bt = Bt;
+    a.beta = (const __nv_bfloat16 *)beta;
     a.h0 = h0;
     a.out = out;
     a.hT = hT;
@@ -1117,7 +1117,8 @@ cudaError_t launch_tc_forward(const void *q, const void *k, const void *v, const
         ProfScope prof(stream, "tc_horizon_kernel");
         const int64_t nslots = nseg * H;   // one warp each
         tc_horizon_kernel<<<(unsigned)((nslots + 3) / 4), 128, 0, stream>>>(
-            G, Bt, (const __nv_bfloat16 *)k, plan, H, T_total, nslots, first, mneed, truncate);
+            G, (const __nv_bfloat16 *)beta, (const __nv_bfloat16 *)k, plan, H, T_total, nslots, first, mneed,
+            truncate);
         count_launch();
     }
     cudaError_t err = cudaFuncSetAttribute(tc_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

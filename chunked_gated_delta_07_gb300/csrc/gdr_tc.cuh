@@ -13,12 +13,13 @@ bool tc_supported(gdr_dtype_t dtype, int dk, int dv, int chunk);
 // Tiles per segment for the segment-parallel state pass.
 int tc_segment_chunks(int N, int H, int64_t T_total, int C, bool varlen);
 
-// Scratch bytes of the tensor-core path beyond the plan, G and Bt.
+// Scratch bytes of the tensor-core path beyond the plan and G.
 size_t tc_workspace_bytes(int N, int H, int64_t T_total, int C, bool varlen);
 
-// Stages 2-4 on the tensor cores (stage 1, plan and G/Bt already enqueued).
+// Stages 2-4 on the tensor cores (stage 1 and the plan already enqueued; beta is read
+// as given, [rows][H] bf16).
 cudaError_t launch_tc_forward(const void *q, const void *k, const void *v, const float *G,
-                              const float *Bt, const float *h0, void *out, float *hT, Plan plan,
+                              const void *beta, const float *h0, void *out, float *hT, Plan plan,
                               int H, int64_t T_total, int64_t max_chunks, void *scratch,
                               int *status, cudaStream_t stream);
 
