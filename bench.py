@@ -65,6 +65,31 @@ def algorithmic(w, n_tokens, with_h0):
     return byt, flops, per_tok
 
 
+def kernel_breakdown(gdr, torch, step, n=2):
+    """Per-kernel device times over n untimed steps with every launch bracketed by
+    events: ({kernel: (ms_total, launches)}, name of the largest).  The timed region
+    that follows brackets the launches of that one kernel only, so that no events sit
+    between the step's other launches."""
+    gdr.gdr_profile_select(None)
+    gdr.gdr_profile_read()
+    gdr.gdr_profile_enable(True)
+    for _ in range(n):
+        step()
+    torch.cuda.synchronize()
+    gdr.gdr_profile_enable(False)
+    prof = gdr.gdr_profile_read()
+    dom = max(prof.items(), key=lambda kv: kv[1][0])[0] if prof else None
+    return prof, dom
+
+
+def kernels_json(prof, n):
+    return {k: {"ms_per_step": v[0] / n, "launches_per_step": v[1] / n} for k, v in prof.items()}
+
+
+KERNELS_NOTE = ("per-kernel times from 2 untimed steps with every launch bracketed by events; "
+                "the timed region brackets the dominant kernel's launches only")
+
+
 def source_hash(path):
     with open(path, "rb") as f:
         return hashlib.sha1(f.read()).hexdigest()[:12]
@@ -419,6 +444,8 @@ def main(argv=None):
     # (a buffer of twice its size written) between steps, outside the timed steps.
     in_bytes = sum(t.numel() * t.element_size() for t in (x["q"], x["k"], x["v"], x["a"], x["beta"]))
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if in_bytes < 2 * L2_BYTES else None
+    breakdown, dom_sel = kernel_breakdown(gdr, torch, step)
+    gdr.gdr_profile_select(dom_sel)
     gdr.gdr_profile_read()           # drop anything recorded so far
     gdr.gdr_profile_enable(True)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -442,6 +469,7 @@ def main(argv=None):
         torch.cuda.synchronize()
         n_launch = gdr.gdr_launch_count() - n_launch0
     gdr.gdr_profile_enable(False)
+    gdr.gdr_profile_select(None)
     ms = sum(e0.elapsed_time(e1) for e0, e1 in evs)
     ms = max_over_ranks(ms, dist, dev)
     if dist:
@@ -474,7 +502,8 @@ def main(argv=None):
                 "peak_source": f"{peak_src} hbm_gbs",
                 "algorithmic_bytes_per_unit": per_tok, "units_per_launch": units,
                 "kernel_avg_ms": dom_avg_s * 1e3,
-                "kernel_share": dom_ms / sum(v[0] for v in prof.values()) if prof else None}
+                "kernel_share": (breakdown[dom_name][0] / sum(v[0] for v in breakdown.values())
+                                 if dom_name in breakdown else None)}
 
     # ---- end to end through the host-buffer entry point ----
     e2e = None
@@ -498,7 +527,7 @@ def main(argv=None):
             "step_roofline": {"t_roof_ms": t_roof * 1e3, "bytes": byt, "flops": flops,
                               "hbm_gbs": hbm, "bf16_tflops": tf_sust, "peak_source": peak_src},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_launch,
-            "kernels": {k: {"ms_total": v[0], "launches": v[1]} for k, v in prof.items()},
+            "kernels": kernels_json(breakdown, 2), "kernels_note": KERNELS_NOTE,
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
@@ -601,6 +630,8 @@ def bench_backward(args):
         step()
     torch.cuda.synchronize()
     steps = max(args.steps, 3)
+    breakdown, dom_sel = kernel_breakdown(gdr, torch, step)
+    gdr.gdr_profile_select(dom_sel)
     gdr.gdr_profile_read()
     gdr.gdr_profile_enable(True)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -613,6 +644,7 @@ def bench_backward(args):
         torch.cuda.synchronize()
         n_launch = gdr.gdr_launch_count() - n0
     gdr.gdr_profile_enable(False)
+    gdr.gdr_profile_select(None)
     prof = gdr.gdr_profile_read()
     st = gdr.gdr_get_status(stream)
     if st != gdr.GDR_OK:
@@ -653,9 +685,10 @@ def bench_backward(args):
                      "frac": achieved / peak, "traffic": None, "kernel": "whole step",
                      "peak_source": f"{peak_src} bf16_tflops x 0.5 (tf32)",
                      "algorithmic_flops_per_step": flops, "dominant_kernel": dom_name,
-                     "dominant_share": dom_ms / sum(v[0] for v in prof.values()) if prof else None},
+                     "dominant_share": (breakdown[dom_name][0] / sum(v[0] for v in breakdown.values())
+                                        if dom_name in breakdown else None)},
         "roofline_bytes": bytes_roof,
-        "kernels": {k: {"ms_total": v[0], "launches": v[1]} for k, v in prof.items()},
+        "kernels": kernels_json(breakdown, 2), "kernels_note": KERNELS_NOTE,
         "cpu_baseline": cpu, "gpu_launches": n_launch, "clocks": summ or None,
     }), flush=True)
 
@@ -686,6 +719,8 @@ def bench_vec(args, w):
         step()
     torch.cuda.synchronize()
     steps = max(args.steps, 3)
+    breakdown, dom_sel = kernel_breakdown(gdr, torch, step)
+    gdr.gdr_profile_select(dom_sel)
     gdr.gdr_profile_read()
     gdr.gdr_profile_enable(True)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -698,6 +733,7 @@ def bench_vec(args, w):
         torch.cuda.synchronize()
         n_launch = gdr.gdr_launch_count() - n0
     gdr.gdr_profile_enable(False)
+    gdr.gdr_profile_select(None)
     prof = gdr.gdr_profile_read()
     st = gdr.gdr_get_status(stream)
     if st != gdr.GDR_OK:
@@ -723,8 +759,9 @@ def bench_vec(args, w):
                      "frac": achieved / hbm, "traffic": None, "kernel": "whole step",
                      "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_step": byt,
                      "dominant_kernel": dom_name, "dominant_share":
-                         dom_ms / sum(v[0] for v in prof.values()) if prof else None},
-        "kernels": {k: {"ms_total": v[0], "launches": v[1]} for k, v in prof.items()},
+                         (breakdown[dom_name][0] / sum(v[0] for v in breakdown.values())
+                          if dom_name in breakdown else None)},
+        "kernels": kernels_json(breakdown, 2), "kernels_note": KERNELS_NOTE,
         "cpu_baseline": cpu, "gpu_launches": n_launch, "clocks": clk.summary(),
     }), flush=True)
 
@@ -758,6 +795,8 @@ def bench_router(args):
         step()
     torch.cuda.synchronize()
     steps = max(args.steps, 10)
+    breakdown, _ = kernel_breakdown(gdr, torch, step)
+    gdr.gdr_profile_select("router_topk_kernel")
     gdr.gdr_profile_read()
     gdr.gdr_profile_enable(True)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -770,6 +809,7 @@ def bench_router(args):
         torch.cuda.synchronize()
         n_launch = gdr.gdr_launch_count() - n0
     gdr.gdr_profile_enable(False)
+    gdr.gdr_profile_select(None)
     prof = gdr.gdr_profile_read()
     ms = ev0.elapsed_time(ev1) / steps
     kern_total, kern_n = prof.get("router_topk_kernel", (0.0, 1))
@@ -791,7 +831,7 @@ def bench_router(args):
                      "frac": achieved / hbm, "traffic": None, "kernel": "router_topk_kernel",
                      "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": byt,
                      "kernel_ms": kern_ms},
-        "kernels": {kk: {"ms_total": v[0], "launches": v[1]} for kk, v in prof.items()},
+        "kernels": kernels_json(breakdown, 2), "kernels_note": KERNELS_NOTE,
         "cpu_baseline": cpu, "gpu_launches": n_launch, "clocks": clk.summary(),
     }), flush=True)
 

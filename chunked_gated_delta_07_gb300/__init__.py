@@ -29,7 +29,7 @@ GDR_PATH_AUTO, GDR_PATH_SIMT, GDR_PATH_TC = 0, 1, 2
 EXPORTS = ("gdr_chunk_fwd", "gdr_chunk_fwd_ex", "gdr_chunk_fwd_workspace_size",
            "gdr_chunk_fwd_host", "gdr_gate_cumsum", "gdr_wy_repr", "gdr_get_status",
            "gdr_status_string", "gdr_release", "gdr_launch_count", "gdr_profile_enable",
-           "gdr_profile_read", "gdr_chunk_fwd_noalloc", "gdr_recurrent_fwd", "gdr_chunk_bwd", "gdr_chunk_fwd_vec",
+           "gdr_profile_read", "gdr_profile_select", "gdr_chunk_fwd_noalloc", "gdr_recurrent_fwd", "gdr_chunk_bwd", "gdr_chunk_fwd_vec",
            "gdr_router_topk", "gdr_router_bias_update", "gdr_chunk_bwd_vec")
 
 _lock = threading.Lock()
@@ -49,6 +49,7 @@ _SIGS = {
     "gdr_launch_count": (ctypes.c_uint64, []),
     "gdr_profile_enable": (None, [_I]),
     "gdr_profile_read": (_I, [_P, _P, _P, _I]),
+    "gdr_profile_select": (None, [ctypes.c_char_p]),
     "gdr_chunk_fwd_noalloc": (_I, [_P] * 8 + [_I, _I64, _I, _I, _I, _I, _F, _I, _I, _P]),
     "gdr_recurrent_fwd": (_I, [_P] * 7 + [_I, _I64, _I, _I, _I, _F, _I, _I, _P]),
     "gdr_chunk_bwd": (_I, [_P] * 15 + [_I, _I64, _I, _I, _I, _I, _F, _I, _I, _P]),
@@ -317,6 +318,11 @@ def gdr_launch_count() -> int:
 
 def gdr_profile_enable(on: bool) -> None:
     lib().gdr_profile_enable(1 if on else 0)
+
+
+def gdr_profile_select(name) -> None:
+    """Time only the launches of kernel `name` (None: every kernel)."""
+    lib().gdr_profile_select(None if name is None else name.encode())
 
 
 def gdr_profile_read(max_kernels: int = 32) -> dict:

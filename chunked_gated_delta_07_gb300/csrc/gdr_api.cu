@@ -7,6 +7,7 @@
 #include <cstring>
 #include <deque>
 #include <mutex>
+#include <string>
 #include <vector>
 
 #include "gdr_internal.cuh"
@@ -43,6 +44,7 @@ struct ProfRec {
 };
 std::mutex g_prof_mu;
 std::atomic<bool> g_prof_on{false};
+std::string g_prof_only;   // record only launches of this kernel ("" = all); guarded by g_prof_mu
 std::vector<ProfRec> g_prof;
 std::vector<cudaEvent_t> g_prof_pool;
 
@@ -61,6 +63,7 @@ cudaEvent_t prof_event() {
 ProfScope::ProfScope(cudaStream_t stream, const char *name) : stream_(stream), slot_(-1) {
     if (!g_prof_on.load(std::memory_order_relaxed)) return;
     std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (!g_prof_only.empty() && g_prof_only != name) return;
     ProfRec r{name, prof_event(), prof_event()};
     if (!r.start || !r.stop) return;
     cudaEventRecord(r.start, stream_);
@@ -1000,6 +1003,11 @@ void gdr_release(void) {
 uint64_t gdr_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 void gdr_profile_enable(int on) { g_prof_on.store(on != 0); }
+
+void gdr_profile_select(const char *name) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof_only = name ? name : "";
+}
 
 int gdr_profile_read(const char **names, double *total_ms, int *launches, int max) {
     std::lock_guard<std::mutex> lk(g_prof_mu);

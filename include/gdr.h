@@ -389,6 +389,10 @@ GDR_API uint64_t gdr_launch_count(void);
  */
 GDR_API void gdr_profile_enable(int on);
 GDR_API int gdr_profile_read(const char **names, double *total_ms, int *launches, int max);
+/* Restrict the timing to the launches of one kernel, named as gdr_profile_read
+ * reports it (NULL or "": every kernel, the default), so that a measurement of
+ * that kernel puts no events between the other launches.  The name is copied. */
+GDR_API void gdr_profile_select(const char *name);
 
 #ifdef __cplusplus
 }
