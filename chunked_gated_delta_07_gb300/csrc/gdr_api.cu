@@ -738,8 +738,8 @@ static gdr_status_t chunk_bwd_impl(const void *q, const void *k, const void *v, 
         return GDR_ERR_CUDA;
     if (chunked)
         return launch_chunk_bwd(q, k, v, a, beta, h0, dout, dhT, dq, dk_out, dv_out, da, dbeta, dh0,
-                                plan, H, tiles, segs, b, per_channel, ws + plan_b, stream,
-                                aux_stream(ctx)) == cudaSuccess
+                                plan, H, s.T_total, tiles, segs, b, per_channel, ws + plan_b,
+                                ctx->d_status, stream, aux_stream(ctx)) == cudaSuccess
                    ? GDR_OK
                    : GDR_ERR_CUDA;
     return launch_bwd(q, k, v, a, beta, h0, dout, dhT, dq, dk_out, dv_out, da, dbeta, dh0, dtype,

@@ -22,7 +22,8 @@
 //   bwd_fwd_chain_kernel  per (segment, head): the state chain (state in registers);
 //                         stores H0 and D of every tile
 //   bwd_adj_chain_kernel  per (segment, head), tiles in reverse: the dH chain (state in
-//                         shared memory); stores dH1 of every tile, and dh0
+//                         shared memory); stores X = diag(e^{G_C}) dH1 of every tile, and dh0
+//                         (tc_adj_kernel in gdr_tc_adj.cu is the same chain on tcgen05)
 //   bwd_tile_kernel       per (tile, head), all tiles at once: every input gradient
 // The scalar-gate form is the per-channel form with every channel's gate equal.
 //
@@ -36,6 +37,9 @@
 // head) pair without such a warm-up within 4 S tiles of every segment
 // boundary runs as one block, as without segments (bwd_decide_kernel).
 // The stored states are bf16 (they only feed the per-tile products).
+#include <cstdlib>
+
+#include "gdr_bwd_chunk.cuh"
 #include "gdr_internal.cuh"
 #include "gdr_mma.cuh"
 
@@ -50,22 +54,14 @@ constexpr int kThreads = 256;
 constexpr int kTile2 = kT * kLd;   // floats of one [16][kLd] buffer
 constexpr int kSegMin = 64, kSegMax = 256;   // segment lengths in tiles
 constexpr int kWarmFactor = 4;   // longest warm-up, in segments
-constexpr float kHorizonLog = -46.0f;   // below ln(2^-64) = -44.4, with room for fp32 sums
 constexpr int kLdh = 136;               // row stride (elements) of the bf16 state in shared memory
 
-struct BcArgs {
-    const __nv_bfloat16 *q, *k, *v, *a, *beta, *dout;
-    const float *h0, *dhT;
-    __nv_bfloat16 *dq, *dk, *dv, *da, *dbeta;
-    float *dh0;
-    __nv_bfloat16 *Hst, *dHst;   // [tiles][H][128][128]: entering state, end gradient
-    float *Dst;                  // [tiles][H][16][128]
-    const float *lam;            // [tiles][H]: log bound of each tile's transition
-    const int *seg_ok;           // [N][H]: 1 if the pair runs in segments
-    Plan p;
-    int H;
-    float b;
-};
+using bwdc::BcArgs;
+using bwdc::kHorizonLog;
+using bwdc::segment_of;
+using bwdc::warm_walk;
+
+
 
 template <bool VEC>
 __device__ __forceinline__ float gate_in(const __nv_bfloat16 *a, int64_t row, int d) {
@@ -306,13 +302,19 @@ __device__ __forceinline__ void copy_state_out(const float *Hs, float *dst) {
     }
 }
 
-// bf16 copy of the fp32 state by threads [first, kThreads)
-__device__ __forceinline__ void copy_state_out_h(const float *Hs, __nv_bfloat16 *dst, int first = 0) {
+// bf16 copy of the fp32 state by threads [first, kThreads), row r scaled by rs[r]
+__device__ __forceinline__ void copy_state_out_h(const float *Hs, __nv_bfloat16 *dst, const float *rs,
+                                                 int first = 0) {
     if ((int)threadIdx.x < first) return;
     const int n = kThreads - first;
     for (int e = ((int)threadIdx.x - first) * 4; e < kD * kD; e += n * 4) {
         const int r = e >> 7, c = e & (kD - 1);
-        const float4 x = *(const float4 *)&Hs[r * kLd + c];
+        float4 x = *(const float4 *)&Hs[r * kLd + c];
+        const float sr = rs[r];
+        x.x *= sr;
+        x.y *= sr;
+        x.z *= sr;
+        x.w *= sr;
         __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y), hi = __floats2bfloat162_rn(x.z, x.w);
         uint2 u;
         u.x = *(uint32_t *)&lo;
@@ -397,58 +399,6 @@ bwd_decide_kernel(const float *__restrict__ lam, int *__restrict__ ok, Plan p, i
         good = (B <= max_warm || before <= kHorizonLog) && (B + max_warm >= nt || after <= kHorizonLog);
     }
     if (lane == 0) ok[(int64_t)n * H + h] = good;
-}
-
-// Warp-wide walk over the per-tile log bounds from tile `from` of a sequence with
-// `nt` tiles: backwards (dir < 0) to the latest start w <= from whose tiles
-// [w, from) sum to <= e^-46, or 0; forwards (dir > 0) to the earliest end
-// e >= from whose tiles [from, e) do, or nt.
-__device__ __forceinline__ int64_t warm_walk(const float *lam, int64_t tile0, int64_t nt, int H, int h,
-                                             int64_t from, int dir) {
-    const int lane = threadIdx.x & 31;
-    int64_t w = from;
-    float acc = 0.f;
-    bool done = dir < 0 ? from == 0 : from >= nt;
-    while (!done) {
-        const int64_t i = dir < 0 ? w - 1 - lane : w + lane;
-        const bool in = i >= 0 && i < nt;
-        float x = in ? lam[(tile0 + i) * H + h] : 0.f;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
-        }
-        const unsigned hit = __ballot_sync(0xffffffffu, in && acc + x <= kHorizonLog);
-        if (hit) {
-            const int l = __ffs(hit) - 1;
-            w = dir < 0 ? w - 1 - l : w + 1 + l;
-            done = true;
-        } else {
-            acc += __shfl_sync(0xffffffffu, x, 31);
-            w = dir < 0 ? max(w - 32, (int64_t)0) : min(w + 32, nt);
-            done = dir < 0 ? w == 0 : w == nt;
-        }
-    }
-    return w;
-}
-
-// Segment of block `sg` (global segment index): sequence n and tiles [s0, s1);
-// false when the block has nothing to do.
-__device__ __forceinline__ bool segment_of(const BcArgs &A, int64_t sg, int h, int &n, int64_t &s0,
-                                           int64_t &s1) {
-    n = find_owner(A.p.seg_base, A.p.N, sg);
-    if (n < 0) return false;
-    const int64_t nt = A.p.chunk_base[n + 1] - A.p.chunk_base[n];
-    const int64_t j = sg - A.p.seg_base[n];
-    if (A.seg_ok[(int64_t)n * A.H + h]) {
-        s0 = j * A.p.seg_chunks;
-        s1 = min(nt, s0 + (int64_t)A.p.seg_chunks);
-    } else {
-        if (j > 0) return false;
-        s0 = 0;
-        s1 = nt;
-    }
-    return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -593,7 +543,7 @@ bwd_fwd_chain_kernel(const BcArgs A) {
 }
 
 // ---------------------------------------------------------------------------
-// adjoint state chain, tiles in reverse: stores dH1 of every tile, writes dh0
+// adjoint state chain, tiles in reverse: stores X = diag(e^{G_C}) dH1 of every tile, writes dh0
 // ---------------------------------------------------------------------------
 constexpr int kA_H = 0, kA_Kt = kA_H + kD * kLd, kA_Kh = kA_Kt + kTile2, kA_Qt = kA_Kh + kTile2,
               kA_O = kA_Qt + kTile2, kA_E = kA_O + kTile2, kA_A = kA_E + kTile2,
@@ -631,7 +581,7 @@ bwd_adj_chain_kernel(const BcArgs A) {
         __syncthreads();
         if (warp < 2) build_A(Kt, Kh, bs, Am, nullptr, warp, g, t);
         else if (warp < 4) build_lower(Qt, Kh, Sm, warp - 2, g, t);
-        else if (tt < s1) copy_state_out_h(dH, A.dHst + ((size_t)c * A.H + h) * kD * kD, 128);
+        else if (tt < s1) copy_state_out_h(dH, A.dHst + ((size_t)c * A.H + h) * kD * kD, eg, 128);   // X
         __syncthreads();
         if (tid < kD) {
             fwd_subst(Kt, tid, Am, bs);   // Kt -> W
@@ -792,7 +742,7 @@ bwd_tile_kernel(const BcArgs A) {
     }
     cp_async_wait_all();
     __syncthreads();
-    // ---- Ke dH1 (this warp's dv columns) and dKe = D dH1^T (this warp's dk columns),
+    // ---- Ke dH1 = Kh X (this warp's dv columns) and dKe (.) e^{G_C} = D X^T (this warp's dk columns),
     // then the 16 x 16 products
     float dke[2][4], dd[2][4];
 #pragma unroll
@@ -802,21 +752,22 @@ bwd_tile_kernel(const BcArgs A) {
 #pragma unroll 2
     for (int k0 = 0; k0 < kD; k0 += 8) {
         uint32_t ak[4], ad[4];
-        ak[0] = tf32(Kh[g * kLd + k0 + t] * eg[k0 + t]);   // Ke = Kh (.) e^{G_C}
-        ak[1] = tf32(Kh[(g + 8) * kLd + k0 + t] * eg[k0 + t]);
-        ak[2] = tf32(Kh[g * kLd + k0 + t + 4] * eg[k0 + t + 4]);
-        ak[3] = tf32(Kh[(g + 8) * kLd + k0 + t + 4] * eg[k0 + t + 4]);
+        ak[0] = tf32(Kh[g * kLd + k0 + t]);   // Ke dH1 = Kh X
+        ak[1] = tf32(Kh[(g + 8) * kLd + k0 + t]);
+        ak[2] = tf32(Kh[g * kLd + k0 + t + 4]);
+        ak[3] = tf32(Kh[(g + 8) * kLd + k0 + t + 4]);
         load_a(ad, Db, kLd, 0, k0, g, t);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             uint32_t b0, b1;
-            load_b_h(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);    // dH1[k][c]
+            load_b_h(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);    // X[k][c]
             mma8(dd[nt], ak, b0, b1);
-            load_bt_h(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);   // dH1^T[k][d] = dH1[d][k]
+            load_bt_h(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);   // X^T[k][d] = X[d][k]
             mma8(dke[nt], ad, b0, b1);
         }
     }
-    // e^{G_C} rowsum(dH1 (.) H0): dH1 from shared memory, H0 rows from the stored copy
+    // e^{G_C} rowsum(dH1 (.) H0) = rowsum(X (.) H0): X from shared memory, H0 rows from
+    // the stored copy
     {
         const __nv_bfloat16 *H0g = A.Hst + st;
         uint2 xh[kD / 8];
@@ -832,7 +783,7 @@ bwd_tile_kernel(const BcArgs A) {
             float pr = xa.x * ya.x + xa.y * ya.y + xb.x * yb.x + xb.y * yb.y;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) pr += __shfl_xor_sync(0xffffffffu, pr, o);
-            if (lane == 0) rG[r] = eg[r] * pr;
+            if (lane == 0) rG[r] = pr;
         }
     }
     if (warp < 2) build_A(Kt, Kh, bs, Am, KK, warp, g, t);
@@ -995,7 +946,7 @@ bwd_tile_kernel(const BcArgs A) {
                 const int i = g + 8 * (u >> 1), d = c0 + 8 * nt + 2 * t + (u & 1);
                 const float kt = Kt[i * kLd + d], kh = Kh[i * kLd + d], qt = Qt[i * kLd + d];
                 const float dKt = dkt[nt][u] + bs[i] * Db[i * kLd + d];
-                const float dKh = dkh[nt][u] + dke[nt][u] * eg[d];
+                const float dKh = dkh[nt][u] + dke[nt][u];   // dke = D X^T = dKe (.) e^{G_C}
                 Ob[i * kLd + d] = dq[nt][u] * qt + dKt * kt - dKh * kh;
                 if (i < len) {
                     const float G = VEC ? Gb[i * kLd + d] : Gb[i];
@@ -1003,7 +954,7 @@ bwd_tile_kernel(const BcArgs A) {
                     A.dq[r] = __float2bfloat16_rn(dq[nt][u] * expf(G));
                     A.dk[r] = __float2bfloat16_rn(dKt * expf(G) + dKh * expf(-G));
                 }
-                dke[nt][u] *= kh * eg[d];   // dKe (.) Ke, summed over the tile below
+                dke[nt][u] *= kh;   // dKe (.) Ke, summed over the tile below
             }
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
@@ -1060,9 +1011,15 @@ bwd_tile_kernel(const BcArgs A) {
     }
 }
 
+// GDR_BWD_ADJ_MMA=1 runs the adjoint chain on the mma.sync kernel (for comparisons).
+bool adj_use_mma_sync() {
+    const char *e = std::getenv("GDR_BWD_ADJ_MMA");
+    return e && e[0] == '1';
+}
+
 template <bool VEC>
-cudaError_t run_chunk_bwd(const BcArgs &A, int64_t max_tiles, int64_t max_segs, float *lam, int *ok,
-                          cudaStream_t stream, const AuxStream &aux) {
+cudaError_t run_chunk_bwd(const BcArgs &A, int64_t T_total, int64_t max_tiles, int64_t max_segs, float *lam,
+                          int *ok, int *status, cudaStream_t stream, const AuxStream &aux) {
     cudaError_t err;
     const int H = A.H;
     auto kf = bwd_fwd_chain_kernel<VEC>;
@@ -1095,11 +1052,18 @@ cudaError_t run_chunk_bwd(const BcArgs &A, int64_t max_tiles, int64_t max_segs, 
         if ((err = cudaStreamWaitEvent(aux.stream, aux.fork, 0)) != cudaSuccess) return err;
     }
     {
+        // the adjoint chain on tcgen05 unless a tensor map cannot be made (or the
+        // mma.sync chain is asked for)
         cudaStream_t sa_stream = fork ? aux.stream : stream;
-        ProfScope prof(sa_stream, "bwd_adj_chain_kernel");
-        ka<<<(unsigned)segs, kThreads, sa, sa_stream>>>(A);
-        count_launch();
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        err = adj_use_mma_sync() ? cudaErrorNotSupported
+                                 : launch_tc_adj(A, VEC, T_total, max_tiles, max_segs, status, sa_stream);
+        if (err == cudaErrorNotSupported) {
+            ProfScope prof(sa_stream, "bwd_adj_chain_kernel");
+            ka<<<(unsigned)segs, kThreads, sa, sa_stream>>>(A);
+            count_launch();
+            err = cudaGetLastError();
+        }
+        if (err != cudaSuccess) return err;
     }
     if (fork && (err = cudaEventRecord(aux.join, aux.stream)) != cudaSuccess) return err;
     {
@@ -1136,8 +1100,8 @@ size_t chunk_bwd_scratch_bytes(int64_t tiles, int N, int H) {
 cudaError_t launch_chunk_bwd(const void *q, const void *k, const void *v, const void *a,
                              const void *beta, const float *h0, const void *dout, const float *dhT,
                              void *dq, void *dk, void *dv, void *da, void *dbeta, float *dh0,
-                             Plan plan, int H, int64_t max_tiles, int64_t max_segs, float b,
-                             bool per_channel, void *scratch, cudaStream_t stream,
+                             Plan plan, int H, int64_t T_total, int64_t max_tiles, int64_t max_segs,
+                             float b, bool per_channel, void *scratch, int *status, cudaStream_t stream,
                              const AuxStream &aux) {
     if (plan.C != kT || plan.seg_chunks < kSegMin || plan.seg_chunks > kSegMax) return cudaErrorInvalidValue;
     auto al = [](size_t x) { return (x + 255) / 256 * 256; };
@@ -1172,8 +1136,8 @@ cudaError_t launch_chunk_bwd(const void *q, const void *k, const void *v, const 
     A.p = plan;
     A.H = H;
     A.b = b;
-    return per_channel ? run_chunk_bwd<true>(A, max_tiles, max_segs, lam, ok, stream, aux)
-                       : run_chunk_bwd<false>(A, max_tiles, max_segs, lam, ok, stream, aux);
+    return per_channel ? run_chunk_bwd<true>(A, T_total, max_tiles, max_segs, lam, ok, status, stream, aux)
+                       : run_chunk_bwd<false>(A, T_total, max_tiles, max_segs, lam, ok, status, stream, aux);
 }
 
 }  // namespace gdr

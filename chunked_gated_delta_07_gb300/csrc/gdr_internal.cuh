@@ -181,8 +181,8 @@ size_t chunk_bwd_scratch_bytes(int64_t tiles, int N, int H);
 cudaError_t launch_chunk_bwd(const void *q, const void *k, const void *v, const void *a,
                              const void *beta, const float *h0, const void *dout, const float *dhT,
                              void *dq, void *dk, void *dv, void *da, void *dbeta, float *dh0,
-                             Plan plan, int H, int64_t max_tiles, int64_t max_segs, float b,
-                             bool per_channel, void *scratch, cudaStream_t stream,
+                             Plan plan, int H, int64_t T_total, int64_t max_tiles, int64_t max_segs,
+                             float b, bool per_channel, void *scratch, int *status, cudaStream_t stream,
                              const AuxStream &aux);
 
 // quantile-balancing router-bias update (gdr_router.cu)

@@ -100,3 +100,18 @@ def test_vec_backward_rejects_what_it_does_not_cover():
     assert gdr.gdr_chunk_bwd_vec(*base, 16, 6.0, gdr.GDR_BF16) == gdr.GDR_ERR_UNSUPPORTED
     assert gdr.gdr_chunk_bwd_vec(*base, 16, 2.0, gdr.GDR_F32) == gdr.GDR_ERR_UNSUPPORTED
     assert gdr.gdr_chunk_bwd_vec(*base, 16, -1.0, gdr.GDR_BF16) == gdr.GDR_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("T,a_mean", [(2500, 0.0), (600, -6.0)])
+def test_vec_adjoint_chain_kernels_agree(monkeypatch, T, a_mean):
+    """Per-channel decay: the adjoint chain on tcgen05 (the default) and on mma.sync
+    (GDR_BWD_ADJ_MMA=1) both match the oracle and agree with each other."""
+    x = _inputs(T, seed=7400 + T, N=2, H=2, a_mean=a_mean)
+    tc, ref = _run(x)
+    monkeypatch.setenv("GDR_BWD_ADJ_MMA", "1")
+    mma, _ = _run(x)
+    _check(tc, ref)
+    _check(mma, ref)
+    for name in NAMES:
+        r = rel_l2(to64(tc[name]), to64(mma[name]))
+        assert r <= 1e-2, f"{name}: tcgen05 vs mma.sync adjoint chain rel-L2 {r:.3e}"
