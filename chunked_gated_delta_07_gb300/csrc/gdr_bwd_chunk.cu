@@ -20,7 +20,8 @@
 //   dq = dQt (.) e^G,  dk = dKt (.) e^G + dKh (.) e^-G,  da = dg g'(a)
 // Three kernels:
 //   bwd_fwd_chain_kernel  per (segment, head): the state chain (state in registers);
-//                         stores H0 and D of every tile
+//                         stores H0 and D of every tile (tc_fwd_chain_kernel in
+//                         gdr_tc_fwd_chain.cu is the same chain on tcgen05)
 //   bwd_adj_chain_kernel  per (segment, head), tiles in reverse: the dH chain (state in
 //                         shared memory); stores X = diag(e^{G_C}) dH1 of every tile, and dh0
 //                         (tc_adj_kernel in gdr_tc_adj.cu is the same chain on tcgen05)
@@ -1011,9 +1012,10 @@ bwd_tile_kernel(const BcArgs A) {
     }
 }
 
-// GDR_BWD_ADJ_MMA=1 runs the adjoint chain on the mma.sync kernel (for comparisons).
-bool adj_use_mma_sync() {
-    const char *e = std::getenv("GDR_BWD_ADJ_MMA");
+// GDR_BWD_ADJ_MMA=1 / GDR_BWD_FWD_MMA=1 run the adjoint / forward state chain on the
+// mma.sync kernel (for comparisons).
+bool env_on(const char *name) {
+    const char *e = std::getenv(name);
     return e && e[0] == '1';
 }
 
@@ -1055,7 +1057,7 @@ cudaError_t run_chunk_bwd(const BcArgs &A, int64_t T_total, int64_t max_tiles, i
         // the adjoint chain on tcgen05 unless a tensor map cannot be made (or the
         // mma.sync chain is asked for)
         cudaStream_t sa_stream = fork ? aux.stream : stream;
-        err = adj_use_mma_sync() ? cudaErrorNotSupported
+        err = env_on("GDR_BWD_ADJ_MMA") ? cudaErrorNotSupported
                                  : launch_tc_adj(A, VEC, T_total, max_tiles, max_segs, status, sa_stream);
         if (err == cudaErrorNotSupported) {
             ProfScope prof(sa_stream, "bwd_adj_chain_kernel");
@@ -1067,10 +1069,15 @@ cudaError_t run_chunk_bwd(const BcArgs &A, int64_t T_total, int64_t max_tiles, i
     }
     if (fork && (err = cudaEventRecord(aux.join, aux.stream)) != cudaSuccess) return err;
     {
-        ProfScope prof(stream, "bwd_fwd_chain_kernel");
-        kf<<<(unsigned)segs, kThreads, sf, stream>>>(A);
-        count_launch();
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        err = env_on("GDR_BWD_FWD_MMA") ? cudaErrorNotSupported
+                                        : launch_tc_fwd_chain(A, VEC, T_total, max_tiles, max_segs, status, stream);
+        if (err == cudaErrorNotSupported) {
+            ProfScope prof(stream, "bwd_fwd_chain_kernel");
+            kf<<<(unsigned)segs, kThreads, sf, stream>>>(A);
+            count_launch();
+            err = cudaGetLastError();
+        }
+        if (err != cudaSuccess) return err;
     }
     if (fork && (err = cudaStreamWaitEvent(stream, aux.join, 0)) != cudaSuccess) return err;
     if (max_tiles > 0) {

@@ -90,4 +90,9 @@ __device__ __forceinline__ bool segment_of(const BcArgs &A, int64_t sg, int h, i
 cudaError_t launch_tc_adj(const bwdc::BcArgs &A, bool per_channel, int64_t T_total, int64_t max_tiles,
                           int64_t max_segs, int *status, cudaStream_t stream);
 
+// The forward state chain on tcgen05 (gdr_tc_fwd_chain.cu), a drop-in for
+// bwd_fwd_chain_kernel, with the same fallback rule.
+cudaError_t launch_tc_fwd_chain(const bwdc::BcArgs &A, bool per_channel, int64_t T_total, int64_t max_tiles,
+                                int64_t max_segs, int *status, cudaStream_t stream);
+
 }  // namespace gdr

@@ -39,6 +39,7 @@
 #include "gdr_bwd_chunk.cuh"
 #include "gdr_sm100.cuh"
 #include "gdr_tc.cuh"
+#include "gdr_tc_prep.cuh"
 
 namespace gdr {
 
@@ -47,6 +48,7 @@ GDR_DEBUG_TU()
 namespace {
 
 using namespace sm100;
+using namespace tcp;
 using bwdc::BcArgs;
 
 constexpr int kD = 128;          // dk = dv
@@ -105,40 +107,6 @@ __device__ __forceinline__ uint32_t tile_off(int row, int col) {
 // groups at 128 B)
 __device__ __forceinline__ uint32_t st_off(int n, int k) {
     return core_off((uint32_t)n, (uint32_t)k * 2u, (kC / 8) * 128u, 128u);
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-__device__ __forceinline__ float2 unpack_bf16(uint32_t x) {
-    return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
-}
-// sigma(a) on the hardware exp2 and reciprocal approximations (relative error ~1e-7)
-__device__ __forceinline__ float fast_sigmoid(float a) { return __fdividef(1.f, 1.f + __expf(-a)); }
-
-__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9},"
-        " {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 template <bool VEC>

@@ -43,6 +43,7 @@
 
 #include "gdr_sm100.cuh"
 #include "gdr_tc.cuh"
+#include "gdr_tc_prep.cuh"
 
 namespace gdr {
 
@@ -51,6 +52,7 @@ GDR_DEBUG_TU()
 namespace {
 
 using namespace sm100;
+using namespace tcp;
 
 constexpr int kD = 128;          // dk = dv
 constexpr int kC = 16;           // tile length
@@ -125,39 +127,6 @@ struct TvArgs {
     int *status;
     uint64_t wait_ns;    // limit of every pipeline wait
 };
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-__device__ __forceinline__ float2 unpack_bf16(uint32_t x) {
-    return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
-}
-
-// sigma(a) = 1 / (1 + e^-a) on the hardware exp2 and reciprocal approximations
-// (relative error ~1e-7; a << 0 gives e^-a = inf and sigma = 0)
-__device__ __forceinline__ float fast_sigmoid(float a) { return __fdividef(1.f, 1.f + __expf(-a)); }
-
-// two fp32 products in one instruction
-__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9},"
-        " {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 
 __global__ void __launch_bounds__(kThreads, 2)
 tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,

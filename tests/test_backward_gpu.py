@@ -164,16 +164,19 @@ def test_chunked_backward_segments(T, a_mean):
 
 
 @pytest.mark.parametrize("T,a_mean,h0", [(2500, 0.0, True), (1500, -6.0, False), (77, 0.0, True)])
-def test_adjoint_chain_kernels_agree(monkeypatch, T, a_mean, h0):
-    """The adjoint chain on tcgen05 (the default) and on mma.sync (GDR_BWD_ADJ_MMA=1):
-    both match the oracle, and they agree with each other more closely than either
-    does with the oracle's bf16 tolerance."""
+@pytest.mark.parametrize("chains", [("GDR_BWD_ADJ_MMA", "GDR_BWD_FWD_MMA"), ("GDR_BWD_ADJ_MMA",),
+                                    ("GDR_BWD_FWD_MMA",)])
+def test_chain_kernels_agree(monkeypatch, T, a_mean, h0, chains):
+    """The state chains on tcgen05 (the default) and on mma.sync (GDR_BWD_ADJ_MMA=1 for
+    the adjoint chain, GDR_BWD_FWD_MMA=1 for the forward chain): both match the oracle,
+    and they agree with each other within the bf16 tolerance."""
     x = _inputs("bf16", 128, T, "bounded", seed=4900 + T, N=2, H=2, a_mean=a_mean, h0=h0)
     tc, ref = _run(x, "bounded", h0=h0)
-    monkeypatch.setenv("GDR_BWD_ADJ_MMA", "1")
+    for name in chains:
+        monkeypatch.setenv(name, "1")
     mma, _ = _run(x, "bounded", h0=h0)
     _check(tc, ref, "bf16")
     _check(mma, ref, "bf16")
     for name in NAMES:
         r = rel_l2(to64(tc[name]), to64(mma[name]))
-        assert r <= 1e-2, f"{name}: tcgen05 vs mma.sync adjoint chain rel-L2 {r:.3e}"
+        assert r <= 1e-2, f"{name}: tcgen05 vs mma.sync chains rel-L2 {r:.3e}"

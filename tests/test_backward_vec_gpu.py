@@ -103,15 +103,16 @@ def test_vec_backward_rejects_what_it_does_not_cover():
 
 
 @pytest.mark.parametrize("T,a_mean", [(2500, 0.0), (600, -6.0)])
-def test_vec_adjoint_chain_kernels_agree(monkeypatch, T, a_mean):
-    """Per-channel decay: the adjoint chain on tcgen05 (the default) and on mma.sync
-    (GDR_BWD_ADJ_MMA=1) both match the oracle and agree with each other."""
+def test_vec_chain_kernels_agree(monkeypatch, T, a_mean):
+    """Per-channel decay: the state chains on tcgen05 (the default) and on mma.sync
+    (GDR_BWD_ADJ_MMA=1, GDR_BWD_FWD_MMA=1) both match the oracle and agree."""
     x = _inputs(T, seed=7400 + T, N=2, H=2, a_mean=a_mean)
     tc, ref = _run(x)
     monkeypatch.setenv("GDR_BWD_ADJ_MMA", "1")
+    monkeypatch.setenv("GDR_BWD_FWD_MMA", "1")
     mma, _ = _run(x)
     _check(tc, ref)
     _check(mma, ref)
     for name in NAMES:
         r = rel_l2(to64(tc[name]), to64(mma[name]))
-        assert r <= 1e-2, f"{name}: tcgen05 vs mma.sync adjoint chain rel-L2 {r:.3e}"
+        assert r <= 1e-2, f"{name}: tcgen05 vs mma.sync chains rel-L2 {r:.3e}"
