@@ -43,6 +43,7 @@
 #include "gdr_bwd_chunk.cuh"
 #include "gdr_internal.cuh"
 #include "gdr_mma.cuh"
+#include "gdr_tc_prep.cuh"
 
 namespace gdr {
 namespace {
@@ -63,11 +64,6 @@ using bwdc::segment_of;
 using bwdc::warm_walk;
 
 
-
-template <bool VEC>
-__device__ __forceinline__ float gate_in(const __nv_bfloat16 *a, int64_t row, int d) {
-    return __bfloat162float(VEC ? a[row * kD + d] : a[row]);
-}
 
 // Staging of one tile over all 256 threads: lanes 2d and 2d + 1 of a warp take key
 // channel d (and column d of the 128-wide input `other`, V or dO), tokens 0-7 and 8-15;
@@ -221,6 +217,19 @@ __device__ __forceinline__ void stage_tile(const BcArgs &A, int64_t t0, int len,
     stage_compute(A, len, R, Kt, Kh, Qt, Gb, eg, other != nullptr, Ob, bs);
 }
 
+// bf16 A fragment (m16n8k16) of rows 0..15, columns k0..k0+15 of a fp32 [16][kLd]
+// buffer, rounded to bf16
+__device__ __forceinline__ void load_a16(uint32_t (&a)[4], const float *M, int k0, int g, int t) {
+    const float2 x0 = *(const float2 *)&M[g * kLd + k0 + 2 * t];
+    const float2 x1 = *(const float2 *)&M[(g + 8) * kLd + k0 + 2 * t];
+    const float2 x2 = *(const float2 *)&M[g * kLd + k0 + 8 + 2 * t];
+    const float2 x3 = *(const float2 *)&M[(g + 8) * kLd + k0 + 8 + 2 * t];
+    a[0] = tcp::pack_bf16(x0.x, x0.y);
+    a[1] = tcp::pack_bf16(x1.x, x1.y);
+    a[2] = tcp::pack_bf16(x2.x, x2.y);
+    a[3] = tcp::pack_bf16(x3.x, x3.y);
+}
+
 // 16 x 16 product X Y^T over K = 128 (one 8-column half of the output per warp):
 // out[i][j] for j in j0..j0+7.
 __device__ __forceinline__ void gram_half(float (&acc)[4], const float *X, const float *Y, int j0,
@@ -236,45 +245,68 @@ __device__ __forceinline__ void gram_half(float (&acc)[4], const float *X, const
 }
 
 // Forward substitution x = (I + A)^{-1} diag(beta) y on one column of a [16][kLd]
-// buffer, in place (A strictly lower, row stride kPd).
+// buffer, in place (A strictly lower, row stride kPd; its rows are read as float4,
+// so Am is 16-byte aligned).
 __device__ __forceinline__ void fwd_subst(float *X, int col, const float *Am, const float *bs) {
     float x[kT];
 #pragma unroll
     for (int i = 0; i < kT; ++i) {
         float acc = bs[i] * X[i * kLd + col];
 #pragma unroll
-        for (int j = 0; j < i; ++j) acc = fmaf(-Am[i * kPd + j], x[j], acc);
+        for (int j4 = 0; j4 < i; j4 += 4) {
+            const float4 r = *(const float4 *)&Am[i * kPd + j4];
+            acc = fmaf(-r.x, x[j4], acc);
+            if (j4 + 1 < i) acc = fmaf(-r.y, x[j4 + 1], acc);
+            if (j4 + 2 < i) acc = fmaf(-r.z, x[j4 + 2], acc);
+            if (j4 + 3 < i) acc = fmaf(-r.w, x[j4 + 3], acc);
+        }
         x[i] = acc;
     }
 #pragma unroll
     for (int i = 0; i < kT; ++i) X[i * kLd + col] = x[i];
 }
 
-// Back substitution y = (I + A)^{-T} x on one column, from src into dst.
-__device__ __forceinline__ void back_subst(const float *src, float *dst, int col, const float *Am) {
+// Back substitution y = (I + A)^{-T} x on one column, from src into dst; AmT holds
+// A^T (row i = column i of A), read as float4.
+__device__ __forceinline__ void back_subst(const float *src, float *dst, int col, const float *AmT) {
     float y[kT];
 #pragma unroll
     for (int i = kT - 1; i >= 0; --i) {
         float acc = src[i * kLd + col];
 #pragma unroll
-        for (int j = i + 1; j < kT; ++j) acc = fmaf(-Am[j * kPd + i], y[j], acc);
+        for (int j4 = (i + 1) & ~3; j4 < kT; j4 += 4) {
+            const float4 r = *(const float4 *)&AmT[i * kPd + j4];
+            if (j4 > i) acc = fmaf(-r.x, y[j4], acc);
+            if (j4 + 1 > i) acc = fmaf(-r.y, y[j4 + 1], acc);
+            if (j4 + 2 > i) acc = fmaf(-r.z, y[j4 + 2], acc);
+            acc = fmaf(-r.w, y[j4 + 3], acc);
+        }
         y[i] = acc;
     }
 #pragma unroll
     for (int i = 0; i < kT; ++i) dst[i * kLd + col] = y[i];
 }
 
-// A = beta (.) strict_lower(Kt Kh^T) into Am (warps 0-1 call this)
+// A = beta (.) strict_lower(Kt Kh^T) into Am, and its transpose into AmT if given
+// (warps 0-1 call this)
 __device__ __forceinline__ void build_A(const float *Kt, const float *Kh, const float *bs, float *Am,
-                                        float *KK, int half, int g, int t) {
+                                        float *KK, int half, int g, int t, float *AmT = nullptr) {
     float acc[4];
     const int j0 = 8 * half;
     gram_half(acc, Kt, Kh, j0, g, t);
     const int i0 = g, i1 = g + 8, ja = j0 + 2 * t, jb = ja + 1;
-    Am[i0 * kPd + ja] = ja < i0 ? bs[i0] * acc[0] : 0.f;
-    Am[i0 * kPd + jb] = jb < i0 ? bs[i0] * acc[1] : 0.f;
-    Am[i1 * kPd + ja] = ja < i1 ? bs[i1] * acc[2] : 0.f;
-    Am[i1 * kPd + jb] = jb < i1 ? bs[i1] * acc[3] : 0.f;
+    const float a00 = ja < i0 ? bs[i0] * acc[0] : 0.f, a01 = jb < i0 ? bs[i0] * acc[1] : 0.f;
+    const float a10 = ja < i1 ? bs[i1] * acc[2] : 0.f, a11 = jb < i1 ? bs[i1] * acc[3] : 0.f;
+    Am[i0 * kPd + ja] = a00;
+    Am[i0 * kPd + jb] = a01;
+    Am[i1 * kPd + ja] = a10;
+    Am[i1 * kPd + jb] = a11;
+    if (AmT) {
+        AmT[ja * kPd + i0] = a00;
+        AmT[jb * kPd + i0] = a01;
+        AmT[ja * kPd + i1] = a10;
+        AmT[jb * kPd + i1] = a11;
+    }
     if (KK) {
         KK[i0 * kPd + ja] = acc[0];
         KK[i0 * kPd + jb] = acc[1];
@@ -332,49 +364,85 @@ __device__ __forceinline__ void copy_state_in(float *Hs, const float *src) {
 }
 
 // Per (tile, head): sum over its tokens of max_d g_{t,d} + ln max(1, |1 - beta |k|^2|).
+// One warp per (tile, head): lane l reads key channels 4l..4l+3 of every token (8-byte
+// loads), and the 16 per-token partial sums (and gate minima) are reduced across the
+// warp by halving exchanges (16 + 8 + 4 + 2 + 1 values), after which lane pair
+// (2i, 2i + 1) holds token i's totals.
+constexpr int kBoundWarps = 8;   // (tile, head) pairs per block
+
+// v[0..15] summed (MIN: minimised) over the warp; token (lane >> 1)'s result in v[0]
+template <bool MIN>
+__device__ __forceinline__ void fold16(float (&v)[kT], int lane) {
+#pragma unroll
+    for (int w = kT / 2; w >= 1; w >>= 1) {
+        const bool hi = (lane & (2 * w)) != 0;   // keeps the upper w of the 2w values
+#pragma unroll
+        for (int j = 0; j < w; ++j) {
+            const float keep = hi ? v[j + w] : v[j], send = hi ? v[j] : v[j + w];
+            const float r = __shfl_xor_sync(0xffffffffu, send, 2 * w);
+            v[j] = MIN ? fminf(keep, r) : keep + r;
+        }
+    }
+    const float r = __shfl_xor_sync(0xffffffffu, v[0], 1);
+    v[0] = MIN ? fminf(v[0], r) : v[0] + r;
+}
+
+// four consecutive bf16 values: one 8-byte load when the tensors are 8-byte aligned
+__device__ __forceinline__ void load4(const __nv_bfloat16 *p, bool wide, float (&x)[4]) {
+    if (wide) {
+        const uint2 r = *(const uint2 *)p;
+        const float2 lo = __bfloat1622float2(*(const __nv_bfloat162 *)&r.x);
+        const float2 hi = __bfloat1622float2(*(const __nv_bfloat162 *)&r.y);
+        x[0] = lo.x;
+        x[1] = lo.y;
+        x[2] = hi.x;
+        x[3] = hi.y;
+    } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) x[u] = __bfloat162float(p[u]);
+    }
+}
+
 template <bool VEC>
-__global__ void __launch_bounds__(128)
-bwd_bound_kernel(const BcArgs A, float *lam) {
-    __shared__ float red[2][4][kT];
-    const int64_t c = blockIdx.x;
+__global__ void __launch_bounds__(32 * kBoundWarps)
+bwd_bound_kernel(const BcArgs A, float *lam, int64_t max_tiles, bool wide) {
+    const int lane = threadIdx.x & 31;
+    const int64_t c = (int64_t)blockIdx.x * kBoundWarps + (threadIdx.x >> 5);
     const int h = blockIdx.y;
+    if (c >= max_tiles) return;
     const int n = find_owner(A.p.chunk_base, A.p.N, c);
     if (n < 0) return;
     const int64_t t0 = A.p.seq_start[n] + (c - A.p.chunk_base[n]) * kT;
     const int len = (int)min((int64_t)kT, A.p.seq_start[n + 1] - t0);
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    float kk[kT], m[kT];
 #pragma unroll
     for (int i = 0; i < kT; ++i) {
-        float m = 3.0e38f, kk = 0.f;
+        kk[i] = 0.f;
+        m[i] = 3.0e38f;
         if (i < len) {
             const int64_t row = (t0 + i) * A.H + h;
-            m = gate_in<VEC>(A.a, row, tid);
-            const float kd = __bfloat162float(A.k[row * kD + tid]);
-            kk = kd * kd;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            m = fminf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            kk += __shfl_xor_sync(0xffffffffu, kk, o);
-        }
-        if (lane == 0) {
-            red[0][w][i] = m;
-            red[1][w][i] = kk;
+            float kv[4], av[4];
+            load4(&A.k[row * kD + 4 * lane], wide, kv);
+            kk[i] = kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3];
+            if (VEC) {
+                load4(&A.a[row * kD + 4 * lane], wide, av);
+                m[i] = fminf(fminf(av[0], av[1]), fminf(av[2], av[3]));
+            }
         }
     }
-    __syncthreads();
-    if (tid < 32) {
-        float x = 0.f;
-        if (tid < len) {
-            const float m = fminf(fminf(red[0][0][tid], red[0][1][tid]), fminf(red[0][2][tid], red[0][3][tid]));
-            const float kk = red[1][0][tid] + red[1][1][tid] + red[1][2][tid] + red[1][3][tid];
-            const float bt = __bfloat162float(A.beta[(t0 + tid) * A.H + h]);
-            x = gate_logdecay(m, A.b, GDR_GATE_BOUNDED) + logf(fmaxf(1.f, fabsf(1.f - bt * kk)));
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-        if (tid == 0) lam[c * A.H + h] = x;
+    fold16<false>(kk, lane);
+    if (VEC) fold16<true>(m, lane);
+    const int i = lane >> 1;
+    float x = 0.f;
+    if ((lane & 1) == 0 && i < len) {
+        const int64_t row = (t0 + i) * A.H + h;
+        const float mi = VEC ? m[0] : __bfloat162float(A.a[row]);
+        const float bt = __bfloat162float(A.beta[row]);
+        x = gate_logdecay(mi, A.b, GDR_GATE_BOUNDED) + logf(fmaxf(1.f, fabsf(1.f - bt * kk[0])));
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (lane == 0) lam[c * A.H + h] = x;
 }
 
 // Per (sequence, head): 1 if every interior segment boundary has a bound <= e^-46
@@ -674,7 +742,7 @@ template <bool VEC> struct TileLayout {
                          db = ob + kTile2, ub = db + kTile2, wb = ub + kTile2, eb = wb + kTile2,
                          am = eb + kTile2, kk = am + kT * kPd, smx = kk + kT * kPd,
                          ds = smx + kT * kPd, da = ds + kT * kPd, bda = da + kT * kPd,
-                         eg = bda + kT * kPd, rg = eg + kD, bs = rg + kD, rs = bs + kT,
+                         amt = bda + kT * kPd, eg = amt + kT * kPd, rg = eg + kD, bs = rg + kD, rs = bs + kT,
                          rs2 = rs + 4 * kT, gb = rs2 + kT, sh = gb + (VEC ? kTile2 : 2 * kT), total_f = sh;
     static constexpr size_t bytes = sizeof(float) * total_f + sizeof(__nv_bfloat16) * kD * kLdh;
 };
@@ -687,7 +755,8 @@ bwd_tile_kernel(const BcArgs A) {
     float *Kt = sm + L::kt, *Kh = sm + L::kh, *Qt = sm + L::qt, *Ob = sm + L::ob, *Db = sm + L::db;
     float *Ub = sm + L::ub, *Wb = sm + L::wb, *Eb = sm + L::eb;
     float *Am = sm + L::am, *KK = sm + L::kk, *Sm = sm + L::smx, *dS = sm + L::ds, *dA = sm + L::da;
-    float *bdA = sm + L::bda, *eg = sm + L::eg, *rG = sm + L::rg, *bs = sm + L::bs, *rowsum = sm + L::rs;
+    float *bdA = sm + L::bda, *AmT = sm + L::amt, *eg = sm + L::eg, *rG = sm + L::rg, *bs = sm + L::bs,
+          *rowsum = sm + L::rs;
     float *rowsum2 = sm + L::rs2;   // per-token dG sums for da
     float *Gb = sm + L::gb;
     __nv_bfloat16 *Sh = (__nv_bfloat16 *)(sm + L::sh);
@@ -745,27 +814,28 @@ bwd_tile_kernel(const BcArgs A) {
     __syncthreads();
     // ---- Ke dH1 = Kh X (this warp's dv columns) and dKe (.) e^{G_C} = D X^T (this warp's dk columns),
     // then the 16 x 16 products
+    // bf16 products (m16n8k16): A rows rounded from fp32, X fragments by ldmatrix
+    // (rows at 272-byte stride: conflict-free); lanes 0-7 / 8-15 / 16-23 / 24-31 address
+    // the 8x8 blocks (rows 0-7, cols 0-7) / (8-15, 0-7) / (0-7, 8-15) / (8-15, 8-15)
+    const int lr = (lane & 7) + 8 * ((lane >> 3) & 1), lc = lane >> 4;
     float dke[2][4], dd[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int u = 0; u < 4; ++u) dke[nt][u] = dd[nt][u] = 0.f;
 #pragma unroll 2
-    for (int k0 = 0; k0 < kD; k0 += 8) {
-        uint32_t ak[4], ad[4];
-        ak[0] = tf32(Kh[g * kLd + k0 + t]);   // Ke dH1 = Kh X
-        ak[1] = tf32(Kh[(g + 8) * kLd + k0 + t]);
-        ak[2] = tf32(Kh[g * kLd + k0 + t + 4]);
-        ak[3] = tf32(Kh[(g + 8) * kLd + k0 + t + 4]);
-        load_a(ad, Db, kLd, 0, k0, g, t);
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            uint32_t b0, b1;
-            load_b_h(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);    // X[k][c]
-            mma8(dd[nt], ak, b0, b1);
-            load_bt_h(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);   // X^T[k][d] = X[d][k]
-            mma8(dke[nt], ad, b0, b1);
-        }
+    for (int k0 = 0; k0 < kD; k0 += 16) {
+        uint32_t ak[4], ad[4], bx[4], bxt[4];
+        load_a16(ak, Kh, k0, g, t);   // Ke dH1 = Kh X
+        load_a16(ad, Db, k0, g, t);
+        // X[k][c] (k = key k0.., c = this warp's value columns): transposed blocks
+        tcp::ldsm_x4_trans((uint32_t)__cvta_generic_to_shared(&Sh[(k0 + lr) * kLdh + c0 + 8 * lc]), bx);
+        // X^T[k][d] = X[d][k] (d = this warp's key columns, k = value k0..)
+        tcp::ldsm_x4((uint32_t)__cvta_generic_to_shared(&Sh[(c0 + lr) * kLdh + k0 + 8 * lc]), bxt);
+        tcp::mma16816(dd[0], ak, bx[0], bx[1]);
+        tcp::mma16816(dd[1], ak, bx[2], bx[3]);
+        tcp::mma16816(dke[0], ad, bxt[0], bxt[2]);
+        tcp::mma16816(dke[1], ad, bxt[1], bxt[3]);
     }
     // e^{G_C} rowsum(dH1 (.) H0) = rowsum(X (.) H0): X from shared memory, H0 rows from
     // the stored copy
@@ -787,7 +857,7 @@ bwd_tile_kernel(const BcArgs A) {
             if (lane == 0) rG[r] = pr;
         }
     }
-    if (warp < 2) build_A(Kt, Kh, bs, Am, KK, warp, g, t);
+    if (warp < 2) build_A(Kt, Kh, bs, Am, KK, warp, g, t, AmT);
     else if (warp < 4) build_lower(Qt, Kh, Sm, warp - 2, g, t);
     else if (warp < 6) build_lower(Ob, Db, dS, warp - 4, g, t);   // dS = lower(dO D^T)
     else if (!VEC && warp == 7) {
@@ -838,19 +908,18 @@ bwd_tile_kernel(const BcArgs A) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) dq[nt][u] = dw[nt][u] = 0.f;
 #pragma unroll 2
-        for (int k0 = 0; k0 < kD; k0 += 8) {
-            uint32_t ao[4], ae[4];
-            load_a(ao, Ob, kLd, 0, k0, g, t);
-            load_a(ae, Eb, kLd, 0, k0, g, t);
+        for (int k0 = 0; k0 < kD; k0 += 16) {
+            uint32_t ao[4], ae[4], bh[4];
+            load_a16(ao, Ob, k0, g, t);
+            load_a16(ae, Eb, k0, g, t);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) ae[u] ^= 0x80000000u;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                uint32_t b0, b1;
-                load_bt_h(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);   // H0^T[k][d] = H0[d][k]
-                mma8(dq[nt], ao, b0, b1);
-                mma8(dw[nt], ae, b0, b1);
-            }
+            for (int u = 0; u < 4; ++u) ae[u] ^= 0x80008000u;   // -dD
+            // H0^T[k][d] = H0[d][k] (d = this warp's key columns, k = value k0..)
+            tcp::ldsm_x4((uint32_t)__cvta_generic_to_shared(&Sh[(c0 + lr) * kLdh + k0 + 8 * lc]), bh);
+            tcp::mma16816(dq[0], ao, bh[0], bh[2]);
+            tcp::mma16816(dq[1], ao, bh[1], bh[3]);
+            tcp::mma16816(dw[0], ae, bh[0], bh[2]);
+            tcp::mma16816(dw[1], ae, bh[1], bh[3]);
         }
         // D's last readers (dS and dKe) finished two barriers ago: dW can take its place
 #pragma unroll
@@ -864,7 +933,7 @@ bwd_tile_kernel(const BcArgs A) {
     }
     __syncthreads();
     // ---- dYw = T^T dW in place (dk columns, threads 0..127); dYu = T^T dD in place
-    back_subst(tid < kD ? Db : Eb, tid < kD ? Db : Eb, tid & (kD - 1), Am);
+    back_subst(tid < kD ? Db : Eb, tid < kD ? Db : Eb, tid & (kD - 1), AmT);
     __syncthreads();
     // ---- dA = -strict_lower(dYu U^T + dYw W^T) (warps 0-1); dV = diag(beta) dYu
     if (warp < 2) {
@@ -1035,7 +1104,10 @@ cudaError_t run_chunk_bwd(const BcArgs &A, int64_t T_total, int64_t max_tiles, i
     if (segs > 0x7fffffff) return cudaErrorInvalidValue;
     if (max_tiles > 0) {
         ProfScope prof(stream, "bwd_bound_kernel");
-        bwd_bound_kernel<VEC><<<dim3((unsigned)max_tiles, (unsigned)H), 128, 0, stream>>>(A, lam);
+        const int64_t nb = (max_tiles + kBoundWarps - 1) / kBoundWarps;
+        const bool wide = (uintptr_t)A.k % 8 == 0 && (!VEC || (uintptr_t)A.a % 8 == 0);
+        bwd_bound_kernel<VEC><<<dim3((unsigned)nb, (unsigned)H), 32 * kBoundWarps, 0, stream>>>(A, lam, max_tiles,
+                                                                                               wide);
         count_launch();
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }

@@ -1,4 +1,4 @@
-"""Runs small parity cases of the forward pass on the checking build of the library
+"""Runs small parity cases of the forward and backward passes on the checking build of the library
 (device-side index checks, GDR_DEBUG), named by GDR_LIB: every case must match the
 oracle at the usual tolerances and leave the status word clean (no check failed).
 Started by tests/test_debug_build_gpu.py in a process of its own."""
@@ -61,6 +61,26 @@ def main():
                                        b=w.b)
         assert_close(to64(out), ro, "bf16", f"{w.name} per-channel out")
         assert_close(to64(hT), rh, "bf16", f"{w.name} per-channel hT")
+    # the chunked backward (the two tcgen05 state chains and the per-tile kernel):
+    # 64-tile segments with warm-up tiles and a ragged end, one decay per token or per
+    # key channel
+    from gpu_helpers import rel_l2
+    for per_channel in (False, True):
+        w = WORKLOADS["b2_t4k"].with_(B=1, H=2, seed=1038, h0_std=0.05)
+        x = make_inputs(w, device="cuda", T=2503)
+        g = torch.Generator(device="cpu").manual_seed(1039)
+        dout = torch.randn(x["v"].shape, generator=g).to(torch.bfloat16).cuda()
+        dhT = (0.1 * torch.randn((1, 2, 128, 128), generator=g)).cuda()
+        a = make_channel_gate(x, 1040) if per_channel else x["a"]
+        fn = gdr.chunk_bwd_vec if per_channel else gdr.chunk_bwd
+        ofn = oracle.oracle_bwd_vec if per_channel else oracle.oracle_bwd
+        got = fn(x["q"], x["k"], x["v"], a, x["beta"], dout=dout, dhT=dhT, h0=x["h0"], b=w.b)
+        st = gdr.gdr_get_status()
+        assert st == gdr.GDR_OK, gdr.gdr_status_string(st)
+        ref = ofn(x["q"], x["k"], x["v"], a, x["beta"], dout=dout, dhT=dhT, h0=x["h0"], b=w.b)
+        for name, gv in zip(("dq", "dk", "dv", "da", "dbeta", "dh0"), got):
+            rl = rel_l2(to64(gv), ref[name])
+            assert rl <= 1e-2, f"backward (per channel: {per_channel}) {name}: rel-L2 {rl:.3e}"
     # zero tokens
     x = make_inputs(WORKLOADS["b2_t4k"].with_(H=2, seed=1034), device="cuda", T=0)
     for path in ("simt", "tc"):

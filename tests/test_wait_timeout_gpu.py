@@ -83,3 +83,46 @@ def test_per_channel_kernel_waits_that_run_out_unwind(monkeypatch, limit_ns):
         assert gdr.gdr_get_status() == gdr.GDR_OK
         assert_close(to64(out), ro, "bf16", "out")
         assert_close(to64(hT), rh, "bf16", "hT")
+
+
+@pytest.mark.parametrize("per_channel", [False, True])
+@pytest.mark.parametrize("limit_ns", [0, 1500])
+def test_backward_chain_waits_that_run_out_unwind(monkeypatch, limit_ns, per_channel):
+    """The same for the backward's two tcgen05 state chains (tc_fwd_chain_kernel and
+    tc_adj_kernel, bf16 d = 128, segments with warm-up tiles): the timed-out call
+    reports GDR_ERR_TIMEOUT (limit 0), and the next two calls match the oracle."""
+    import numpy as np
+    import oracle
+    from gdr_inputs import make_channel_gate
+    from gpu_helpers import rel_l2
+    w = WORKLOADS["b2_t4k"].with_(B=1, H=2, seed=1030, h0_std=0.05)
+    x = make_inputs(w, device="cuda", T=2000)
+    g = torch.Generator(device="cpu").manual_seed(1031)
+    dout = torch.randn(x["v"].shape, generator=g).to(torch.bfloat16).cuda()
+    dhT = (0.1 * torch.randn((1, 2, 128, 128), generator=g)).cuda()
+    a = make_channel_gate(x, 1032) if per_channel else x["a"]
+    fn = gdr.chunk_bwd_vec if per_channel else gdr.chunk_bwd
+    ofn = oracle.oracle_bwd_vec if per_channel else oracle.oracle_bwd
+
+    def call():
+        return fn(x["q"], x["k"], x["v"], a, x["beta"], dout=dout, dhT=dhT, h0=x["h0"], b=w.b)
+
+    assert gdr.gdr_get_status() == gdr.GDR_OK
+    monkeypatch.setenv("GDR_TC_WAIT_NS", str(limit_ns))
+    call()
+    st = gdr.gdr_get_status()
+    if limit_ns == 0:
+        assert st == gdr.GDR_ERR_TIMEOUT, gdr.gdr_status_string(st)
+    else:
+        assert st in (gdr.GDR_OK, gdr.GDR_ERR_TIMEOUT), gdr.gdr_status_string(st)
+    monkeypatch.delenv("GDR_TC_WAIT_NS")
+    ref = ofn(x["q"], x["k"], x["v"], a, x["beta"], dout=dout, dhT=dhT, h0=x["h0"], b=w.b)
+    for _ in range(2):
+        got = call()
+        torch.cuda.synchronize()
+        assert gdr.gdr_get_status() == gdr.GDR_OK
+        for name, gv in zip(("dq", "dk", "dv", "da", "dbeta", "dh0"), got):
+            r = ref[name]
+            assert rel_l2(to64(gv), r) <= 1e-2, name
+            lim = 5e-2 * max(1.0, float(np.abs(r).max()))
+            assert float(np.abs(to64(gv) - r).max()) <= lim, name
