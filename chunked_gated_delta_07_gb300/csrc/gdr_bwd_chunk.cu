@@ -43,7 +43,6 @@
 #include "gdr_bwd_chunk.cuh"
 #include "gdr_internal.cuh"
 #include "gdr_mma.cuh"
-#include "gdr_tc_prep.cuh"
 
 namespace gdr {
 namespace {
@@ -217,19 +216,6 @@ __device__ __forceinline__ void stage_tile(const BcArgs &A, int64_t t0, int len,
     stage_compute(A, len, R, Kt, Kh, Qt, Gb, eg, other != nullptr, Ob, bs);
 }
 
-// bf16 A fragment (m16n8k16) of rows 0..15, columns k0..k0+15 of a fp32 [16][kLd]
-// buffer, rounded to bf16
-__device__ __forceinline__ void load_a16(uint32_t (&a)[4], const float *M, int k0, int g, int t) {
-    const float2 x0 = *(const float2 *)&M[g * kLd + k0 + 2 * t];
-    const float2 x1 = *(const float2 *)&M[(g + 8) * kLd + k0 + 2 * t];
-    const float2 x2 = *(const float2 *)&M[g * kLd + k0 + 8 + 2 * t];
-    const float2 x3 = *(const float2 *)&M[(g + 8) * kLd + k0 + 8 + 2 * t];
-    a[0] = tcp::pack_bf16(x0.x, x0.y);
-    a[1] = tcp::pack_bf16(x1.x, x1.y);
-    a[2] = tcp::pack_bf16(x2.x, x2.y);
-    a[3] = tcp::pack_bf16(x3.x, x3.y);
-}
-
 // 16 x 16 product X Y^T over K = 128 (one 8-column half of the output per warp):
 // out[i][j] for j in j0..j0+7.
 __device__ __forceinline__ void gram_half(float (&acc)[4], const float *X, const float *Y, int j0,
@@ -245,68 +231,45 @@ __device__ __forceinline__ void gram_half(float (&acc)[4], const float *X, const
 }
 
 // Forward substitution x = (I + A)^{-1} diag(beta) y on one column of a [16][kLd]
-// buffer, in place (A strictly lower, row stride kPd; its rows are read as float4,
-// so Am is 16-byte aligned).
+// buffer, in place (A strictly lower, row stride kPd).
 __device__ __forceinline__ void fwd_subst(float *X, int col, const float *Am, const float *bs) {
     float x[kT];
 #pragma unroll
     for (int i = 0; i < kT; ++i) {
         float acc = bs[i] * X[i * kLd + col];
 #pragma unroll
-        for (int j4 = 0; j4 < i; j4 += 4) {
-            const float4 r = *(const float4 *)&Am[i * kPd + j4];
-            acc = fmaf(-r.x, x[j4], acc);
-            if (j4 + 1 < i) acc = fmaf(-r.y, x[j4 + 1], acc);
-            if (j4 + 2 < i) acc = fmaf(-r.z, x[j4 + 2], acc);
-            if (j4 + 3 < i) acc = fmaf(-r.w, x[j4 + 3], acc);
-        }
+        for (int j = 0; j < i; ++j) acc = fmaf(-Am[i * kPd + j], x[j], acc);
         x[i] = acc;
     }
 #pragma unroll
     for (int i = 0; i < kT; ++i) X[i * kLd + col] = x[i];
 }
 
-// Back substitution y = (I + A)^{-T} x on one column, from src into dst; AmT holds
-// A^T (row i = column i of A), read as float4.
-__device__ __forceinline__ void back_subst(const float *src, float *dst, int col, const float *AmT) {
+// Back substitution y = (I + A)^{-T} x on one column, from src into dst.
+__device__ __forceinline__ void back_subst(const float *src, float *dst, int col, const float *Am) {
     float y[kT];
 #pragma unroll
     for (int i = kT - 1; i >= 0; --i) {
         float acc = src[i * kLd + col];
 #pragma unroll
-        for (int j4 = (i + 1) & ~3; j4 < kT; j4 += 4) {
-            const float4 r = *(const float4 *)&AmT[i * kPd + j4];
-            if (j4 > i) acc = fmaf(-r.x, y[j4], acc);
-            if (j4 + 1 > i) acc = fmaf(-r.y, y[j4 + 1], acc);
-            if (j4 + 2 > i) acc = fmaf(-r.z, y[j4 + 2], acc);
-            acc = fmaf(-r.w, y[j4 + 3], acc);
-        }
+        for (int j = i + 1; j < kT; ++j) acc = fmaf(-Am[j * kPd + i], y[j], acc);
         y[i] = acc;
     }
 #pragma unroll
     for (int i = 0; i < kT; ++i) dst[i * kLd + col] = y[i];
 }
 
-// A = beta (.) strict_lower(Kt Kh^T) into Am, and its transpose into AmT if given
-// (warps 0-1 call this)
+// A = beta (.) strict_lower(Kt Kh^T) into Am (warps 0-1 call this)
 __device__ __forceinline__ void build_A(const float *Kt, const float *Kh, const float *bs, float *Am,
-                                        float *KK, int half, int g, int t, float *AmT = nullptr) {
+                                        float *KK, int half, int g, int t) {
     float acc[4];
     const int j0 = 8 * half;
     gram_half(acc, Kt, Kh, j0, g, t);
     const int i0 = g, i1 = g + 8, ja = j0 + 2 * t, jb = ja + 1;
-    const float a00 = ja < i0 ? bs[i0] * acc[0] : 0.f, a01 = jb < i0 ? bs[i0] * acc[1] : 0.f;
-    const float a10 = ja < i1 ? bs[i1] * acc[2] : 0.f, a11 = jb < i1 ? bs[i1] * acc[3] : 0.f;
-    Am[i0 * kPd + ja] = a00;
-    Am[i0 * kPd + jb] = a01;
-    Am[i1 * kPd + ja] = a10;
-    Am[i1 * kPd + jb] = a11;
-    if (AmT) {
-        AmT[ja * kPd + i0] = a00;
-        AmT[jb * kPd + i0] = a01;
-        AmT[ja * kPd + i1] = a10;
-        AmT[jb * kPd + i1] = a11;
-    }
+    Am[i0 * kPd + ja] = ja < i0 ? bs[i0] * acc[0] : 0.f;
+    Am[i0 * kPd + jb] = jb < i0 ? bs[i0] * acc[1] : 0.f;
+    Am[i1 * kPd + ja] = ja < i1 ? bs[i1] * acc[2] : 0.f;
+    Am[i1 * kPd + jb] = jb < i1 ? bs[i1] * acc[3] : 0.f;
     if (KK) {
         KK[i0 * kPd + ja] = acc[0];
         KK[i0 * kPd + jb] = acc[1];
@@ -742,7 +705,7 @@ template <bool VEC> struct TileLayout {
                          db = ob + kTile2, ub = db + kTile2, wb = ub + kTile2, eb = wb + kTile2,
                          am = eb + kTile2, kk = am + kT * kPd, smx = kk + kT * kPd,
                          ds = smx + kT * kPd, da = ds + kT * kPd, bda = da + kT * kPd,
-                         amt = bda + kT * kPd, eg = amt + kT * kPd, rg = eg + kD, bs = rg + kD, rs = bs + kT,
+                         eg = bda + kT * kPd, rg = eg + kD, bs = rg + kD, rs = bs + kT,
                          rs2 = rs + 4 * kT, gb = rs2 + kT, sh = gb + (VEC ? kTile2 : 2 * kT), total_f = sh;
     static constexpr size_t bytes = sizeof(float) * total_f + sizeof(__nv_bfloat16) * kD * kLdh;
 };
@@ -755,8 +718,7 @@ bwd_tile_kernel(const BcArgs A) {
     float *Kt = sm + L::kt, *Kh = sm + L::kh, *Qt = sm + L::qt, *Ob = sm + L::ob, *Db = sm + L::db;
     float *Ub = sm + L::ub, *Wb = sm + L::wb, *Eb = sm + L::eb;
     float *Am = sm + L::am, *KK = sm + L::kk, *Sm = sm + L::smx, *dS = sm + L::ds, *dA = sm + L::da;
-    float *bdA = sm + L::bda, *AmT = sm + L::amt, *eg = sm + L::eg, *rG = sm + L::rg, *bs = sm + L::bs,
-          *rowsum = sm + L::rs;
+    float *bdA = sm + L::bda, *eg = sm + L::eg, *rG = sm + L::rg, *bs = sm + L::bs, *rowsum = sm + L::rs;
     float *rowsum2 = sm + L::rs2;   // per-token dG sums for da
     float *Gb = sm + L::gb;
     __nv_bfloat16 *Sh = (__nv_bfloat16 *)(sm + L::sh);
@@ -814,28 +776,27 @@ bwd_tile_kernel(const BcArgs A) {
     __syncthreads();
     // ---- Ke dH1 = Kh X (this warp's dv columns) and dKe (.) e^{G_C} = D X^T (this warp's dk columns),
     // then the 16 x 16 products
-    // bf16 products (m16n8k16): A rows rounded from fp32, X fragments by ldmatrix
-    // (rows at 272-byte stride: conflict-free); lanes 0-7 / 8-15 / 16-23 / 24-31 address
-    // the 8x8 blocks (rows 0-7, cols 0-7) / (8-15, 0-7) / (0-7, 8-15) / (8-15, 8-15)
-    const int lr = (lane & 7) + 8 * ((lane >> 3) & 1), lc = lane >> 4;
     float dke[2][4], dd[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int u = 0; u < 4; ++u) dke[nt][u] = dd[nt][u] = 0.f;
 #pragma unroll 2
-    for (int k0 = 0; k0 < kD; k0 += 16) {
-        uint32_t ak[4], ad[4], bx[4], bxt[4];
-        load_a16(ak, Kh, k0, g, t);   // Ke dH1 = Kh X
-        load_a16(ad, Db, k0, g, t);
-        // X[k][c] (k = key k0.., c = this warp's value columns): transposed blocks
-        tcp::ldsm_x4_trans((uint32_t)__cvta_generic_to_shared(&Sh[(k0 + lr) * kLdh + c0 + 8 * lc]), bx);
-        // X^T[k][d] = X[d][k] (d = this warp's key columns, k = value k0..)
-        tcp::ldsm_x4((uint32_t)__cvta_generic_to_shared(&Sh[(c0 + lr) * kLdh + k0 + 8 * lc]), bxt);
-        tcp::mma16816(dd[0], ak, bx[0], bx[1]);
-        tcp::mma16816(dd[1], ak, bx[2], bx[3]);
-        tcp::mma16816(dke[0], ad, bxt[0], bxt[2]);
-        tcp::mma16816(dke[1], ad, bxt[1], bxt[3]);
+    for (int k0 = 0; k0 < kD; k0 += 8) {
+        uint32_t ak[4], ad[4];
+        ak[0] = tf32(Kh[g * kLd + k0 + t]);   // Ke dH1 = Kh X
+        ak[1] = tf32(Kh[(g + 8) * kLd + k0 + t]);
+        ak[2] = tf32(Kh[g * kLd + k0 + t + 4]);
+        ak[3] = tf32(Kh[(g + 8) * kLd + k0 + t + 4]);
+        load_a(ad, Db, kLd, 0, k0, g, t);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            uint32_t b0, b1;
+            load_b_h(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);    // X[k][c]
+            mma8(dd[nt], ak, b0, b1);
+            load_bt_h(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);   // X^T[k][d] = X[d][k]
+            mma8(dke[nt], ad, b0, b1);
+        }
     }
     // e^{G_C} rowsum(dH1 (.) H0) = rowsum(X (.) H0): X from shared memory, H0 rows from
     // the stored copy
@@ -857,7 +818,7 @@ bwd_tile_kernel(const BcArgs A) {
             if (lane == 0) rG[r] = pr;
         }
     }
-    if (warp < 2) build_A(Kt, Kh, bs, Am, KK, warp, g, t, AmT);
+    if (warp < 2) build_A(Kt, Kh, bs, Am, KK, warp, g, t);
     else if (warp < 4) build_lower(Qt, Kh, Sm, warp - 2, g, t);
     else if (warp < 6) build_lower(Ob, Db, dS, warp - 4, g, t);   // dS = lower(dO D^T)
     else if (!VEC && warp == 7) {
@@ -908,18 +869,19 @@ bwd_tile_kernel(const BcArgs A) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) dq[nt][u] = dw[nt][u] = 0.f;
 #pragma unroll 2
-        for (int k0 = 0; k0 < kD; k0 += 16) {
-            uint32_t ao[4], ae[4], bh[4];
-            load_a16(ao, Ob, k0, g, t);
-            load_a16(ae, Eb, k0, g, t);
+        for (int k0 = 0; k0 < kD; k0 += 8) {
+            uint32_t ao[4], ae[4];
+            load_a(ao, Ob, kLd, 0, k0, g, t);
+            load_a(ae, Eb, kLd, 0, k0, g, t);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) ae[u] ^= 0x80008000u;   // -dD
-            // H0^T[k][d] = H0[d][k] (d = this warp's key columns, k = value k0..)
-            tcp::ldsm_x4((uint32_t)__cvta_generic_to_shared(&Sh[(c0 + lr) * kLdh + k0 + 8 * lc]), bh);
-            tcp::mma16816(dq[0], ao, bh[0], bh[2]);
-            tcp::mma16816(dq[1], ao, bh[1], bh[3]);
-            tcp::mma16816(dw[0], ae, bh[0], bh[2]);
-            tcp::mma16816(dw[1], ae, bh[1], bh[3]);
+            for (int u = 0; u < 4; ++u) ae[u] ^= 0x80000000u;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                uint32_t b0, b1;
+                load_bt_h(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);   // H0^T[k][d] = H0[d][k]
+                mma8(dq[nt], ao, b0, b1);
+                mma8(dw[nt], ae, b0, b1);
+            }
         }
         // D's last readers (dS and dKe) finished two barriers ago: dW can take its place
 #pragma unroll
@@ -933,7 +895,7 @@ bwd_tile_kernel(const BcArgs A) {
     }
     __syncthreads();
     // ---- dYw = T^T dW in place (dk columns, threads 0..127); dYu = T^T dD in place
-    back_subst(tid < kD ? Db : Eb, tid < kD ? Db : Eb, tid & (kD - 1), AmT);
+    back_subst(tid < kD ? Db : Eb, tid < kD ? Db : Eb, tid & (kD - 1), Am);
     __syncthreads();
     // ---- dA = -strict_lower(dYu U^T + dYw W^T) (warps 0-1); dV = diag(beta) dYu
     if (warp < 2) {
