@@ -356,7 +356,11 @@ GDR_API gdr_status_t gdr_router_bias_update(const int64_t *load, float *bias, do
  * chunked form runs its two state chains (forward and adjoint, independent of
  * each other) concurrently: the adjoint chain on a second stream the library
  * keeps per device (freed by gdr_release), forked from and joined back to
- * `stream` with events, so the call is ordered on `stream` as a whole.
+ * `stream` with events, so the call is ordered on `stream` as a whole.  Both
+ * chains run on the tcgen05 tensor cores with the state in tensor memory when
+ * q, k, v, dout (and a per-channel a) are 16-byte aligned, and on warp-level
+ * tensor-core kernels otherwise; their waits are bounded like the forward's
+ * (GDR_ERR_TIMEOUT in the status word).
  */
 GDR_API gdr_status_t gdr_chunk_bwd(const void *q, const void *k, const void *v, const void *a,
                            const void *beta, const float *h0, const void *dout,
