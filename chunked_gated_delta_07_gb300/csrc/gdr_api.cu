@@ -178,7 +178,18 @@ struct Layout {
     size_t plan = 0, G = 0, W = 0, U = 0, tc = 0, total = 0;
 };
 
-Layout layout_for(const Shape &s, gdr_path_t path) {
+// The shape a path runs: the tensor-core path tiles by kTcTile whatever chunk the
+// caller named (16, 32 or 64).
+Shape run_shape(Shape s, gdr_path_t path) {
+    if (path == GDR_PATH_TC && s.C != kTcTile) {
+        s.C = kTcTile;
+        s.max_chunks = tile_bound(s.varlen, s.N, s.varlen ? s.T_total : s.T_per, kTcTile);
+    }
+    return s;
+}
+
+Layout layout_for(const Shape &s_in, gdr_path_t path) {
+    const Shape s = run_shape(s_in, path);
     Layout L;
     size_t off = 0;
     L.plan = off;
@@ -262,9 +273,10 @@ gdr_path_t resolve_path(gdr_path_t path, gdr_dtype_t dtype, int dk, int dv, int 
 
 gdr_status_t run_forward(const void *q, const void *k, const void *v, const void *a,
                          const void *beta, const float *h0, void *out, float *hT,
-                         const int32_t *cu, const Shape &s, float b, gdr_dtype_t dtype,
+                         const int32_t *cu, const Shape &s_in, float b, gdr_dtype_t dtype,
                          gdr_gate_t gate, gdr_path_t path, void *workspace,
                          size_t workspace_bytes, cudaStream_t stream) {
+    const Shape s = run_shape(s_in, path);
     DeviceCtx *ctx = device_ctx();
     if (!ctx) return GDR_ERR_CUDA;
     const Layout L = layout_for(s, path);

@@ -1030,7 +1030,8 @@ bool tc_make_map(CUtensorMap *map, const void *base, int H, int64_t rows) {
 }
 
 bool tc_supported(gdr_dtype_t dtype, int dk, int dv, int chunk) {
-    return dtype == GDR_BF16 && dk == kD && dv == kD && chunk == kC;
+    static_assert(kC == kTcTile, "tile length");
+    return dtype == GDR_BF16 && dk == kD && dv == kD && (chunk == 16 || chunk == 32 || chunk == 64);
 }
 
 // Tiles per segment.  The output pass runs one CTA per (segment, head), two per SM,

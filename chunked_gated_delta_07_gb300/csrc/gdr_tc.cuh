@@ -7,6 +7,12 @@
 
 namespace gdr {
 
+// Tile length of the tensor-core path.  A call with chunk 32 or 64 runs it on 16-token
+// tiles: the chunked form's result does not depend on the tile length (it is exact, and
+// the pairwise in-tile decays need no bound at any length), so the chunk a caller names
+// is a statement of blocking that this path is free to refine.
+constexpr int kTcTile = 16;
+
 // True when the tensor-core path implements this shape and dtype.
 bool tc_supported(gdr_dtype_t dtype, int dk, int dv, int chunk);
 

@@ -120,7 +120,11 @@ typedef enum {
  *   cu_seqlens   : NULL (dense) or N+1 int32 device offsets (varlen)
  *   B, T, H      : batch (or N), tokens per sequence (or total), heads
  *   dk, dv       : key / value width, each 64 or 128
- *   chunk        : tile length, 16, 32 or 64
+ *   chunk        : tile length, 16, 32 or 64.  The CUDA-core path tiles by
+ *                  chunk; the tensor-core path (bf16, dk = dv = 128) tiles by
+ *                  16 tokens for every chunk, since the result does not depend
+ *                  on the tile length beyond rounding (its in-tile decays are
+ *                  pairwise, bounded for any tile length and gate)
  *   b            : gate bound, > 0 and finite
  * Supported sizes: B, H >= 1, T >= 0 (T = 0 copies h0 to hT, or zeroes hT).
  */

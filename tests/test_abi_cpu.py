@@ -166,3 +166,14 @@ def test_noalloc_refuses_what_the_regular_entry_point_refuses(lib):
     for kw in (dict(out=1 << 20), dict(hT=(5 << 20) + 8), dict(h0=7 << 20, hT=(7 << 20) + 4),
                dict(B=0), dict(dk=96), dict(b=float("nan"))):
         assert _noalloc(**kw) == _call(**kw) != gdr.GDR_OK, kw
+
+
+def test_tc_path_tiles_by_16_for_every_chunk(lib):
+    # bf16, d = 128: the tensor-core path takes chunk 16, 32 and 64 and runs all of them
+    # on 16-token tiles (the same scratch); the CUDA-core path's scratch follows chunk
+    for B, T in [(2, 4096), (3, 1000)]:
+        tc = [gdr.gdr_chunk_fwd_workspace_size(B, T, 16, 128, 128, c, gdr.GDR_BF16, gdr.GDR_PATH_TC)
+              for c in (16, 32, 64)]
+        assert tc[0] > 0 and tc[0] == tc[1] == tc[2]
+    # fp32 has no tensor-core path at any chunk
+    assert gdr.gdr_chunk_fwd_workspace_size(2, 4096, 16, 128, 128, 32, gdr.GDR_F32, gdr.GDR_PATH_TC) == 0

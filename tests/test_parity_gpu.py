@@ -125,6 +125,23 @@ def test_h32_sweep_reduced(chunk, b):
         assert_close(to64(hT), rh, "bf16", f"hT[{path}]")
 
 
+@pytest.mark.parametrize("chunk", [32, 64])
+def test_tc_path_tiles_by_16_for_any_chunk(chunk):
+    """The tensor-core path runs 16-token tiles for chunk 32 and 64 (the chunked form's
+    result does not depend on the tile length): the same bits as a chunk-16 call, with
+    segments and a ragged tail; the CUDA-core path tiles by chunk (test above)."""
+    if not _tc_available():
+        pytest.skip("tensor-core path unavailable")
+    w = h32_variant(chunk, 8)
+    x = make_inputs(w, device="cuda", T=2500)
+    o16, h16 = run_gpu(x, path="tc", chunk=16)
+    oc, hc = run_gpu(x, path="tc", chunk=chunk)
+    assert torch.equal(o16, oc) and torch.equal(h16, hc)
+    ro, rh = run_oracle(x)
+    assert_close(to64(oc), ro, "bf16", "out")
+    assert_close(to64(hc), rh, "bf16", "hT")
+
+
 @pytest.mark.parametrize("gate", ["bounded", "softplus"])
 def test_varlen_reduced(gate):
     w = WORKLOADS["varlen_1m"].with_(len_min=40, len_max=2000)
