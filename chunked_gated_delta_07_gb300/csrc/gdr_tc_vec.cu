@@ -58,6 +58,7 @@ constexpr int kD = 128;          // dk = dv
 constexpr int kC = 16;           // tile length
 constexpr int kNS = 4;           // pipeline stages, one per prep warp
 constexpr int kThreads = 32 * (4 + kNS + 1);   // 4 state warps, kNS prep warps, 1 MMA issuer
+static_assert(kNS == 4, "the prep warps form warpgroup 1 (register hand-over below)");
 constexpr uint64_t kWaitNs = 2000000000ull;    // default pipeline wait limit: 2 s
 constexpr uint64_t kDrainNs = 2000000000ull;   // drains before exit: 2 s
 
@@ -221,6 +222,10 @@ tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
     if (warp >= 4 && warp < 4 + kNS) {
         // ============================ prep warps ============================
+        // The state warps (warpgroup 0) hand 8 registers per thread over to the prep
+        // warps (warpgroup 1): 4 x 32 x (88 + 104) = 2 x 4 x 32 x 96, the two warpgroups'
+        // launch allocation, so the increase never waits on more than the decrease frees.
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 104;");
         const int pw = warp - 4;
         const int g = lane >> 2, t = lane & 3;
         int pend_st = -1;          // stage whose TMA is issued but not yet seen complete
@@ -534,6 +539,7 @@ tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         __syncwarp();
     } else {
         // ============================ state warps ============================
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 88;");
         const int e = tid;                       // value index = TMEM lane
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         for (int d0 = 0; d0 < kD; d0 += 16) {
