@@ -706,7 +706,7 @@ template <bool VEC> struct TileLayout {
                          am = eb + kTile2, kk = am + kT * kPd, smx = kk + kT * kPd,
                          ds = smx + kT * kPd, da = ds + kT * kPd, bda = da + kT * kPd,
                          eg = bda + kT * kPd, rg = eg + kD, bs = rg + kD, rs = bs + kT,
-                         rs2 = rs + 4 * kT, gb = rs2 + kT, sh = gb + (VEC ? kTile2 : 2 * kT), total_f = sh;
+                         rs2 = rs + 4 * kT, gb = rs2 + kT, sh = gb + 2 * kT, total_f = sh;
     static constexpr size_t bytes = sizeof(float) * total_f + sizeof(__nv_bfloat16) * kD * kLdh;
 };
 
@@ -750,7 +750,20 @@ bwd_tile_kernel(const BcArgs A) {
         }
     }
     cp_async_commit();
-    stage_tile<VEC>(A, t0, len, h, Kt, Kh, Qt, VEC ? Gb : nullptr, eg, A.dout, Ob, bs);
+    // per-channel gate: the raw inputs of this thread's (channel, 8 tokens) stay packed in
+    // registers, and G is formed again from them once V's buffer is free (see below),
+    // so that no [16][128] G buffer holds shared memory through the tile
+    uint32_t ra_keep[kT / 4] = {};
+    {
+        StageRegs R;
+        stage_fetch<VEC>(A, t0, len, h, true, A.dout, R);
+        stage_compute(A, len, R, Kt, Kh, Qt, nullptr, eg, true, Ob, bs);
+        if (VEC)
+#pragma unroll
+            for (int m = 0; m < kT / 4; ++m)
+                ra_keep[m] = (uint32_t)__bfloat16_as_ushort(R.ra[2 * m]) |
+                             ((uint32_t)__bfloat16_as_ushort(R.ra[2 * m + 1]) << 16);
+    }
     if (!VEC && tid >= kThreads - kT) {
         // scalar gate: g and g'(a) per token, one load each (the cumsum follows the barrier)
         const int i = tid - (kThreads - kT);
@@ -945,6 +958,30 @@ bwd_tile_kernel(const BcArgs A) {
         }
     }
     __syncthreads();
+    // ---- per-channel gate: G again, into V's buffer (its last reader was dA, above), in
+    // the staging's order (lane pair (2d, 2d + 1): channel d, tokens 0-7 and 8-15)
+    float *Gv = VEC ? Ub : Gb;
+    if (VEC) {
+        const int d = tid >> 1, half = tid & 1, i0 = 8 * half;
+        float gl[8], G = 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            gl[u] = i0 + u < len ? gate_logdecay(bf_half(ra_keep[u >> 1], u & 1), A.b, GDR_GATE_BOUNDED) : 0.f;
+            G += gl[u];
+        }
+        const float Gfirst = __shfl_xor_sync(0xffffffffu, G, 1);
+        G = half ? Gfirst : 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u;
+            float gg = 0.f;
+            if (i < len) {
+                G += gl[u];
+                gg = G;
+            }
+            Ub[i * kLd + d] = gg;
+        }
+    }
     // ---- dKt, dKh, dQt on this warp's dk columns; dG into Ob
     {
         float dkt[2][4], dkh[2][4];
@@ -971,6 +1008,7 @@ bwd_tile_kernel(const BcArgs A) {
                 mma8(dq[nt], a_dS, bh0, bh1);      // dS Kh
             }
         }
+        if (VEC) __syncthreads();   // G (written above by other threads) is complete
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -981,7 +1019,7 @@ bwd_tile_kernel(const BcArgs A) {
                 const float dKh = dkh[nt][u] + dke[nt][u];   // dke = D X^T = dKe (.) e^{G_C}
                 Ob[i * kLd + d] = dq[nt][u] * qt + dKt * kt - dKh * kh;
                 if (i < len) {
-                    const float G = VEC ? Gb[i * kLd + d] : Gb[i];
+                    const float G = VEC ? Gv[i * kLd + d] : Gv[i];
                     const int64_t r = ((t0 + i) * A.H + h) * kD + d;
                     A.dq[r] = __float2bfloat16_rn(dq[nt][u] * expf(G));
                     A.dk[r] = __float2bfloat16_rn(dKt * expf(G) + dKh * expf(-G));
@@ -1014,7 +1052,7 @@ bwd_tile_kernel(const BcArgs A) {
             for (int i = len - 1; i >= 0; --i) {
                 acc += Ob[i * kLd + d] + (i == len - 1 ? rG[d] : 0.f);
                 // g'(a) = -b s (1 - s) with s = -g / b, i.e. g (1 + g / b); g from the cumsum
-                const float gi = Gb[i * kLd + d] - (i > 0 ? Gb[(i - 1) * kLd + d] : 0.f);
+                const float gi = Gv[i * kLd + d] - (i > 0 ? Gv[(i - 1) * kLd + d] : 0.f);
                 const int64_t r = ((t0 + i) * A.H + h) * kD + d;
                 A.da[r] = __float2bfloat16_rn(acc * gi * (1.f + gi / A.b));
             }
