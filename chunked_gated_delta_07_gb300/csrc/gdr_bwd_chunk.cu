@@ -653,6 +653,12 @@ bwd_adj_chain_kernel(const BcArgs A) {
             Eb[(g + 8) * kLd + col + 1] = acc[nt][3];
         }
         __syncwarp();
+        if (tt < s1) {   // dD of the segment's tiles for the tile kernel (this warp's columns)
+            const int i = lane >> 1, cc = c0 + 8 * (lane & 1);
+            float *dst = A.dDst + ((size_t)c * A.H + h) * kT * kD + (size_t)i * kD + cc;
+            *(float4 *)dst = *(const float4 *)&Eb[i * kLd + cc];
+            *(float4 *)(dst + 4) = *(const float4 *)&Eb[i * kLd + cc + 4];
+        }
         // dH0 = diag(e^{G_C}) dH1 + Qt^T dO - W^T dD on this warp's columns
         uint32_t bo[2][2][2], be[2][2][2];
 #pragma unroll
@@ -703,8 +709,8 @@ bwd_adj_chain_kernel(const BcArgs A) {
 template <bool VEC> struct TileLayout {
     static constexpr int kt = 0, kh = kt + kTile2, qt = kh + kTile2, ob = qt + kTile2,
                          db = ob + kTile2, ub = db + kTile2, wb = ub + kTile2, eb = wb + kTile2,
-                         am = eb + kTile2, kk = am + kT * kPd, smx = kk + kT * kPd,
-                         ds = smx + kT * kPd, da = ds + kT * kPd, bda = da + kT * kPd,
+                         am = eb + kTile2, kk = am + kT * kPd,
+                         ds = kk + kT * kPd, da = ds + kT * kPd, bda = da + kT * kPd,
                          eg = bda + kT * kPd, rg = eg + kD, bs = rg + kD, rs = bs + kT,
                          rs2 = rs + 4 * kT, gb = rs2 + kT, sh = gb + 2 * kT, total_f = sh;
     static constexpr size_t bytes = sizeof(float) * total_f + sizeof(__nv_bfloat16) * kD * kLdh;
@@ -717,7 +723,7 @@ bwd_tile_kernel(const BcArgs A) {
     extern __shared__ float sm[];
     float *Kt = sm + L::kt, *Kh = sm + L::kh, *Qt = sm + L::qt, *Ob = sm + L::ob, *Db = sm + L::db;
     float *Ub = sm + L::ub, *Wb = sm + L::wb, *Eb = sm + L::eb;
-    float *Am = sm + L::am, *KK = sm + L::kk, *Sm = sm + L::smx, *dS = sm + L::ds, *dA = sm + L::da;
+    float *Am = sm + L::am, *KK = sm + L::kk, *dS = sm + L::ds, *dA = sm + L::da;
     float *bdA = sm + L::bda, *eg = sm + L::eg, *rG = sm + L::rg, *bs = sm + L::bs, *rowsum = sm + L::rs;
     float *rowsum2 = sm + L::rs2;   // per-token dG sums for da
     float *Gb = sm + L::gb;
@@ -739,14 +745,16 @@ bwd_tile_kernel(const BcArgs A) {
             cp_async16(&Sh[r * kLdh + col], &src[e]);
         }
     };
-    // ---- stage: dH1 and D by asynchronous copies, then the factored rows, G, dO, V
+    // ---- stage: X, D and dD by asynchronous copies, then the factored rows, G, dO, V
     stage_state(A.dHst + st);
     {
         const float *Dg = A.Dst + ((size_t)c * A.H + h) * kT * kD;
+        const float *dDg = A.dDst + ((size_t)c * A.H + h) * kT * kD;
 #pragma unroll
         for (int e = tid * 4; e < kT * kD; e += kThreads * 4) {
             const int i = e >> 7, col = e & (kD - 1);
             cp_async16(&Db[i * kLd + col], &Dg[e]);
+            cp_async16(&Eb[i * kLd + col], &dDg[e]);
         }
     }
     cp_async_commit();
@@ -787,26 +795,20 @@ bwd_tile_kernel(const BcArgs A) {
     }
     cp_async_wait_all();
     __syncthreads();
-    // ---- Ke dH1 = Kh X (this warp's dv columns) and dKe (.) e^{G_C} = D X^T (this warp's dk columns),
-    // then the 16 x 16 products
-    float dke[2][4], dd[2][4];
+    // ---- dKe (.) e^{G_C} = D X^T (this warp's dk columns), then the 16 x 16 products
+    // (dD = S^T dO + Kh X comes from the adjoint chain, which forms it for its own step)
+    float dke[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int u = 0; u < 4; ++u) dke[nt][u] = dd[nt][u] = 0.f;
+        for (int u = 0; u < 4; ++u) dke[nt][u] = 0.f;
 #pragma unroll 2
     for (int k0 = 0; k0 < kD; k0 += 8) {
-        uint32_t ak[4], ad[4];
-        ak[0] = tf32(Kh[g * kLd + k0 + t]);   // Ke dH1 = Kh X
-        ak[1] = tf32(Kh[(g + 8) * kLd + k0 + t]);
-        ak[2] = tf32(Kh[g * kLd + k0 + t + 4]);
-        ak[3] = tf32(Kh[(g + 8) * kLd + k0 + t + 4]);
+        uint32_t ad[4];
         load_a(ad, Db, kLd, 0, k0, g, t);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             uint32_t b0, b1;
-            load_b_h(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);    // X[k][c]
-            mma8(dd[nt], ak, b0, b1);
             load_bt_h(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);   // X^T[k][d] = X[d][k]
             mma8(dke[nt], ad, b0, b1);
         }
@@ -832,8 +834,7 @@ bwd_tile_kernel(const BcArgs A) {
         }
     }
     if (warp < 2) build_A(Kt, Kh, bs, Am, KK, warp, g, t);
-    else if (warp < 4) build_lower(Qt, Kh, Sm, warp - 2, g, t);
-    else if (warp < 6) build_lower(Ob, Db, dS, warp - 4, g, t);   // dS = lower(dO D^T)
+    else if (warp < 4) build_lower(Ob, Db, dS, warp - 2, g, t);   // dS = lower(dO D^T)
     else if (!VEC && warp == 7) {
         // in-tile inclusive cumsum of g (lanes 0..15), in place
         float x = lane < kT ? Gb[lane] : 0.f;
@@ -850,28 +851,9 @@ bwd_tile_kernel(const BcArgs A) {
     // ---- H0 into the state buffer (asynchronous: dH1 is no longer needed)
     stage_state(A.Hst + st);
     cp_async_commit();
-    // ---- W and U; dD = Ke dH1 + S^T dO into Eb (this warp's dv columns)
+    // ---- W and U
     fwd_subst(tid < kD ? Wb : Ub, tid & (kD - 1), Am, bs);
-#pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {
-        uint32_t as[4];
-        load_at(as, Sm, kPd, 0, 8 * ks, g, t);
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            uint32_t b0, b1;
-            load_b(b0, b1, Ob, kLd, 8 * ks, c0 + 8 * nt, g, t);
-            mma8(dd[nt], as, b0, b1);
-        }
-    }
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-        const int col = c0 + 8 * nt + 2 * t;
-        Eb[g * kLd + col] = dd[nt][0];
-        Eb[g * kLd + col + 1] = dd[nt][1];
-        Eb[(g + 8) * kLd + col] = dd[nt][2];
-        Eb[(g + 8) * kLd + col + 1] = dd[nt][3];
-    }
-    cp_async_wait_all();   // H0 landed (own copies); the barrier publishes them and dD
+    cp_async_wait_all();   // H0 landed (own copies); the barrier publishes them
     __syncthreads();
     // ---- dQt_a = dO H0^T and dW = -dD H0^T (this warp's dk columns); dW into Db
     float dq[2][4];
@@ -1173,7 +1155,7 @@ int chunk_bwd_segment_tiles(int64_t tiles, int H, int sms) {
 
 size_t chunk_bwd_scratch_bytes(int64_t tiles, int N, int H) {
     return sizeof(__nv_bfloat16) * (size_t)tiles * H * 2 * kD * kD +
-           sizeof(float) * (size_t)tiles * H * (kT * kD + 1) + sizeof(int) * (size_t)N * H + 5 * 256;
+           sizeof(float) * (size_t)tiles * H * (2 * kT * kD + 1) + sizeof(int) * (size_t)N * H + 6 * 256;
 }
 
 cudaError_t launch_chunk_bwd(const void *q, const void *k, const void *v, const void *a,
@@ -1206,6 +1188,8 @@ cudaError_t launch_chunk_bwd(const void *q, const void *k, const void *v, const 
     A.dHst = (__nv_bfloat16 *)p;
     p += al(sth);
     A.Dst = (float *)p;
+    p += al(sizeof(float) * (size_t)max_tiles * H * kT * kD);
+    A.dDst = (float *)p;
     p += al(sizeof(float) * (size_t)max_tiles * H * kT * kD);
     float *lam = (float *)p;
     p += al(sizeof(float) * (size_t)max_tiles * H);

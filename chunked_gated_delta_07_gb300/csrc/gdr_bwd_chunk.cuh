@@ -22,7 +22,8 @@ struct BcArgs {
     __nv_bfloat16 *dq, *dk, *dv, *da, *dbeta;
     float *dh0;
     __nv_bfloat16 *Hst, *dHst;   // [tiles][H][128][128]: H0, and X = diag(e^{G_C}) dH1
-    float *Dst;                  // [tiles][H][16][128]
+    float *Dst;                  // [tiles][H][16][128]: D of the forward chain
+    float *dDst;                 // [tiles][H][16][128]: dD of the adjoint chain
     const float *lam;            // [tiles][H]: log bound of each tile's transition
     const int *seg_ok;           // [N][H]: 1 if the pair runs in segments
     Plan p;

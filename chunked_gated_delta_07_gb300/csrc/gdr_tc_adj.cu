@@ -18,7 +18,8 @@
 //                                              goes out in bf16 for the tile kernel
 //   tensor cores  dD^T  = dO^T S + X^T Kh^T     kind::f16, then kind::tf32 with the
 //                                              state as the A operand (16 K-steps)
-//   state warps   dD^T -> bf16                 the A operand of the next product
+//   state warps   dD^T -> bf16                 the A operand of the next product; dD
+//                                              also goes out (fp32) for the tile kernel
 //   tensor cores  dH0^T = X^T + dO^T Qt + dD^T (-W)   kind::f16, into the state
 // Every product that reads the state waits (on an mbarrier) for the pass that wrote
 // it, and the pass waits for the products that wrote it before.
@@ -568,7 +569,8 @@ tc_adj_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 break;
             }
             tc_fence_after();
-            // dD^T to bf16: the A operand of dD^T (-W)
+            // dD^T to bf16: the A operand of dD^T (-W); dD of the segment's tiles also goes
+            // out, [C][dv] fp32, for the tile kernel
             {
                 uint32_t dr[kC], a2[kC / 2];
                 tmem_ld16(tm + lane_base + kColD, dr);
@@ -577,6 +579,11 @@ tc_adj_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 for (int i = 0; i < kC / 2; ++i)
                     a2[i] = pack_bf16(__uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1]));
                 tmem_st8(tm + lane_base + kColA, a2);
+                if (hdr->emit) {
+                    float *dst = A.dDst + ((size_t)(tile0 + e0 - 1 - c) * H + h) * kC * kD + e;
+#pragma unroll
+                    for (int i = 0; i < kC; ++i) dst[i * kD] = __uint_as_float(dr[i]);
+                }
             }
             tmem_st_wait();
             tc_fence_before();
