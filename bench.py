@@ -659,13 +659,13 @@ def bench_backward(args):
     # bytes: per (token, head) the inputs q, k, v, dout and a, beta, the gradients dq, dk, dv,
     # da, dbeta (a and da carry dk entries with the per-channel gate); per (sequence, head)
     # h0, dhT and dh0.  The chunked form also writes and reads back, per (16-token tile,
-    # head), the entering state and the end gradient (bf16) and the tile's delta (fp32):
-    # scratch, not algorithmic, reported beside it.
+    # head), the entering state and the scaled end gradient (bf16) and the tile's delta
+    # and its gradient (fp32): scratch, not algorithmic, reported beside it.
     hbm, _, _, _ = peaks()
     ga = 2 * d if vec else 2
     alg_bytes = (2 * (3 * d + d) + ga + 2 + 2 * 3 * d + ga + 2) * N * T * H + 3 * 4 * d * d * N * H
     tiles = N * ((T + 15) // 16)
-    scratch_bytes = 2 * tiles * H * (2 * 2 * d * d + 4 * 16 * d)
+    scratch_bytes = 2 * tiles * H * (2 * 2 * d * d + 2 * 4 * 16 * d)
     bytes_roof = {"bound": "hbm", "algorithmic_bytes": alg_bytes, "scratch_bytes": scratch_bytes,
                   "achieved": alg_bytes / (ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
                   "frac": alg_bytes / (ms / 1e3) / 1e9 / hbm,
