@@ -737,6 +737,9 @@ bwd_tile_kernel(const BcArgs A) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
     const int c0 = 16 * warp;
     const size_t st = ((size_t)c * A.H + h) * kD * kD;
+    // this tile's H0 goes to L2 now (one 128-byte line per thread): the row sums below
+    // and its copy into shared memory then wait on L2 rather than HBM
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(A.Hst + st + threadIdx.x * 64));
     // a bf16 state into Sh and, asynchronously, without registers
     auto stage_state = [&](const __nv_bfloat16 *src) {
 #pragma unroll
