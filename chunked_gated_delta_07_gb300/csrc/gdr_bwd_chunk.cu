@@ -765,9 +765,20 @@ bwd_tile_kernel(const BcArgs A) {
     // registers, and G is formed again from them once V's buffer is free (see below),
     // so that no [16][128] G buffer holds shared memory through the tile
     uint32_t ra_keep[kT / 4] = {};
+    // V, kept in registers for the dV / dbeta pass (same element per thread there), and
+    // the scalar gate's inputs: loaded with the tile's other inputs, before any is used
+    __nv_bfloat16 rv[kT / 2];
+    float av = 0.f;
     {
         StageRegs R;
         stage_fetch<VEC>(A, t0, len, h, true, A.dout, R);
+#pragma unroll
+        for (int m = 0; m < kT / 2; ++m) {
+            const int i = (tid >> 7) + 2 * m, col = tid & (kD - 1);
+            rv[m] = i < len ? A.v[((t0 + i) * A.H + h) * kD + col] : __float2bfloat16_rn(0.f);
+        }
+        if (!VEC && tid >= kThreads - kT && tid - (kThreads - kT) < len)
+            av = __bfloat162float(A.a[(t0 + tid - (kThreads - kT)) * A.H + h]);
         stage_compute(A, len, R, Kt, Kh, Qt, nullptr, eg, true, Ob, bs);
         if (VEC)
 #pragma unroll
@@ -776,11 +787,10 @@ bwd_tile_kernel(const BcArgs A) {
                              ((uint32_t)__bfloat16_as_ushort(R.ra[2 * m + 1]) << 16);
     }
     if (!VEC && tid >= kThreads - kT) {
-        // scalar gate: g and g'(a) per token, one load each (the cumsum follows the barrier)
+        // scalar gate: g and g'(a) per token (the cumsum follows the barrier)
         const int i = tid - (kThreads - kT);
         float gi = 0.f, dgi = 0.f;
         if (i < len) {
-            const float av = __bfloat162float(A.a[(t0 + i) * A.H + h]);
             const float sg = 1.f / (1.f + expf(-av));
             gi = -A.b * sg;
             dgi = -A.b * sg * (1.f - sg);
@@ -788,12 +798,9 @@ bwd_tile_kernel(const BcArgs A) {
         Gb[i] = gi;
         Gb[kT + i] = dgi;
     }
-    // V, kept in registers for the dV / dbeta pass (same element per thread there)
-    __nv_bfloat16 rv[kT / 2];
 #pragma unroll
     for (int m = 0; m < kT / 2; ++m) {
         const int i = (tid >> 7) + 2 * m, col = tid & (kD - 1);
-        rv[m] = i < len ? A.v[((t0 + i) * A.H + h) * kD + col] : __float2bfloat16_rn(0.f);
         Ub[i * kLd + col] = __bfloat162float(rv[m]);
     }
     cp_async_wait_all();
