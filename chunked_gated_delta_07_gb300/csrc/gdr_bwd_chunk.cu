@@ -807,6 +807,12 @@ bwd_tile_kernel(const BcArgs A) {
     __syncthreads();
     // ---- dKe (.) e^{G_C} = D X^T (this warp's dk columns), then the 16 x 16 products
     // (dD = S^T dO + Kh X comes from the adjoint chain, which forms it for its own step)
+    // this warp's H0 rows for the row sums below, loaded first so that the product's
+    // time covers their latency
+    const __nv_bfloat16 *H0g = A.Hst + st;
+    uint2 xh[kD / 8];
+#pragma unroll
+    for (int m = 0; m < kD / 8; ++m) xh[m] = *(const uint2 *)&H0g[(warp + 8 * m) * kD + 4 * lane];
     float dke[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
@@ -826,10 +832,6 @@ bwd_tile_kernel(const BcArgs A) {
     // e^{G_C} rowsum(dH1 (.) H0) = rowsum(X (.) H0): X from shared memory, H0 rows from
     // the stored copy
     {
-        const __nv_bfloat16 *H0g = A.Hst + st;
-        uint2 xh[kD / 8];
-#pragma unroll
-        for (int m = 0; m < kD / 8; ++m) xh[m] = *(const uint2 *)&H0g[(warp + 8 * m) * kD + 4 * lane];
 #pragma unroll
         for (int m = 0; m < kD / 8; ++m) {
             const int r = warp + 8 * m;
