@@ -730,10 +730,6 @@ bwd_tile_kernel(const BcArgs A) {
     __nv_bfloat16 *Sh = (__nv_bfloat16 *)(sm + L::sh);
     const int64_t c = blockIdx.x;
     const int h = blockIdx.y;
-    const int n = find_owner(A.p.chunk_base, A.p.N, c);
-    if (n < 0) return;
-    const int64_t t0 = A.p.seq_start[n] + (c - A.p.chunk_base[n]) * kT;
-    const int len = (int)min((int64_t)kT, A.p.seq_start[n + 1] - t0);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
     const int c0 = 16 * warp;
     const size_t st = ((size_t)c * A.H + h) * kD * kD;
@@ -761,15 +757,24 @@ bwd_tile_kernel(const BcArgs A) {
         }
     }
     cp_async_commit();
+    // the tile's sequence and tokens (its copies above need only the tile index); a block
+    // past the last tile leaves once its own copies have landed
+    const int n = find_owner(A.p.chunk_base, A.p.N, c);
+    if (n < 0) {
+        cp_async_wait_all();
+        return;
+    }
+    const int64_t t0 = A.p.seq_start[n] + (c - A.p.chunk_base[n]) * kT;
+    const int len = (int)min((int64_t)kT, A.p.seq_start[n + 1] - t0);
     // per-channel gate: the raw inputs of this thread's (channel, 8 tokens) stay packed in
     // registers, and G is formed again from them once V's buffer is free (see below),
     // so that no [16][128] G buffer holds shared memory through the tile
     uint32_t ra_keep[kT / 4] = {};
     // V, kept in registers for the dV / dbeta pass (same element per thread there), and
     // the scalar gate's inputs: loaded with the tile's other inputs, before any is used
-    __nv_bfloat16 rv[kT / 2];
-    float av = 0.f;
-    {
+    __nv_bfloat16 rv[kT / 2];   // per-channel gate: V by (channel, token pair)
+    uint4 rv8 = make_uint4(0, 0, 0, 0);   // scalar gate: V by (token, 8 channels)
+    if constexpr (VEC) {
         StageRegs R;
         stage_fetch<VEC>(A, t0, len, h, true, A.dout, R);
 #pragma unroll
@@ -777,31 +782,85 @@ bwd_tile_kernel(const BcArgs A) {
             const int i = (tid >> 7) + 2 * m, col = tid & (kD - 1);
             rv[m] = i < len ? A.v[((t0 + i) * A.H + h) * kD + col] : __float2bfloat16_rn(0.f);
         }
-        if (!VEC && tid >= kThreads - kT && tid - (kThreads - kT) < len)
-            av = __bfloat162float(A.a[(t0 + tid - (kThreads - kT)) * A.H + h]);
-        stage_compute(A, len, R, Kt, Kh, Qt, nullptr, eg, true, Ob, bs);
-        if (VEC)
+        stage_compute(A, len, R, Kt, Kh, Qt, nullptr, eg, A.dout != nullptr, Ob, bs);
 #pragma unroll
-            for (int m = 0; m < kT / 4; ++m)
-                ra_keep[m] = (uint32_t)__bfloat16_as_ushort(R.ra[2 * m]) |
-                             ((uint32_t)__bfloat16_as_ushort(R.ra[2 * m + 1]) << 16);
-    }
-    if (!VEC && tid >= kThreads - kT) {
-        // scalar gate: g and g'(a) per token (the cumsum follows the barrier)
-        const int i = tid - (kThreads - kT);
-        float gi = 0.f, dgi = 0.f;
-        if (i < len) {
-            const float sg = 1.f / (1.f + expf(-av));
-            gi = -A.b * sg;
-            dgi = -A.b * sg * (1.f - sg);
+        for (int m = 0; m < kT / 4; ++m)
+            ra_keep[m] = (uint32_t)__bfloat16_as_ushort(R.ra[2 * m]) |
+                         ((uint32_t)__bfloat16_as_ushort(R.ra[2 * m + 1]) << 16);
+#pragma unroll
+        for (int m = 0; m < kT / 2; ++m) {
+            const int i = (tid >> 7) + 2 * m, col = tid & (kD - 1);
+            Ub[i * kLd + col] = __bfloat162float(rv[m]);
         }
-        Gb[i] = gi;
-        Gb[kT + i] = dgi;
-    }
+    } else {
+        // thread (token si, channels 8 sch .. 8 sch + 7): one 16-byte load per tensor; the
+        // gate of the tile's 16 tokens is formed in every warp (lanes 0..15), G by an
+        // inclusive prefix sum over the lanes
+        const int si = tid >> 4, sch = tid & 15;
+        uint4 rq = make_uint4(0, 0, 0, 0), rk = rq, rdo = rq;
+        float a_l = 0.f, b_l = 0.f;
+        if (si < len) {
+            const int64_t off = ((t0 + si) * A.H + h) * kD + 8 * sch;
+            rq = *(const uint4 *)(A.q + off);
+            rk = *(const uint4 *)(A.k + off);
+            if (A.dout) rdo = *(const uint4 *)(A.dout + off);   // NULL: zero
+            rv8 = *(const uint4 *)(A.v + off);
+        }
+        if (lane < len) {
+            const int64_t row = (t0 + lane) * A.H + h;
+            a_l = __bfloat162float(A.a[row]);
+            b_l = __bfloat162float(A.beta[row]);
+        }
+        float G_l = lane < len ? gate_logdecay(a_l, A.b, GDR_GATE_BOUNDED) : 0.f;
 #pragma unroll
-    for (int m = 0; m < kT / 2; ++m) {
-        const int i = (tid >> 7) + 2 * m, col = tid & (kD - 1);
-        Ub[i * kLd + col] = __bfloat162float(rv[m]);
+        for (int o = 1; o < kT; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, G_l, o);
+            if (lane >= o) G_l += y;
+        }
+        const float Gi = __shfl_sync(0xffffffffu, G_l, si & (kT - 1));
+        const float GC = __shfl_sync(0xffffffffu, G_l, kT - 1);   // lanes past the end add 0
+        const float bi = __shfl_sync(0xffffffffu, b_l, si & (kT - 1));
+        const float e = expf(Gi), en = expf(-Gi);
+        const uint32_t wq[4] = {rq.x, rq.y, rq.z, rq.w}, wk[4] = {rk.x, rk.y, rk.z, rk.w};
+        const uint32_t wo[4] = {rdo.x, rdo.y, rdo.z, rdo.w}, wv[4] = {rv8.x, rv8.y, rv8.z, rv8.w};
+        float kt[8], kh[8], qt[8], ob[8], ub[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float kd = bf_half(wk[u >> 1], u & 1);
+            kt[u] = kd * e;
+            kh[u] = kd * en;
+            qt[u] = bf_half(wq[u >> 1], u & 1) * e;
+            ob[u] = bf_half(wo[u >> 1], u & 1);
+            ub[u] = bf_half(wv[u >> 1], u & 1);
+        }
+        const int so = si * kLd + 8 * sch;
+        *(float4 *)&Kt[so] = make_float4(kt[0], kt[1], kt[2], kt[3]);
+        *(float4 *)&Kt[so + 4] = make_float4(kt[4], kt[5], kt[6], kt[7]);
+        *(float4 *)&Kh[so] = make_float4(kh[0], kh[1], kh[2], kh[3]);
+        *(float4 *)&Kh[so + 4] = make_float4(kh[4], kh[5], kh[6], kh[7]);
+        *(float4 *)&Qt[so] = make_float4(qt[0], qt[1], qt[2], qt[3]);
+        *(float4 *)&Qt[so + 4] = make_float4(qt[4], qt[5], qt[6], qt[7]);
+        *(float4 *)&Ob[so] = make_float4(ob[0], ob[1], ob[2], ob[3]);
+        *(float4 *)&Ob[so + 4] = make_float4(ob[4], ob[5], ob[6], ob[7]);
+        *(float4 *)&Ub[so] = make_float4(ub[0], ub[1], ub[2], ub[3]);
+        *(float4 *)&Ub[so + 4] = make_float4(ub[4], ub[5], ub[6], ub[7]);
+        if (si == 0) {
+            const float eGC = expf(GC);
+            *(float4 *)&eg[8 * sch] = make_float4(eGC, eGC, eGC, eGC);
+            *(float4 *)&eg[8 * sch + 4] = make_float4(eGC, eGC, eGC, eGC);
+        }
+        if (sch == 0) bs[si] = si < len ? bi : 0.f;
+        if (warp == kThreads / 32 - 1 && lane < kT) {
+            // g and g'(a) per token for the outputs and da (the cumsum follows the barrier)
+            float gi = 0.f, dgi = 0.f;
+            if (lane < len) {
+                const float sg = 1.f / (1.f + expf(-a_l));
+                gi = -A.b * sg;
+                dgi = -A.b * sg * (1.f - sg);
+            }
+            Gb[lane] = gi;
+            Gb[kT + lane] = dgi;
+        }
     }
     cp_async_wait_all();
     __syncthreads();
@@ -932,9 +991,38 @@ bwd_tile_kernel(const BcArgs A) {
         bdA[i1 * kPd + ja] = bs[i1] * v10;
         bdA[i1 * kPd + jb] = bs[i1] * v11;
     }
-    // dV = diag(beta) dYu, and the per-token sums dYu . V + dYw . Kt for dbeta: thread
-    // (tid & 127) takes one column of rows (tid >> 7), (tid >> 7) + 2, ...
-    {
+    // dV = diag(beta) dYu, and the per-token sums dYu . V + dYw . Kt for dbeta: the
+    // scalar gate's staging thread (token i, 8 channels), a 16-byte store of dV each
+    if constexpr (!VEC) {
+        const int i = tid >> 4, ch = tid & 15;
+        float x = 0.f;
+        if (i < len) {
+            const int so = i * kLd + 8 * ch;
+            const float4 y0 = *(const float4 *)&Eb[so], y1 = *(const float4 *)&Eb[so + 4];
+            const float4 d0 = *(const float4 *)&Db[so], d1 = *(const float4 *)&Db[so + 4];
+            const float4 k0 = *(const float4 *)&Kt[so], k1 = *(const float4 *)&Kt[so + 4];
+            const float yu[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+            const float dw[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+            const float kt[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+            const uint32_t wv[4] = {rv8.x, rv8.y, rv8.z, rv8.w};
+            const float bi = bs[i];
+            uint32_t pv[4];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) x = fmaf(yu[u], bf_half(wv[u >> 1], u & 1), fmaf(dw[u], kt[u], x));
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                __nv_bfloat162 v2 = __floats2bfloat162_rn(bi * yu[2 * m], bi * yu[2 * m + 1]);
+                pv[m] = *reinterpret_cast<uint32_t *>(&v2);
+            }
+            *(uint4 *)(A.dv + ((t0 + i) * A.H + h) * kD + 8 * ch) = make_uint4(pv[0], pv[1], pv[2], pv[3]);
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);   // the 16 lanes of token i
+        if (ch == 0) {
+            rowsum[i * 4] = x;
+            rowsum[i * 4 + 1] = rowsum[i * 4 + 2] = rowsum[i * 4 + 3] = 0.f;
+        }
+    } else {
         const int col = tid & (kD - 1), half = tid >> 7;
 #pragma unroll
         for (int m = 0; m < kT / 2; ++m) {

@@ -633,6 +633,8 @@ cudaError_t launch_impl(const CUtensorMap &mq, const CUtensorMap &mk, const CUte
 cudaError_t launch_tc_adj(const bwdc::BcArgs &A, bool per_channel, int64_t T_total, int64_t max_tiles,
                           int64_t max_segs, int *status, cudaStream_t stream) {
     CUtensorMap mq, mk, mo, ma;
+    if (!A.dout)   // dout = NULL (zero): the mma.sync chain reads it as zero
+        return cudaErrorNotSupported;
     if (!tc_make_map(&mq, A.q, A.H, T_total) || !tc_make_map(&mk, A.k, A.H, T_total) ||
         !tc_make_map(&mo, A.dout, A.H, T_total))
         return cudaErrorNotSupported;

@@ -180,3 +180,23 @@ def test_chain_kernels_agree(monkeypatch, T, a_mean, h0, chains):
     for name in NAMES:
         r = rel_l2(to64(tc[name]), to64(mma[name]))
         assert r <= 1e-2, f"{name}: tcgen05 vs mma.sync chains rel-L2 {r:.3e}"
+
+
+@pytest.mark.parametrize("dout,dhT", [(False, True), (True, False)])
+def test_chunked_backward_optional_arguments(dout, dhT):
+    """bf16, d = 128 (the chunked form): dout = NULL (zero) and dhT = NULL (zero)."""
+    x = _inputs("bf16", 128, 700, "bounded", seed=4950, N=2, H=2)
+    got, ref = _run(x, "bounded", dout=dout, dhT=dhT)
+    _check(got, ref, "bf16")
+
+
+def test_chunked_backward_unaligned_inputs_take_the_token_form():
+    """q one element off a 16-byte boundary: the call runs token by token (its tile
+    kernel moves whole 16-byte pieces) and still matches the oracle."""
+    x = _inputs("bf16", 128, 200, "bounded", seed=4960, N=1, H=2)
+    big = torch.empty(x["q"].numel() + 1, dtype=x["q"].dtype, device="cuda")
+    big[1:].copy_(x["q"].reshape(-1))
+    x["q"] = big[1:].view(x["q"].shape)
+    assert x["q"].data_ptr() % 16 != 0
+    got, ref = _run(x, "bounded")
+    _check(got, ref, "bf16")

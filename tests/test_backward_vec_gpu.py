@@ -116,3 +116,15 @@ def test_vec_chain_kernels_agree(monkeypatch, T, a_mean):
     for name in NAMES:
         r = rel_l2(to64(tc[name]), to64(mma[name]))
         assert r <= 1e-2, f"{name}: tcgen05 vs mma.sync chains rel-L2 {r:.3e}"
+
+
+def test_vec_backward_without_dout():
+    """dout = NULL (zero) on the per-channel chunked form."""
+    x = _inputs(500, seed=7500, N=1, H=2)
+    got = gdr.chunk_bwd_vec(x["q"], x["k"], x["v"], x["av"], x["beta"], dout=None, dhT=x["dhT"],
+                            h0=x["h0"], b=2.0)
+    torch.cuda.synchronize()
+    assert gdr.gdr_get_status() == gdr.GDR_OK
+    ref = oracle.oracle_bwd_vec(x["q"], x["k"], x["v"], x["av"], x["beta"], dout=None, dhT=x["dhT"],
+                                h0=x["h0"], b=2.0)
+    _check(dict(zip(NAMES, got)), ref)
