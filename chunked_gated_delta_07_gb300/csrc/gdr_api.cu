@@ -729,10 +729,12 @@ static gdr_status_t chunk_bwd_impl(const void *q, const void *k, const void *v, 
     const size_t plan_b = align_up(3 * sizeof(int64_t) * (size_t)(B + 1));
     // the chunked tensor-core form takes bf16, d = 128 and the bounded gate (its
     // factored in-tile decays need exp(16 b) < FLT_MAX); the rest runs token by token
-    // (the scalar gate's tile kernel moves q, k, v, dout and dv in 16-byte pieces)
+    // (the scalar gate's tile kernel moves q, k, v, dout and dv in 16-byte pieces, dq and
+    // dk in 4-byte pairs)
     const bool chunked = per_channel || (dtype == GDR_BF16 && dk == 128 && dv == 128 &&
                                          gate == GDR_GATE_BOUNDED && b <= kVecMaxB && al16(q) && al16(k) &&
-                                         al16(v) && al16(dout) && al16(dv_out) && !bwd_force_token_path());
+                                         al16(v) && al16(dout) && al16(dv_out) && al16(dq) && al16(dk_out) &&
+                                         !bwd_force_token_path());
     const int seg = chunked ? chunk_bwd_segment_tiles(tiles, H, ctx->sms) : (1 << 30);
     const int64_t segs = s.varlen ? (tiles + seg - 1) / seg + B : (int64_t)B * ((tiles / B + seg - 1) / seg);
     const size_t need = plan_b + (chunked ? chunk_bwd_scratch_bytes(tiles, B, H)

@@ -712,7 +712,7 @@ template <bool VEC> struct TileLayout {
                          am = eb + kTile2, kk = am + kT * kPd,
                          ds = kk + kT * kPd, da = ds + kT * kPd, bda = da + kT * kPd,
                          eg = bda + kT * kPd, rg = eg + kD, bs = rg + kD, rs = bs + kT,
-                         rs2 = rs + 4 * kT, gb = rs2 + kT, sh = gb + 2 * kT, total_f = sh;
+                         rs2 = rs + 4 * kT, gb = rs2 + kT, egt = gb + 2 * kT, sh = egt + 2 * kT, total_f = sh;
     static constexpr size_t bytes = sizeof(float) * total_f + sizeof(__nv_bfloat16) * kD * kLdh;
 };
 
@@ -727,6 +727,7 @@ bwd_tile_kernel(const BcArgs A) {
     float *bdA = sm + L::bda, *eg = sm + L::eg, *rG = sm + L::rg, *bs = sm + L::bs, *rowsum = sm + L::rs;
     float *rowsum2 = sm + L::rs2;   // per-token dG sums for da
     float *Gb = sm + L::gb;
+    float *eGt = sm + L::egt;   // scalar gate: e^{G_i}, then e^{-G_i}, per token
     __nv_bfloat16 *Sh = (__nv_bfloat16 *)(sm + L::sh);
     const int64_t c = blockIdx.x;
     const int h = blockIdx.y;
@@ -914,7 +915,11 @@ bwd_tile_kernel(const BcArgs A) {
             const float y = __shfl_up_sync(0xffffffffu, x, o);
             if (lane >= o) x += y;
         }
-        if (lane < kT) Gb[lane] = x;
+        if (lane < kT) {
+            Gb[lane] = x;
+            eGt[lane] = expf(x);
+            eGt[kT + lane] = expf(-x);
+        }
     }
     if (tid < kD)
         for (int i = 0; i < kT; ++i) Wb[i * kLd + tid] = Kt[i * kLd + tid];
@@ -1094,19 +1099,35 @@ bwd_tile_kernel(const BcArgs A) {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int i = g + 8 * (u >> 1), d = c0 + 8 * nt + 2 * t + (u & 1);
-                const float kt = Kt[i * kLd + d], kh = Kh[i * kLd + d], qt = Qt[i * kLd + d];
-                const float dKt = dkt[nt][u] + bs[i] * Db[i * kLd + d];
-                const float dKh = dkh[nt][u] + dke[nt][u];   // dke = D X^T = dKe (.) e^{G_C}
-                Ob[i * kLd + d] = dq[nt][u] * qt + dKt * kt - dKh * kh;
-                if (i < len) {
-                    const float G = VEC ? Gv[i * kLd + d] : Gv[i];
-                    const int64_t r = ((t0 + i) * A.H + h) * kD + d;
-                    A.dq[r] = __float2bfloat16_rn(dq[nt][u] * expf(G));
-                    A.dk[r] = __float2bfloat16_rn(dKt * expf(G) + dKh * expf(-G));
+            for (int hr = 0; hr < 2; ++hr) {   // the pair (u, u + 1) = columns (d, d + 1) of row i
+                const int i = g + 8 * hr, d = c0 + 8 * nt + 2 * t;
+                float oq[2], ok[2];
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    const int u = 2 * hr + w, dd = d + w;
+                    const float kt = Kt[i * kLd + dd], kh = Kh[i * kLd + dd], qt = Qt[i * kLd + dd];
+                    const float dKt = dkt[nt][u] + bs[i] * Db[i * kLd + dd];
+                    const float dKh = dkh[nt][u] + dke[nt][u];   // dke = D X^T = dKe (.) e^{G_C}
+                    Ob[i * kLd + dd] = dq[nt][u] * qt + dKt * kt - dKh * kh;
+                    // e^G and e^-G: per (token, channel), or per token from the table (scalar gate)
+                    const float ep = VEC ? expf(Gv[i * kLd + dd]) : eGt[i];
+                    const float em = VEC ? expf(-Gv[i * kLd + dd]) : eGt[kT + i];
+                    oq[w] = dq[nt][u] * ep;
+                    ok[w] = dKt * ep + dKh * em;
+                    dke[nt][u] *= kh;   // dKe (.) Ke, summed over the tile below
                 }
-                dke[nt][u] *= kh;   // dKe (.) Ke, summed over the tile below
+                if (i < len) {
+                    const int64_t r = ((t0 + i) * A.H + h) * kD + d;
+                    if constexpr (VEC) {   // (dq and dk of any alignment)
+                        A.dq[r] = __float2bfloat16_rn(oq[0]);
+                        A.dq[r + 1] = __float2bfloat16_rn(oq[1]);
+                        A.dk[r] = __float2bfloat16_rn(ok[0]);
+                        A.dk[r + 1] = __float2bfloat16_rn(ok[1]);
+                    } else {   // (the scalar gate's chunked form takes 16-byte aligned outputs)
+                        *(__nv_bfloat162 *)&A.dq[r] = __floats2bfloat162_rn(oq[0], oq[1]);
+                        *(__nv_bfloat162 *)&A.dk[r] = __floats2bfloat162_rn(ok[0], ok[1]);
+                    }
+                }
             }
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
