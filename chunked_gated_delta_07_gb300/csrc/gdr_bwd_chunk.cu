@@ -712,7 +712,8 @@ template <bool VEC> struct TileLayout {
                          am = eb + kTile2, kk = am + kT * kPd,
                          ds = kk + kT * kPd, da = ds + kT * kPd, bda = da + kT * kPd,
                          eg = bda + kT * kPd, rg = eg + kD, bs = rg + kD, rs = bs + kT,
-                         rs2 = rs + 4 * kT, gb = rs2 + kT, egt = gb + 2 * kT, sh = egt + 2 * kT, total_f = sh;
+                         gb = rs + 4 * kT + kT, egt = gb + 2 * kT, dgp = egt + 2 * kT,
+                         sh = dgp + 8 * kT, total_f = sh;
     static constexpr size_t bytes = sizeof(float) * total_f + sizeof(__nv_bfloat16) * kD * kLdh;
 };
 
@@ -725,9 +726,9 @@ bwd_tile_kernel(const BcArgs A) {
     float *Ub = sm + L::ub, *Wb = sm + L::wb, *Eb = sm + L::eb;
     float *Am = sm + L::am, *KK = sm + L::kk, *dS = sm + L::ds, *dA = sm + L::da;
     float *bdA = sm + L::bda, *eg = sm + L::eg, *rG = sm + L::rg, *bs = sm + L::bs, *rowsum = sm + L::rs;
-    float *rowsum2 = sm + L::rs2;   // per-token dG sums for da
     float *Gb = sm + L::gb;
     float *eGt = sm + L::egt;   // scalar gate: e^{G_i}, then e^{-G_i}, per token
+    float *dGp = sm + L::dgp;   // scalar gate: per (warp, token) partial sums of dG
     __nv_bfloat16 *Sh = (__nv_bfloat16 *)(sm + L::sh);
     const int64_t c = blockIdx.x;
     const int h = blockIdx.y;
@@ -1096,6 +1097,7 @@ bwd_tile_kernel(const BcArgs A) {
             }
         }
         if (VEC) __syncthreads();   // G (written above by other threads) is complete
+        float pg[2] = {0.f, 0.f};   // scalar gate: this thread's part of dG's row sums (rows g, g + 8)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -1108,7 +1110,9 @@ bwd_tile_kernel(const BcArgs A) {
                     const float kt = Kt[i * kLd + dd], kh = Kh[i * kLd + dd], qt = Qt[i * kLd + dd];
                     const float dKt = dkt[nt][u] + bs[i] * Db[i * kLd + dd];
                     const float dKh = dkh[nt][u] + dke[nt][u];   // dke = D X^T = dKe (.) e^{G_C}
-                    Ob[i * kLd + dd] = dq[nt][u] * qt + dKt * kt - dKh * kh;
+                    const float dG = dq[nt][u] * qt + dKt * kt - dKh * kh;
+                    if constexpr (VEC) Ob[i * kLd + dd] = dG;
+                    else pg[hr] += dG;
                     // e^G and e^-G: per (token, channel), or per token from the table (scalar gate)
                     const float ep = VEC ? expf(Gv[i * kLd + dd]) : eGt[i];
                     const float em = VEC ? expf(-Gv[i * kLd + dd]) : eGt[kT + i];
@@ -1138,6 +1142,15 @@ bwd_tile_kernel(const BcArgs A) {
                 for (int o = 4; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
                 if (g == 0) rG[c0 + 8 * nt + 2 * t + u] += x;
             }
+        if constexpr (!VEC) {   // dG's row sums over this warp's 16 columns
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                float x = pg[hr];
+                x += __shfl_xor_sync(0xffffffffu, x, 1);
+                x += __shfl_xor_sync(0xffffffffu, x, 2);
+                if (t == 0) dGp[warp * kT + g + 8 * hr] = x;
+            }
+        }
     }
     __syncthreads();
     // ---- dbeta (threads 0..15, one token each)
@@ -1161,19 +1174,19 @@ bwd_tile_kernel(const BcArgs A) {
             }
         }
     } else {
-        if (warp < 4) {
-            for (int i = warp; i < kT; i += 4) {
-                float x = 0.f;
-                for (int d = lane; d < kD; d += 32) x += Ob[i * kLd + d] + (i == len - 1 ? rG[d] : 0.f);
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-                if (lane == 0) rowsum2[i] = x;
-            }
-        }
-        __syncthreads();
         if (warp == 0) {
-            // reverse cumsum over the tile's tokens (lanes 0..15), times g'(a)
-            float x = lane < len ? rowsum2[lane] : 0.f;
+            // per token: dG's row sum (the warps' partial sums), the last token also
+            // carries dG_C summed over the channels; then the reverse cumsum over the
+            // tile's tokens (lanes 0..15), times g'(a)
+            float rgs = rG[lane] + rG[lane + 32] + rG[lane + 64] + rG[lane + 96];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) rgs += __shfl_xor_sync(0xffffffffu, rgs, o);
+            float x = 0.f;
+            if (lane < len) {
+#pragma unroll
+                for (int w = 0; w < kThreads / 32; ++w) x += dGp[w * kT + lane];
+                if (lane == len - 1) x += rgs;
+            }
 #pragma unroll
             for (int o = 1; o < kT; o <<= 1) {
                 const float y = __shfl_down_sync(0xffffffffu, x, o);
