@@ -893,6 +893,9 @@ bwd_tile_kernel(const BcArgs A) {
     // e^{G_C} rowsum(dH1 (.) H0) = rowsum(X (.) H0): X from shared memory, H0 rows from
     // the stored copy
     {
+        // this lane's part of the 16 rows (warp + 8 m), then one halving reduction over the
+        // warp for all of them: lane pair (2m, 2m + 1) ends with row warp + 8 m
+        float pr[kT];
 #pragma unroll
         for (int m = 0; m < kD / 8; ++m) {
             const int r = warp + 8 * m;
@@ -900,11 +903,10 @@ bwd_tile_kernel(const BcArgs A) {
             const __nv_bfloat162 *x2 = (const __nv_bfloat162 *)&xh[m], *y2 = (const __nv_bfloat162 *)&yh;
             const float2 xa = __bfloat1622float2(x2[0]), xb = __bfloat1622float2(x2[1]);
             const float2 ya = __bfloat1622float2(y2[0]), yb = __bfloat1622float2(y2[1]);
-            float pr = xa.x * ya.x + xa.y * ya.y + xb.x * yb.x + xb.y * yb.y;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) pr += __shfl_xor_sync(0xffffffffu, pr, o);
-            if (lane == 0) rG[r] = pr;
+            pr[m] = xa.x * ya.x + xa.y * ya.y + xb.x * yb.x + xb.y * yb.y;
         }
+        fold16<false>(pr, lane);
+        if ((lane & 1) == 0) rG[warp + 8 * (lane >> 1)] = pr[0];
     }
     if (warp < 2) build_A(Kt, Kh, bs, Am, KK, warp, g, t);
     else if (warp < 4) build_lower(Ob, Db, dS, warp - 2, g, t);   // dS = lower(dO D^T)
@@ -1157,7 +1159,12 @@ bwd_tile_kernel(const BcArgs A) {
     if (tid < kT && tid < len) {
         const int i = tid;
         float acc = rowsum[i * 4] + rowsum[i * 4 + 1] + rowsum[i * 4 + 2] + rowsum[i * 4 + 3];
-        for (int j = 0; j < i; ++j) acc = fmaf(dA[i * kPd + j], KK[i * kPd + j], acc);
+        // sum_j dA_ij (Kt Kh^T)_ij over the whole row: dA is 0 on and above the diagonal
+#pragma unroll
+        for (int j4 = 0; j4 < kT; j4 += 4) {
+            const float4 a4 = *(const float4 *)&dA[i * kPd + j4], k4 = *(const float4 *)&KK[i * kPd + j4];
+            acc = fmaf(a4.x, k4.x, fmaf(a4.y, k4.y, fmaf(a4.z, k4.z, fmaf(a4.w, k4.w, acc))));
+        }
         A.dbeta[(t0 + i) * A.H + h] = __float2bfloat16_rn(acc);
     }
     // ---- da: the last token also carries dG_C; reverse cumsum over the tile
