@@ -1032,20 +1032,32 @@ bwd_tile_kernel(const BcArgs A) {
         }
     } else {
         const int col = tid & (kD - 1), half = tid >> 7;
+        float x[kT / 2];
 #pragma unroll
         for (int m = 0; m < kT / 2; ++m) {
             const int i = half + 2 * m;
-            float x = 0.f;
+            x[m] = 0.f;
             if (i < len) {
                 const int64_t r = ((t0 + i) * A.H + h) * kD + col;
                 const float yu = Eb[i * kLd + col];
                 A.dv[r] = __float2bfloat16_rn(bs[i] * yu);
-                x = fmaf(yu, __bfloat162float(rv[m]), Db[i * kLd + col] * Kt[i * kLd + col]);
+                x[m] = fmaf(yu, __bfloat162float(rv[m]), Db[i * kLd + col] * Kt[i * kLd + col]);
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-            if (lane == 0) rowsum[i * 4 + (warp & 3)] = x;   // 4 warps per half
         }
+        // the 8 row sums by one halving exchange: row half + 2 ((lane >> 1) & 7) in x[0]
+        // of the lanes with bits 0 and 4 clear
+#pragma unroll
+        for (int w = kT / 4; w >= 1; w >>= 1) {
+            const bool hi = (lane & (2 * w)) != 0;
+#pragma unroll
+            for (int j = 0; j < w; ++j) {
+                const float keep = hi ? x[j + w] : x[j], send = hi ? x[j] : x[j + w];
+                x[j] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * w);
+            }
+        }
+        x[0] += __shfl_xor_sync(0xffffffffu, x[0], 1);
+        x[0] += __shfl_xor_sync(0xffffffffu, x[0], 16);
+        if ((lane & 17) == 0) rowsum[(half + 2 * ((lane >> 1) & 7)) * 4 + (warp & 3)] = x[0];   // 4 warps per half
     }
     __syncthreads();
     // ---- per-channel gate: G again, into V's buffer (its last reader was dA, above), in
