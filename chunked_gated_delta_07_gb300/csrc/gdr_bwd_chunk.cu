@@ -56,6 +56,10 @@ constexpr int kTile2 = kT * kLd;   // floats of one [16][kLd] buffer
 constexpr int kSegMin = 64, kSegMax = 256;   // segment lengths in tiles
 constexpr int kWarmFactor = 4;   // longest warm-up, in segments
 constexpr int kLdh = 136;               // row stride (elements) of the bf16 state in shared memory
+// row stride of the per-tile kernel's fp32 [16][.] buffers: 8 mod 32 words, so that its
+// k-permuted fragment loads (8 bytes per lane) meet no bank conflict
+constexpr int kLt = 136;
+constexpr int kTileT = kT * kLt;
 
 using bwdc::BcArgs;
 using bwdc::kHorizonLog;
@@ -91,6 +95,7 @@ __device__ __forceinline__ void stage_fetch(const BcArgs &A, int64_t t0, int len
     R.bt = tid < len ? __bfloat162float(A.beta[(t0 + tid) * A.H + h]) : 0.f;
 }
 
+template <int LD = kLd>
 __device__ __forceinline__ void stage_compute(const BcArgs &A, int len, const StageRegs &R, float *Kt,
                                               float *Kh, float *Qt, float *Gb, float *eg, bool has_other,
                                               float *Ob, float *bs) {
@@ -119,11 +124,11 @@ __device__ __forceinline__ void stage_compute(const BcArgs &A, int len, const St
             eGC = e;
             gg = G;
         }
-        Kt[i * kLd + d] = kt;
-        Kh[i * kLd + d] = kh;
-        if (Qt) Qt[i * kLd + d] = qt;
-        if (Gb) Gb[i * kLd + d] = gg;
-        Ob[i * kLd + d] = ov;
+        Kt[i * LD + d] = kt;
+        Kh[i * LD + d] = kh;
+        if (Qt) Qt[i * LD + d] = qt;
+        if (Gb) Gb[i * LD + d] = gg;
+        Ob[i * LD + d] = ov;
     }
     const float eo = __shfl_xor_sync(0xffffffffu, eGC, 1);
     if (half == 0) eg[d] = len > 8 ? eo : eGC;
@@ -218,53 +223,62 @@ __device__ __forceinline__ void stage_tile(const BcArgs &A, int64_t t0, int len,
 
 // 16 x 16 product X Y^T over K = 128 (one 8-column half of the output per warp):
 // out[i][j] for j in j0..j0+7.
+template <int LD = kLd>
 __device__ __forceinline__ void gram_half(float (&acc)[4], const float *X, const float *Y, int j0,
                                           int g, int t) {
     acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
 #pragma unroll 4
     for (int k0 = 0; k0 < kD; k0 += 8) {
         uint32_t af[4], b0, b1;
-        load_a(af, X, kLd, 0, k0, g, t);
-        load_bt(b0, b1, Y, kLd, k0, j0, g, t);
+        if constexpr (LD % 32 == 8) {
+            load_a_kp(af, X, LD, 0, k0, g, t);
+            load_bt_kp(b0, b1, Y, LD, k0, j0, g, t);
+        } else {
+            load_a(af, X, LD, 0, k0, g, t);
+            load_bt(b0, b1, Y, LD, k0, j0, g, t);
+        }
         mma8(acc, af, b0, b1);
     }
 }
 
 // Forward substitution x = (I + A)^{-1} diag(beta) y on one column of a [16][kLd]
 // buffer, in place (A strictly lower, row stride kPd).
+template <int LD = kLd>
 __device__ __forceinline__ void fwd_subst(float *X, int col, const float *Am, const float *bs) {
     float x[kT];
 #pragma unroll
     for (int i = 0; i < kT; ++i) {
-        float acc = bs[i] * X[i * kLd + col];
+        float acc = bs[i] * X[i * LD + col];
 #pragma unroll
         for (int j = 0; j < i; ++j) acc = fmaf(-Am[i * kPd + j], x[j], acc);
         x[i] = acc;
     }
 #pragma unroll
-    for (int i = 0; i < kT; ++i) X[i * kLd + col] = x[i];
+    for (int i = 0; i < kT; ++i) X[i * LD + col] = x[i];
 }
 
 // Back substitution y = (I + A)^{-T} x on one column, from src into dst.
+template <int LD = kLd>
 __device__ __forceinline__ void back_subst(const float *src, float *dst, int col, const float *Am) {
     float y[kT];
 #pragma unroll
     for (int i = kT - 1; i >= 0; --i) {
-        float acc = src[i * kLd + col];
+        float acc = src[i * LD + col];
 #pragma unroll
         for (int j = i + 1; j < kT; ++j) acc = fmaf(-Am[j * kPd + i], y[j], acc);
         y[i] = acc;
     }
 #pragma unroll
-    for (int i = 0; i < kT; ++i) dst[i * kLd + col] = y[i];
+    for (int i = 0; i < kT; ++i) dst[i * LD + col] = y[i];
 }
 
 // A = beta (.) strict_lower(Kt Kh^T) into Am (warps 0-1 call this)
+template <int LD = kLd>
 __device__ __forceinline__ void build_A(const float *Kt, const float *Kh, const float *bs, float *Am,
                                         float *KK, int half, int g, int t) {
     float acc[4];
     const int j0 = 8 * half;
-    gram_half(acc, Kt, Kh, j0, g, t);
+    gram_half<LD>(acc, Kt, Kh, j0, g, t);
     const int i0 = g, i1 = g + 8, ja = j0 + 2 * t, jb = ja + 1;
     Am[i0 * kPd + ja] = ja < i0 ? bs[i0] * acc[0] : 0.f;
     Am[i0 * kPd + jb] = jb < i0 ? bs[i0] * acc[1] : 0.f;
@@ -279,11 +293,12 @@ __device__ __forceinline__ void build_A(const float *Kt, const float *Kh, const 
 }
 
 // lower (j <= i) part of X Y^T into M
+template <int LD = kLd>
 __device__ __forceinline__ void build_lower(const float *X, const float *Y, float *M, int half, int g,
                                             int t) {
     float acc[4];
     const int j0 = 8 * half;
-    gram_half(acc, X, Y, j0, g, t);
+    gram_half<LD>(acc, X, Y, j0, g, t);
     const int i0 = g, i1 = g + 8, ja = j0 + 2 * t, jb = ja + 1;
     M[i0 * kPd + ja] = ja <= i0 ? acc[0] : 0.f;
     M[i0 * kPd + jb] = jb <= i0 ? acc[1] : 0.f;
@@ -707,9 +722,9 @@ bwd_adj_chain_kernel(const BcArgs A) {
 //   Ub: V, then U          Wb: W                        Sh: dH1, then H0 (bf16)
 // ---------------------------------------------------------------------------
 template <bool VEC> struct TileLayout {
-    static constexpr int kt = 0, kh = kt + kTile2, qt = kh + kTile2, ob = qt + kTile2,
-                         db = ob + kTile2, ub = db + kTile2, wb = ub + kTile2, eb = wb + kTile2,
-                         am = eb + kTile2, kk = am + kT * kPd,
+    static constexpr int kt = 0, kh = kt + kTileT, qt = kh + kTileT, ob = qt + kTileT,
+                         db = ob + kTileT, ub = db + kTileT, wb = ub + kTileT, eb = wb + kTileT,
+                         am = eb + kTileT, kk = am + kT * kPd,
                          ds = kk + kT * kPd, da = ds + kT * kPd, bda = da + kT * kPd,
                          eg = bda + kT * kPd, rg = eg + kD, bs = rg + kD, rs = bs + kT,
                          gb = rs + 4 * kT + kT, egt = gb + 2 * kT, dgp = egt + 2 * kT,
@@ -754,8 +769,8 @@ bwd_tile_kernel(const BcArgs A) {
 #pragma unroll
         for (int e = tid * 4; e < kT * kD; e += kThreads * 4) {
             const int i = e >> 7, col = e & (kD - 1);
-            cp_async16(&Db[i * kLd + col], &Dg[e]);
-            cp_async16(&Eb[i * kLd + col], &dDg[e]);
+            cp_async16(&Db[i * kLt + col], &Dg[e]);
+            cp_async16(&Eb[i * kLt + col], &dDg[e]);
         }
     }
     cp_async_commit();
@@ -784,7 +799,7 @@ bwd_tile_kernel(const BcArgs A) {
             const int i = (tid >> 7) + 2 * m, col = tid & (kD - 1);
             rv[m] = i < len ? A.v[((t0 + i) * A.H + h) * kD + col] : __float2bfloat16_rn(0.f);
         }
-        stage_compute(A, len, R, Kt, Kh, Qt, nullptr, eg, A.dout != nullptr, Ob, bs);
+        stage_compute<kLt>(A, len, R, Kt, Kh, Qt, nullptr, eg, A.dout != nullptr, Ob, bs);
 #pragma unroll
         for (int m = 0; m < kT / 4; ++m)
             ra_keep[m] = (uint32_t)__bfloat16_as_ushort(R.ra[2 * m]) |
@@ -792,7 +807,7 @@ bwd_tile_kernel(const BcArgs A) {
 #pragma unroll
         for (int m = 0; m < kT / 2; ++m) {
             const int i = (tid >> 7) + 2 * m, col = tid & (kD - 1);
-            Ub[i * kLd + col] = __bfloat162float(rv[m]);
+            Ub[i * kLt + col] = __bfloat162float(rv[m]);
         }
     } else {
         // thread (token si, channels 8 sch .. 8 sch + 7): one 16-byte load per tensor; the
@@ -835,7 +850,7 @@ bwd_tile_kernel(const BcArgs A) {
             ob[u] = bf_half(wo[u >> 1], u & 1);
             ub[u] = bf_half(wv[u >> 1], u & 1);
         }
-        const int so = si * kLd + 8 * sch;
+        const int so = si * kLt + 8 * sch;
         *(float4 *)&Kt[so] = make_float4(kt[0], kt[1], kt[2], kt[3]);
         *(float4 *)&Kt[so + 4] = make_float4(kt[4], kt[5], kt[6], kt[7]);
         *(float4 *)&Kh[so] = make_float4(kh[0], kh[1], kh[2], kh[3]);
@@ -882,11 +897,11 @@ bwd_tile_kernel(const BcArgs A) {
 #pragma unroll 2
     for (int k0 = 0; k0 < kD; k0 += 8) {
         uint32_t ad[4];
-        load_a(ad, Db, kLd, 0, k0, g, t);
+        load_a_kp(ad, Db, kLt, 0, k0, g, t);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             uint32_t b0, b1;
-            load_bt_h(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);   // X^T[k][d] = X[d][k]
+            load_bt_h_kp(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);   // X^T[k][d] = X[d][k]
             mma8(dke[nt], ad, b0, b1);
         }
     }
@@ -908,8 +923,8 @@ bwd_tile_kernel(const BcArgs A) {
         fold16<false>(pr, lane);
         if ((lane & 1) == 0) rG[warp + 8 * (lane >> 1)] = pr[0];
     }
-    if (warp < 2) build_A(Kt, Kh, bs, Am, KK, warp, g, t);
-    else if (warp < 4) build_lower(Ob, Db, dS, warp - 2, g, t);   // dS = lower(dO D^T)
+    if (warp < 2) build_A<kLt>(Kt, Kh, bs, Am, KK, warp, g, t);
+    else if (warp < 4) build_lower<kLt>(Ob, Db, dS, warp - 2, g, t);   // dS = lower(dO D^T)
     else if (!VEC && warp == 7) {
         // in-tile inclusive cumsum of g (lanes 0..15), in place
         float x = lane < kT ? Gb[lane] : 0.f;
@@ -925,13 +940,13 @@ bwd_tile_kernel(const BcArgs A) {
         }
     }
     if (tid < kD)
-        for (int i = 0; i < kT; ++i) Wb[i * kLd + tid] = Kt[i * kLd + tid];
+        for (int i = 0; i < kT; ++i) Wb[i * kLt + tid] = Kt[i * kLt + tid];
     __syncthreads();
     // ---- H0 into the state buffer (asynchronous: dH1 is no longer needed)
     stage_state(A.Hst + st);
     cp_async_commit();
     // ---- W and U
-    fwd_subst(tid < kD ? Wb : Ub, tid & (kD - 1), Am, bs);
+    fwd_subst<kLt>(tid < kD ? Wb : Ub, tid & (kD - 1), Am, bs);
     cp_async_wait_all();   // H0 landed (own copies); the barrier publishes them
     __syncthreads();
     // ---- dQt_a = dO H0^T and dW = -dD H0^T (this warp's dk columns); dW into Db
@@ -945,14 +960,14 @@ bwd_tile_kernel(const BcArgs A) {
 #pragma unroll 2
         for (int k0 = 0; k0 < kD; k0 += 8) {
             uint32_t ao[4], ae[4];
-            load_a(ao, Ob, kLd, 0, k0, g, t);
-            load_a(ae, Eb, kLd, 0, k0, g, t);
+            load_a_kp(ao, Ob, kLt, 0, k0, g, t);
+            load_a_kp(ae, Eb, kLt, 0, k0, g, t);
 #pragma unroll
             for (int u = 0; u < 4; ++u) ae[u] ^= 0x80000000u;
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 uint32_t b0, b1;
-                load_bt_h(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);   // H0^T[k][d] = H0[d][k]
+                load_bt_h_kp(b0, b1, Sh, kLdh, k0, c0 + 8 * nt, g, t);   // H0^T[k][d] = H0[d][k]
                 mma8(dq[nt], ao, b0, b1);
                 mma8(dw[nt], ae, b0, b1);
             }
@@ -961,15 +976,13 @@ bwd_tile_kernel(const BcArgs A) {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             const int col = c0 + 8 * nt + 2 * t;
-            Db[g * kLd + col] = dw[nt][0];
-            Db[g * kLd + col + 1] = dw[nt][1];
-            Db[(g + 8) * kLd + col] = dw[nt][2];
-            Db[(g + 8) * kLd + col + 1] = dw[nt][3];
+            *(float2 *)&Db[g * kLt + col] = make_float2(dw[nt][0], dw[nt][1]);
+            *(float2 *)&Db[(g + 8) * kLt + col] = make_float2(dw[nt][2], dw[nt][3]);
         }
     }
     __syncthreads();
     // ---- dYw = T^T dW in place (dk columns, threads 0..127); dYu = T^T dD in place
-    back_subst(tid < kD ? Db : Eb, tid < kD ? Db : Eb, tid & (kD - 1), Am);
+    back_subst<kLt>(tid < kD ? Db : Eb, tid < kD ? Db : Eb, tid & (kD - 1), Am);
     __syncthreads();
     // ---- dA = -strict_lower(dYu U^T + dYw W^T) (warps 0-1); dV = diag(beta) dYu
     if (warp < 2) {
@@ -978,11 +991,11 @@ bwd_tile_kernel(const BcArgs A) {
 #pragma unroll 4
         for (int k0 = 0; k0 < kD; k0 += 8) {
             uint32_t af[4], b0, b1;
-            load_a(af, Eb, kLd, 0, k0, g, t);
-            load_bt(b0, b1, Ub, kLd, k0, j0, g, t);
+            load_a_kp(af, Eb, kLt, 0, k0, g, t);
+            load_bt_kp(b0, b1, Ub, kLt, k0, j0, g, t);
             mma8(acc, af, b0, b1);
-            load_a(af, Db, kLd, 0, k0, g, t);
-            load_bt(b0, b1, Wb, kLd, k0, j0, g, t);
+            load_a_kp(af, Db, kLt, 0, k0, g, t);
+            load_bt_kp(b0, b1, Wb, kLt, k0, j0, g, t);
             mma8(acc2, af, b0, b1);
         }
 #pragma unroll
@@ -1005,7 +1018,7 @@ bwd_tile_kernel(const BcArgs A) {
         const int i = tid >> 4, ch = tid & 15;
         float x = 0.f;
         if (i < len) {
-            const int so = i * kLd + 8 * ch;
+            const int so = i * kLt + 8 * ch;
             const float4 y0 = *(const float4 *)&Eb[so], y1 = *(const float4 *)&Eb[so + 4];
             const float4 d0 = *(const float4 *)&Db[so], d1 = *(const float4 *)&Db[so + 4];
             const float4 k0 = *(const float4 *)&Kt[so], k1 = *(const float4 *)&Kt[so + 4];
@@ -1039,9 +1052,9 @@ bwd_tile_kernel(const BcArgs A) {
             x[m] = 0.f;
             if (i < len) {
                 const int64_t r = ((t0 + i) * A.H + h) * kD + col;
-                const float yu = Eb[i * kLd + col];
+                const float yu = Eb[i * kLt + col];
                 A.dv[r] = __float2bfloat16_rn(bs[i] * yu);
-                x[m] = fmaf(yu, __bfloat162float(rv[m]), Db[i * kLd + col] * Kt[i * kLd + col]);
+                x[m] = fmaf(yu, __bfloat162float(rv[m]), Db[i * kLt + col] * Kt[i * kLt + col]);
             }
         }
         // the 8 row sums by one halving exchange: row half + 2 ((lane >> 1) & 7) in x[0]
@@ -1081,7 +1094,7 @@ bwd_tile_kernel(const BcArgs A) {
                 G += gl[u];
                 gg = G;
             }
-            Ub[i * kLd + d] = gg;
+            Ub[i * kLt + d] = gg;
         }
     }
     // ---- dKt, dKh, dQt on this warp's dk columns; dG into Ob
@@ -1101,9 +1114,9 @@ bwd_tile_kernel(const BcArgs A) {
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 uint32_t bh0, bh1, bt0, bt1, bq0, bq1;
-                load_b(bh0, bh1, Kh, kLd, 8 * ks, c0 + 8 * nt, g, t);
-                load_b(bt0, bt1, Kt, kLd, 8 * ks, c0 + 8 * nt, g, t);
-                load_b(bq0, bq1, Qt, kLd, 8 * ks, c0 + 8 * nt, g, t);
+                load_b(bh0, bh1, Kh, kLt, 8 * ks, c0 + 8 * nt, g, t);
+                load_b(bt0, bt1, Kt, kLt, 8 * ks, c0 + 8 * nt, g, t);
+                load_b(bq0, bq1, Qt, kLt, 8 * ks, c0 + 8 * nt, g, t);
                 mma8(dkt[nt], a_bdA, bh0, bh1);    // (beta dA) Kh
                 mma8(dkh[nt], a_bdAt, bt0, bt1);   // (beta dA)^T Kt
                 mma8(dkh[nt], a_dSt, bq0, bq1);    // dS^T Qt
@@ -1117,19 +1130,21 @@ bwd_tile_kernel(const BcArgs A) {
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {   // the pair (u, u + 1) = columns (d, d + 1) of row i
                 const int i = g + 8 * hr, d = c0 + 8 * nt + 2 * t;
+                const float2 kt2 = *(const float2 *)&Kt[i * kLt + d], kh2 = *(const float2 *)&Kh[i * kLt + d];
+                const float2 qt2 = *(const float2 *)&Qt[i * kLt + d], dw2 = *(const float2 *)&Db[i * kLt + d];
                 float oq[2], ok[2];
 #pragma unroll
                 for (int w = 0; w < 2; ++w) {
                     const int u = 2 * hr + w, dd = d + w;
-                    const float kt = Kt[i * kLd + dd], kh = Kh[i * kLd + dd], qt = Qt[i * kLd + dd];
-                    const float dKt = dkt[nt][u] + bs[i] * Db[i * kLd + dd];
+                    const float kt = w ? kt2.y : kt2.x, kh = w ? kh2.y : kh2.x, qt = w ? qt2.y : qt2.x;
+                    const float dKt = dkt[nt][u] + bs[i] * (w ? dw2.y : dw2.x);
                     const float dKh = dkh[nt][u] + dke[nt][u];   // dke = D X^T = dKe (.) e^{G_C}
                     const float dG = dq[nt][u] * qt + dKt * kt - dKh * kh;
-                    if constexpr (VEC) Ob[i * kLd + dd] = dG;
+                    if constexpr (VEC) Ob[i * kLt + dd] = dG;
                     else pg[hr] += dG;
                     // e^G and e^-G: per (token, channel), or per token from the table (scalar gate)
-                    const float ep = VEC ? expf(Gv[i * kLd + dd]) : eGt[i];
-                    const float em = VEC ? expf(-Gv[i * kLd + dd]) : eGt[kT + i];
+                    const float ep = VEC ? expf(Gv[i * kLt + dd]) : eGt[i];
+                    const float em = VEC ? expf(-Gv[i * kLt + dd]) : eGt[kT + i];
                     oq[w] = dq[nt][u] * ep;
                     ok[w] = dKt * ep + dKh * em;
                     dke[nt][u] *= kh;   // dKe (.) Ke, summed over the tile below
@@ -1185,9 +1200,9 @@ bwd_tile_kernel(const BcArgs A) {
             const int d = tid;
             float acc = 0.f;
             for (int i = len - 1; i >= 0; --i) {
-                acc += Ob[i * kLd + d] + (i == len - 1 ? rG[d] : 0.f);
+                acc += Ob[i * kLt + d] + (i == len - 1 ? rG[d] : 0.f);
                 // g'(a) = -b s (1 - s) with s = -g / b, i.e. g (1 + g / b); g from the cumsum
-                const float gi = Gv[i * kLd + d] - (i > 0 ? Gv[(i - 1) * kLd + d] : 0.f);
+                const float gi = Gv[i * kLt + d] - (i > 0 ? Gv[(i - 1) * kLt + d] : 0.f);
                 const int64_t r = ((t0 + i) * A.H + h) * kD + d;
                 A.da[r] = __float2bfloat16_rn(acc * gi * (1.f + gi / A.b));
             }

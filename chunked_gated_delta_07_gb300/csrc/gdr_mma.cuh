@@ -75,6 +75,38 @@ __device__ __forceinline__ void load_bt_h(uint32_t &b0, uint32_t &b1, const __nv
     b1 = tf32(__bfloat162float(M[(n0 + g) * ld + k0 + t + 4]));
 }
 
+// Fragments of a product whose k index runs along the rows of both operands, with k
+// permuted the same way on both sides (slot t <-> column k0 + 2t, slot t + 4 <-> column
+// k0 + 2t + 1), which leaves the product unchanged: each pair of slots is one 8-byte
+// (fp32) or 4-byte (bf16) load.  A row stride of 8 mod 32 words keeps the fp32 loads
+// free of bank conflicts (a half warp reads 4 rows x 8 words).
+__device__ __forceinline__ void load_a_kp(uint32_t (&a)[4], const float *M, int ld, int r0, int k0,
+                                          int g, int t) {
+    const float2 x = *(const float2 *)&M[(r0 + g) * ld + k0 + 2 * t];
+    const float2 y = *(const float2 *)&M[(r0 + g + 8) * ld + k0 + 2 * t];
+    a[0] = tf32(x.x);
+    a[2] = tf32(x.y);
+    a[1] = tf32(y.x);
+    a[3] = tf32(y.y);
+}
+
+// B[k][n] = M[n][k], k permuted as in load_a_kp
+__device__ __forceinline__ void load_bt_kp(uint32_t &b0, uint32_t &b1, const float *M, int ld, int k0,
+                                           int n0, int g, int t) {
+    const float2 x = *(const float2 *)&M[(n0 + g) * ld + k0 + 2 * t];
+    b0 = tf32(x.x);
+    b1 = tf32(x.y);
+}
+
+// B[k][n] = M[n][k] from a bf16 row-major matrix, k permuted as in load_a_kp (the two
+// values widened exactly: a bf16 is the top half of its fp32)
+__device__ __forceinline__ void load_bt_h_kp(uint32_t &b0, uint32_t &b1, const __nv_bfloat16 *M, int ld,
+                                             int k0, int n0, int g, int t) {
+    const uint32_t x = *(const uint32_t *)&M[(n0 + g) * ld + k0 + 2 * t];
+    b0 = x << 16;
+    b1 = x & 0xffff0000u;
+}
+
 }  // namespace gdr
 
 namespace gdr {
