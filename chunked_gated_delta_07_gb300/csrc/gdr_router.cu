@@ -8,16 +8,18 @@
 //      proportional step (bias += eta (Q - load) / Q), binary64 then rounded.
 //
 // router_topk_kernel is the hot part: it reads the [T, E] logits once.  One
-// warp per token; lane l owns experts 4c..4c+3 for c = l, l + 32, ..., so its
-// slice of the bias stays in registers for every token.  Each score becomes an
-// order-preserving 32-bit key.  The k-th largest of the 32 lane maxima, found
-// with k warp-wide max reductions, is a lower bound tau for the k-th largest
-// score: the k lanes it came from hold k scores >= tau.  Only scores >= tau
-// can be selected; they are gathered (usually a dozen) and ranked exactly by
-// (score, -index).  When more than kCap scores tie at or above tau, the warp
-// falls back to k rounds of a warp-wide arg-max over (score, -index).
-// Loads are counted in a shared-memory histogram per block and added to the
-// int64 counts once per block.
+// warp per token; lane l owns experts 4c..4c+3 for c = l, l + 32, ...  The scores
+// stay in registers as floats and each lane keeps their maximum.  The k-th largest
+// of the 32 lane maxima, found with k warp-wide max reductions, bounds the k-th
+// largest score from below; the reductions run on order-preserving 32-bit keys whose
+// low 5 bits are replaced by the lane index (which makes them distinct, and only
+// lowers the bound).  Only scores >= that bound can be selected: each lane marks
+// them in a bit mask, the warp gathers them (usually a dozen; the logit is read back
+// from a per-warp copy of the row in shared memory) and ranks them exactly by
+// (score, -index).  When more than kCap scores pass, or fewer than k (NaN scores
+// never pass), the warp falls back to k rounds of a warp-wide arg-max over (score,
+// -index).  Loads are counted in a shared-memory histogram per block and added to
+// the int64 counts once per block.
 #include <algorithm>
 
 #include "gdr_internal.cuh"
@@ -36,6 +38,11 @@ __device__ __forceinline__ uint32_t score_key(float s) {
     return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);   // negative: ~u, else u | sign
 }
 
+// The score of a key (the inverse of score_key).
+__device__ __forceinline__ float key_score(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
+}
+
 // (key, -index) packed so that a larger value is the better expert.
 __device__ __forceinline__ uint64_t pack(uint32_t key, int e) {
     return ((uint64_t)key << 32) | (uint64_t)(0xffffffffu - (uint32_t)e);
@@ -50,6 +57,7 @@ template <> struct Vec4<__nv_bfloat16> {
         f[2] = __uint_as_float(x.y << 16);
         f[3] = __uint_as_float(x.y & 0xffff0000u);
     }
+    __device__ static float at(const __nv_bfloat16 *row, int e) { return __bfloat162float(row[e]); }
 };
 template <> struct Vec4<float> {
     using type = float4;
@@ -59,7 +67,16 @@ template <> struct Vec4<float> {
         f[2] = x.z;
         f[3] = x.w;
     }
+    __device__ static float at(const float *row, int e) { return row[e]; }
 };
+
+// Bit mask of a lane's NCH * 4 scores.
+template <int NCH> struct LaneMask { using type = uint32_t; };
+template <> struct LaneMask<16> { using type = uint64_t; };
+__device__ __forceinline__ int lowest_bit(uint32_t m) { return __ffs(m) - 1; }
+__device__ __forceinline__ int lowest_bit(uint64_t m) { return __ffsll((long long)m) - 1; }
+__device__ __forceinline__ int bit_count(uint32_t m) { return __popc(m); }
+__device__ __forceinline__ int bit_count(uint64_t m) { return __popcll(m); }
 
 // ECT > 0 fixes the expert count at compile time (the bounds checks fold away).
 template <typename T, int NCH, int ECT>
@@ -67,12 +84,16 @@ __global__ void __launch_bounds__(kRtThreads, NCH > 8 ? 1 : 2)
 router_topk_kernel(const T *__restrict__ logits, const float *__restrict__ bias,
                    int32_t *__restrict__ idx, float *__restrict__ sel,
                    unsigned long long *__restrict__ load, int64_t Tn, int E_arg, int k) {
+    static_assert(NCH * 4 <= 8 * (int)sizeof(typename LaneMask<NCH>::type), "mask too narrow");
+    using M = typename LaneMask<NCH>::type;
     const int E = ECT > 0 ? ECT : E_arg;
-    extern __shared__ unsigned int hist[];                // [E] counts, then [E] bias
+    // [E] counts, [E] bias, then each warp's current row of logits ([kRtWarps][E])
+    extern __shared__ unsigned int hist[];
     float *bsm = (float *)(hist + E);
     __shared__ uint64_t cand[kRtWarps][kCap];
     __shared__ float cand_x[kRtWarps][kCap];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    T *row = (T *)(bsm + E) + (size_t)warp * E;
     for (int e = threadIdx.x; e < E; e += kRtThreads) {
         hist[e] = 0;
         bsm[e] = bias[e];
@@ -96,8 +117,10 @@ router_topk_kernel(const T *__restrict__ logits, const float *__restrict__ bias,
 #pragma unroll
         for (int j = 0; j < NCH; ++j) cur[j] = nxt[j];
         fetch(t + nwarps);
-        uint32_t key[NCH][4];
-        uint32_t lmax = 0;
+        // the scores and the lane maximum; the row also goes to shared memory, where
+        // the gather below reads its few candidates back
+        float sc[NCH][4];
+        float lmax = -INFINITY;
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
             const int c = lane + 32 * j;
@@ -105,34 +128,41 @@ router_topk_kernel(const T *__restrict__ logits, const float *__restrict__ bias,
                 float x[4];
                 Vec4<T>::unpack(cur[j], x);
                 const float4 bz = *(const float4 *)&bsm[4 * c];
-                key[j][0] = score_key(x[0] + bz.x);
-                key[j][1] = score_key(x[1] + bz.y);
-                key[j][2] = score_key(x[2] + bz.z);
-                key[j][3] = score_key(x[3] + bz.w);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) lmax = max(lmax, key[j][u]);
+                sc[j][0] = x[0] + bz.x;
+                sc[j][1] = x[1] + bz.y;
+                sc[j][2] = x[2] + bz.z;
+                sc[j][3] = x[3] + bz.w;
+                lmax = fmaxf(lmax, fmaxf(fmaxf(sc[j][0], sc[j][1]), fmaxf(sc[j][2], sc[j][3])));
+                *(V *)&row[4 * c] = cur[j];
             } else {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) key[j][u] = 0;
+                for (int u = 0; u < 4; ++u) sc[j][u] = -INFINITY;
             }
         }
-        // tau: the k-th largest lane maximum (lanes without experts offer 0)
-        uint32_t tau = 0;
-        bool alive = true;
-        for (int r = 0; r < k; ++r) {
-            const uint32_t m = __reduce_max_sync(0xffffffffu, alive ? lmax : 0u);
-            const unsigned who = __ballot_sync(0xffffffffu, alive && lmax == m);
-            if (who == 0) break;           // fewer live lanes than k: tau stays 0
-            if (lane == __ffs(who) - 1) alive = false;
-            tau = m;
+        // tau: the k-th largest lane maximum, as a key with the lane index in its low 5
+        // bits (lanes without experts offer 0); fewer than k lanes: tau takes every score
+        uint32_t tau_key = 0;
+        {
+            const uint32_t lk = 4 * lane < E ? (score_key(lmax) & ~31u) | (uint32_t)lane : 0u;
+            bool alive = true;
+            uint32_t m = 0;
+            int r = 0;
+            for (; r < k; ++r) {
+                m = __reduce_max_sync(0xffffffffu, alive ? lk : 0u);
+                if (m == 0) break;
+                if ((int)(m & 31u) == lane) alive = false;
+            }
+            tau_key = r == k ? m & ~31u : 0u;
         }
-        // gather the scores >= tau
-        int cnt = 0;
+        const float tau = key_score(max(tau_key, 0x007fffffu));   // at least -inf
+        // the scores >= tau: a bit per score, then their positions in the warp's list
+        M mask = 0;
 #pragma unroll
         for (int j = 0; j < NCH; ++j)
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-                cnt += (4 * (lane + 32 * j) + u < E && key[j][u] >= tau) ? 1 : 0;
+                if (4 * (lane + 32 * j) + u < E && sc[j][u] >= tau) mask |= (M)1 << (4 * j + u);
+        const int cnt = bit_count(mask);
         int incl = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -140,21 +170,17 @@ router_topk_kernel(const T *__restrict__ logits, const float *__restrict__ bias,
             if (lane >= o) incl += y;
         }
         const int total = __shfl_sync(0xffffffffu, incl, 31);
-        if (total <= kCap) {
+        if (total >= k && total <= kCap) {
             int pos = incl - cnt;
-#pragma unroll
-            for (int j = 0; j < NCH; ++j)
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int e = 4 * (lane + 32 * j) + u;
-                    if (e < E && key[j][u] >= tau) {
-                        float x[4];
-                        Vec4<T>::unpack(cur[j], x);
-                        cand[warp][pos] = pack(key[j][u], e);
-                        cand_x[warp][pos] = x[u];
-                        ++pos;
-                    }
-                }
+            while (mask) {
+                const int b = lowest_bit(mask);
+                mask &= mask - 1;
+                const int e = 4 * (lane + 32 * (b >> 2)) + (b & 3);
+                const float x = Vec4<T>::at(row, e);
+                cand[warp][pos] = pack(score_key(x + bsm[e]), e);
+                cand_x[warp][pos] = x;
+                ++pos;
+            }
             __syncwarp();
             for (int ci = lane; ci < total; ci += 32) {
                 const uint64_t me = cand[warp][ci];
@@ -169,21 +195,22 @@ router_topk_kernel(const T *__restrict__ logits, const float *__restrict__ bias,
             }
             __syncwarp();
         } else {
-            // many ties at the threshold: k rounds of a warp-wide arg-max
+            // many ties at the threshold (or NaN scores): k rounds of a warp-wide arg-max;
+            // a NaN score ranks as -inf, and every pick is a valid expert index
+            M taken = 0;
             for (int r = 0; r < k; ++r) {
                 uint64_t best = 0;
-                float bx = 0.f;
+                int bb = -1;
 #pragma unroll
                 for (int j = 0; j < NCH; ++j)
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const int e = 4 * (lane + 32 * j) + u;
-                        const uint64_t p = e < E ? pack(key[j][u], e) : 0ull;
+                        const int b = 4 * j + u, e = 4 * (lane + 32 * j) + u;
+                        const float s = sc[j][u] != sc[j][u] ? -INFINITY : sc[j][u];
+                        const uint64_t p = (e < E && !((taken >> b) & 1)) ? pack(score_key(s), e) : 0ull;
                         if (p > best) {
-                            float x[4];
-                            Vec4<T>::unpack(cur[j], x);
                             best = p;
-                            bx = x[u];
+                            bb = b;
                         }
                     }
                 uint64_t w = best;
@@ -192,19 +219,12 @@ router_topk_kernel(const T *__restrict__ logits, const float *__restrict__ bias,
                     const uint64_t y = __shfl_xor_sync(0xffffffffu, w, o);
                     w = y > w ? y : w;
                 }
-                const int e = (int)(0xffffffffu - (uint32_t)w);
-                if (best == w) {   // the lane that owns the winner records and removes it
+                if (best == w && bb >= 0) {   // the lane that owns the winner records and removes it
+                    const int e = (int)(0xffffffffu - (uint32_t)w);
+                    taken |= (M)1 << bb;
                     idx[t * k + r] = e;
-                    if (sel) sel[t * k + r] = bx;
+                    if (sel) sel[t * k + r] = Vec4<T>::at(row, e);
                     atomicAdd(&hist[e], 1u);
-                }
-                const int cw = e >> 2, jw = cw >> 5, uw = e & 3;   // e = 4 (lane + 32 j) + u
-                if (lane == (cw & 31)) {
-#pragma unroll
-                    for (int j = 0; j < NCH; ++j)
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            if (j == jw && u == uw) key[j][u] = 0;
                 }
                 __syncwarp();
             }
@@ -267,9 +287,10 @@ template <typename T, int NCH, int ECT = 0>
 cudaError_t launch_topk_t(const void *logits, const float *bias, int32_t *idx, float *sel,
                           int64_t *load, int64_t Tn, int E, int k, cudaStream_t stream) {
     auto kern = router_topk_kernel<T, NCH, ECT>;
-    const size_t smem = (sizeof(unsigned int) + sizeof(float)) * (size_t)E;
+    const size_t smem = (sizeof(unsigned int) + sizeof(float) + sizeof(T) * kRtWarps) * (size_t)E;
     int dev = 0, sms = 0;
-    cudaError_t err = cudaGetDevice(&dev);
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err == cudaSuccess) err = cudaGetDevice(&dev);
     if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
     // a few blocks per SM: enough warps in flight to cover HBM latency, few

@@ -58,6 +58,47 @@ def test_topk_with_many_ties(E, k):
     _topk_case(400, E, k, "bf16", ties=True, seed=E + k)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_topk_signed_zero_ties(dtype):
+    """Scores of -0 and +0 are equal (binary32 comparison): the lower expert index
+    goes first, on both sides, whichever zero each score carries."""
+    T, E, k = 300, 128, 8
+    g = torch.Generator().manual_seed(11)
+    vals = torch.tensor([0.0, -0.0, 0.5, -0.5])
+    x = vals[torch.randint(0, 4, (T, E), generator=g)]
+    x = x.to(torch.bfloat16 if dtype == "bf16" else torch.float32).cuda()
+    bias = torch.zeros(E, dtype=torch.float32, device="cuda")
+    bias[::3] = -0.0
+    load = torch.zeros(E, dtype=torch.int64, device="cuda")
+    idx, sel = gdr.router_topk(x, bias, k, load=load)
+    torch.cuda.synchronize()
+    r_idx, r_sel, r_load = oracle.router_topk(x, bias, k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), r_idx)
+    np.testing.assert_array_equal(load.cpu().numpy(), r_load)
+
+
+def test_topk_nan_scores_stay_in_bounds():
+    """NaN logits give an unspecified selection, but every pick is a distinct valid
+    expert of its token and the counts add up to T k."""
+    T, E, k = 200, 896, 8
+    x, bias = make_router_logits(T, E, 5, "bf16", device="cuda")
+    x = x.clone()
+    x[::2, ::7] = float("nan")      # some NaN in every other token
+    x[1::10, :] = float("nan")      # tokens whose scores are all NaN
+    load = torch.zeros(E, dtype=torch.int64, device="cuda")
+    idx, _ = gdr.router_topk(x, bias, k, load=load)
+    torch.cuda.synchronize()
+    assert gdr.gdr_get_status() == gdr.GDR_OK
+    got = idx.cpu().numpy()
+    assert got.min() >= 0 and got.max() < E
+    assert all(len(set(r)) == k for r in got.tolist())
+    assert int(load.sum()) == T * k
+    # tokens without NaN are still exact
+    clean = np.arange(T)[(np.arange(T) % 2 == 1) & (np.arange(T) % 10 != 1)]
+    r_idx, _, _ = oracle.router_topk(x[torch.as_tensor(clean, device=x.device)], bias, k)
+    np.testing.assert_array_equal(got[clean], r_idx)
+
+
 def test_load_accumulates_and_zero_tokens():
     x, bias, load = _topk_case(500, 896, 8, seed=1)
     _topk_case(300, 896, 8, seed=2, load0=load)
