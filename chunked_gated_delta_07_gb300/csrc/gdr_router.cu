@@ -30,7 +30,6 @@ namespace {
 constexpr int kRtThreads = 256;
 constexpr int kRtWarps = kRtThreads / 32;
 constexpr int kCap = 64;     // gathered candidates per warp
-constexpr int kRtBlocksPerSm = 4;
 
 // Order-preserving map of a binary32 score onto uint32 (-0 taken as +0).
 __device__ __forceinline__ uint32_t score_key(float s) {
@@ -46,6 +45,16 @@ __device__ __forceinline__ float key_score(uint32_t key) {
 // (key, -index) packed so that a larger value is the better expert.
 __device__ __forceinline__ uint64_t pack(uint32_t key, int e) {
     return ((uint64_t)key << 32) | (uint64_t)(0xffffffffu - (uint32_t)e);
+}
+
+// Asynchronous copy of one lane's four logits (8 or 16 bytes) into shared memory;
+// complete for the issuing thread after cp.async.wait_group.
+__device__ __forceinline__ void copy_async(void *smem, const void *gmem, int bytes) {
+    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+    if (bytes == 16)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+    else
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(sa), "l"(gmem) : "memory");
 }
 
 template <typename T> struct Vec4;
@@ -78,47 +87,51 @@ __device__ __forceinline__ int lowest_bit(uint64_t m) { return __ffsll((long lon
 __device__ __forceinline__ int bit_count(uint32_t m) { return __popc(m); }
 __device__ __forceinline__ int bit_count(uint64_t m) { return __popcll(m); }
 
-// ECT > 0 fixes the expert count at compile time (the bounds checks fold away).
-template <typename T, int NCH, int ECT>
-__global__ void __launch_bounds__(kRtThreads, NCH > 8 ? 1 : 2)
+// ECT > 0 fixes the expert count and KCT > 0 the pick count at compile time (the
+// bounds checks fold away, the threshold rounds unroll).
+template <typename T, int NCH, int ECT, int KCT>
+__global__ void __launch_bounds__(kRtThreads, NCH > 8 ? 1 : (NCH > 7 ? 2 : 3))
 router_topk_kernel(const T *__restrict__ logits, const float *__restrict__ bias,
                    int32_t *__restrict__ idx, float *__restrict__ sel,
-                   unsigned long long *__restrict__ load, int64_t Tn, int E_arg, int k) {
+                   unsigned long long *__restrict__ load, int64_t Tn, int E_arg, int k_arg) {
     static_assert(NCH * 4 <= 8 * (int)sizeof(typename LaneMask<NCH>::type), "mask too narrow");
     using M = typename LaneMask<NCH>::type;
+    using V = typename Vec4<T>::type;
     const int E = ECT > 0 ? ECT : E_arg;
-    // [E] counts, [E] bias, then each warp's current row of logits ([kRtWarps][E])
+    const int k = KCT > 0 ? KCT : k_arg;
+    // [E] counts, [E] bias, then two rows of logits per warp ([kRtWarps][2][E]): the
+    // current token's, and the next one's, in flight
     extern __shared__ unsigned int hist[];
     float *bsm = (float *)(hist + E);
-    __shared__ uint64_t cand[kRtWarps][kCap];
+    __shared__ __align__(16) uint64_t cand[kRtWarps][kCap];
     __shared__ float cand_x[kRtWarps][kCap];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    T *row = (T *)(bsm + E) + (size_t)warp * E;
+    T *rows = (T *)(bsm + E) + (size_t)warp * 2 * E;
     for (int e = threadIdx.x; e < E; e += kRtThreads) {
         hist[e] = 0;
         bsm[e] = bias[e];
     }
     __syncthreads();
-    using V = typename Vec4<T>::type;
     const int64_t nwarps = (int64_t)gridDim.x * kRtWarps;
-    // the next token's row is loaded while the current one is ranked
-    V nxt[NCH];
+    // each lane copies its own chunks of a row (and reads only those), so the row
+    // buffers need no barrier between the lanes
     int64_t t = (int64_t)blockIdx.x * kRtWarps + warp;
-    auto fetch = [&](int64_t tt) {
+    auto fetch = [&](int64_t tt, T *dst) {
+        if (tt < Tn) {
 #pragma unroll
-        for (int j = 0; j < NCH; ++j) {
-            const int c = lane + 32 * j;
-            if (tt < Tn && 4 * c < E) nxt[j] = __ldcs((const V *)(logits + tt * E + 4 * c));
+            for (int j = 0; j < NCH; ++j) {
+                const int c = lane + 32 * j;
+                if (4 * c < E) copy_async(dst + 4 * c, logits + tt * E + 4 * c, (int)sizeof(V));
+            }
         }
+        asm volatile("cp.async.commit_group;" ::: "memory");
     };
-    fetch(t);
-    for (; t < Tn; t += nwarps) {
-        V cur[NCH];
-#pragma unroll
-        for (int j = 0; j < NCH; ++j) cur[j] = nxt[j];
-        fetch(t + nwarps);
-        // the scores and the lane maximum; the row also goes to shared memory, where
-        // the gather below reads its few candidates back
+    fetch(t, rows);
+    for (int buf = 0; t < Tn; t += nwarps, buf ^= 1) {
+        const T *row = rows + buf * E;
+        fetch(t + nwarps, rows + (buf ^ 1) * E);
+        asm volatile("cp.async.wait_group 1;" ::: "memory");   // this row's copies landed
+        // the scores and the lane maximum
         float sc[NCH][4];
         float lmax = -INFINITY;
 #pragma unroll
@@ -126,33 +139,32 @@ router_topk_kernel(const T *__restrict__ logits, const float *__restrict__ bias,
             const int c = lane + 32 * j;
             if (4 * c < E) {
                 float x[4];
-                Vec4<T>::unpack(cur[j], x);
+                Vec4<T>::unpack(*(const V *)&row[4 * c], x);
                 const float4 bz = *(const float4 *)&bsm[4 * c];
                 sc[j][0] = x[0] + bz.x;
                 sc[j][1] = x[1] + bz.y;
                 sc[j][2] = x[2] + bz.z;
                 sc[j][3] = x[3] + bz.w;
                 lmax = fmaxf(lmax, fmaxf(fmaxf(sc[j][0], sc[j][1]), fmaxf(sc[j][2], sc[j][3])));
-                *(V *)&row[4 * c] = cur[j];
             } else {
 #pragma unroll
                 for (int u = 0; u < 4; ++u) sc[j][u] = -INFINITY;
             }
         }
         // tau: the k-th largest lane maximum, as a key with the lane index in its low 5
-        // bits (lanes without experts offer 0); fewer than k lanes: tau takes every score
-        uint32_t tau_key = 0;
+        // bits (lanes without experts offer 0); with fewer than k lanes the last rounds
+        // find 0, and tau takes every score
+        uint32_t tau_key;
         {
             const uint32_t lk = 4 * lane < E ? (score_key(lmax) & ~31u) | (uint32_t)lane : 0u;
             bool alive = true;
             uint32_t m = 0;
-            int r = 0;
-            for (; r < k; ++r) {
+#pragma unroll
+            for (int r = 0; r < k; ++r) {
                 m = __reduce_max_sync(0xffffffffu, alive ? lk : 0u);
-                if (m == 0) break;
-                if ((int)(m & 31u) == lane) alive = false;
+                alive = alive && (int)(m & 31u) != lane;
             }
-            tau_key = r == k ? m & ~31u : 0u;
+            tau_key = m & ~31u;
         }
         const float tau = key_score(max(tau_key, 0x007fffffu));   // at least -inf
         // the scores >= tau: a bit per score, then their positions in the warp's list
@@ -181,11 +193,15 @@ router_topk_kernel(const T *__restrict__ logits, const float *__restrict__ bias,
                 cand_x[warp][pos] = x;
                 ++pos;
             }
+            if (lane == 0 && (total & 1)) cand[warp][total] = 0;   // pads the list to pairs
             __syncwarp();
             for (int ci = lane; ci < total; ci += 32) {
                 const uint64_t me = cand[warp][ci];
                 int rank = 0;
-                for (int cj = 0; cj < total; ++cj) rank += cand[warp][cj] > me ? 1 : 0;
+                for (int cj = 0; cj < total; cj += 2) {   // two candidates per load
+                    const ulonglong2 q = *(const ulonglong2 *)&cand[warp][cj];
+                    rank += (q.x > me ? 1 : 0) + (q.y > me ? 1 : 0);
+                }
                 if (rank < k) {
                     const int e = (int)(0xffffffffu - (uint32_t)me);
                     idx[t * k + rank] = e;
@@ -230,6 +246,7 @@ router_topk_kernel(const T *__restrict__ logits, const float *__restrict__ bias,
             }
         }
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");   // (the last, empty group)
     __syncthreads();
     if (load)
         for (int e = threadIdx.x; e < E; e += kRtThreads)
@@ -283,20 +300,23 @@ router_update_kernel(const long long *__restrict__ load, float *__restrict__ bia
     }
 }
 
-template <typename T, int NCH, int ECT = 0>
+template <typename T, int NCH, int ECT = 0, int KCT = 0>
 cudaError_t launch_topk_t(const void *logits, const float *bias, int32_t *idx, float *sel,
                           int64_t *load, int64_t Tn, int E, int k, cudaStream_t stream) {
-    auto kern = router_topk_kernel<T, NCH, ECT>;
-    const size_t smem = (sizeof(unsigned int) + sizeof(float) + sizeof(T) * kRtWarps) * (size_t)E;
+    auto kern = router_topk_kernel<T, NCH, ECT, KCT>;
+    const size_t smem = (sizeof(unsigned int) + sizeof(float) + sizeof(T) * 2 * kRtWarps) * (size_t)E;
     int dev = 0, sms = 0;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err == cudaSuccess) err = cudaGetDevice(&dev);
     if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
-    // a few blocks per SM: enough warps in flight to cover HBM latency, few
-    // enough that the per-block count flush stays small
+    // one wave of resident blocks (each warp then walks its tokens with the next row
+    // in flight), so that every SM holds as many warps as registers allow
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRtThreads, smem);
+    if (err != cudaSuccess) return err;
     const int64_t want = (Tn + kRtWarps - 1) / kRtWarps;
-    const int64_t grid = std::min<int64_t>(want, (int64_t)sms * kRtBlocksPerSm);
+    const int64_t grid = std::min<int64_t>(want, (int64_t)sms * std::max(per_sm, 1));
     ProfScope prof(stream, "router_topk_kernel");
     kern<<<(unsigned)grid, kRtThreads, smem, stream>>>((const T *)logits, bias, idx, sel,
                                                        (unsigned long long *)load, Tn, E, k);
@@ -310,6 +330,7 @@ cudaError_t launch_topk_dt(const void *logits, const float *bias, int32_t *idx, 
     if (E <= 128) return launch_topk_t<T, 1>(logits, bias, idx, sel, load, Tn, E, k, stream);
     if (E <= 256) return launch_topk_t<T, 2>(logits, bias, idx, sel, load, Tn, E, k, stream);
     if (E <= 512) return launch_topk_t<T, 4>(logits, bias, idx, sel, load, Tn, E, k, stream);
+    if (E == 896 && k == 8) return launch_topk_t<T, 7, 896, 8>(logits, bias, idx, sel, load, Tn, E, k, stream);
     if (E == 896) return launch_topk_t<T, 7, 896>(logits, bias, idx, sel, load, Tn, E, k, stream);
     if (E <= 896) return launch_topk_t<T, 7>(logits, bias, idx, sel, load, Tn, E, k, stream);
     if (E <= 1024) return launch_topk_t<T, 8>(logits, bias, idx, sel, load, Tn, E, k, stream);
