@@ -42,6 +42,16 @@ __device__ __forceinline__ float key_score(uint32_t key) {
     return __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
 }
 
+// max(a, b, c) in one instruction (the three-input form of max.f32).  Only the lane
+// maxima use it; they feed a lower bound, so its choice between -0 and +0, or its
+// handling of NaN, cannot change a selection (a NaN bound sends the token to the
+// arg-max rounds).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // (key, -index) packed so that a larger value is the better expert.
 __device__ __forceinline__ uint64_t pack(uint32_t key, int e) {
     return ((uint64_t)key << 32) | (uint64_t)(0xffffffffu - (uint32_t)e);
@@ -145,7 +155,7 @@ router_topk_kernel(const T *__restrict__ logits, const float *__restrict__ bias,
                 sc[j][1] = x[1] + bz.y;
                 sc[j][2] = x[2] + bz.z;
                 sc[j][3] = x[3] + bz.w;
-                lmax = fmaxf(lmax, fmaxf(fmaxf(sc[j][0], sc[j][1]), fmaxf(sc[j][2], sc[j][3])));
+                lmax = max3(lmax, max3(sc[j][0], sc[j][1], sc[j][2]), sc[j][3]);
             } else {
 #pragma unroll
                 for (int u = 0; u < 4; ++u) sc[j][u] = -INFINITY;
