@@ -294,21 +294,40 @@ tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             {
                 const int d = 4 * lane;
                 const float nb = -args.b;
-                float G0 = 0.f, G1 = 0.f, G2 = 0.f, G3 = 0.f;
-#pragma unroll 8
-                for (int i = 0; i < kC; ++i) {
-                    if (i < len) {
-                        const uint2 raw = *(const uint2 *)(stg + a_box(d >> 6) +
-                                                           sw128_off((uint32_t)i, (uint32_t)(d & 63) * 2u));
-                        const float2 x0 = unpack_bf16(raw.x), x1 = unpack_bf16(raw.y);
-                        G0 = fmaf(nb, fast_sigmoid(x0.x), G0);
-                        G1 = fmaf(nb, fast_sigmoid(x0.y), G1);
-                        G2 = fmaf(nb, fast_sigmoid(x1.x), G2);
-                        G3 = fmaf(nb, fast_sigmoid(x1.y), G3);
+                const uint8_t *abase = stg + a_box(d >> 6);
+                const uint32_t dcol = (uint32_t)(d & 63) * 2u;
+                float G[4] = {0.f, 0.f, 0.f, 0.f};
+                // four tokens per group; the next group's raw rows are read before this
+                // group's exp(G) rows are stored (rows C..2C-1, never the raw rows 0..C-1,
+                // which the compiler cannot see), so their latency overlaps the gates
+                uint2 raw[4], nxt[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) raw[u] = *(const uint2 *)(abase + sw128_off((uint32_t)u, dcol));
+                float e[4];
+#pragma unroll 1
+                for (int grp = 0; grp < kC / 4; ++grp) {
+                    if (grp + 1 < kC / 4) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            nxt[u] = *(const uint2 *)(abase + sw128_off((uint32_t)(4 * grp + 4 + u), dcol));
                     }
-                    *(float4 *)(stg + wq_off(kC + i, d)) = make_float4(__expf(G0), __expf(G1), __expf(G2), __expf(G3));
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float2 x0 = unpack_bf16(raw[u].x), x1 = unpack_bf16(raw[u].y);
+                        const float xs[4] = {x0.x, x0.y, x1.x, x1.y};
+                        const bool live = 4 * grp + u < len;   // gates past the end are 0
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            G[v] = live ? fmaf(nb, fast_sigmoid(xs[v]), G[v]) : G[v];
+                            e[v] = __expf(G[v]);
+                        }
+                        *(float4 *)(stg + wq_off(kC + 4 * grp + u, d)) = make_float4(e[0], e[1], e[2], e[3]);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) raw[u] = nxt[u];
                 }
-                *(float4 *)&hdr->gam[d] = make_float4(__expf(G0), __expf(G1), __expf(G2), __expf(G3));
+                // exp(G_C): G stops at the tile's last token, so the last row's values
+                *(float4 *)&hdr->gam[d] = make_float4(e[0], e[1], e[2], e[3]);
             }
             __syncwarp();
             // ---- per 16-column slab s: lane (row i = lane / 2, 8 columns of half lane & 1)
