@@ -602,6 +602,9 @@ tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             }
             tc_fence_after();
             const Hdr *hdr = (const Hdr *)(stg + kOffHdr);
+            // the header is read before the arrive below: the update that follows it frees
+            // the stage, and the prep warp then writes the header of the stage's next tile
+            const int len_c = hdr->len, emit_c = hdr->emit;
             // D^T of this tile (to bf16, the A operand of the update and the output
             // term) and the previous tile's output (complete with this tile's bar_x; read
             // before the arrive, since the next front overwrites its buffer)
@@ -651,8 +654,8 @@ tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             if (lane == 0) mbar_arrive(&bar_a[0]);
             if (emit_prev) store_out(ob, len_prev, t0_prev);
             t0_prev = sstart + (w0 + c) * kC;
-            len_prev = hdr->len;
-            emit_prev = hdr->emit;
+            len_prev = len_c;
+            emit_prev = emit_c;
             done = c + 1;
         }
         // drain: the last tile's output, then the final state
