@@ -51,6 +51,14 @@ def test_topk_bit_exact(T, E, k, dtype):
     _topk_case(T, E, k, dtype, seed=T + E + k)
 
 
+@pytest.mark.parametrize("T,E,k,dtype", [(12000, 132, 9, "bf16"), (12000, 896, 8, "f32"),
+                                         (6000, 2048, 32, "f32"), (12000, 512, 4, "bf16")])
+def test_topk_bit_exact_many_tokens_per_warp(T, E, k, dtype):
+    """Enough tokens that every warp ranks several (one resident wave of blocks, each warp
+    walking its tokens with the next row in flight), so the row buffers rotate."""
+    _topk_case(T, E, k, dtype, seed=T + 7 * E + k)
+
+
 @pytest.mark.parametrize("E,k", [(896, 8), (64, 16), (256, 32)])
 def test_topk_with_many_ties(E, k):
     """Logits on a half-integer grid and a zero bias: many equal scores, so the
