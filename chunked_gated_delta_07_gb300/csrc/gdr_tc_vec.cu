@@ -330,78 +330,68 @@ tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 *(float4 *)&hdr->gam[d] = make_float4(e[0], e[1], e[2], e[3]);
             }
             __syncwarp();
-            // ---- per 16-column slab s: lane (row i = lane / 2, 8 columns of half lane & 1)
-            // forms Kt, Kh, Qt, K'' = Kh (.) gamma from the raw tiles and exp(G); writes K''
-            // over the raw K, -Kt (tf32) over the raw gate inputs / raw Q, Qt (tf32) over
-            // exp(G), and Kt, Kh, Qt in bf16 to a 16 x 16 scratch from which the Gram
-            // products take their fragments.  Slab s writes -Kt over raw data that slabs
-            // <= s have read: raw gate inputs (slabs 0-3), raw Q columns 0..63 (slabs 4, 5)
-            // and 64..127 (slabs 6, 7, after their own reads).
+            // ---- per 16-column slab s: lane (g, t) = (lane / 4, lane % 4) forms rows g and
+            // g + 8, columns 2t, 2t + 1, 2t + 8, 2t + 9 of Kt, Kh, Qt and K'' = Kh (.) gamma
+            // from the raw tiles and exp(G), which is the m16n8k16 fragment layout: its own
+            // bf16 pairs are the A fragments of Kt and Qt and the B fragments of Kh^T, so the
+            // Gram products Skk = Kt Kh^T and Sqk = Qt Kh^T need no scratch.  It writes K''
+            // over the raw K, -Kt (tf32) over the raw gate inputs / raw Q and Qt (tf32) over
+            // exp(G).  Slab s writes -Kt over raw data that slabs <= s have read: raw gate
+            // inputs (slabs 0-3), raw Q columns 0..63 (slabs 4, 5) and 64..127 (slabs 6, 7).
             float skk[2][4] = {}, sqk[2][4] = {};
             {
-                const int i = lane >> 1, hw = lane & 1;
-                const uint32_t srow = (uint32_t)i * 32u + 16u * (uint32_t)(hw ^ ((i >> 2) & 1));
-                const uint32_t lrow = (uint32_t)(lane & 15) * 32u +
-                                      16u * (uint32_t)((lane >> 4) ^ (((lane & 15) >> 2) & 1));
-#pragma unroll 2
+#pragma unroll 1
                 for (int sl = 0; sl < kD / 16; ++sl) {
-                    const int d0 = 16 * sl + 8 * hw;
-                    const uint32_t kq_off = sw128_off((uint32_t)i, (uint32_t)(d0 & 63) * 2u);
-                    const uint4 kr = *(const uint4 *)(stg + kOffK + (d0 >> 6) * kBox + kq_off);
-                    uint4 qr = make_uint4(0, 0, 0, 0);
-                    if (use_q) qr = *(const uint4 *)(stg + q_box(d0 >> 6) + kq_off);
-                    const float4 ea = *(const float4 *)(stg + wq_off(kC + i, d0));
-                    const float4 eb = *(const float4 *)(stg + wq_off(kC + i, d0 + 4));
-                    const float4 ga = *(const float4 *)&hdr->gam[d0];
-                    const float4 gb = *(const float4 *)&hdr->gam[d0 + 4];
-                    __syncwarp();   // the slab's raw data is read before anything overwrites it
-                    const float E[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
-                    const float gmv[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-                    const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
-                    const uint32_t qw[4] = {qr.x, qr.y, qr.z, qr.w};
-                    float kt[8], kh[8], qt[8], kp[8];
+                    // element (hr, w, u): row g + 8 hr, column 16 sl + 2t + 8 w + u
+                    uint32_t kw[2][2], qw[2][2];
+                    float2 ev[2][2];
+                    float2 gm[2];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const float kv = __uint_as_float(u & 1 ? kw[u / 2] & 0xffff0000u : kw[u / 2] << 16);
-                        const float qv = __uint_as_float(u & 1 ? qw[u / 2] & 0xffff0000u : qw[u / 2] << 16);
-                        const float n = __fdividef(1.f, E[u]);
-                        kt[u] = kv * E[u];
-                        kh[u] = kv * n;
-                        kp[u] = kh[u] * gmv[u];
-                        qt[u] = qv * E[u];
+                    for (int w = 0; w < 2; ++w) {
+                        const int c = 16 * sl + 2 * t + 8 * w;
+                        gm[w] = *(const float2 *)&hdr->gam[c];
+#pragma unroll
+                        for (int hr = 0; hr < 2; ++hr) {
+                            const int r = g + 8 * hr;
+                            const uint32_t kq_off = sw128_off((uint32_t)r, (uint32_t)(c & 63) * 2u);
+                            kw[hr][w] = *(const uint32_t *)(stg + kOffK + (c >> 6) * kBox + kq_off);
+                            qw[hr][w] = use_q ? *(const uint32_t *)(stg + q_box(c >> 6) + kq_off) : 0u;
+                            ev[hr][w] = *(const float2 *)(stg + wq_off(kC + r, c));
+                        }
                     }
-                    *(uint4 *)(stg + kOffK + (d0 >> 6) * kBox + kq_off) =
-                        make_uint4(pack_bf16(kp[0], kp[1]), pack_bf16(kp[2], kp[3]), pack_bf16(kp[4], kp[5]),
-                                   pack_bf16(kp[6], kp[7]));
-                    *(float4 *)(stg + wq_off(i, d0)) = make_float4(-kt[0], -kt[1], -kt[2], -kt[3]);
-                    *(float4 *)(stg + wq_off(i, d0 + 4)) = make_float4(-kt[4], -kt[5], -kt[6], -kt[7]);
-                    *(uint4 *)(stg + kOffBT + srow) =
-                        make_uint4(pack_bf16(kt[0], kt[1]), pack_bf16(kt[2], kt[3]), pack_bf16(kt[4], kt[5]),
-                                   pack_bf16(kt[6], kt[7]));
-                    *(uint4 *)(stg + kOffBT + 512 + srow) =
-                        make_uint4(pack_bf16(kh[0], kh[1]), pack_bf16(kh[2], kh[3]), pack_bf16(kh[4], kh[5]),
-                                   pack_bf16(kh[6], kh[7]));
-                    if (use_q) {
-                        *(float4 *)(stg + wq_off(kC + i, d0)) = make_float4(qt[0], qt[1], qt[2], qt[3]);
-                        *(float4 *)(stg + wq_off(kC + i, d0 + 4)) = make_float4(qt[4], qt[5], qt[6], qt[7]);
-                        *(uint4 *)(stg + kOffBU + srow) =
-                            make_uint4(pack_bf16(qt[0], qt[1]), pack_bf16(qt[2], qt[3]),
-                                       pack_bf16(qt[4], qt[5]), pack_bf16(qt[6], qt[7]));
+                    __syncwarp();   // the slab's raw data is read before anything overwrites it
+                    uint32_t ktf[4], khf[4], qtf[4];   // fragment order: (g, w 0), (g+8, w 0), (g, w 1), (g+8, w 1)
+#pragma unroll
+                    for (int w = 0; w < 2; ++w) {
+                        const int c = 16 * sl + 2 * t + 8 * w;
+#pragma unroll
+                        for (int hr = 0; hr < 2; ++hr) {
+                            const int r = g + 8 * hr;
+                            const float2 kv = unpack_bf16(kw[hr][w]), qv = unpack_bf16(qw[hr][w]);
+                            const float2 E = ev[hr][w];
+                            const float n0 = __fdividef(1.f, E.x), n1 = __fdividef(1.f, E.y);
+                            const float kt0 = kv.x * E.x, kt1 = kv.y * E.y;
+                            const float kh0 = kv.x * n0, kh1 = kv.y * n1;
+                            const float qt0 = qv.x * E.x, qt1 = qv.y * E.y;
+                            const uint32_t kq_off = sw128_off((uint32_t)r, (uint32_t)(c & 63) * 2u);
+                            *(uint32_t *)(stg + kOffK + (c >> 6) * kBox + kq_off) =
+                                pack_bf16(kh0 * gm[w].x, kh1 * gm[w].y);
+                            *(float2 *)(stg + wq_off(r, c)) = make_float2(-kt0, -kt1);
+                            if (use_q) *(float2 *)(stg + wq_off(kC + r, c)) = make_float2(qt0, qt1);
+                            ktf[2 * w + hr] = pack_bf16(kt0, kt1);
+                            khf[2 * w + hr] = pack_bf16(kh0, kh1);
+                            qtf[2 * w + hr] = pack_bf16(qt0, qt1);
+                        }
                     }
-                    __syncwarp();   // the scratch is written before the fragments are read
-                    uint32_t ktf[4], khf[4], qtf[4];
-                    ldsm_x4(smem_u32(stg + kOffBT + lrow), ktf);
-                    ldsm_x4(smem_u32(stg + kOffBT + 512 + lrow), khf);
                     mma16816(skk[0], ktf, khf[0], khf[2]);
                     mma16816(skk[1], ktf, khf[1], khf[3]);
                     if (use_q) {
-                        ldsm_x4(smem_u32(stg + kOffBU + lrow), qtf);
                         mma16816(sqk[0], qtf, khf[0], khf[2]);
                         mma16816(sqk[1], qtf, khf[1], khf[3]);
                     }
                 }
             }
-            __syncwarp();   // the last fragments are read before A and P overwrite the scratch
+            __syncwarp();   // every lane's slab stores are done before A and P are formed
             // ---- A = beta (.) strict_lower(Skk) (fp32, for the substitution) and
             // P = lower(Sqk) (bf16, the output term's operand), from the accumulators:
             // skk[nt][r] is (row g + 8 (r >> 1), column 8 nt + 2t + (r & 1))
