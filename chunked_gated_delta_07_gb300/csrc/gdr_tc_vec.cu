@@ -84,8 +84,8 @@ constexpr uint32_t kOffA0 = kOffWQ;                  // raw gate inputs, columns
 constexpr uint32_t kOffA1 = kOffWQ + kWQBlock;       // raw gate inputs, columns 64..127
 constexpr uint32_t kOffQ0 = kOffWQ + 2 * kWQBlock;   // raw Q, columns 0..63
 constexpr uint32_t kOffQ1 = kOffWQ + 3 * kWQBlock;   // raw Q, columns 64..127
-constexpr uint32_t kOffBT = kOffWQ + 4 * kWQBlock;   // Gram scratch (Kt, Kh bf16), A (fp32 [C][C]), then Bu in tf32
-constexpr uint32_t kOffBU = kOffBT + kC * kC * 4;    // Gram scratch (Qt bf16), then Bu in bf16
+constexpr uint32_t kOffBT = kOffWQ + 4 * kWQBlock;   // A (fp32 [C][C]), then Bu in tf32
+constexpr uint32_t kOffBU = kOffBT + kC * kC * 4;    // Bu in bf16
 constexpr uint32_t kOffP = kOffBU + kC * kC * 2;     // P in bf16
 constexpr uint32_t kOffHdr = kOffP + kC * kC * 2;
 constexpr uint32_t kStage = 27648;
