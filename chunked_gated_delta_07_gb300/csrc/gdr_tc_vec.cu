@@ -359,7 +359,11 @@ tc_vec_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                             ev[hr][w] = *(const float2 *)(stg + wq_off(kC + r, c));
                         }
                     }
-                    __syncwarp();   // the slab's raw data is read before anything overwrites it
+                    // -Kt overwrites raw Q that other lanes read: slabs 4 and 5 that of slabs
+                    // 0-3, slab 6 that of slabs 4 and 5, slab 7 that of slabs 6 and 7 (its
+                    // own); slabs 0-3 overwrite only gate inputs (read before the slabs) and
+                    // each lane's own elements
+                    if (sl == 4 || sl >= 6) __syncwarp();
                     uint32_t ktf[4], khf[4], qtf[4];   // fragment order: (g, w 0), (g+8, w 0), (g, w 1), (g+8, w 1)
 #pragma unroll
                     for (int w = 0; w < 2; ++w) {
